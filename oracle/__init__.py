@@ -1,0 +1,8 @@
+"""Float64 CPU oracle of the triangle multiplicative update (test infrastructure).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this package. It shares no code with the CUDA library.
+"""
+from .trimul import (LN_EPS, DIRECTIONS, sigmoid, layer_norm, round_to_bf16, normalise_input,  # noqa: F401
+                     gated_projection, contract, output, full, intermediates, sampled,
+                     half_ulp_bf16, errors)
