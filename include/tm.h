@@ -1,0 +1,172 @@
+/*
+ * tm.h -- C ABI of libtm, the B300 (sm_103a) triangle multiplicative update.
+ *
+ * The operation. The pages name the layer -- TriangleMultiplicationOutgoing,
+ * built once on the CPU and applied as layer(x, mask), with an Outgoing
+ * direction selector, in the code-sample section ("Exemplo de código: triangle
+ * multiplication CP-aware") of "NVIDIA BioNeMo escala modelagem biomolecular com
+ * context parallelism e quebra barreira de memória da GPU" -- and work it over
+ * the N x N pair representation of that page's "2D tiling da pair
+ * representation" section, but they do not write its arithmetic out. libtm
+ * computes the standard AlphaFold3/Boltz Pairformer definition over z [N][N][c_z]:
+ *
+ *   zh_ij  = LayerNorm_in(z_ij)                              over c_z, eps 1e-5
+ *   a_ik   = sigmoid(W_ga zh_ik) * (W_a zh_ik) * m_i m_k     c_h channels
+ *   b_ik   = sigmoid(W_gb zh_ik) * (W_b zh_ik) * m_i m_k
+ *   x_ij   = sum_k a_ik b_jk      (TM_OUTGOING)
+ *   x_ij   = sum_k a_ki b_kj      (TM_INCOMING)
+ *   out_ij = sigmoid(W_g zh_ij) * W_o LayerNorm_out(x_ij)    LayerNorm over c_h
+ *
+ * m is a token mask [N] of 0/1 values; Linear layers have no bias; LayerNorm
+ * uses the biased variance.
+ *
+ * Precisions. TM_BF16: z and out are bf16, a and b are stored as bf16
+ * channel-major [c_h][N][ld], x is float32; every contraction accumulates in
+ * float32 on the tensor cores (tcgen05); c_z = c_h = 128 only. TM_F32: z, out
+ * and every intermediate are float32, computed with FP32 FMA on the CUDA
+ * cores; any 1 <= c_z, c_h <= 256.
+ *
+ * Conventions for every call below.
+ *  - Pointers named "device" are device memory of the ctx's GPU; "host" ones
+ *    are host memory. Tensors are dense, row-major, 16-byte aligned.
+ *  - The caller owns z, mask and out; libtm owns its workspace (a, b and a
+ *    block of x), grows it with cudaMallocAsync on the call's stream, and frees
+ *    it in tm_destroy.
+ *  - Calls are asynchronous and stream-ordered on `stream` (a cudaStream_t,
+ *    NULL for the legacy default stream). Argument errors return
+ *    synchronously, before any launch. A device-side wait that exceeds its
+ *    time limit stores TM_ERR_TIMEOUT in the ctx's status word; the next
+ *    tm_forward* or tm_sync_status returns it.
+ *  - A ctx may be used from one host thread and one stream at a time.
+ */
+#ifndef TM_H
+#define TM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct tm_ctx tm_ctx; /* opaque, owned by libtm */
+
+typedef enum {
+  TM_OK = 0,
+  TM_ERR_INVALID = 1,     /* bad pointer, size, alignment, aliasing or enum value      */
+  TM_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. bf16 with c != 128)       */
+  TM_ERR_OOM = 3,         /* workspace would exceed the limit, or allocation failed    */
+  TM_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (see tm_last_error)     */
+  TM_ERR_TIMEOUT = 5      /* a device-side wait ran out of time (status word)          */
+} tm_status;
+
+typedef enum { TM_OUTGOING = 0, TM_INCOMING = 1 } tm_direction;
+typedef enum { TM_F32 = 0, TM_BF16 = 1 } tm_dtype;
+
+/* Layer parameters: host float32 arrays, Linear layout [out][in] (y = W x). */
+typedef struct {
+  const float *ln_in_gamma, *ln_in_beta;   /* [c_z]        */
+  const float *w_a, *w_ga, *w_b, *w_gb;    /* [c_h][c_z]   */
+  const float *w_g;                        /* [c_z][c_z]   */
+  const float *ln_out_gamma, *ln_out_beta; /* [c_h]        */
+  const float *w_o;                        /* [c_z][c_h]   */
+} tm_weights;
+
+typedef struct {
+  int block;              /* edge of the square output blocks of the streamed
+                             schedule; 0 = automatic (whole grid while its float32
+                             x fits the workspace limit, else about 2500)          */
+  int timeout_ms;         /* limit of every device-side wait; 0 = 2000 ms           */
+  size_t workspace_limit; /* bytes; 0 = env TM_WORKSPACE_LIMIT, else no limit      */
+  int reserved[8];        /* must be zero                                          */
+} tm_options;
+
+/* Create a context on the current CUDA device. Copies and converts the
+ * weights (host float32, freed by the caller at will) into the device layouts
+ * of both precisions. Returns TM_ERR_INVALID for a NULL argument or c_z, c_h
+ * outside [1, 256]. *out_ctx is set only on TM_OK. Synchronous. */
+tm_status tm_create(int c_z, int c_hidden, const tm_weights* w, tm_ctx** out_ctx);
+
+/* One triangle multiplicative update: out = update(z, mask) in direction dir.
+ *   z     device, [N][N][c_z] of dtype;
+ *   mask  device float32 [N] of 0/1 token-mask values, or NULL for all ones;
+ *   N     >= 1 tokens;
+ *   out   device, [N][N][c_z] of dtype; must not overlap z.
+ * The pages' "layer(x, mask)" call of the code-sample section named above. */
+tm_status tm_forward(tm_ctx* ctx, const void* z, const float* mask, int N, tm_dtype dtype,
+                     tm_direction dir, void* out, void* stream);
+
+/* tm_forward with options (NULL = defaults). */
+tm_status tm_forward_ex(tm_ctx* ctx, const void* z, const float* mask, int N, tm_dtype dtype,
+                        tm_direction dir, void* out, void* stream, const tm_options* opt);
+
+/* The three steps of tm_forward, for callers that keep intermediates.
+ *
+ * tm_project: a, b = gated, masked projections of LayerNorm(z).
+ *   a, b  device, channel-major [c_h][N][ld] of dtype (bf16 or float32);
+ *   ld    >= N, and a multiple of 8 for TM_BF16 (16-byte rows).
+ */
+tm_status tm_project(tm_ctx* ctx, const void* z, const float* mask, int N, tm_dtype dtype,
+                     void* a, void* b, int ld, void* stream);
+
+/* tm_contract: the per-channel contraction over one output block.
+ *   a, b    device, [c_h][N][ld] of dtype, as written by tm_project;
+ *   i0, j0  first row / column of the block; bi, bj its extents (>= 1);
+ *   x       device float32 [c_h][bi][ldx], ldx >= bj and a multiple of 4;
+ *           x[c][i - i0][j - j0] = sum_k a.. b.. as in the header comment.
+ */
+tm_status tm_contract(tm_ctx* ctx, const void* a, const void* b, int N, int ld, tm_dtype dtype,
+                      tm_direction dir, int i0, int j0, int bi, int bj, float* x, int ldx,
+                      void* stream);
+
+/* tm_finish: out over one block from its x block and z.
+ *   x    device float32 [c_h][bi][ldx] (as tm_contract writes it);
+ *   z    device [N][N][c_z] of dtype;
+ *   out  device [N][N][c_z] of dtype; only entries of the block are written.
+ */
+tm_status tm_finish(tm_ctx* ctx, const float* x, int ldx, const void* z, int N, tm_dtype dtype,
+                    int i0, int j0, int bi, int bj, void* out, void* stream);
+
+/* Synchronise `stream` and return the device status word (TM_OK or
+ * TM_ERR_TIMEOUT), clearing it. */
+tm_status tm_sync_status(tm_ctx* ctx, void* stream);
+
+/* Per-kernel timing with CUDA events recorded on the launch stream.
+ * enable != 0 starts recording (and clears the totals). */
+typedef struct {
+  int launches[4];     /* projection, contraction, finish, float32 kernels */
+  double ms[4];        /* summed event-measured durations                  */
+  long long units[4];  /* pairs processed (projection, finish) or
+                          channel x output-pair products (contraction)     */
+} tm_timing;
+tm_status tm_set_timing(tm_ctx* ctx, int enable);
+/* Synchronises the recorded events and fills *t. */
+tm_status tm_get_timing(tm_ctx* ctx, tm_timing* t);
+
+/* Number of kernel launches made by this ctx since creation. */
+long long tm_launch_count(const tm_ctx* ctx);
+
+/* Bytes of workspace currently held by the ctx. */
+size_t tm_workspace_bytes(const tm_ctx* ctx);
+
+/* Watchdog self-test: launches one small kernel whose wait on an mbarrier
+ * that nothing arrives at runs out after timeout_ms (1..10000) and records
+ * TM_ERR_TIMEOUT in the ctx's status word, then returns. The call itself
+ * returns TM_OK once launched; a following tm_sync_status returns
+ * TM_ERR_TIMEOUT, and the ctx stays usable. Exercises the same bounded wait
+ * every libtm kernel uses, without faulting or hanging the GPU. */
+tm_status tm_watchdog_selftest(tm_ctx* ctx, int timeout_ms, void* stream);
+
+/* Static text of a status code; never NULL. */
+const char* tm_status_string(tm_status s);
+
+/* Detail of the ctx's last error ("" if none); valid until the next call. */
+const char* tm_last_error(const tm_ctx* ctx);
+
+/* Free the workspace and weights (after synchronising the device). NULL is a no-op. */
+void tm_destroy(tm_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TM_H */

@@ -1,0 +1,254 @@
+// k2_contract.cu -- the per-channel contraction of the triangle multiplicative
+// update on the sm_103a tensor cores.
+//
+//   outgoing: x_ij = sum_k a_ik b_jk   (X_c = A_c B_c^T)
+//   incoming: x_ij = sum_k a_ki b_kj   (X_c = A_c^T B_c)
+//
+// a and b are channel-major bf16 [128][N][ld]; x is float32 [128][bi][ldx]
+// for one output block (i0, j0, bi, bj). This is the O(N^3 c) step that the
+// 2D block tiling of the pair representation exists for ("2D tiling da pair
+// representation" section of "NVIDIA BioNeMo escala modelagem biomolecular com
+// context parallelism e quebra barreira de memória da GPU"); here the N x N
+// grid is tiled inside one GPU.
+//
+// Design (one CTA per SM, persistent over (channel, i-tile, j-tile)):
+//   warp 0      TMA producer: 128 x 64 A tile and 256 x 64 B tile per stage,
+//               128-byte swizzle, 4-stage ring of mbarriers.
+//   warp 1      TMEM allocator and single-thread tcgen05.mma issuer
+//               (M = 128, N = 256, K = 16 per instruction, f32 accumulate),
+//               two TMEM accumulators so the epilogue of one tile overlaps the
+//               main loop of the next.
+//   warps 2..5  epilogue: tcgen05.ld 32 columns at a time, 16-byte stores of x.
+// Incoming reads the same a/b buffers through tensor maps whose box runs
+// along the other pair index ("transposed" boxes), and tells the MMA that A
+// and B are M/N-major; no transpose is ever materialised. k beyond N is
+// zero-filled by TMA.
+#include "tm_kernels.h"
+
+namespace tmk {
+namespace {
+
+constexpr int BM = kContractBM, BN = kContractBN, BK = kContractBK;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;          // 16 KB
+constexpr int B_BYTES = BN * BK * 2;          // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TMEM_COLS = 2 * BN;             // two accumulators
+constexpr int THREADS = 192;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 256;
+
+static_assert(TMEM_COLS == 512, "two 256-column accumulators fill TMEM");
+
+struct Tile {
+  int c, ti, tj;
+};
+__device__ __forceinline__ Tile decode(long long t, const ContractParams& p) {
+  const long long per_c = (long long)p.tiles_i * p.tiles_j;
+  Tile r;
+  r.c = (int)(t / per_c);
+  const int rem = (int)(t - (long long)r.c * per_c);
+  r.ti = rem / p.tiles_j;
+  r.tj = rem - r.ti * p.tiles_j;
+  return r;
+}
+
+template <bool INCOMING>
+__global__ void __launch_bounds__(THREADS, 1)
+    k2_contract(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap,
+                const ContractParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* tiles = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* fin = tempty + 2;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(fin + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    *abort_flag = (smem_u32(smem) & 1023u) ? 1 : 0;  // swizzled tiles need 1024-byte alignment
+    if (*abort_flag) raise_status(p.w, ST_TIMEOUT, 90);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);
+    }
+    mbar_init(fin, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&amap);
+    tma_prefetch_desc(&bmap);
+  }
+  if (warp == 1) {
+    tmem_alloc(tslot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tslot;
+  const int KB = (p.N + BK - 1) / BK;
+
+  if (!*abort_flag) {
+    if (warp == 0) {
+      // ------------------------------------------------------------ TMA producer
+      if (lane == 0) {
+        int s = 0;
+        uint32_t ph = 0;
+        for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+          const Tile tl = decode(t, p);
+          const int ia = p.i0 + tl.ti * BM;
+          const int jb = p.j0 + tl.tj * BN;
+          for (int kb = 0; kb < KB; ++kb) {
+            if (!wait_bounded(&empty[s], ph ^ 1u, p.w, abort_flag, 1)) goto producer_done;
+            uint8_t* sa = tiles + s * STAGE_BYTES;
+            uint8_t* sb = sa + A_BYTES;
+            mbar_expect_tx(&full[s], STAGE_BYTES);
+            if (!INCOMING) {
+              // A_c[i][k] = a_ik: rows i, k contiguous (K-major); B_c[j][k] = b_jk likewise.
+              tma_load_3d(sa, &amap, &full[s], kb * BK, ia, tl.c);
+              tma_load_3d(sb, &bmap, &full[s], kb * BK, jb, tl.c);
+            } else {
+              // a_ki, b_kj: rows k, i (or j) contiguous; 64-wide slabs along i / j (M/N-major).
+              tma_load_3d(sa, &amap, &full[s], ia, kb * BK, tl.c);
+              tma_load_3d(sa + 8192, &amap, &full[s], ia + 64, kb * BK, tl.c);
+#pragma unroll
+              for (int h = 0; h < BN / 64; ++h) tma_load_3d(sb + h * 8192, &bmap, &full[s], jb + 64 * h, kb * BK, tl.c);
+            }
+            if (++s == STAGES) {
+              s = 0;
+              ph ^= 1u;
+            }
+          }
+        }
+      producer_done:;
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t idesc = make_idesc(BM, BN, FMT_BF16, INCOMING, INCOMING);
+        int s = 0;
+        uint32_t ph = 0;
+        int local = 0;
+        for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++local) {
+          const int buf = local & 1;
+          const uint32_t use = (uint32_t)(local >> 1);
+          if (!wait_bounded(&tempty[buf], (use & 1u) ^ 1u, p.w, abort_flag, 2)) break;
+          tc_fence_after();
+          const uint32_t d = tmem_base + (uint32_t)(buf * BN);
+          bool ok = true;
+          for (int kb = 0; kb < KB; ++kb) {
+            if (!wait_bounded(&full[s], ph, p.w, abort_flag, 3)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(tiles + s * STAGE_BYTES);
+            const uint32_t b0 = a0 + A_BYTES;
+#pragma unroll
+            for (int ks = 0; ks < BK / 16; ++ks) {
+              uint64_t ad, bd;
+              if (!INCOMING) {
+                ad = make_sdesc_sw128(a0 + ks * 32, 16, 1024);
+                bd = make_sdesc_sw128(b0 + ks * 32, 16, 1024);
+              } else {
+                ad = make_sdesc_sw128(a0 + ks * 2048, 8192, 1024);
+                bd = make_sdesc_sw128(b0 + ks * 2048, 8192, 1024);
+              }
+              mma_f16(d, ad, bd, idesc, (kb | ks) != 0);
+            }
+            mma_commit(&empty[s]);
+            if (++s == STAGES) {
+              s = 0;
+              ph ^= 1u;
+            }
+          }
+          if (!ok) break;
+          mma_commit(&tfull[buf]);
+        }
+        // every MMA issued by this thread has completed before TMEM is released
+        mma_commit(fin);
+        wait_bounded(fin, 0, p.w, abort_flag, 4);
+      }
+    } else {
+      // ------------------------------------------------------------ epilogue
+      const int q = warp & 3;  // TMEM lanes 32q .. 32q+31 belong to this warp
+      const int r = q * 32 + lane;
+      int local = 0;
+      for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++local) {
+        const Tile tl = decode(t, p);
+        const int buf = local & 1;
+        const uint32_t use = (uint32_t)(local >> 1);
+        if (!warp_wait_bounded(&tfull[buf], use & 1u, p.w, abort_flag, 5)) break;
+        tc_fence_after();
+        const int il = tl.ti * BM + r;  // block-local row
+        const int jl0 = tl.tj * BN;
+        float* xrow = p.x + (long long)tl.c * p.chan_stride + (long long)il * p.ldx + jl0;
+#pragma unroll 1
+        for (int ch = 0; ch < BN / 32; ++ch) {
+          uint32_t v[32];
+          tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + ch * 32), v);
+          tmem_ld_wait();
+          const int jc = jl0 + ch * 32;
+          if (il < p.bi && jc < p.bj) {
+            float* dst = xrow + ch * 32;
+            if (jc + 32 <= p.bj) {
+#pragma unroll
+              for (int e = 0; e < 32; e += 4)
+                *reinterpret_cast<uint4*>(dst + e) = make_uint4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                if (jc + e < p.bj) dst[e] = __uint_as_float(v[e]);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[buf]);
+      }
+    }
+  }
+
+  __syncthreads();
+  if (*abort_flag) {
+    // give in-flight TMA copies time to land before the CTA's shared memory is released
+    const uint64_t t0 = gtimer();
+    while (gtimer() - t0 < 2000000ull) {
+    }
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_contract_bf16(bool incoming, const CUtensorMap& amap, const CUtensorMap& bmap,
+                                 const ContractParams& p, int num_sms, cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k2_contract<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k2_contract<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  if (p.total_tiles <= 0) return cudaSuccess;
+  const int grid = (int)(p.total_tiles < num_sms ? p.total_tiles : num_sms);
+  if (incoming)
+    k2_contract<true><<<grid, THREADS, SMEM_BYTES, s>>>(amap, bmap, p);
+  else
+    k2_contract<false><<<grid, THREADS, SMEM_BYTES, s>>>(amap, bmap, p);
+  return cudaGetLastError();
+}
+
+}  // namespace tmk

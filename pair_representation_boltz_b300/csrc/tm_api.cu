@@ -1,0 +1,698 @@
+// tm_api.cu -- the C ABI of libtm (declared in include/tm.h): argument
+// checking, weight preparation, the workspace, TMA tensor maps and the
+// block-streamed schedule of the triangle multiplicative update.
+//
+// Schedule of one bf16 update (tm_forward):
+//   projection       z -> a, b                    (one launch, whole grid)
+//   for each output block (I, J) of the B x B block grid:
+//     contraction    a, b -> x block (float32)    (one launch)
+//     finish         x block, z -> out block      (one launch)
+// Only one float32 x block is alive at a time, so for N = 10000 and
+// B = 2500 the device holds z, a, b and out plus a 3.2 GB x block. The 2D
+// block tiling of the pair representation is the one the pages use across
+// GPUs ("2D tiling da pair representation" section of "NVIDIA BioNeMo escala
+// modelagem biomolecular com context parallelism e quebra barreira de memória
+// da GPU"), and streaming the blocks replaces the in-model chunking that the
+// "O problema dos workarounds atuais" section of that page describes.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "tm.h"
+#include "tm_kernels.h"
+
+using namespace tmk;
+
+namespace {
+
+const char* kStatusText[] = {"ok", "invalid argument", "unsupported configuration", "out of workspace memory",
+                             "CUDA error", "device wait timed out"};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct TimedLaunch {
+  cudaEvent_t start, stop;
+  int kind;
+  long long units;
+};
+
+}  // namespace
+
+struct tm_ctx {
+  int device = 0, num_sms = 0;
+  int c_z = 0, c_h = 0;
+  // float32 weights (device), one allocation
+  float* w32 = nullptr;
+  F32Weights f32w{};
+  // tensor-core path (c_z = c_h = 128)
+  bool tc = false;
+  __nv_bfloat16* wk1 = nullptr;  // [2 halves][hi, lo][256][128]
+  float* k1c = nullptr;          // [2][512]
+  __half* wo16 = nullptr;        // [128][128], scaled
+  __nv_bfloat16* wg16 = nullptr; // [hi, lo][128][128]
+  float* k3c = nullptr;          // [3][128]
+  float inv_scale_o = 1.f;
+  CUtensorMap wk1_map, wo_map, wg_map;
+  // status word (mapped host memory)
+  int* status_h = nullptr;
+  int* status_d = nullptr;
+  // workspace
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  cudaStream_t ws_stream = nullptr;
+  size_t env_limit = 0;
+  // instrumentation
+  bool timing = false;
+  std::vector<TimedLaunch> timed;
+  std::vector<cudaEvent_t> event_pool;
+  long long launches = 0;
+  std::string err;
+};
+
+namespace {
+
+tm_status fail(tm_ctx* c, tm_status s, const char* fmt, ...) {
+  if (c) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    c->err = buf;
+  }
+  return s;
+}
+
+tm_status cuda_fail(tm_ctx* c, cudaError_t e, const char* what) {
+  cudaGetLastError();
+  return fail(c, TM_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const cuuint64_t* dims,
+            const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle sw) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  return fn(m, dt, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+Watch watch(const tm_ctx* c, int kernel, const tm_options* opt) {
+  Watch w;
+  w.status = c->status_d;
+  const int ms = (opt && opt->timeout_ms > 0) ? opt->timeout_ms : 2000;
+  w.limit_ns = (unsigned long long)ms * 1000000ull;
+  w.kernel = kernel;
+  return w;
+}
+
+cudaEvent_t take_event(tm_ctx* c) {
+  if (!c->event_pool.empty()) {
+    cudaEvent_t e = c->event_pool.back();
+    c->event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Launch wrapper: counts launches and, when timing is on, brackets the launch with events on `s`.
+template <typename F>
+cudaError_t timed(tm_ctx* c, int kind, long long units, cudaStream_t s, F&& launch) {
+  TimedLaunch tl{};
+  if (c->timing) {
+    tl.start = take_event(c);
+    tl.stop = take_event(c);
+    tl.kind = kind;
+    tl.units = units;
+    cudaEventRecord(tl.start, s);
+  }
+  cudaError_t e = launch();
+  if (e == cudaSuccess) ++c->launches;
+  if (c->timing) {
+    cudaEventRecord(tl.stop, s);
+    c->timed.push_back(tl);
+  }
+  return e;
+}
+
+tm_status check_device_status(tm_ctx* c) {
+  volatile int* st = c->status_h;
+  if (st[0] != 0) {
+    const int code = st[0];
+    c->err = "device wait timed out in kernel " + std::to_string(st[1]) + " at site " + std::to_string(st[2]) +
+             " (block " + std::to_string(st[3]) + ")";
+    st[0] = 0;
+    return code == TM_ERR_TIMEOUT ? TM_ERR_TIMEOUT : TM_ERR_CUDA;
+  }
+  return TM_OK;
+}
+
+size_t limit_of(const tm_ctx* c, const tm_options* opt) {
+  if (opt && opt->workspace_limit) return opt->workspace_limit;
+  return c->env_limit;  // 0 = none
+}
+
+tm_status ensure_workspace(tm_ctx* c, size_t bytes, cudaStream_t s, const tm_options* opt) {
+  const size_t lim = limit_of(c, opt);
+  if (lim && bytes > lim)
+    return fail(c, TM_ERR_OOM, "workspace of %zu bytes exceeds the limit of %zu bytes", bytes, lim);
+  if (c->ws_bytes >= bytes) return TM_OK;
+  if (c->ws) {
+    cudaError_t e = cudaFreeAsync(c->ws, s);
+    if (e != cudaSuccess) return cuda_fail(c, e, "cudaFreeAsync(workspace)");
+    c->ws = nullptr;
+    c->ws_bytes = 0;
+  }
+  cudaError_t e = cudaMallocAsync(&c->ws, bytes, s);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    c->ws = nullptr;
+    return fail(c, TM_ERR_OOM, "cudaMallocAsync(%zu bytes): %s", bytes, cudaGetErrorString(e));
+  }
+  c->ws_bytes = bytes;
+  c->ws_stream = s;
+  return TM_OK;
+}
+
+bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+// ------------------------------------------------------------------ host weight preparation
+inline void split_bf16(double v, __nv_bfloat16* hi, __nv_bfloat16* lo) {
+  *hi = __float2bfloat16_rn((float)v);
+  *lo = __float2bfloat16_rn((float)(v - (double)__bfloat162float(*hi)));
+}
+
+tm_status prepare_tensor_core_weights(tm_ctx* c, const tm_weights* w) {
+  const int C = kC;
+  std::vector<__nv_bfloat16> k1(2 * 2 * 256 * C);
+  std::vector<float> k1c(2 * 512);
+  for (int h = 0; h < 2; ++h) {
+    const float* wp = h == 0 ? w->w_a : w->w_b;
+    const float* wgt = h == 0 ? w->w_ga : w->w_gb;
+    for (int n = 0; n < 256; ++n) {
+      const float* src = n < C ? wp + (size_t)n * C : wgt + (size_t)(n - C) * C;
+      double rs = 0, bias = 0;
+      for (int k = 0; k < C; ++k) {
+        const double v = (double)src[k] * (double)w->ln_in_gamma[k];
+        __nv_bfloat16 hi, lo;
+        split_bf16(v, &hi, &lo);
+        k1[((size_t)(h * 2 + 0) * 256 + n) * C + k] = hi;
+        k1[((size_t)(h * 2 + 1) * 256 + n) * C + k] = lo;
+        rs += (double)__bfloat162float(hi) + (double)__bfloat162float(lo);
+        bias += (double)src[k] * (double)w->ln_in_beta[k];
+      }
+      k1c[h * 512 + n] = (float)rs;
+      k1c[h * 512 + 256 + n] = (float)bias;
+    }
+  }
+  // W_o' = W_o diag(gamma_out), scaled by 2^e into fp16's top binades
+  double maxabs = 0;
+  for (int o = 0; o < C; ++o)
+    for (int k = 0; k < C; ++k)
+      maxabs = std::max(maxabs, std::fabs((double)w->w_o[(size_t)o * C + k] * (double)w->ln_out_gamma[k]));
+  int e = 0;
+  if (maxabs > 0) e = 14 - (int)std::floor(std::log2(maxabs));
+  const double sc = std::ldexp(1.0, e);
+  std::vector<__half> wo(C * C);
+  std::vector<__nv_bfloat16> wg(2 * C * C);
+  std::vector<float> k3c(3 * C);
+  for (int o = 0; o < C; ++o) {
+    double bo = 0, rs = 0, bg = 0;
+    for (int k = 0; k < C; ++k) {
+      wo[(size_t)o * C + k] = __float2half_rn((float)((double)w->w_o[(size_t)o * C + k] * w->ln_out_gamma[k] * sc));
+      bo += (double)w->w_o[(size_t)o * C + k] * (double)w->ln_out_beta[k];
+      const double vg = (double)w->w_g[(size_t)o * C + k] * (double)w->ln_in_gamma[k];
+      __nv_bfloat16 hi, lo;
+      split_bf16(vg, &hi, &lo);
+      wg[(size_t)o * C + k] = hi;
+      wg[(size_t)(C + o) * C + k] = lo;
+      rs += (double)__bfloat162float(hi) + (double)__bfloat162float(lo);
+      bg += (double)w->w_g[(size_t)o * C + k] * (double)w->ln_in_beta[k];
+    }
+    k3c[o] = (float)rs;
+    k3c[C + o] = (float)bg;
+    k3c[2 * C + o] = (float)bo;
+  }
+  c->inv_scale_o = (float)std::ldexp(1.0, -e);
+
+  cudaError_t err;
+#define TM_UP(dst, vec)                                                                       \
+  err = cudaMalloc(&dst, vec.size() * sizeof(vec[0]));                                        \
+  if (err != cudaSuccess) return cuda_fail(c, err, "cudaMalloc(weights)");                    \
+  err = cudaMemcpy(dst, vec.data(), vec.size() * sizeof(vec[0]), cudaMemcpyHostToDevice);     \
+  if (err != cudaSuccess) return cuda_fail(c, err, "cudaMemcpy(weights)");
+  TM_UP(c->wk1, k1)
+  TM_UP(c->k1c, k1c)
+  TM_UP(c->wo16, wo)
+  TM_UP(c->wg16, wg)
+  TM_UP(c->k3c, k3c)
+#undef TM_UP
+
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)C, 1024};
+    const cuuint64_t str[1] = {(cuuint64_t)C * 2};
+    const cuuint32_t box[2] = {64, 256};
+    if (!encode(&c->wk1_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c->wk1, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return fail(c, TM_ERR_CUDA, "tensor map (projection weights)");
+  }
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)C};
+    const cuuint64_t str[1] = {(cuuint64_t)C * 2};
+    const cuuint32_t box[2] = {64, 128};
+    if (!encode(&c->wo_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, c->wo16, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return fail(c, TM_ERR_CUDA, "tensor map (W_o)");
+    const cuuint64_t dims2[2] = {(cuuint64_t)C, (cuuint64_t)(2 * C)};
+    if (!encode(&c->wg_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c->wg16, dims2, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return fail(c, TM_ERR_CUDA, "tensor map (W_g)");
+  }
+  return TM_OK;
+}
+
+// ------------------------------------------------------------------ bf16 stage launchers (arguments checked)
+tm_status run_project_bf16(tm_ctx* c, const void* z, const float* mask, int N, __nv_bfloat16* a,
+                           __nv_bfloat16* b, int ld, cudaStream_t s, const tm_options* opt) {
+  CUtensorMap zmap;
+  const cuuint64_t dims[3] = {(cuuint64_t)kC, (cuuint64_t)N, (cuuint64_t)N};
+  const cuuint64_t str[2] = {(cuuint64_t)kC * 2, (cuuint64_t)N * kC * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)kProjTileJ, 1};
+  if (!encode(&zmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, z, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+    return fail(c, TM_ERR_CUDA, "tensor map (z, projection)");
+  ProjectParams p;
+  p.a = a;
+  p.b = b;
+  p.mask = mask;
+  p.consts = c->k1c;
+  p.N = N;
+  p.ld = ld;
+  p.tiles_per_row = (N + kProjTileJ - 1) / kProjTileJ;
+  p.total_tiles = (long long)N * p.tiles_per_row;
+  p.w = watch(c, KID_PROJECT, opt);
+  cudaError_t e = timed(c, 0, (long long)N * N, s, [&] { return launch_project_bf16(zmap, c->wk1_map, p, c->num_sms, s); });
+  return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "projection launch");
+}
+
+tm_status run_contract_bf16(tm_ctx* c, const __nv_bfloat16* a, const __nv_bfloat16* b, int N, int ld, bool incoming,
+                            int i0, int j0, int bi, int bj, float* x, int ldx, cudaStream_t s,
+                            const tm_options* opt) {
+  CUtensorMap amap, bmap;
+  const cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)N, (cuuint64_t)kC};
+  const cuuint64_t str[2] = {(cuuint64_t)ld * 2, (cuuint64_t)N * ld * 2};
+  if (!incoming) {
+    const cuuint32_t boxa[3] = {(cuuint32_t)kContractBK, (cuuint32_t)kContractBM, 1};
+    const cuuint32_t boxb[3] = {(cuuint32_t)kContractBK, (cuuint32_t)kContractBN, 1};
+    if (!encode(&amap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a, dims, str, boxa, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode(&bmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, b, dims, str, boxb, CU_TENSOR_MAP_SWIZZLE_128B))
+      return fail(c, TM_ERR_CUDA, "tensor map (a/b, outgoing)");
+  } else {
+    const cuuint32_t box[3] = {64, (cuuint32_t)kContractBK, 1};
+    if (!encode(&amap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode(&bmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, b, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return fail(c, TM_ERR_CUDA, "tensor map (a/b, incoming)");
+  }
+  ContractParams p;
+  p.x = x;
+  p.ldx = ldx;
+  p.chan_stride = (long long)bi * ldx;
+  p.N = N;
+  p.i0 = i0;
+  p.j0 = j0;
+  p.bi = bi;
+  p.bj = bj;
+  p.tiles_i = (bi + kContractBM - 1) / kContractBM;
+  p.tiles_j = (bj + kContractBN - 1) / kContractBN;
+  p.total_tiles = (long long)kC * p.tiles_i * p.tiles_j;
+  p.w = watch(c, KID_CONTRACT, opt);
+  cudaError_t e = timed(c, 1, (long long)kC * bi * bj, s,
+                        [&] { return launch_contract_bf16(incoming, amap, bmap, p, c->num_sms, s); });
+  return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "contraction launch");
+}
+
+tm_status run_finish_bf16(tm_ctx* c, const float* x, int ldx, const void* z, int N, int i0, int j0, int bi, int bj,
+                          void* out, cudaStream_t s, const tm_options* opt) {
+  CUtensorMap xmap, zmap;
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)bj, (cuuint64_t)bi, (cuuint64_t)kC};
+    const cuuint64_t str[2] = {(cuuint64_t)ldx * 4, (cuuint64_t)bi * ldx * 4};
+    const cuuint32_t box[3] = {(cuuint32_t)kFinishTileJ, 1, (cuuint32_t)kC};
+    if (!encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, x, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return fail(c, TM_ERR_CUDA, "tensor map (x)");
+  }
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)kC, (cuuint64_t)N, (cuuint64_t)N};
+    const cuuint64_t str[2] = {(cuuint64_t)kC * 2, (cuuint64_t)N * kC * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)kFinishTileJ, 1};
+    if (!encode(&zmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, z, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return fail(c, TM_ERR_CUDA, "tensor map (z, finish)");
+  }
+  FinishParams p;
+  p.out = reinterpret_cast<__nv_bfloat16*>(out);
+  p.consts = c->k3c;
+  p.inv_scale_o = c->inv_scale_o;
+  p.N = N;
+  p.i0 = i0;
+  p.j0 = j0;
+  p.bi = bi;
+  p.bj = bj;
+  p.tiles_j = (bj + kFinishTileJ - 1) / kFinishTileJ;
+  p.total_tiles = (long long)bi * p.tiles_j;
+  p.w = watch(c, KID_FINISH, opt);
+  cudaError_t e = timed(c, 2, (long long)bi * bj, s,
+                        [&] { return launch_finish_bf16(xmap, zmap, c->wo_map, c->wg_map, p, c->num_sms, s); });
+  return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "finish launch");
+}
+
+tm_status check_common(tm_ctx* c, int N, tm_dtype dtype) {
+  if (!c) return TM_ERR_INVALID;
+  c->err.clear();
+  if (N < 1 || N > 65535) return fail(c, TM_ERR_INVALID, "N=%d outside [1, 65535]", N);
+  if (dtype != TM_F32 && dtype != TM_BF16) return fail(c, TM_ERR_INVALID, "unknown dtype %d", (int)dtype);
+  if (dtype == TM_BF16 && !c->tc)
+    return fail(c, TM_ERR_UNSUPPORTED, "bf16 needs c_z = c_h = 128 (have %d, %d)", c->c_z, c->c_h);
+  int dev = -1;
+  cudaGetDevice(&dev);
+  if (dev != c->device) return fail(c, TM_ERR_INVALID, "current device %d is not the ctx's device %d", dev, c->device);
+  return check_device_status(c);
+}
+
+int choose_block(const tm_ctx* c, int N, const tm_options* opt, size_t ab_bytes) {
+  if (opt && opt->block > 0) return std::min(opt->block, N);
+  const size_t full_x = (size_t)c->c_h * N * align_up(N, 4) * 4;
+  size_t budget = (size_t)32 << 30;
+  const size_t lim = limit_of(c, opt);
+  if (lim) budget = lim > ab_bytes ? std::min(budget, lim - ab_bytes) : 0;
+  if (full_x <= budget) return N;
+  int nb = (N + 2499) / 2500;
+  for (;; ++nb) {
+    const int B = (N + nb - 1) / nb;
+    if ((size_t)c->c_h * B * align_up(B, 4) * 4 <= budget || B <= 256) return B;
+  }
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+
+extern "C" {
+
+const char* tm_status_string(tm_status s) {
+  const int i = (int)s;
+  return (i >= 0 && i < (int)(sizeof kStatusText / sizeof kStatusText[0])) ? kStatusText[i] : "unknown status";
+}
+
+const char* tm_last_error(const tm_ctx* ctx) { return ctx ? ctx->err.c_str() : ""; }
+
+long long tm_launch_count(const tm_ctx* ctx) { return ctx ? ctx->launches : 0; }
+
+size_t tm_workspace_bytes(const tm_ctx* ctx) { return ctx ? ctx->ws_bytes : 0; }
+
+tm_status tm_create(int c_z, int c_hidden, const tm_weights* w, tm_ctx** out_ctx) {
+  if (!w || !out_ctx) return TM_ERR_INVALID;
+  if (c_z < 1 || c_z > 256 || c_hidden < 1 || c_hidden > 256) return TM_ERR_INVALID;
+  const float* req[] = {w->ln_in_gamma, w->ln_in_beta, w->w_a, w->w_ga, w->w_b,
+                        w->w_gb, w->w_g, w->ln_out_gamma, w->ln_out_beta, w->w_o};
+  for (const float* p : req)
+    if (!p) return TM_ERR_INVALID;
+  tm_ctx* c = new tm_ctx();
+  cudaError_t e = cudaGetDevice(&c->device);
+  if (e != cudaSuccess) {
+    delete c;
+    cudaGetLastError();
+    return TM_ERR_CUDA;
+  }
+  cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
+  c->c_z = c_z;
+  c->c_h = c_hidden;
+  if (const char* env = std::getenv("TM_WORKSPACE_LIMIT")) c->env_limit = (size_t)std::strtoull(env, nullptr, 10);
+
+  // float32 weights
+  const size_t n_in = c_z, n_h = c_hidden;
+  const size_t sizes[10] = {n_in, n_in, n_h * n_in, n_h * n_in, n_h * n_in, n_h * n_in, n_in * n_in, n_h, n_h, n_in * n_h};
+  size_t total = 0;
+  for (size_t s : sizes) total += align_up(s, 64);
+  e = cudaMalloc(&c->w32, total * sizeof(float));
+  if (e != cudaSuccess) {
+    delete c;
+    cudaGetLastError();
+    return TM_ERR_CUDA;
+  }
+  const float* ptrs[10];
+  size_t off = 0;
+  for (int k = 0; k < 10; ++k) {
+    cudaMemcpy(c->w32 + off, req[k], sizes[k] * sizeof(float), cudaMemcpyHostToDevice);
+    ptrs[k] = c->w32 + off;
+    off += align_up(sizes[k], 64);
+  }
+  c->f32w = F32Weights{ptrs[0], ptrs[1], ptrs[2], ptrs[3], ptrs[4], ptrs[5], ptrs[6], ptrs[7], ptrs[8], ptrs[9],
+                       c_z, c_hidden};
+
+  e = cudaHostAlloc(reinterpret_cast<void**>(&c->status_h), 64, cudaHostAllocMapped);
+  if (e != cudaSuccess) {
+    tm_destroy(c);
+    cudaGetLastError();
+    return TM_ERR_CUDA;
+  }
+  std::memset(c->status_h, 0, 64);
+  cudaHostGetDevicePointer(reinterpret_cast<void**>(&c->status_d), c->status_h, 0);
+
+  if (c_z == kC && c_hidden == kC) {
+    if (prepare_tensor_core_weights(c, w) != TM_OK) {
+      tm_destroy(c);
+      return TM_ERR_CUDA;
+    }
+    c->tc = true;
+  }
+  *out_ctx = c;
+  return TM_OK;
+}
+
+void tm_destroy(tm_ctx* c) {
+  if (!c) return;
+  cudaDeviceSynchronize();
+  if (c->ws) cudaFree(c->ws);
+  for (void* p : {(void*)c->w32, (void*)c->wk1, (void*)c->k1c, (void*)c->wo16, (void*)c->wg16, (void*)c->k3c})
+    if (p) cudaFree(p);
+  if (c->status_h) cudaFreeHost(c->status_h);
+  for (auto& t : c->timed) {
+    cudaEventDestroy(t.start);
+    cudaEventDestroy(t.stop);
+  }
+  for (auto e : c->event_pool) cudaEventDestroy(e);
+  cudaGetLastError();
+  delete c;
+}
+
+tm_status tm_project(tm_ctx* c, const void* z, const float* mask, int N, tm_dtype dtype, void* a, void* b, int ld,
+                     void* stream) {
+  tm_status st = check_common(c, N, dtype);
+  if (st != TM_OK) return st;
+  if (!z || !a || !b || !aligned16(z) || !aligned16(a) || !aligned16(b))
+    return fail(c, TM_ERR_INVALID, "z, a, b must be non-null and 16-byte aligned");
+  if (mask && (reinterpret_cast<uintptr_t>(mask) & 3u)) return fail(c, TM_ERR_INVALID, "mask must be 4-byte aligned");
+  if (ld < N || (dtype == TM_BF16 && ld % 8)) return fail(c, TM_ERR_INVALID, "ld=%d must be >= N (and a multiple of 8 for bf16)", ld);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == TM_BF16)
+    return run_project_bf16(c, z, mask, N, reinterpret_cast<__nv_bfloat16*>(a), reinterpret_cast<__nv_bfloat16*>(b),
+                            ld, s, nullptr);
+  cudaError_t e = timed(c, 3, (long long)N * N, s, [&] {
+    return launch_project_f32(reinterpret_cast<const float*>(z), mask, c->f32w, reinterpret_cast<float*>(a),
+                              reinterpret_cast<float*>(b), N, ld, s);
+  });
+  return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "projection (f32) launch");
+}
+
+tm_status tm_contract(tm_ctx* c, const void* a, const void* b, int N, int ld, tm_dtype dtype, tm_direction dir,
+                      int i0, int j0, int bi, int bj, float* x, int ldx, void* stream) {
+  tm_status st = check_common(c, N, dtype);
+  if (st != TM_OK) return st;
+  if (dir != TM_OUTGOING && dir != TM_INCOMING) return fail(c, TM_ERR_INVALID, "unknown direction %d", (int)dir);
+  if (!a || !b || !x || !aligned16(a) || !aligned16(b) || !aligned16(x))
+    return fail(c, TM_ERR_INVALID, "a, b, x must be non-null and 16-byte aligned");
+  if (ld < N || (dtype == TM_BF16 && ld % 8)) return fail(c, TM_ERR_INVALID, "bad ld=%d", ld);
+  if (i0 < 0 || j0 < 0 || bi < 1 || bj < 1 || i0 + bi > N || j0 + bj > N)
+    return fail(c, TM_ERR_INVALID, "block (%d,%d)+(%d,%d) outside the %d x %d grid", i0, j0, bi, bj, N, N);
+  if (ldx < bj || ldx % 4) return fail(c, TM_ERR_INVALID, "ldx=%d must be >= bj and a multiple of 4", ldx);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool inc = dir == TM_INCOMING;
+  if (dtype == TM_BF16)
+    return run_contract_bf16(c, reinterpret_cast<const __nv_bfloat16*>(a), reinterpret_cast<const __nv_bfloat16*>(b),
+                             N, ld, inc, i0, j0, bi, bj, x, ldx, s, nullptr);
+  cudaError_t e = timed(c, 3, (long long)c->c_h * bi * bj, s, [&] {
+    return launch_contract_f32(inc, reinterpret_cast<const float*>(a), reinterpret_cast<const float*>(b), N, ld,
+                               c->c_h, i0, j0, bi, bj, x, ldx, (long long)bi * ldx, s);
+  });
+  return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "contraction (f32) launch");
+}
+
+tm_status tm_finish(tm_ctx* c, const float* x, int ldx, const void* z, int N, tm_dtype dtype, int i0, int j0, int bi,
+                    int bj, void* out, void* stream) {
+  tm_status st = check_common(c, N, dtype);
+  if (st != TM_OK) return st;
+  if (!x || !z || !out || !aligned16(x) || !aligned16(z) || !aligned16(out))
+    return fail(c, TM_ERR_INVALID, "x, z, out must be non-null and 16-byte aligned");
+  if (i0 < 0 || j0 < 0 || bi < 1 || bj < 1 || i0 + bi > N || j0 + bj > N)
+    return fail(c, TM_ERR_INVALID, "block outside the grid");
+  if (ldx < bj || ldx % 4) return fail(c, TM_ERR_INVALID, "ldx=%d must be >= bj and a multiple of 4", ldx);
+  const size_t zbytes = (size_t)N * N * c->c_z * (dtype == TM_BF16 ? 2 : 4);
+  if (ranges_overlap(z, zbytes, out, zbytes)) return fail(c, TM_ERR_INVALID, "out overlaps z");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == TM_BF16) return run_finish_bf16(c, x, ldx, z, N, i0, j0, bi, bj, out, s, nullptr);
+  cudaError_t e = timed(c, 3, (long long)bi * bj, s, [&] {
+    return launch_finish_f32(x, ldx, (long long)bi * ldx, reinterpret_cast<const float*>(z), c->f32w, N, i0, j0, bi,
+                             bj, reinterpret_cast<float*>(out), s);
+  });
+  return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "finish (f32) launch");
+}
+
+tm_status tm_forward_ex(tm_ctx* c, const void* z, const float* mask, int N, tm_dtype dtype, tm_direction dir,
+                        void* out, void* stream, const tm_options* opt) {
+  tm_status st = check_common(c, N, dtype);
+  if (st != TM_OK) return st;
+  if (dir != TM_OUTGOING && dir != TM_INCOMING) return fail(c, TM_ERR_INVALID, "unknown direction %d", (int)dir);
+  if (!z || !out || !aligned16(z) || !aligned16(out))
+    return fail(c, TM_ERR_INVALID, "z and out must be non-null and 16-byte aligned");
+  if (mask && (reinterpret_cast<uintptr_t>(mask) & 3u)) return fail(c, TM_ERR_INVALID, "mask must be 4-byte aligned");
+  if (opt) {
+    for (int r : opt->reserved)
+      if (r) return fail(c, TM_ERR_INVALID, "tm_options.reserved must be zero");
+    if (opt->block < 0 || opt->timeout_ms < 0) return fail(c, TM_ERR_INVALID, "negative option");
+  }
+  const size_t esz = dtype == TM_BF16 ? 2 : 4;
+  const size_t zbytes = (size_t)N * N * c->c_z * esz;
+  if (ranges_overlap(z, zbytes, out, zbytes)) return fail(c, TM_ERR_INVALID, "out overlaps z");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool inc = dir == TM_INCOMING;
+
+  const int ld = dtype == TM_BF16 ? (int)align_up(N, 8) : N;
+  const size_t ab_bytes = align_up((size_t)c->c_h * N * ld * esz, 256);
+  const int B = choose_block(c, N, opt, 2 * ab_bytes);
+  const int ldx = (int)align_up(B, 4);
+  const size_t x_bytes = align_up((size_t)c->c_h * B * ldx * 4, 256);
+  st = ensure_workspace(c, 2 * ab_bytes + x_bytes, s, opt);
+  if (st != TM_OK) return st;
+  uint8_t* base = reinterpret_cast<uint8_t*>(c->ws);
+  void* a = base;
+  void* b = base + ab_bytes;
+  float* x = reinterpret_cast<float*>(base + 2 * ab_bytes);
+
+  if (dtype == TM_BF16) {
+    st = run_project_bf16(c, z, mask, N, reinterpret_cast<__nv_bfloat16*>(a), reinterpret_cast<__nv_bfloat16*>(b),
+                          ld, s, opt);
+    if (st != TM_OK) return st;
+    for (int i0 = 0; i0 < N; i0 += B)
+      for (int j0 = 0; j0 < N; j0 += B) {
+        const int bi = std::min(B, N - i0), bj = std::min(B, N - j0);
+        st = run_contract_bf16(c, reinterpret_cast<const __nv_bfloat16*>(a), reinterpret_cast<const __nv_bfloat16*>(b),
+                               N, ld, inc, i0, j0, bi, bj, x, ldx, s, opt);
+        if (st != TM_OK) return st;
+        st = run_finish_bf16(c, x, ldx, z, N, i0, j0, bi, bj, out, s, opt);
+        if (st != TM_OK) return st;
+      }
+    return TM_OK;
+  }
+  // float32 CUDA-core path
+  cudaError_t e = timed(c, 3, (long long)N * N, s, [&] {
+    return launch_project_f32(reinterpret_cast<const float*>(z), mask, c->f32w, reinterpret_cast<float*>(a),
+                              reinterpret_cast<float*>(b), N, ld, s);
+  });
+  if (e != cudaSuccess) return cuda_fail(c, e, "projection (f32) launch");
+  for (int i0 = 0; i0 < N; i0 += B)
+    for (int j0 = 0; j0 < N; j0 += B) {
+      const int bi = std::min(B, N - i0), bj = std::min(B, N - j0);
+      e = timed(c, 3, (long long)c->c_h * bi * bj, s, [&] {
+        return launch_contract_f32(inc, reinterpret_cast<const float*>(a), reinterpret_cast<const float*>(b), N, ld,
+                                   c->c_h, i0, j0, bi, bj, x, ldx, (long long)bi * ldx, s);
+      });
+      if (e != cudaSuccess) return cuda_fail(c, e, "contraction (f32) launch");
+      e = timed(c, 3, (long long)bi * bj, s, [&] {
+        return launch_finish_f32(x, ldx, (long long)bi * ldx, reinterpret_cast<const float*>(z), c->f32w, N, i0, j0,
+                                 bi, bj, reinterpret_cast<float*>(out), s);
+      });
+      if (e != cudaSuccess) return cuda_fail(c, e, "finish (f32) launch");
+    }
+  return TM_OK;
+}
+
+tm_status tm_forward(tm_ctx* c, const void* z, const float* mask, int N, tm_dtype dtype, tm_direction dir, void* out,
+                     void* stream) {
+  return tm_forward_ex(c, z, mask, N, dtype, dir, out, stream, nullptr);
+}
+
+tm_status tm_sync_status(tm_ctx* c, void* stream) {
+  if (!c) return TM_ERR_INVALID;
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(c, e, "cudaStreamSynchronize");
+  return check_device_status(c);
+}
+
+tm_status tm_watchdog_selftest(tm_ctx* c, int timeout_ms, void* stream) {
+  if (!c) return TM_ERR_INVALID;
+  c->err.clear();
+  if (timeout_ms < 1 || timeout_ms > 10000) return fail(c, TM_ERR_INVALID, "timeout_ms=%d outside [1, 10000]", timeout_ms);
+  tm_options o{};
+  o.timeout_ms = timeout_ms;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const Watch w = watch(c, KID_SELFTEST, &o);
+  cudaError_t e = timed(c, 3, 0, s, [&] { return launch_watchdog_selftest(w, s); });
+  return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "self-test launch");
+}
+
+tm_status tm_set_timing(tm_ctx* c, int enable) {
+  if (!c) return TM_ERR_INVALID;
+  for (auto& t : c->timed) {
+    c->event_pool.push_back(t.start);
+    c->event_pool.push_back(t.stop);
+  }
+  c->timed.clear();
+  c->timing = enable != 0;
+  return TM_OK;
+}
+
+tm_status tm_get_timing(tm_ctx* c, tm_timing* out) {
+  if (!c || !out) return TM_ERR_INVALID;
+  std::memset(out, 0, sizeof *out);
+  for (auto& t : c->timed) {
+    cudaError_t e = cudaEventSynchronize(t.stop);
+    if (e != cudaSuccess) return cuda_fail(c, e, "cudaEventSynchronize");
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, t.start, t.stop);
+    out->launches[t.kind] += 1;
+    out->ms[t.kind] += ms;
+    out->units[t.kind] += t.units;
+  }
+  return TM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,85 @@
+// tm_kernels.h -- parameter blocks and host launchers of the libtm kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sm100.cuh"
+
+namespace tmk {
+
+// ----------------------------------------------------------------- bf16 tensor-core path (c_z = c_h = 128)
+constexpr int kC = 128;  // channels of z and of the hidden a/b/x on the tensor-core path
+
+// Projection: a, b = sigmoid(W_g* zh) * (W_* zh) * m_i m_j, channel-major bf16.
+struct ProjectParams {
+  __nv_bfloat16* a;       // [128][N][ld]
+  __nv_bfloat16* b;       // [128][N][ld]
+  const float* mask;      // [N] or nullptr
+  const float* consts;    // [2 halves][512]: rowsum[256] then bias[256] of the folded LayerNorm
+  int N, ld;
+  int tiles_per_row;      // ceil(N / 128)
+  long long total_tiles;  // N * tiles_per_row
+  Watch w;
+};
+
+// Contraction of one output block: x[c][i-i0][j-j0] over k in [0, N).
+struct ContractParams {
+  float* x;               // block buffer [128][bi][ldx]
+  long long ldx;          // row stride (elements)
+  long long chan_stride;  // channel stride (elements)
+  int N;                  // contraction length
+  int i0, j0, bi, bj;     // block origin and extents
+  int tiles_i, tiles_j;   // tiles of the block
+  long long total_tiles;  // 128 * tiles_i * tiles_j
+  Watch w;
+};
+
+// Output epilogue of one block: out = sigmoid(g) * (W_o LayerNorm(x)).
+struct FinishParams {
+  __nv_bfloat16* out;     // [N][N][128]
+  const float* consts;    // [3][128]: rowsum of W_g' (hi+lo), bias W_g beta_in, bias W_o beta_out
+  float inv_scale_o;      // W_o is stored scaled by a power of two; this undoes it
+  int N;
+  int i0, j0, bi, bj;
+  int tiles_j;            // ceil(bj / 128)
+  long long total_tiles;  // bi * tiles_j
+  Watch w;
+};
+
+cudaError_t launch_project_bf16(const CUtensorMap& zmap, const CUtensorMap& wmap, const ProjectParams& p,
+                                int num_sms, cudaStream_t s);
+cudaError_t launch_contract_bf16(bool incoming, const CUtensorMap& amap, const CUtensorMap& bmap,
+                                 const ContractParams& p, int num_sms, cudaStream_t s);
+cudaError_t launch_finish_bf16(const CUtensorMap& xmap, const CUtensorMap& zmap, const CUtensorMap& womap,
+                               const CUtensorMap& wgmap, const FinishParams& p, int num_sms, cudaStream_t s);
+
+// Box shapes of the tensor maps each kernel expects (elements, innermost first).
+constexpr int kProjTileJ = 128;     // pairs per projection tile
+constexpr int kContractBM = 128;    // output rows per contraction tile
+constexpr int kContractBN = 256;    // output columns per contraction tile
+constexpr int kContractBK = 64;     // k per pipeline stage
+constexpr int kFinishTileJ = 128;   // pairs per finish tile
+
+// ----------------------------------------------------------------- float32 CUDA-core path (any c <= 256)
+struct F32Weights {
+  const float *ln_in_g, *ln_in_b, *w_a, *w_ga, *w_b, *w_gb, *w_g, *ln_out_g, *ln_out_b, *w_o;
+  int c_z, c_h;
+};
+
+cudaError_t launch_project_f32(const float* z, const float* mask, const F32Weights& w, float* a, float* b,
+                               int N, int ld, cudaStream_t s);
+cudaError_t launch_contract_f32(bool incoming, const float* a, const float* b, int N, int ld, int c_h, int i0,
+                                int j0, int bi, int bj, float* x, long long ldx, long long chan_stride,
+                                cudaStream_t s);
+cudaError_t launch_finish_f32(const float* x, long long ldx, long long chan_stride, const float* z,
+                              const F32Weights& w, int N, int i0, int j0, int bi, int bj, float* out,
+                              cudaStream_t s);
+
+// ----------------------------------------------------------------- diagnostics
+enum : int { KID_SELFTEST = 9 };
+cudaError_t launch_watchdog_selftest(const Watch& w, cudaStream_t s);
+
+}  // namespace tmk

@@ -1,0 +1,254 @@
+"""Python binding of libtm (include/tm.h): argument marshalling only.
+
+Every step of the update runs in libtm's CUDA kernels; this module converts
+torch tensors to device pointers and the current CUDA stream to a handle, and
+raises ``TmError`` on a non-OK status. torch is used for device memory and
+streams only. There is no fallback: without the built library or without a
+GPU every call raises.
+
+The function names mirror the C ABI: tm_create, tm_forward, tm_forward_ex,
+tm_project, tm_contract, tm_finish, tm_sync_status, tm_watchdog_selftest, tm_set_timing,
+tm_get_timing, tm_launch_count, tm_workspace_bytes, tm_status_string,
+tm_last_error, tm_destroy. ``TriMul`` wraps a context for convenience.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import re
+
+import numpy as np
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "_lib", "libtm.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "tm.h")
+
+TM_OK, TM_ERR_INVALID, TM_ERR_UNSUPPORTED, TM_ERR_OOM, TM_ERR_CUDA, TM_ERR_TIMEOUT = range(6)
+TM_OUTGOING, TM_INCOMING = 0, 1
+TM_F32, TM_BF16 = 0, 1
+DIRECTIONS = {"outgoing": TM_OUTGOING, "incoming": TM_INCOMING}
+
+WEIGHT_FIELDS = ("ln_in_gamma", "ln_in_beta", "w_a", "w_ga", "w_b", "w_gb", "w_g",
+                 "ln_out_gamma", "ln_out_beta", "w_o")
+
+
+class TmWeights(C.Structure):
+    _fields_ = [(n, C.POINTER(C.c_float)) for n in WEIGHT_FIELDS]
+
+
+class TmOptions(C.Structure):
+    _fields_ = [("block", C.c_int), ("timeout_ms", C.c_int), ("workspace_limit", C.c_size_t),
+                ("reserved", C.c_int * 8)]
+
+
+class TmTiming(C.Structure):
+    _fields_ = [("launches", C.c_int * 4), ("ms", C.c_double * 4), ("units", C.c_longlong * 4)]
+
+
+class TmError(RuntimeError):
+    def __init__(self, status, detail=""):
+        self.status = status
+        super().__init__(f"libtm: {tm_status_string(status)} ({status}){': ' + detail if detail else ''}")
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libtm.so and declare its prototypes. Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libtm.so not found at {path}; build it with "
+                           "`python -m pair_representation_boltz_b300.build`")
+    lib = C.CDLL(path)
+    vp, i, st = C.c_void_p, C.c_int, C.c_int
+    sigs = {
+        "tm_create": (st, [i, i, C.POINTER(TmWeights), C.POINTER(vp)]),
+        "tm_forward": (st, [vp, vp, vp, i, i, i, vp, vp]),
+        "tm_forward_ex": (st, [vp, vp, vp, i, i, i, vp, vp, C.POINTER(TmOptions)]),
+        "tm_project": (st, [vp, vp, vp, i, i, vp, vp, i, vp]),
+        "tm_contract": (st, [vp, vp, vp, i, i, i, i, i, i, i, i, vp, i, vp]),
+        "tm_finish": (st, [vp, vp, i, vp, i, i, i, i, i, i, vp, vp]),
+        "tm_sync_status": (st, [vp, vp]),
+        "tm_watchdog_selftest": (st, [vp, i, vp]),
+        "tm_set_timing": (st, [vp, i]),
+        "tm_get_timing": (st, [vp, C.POINTER(TmTiming)]),
+        "tm_launch_count": (C.c_longlong, [vp]),
+        "tm_workspace_bytes": (C.c_size_t, [vp]),
+        "tm_status_string": (C.c_char_p, [st]),
+        "tm_last_error": (C.c_char_p, [vp]),
+        "tm_destroy": (None, [vp]),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def header_functions(path: str = HEADER) -> list[str]:
+    """Names of the functions include/tm.h declares."""
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tm_[a-z_]+)\s*\(", text)))
+
+
+# ------------------------------------------------------------------ marshalling helpers
+
+def _ptr(t):
+    if t is None:
+        return None
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError("tensor must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return TM_BF16
+    if t.dtype == torch.float32:
+        return TM_F32
+    raise TypeError(f"unsupported dtype {t.dtype}; use torch.bfloat16 or torch.float32")
+
+
+def _check(ctx, status):
+    if status != TM_OK:
+        detail = load_library().tm_last_error(ctx).decode() if ctx else ""
+        raise TmError(status, detail)
+
+
+def _direction(d):
+    if isinstance(d, str):
+        if d not in DIRECTIONS:
+            raise ValueError(f"direction must be one of {tuple(DIRECTIONS)}")
+        return DIRECTIONS[d]
+    return int(d)
+
+
+# ------------------------------------------------------------------ C-ABI mirrors
+
+def tm_status_string(status: int) -> str:
+    return load_library().tm_status_string(status).decode()
+
+
+def tm_last_error(ctx) -> str:
+    return load_library().tm_last_error(ctx).decode()
+
+
+def tm_create(c_z: int, c_hidden: int, weights: dict):
+    """Create a context from host float32 weights (dict of numpy arrays, Linear layout [out][in])."""
+    lib = load_library()
+    arrays = {k: np.ascontiguousarray(weights[k], dtype=np.float32) for k in WEIGHT_FIELDS}
+    w = TmWeights(*[a.ctypes.data_as(C.POINTER(C.c_float)) for a in (arrays[k] for k in WEIGHT_FIELDS)])
+    ctx = C.c_void_p()
+    _check(None, lib.tm_create(c_z, c_hidden, C.byref(w), C.byref(ctx)))
+    return ctx
+
+
+def tm_destroy(ctx) -> None:
+    if ctx:
+        load_library().tm_destroy(ctx)
+
+
+def tm_forward_ex(ctx, z, mask, direction, out, stream=None, block=0, timeout_ms=0, workspace_limit=0):
+    N = z.shape[0]
+    opt = TmOptions(block, timeout_ms, workspace_limit)
+    _check(ctx, load_library().tm_forward_ex(ctx, _ptr(z), _ptr(mask), N, _dtype_code(z), _direction(direction),
+                                             _ptr(out), _stream(stream), C.byref(opt)))
+    return out
+
+
+def tm_forward(ctx, z, mask, direction, out, stream=None):
+    N = z.shape[0]
+    _check(ctx, load_library().tm_forward(ctx, _ptr(z), _ptr(mask), N, _dtype_code(z), _direction(direction),
+                                          _ptr(out), _stream(stream)))
+    return out
+
+
+def tm_project(ctx, z, mask, a, b, ld, stream=None):
+    N = z.shape[0]
+    _check(ctx, load_library().tm_project(ctx, _ptr(z), _ptr(mask), N, _dtype_code(z), _ptr(a), _ptr(b), ld,
+                                          _stream(stream)))
+
+
+def tm_contract(ctx, a, b, N, ld, direction, i0, j0, bi, bj, x, ldx, stream=None):
+    _check(ctx, load_library().tm_contract(ctx, _ptr(a), _ptr(b), N, ld, _dtype_code(a), _direction(direction),
+                                           i0, j0, bi, bj, _ptr(x), ldx, _stream(stream)))
+
+
+def tm_finish(ctx, x, ldx, z, i0, j0, bi, bj, out, stream=None):
+    N = z.shape[0]
+    _check(ctx, load_library().tm_finish(ctx, _ptr(x), ldx, _ptr(z), N, _dtype_code(z), i0, j0, bi, bj, _ptr(out),
+                                         _stream(stream)))
+
+
+def tm_sync_status(ctx, stream=None) -> int:
+    return load_library().tm_sync_status(ctx, _stream(stream))
+
+
+def tm_watchdog_selftest(ctx, timeout_ms: int, stream=None) -> None:
+    _check(ctx, load_library().tm_watchdog_selftest(ctx, timeout_ms, _stream(stream)))
+
+
+def tm_set_timing(ctx, enable: bool) -> None:
+    _check(ctx, load_library().tm_set_timing(ctx, 1 if enable else 0))
+
+
+def tm_get_timing(ctx) -> dict:
+    t = TmTiming()
+    _check(ctx, load_library().tm_get_timing(ctx, C.byref(t)))
+    names = ("project", "contract", "finish", "f32")
+    return {n: {"launches": t.launches[k], "ms": t.ms[k], "units": t.units[k]} for k, n in enumerate(names)}
+
+
+def tm_launch_count(ctx) -> int:
+    return load_library().tm_launch_count(ctx)
+
+
+def tm_workspace_bytes(ctx) -> int:
+    return load_library().tm_workspace_bytes(ctx)
+
+
+# ------------------------------------------------------------------ convenience wrapper
+
+class TriMul:
+    """A libtm context: ``TriMul(c_z, c_hidden, weights)(z, mask, "outgoing")``."""
+
+    def __init__(self, c_z: int, c_hidden: int, weights: dict):
+        self.c_z, self.c_hidden = c_z, c_hidden
+        self.ctx = tm_create(c_z, c_hidden, weights)
+
+    def __call__(self, z, mask=None, direction="outgoing", out=None, stream=None, **opts):
+        import torch
+        if out is None:
+            out = torch.empty_like(z)
+        if opts:
+            return tm_forward_ex(self.ctx, z, mask, direction, out, stream, **opts)
+        return tm_forward(self.ctx, z, mask, direction, out, stream)
+
+    def close(self):
+        if self.ctx:
+            tm_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
