@@ -1,0 +1,375 @@
+#!/usr/bin/env python
+"""Benchmark of the triangle multiplicative update on B300 (one JSON line on rank 0).
+
+A step is one pass of the whole path over one synthetic input: the projection,
+contraction and finish kernels of the outgoing update and then of the incoming
+update of the four-chain-complex workload (N = 3605 tokens, c_z = c_h = 128,
+bf16, full mask), both on the same resident z. ``value`` is the algorithmic
+FLOP rate of the whole job, 2 * (2 N^3 c_h + 2 (4 c_h c_z + c_z^2 + c_z c_h) N^2)
+per step, over the device-timed region (CUDA events, max over ranks).
+
+Under torchrun each rank runs an independent replica on its own GPU (the update
+has no data-path exchange step), so per-GPU work is fixed and scaling is weak.
+
+``--impl reference`` times the float64 CPU oracle instead (rank 0 only), each
+step a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "ms per tri-mult update & TFLOP/s (frac of bf16 peak) at N=768/3605/6500"
+FALLBACK_PEAKS = {"bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "hbm_gbs": 6400.0}
+K2_SOURCE = os.path.join(ROOT, "pair_representation_boltz_b300", "csrc", "k2_contract.cu")
+K2_PROFILE = os.path.join(ROOT, "profiles", "k2_contract_complex3605.md")
+
+
+def flops_update(N: int, c_z: int, c_h: int) -> float:
+    """Algorithmic FLOPs of one update: the contraction plus every projection (masked pairs counted)."""
+    return 2.0 * N ** 3 * c_h + 2.0 * (4 * c_h * c_z + c_z * c_z + c_z * c_h) * N ** 2
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def profiled_traffic():
+    """dram bytes per contraction launch from the committed ncu summary, if the kernel is unchanged."""
+    if not os.path.exists(K2_PROFILE):
+        return None
+    text = open(K2_PROFILE).read()
+    h = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    t = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not h or not t:
+        return None
+    cur = hashlib.sha256(open(K2_SOURCE, "rb").read()).hexdigest()
+    return float(t.group(1)) if cur == h.group(1) else None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu = gpu
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu), "-lms", "100"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        sm, mx, reasons = [], 0.0, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def host_cores():
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        blas = [i["num_threads"] for i in info if i.get("user_api") == "blas"]
+        if blas:
+            return max(blas)
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def oracle_sample(z, m, W, w, n_rows, n_cols, seed):
+    """Time the float64 oracle on an n_rows x n_cols grid of entries per direction; returns
+    (seconds, effective TFLOP/s in the update's own FLOP count, description)."""
+    import numpy as np
+
+    import oracle
+    rng = np.random.default_rng(seed)
+    rows = np.sort(rng.choice(w.N, n_rows, replace=False))
+    cols = np.sort(rng.choice(w.N, n_cols, replace=False))
+    t0 = time.perf_counter()
+    for d in w.directions:
+        oracle.sampled(z, m, W, d, rows, cols)
+    dt = time.perf_counter() - t0
+    frac = n_rows * n_cols / float(w.N) ** 2
+    flops = frac * len(w.directions) * flops_update(w.N, w.c_z, w.c_h)
+    desc = (f"{n_rows}x{n_cols} (i,j) entries of each of {len(w.directions)} directions at N={w.N}, exact "
+            f"float64 oracle (a/b rows or columns recomputed); value = their share of the update's FLOPs / time")
+    return dt, flops / dt / 1e12, desc
+
+
+# --------------------------------------------------------------------------- reference arm (CPU oracle)
+
+def run_reference(args, w):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    import numpy as np  # noqa: F401
+
+    import workloads as wl
+    z, m, W = wl.make_inputs(w)
+    for s in range(args.warmup):
+        oracle_sample(z, m, W, w, 2, 2, 1000 + s)
+    total, tfs, desc = 0.0, [], ""
+    for s in range(args.steps):
+        dt, tf, desc = oracle_sample(z, m, W, w, 8, 8, 2000 + s)
+        total += dt
+        tfs.append(tf)
+    value = sum(tfs) / len(tfs)
+    cores = host_cores()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w):
+    return {"workload": f"{w.name}: N={w.N} c_z={w.c_z} c_h={w.c_h} {w.dtype} {w.mask} mask, "
+                        f"{' then '.join(w.directions)} per step",
+            "N": w.N, "c_z": w.c_z, "c_h": w.c_h, "directions": list(w.directions),
+            "block": w.block or None, "chains": list(w.chains) or None,
+            "l2": "inputs larger than L2 (z alone is %.2f GB)" % (w.N * w.N * w.c_z * 2 / 1e9),
+            "parallelism": "replicas"}
+
+
+# --------------------------------------------------------------------------- our arm
+
+def run_ours(args, w):
+    import numpy as np
+    import torch
+
+    import workloads as wl
+    from pair_representation_boltz_b300 import build, tm
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    build.build()
+    tm.load_library()
+
+    z_np, m_np, W = wl.make_inputs(w)
+    zt = torch.from_numpy(z_np.view(np.int16)).view(torch.bfloat16)
+    mt = torch.from_numpy(m_np)
+    z = zt.cuda()
+    mask = mt.cuda()
+    mod = tm.TriMul(w.c_z, w.c_h, W)
+    outs = [torch.empty_like(z) for _ in w.directions]
+    opts = {"block": w.block} if w.block else {}
+
+    def step():
+        for d, o in zip(w.directions, outs):
+            if opts:
+                tm.tm_forward_ex(mod.ctx, z, mask, d, o, **opts)
+            else:
+                tm.tm_forward(mod.ctx, z, mask, d, o)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if tm.tm_sync_status(mod.ctx) != tm.TM_OK:
+        raise RuntimeError("device status after warm-up: " + tm.tm_last_error(mod.ctx))
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    barrier()
+    clocks.start()
+    time.sleep(0.3)                         # let the sampler see the load from its first sample
+    launches0 = tm.tm_launch_count(mod.ctx)
+    tm.tm_set_timing(mod.ctx, True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for _ in range(args.steps):
+        step()
+    ev1.record()
+    barrier()
+    clk = clocks.stop()
+    ms_total = ev0.elapsed_time(ev1)
+    launches = tm.tm_launch_count(mod.ctx) - launches0
+    ktime = tm.tm_get_timing(mod.ctx)
+    tm.tm_set_timing(mod.ctx, False)
+    if tm.tm_sync_status(mod.ctx) != tm.TM_OK:
+        raise RuntimeError("device status after the timed region: " + tm.tm_last_error(mod.ctx))
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_total], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+
+    flops_step = len(w.directions) * flops_update(w.N, w.c_z, w.c_h)
+    value = world * args.steps * flops_step / (ms_total / 1e3) / 1e12
+    peaks, peak_src = read_peaks()
+
+    # dominant kernel: the contraction. FLOPs per launch = 2 * N(k) * channels * output pairs.
+    kc = ktime["contract"]
+    k2_flops = 2.0 * w.N * kc["units"]
+    k2_ms_per_launch = kc["ms"] / max(kc["launches"], 1)
+    k2_tflops = k2_flops / (kc["ms"] / 1e3) / 1e12 if kc["ms"] > 0 else None
+    traffic = profiled_traffic()
+    roofline = {"bound": "tensor", "achieved": k2_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": (k2_tflops / peaks["bf16_tflops"]) if k2_tflops else None,
+                "traffic": traffic, "kernel": "k2_contract", "peak_source": f"bf16 burst, {peak_src}",
+                "frac_of_sustained": (k2_tflops / peaks["bf16_tflops_sustained"]) if k2_tflops else None,
+                "ms_per_launch": k2_ms_per_launch,
+                "flops_per_launch": k2_flops / max(kc["launches"], 1)}
+    kernels = {}
+    tot = sum(v["ms"] for v in ktime.values()) or 1.0
+    for name in ("project", "contract", "finish", "f32"):
+        v = ktime[name]
+        if v["launches"]:
+            kernels[name] = {"launches": v["launches"], "ms_per_launch": v["ms"] / v["launches"],
+                             "share": v["ms"] / tot}
+    # HBM-bound passes: algorithmic bytes per pair (projection: z read + a, b written; finish: x fp32 +
+    # z read + out written)
+    pairs = float(w.N) ** 2
+    kp, kf = ktime["project"], ktime["finish"]
+    if kp["ms"] > 0:
+        kernels["project"]["gbs"] = (kp["units"] * (256 + 512)) / (kp["ms"] / 1e3) / 1e9
+    if kf["ms"] > 0:
+        kernels["finish"]["gbs"] = (kf["units"] * (512 + 256 + 256)) / (kf["ms"] / 1e3) / 1e9
+
+    # e2e: the same step through the C ABI on host buffers (pinned), copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        zp = zt.pin_memory()
+        mp = mt.pin_memory()
+        outs_h = [torch.empty_like(zt).pin_memory() for _ in w.directions]
+
+        def step_host():
+            for d, o in zip(w.directions, outs_h):
+                tm.tm_forward_host(mod.ctx, zp, mp, d, o)
+
+        step_host()
+        torch.cuda.synchronize()
+        k_e2e = max(1, min(args.steps, 5))
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(k_e2e):
+            step_host()
+        e1.record()
+        barrier()
+        ms_e2e = e0.elapsed_time(e1)
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([ms_e2e], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms_e2e = float(t.item())
+        zbytes = z_np.nbytes
+        e2e = {"value": world * k_e2e * flops_step / (ms_e2e / 1e3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": len(w.directions) * (zbytes + m_np.nbytes),
+               "d2h_bytes_per_step": len(w.directions) * zbytes, "steps": k_e2e,
+               "ms_per_step": ms_e2e / k_e2e}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        dt, tf, desc = oracle_sample(z_np, m_np, W, w, args.cpu_rows, args.cpu_rows, 7)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle", "sample": desc,
+               "seconds": dt}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": workload_config(w),
+            "ms_per_update": ms_total / args.steps / len(w.directions),
+            "frac_of_bf16_peak": value / world / peaks["bf16_tflops"],
+            "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches, "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    mod.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="complex3605")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=48, help="side of the oracle's sampled grid")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    import workloads as wl
+    w = wl.WORKLOADS[args.workload]
+    if w.dtype != "bf16":
+        ap.error("the benchmark runs the bf16 workloads")
+    return run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

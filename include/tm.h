@@ -100,6 +100,18 @@ tm_status tm_forward(tm_ctx* ctx, const void* z, const float* mask, int N, tm_dt
 tm_status tm_forward_ex(tm_ctx* ctx, const void* z, const float* mask, int N, tm_dtype dtype,
                         tm_direction dir, void* out, void* stream, const tm_options* opt);
 
+/* tm_forward on HOST buffers: copies z (and mask) host -> device into
+ * ctx-owned device buffers, runs the update, and copies out device -> host,
+ * all stream-ordered on `stream`; returns after enqueueing (synchronise the
+ * stream before reading out).
+ *   z_host     host [N][N][c_z] of dtype (page-locked memory lets the copies
+ *              run asynchronously; pageable memory works but blocks);
+ *   mask_host  host float32 [N] or NULL;
+ *   out_host   host [N][N][c_z] of dtype.
+ * The device copies of z and out are owned by the ctx and freed by tm_destroy. */
+tm_status tm_forward_host(tm_ctx* ctx, const void* z_host, const float* mask_host, int N,
+                          tm_dtype dtype, tm_direction dir, void* out_host, void* stream);
+
 /* The three steps of tm_forward, for callers that keep intermediates.
  *
  * tm_project: a, b = gated, masked projections of LayerNorm(z).

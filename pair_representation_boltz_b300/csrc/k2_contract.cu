@@ -103,8 +103,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t ph = 0;
         for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
           const Tile tl = decode(t, p);
-          const int ia = p.i0 + tl.ti * BM;
-          const int jb = p.j0 + tl.tj * BN;
+          // ia, jb are multiples of 8: the incoming boxes start there along their inner axis
+          const int ia = p.i_base + tl.ti * BM;
+          const int jb = p.j_base + tl.tj * BN;
           for (int kb = 0; kb < KB; ++kb) {
             if (!wait_bounded(&empty[s], ph ^ 1u, p.w, abort_flag, 1)) goto producer_done;
             uint8_t* sa = tiles + s * STAGE_BYTES;
@@ -187,25 +188,27 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t use = (uint32_t)(local >> 1);
         if (!warp_wait_bounded(&tfull[buf], use & 1u, p.w, abort_flag, 5)) break;
         tc_fence_after();
-        const int il = tl.ti * BM + r;  // block-local row
-        const int jl0 = tl.tj * BN;
-        float* xrow = p.x + (long long)tl.c * p.chan_stride + (long long)il * p.ldx + jl0;
+        // block-local row of this thread's TMEM lane, and block-local column of the tile's first column
+        const int il = p.i_base + tl.ti * BM + r - p.i0;
+        const bool row_ok = il >= 0 && il < p.bi;
+        const int jl0 = p.j_base + tl.tj * BN - p.j0;   // in (-8, bj)
+        float* xrow = p.x + (long long)tl.c * p.chan_stride + (long long)(row_ok ? il : 0) * p.ldx;
 #pragma unroll 1
         for (int ch = 0; ch < BN / 32; ++ch) {
           uint32_t v[32];
           tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + ch * 32), v);
           tmem_ld_wait();
           const int jc = jl0 + ch * 32;
-          if (il < p.bi && jc < p.bj) {
-            float* dst = xrow + ch * 32;
-            if (jc + 32 <= p.bj) {
+          if (row_ok && jc < p.bj && jc + 32 > 0) {
+            if (jc >= 0 && jc + 32 <= p.bj && (jc & 3) == 0) {
+              float* dst = xrow + jc;   // 16-byte aligned: x, ldx and chan_stride are multiples of 4
 #pragma unroll
               for (int e = 0; e < 32; e += 4)
                 *reinterpret_cast<uint4*>(dst + e) = make_uint4(v[e], v[e + 1], v[e + 2], v[e + 3]);
             } else {
 #pragma unroll
               for (int e = 0; e < 32; ++e)
-                if (jc + e < p.bj) dst[e] = __uint_as_float(v[e]);
+                if (jc + e >= 0 && jc + e < p.bj) xrow[jc + e] = __uint_as_float(v[e]);
             }
           }
         }

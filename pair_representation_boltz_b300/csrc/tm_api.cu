@@ -89,6 +89,9 @@ struct tm_ctx {
   size_t ws_bytes = 0;
   cudaStream_t ws_stream = nullptr;
   size_t env_limit = 0;
+  // device staging of tm_forward_host
+  void* io = nullptr;
+  size_t io_bytes = 0;
   // instrumentation
   bool timing = false;
   std::vector<TimedLaunch> timed;
@@ -351,8 +354,10 @@ tm_status run_contract_bf16(tm_ctx* c, const __nv_bfloat16* a, const __nv_bfloat
   p.j0 = j0;
   p.bi = bi;
   p.bj = bj;
-  p.tiles_i = (bi + kContractBM - 1) / kContractBM;
-  p.tiles_j = (bj + kContractBN - 1) / kContractBN;
+  p.i_base = i0 & ~7;
+  p.j_base = j0 & ~7;
+  p.tiles_i = (i0 + bi - p.i_base + kContractBM - 1) / kContractBM;
+  p.tiles_j = (j0 + bj - p.j_base + kContractBN - 1) / kContractBN;
   p.total_tiles = (long long)kC * p.tiles_i * p.tiles_j;
   p.w = watch(c, KID_CONTRACT, opt);
   cudaError_t e = timed(c, 1, (long long)kC * bi * bj, s,
@@ -502,6 +507,7 @@ void tm_destroy(tm_ctx* c) {
   if (!c) return;
   cudaDeviceSynchronize();
   if (c->ws) cudaFree(c->ws);
+  if (c->io) cudaFree(c->io);
   for (void* p : {(void*)c->w32, (void*)c->wk1, (void*)c->k1c, (void*)c->wo16, (void*)c->wg16, (void*)c->k3c})
     if (p) cudaFree(p);
   if (c->status_h) cudaFreeHost(c->status_h);
@@ -648,6 +654,44 @@ tm_status tm_forward_ex(tm_ctx* c, const void* z, const float* mask, int N, tm_d
 tm_status tm_forward(tm_ctx* c, const void* z, const float* mask, int N, tm_dtype dtype, tm_direction dir, void* out,
                      void* stream) {
   return tm_forward_ex(c, z, mask, N, dtype, dir, out, stream, nullptr);
+}
+
+tm_status tm_forward_host(tm_ctx* c, const void* z_host, const float* mask_host, int N, tm_dtype dtype,
+                          tm_direction dir, void* out_host, void* stream) {
+  tm_status st = check_common(c, N, dtype);
+  if (st != TM_OK) return st;
+  if (!z_host || !out_host) return fail(c, TM_ERR_INVALID, "z_host and out_host must be non-null");
+  const size_t esz = dtype == TM_BF16 ? 2 : 4;
+  const size_t zbytes = (size_t)N * N * c->c_z * esz;
+  if (ranges_overlap(z_host, zbytes, out_host, zbytes)) return fail(c, TM_ERR_INVALID, "out_host overlaps z_host");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t zb = align_up(zbytes, 256), mb = align_up((size_t)N * 4, 256);
+  const size_t need = 2 * zb + mb;
+  if (c->io_bytes < need) {
+    if (c->io) {
+      cudaError_t e = cudaFreeAsync(c->io, s);
+      if (e != cudaSuccess) return cuda_fail(c, e, "cudaFreeAsync(io)");
+      c->io = nullptr;
+      c->io_bytes = 0;
+    }
+    cudaError_t e = cudaMallocAsync(&c->io, need, s);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      c->io = nullptr;
+      return fail(c, TM_ERR_OOM, "cudaMallocAsync(%zu bytes) for host-buffer staging", need);
+    }
+    c->io_bytes = need;
+  }
+  uint8_t* zd = reinterpret_cast<uint8_t*>(c->io);
+  uint8_t* od = zd + zb;
+  float* md = mask_host ? reinterpret_cast<float*>(zd + 2 * zb) : nullptr;
+  cudaError_t e = cudaMemcpyAsync(zd, z_host, zbytes, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess && md) e = cudaMemcpyAsync(md, mask_host, (size_t)N * 4, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(c, e, "cudaMemcpyAsync(host to device)");
+  st = tm_forward_ex(c, zd, md, N, dtype, dir, od, stream, nullptr);
+  if (st != TM_OK) return st;
+  e = cudaMemcpyAsync(out_host, od, zbytes, cudaMemcpyDeviceToHost, s);
+  return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "cudaMemcpyAsync(device to host)");
 }
 
 tm_status tm_sync_status(tm_ctx* c, void* stream) {

@@ -32,7 +32,9 @@ struct ContractParams {
   long long chan_stride;  // channel stride (elements)
   int N;                  // contraction length
   int i0, j0, bi, bj;     // block origin and extents
-  int tiles_i, tiles_j;   // tiles of the block
+  int i_base, j_base;     // tile grid origin: i0, j0 rounded down to a multiple of 8, so that
+                          // every TMA box starts on a 16-byte boundary along its inner axis
+  int tiles_i, tiles_j;   // tiles covering [i_base, i0 + bi) x [j_base, j0 + bj)
   long long total_tiles;  // 128 * tiles_i * tiles_j
   Watch w;
 };

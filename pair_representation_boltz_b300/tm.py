@@ -6,7 +6,7 @@ raises ``TmError`` on a non-OK status. torch is used for device memory and
 streams only. There is no fallback: without the built library or without a
 GPU every call raises.
 
-The function names mirror the C ABI: tm_create, tm_forward, tm_forward_ex,
+The function names mirror the C ABI: tm_create, tm_forward, tm_forward_ex, tm_forward_host,
 tm_project, tm_contract, tm_finish, tm_sync_status, tm_watchdog_selftest, tm_set_timing,
 tm_get_timing, tm_launch_count, tm_workspace_bytes, tm_status_string,
 tm_last_error, tm_destroy. ``TriMul`` wraps a context for convenience.
@@ -68,6 +68,7 @@ def load_library(path: str = LIB_PATH):
         "tm_create": (st, [i, i, C.POINTER(TmWeights), C.POINTER(vp)]),
         "tm_forward": (st, [vp, vp, vp, i, i, i, vp, vp]),
         "tm_forward_ex": (st, [vp, vp, vp, i, i, i, vp, vp, C.POINTER(TmOptions)]),
+        "tm_forward_host": (st, [vp, vp, vp, i, i, i, vp, vp]),
         "tm_project": (st, [vp, vp, vp, i, i, vp, vp, i, vp]),
         "tm_contract": (st, [vp, vp, vp, i, i, i, i, i, i, i, i, vp, i, vp]),
         "tm_finish": (st, [vp, vp, i, vp, i, i, i, i, i, i, vp, vp]),
@@ -178,6 +179,21 @@ def tm_forward(ctx, z, mask, direction, out, stream=None):
     N = z.shape[0]
     _check(ctx, load_library().tm_forward(ctx, _ptr(z), _ptr(mask), N, _dtype_code(z), _direction(direction),
                                           _ptr(out), _stream(stream)))
+    return out
+
+
+def tm_forward_host(ctx, z, mask, direction, out, stream=None):
+    """z, mask, out: CPU tensors (pin_memory() for asynchronous copies); the stream must be synchronised
+    before out is read."""
+    import torch
+    for t in (z, out) + ((mask,) if mask is not None else ()):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("tm_forward_host takes contiguous host tensors")
+    code = TM_BF16 if z.dtype == torch.bfloat16 else TM_F32
+    N = z.shape[0]
+    _check(ctx, load_library().tm_forward_host(ctx, C.c_void_p(z.data_ptr()),
+                                               C.c_void_p(mask.data_ptr()) if mask is not None else None, N, code,
+                                               _direction(direction), C.c_void_p(out.data_ptr()), _stream(stream)))
     return out
 
 

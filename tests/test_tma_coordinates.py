@@ -1,0 +1,86 @@
+"""Host-side check of the TMA box coordinates the kernels issue (no GPU needed).
+
+A tiled TMA copy must start at an inner-axis coordinate whose byte offset is a
+multiple of 16 (8 elements for bf16/fp16, 4 for fp32). This test replays the
+coordinate arithmetic of the projection, contraction and finish kernels for
+every workload and block schedule the tests and the benchmark use, including
+unaligned block origins, and asserts that rule for each box.
+"""
+import itertools
+
+import pytest
+
+BM, BN, BK = 128, 256, 64          # contraction tile
+PROJ_J = 128                       # projection tile (pairs)
+FIN_J = 128                        # finish tile (pairs)
+
+
+def contraction_boxes(N, i0, j0, bi, bj, incoming):
+    """Yield (tensor, inner coordinate, element bytes) for every box of one contraction launch."""
+    i_base, j_base = i0 & ~7, j0 & ~7
+    tiles_i = (i0 + bi - i_base + BM - 1) // BM
+    tiles_j = (j0 + bj - j_base + BN - 1) // BN
+    kb_n = (N + BK - 1) // BK
+    for ti in range(tiles_i):
+        for tj in range(tiles_j):
+            ia, jb = i_base + ti * BM, j_base + tj * BN
+            for kb in range(kb_n):
+                if not incoming:
+                    yield ("a", kb * BK, 2)
+                    yield ("b", kb * BK, 2)
+                else:
+                    yield ("a", ia, 2)
+                    yield ("a", ia + 64, 2)
+                    for h in range(BN // 64):
+                        yield ("b", jb + 64 * h, 2)
+
+
+def projection_boxes(N):
+    for kc in (0, 1):
+        yield ("z", kc * 64, 2)
+    for kc in (0, 1):
+        yield ("w", kc * 64, 2)
+
+
+def finish_boxes(N, i0, j0, bi, bj):
+    for jt in range((bj + FIN_J - 1) // FIN_J):
+        yield ("x", jt * FIN_J, 4)
+    for kc in (0, 1):
+        yield ("z", kc * 64, 2)
+        yield ("w_o", kc * 64, 2)
+        yield ("w_g", kc * 64, 2)
+
+
+def schedule(N, B):
+    for i0 in range(0, N, B):
+        for j0 in range(0, N, B):
+            yield i0, j0, min(B, N - i0), min(B, N - j0)
+
+
+CASES = [(1, 1), (7, 7), (129, 129), (300, 300), (300, 128), (300, 100), (300, 257), (768, 768),
+         (3605, 3605), (6500, 6500), (10000, 2500), (10000, 2504), (45, 16)]
+
+
+@pytest.mark.parametrize("N,B", CASES)
+def test_inner_coordinates_are_16_byte_aligned(N, B):
+    for incoming in (False, True):
+        for (i0, j0, bi, bj) in schedule(N, B):
+            if N > 3000 and (i0, j0) != (0, 0) and (i0, j0) != (B, B):
+                continue                      # the arithmetic is the same for every interior block
+            for name, x, esz in itertools.chain(contraction_boxes(N, i0, j0, bi, bj, incoming),
+                                                finish_boxes(N, i0, j0, bi, bj)):
+                assert x >= 0 and (x * esz) % 16 == 0, (N, B, incoming, (i0, j0), name, x)
+    for name, x, esz in projection_boxes(N):
+        assert (x * esz) % 16 == 0
+
+
+def test_unaligned_block_origins_are_covered():
+    """Block origins that are not multiples of 8 still yield aligned boxes, and the tiles cover the block."""
+    for (N, i0, j0, bi, bj) in [(129, 3, 43, 121, 85), (300, 100, 257, 200, 43), (50, 1, 2, 49, 48)]:
+        for name, x, esz in contraction_boxes(N, i0, j0, bi, bj, incoming=True):
+            assert (x * esz) % 16 == 0
+        i_base, j_base = i0 & ~7, j0 & ~7
+        tiles_i = (i0 + bi - i_base + BM - 1) // BM
+        tiles_j = (j0 + bj - j_base + BN - 1) // BN
+        assert i_base + tiles_i * BM >= i0 + bi and j_base + tiles_j * BN >= j0 + bj
+        assert 0 <= i0 - i_base < 8 and 0 <= j0 - j_base < 8
