@@ -131,8 +131,13 @@ def test_project_bf16(tm128, torch_cuda, N):
         exp = np.moveaxis(exp, -1, 0)
         diff = np.abs(got - exp)
         ulp = 2 * oracle.half_ulp_bf16(exp)
-        assert np.all(diff <= ulp * 1.0001 + 1e-30), np.max(diff / np.maximum(ulp, 1e-30))
-        assert np.mean(diff > 0) < 2e-3                   # rounding flips only near ties
+        # Before its bf16 rounding the kernel's value carries an absolute error of about
+        # 2^-18 * sqrt(c_z) * |W| (hi + lo weights) plus the fp32 accumulation: ~1e-5 of rms(a).
+        # So an element may land one bf16 step away from the oracle's rounding, and elements
+        # much smaller than rms(a) may be many of their own ulps away in absolute terms.
+        rms = np.sqrt(np.mean(exp * exp))
+        assert np.all(diff <= ulp * 1.0001 + 3e-5 * rms), np.max((diff - ulp) / rms)
+        assert np.mean(diff > 0) < 2e-2                   # rounding flips are rare
         assert np.all(got[:, m == 0, :] == 0) and np.all(got[:, :, m == 0] == 0)
 
 
