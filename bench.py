@@ -361,11 +361,15 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=48, help="side of the oracle's sampled grid")
+    ap.add_argument("--N", type=int, default=0, help="override the workload's token count (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     import workloads as wl
     w = wl.WORKLOADS[args.workload]
+    if args.N:
+        import dataclasses
+        w = dataclasses.replace(w, name=f"{w.name}@N={args.N}", N=args.N, chains=())
     if w.dtype != "bf16":
         ap.error("the benchmark runs the bf16 workloads")
     return run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
