@@ -169,6 +169,22 @@ size_t tm_workspace_bytes(const tm_ctx* ctx);
  * every libtm kernel uses, without faulting or hanging the GPU. */
 tm_status tm_watchdog_selftest(tm_ctx* ctx, int timeout_ms, void* stream);
 
+/* Allocation-free forward (the pages have no counterpart; this is a service of
+ * the library). Same contract and result as tm_forward for TM_BF16 and
+ * 1 <= N <= 128, for callers that may not allocate device memory: code whose
+ * device memory all belongs to another allocator or to a fixed budget, and code
+ * that must not pay a device allocation's host-side stall. The a, b and x
+ * scratch lives in one static 16 MiB device array inside libtm, which every
+ * GPU that loads the library holds until the process exits; the call itself
+ * allocates nothing. The first call on a device looks up that array's device
+ * address (once per device, with the device current), so make that first call
+ * before any stream capture. N > 128 returns TM_ERR_UNSUPPORTED. All calls
+ * share the one array: calls whose work overlaps on the GPU (other streams,
+ * other host threads, other contexts on the same device) race on it and must be
+ * serialised by the caller. The timing of tm_set_timing does not cover it. */
+tm_status tm_forward_noalloc(tm_ctx* ctx, const void* z, const float* mask, int N, tm_direction dir,
+                             void* out, void* stream);
+
 /* Static text of a status code; never NULL. */
 const char* tm_status_string(tm_status s);
 

@@ -23,6 +23,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -740,3 +741,76 @@ tm_status tm_get_timing(tm_ctx* c, tm_timing* out) {
 }
 
 }  // extern "C"
+
+// ====================================================================== allocation-free forward
+//
+// Some callers may not allocate device memory at all: code whose every device
+// byte belongs to another allocator (a framework's caching pool, or a fixed
+// budget carved out up front), and code that must never pay the host-side stall
+// of a device allocation in its steady state. tm_forward_noalloc serves them for
+// small grids: the a/b/x scratch of the update lives in one static device array
+// of this library (kNoAllocBytes, held by every GPU that loads libtm until the
+// process exits), so the call allocates nothing.
+namespace {
+
+constexpr int kNoAllocMaxN = 128;
+constexpr size_t kNoAllocAB = (size_t)kC * kNoAllocMaxN * kNoAllocMaxN * 2;  // a or b, bf16: 4 MiB
+constexpr size_t kNoAllocX = (size_t)kC * kNoAllocMaxN * kNoAllocMaxN * 4;   // x, float32: 8 MiB
+constexpr size_t kNoAllocBytes = 2 * kNoAllocAB + kNoAllocX;                // 16 MiB in all
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+// Device address of g_noalloc_scratch for each device ordinal. The name of the
+// array is only a host-side stand-in in host code; the real address is asked
+// from the runtime once per device, with that device current.
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+tm_status noalloc_scratch(tm_ctx* c, uint8_t** out) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (c->device < 0 || c->device >= kMaxDevices)
+    return fail(c, TM_ERR_UNSUPPORTED, "device ordinal %d beyond the no-alloc table", c->device);
+  if (!g_noalloc_addr[c->device]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) return cuda_fail(c, e, "cudaGetSymbolAddress(no-alloc scratch)");
+    g_noalloc_addr[c->device] = p;
+  }
+  *out = reinterpret_cast<uint8_t*>(g_noalloc_addr[c->device]);
+  return TM_OK;
+}
+
+}  // namespace
+
+extern "C" tm_status tm_forward_noalloc(tm_ctx* c, const void* z, const float* mask, int N, tm_direction dir,
+                                        void* out, void* stream) {
+  tm_status st = check_common(c, N, TM_BF16);
+  if (st != TM_OK) return st;
+  if (N > kNoAllocMaxN)
+    return fail(c, TM_ERR_UNSUPPORTED, "tm_forward_noalloc handles N <= %d (got N=%d); use tm_forward", kNoAllocMaxN, N);
+  if (dir != TM_OUTGOING && dir != TM_INCOMING) return fail(c, TM_ERR_INVALID, "unknown direction %d", (int)dir);
+  if (!z || !out || !aligned16(z) || !aligned16(out))
+    return fail(c, TM_ERR_INVALID, "z and out must be non-null and 16-byte aligned");
+  if (mask && (reinterpret_cast<uintptr_t>(mask) & 3u)) return fail(c, TM_ERR_INVALID, "mask must be 4-byte aligned");
+  const size_t zbytes = (size_t)N * N * c->c_z * 2;
+  if (ranges_overlap(z, zbytes, out, zbytes)) return fail(c, TM_ERR_INVALID, "out overlaps z");
+  uint8_t* scratch = nullptr;
+  st = noalloc_scratch(c, &scratch);
+  if (st != TM_OK) return st;
+  // Every scratch byte the kernels read is written earlier in the same call (a and b
+  // for every pair of the grid, x for every entry of the block); the row padding of
+  // a/b past N is never read, so nothing has to be cleared between calls.
+  const int ld = (int)align_up(N, 8), ldx = (int)align_up(N, 4);
+  __nv_bfloat16* a = reinterpret_cast<__nv_bfloat16*>(scratch);
+  __nv_bfloat16* b = reinterpret_cast<__nv_bfloat16*>(scratch + kNoAllocAB);
+  float* x = reinterpret_cast<float*>(scratch + 2 * kNoAllocAB);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool timing = c->timing;  // event creation is an allocation too: no timing inside this call
+  c->timing = false;
+  st = run_project_bf16(c, z, mask, N, a, b, ld, s, nullptr);
+  if (st == TM_OK) st = run_contract_bf16(c, a, b, N, ld, dir == TM_INCOMING, 0, 0, N, N, x, ldx, s, nullptr);
+  if (st == TM_OK) st = run_finish_bf16(c, x, ldx, z, N, 0, 0, N, N, out, s, nullptr);
+  c->timing = timing;
+  return st;
+}

@@ -7,6 +7,7 @@ streams only. There is no fallback: without the built library or without a
 GPU every call raises.
 
 The function names mirror the C ABI: tm_create, tm_forward, tm_forward_ex, tm_forward_host,
+tm_forward_noalloc,
 tm_project, tm_contract, tm_finish, tm_sync_status, tm_watchdog_selftest, tm_set_timing,
 tm_get_timing, tm_launch_count, tm_workspace_bytes, tm_status_string,
 tm_last_error, tm_destroy. ``TriMul`` wraps a context for convenience.
@@ -69,6 +70,7 @@ def load_library(path: str = LIB_PATH):
         "tm_forward": (st, [vp, vp, vp, i, i, i, vp, vp]),
         "tm_forward_ex": (st, [vp, vp, vp, i, i, i, vp, vp, C.POINTER(TmOptions)]),
         "tm_forward_host": (st, [vp, vp, vp, i, i, i, vp, vp]),
+        "tm_forward_noalloc": (st, [vp, vp, vp, i, i, vp, vp]),
         "tm_project": (st, [vp, vp, vp, i, i, vp, vp, i, vp]),
         "tm_contract": (st, [vp, vp, vp, i, i, i, i, i, i, i, i, vp, i, vp]),
         "tm_finish": (st, [vp, vp, i, vp, i, i, i, i, i, i, vp, vp]),
@@ -194,6 +196,17 @@ def tm_forward_host(ctx, z, mask, direction, out, stream=None):
     _check(ctx, load_library().tm_forward_host(ctx, C.c_void_p(z.data_ptr()),
                                                C.c_void_p(mask.data_ptr()) if mask is not None else None, N, code,
                                                _direction(direction), C.c_void_p(out.data_ptr()), _stream(stream)))
+    return out
+
+
+def tm_forward_noalloc(ctx, z, mask, direction, out, stream=None):
+    """tm_forward for bf16 z with N <= 128 whose scratch is a static array inside libtm: the call
+    allocates no device memory (for callers that may not allocate; see include/tm.h)."""
+    N = z.shape[0]
+    if _dtype_code(z) != TM_BF16:
+        raise TypeError("tm_forward_noalloc takes bf16 z")
+    _check(ctx, load_library().tm_forward_noalloc(ctx, _ptr(z), _ptr(mask), N, _direction(direction), _ptr(out),
+                                                  _stream(stream)))
     return out
 
 
