@@ -126,6 +126,8 @@ tm_status tm_project(tm_ctx* ctx, const void* z, const float* mask, int N, tm_dt
  *   i0, j0  first row / column of the block; bi, bj its extents (>= 1);
  *   x       device float32 [c_h][bi][ldx], ldx >= bj and a multiple of 4;
  *           x[c][i - i0][j - j0] = sum_k a.. b.. as in the header comment.
+ *           Columns [bj, roundup(bj, 4)) of each row may be overwritten (the
+ *           stores move whole 16-byte granules); nothing past them is.
  */
 tm_status tm_contract(tm_ctx* ctx, const void* a, const void* b, int N, int ld, tm_dtype dtype,
                       tm_direction dir, int i0, int j0, int bi, int bj, float* x, int ldx,

@@ -14,44 +14,62 @@
 // exact bf16 z: with W' = W diag(gamma_in),
 //   W zh = rstd * (W' z - mu * rowsum(W')) + W beta_in.
 // W' is split into bf16 hi + lo parts (two MMAs into one fp32 accumulator),
-// which keeps the weights accurate to ~2^-17; mu and rstd come from the same
+// which keeps the weights accurate to ~2^-18; mu and rstd come from the same
 // smem tile in fp32.
 //
 // One CTA per SM. CTA parity selects the half it computes (a: W_a | W_ga, or
 // b: W_b | W_gb), so the two CTAs of a pair read each z tile once from HBM and
 // once from L2. Per tile of 128 pairs (one row i, 128 consecutive j):
-//   warp 0      TMA: z tile (two 64-channel boxes, 128-byte swizzle), 3 stages;
-//               the 256 x 128 hi and lo weights once at start (128 KB).
-//   warp 1      TMEM (2 x 256 columns) and tcgen05.mma: D[p][0..256) =
-//               z_tile x [W'_proj | W'_gate]^T, M = 128, N = 256.
-//   warps 2..5  thread = pair: LayerNorm statistics from the z tile, then the
-//               gated, masked epilogue from TMEM; each channel row of a/b gets
-//               64 contiguous bytes per warp store.
+//   warp 0      TMA: z tile (two 64-channel boxes, 128-byte swizzle), 2 stages;
+//               the hi and lo weights of the half once at start (128 KB).
+//   warp 1      TMEM (2 x 256 columns) and tcgen05.mma with the channels on
+//               the TMEM lanes: D_proj[c][p] = W'_proj z^T and D_gate[c][p] =
+//               W'_gate z^T (M = 128 channels, N = 128 pairs), hi + lo each.
+//   warps 2..9  epilogue, thread = channel: two warps per TMEM lane quadrant
+//               split the 128 pairs; per-channel folding constants live in
+//               registers, per-pair LayerNorm statistics (computed from the z
+//               tile by warps 2..5, one thread per pair) come from shared
+//               memory as one broadcast 16-byte load per pair; the element
+//               math is branch-free (mask as a multiply, two-MUFU sigmoid).
+//               Results go through shared memory: each group of four warps
+//               fills a 128-channel x 64-pair staging box (128-byte swizzle)
+//               that one thread writes out with a TMA store, so every channel
+//               row leaves as a 128-byte line. (Stores straight from the
+//               threads, one channel row per lane, scatter each warp
+//               instruction over 32 DRAM pages and ran 6x slower.) Two named
+//               barriers per tile fence the statistics and staging buffers.
 #include "tm_kernels.h"
 
 namespace tmk {
 namespace {
 
 constexpr int BM = kProjTileJ;                 // pairs per tile
-constexpr int NOUT = 256;                      // outputs per half: projection 128 + gate 128
-constexpr int STAGES = 3;
+constexpr int STAGES = 2;
 constexpr int Z_BYTES = BM * kC * 2;           // 32 KB (two 16 KB K-chunks)
-constexpr int W_CHUNK = NOUT * 64 * 2;         // 32 KB: 256 rows x 64 channels
-constexpr int W_BYTES = 4 * W_CHUNK;           // hi/lo x two K-chunks
-constexpr int THREADS = 192;
-constexpr int SMEM_BYTES = STAGES * Z_BYTES + W_BYTES + 512 * 4 + 256;
+constexpr int W_MAT = kC * kC * 2;             // one 128 x 128 bf16 matrix, two K-chunks: 32 KB
+constexpr int W_BYTES = 4 * W_MAT;             // proj hi, proj lo, gate hi, gate lo
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = 64 + 32 * EPI_WARPS;   // TMA warp, MMA warp, epilogue warps
+constexpr int OUT_BYTES = 2 * (int)kBoxProjOut.bytes();  // two staging boxes: pairs 0-63 and 64-127
+constexpr int STAT_BYTES = BM * 16;            // one float4 per pair: rstd, -rstd*mu, mask, 0
+constexpr int SMEM_BYTES = STAGES * Z_BYTES + W_BYTES + OUT_BYTES + STAT_BYTES + 128;
 constexpr int TMEM_COLS = 512;
 
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(2 * kBoxProjZ.bytes() == Z_BYTES, "z tile = two boxes");
+static_assert(2 * kBoxProjW.bytes() == W_MAT, "weight matrix = two boxes");
+static_assert(kBoxProjOut.d0 * 2 == 128, "a staging row is one 128-byte swizzle row");
 
 __global__ void __launch_bounds__(THREADS, 1)
     k1_project(const __grid_constant__ CUtensorMap zmap, const __grid_constant__ CUtensorMap wmap,
+               const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap,
                const ProjectParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* zs = smem;
-  uint8_t* ws = smem + STAGES * Z_BYTES;
-  float* cst = reinterpret_cast<float*>(ws + W_BYTES);  // rowsum[256], bias[256]
-  uint64_t* zfull = reinterpret_cast<uint64_t*>(cst + 512);
+  uint8_t* ws = smem + STAGES * Z_BYTES;                  // [proj hi, proj lo, gate hi, gate lo]
+  uint8_t* ostg = ws + W_BYTES;                           // [2 boxes][128 channels][128 B], swizzled
+  float4* stats = reinterpret_cast<float4*>(ostg + OUT_BYTES); // [128]: rstd, -rstd*mu, pair mask, 0
+  uint64_t* zfull = reinterpret_cast<uint64_t*>(stats + BM);
   uint64_t* zempty = zfull + STAGES;
   uint64_t* tfull = zempty + STAGES;
   uint64_t* tempty = tfull + 2;
@@ -70,18 +88,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (*abort_flag) raise_status(p.w, ST_TIMEOUT, 90);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&zfull[s], 1);
-      mbar_init(&zempty[s], 1 + 4);  // MMA commit + 4 epilogue warps (statistics read)
+      mbar_init(&zempty[s], 1 + 4);  // MMA commit + the 4 statistics warps
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 4);
+      mbar_init(&tempty[b], EPI_WARPS);
     }
     mbar_init(wfull, 1);
     mbar_init(fin, 1);
     fence_mbar_init();
-  }
-  if (threadIdx.x >= 64) {
-    for (int t = threadIdx.x - 64; t < 512; t += THREADS - 64) cst[t] = p.consts[half * 512 + t];
   }
   if (warp == 1) {
     tmem_alloc(tslot, TMEM_COLS);
@@ -97,10 +112,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0) {
         tma_prefetch_desc(&zmap);
         tma_prefetch_desc(&wmap);
+        // weights: rows (half*2 + hl)*256 + {0: projection, 128: gate} of the [2][2][256][128] array
         mbar_expect_tx(wfull, W_BYTES);
-        for (int hl = 0; hl < 2; ++hl)
+        for (int m = 0; m < 4; ++m) {
+          const int hl = m & 1, gate = m >> 1;
           for (int kc = 0; kc < 2; ++kc)
-            tma_load_2d(ws + (hl * 2 + kc) * W_CHUNK, &wmap, wfull, kc * 64, (half * 2 + hl) * NOUT);
+            tma_load_2d(ws + m * W_MAT + kc * (W_MAT / 2), &wmap, wfull, kc * 64, (half * 2 + hl) * 256 + gate * 128);
+        }
         int s = 0;
         uint32_t ph = 0;
         for (long long u = cta; u < p.total_tiles; u += nctas) {
@@ -119,7 +137,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     } else if (warp == 1) {
       if (lane == 0) {
-        constexpr uint32_t idesc = make_idesc(BM, NOUT, FMT_BF16, false, false);
+        constexpr uint32_t idesc = make_idesc(kC, BM, FMT_BF16, false, false);
         int s = 0;
         uint32_t ph = 0;
         int local = 0;
@@ -131,17 +149,19 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (!wait_bounded(&tempty[buf], (use & 1u) ^ 1u, p.w, abort_flag, 13)) break;
             if (!wait_bounded(&zfull[s], ph, p.w, abort_flag, 14)) break;
             tc_fence_after();
-            const uint32_t d = tmem_base + (uint32_t)(buf * NOUT);
+            const uint32_t d = tmem_base + (uint32_t)(buf * 2 * BM);
             const uint32_t z0 = smem_u32(zs + s * Z_BYTES);
 #pragma unroll
             for (int kc = 0; kc < 2; ++kc) {
 #pragma unroll
               for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t ad = make_sdesc_sw128(z0 + kc * (Z_BYTES / 2) + ks * 32, 16, 1024);
-                const uint64_t bh = make_sdesc_sw128(w0 + (0 * 2 + kc) * W_CHUNK + ks * 32, 16, 1024);
-                const uint64_t bl = make_sdesc_sw128(w0 + (1 * 2 + kc) * W_CHUNK + ks * 32, 16, 1024);
-                mma_f16(d, ad, bh, idesc, (kc | ks) != 0);
-                mma_f16(d, ad, bl, idesc, 1u);
+                const uint32_t off = kc * (W_MAT / 2) + ks * 32;
+                const uint64_t bd = make_sdesc_sw128(z0 + kc * (Z_BYTES / 2) + ks * 32, 16, 1024);
+                const uint32_t acc = (kc | ks) != 0;
+                mma_f16(d, make_sdesc_sw128(w0 + 0 * W_MAT + off, 16, 1024), bd, idesc, acc);
+                mma_f16(d, make_sdesc_sw128(w0 + 1 * W_MAT + off, 16, 1024), bd, idesc, 1u);
+                mma_f16(d + BM, make_sdesc_sw128(w0 + 2 * W_MAT + off, 16, 1024), bd, idesc, acc);
+                mma_f16(d + BM, make_sdesc_sw128(w0 + 3 * W_MAT + off, 16, 1024), bd, idesc, 1u);
               }
             }
             mma_commit(&zempty[s]);
@@ -156,88 +176,125 @@ __global__ void __launch_bounds__(THREADS, 1)
         wait_bounded(fin, 0, p.w, abort_flag, 15);
       }
     } else {
-      // ------------------------------------------------------------ statistics + epilogue, thread = pair
-      const int q = warp & 3;
-      const int r = q * 32 + lane;
-      __nv_bfloat16* const outp = half ? p.b : p.a;
-      const size_t chan = (size_t)p.N * (size_t)p.ld;
+      // ------------------------------------------------------------ epilogue, thread = channel
+      const int ew = warp - 2;                 // 0..7
+      const int q = warp & 3;                  // TMEM lane quadrant: channels 32q .. 32q+31
+      const int c = q * 32 + lane;
+      const int grp = ew >> 2;                 // staging box: pairs 64*grp .. 64*grp + 63
+      const int pbase = grp * 64;              // this warp's 64 pair columns
+      const bool issuer = (ew & 3) == 0 && lane == 0;   // one thread per box issues its TMA store
+      const CUtensorMap* omap = half ? &bmap : &amap;
+      uint8_t* const box = ostg + grp * (int)kBoxProjOut.bytes();
+      const bool stat_warp = ew < 4;           // warps 2..5 also compute the per-pair statistics
+      const float* cst = p.consts + half * 512;
+      const float rs_p = cst[c], rs_g = cst[kC + c], b_p = cst[256 + c], b_g = cst[256 + kC + c];
+      if (issuer) tma_prefetch_desc(omap);
       int s = 0;
       uint32_t ph = 0;
       int local = 0;
       for (long long u = cta; u < p.total_tiles; u += nctas, ++local) {
         const int i = (int)(u / p.tiles_per_row);
         const int jt = (int)(u - (long long)i * p.tiles_per_row);
-        const int j = jt * BM + r;
-        const bool valid = j < p.N;
-        // LayerNorm statistics of z_ij over its 128 channels (fp32, two passes over registers)
-        if (!warp_wait_bounded(&zfull[s], ph, p.w, abort_flag, 16)) break;
-        const uint8_t* zt = zs + s * Z_BYTES;
-        uint4 raw[16];
+        bool ok = true;
+        if (stat_warp) ok = warp_wait_bounded(&zfull[s], ph, p.w, abort_flag, 16);
+        if (stat_warp && ok) {
+          // LayerNorm statistics of pair t = ew*32 + lane over its 128 channels (fp32, two passes)
+          const int t = ew * 32 + lane;
+          const uint8_t* zt = zs + s * Z_BYTES;
+          uint4 raw[16];
 #pragma unroll
-        for (int kc = 0; kc < 2; ++kc)
+          for (int kc = 0; kc < 2; ++kc)
 #pragma unroll
-          for (int uu = 0; uu < 8; ++uu)
-            raw[kc * 8 + uu] = *reinterpret_cast<const uint4*>(zt + kc * (Z_BYTES / 2) + sw128_offset(r, uu));
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&zempty[s]);
+            for (int uu = 0; uu < 8; ++uu)
+              raw[kc * 8 + uu] = *reinterpret_cast<const uint4*>(zt + kc * (Z_BYTES / 2) + sw128_offset(t, uu));
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&zempty[s]);
+          float sum = 0.f;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[k]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = __bfloat1622float2(h[e]);
+              sum += f.x + f.y;
+            }
+          }
+          const float mu = sum * (1.0f / kC);
+          float ss = 0.f;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[k]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = __bfloat1622float2(h[e]);
+              ss += (f.x - mu) * (f.x - mu) + (f.y - mu) * (f.y - mu);
+            }
+          }
+          const float rstd = rsqrtf(ss * (1.0f / kC) + 1e-5f);
+          const int j = jt * BM + t;
+          float m = 0.f;
+          if (j < p.N) m = p.mask ? p.mask[i] * p.mask[j] : 1.0f;
+          stats[t] = make_float4(rstd, -rstd * mu, m, 0.f);
+        }
         if (++s == STAGES) {
           s = 0;
           ph ^= 1u;
         }
-        float sum = 0.f;
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[k]);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 f = __bfloat1622float2(h[e]);
-            sum += f.x + f.y;
-          }
-        }
-        const float mu = sum * (1.0f / kC);
-        float ss = 0.f;
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[k]);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 f = __bfloat1622float2(h[e]);
-            ss += (f.x - mu) * (f.x - mu) + (f.y - mu) * (f.y - mu);
-          }
-        }
-        const float rstd = rsqrtf(ss * (1.0f / kC) + 1e-5f);
-        float m = 0.f;
-        if (valid) m = p.mask ? p.mask[i] * p.mask[j] : 1.0f;
+        // the previous tile's stores have finished reading the staging boxes
+        if (issuer) bulk_wait_read<0>();
+        // barrier 1: the tile's statistics are complete and the staging boxes are free. Every warp stops
+        // here together once any wait of the CTA has given up (a warp that left alone would strand the
+        // others at the barrier).
+        if (named_bar_or(1, 32 * EPI_WARPS, !ok || *abort_flag != 0)) break;
 
         const int buf = local & 1;
         const uint32_t use = (uint32_t)(local >> 1);
-        if (!warp_wait_bounded(&tfull[buf], use & 1u, p.w, abort_flag, 17)) break;
-        tc_fence_after();
-        __nv_bfloat16* dst = outp + (size_t)i * p.ld + j;
+        ok = warp_wait_bounded(&tfull[buf], use & 1u, p.w, abort_flag, 17);
+        if (ok) {
+          tc_fence_after();
 #pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t pr[32], gt[32];
-          const uint32_t ta = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * NOUT + cc * 32);
-          tmem_ld32(ta, pr);
-          tmem_ld32(ta + 128, gt);
-          tmem_ld_wait();
-          if (valid) {
+          for (int cc = 0; cc < 2; ++cc) {
+            const int p0 = pbase + cc * 32;       // first pair column of this chunk
+            uint32_t pr[32], gt[32];
+            const uint32_t ta = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * 2 * BM + p0);
+            tmem_ld32(ta, pr);
+            tmem_ld32(ta + BM, gt);
+            tmem_ld_wait();
+            uint32_t packed[16];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int c = cc * 32 + e;
-              const float pre = rstd * (__uint_as_float(pr[e]) - mu * cst[c]) + cst[256 + c];
-              const float gpre = rstd * (__uint_as_float(gt[e]) - mu * cst[128 + c]) + cst[384 + c];
-              dst[(size_t)c * chan] = __float2bfloat16_rn(sigmoidf_fast(gpre) * pre * m);
+            for (int e = 0; e < 32; e += 2) {
+              const float4 s0 = stats[p0 + e];
+              const float4 s1 = stats[p0 + e + 1];
+              const float pre0 = fmaf(s0.x, __uint_as_float(pr[e]), fmaf(s0.y, rs_p, b_p));
+              const float pre1 = fmaf(s1.x, __uint_as_float(pr[e + 1]), fmaf(s1.y, rs_p, b_p));
+              const float g0 = fmaf(s0.x, __uint_as_float(gt[e]), fmaf(s0.y, rs_g, b_g));
+              const float g1 = fmaf(s1.x, __uint_as_float(gt[e + 1]), fmaf(s1.y, rs_g, b_g));
+              packed[e >> 1] = pack_bf16x2(sigmoid_mufu(g0) * pre0 * s0.z, sigmoid_mufu(g1) * pre1 * s1.z);
             }
+            // 64 bytes of this channel's row of the staging box: 16-byte units 4cc .. 4cc+3
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              *reinterpret_cast<uint4*>(box + sw128_offset(c, cc * 4 + k)) =
+                  make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
           }
+          fence_proxy_async_smem();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[buf]);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[buf]);
+        // barrier 2: the staging boxes are complete, and every warp is done with this tile's statistics
+        // before they are overwritten
+        if (named_bar_or(2, 32 * EPI_WARPS, !ok || *abort_flag != 0)) break;
+        // pairs past N are clipped by TMA (whole 16-byte granules, inside the row padding of ld)
+        if (issuer && jt * BM + pbase < p.N) {
+          tma_store_3d(omap, box, jt * BM + pbase, i, 0);
+          bulk_commit();
+        }
       }
     }
   }
 
+  if (warp >= 2 && lane == 0 && ((warp - 2) & 3) == 0) bulk_wait_all();   // stores out before exit
   __syncthreads();
   if (*abort_flag) {
     const uint64_t t0 = gtimer();
@@ -252,8 +309,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 }  // namespace
 
-cudaError_t launch_project_bf16(const CUtensorMap& zmap, const CUtensorMap& wmap, const ProjectParams& p,
-                                int num_sms, cudaStream_t s) {
+cudaError_t launch_project_bf16(const CUtensorMap& zmap, const CUtensorMap& wmap, const CUtensorMap& amap,
+                                const CUtensorMap& bmap, const ProjectParams& p, int num_sms, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(k1_project, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
@@ -264,7 +321,7 @@ cudaError_t launch_project_bf16(const CUtensorMap& zmap, const CUtensorMap& wmap
   long long pairs = num_sms / 2;
   if (pairs > p.total_tiles) pairs = p.total_tiles;
   if (pairs < 1) pairs = 1;
-  k1_project<<<(int)(2 * pairs), THREADS, SMEM_BYTES, s>>>(zmap, wmap, p);
+  k1_project<<<(int)(2 * pairs), THREADS, SMEM_BYTES, s>>>(zmap, wmap, amap, bmap, p);
   return cudaGetLastError();
 }
 

@@ -18,7 +18,12 @@
 //               (M = 128, N = 256, K = 16 per instruction, f32 accumulate),
 //               two TMEM accumulators so the epilogue of one tile overlaps the
 //               main loop of the next.
-//   warps 2..5  epilogue: tcgen05.ld 32 columns at a time, 16-byte stores of x.
+//   warps 2..5  epilogue: tcgen05.ld 32 columns at a time into a per-warp
+//               128-byte-swizzled staging tile (two per warp), TMA store of
+//               each 32 x 32 float32 sub-tile; TMA clips the block edges.
+//               (Blocks whose origin is not a multiple of 8 fall back to
+//               direct 16-byte stores: a TMA box must not start below zero or
+//               off its 16-byte inner-axis grid.)
 // Incoming reads the same a/b buffers through tensor maps whose box runs
 // along the other pair index ("transposed" boxes), and tells the MMA that A
 // and B are M/N-major; no transpose is ever materialised. k beyond N is
@@ -35,9 +40,14 @@ constexpr int B_BYTES = BN * BK * 2;          // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 2 * BN;             // two accumulators
 constexpr int THREADS = 192;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 256;
+constexpr int STG_BYTES = 32 * 32 * 4;         // one 32 x 32 float32 staging tile
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 4 * 2 * STG_BYTES + 256;
 
 static_assert(TMEM_COLS == 512, "two 256-column accumulators fill TMEM");
+static_assert(kBoxContractOutA.bytes() == A_BYTES && kBoxContractOutB.bytes() == B_BYTES, "outgoing boxes");
+static_assert(2 * kBoxContractIn.bytes() == A_BYTES && (BN / 64) * kBoxContractIn.bytes() == B_BYTES,
+              "incoming boxes");
+static_assert(kBoxContractX.bytes() == 32 * 32 * 4, "x store box");
 
 struct Tile {
   int c, ti, tj;
@@ -55,10 +65,11 @@ __device__ __forceinline__ Tile decode(long long t, const ContractParams& p) {
 template <bool INCOMING>
 __global__ void __launch_bounds__(THREADS, 1)
     k2_contract(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap,
-                const ContractParams p) {
+                const __grid_constant__ CUtensorMap xmap, const ContractParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* tiles = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* stg = smem + STAGES * STAGE_BYTES;     // [epilogue warp][2][32 x 32 float32], 1024-aligned
+  uint64_t* full = reinterpret_cast<uint64_t*>(stg + 4 * 2 * STG_BYTES);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
@@ -181,6 +192,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       // ------------------------------------------------------------ epilogue
       const int q = warp & 3;  // TMEM lanes 32q .. 32q+31 belong to this warp
       const int r = q * 32 + lane;
+      uint8_t* const my_stg = stg + (warp - 2) * 2 * STG_BYTES;
+      int sb = 0;
+      if (lane == 0 && p.tma_store) tma_prefetch_desc(&xmap);
       int local = 0;
       for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++local) {
         const Tile tl = decode(t, p);
@@ -188,6 +202,39 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t use = (uint32_t)(local >> 1);
         if (!warp_wait_bounded(&tfull[buf], use & 1u, p.w, abort_flag, 5)) break;
         tc_fence_after();
+        if (p.tma_store) {
+          // i_base == i0 and j_base == j0 here, so every coordinate is >= 0 and 32-aligned along j
+          const int row0 = tl.ti * BM + q * 32;
+#pragma unroll 1
+          for (int ch = 0; ch < BN / 32; ++ch) {
+            const int col0 = tl.tj * BN + ch * 32;
+            // Sub-tiles wholly outside the block are neither staged nor stored (warp-uniform). Every
+            // staging write below is followed by exactly one committed store, which is what makes
+            // "at most one group still reading" mean "the other buffer's store, not this one's".
+            if (row0 >= p.bi || col0 >= p.bj) break;
+            uint32_t v[32];
+            tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + ch * 32), v);
+            tmem_ld_wait();
+            uint8_t* sbuf = my_stg + sb * STG_BYTES;
+            if (lane == 0) bulk_wait_read<1>();   // the store that last read this buffer is done with it
+            __syncwarp();
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              *reinterpret_cast<uint4*>(sbuf + sw128_offset(lane, u)) =
+                  make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&xmap, sbuf, col0, row0, tl.c);
+              bulk_commit();
+            }
+            sb ^= 1;
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[buf]);
+          continue;
+        }
         // block-local row of this thread's TMEM lane, and block-local column of the tile's first column
         const int il = p.i_base + tl.ti * BM + r - p.i0;
         const bool row_ok = il >= 0 && il < p.bi;
@@ -216,6 +263,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[buf]);
       }
+      if (lane == 0) bulk_wait_all();   // stores done before the CTA's shared memory goes away
     }
   }
 
@@ -235,7 +283,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 }  // namespace
 
 cudaError_t launch_contract_bf16(bool incoming, const CUtensorMap& amap, const CUtensorMap& bmap,
-                                 const ContractParams& p, int num_sms, cudaStream_t s) {
+                                 const CUtensorMap& xmap, const ContractParams& p, int num_sms, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(k2_contract<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -248,9 +296,9 @@ cudaError_t launch_contract_bf16(bool incoming, const CUtensorMap& amap, const C
   if (p.total_tiles <= 0) return cudaSuccess;
   const int grid = (int)(p.total_tiles < num_sms ? p.total_tiles : num_sms);
   if (incoming)
-    k2_contract<true><<<grid, THREADS, SMEM_BYTES, s>>>(amap, bmap, p);
+    k2_contract<true><<<grid, THREADS, SMEM_BYTES, s>>>(amap, bmap, xmap, p);
   else
-    k2_contract<false><<<grid, THREADS, SMEM_BYTES, s>>>(amap, bmap, p);
+    k2_contract<false><<<grid, THREADS, SMEM_BYTES, s>>>(amap, bmap, xmap, p);
   return cudaGetLastError();
 }
 

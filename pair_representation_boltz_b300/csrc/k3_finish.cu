@@ -36,6 +36,9 @@ constexpr int SMEM_BYTES = X_BYTES + XH_BYTES + Z_BYTES + WO_BYTES + WG_BYTES + 
 constexpr int TMEM_COLS = 512;
 
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(kBoxFinishX.bytes() == X_BYTES, "x tile = one box");
+static_assert(2 * kBoxFinishZ.bytes() == Z_BYTES, "z tile = two boxes");
+static_assert(2 * kBoxFinishW.bytes() == WO_BYTES && 4 * kBoxFinishW.bytes() == WG_BYTES, "weight boxes");
 
 __global__ void __launch_bounds__(THREADS, 1)
     k3_finish(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap zmap,

@@ -121,12 +121,16 @@ tm_status cuda_fail(tm_ctx* c, cudaError_t e, const char* what) {
 }
 
 bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const cuuint64_t* dims,
-            const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle sw) {
+            const cuuint64_t* strides, const Box& b, CUtensorMapSwizzle sw) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
+  const uint32_t esz = dt == CU_TENSOR_MAP_DATA_TYPE_FLOAT32 ? 4u : 2u;
+  if (esz != b.esz || (rank == 2 && b.d2 != 1)) return false;   // the box constant must match the map
+  const cuuint32_t shape[3] = {b.d0, b.d1, b.d2};
   cuuint32_t es[5] = {1, 1, 1, 1, 1};
-  return fn(m, dt, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fn(m, dt, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, shape, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 Watch watch(const tm_ctx* c, int kernel, const tm_options* opt) {
@@ -288,18 +292,16 @@ tm_status prepare_tensor_core_weights(tm_ctx* c, const tm_weights* w) {
   {
     const cuuint64_t dims[2] = {(cuuint64_t)C, 1024};
     const cuuint64_t str[1] = {(cuuint64_t)C * 2};
-    const cuuint32_t box[2] = {64, 256};
-    if (!encode(&c->wk1_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c->wk1, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!encode(&c->wk1_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c->wk1, dims, str, kBoxProjW, CU_TENSOR_MAP_SWIZZLE_128B))
       return fail(c, TM_ERR_CUDA, "tensor map (projection weights)");
   }
   {
     const cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)C};
     const cuuint64_t str[1] = {(cuuint64_t)C * 2};
-    const cuuint32_t box[2] = {64, 128};
-    if (!encode(&c->wo_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, c->wo16, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!encode(&c->wo_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, c->wo16, dims, str, kBoxFinishW, CU_TENSOR_MAP_SWIZZLE_128B))
       return fail(c, TM_ERR_CUDA, "tensor map (W_o)");
     const cuuint64_t dims2[2] = {(cuuint64_t)C, (cuuint64_t)(2 * C)};
-    if (!encode(&c->wg_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c->wg16, dims2, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!encode(&c->wg_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c->wg16, dims2, str, kBoxFinishW, CU_TENSOR_MAP_SWIZZLE_128B))
       return fail(c, TM_ERR_CUDA, "tensor map (W_g)");
   }
   return TM_OK;
@@ -311,9 +313,16 @@ tm_status run_project_bf16(tm_ctx* c, const void* z, const float* mask, int N, _
   CUtensorMap zmap;
   const cuuint64_t dims[3] = {(cuuint64_t)kC, (cuuint64_t)N, (cuuint64_t)N};
   const cuuint64_t str[2] = {(cuuint64_t)kC * 2, (cuuint64_t)N * kC * 2};
-  const cuuint32_t box[3] = {64, (cuuint32_t)kProjTileJ, 1};
-  if (!encode(&zmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, z, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+  if (!encode(&zmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, z, dims, str, kBoxProjZ, CU_TENSOR_MAP_SWIZZLE_128B))
     return fail(c, TM_ERR_CUDA, "tensor map (z, projection)");
+  CUtensorMap amap, bmap;
+  {
+    const cuuint64_t od[3] = {(cuuint64_t)N, (cuuint64_t)N, (cuuint64_t)kC};
+    const cuuint64_t os[2] = {(cuuint64_t)ld * 2, (cuuint64_t)N * ld * 2};
+    if (!encode(&amap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a, od, os, kBoxProjOut, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode(&bmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, b, od, os, kBoxProjOut, CU_TENSOR_MAP_SWIZZLE_128B))
+      return fail(c, TM_ERR_CUDA, "tensor map (a/b, projection store)");
+  }
   ProjectParams p;
   p.a = a;
   p.b = b;
@@ -324,7 +333,7 @@ tm_status run_project_bf16(tm_ctx* c, const void* z, const float* mask, int N, _
   p.tiles_per_row = (N + kProjTileJ - 1) / kProjTileJ;
   p.total_tiles = (long long)N * p.tiles_per_row;
   p.w = watch(c, KID_PROJECT, opt);
-  cudaError_t e = timed(c, 0, (long long)N * N, s, [&] { return launch_project_bf16(zmap, c->wk1_map, p, c->num_sms, s); });
+  cudaError_t e = timed(c, 0, (long long)N * N, s, [&] { return launch_project_bf16(zmap, c->wk1_map, amap, bmap, p, c->num_sms, s); });
   return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "projection launch");
 }
 
@@ -335,15 +344,12 @@ tm_status run_contract_bf16(tm_ctx* c, const __nv_bfloat16* a, const __nv_bfloat
   const cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)N, (cuuint64_t)kC};
   const cuuint64_t str[2] = {(cuuint64_t)ld * 2, (cuuint64_t)N * ld * 2};
   if (!incoming) {
-    const cuuint32_t boxa[3] = {(cuuint32_t)kContractBK, (cuuint32_t)kContractBM, 1};
-    const cuuint32_t boxb[3] = {(cuuint32_t)kContractBK, (cuuint32_t)kContractBN, 1};
-    if (!encode(&amap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a, dims, str, boxa, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode(&bmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, b, dims, str, boxb, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!encode(&amap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a, dims, str, kBoxContractOutA, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode(&bmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, b, dims, str, kBoxContractOutB, CU_TENSOR_MAP_SWIZZLE_128B))
       return fail(c, TM_ERR_CUDA, "tensor map (a/b, outgoing)");
   } else {
-    const cuuint32_t box[3] = {64, (cuuint32_t)kContractBK, 1};
-    if (!encode(&amap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode(&bmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, b, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!encode(&amap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a, dims, str, kBoxContractIn, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode(&bmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, b, dims, str, kBoxContractIn, CU_TENSOR_MAP_SWIZZLE_128B))
       return fail(c, TM_ERR_CUDA, "tensor map (a/b, incoming)");
   }
   ContractParams p;
@@ -360,9 +366,19 @@ tm_status run_contract_bf16(tm_ctx* c, const __nv_bfloat16* a, const __nv_bfloat
   p.tiles_i = (i0 + bi - p.i_base + kContractBM - 1) / kContractBM;
   p.tiles_j = (j0 + bj - p.j_base + kContractBN - 1) / kContractBN;
   p.total_tiles = (long long)kC * p.tiles_i * p.tiles_j;
+  // TMA stores need every box to start at a non-negative, 16-byte-aligned coordinate: block origins on the
+  // 8-element grid give i_base == i0 and j_base == j0, so the tiles start at 0 in the block's own x map.
+  p.tma_store = ((i0 & 7) == 0 && (j0 & 7) == 0) ? 1 : 0;
+  CUtensorMap xmap;
+  {
+    const cuuint64_t xd[3] = {(cuuint64_t)bj, (cuuint64_t)bi, (cuuint64_t)kC};
+    const cuuint64_t xs[2] = {(cuuint64_t)ldx * 4, (cuuint64_t)bi * ldx * 4};
+    if (!encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, x, xd, xs, kBoxContractX, CU_TENSOR_MAP_SWIZZLE_128B))
+      return fail(c, TM_ERR_CUDA, "tensor map (x, contraction store)");
+  }
   p.w = watch(c, KID_CONTRACT, opt);
   cudaError_t e = timed(c, 1, (long long)kC * bi * bj, s,
-                        [&] { return launch_contract_bf16(incoming, amap, bmap, p, c->num_sms, s); });
+                        [&] { return launch_contract_bf16(incoming, amap, bmap, xmap, p, c->num_sms, s); });
   return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "contraction launch");
 }
 
@@ -372,15 +388,13 @@ tm_status run_finish_bf16(tm_ctx* c, const float* x, int ldx, const void* z, int
   {
     const cuuint64_t dims[3] = {(cuuint64_t)bj, (cuuint64_t)bi, (cuuint64_t)kC};
     const cuuint64_t str[2] = {(cuuint64_t)ldx * 4, (cuuint64_t)bi * ldx * 4};
-    const cuuint32_t box[3] = {(cuuint32_t)kFinishTileJ, 1, (cuuint32_t)kC};
-    if (!encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, x, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (!encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, x, dims, str, kBoxFinishX, CU_TENSOR_MAP_SWIZZLE_NONE))
       return fail(c, TM_ERR_CUDA, "tensor map (x)");
   }
   {
     const cuuint64_t dims[3] = {(cuuint64_t)kC, (cuuint64_t)N, (cuuint64_t)N};
     const cuuint64_t str[2] = {(cuuint64_t)kC * 2, (cuuint64_t)N * kC * 2};
-    const cuuint32_t box[3] = {64, (cuuint32_t)kFinishTileJ, 1};
-    if (!encode(&zmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, z, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!encode(&zmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, z, dims, str, kBoxFinishZ, CU_TENSOR_MAP_SWIZZLE_128B))
       return fail(c, TM_ERR_CUDA, "tensor map (z, finish)");
   }
   FinishParams p;
@@ -422,7 +436,7 @@ int choose_block(const tm_ctx* c, int N, const tm_options* opt, size_t ab_bytes)
   if (full_x <= budget) return N;
   int nb = (N + 2499) / 2500;
   for (;; ++nb) {
-    const int B = (N + nb - 1) / nb;
+    const int B = (int)align_up((size_t)((N + nb - 1) / nb), 8);   // block origins on the 8-element grid
     if ((size_t)c->c_h * B * align_up(B, 4) * 4 <= budget || B <= 256) return B;
   }
 }

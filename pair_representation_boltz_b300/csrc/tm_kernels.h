@@ -36,6 +36,7 @@ struct ContractParams {
                           // every TMA box starts on a 16-byte boundary along its inner axis
   int tiles_i, tiles_j;   // tiles covering [i_base, i0 + bi) x [j_base, j0 + bj)
   long long total_tiles;  // 128 * tiles_i * tiles_j
+  int tma_store;          // 1: x leaves through TMA stores (needs i0, j0 multiples of 8); 0: direct stores
   Watch w;
 };
 
@@ -51,19 +52,37 @@ struct FinishParams {
   Watch w;
 };
 
-cudaError_t launch_project_bf16(const CUtensorMap& zmap, const CUtensorMap& wmap, const ProjectParams& p,
-                                int num_sms, cudaStream_t s);
+cudaError_t launch_project_bf16(const CUtensorMap& zmap, const CUtensorMap& wmap, const CUtensorMap& amap,
+                                const CUtensorMap& bmap, const ProjectParams& p, int num_sms, cudaStream_t s);
 cudaError_t launch_contract_bf16(bool incoming, const CUtensorMap& amap, const CUtensorMap& bmap,
-                                 const ContractParams& p, int num_sms, cudaStream_t s);
+                                 const CUtensorMap& xmap, const ContractParams& p, int num_sms, cudaStream_t s);
 cudaError_t launch_finish_bf16(const CUtensorMap& xmap, const CUtensorMap& zmap, const CUtensorMap& womap,
                                const CUtensorMap& wgmap, const FinishParams& p, int num_sms, cudaStream_t s);
 
-// Box shapes of the tensor maps each kernel expects (elements, innermost first).
+// Tile sizes.
 constexpr int kProjTileJ = 128;     // pairs per projection tile
 constexpr int kContractBM = 128;    // output rows per contraction tile
 constexpr int kContractBN = 256;    // output columns per contraction tile
 constexpr int kContractBK = 64;     // k per pipeline stage
 constexpr int kFinishTileJ = 128;   // pairs per finish tile
+
+// Box shape (elements, innermost first) and element size of every tensor map. The host encodes the
+// maps from these and each kernel checks at compile time that a box fills exactly the shared-memory
+// slot it is copied into (a larger box would write past the slot).
+struct Box {
+  uint32_t d0, d1, d2, esz;
+  __host__ __device__ constexpr uint32_t bytes() const { return d0 * d1 * d2 * esz; }
+};
+constexpr Box kBoxProjZ{64, (uint32_t)kProjTileJ, 1, 2};              // z tile, one 64-channel half
+constexpr Box kBoxProjW{64, 128, 1, 2};                               // one K-half of a 128 x 128 weight
+constexpr Box kBoxProjOut{64, 1, (uint32_t)kC, 2};                    // a or b store: 64 pairs x 128 channels
+constexpr Box kBoxContractOutA{(uint32_t)kContractBK, (uint32_t)kContractBM, 1, 2};
+constexpr Box kBoxContractOutB{(uint32_t)kContractBK, (uint32_t)kContractBN, 1, 2};
+constexpr Box kBoxContractIn{64, (uint32_t)kContractBK, 1, 2};        // incoming: 64-wide slab of i or j
+constexpr Box kBoxContractX{32, 32, 1, 4};                            // x store sub-tile
+constexpr Box kBoxFinishX{(uint32_t)kFinishTileJ, 1, (uint32_t)kC, 4};
+constexpr Box kBoxFinishZ{64, (uint32_t)kFinishTileJ, 1, 2};
+constexpr Box kBoxFinishW{64, (uint32_t)kC, 1, 2};                    // W_o (fp16) and W_g (bf16) halves
 
 // ----------------------------------------------------------------- float32 CUDA-core path (any c <= 256)
 struct F32Weights {

@@ -101,7 +101,8 @@ def test_contract_bf16_matches_matmul(tm128, torch_cuda, direction, N):
     if N >= 129:
         blocks.append((3, N // 3, N - 3 - 5, N - N // 3 - 1))
     for (i0, j0, bi, bj) in blocks:
-        ldx = (bj + 3) // 4 * 4
+        granule = (bj + 3) // 4 * 4          # stores may fill the 16-byte granule holding column bj-1
+        ldx = granule + 8
         x = torch.full((128, bi, ldx), float("nan"), device="cuda")
         tm.tm_contract(mod.ctx, ad, bd, N, ld, direction, i0, j0, bi, bj, x, ldx)
         got = to_f64(x)[:, :, :bj]
@@ -109,7 +110,7 @@ def test_contract_bf16_matches_matmul(tm128, torch_cuda, direction, N):
         rms = np.sqrt(np.mean(exp * exp))
         err = np.max(np.abs(got - exp)) / rms
         assert err <= 2e-5, (direction, N, (i0, j0, bi, bj), err)
-        assert np.all(np.isnan(to_f64(x)[:, :, bj:])), "wrote outside the block"
+        assert np.all(np.isnan(to_f64(x)[:, :, granule:])), "wrote outside the block's row granules"
 
 
 # --------------------------------------------------------------------------- projection and finish alone

@@ -35,11 +35,33 @@ def contraction_boxes(N, i0, j0, bi, bj, incoming):
                         yield ("b", jb + 64 * h, 2)
 
 
+def contraction_store_boxes(N, i0, j0, bi, bj):
+    """TMA stores of x (float32) when the block origin is on the 8-element grid; else direct stores."""
+    if i0 % 8 or j0 % 8:
+        return
+    tiles_i = (bi + BM - 1) // BM
+    tiles_j = (bj + BN - 1) // BN
+    for ti in range(tiles_i):
+        for tj in range(tiles_j):
+            for q in range(4):
+                for ch in range(BN // 32):
+                    row0, col0 = ti * BM + 32 * q, tj * BN + 32 * ch
+                    if row0 < bi and col0 < bj:
+                        yield ("x-store", col0, 4, row0)
+
+
 def projection_boxes(N):
     for kc in (0, 1):
         yield ("z", kc * 64, 2)
     for kc in (0, 1):
         yield ("w", kc * 64, 2)
+    # stores of a / b: 64 pairs x 128 channels per box, two boxes per 128-pair tile
+    tiles_per_row = (N + PROJ_J - 1) // PROJ_J
+    for jt in range(tiles_per_row):
+        for g in (0, 1):
+            x = jt * PROJ_J + 64 * g
+            if x < N:
+                yield ("ab-store", x, 2)
 
 
 def finish_boxes(N, i0, j0, bi, bj):
@@ -72,6 +94,10 @@ def test_inner_coordinates_are_16_byte_aligned(N, B):
                 assert x >= 0 and (x * esz) % 16 == 0, (N, B, incoming, (i0, j0), name, x)
     for name, x, esz in projection_boxes(N):
         assert (x * esz) % 16 == 0
+    for (i0, j0, bi, bj) in list(schedule(N, B))[:2]:
+        for name, x, esz, y in contraction_store_boxes(N, i0, j0, bi, bj):
+            # a store box starts at a non-negative, 16-byte-aligned coordinate inside the block
+            assert x >= 0 and y >= 0 and (x * esz) % 16 == 0 and x < bj and y < bi
 
 
 def test_unaligned_block_origins_are_covered():
