@@ -429,7 +429,7 @@ tm_status check_common(tm_ctx* c, int N, tm_dtype dtype) {
 
 int choose_block(const tm_ctx* c, int N, const tm_options* opt, size_t ab_bytes) {
   if (opt && opt->block > 0) return std::min(opt->block, N);
-  const size_t full_x = (size_t)c->c_h * N * align_up(N, 4) * 4;
+  const size_t full_x = (size_t)c->c_h * N * align_up(N, 32) * 4;
   size_t budget = (size_t)32 << 30;
   const size_t lim = limit_of(c, opt);
   if (lim) budget = lim > ab_bytes ? std::min(budget, lim - ab_bytes) : 0;
@@ -437,7 +437,7 @@ int choose_block(const tm_ctx* c, int N, const tm_options* opt, size_t ab_bytes)
   int nb = (N + 2499) / 2500;
   for (;; ++nb) {
     const int B = (int)align_up((size_t)((N + nb - 1) / nb), 8);   // block origins on the 8-element grid
-    if ((size_t)c->c_h * B * align_up(B, 4) * 4 <= budget || B <= 256) return B;
+    if ((size_t)c->c_h * B * align_up(B, 32) * 4 <= budget || B <= 256) return B;
   }
 }
 
@@ -616,10 +616,12 @@ tm_status tm_forward_ex(tm_ctx* c, const void* z, const float* mask, int N, tm_d
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool inc = dir == TM_INCOMING;
 
-  const int ld = dtype == TM_BF16 ? (int)align_up(N, 8) : N;
+  // Rows of a, b and x start on 128-byte boundaries: a TMA box row then maps onto whole L2 lines
+  // (with N = 3605 and 16-byte-aligned rows every 128-byte row segment straddled two lines).
+  const int ld = dtype == TM_BF16 ? (int)align_up(N, 64) : N;
   const size_t ab_bytes = align_up((size_t)c->c_h * N * ld * esz, 256);
   const int B = choose_block(c, N, opt, 2 * ab_bytes);
-  const int ldx = (int)align_up(B, 4);
+  const int ldx = (int)align_up(B, 32);
   const size_t x_bytes = align_up((size_t)c->c_h * B * ldx * 4, 256);
   st = ensure_workspace(c, 2 * ab_bytes + x_bytes, s, opt);
   if (st != TM_OK) return st;
