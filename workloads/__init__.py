@@ -205,17 +205,21 @@ def sample_grid(N: int, n_rows: int = 64, n_cols: int = 64, seed: int = 2, edges
     rng = np.random.default_rng(np.random.SeedSequence([seed, 15485863]))
     rows = set(rng.integers(0, N, n_rows).tolist())
     cols = set(rng.integers(0, N, n_cols).tolist())
-    special = {0, N - 1}
-    for e in edges:
+    # the last entry of `edges` is the block edge: all its boundaries are kept
+    keep = {0, N - 1}
+    for k in range(edges[-1], N, edges[-1]):
+        keep.update((k - 1, k, k + 1))
+    special = set()
+    for e in edges[:-1]:
         for k in range(e, N, e):
             special.update((k - 1, k, k + 1))
-    special = {s for s in special if 0 <= s < N}
-    # keep the edge set bounded so the oracle stays cheap
-    special = sorted(special)
+    special = sorted(s for s in special - keep if 0 <= s < N)
+    # keep the tile-edge set bounded so the oracle stays cheap
     if len(special) > 48:
         pick = np.random.default_rng(np.random.SeedSequence([seed, 1299709])).choice(
             len(special), 48, replace=False)
-        special = [special[k] for k in sorted(pick)] + [0, N - 1]
-    rows.update(special)
-    cols.update(special)
+        special = [special[k] for k in sorted(pick)]
+    keep = {s for s in keep if 0 <= s < N}
+    rows.update(special, keep)
+    cols.update(special, keep)
     return np.array(sorted(rows), np.int64), np.array(sorted(cols), np.int64)
