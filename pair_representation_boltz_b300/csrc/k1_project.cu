@@ -25,19 +25,21 @@
 //   warp 1      TMEM (2 x 256 columns) and tcgen05.mma with the channels on
 //               the TMEM lanes: D_proj[c][p] = W'_proj z^T and D_gate[c][p] =
 //               W'_gate z^T (M = 128 channels, N = 128 pairs), hi + lo each.
-//   warps 2..9  epilogue, thread = channel: two warps per TMEM lane quadrant
+//   warps 2..5  LayerNorm statistics, thread = pair, from the z tile in fp32
+//               (packed fp32x2 arithmetic), one tile ahead of the epilogue:
+//               double-buffered in shared memory behind mbarriers, with the
+//               pair mask as one bit per pair (warp ballot).
+//   warps 6..13 epilogue, thread = channel: two warps per TMEM lane quadrant
 //               split the 128 pairs; per-channel folding constants live in
-//               registers, per-pair LayerNorm statistics (computed from the z
-//               tile by warps 2..5, one thread per pair) come from shared
-//               memory as one broadcast 16-byte load per pair; the element
-//               math is branch-free (mask as a multiply, two-MUFU sigmoid).
-//               Results go through shared memory: each group of four warps
-//               fills a 128-channel x 64-pair staging box (128-byte swizzle)
-//               that one thread writes out with a TMA store, so every channel
-//               row leaves as a 128-byte line. (Stores straight from the
-//               threads, one channel row per lane, scatter each warp
-//               instruction over 32 DRAM pages and ran 6x slower.) Two named
-//               barriers per tile fence the statistics and staging buffers.
+//               registers; two pairs at a time in fp32x2 arithmetic, the
+//               sigmoid as two MUFU operations, no branch. Results go through
+//               shared memory: each group of four warps fills a 128-channel x
+//               64-pair staging box (128-byte swizzle) that one thread writes
+//               out with a TMA store, so every channel row leaves as a
+//               128-byte line. (Stores straight from the threads, one channel
+//               row per lane, scatter each warp instruction over 32 DRAM pages
+//               and ran 6x slower.) Two group-local named barriers per tile
+//               fence the staging box.
 #include "tm_kernels.h"
 
 namespace tmk {
@@ -48,11 +50,11 @@ constexpr int STAGES = 2;
 constexpr int Z_BYTES = BM * kC * 2;           // 32 KB (two 16 KB K-chunks)
 constexpr int W_MAT = kC * kC * 2;             // one 128 x 128 bf16 matrix, two K-chunks: 32 KB
 constexpr int W_BYTES = 4 * W_MAT;             // proj hi, proj lo, gate hi, gate lo
-constexpr int EPI_WARPS = 8;
-constexpr int THREADS = 64 + 32 * EPI_WARPS;   // TMA warp, MMA warp, epilogue warps
-constexpr int OUT_BYTES = 2 * (int)kBoxProjOut.bytes();  // two staging boxes: pairs 0-63 and 64-127
-constexpr int STAT_BYTES = BM * 16;            // one float4 per pair: rstd, -rstd*mu, mask, 0
-constexpr int SMEM_BYTES = STAGES * Z_BYTES + W_BYTES + OUT_BYTES + STAT_BYTES + 128;
+constexpr int STAT_WARPS = 4, EPI_WARPS = 8;
+constexpr int THREADS = 64 + 32 * (STAT_WARPS + EPI_WARPS);   // TMA, MMA, statistics, epilogue warps
+constexpr int OUT_BYTES = 2 * (int)kBoxProjOut.bytes();        // two staging boxes: pairs 0-63 and 64-127
+constexpr int STAT_BUF = (BM / 2) * 16 + 16;   // float4 {rstd_2k, rstd_2k+1, nmu_2k, nmu_2k+1} + 4 mask words
+constexpr int SMEM_BYTES = STAGES * Z_BYTES + W_BYTES + OUT_BYTES + 2 * STAT_BUF + 256;
 constexpr int TMEM_COLS = 512;
 
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -68,12 +70,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* zs = smem;
   uint8_t* ws = smem + STAGES * Z_BYTES;                  // [proj hi, proj lo, gate hi, gate lo]
   uint8_t* ostg = ws + W_BYTES;                           // [2 boxes][128 channels][128 B], swizzled
-  float4* stats = reinterpret_cast<float4*>(ostg + OUT_BYTES); // [128]: rstd, -rstd*mu, pair mask, 0
-  uint64_t* zfull = reinterpret_cast<uint64_t*>(stats + BM);
+  uint8_t* sbase = ostg + OUT_BYTES;                      // [2][STAT_BUF]
+  uint64_t* zfull = reinterpret_cast<uint64_t*>(sbase + 2 * STAT_BUF);
   uint64_t* zempty = zfull + STAGES;
   uint64_t* tfull = zempty + STAGES;
   uint64_t* tempty = tfull + 2;
-  uint64_t* wfull = tempty + 2;
+  uint64_t* sfull = tempty + 2;
+  uint64_t* sempty = sfull + 2;
+  uint64_t* wfull = sempty + 2;
   uint64_t* fin = wfull + 1;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(fin + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
@@ -88,11 +92,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (*abort_flag) raise_status(p.w, ST_TIMEOUT, 90);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&zfull[s], 1);
-      mbar_init(&zempty[s], 1 + 4);  // MMA commit + the 4 statistics warps
+      mbar_init(&zempty[s], 1 + STAT_WARPS);  // MMA commit + the statistics warps
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], EPI_WARPS);
+      mbar_init(&sfull[b], STAT_WARPS);
+      mbar_init(&sempty[b], EPI_WARPS);
     }
     mbar_init(wfull, 1);
     mbar_init(fin, 1);
@@ -109,6 +115,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (!*abort_flag) {
     if (warp == 0) {
+      // ------------------------------------------------------------ TMA producer
       if (lane == 0) {
         tma_prefetch_desc(&zmap);
         tma_prefetch_desc(&wmap);
@@ -136,6 +143,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
     } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer
       if (lane == 0) {
         constexpr uint32_t idesc = make_idesc(kC, BM, FMT_BF16, false, false);
         int s = 0;
@@ -175,126 +183,154 @@ __global__ void __launch_bounds__(THREADS, 1)
         mma_commit(fin);
         wait_bounded(fin, 0, p.w, abort_flag, 15);
       }
-    } else {
-      // ------------------------------------------------------------ epilogue, thread = channel
-      const int ew = warp - 2;                 // 0..7
-      const int q = warp & 3;                  // TMEM lane quadrant: channels 32q .. 32q+31
-      const int c = q * 32 + lane;
-      const int grp = ew >> 2;                 // staging box: pairs 64*grp .. 64*grp + 63
-      const int pbase = grp * 64;              // this warp's 64 pair columns
-      const bool issuer = (ew & 3) == 0 && lane == 0;   // one thread per box issues its TMA store
-      const CUtensorMap* omap = half ? &bmap : &amap;
-      uint8_t* const box = ostg + grp * (int)kBoxProjOut.bytes();
-      const bool stat_warp = ew < 4;           // warps 2..5 also compute the per-pair statistics
-      const float* cst = p.consts + half * 512;
-      const float rs_p = cst[c], rs_g = cst[kC + c], b_p = cst[256 + c], b_g = cst[256 + kC + c];
-      if (issuer) tma_prefetch_desc(omap);
+    } else if (warp < 2 + STAT_WARPS) {
+      // ------------------------------------------------------------ statistics, thread = pair
+      const int sw = warp - 2;
+      const int t = sw * 32 + lane;
       int s = 0;
       uint32_t ph = 0;
       int local = 0;
       for (long long u = cta; u < p.total_tiles; u += nctas, ++local) {
         const int i = (int)(u / p.tiles_per_row);
         const int jt = (int)(u - (long long)i * p.tiles_per_row);
-        bool ok = true;
-        if (stat_warp) ok = warp_wait_bounded(&zfull[s], ph, p.w, abort_flag, 16);
-        if (stat_warp && ok) {
-          // LayerNorm statistics of pair t = ew*32 + lane over its 128 channels (fp32, two passes)
-          const int t = ew * 32 + lane;
-          const uint8_t* zt = zs + s * Z_BYTES;
-          uint4 raw[16];
+        const int sb = local & 1;
+        const uint32_t sph = (uint32_t)(local >> 1) & 1u;
+        if (!warp_wait_bounded(&zfull[s], ph, p.w, abort_flag, 16)) break;
+        const uint8_t* zt = zs + s * Z_BYTES;
+        // mean and biased variance over the 128 channels: two passes over the z row in shared memory
+        // (re-read rather than held in registers), fp32x2 arithmetic
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll 4
+        for (int k = 0; k < 16; ++k) {
+          const uint4 w4 = *reinterpret_cast<const uint4*>(zt + (k >> 3) * (Z_BYTES / 2) + sw128_offset(t, k & 7));
+          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w4);
 #pragma unroll
-          for (int kc = 0; kc < 2; ++kc)
-#pragma unroll
-            for (int uu = 0; uu < 8; ++uu)
-              raw[kc * 8 + uu] = *reinterpret_cast<const uint4*>(zt + kc * (Z_BYTES / 2) + sw128_offset(t, uu));
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&zempty[s]);
-          float sum = 0.f;
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[k]);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 f = __bfloat1622float2(h[e]);
-              sum += f.x + f.y;
-            }
-          }
-          const float mu = sum * (1.0f / kC);
-          float ss = 0.f;
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[k]);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 f = __bfloat1622float2(h[e]);
-              ss += (f.x - mu) * (f.x - mu) + (f.y - mu) * (f.y - mu);
-            }
-          }
-          const float rstd = rsqrtf(ss * (1.0f / kC) + 1e-5f);
-          const int j = jt * BM + t;
-          float m = 0.f;
-          if (j < p.N) m = p.mask ? p.mask[i] * p.mask[j] : 1.0f;
-          stats[t] = make_float4(rstd, -rstd * mu, m, 0.f);
+          for (int e = 0; e < 4; ++e) acc[e] = __fadd2_rn(acc[e], __bfloat1622float2(h[e]));
         }
+        const float2 a01 = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+        const float mu = (a01.x + a01.y) * (1.0f / kC);
+        const float2 mu2 = make_float2(-mu, -mu);
+        float2 sq[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll 4
+        for (int k = 0; k < 16; ++k) {
+          const uint4 w4 = *reinterpret_cast<const uint4*>(zt + (k >> 3) * (Z_BYTES / 2) + sw128_offset(t, k & 7));
+          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w4);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 d = __fadd2_rn(__bfloat1622float2(h[e]), mu2);
+            sq[e] = __ffma2_rn(d, d, sq[e]);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&zempty[s]);     // this warp has finished reading the z tile
         if (++s == STAGES) {
           s = 0;
           ph ^= 1u;
         }
-        // the previous tile's stores have finished reading the staging boxes
-        if (issuer) bulk_wait_read<0>();
-        // barrier 1: the tile's statistics are complete and the staging boxes are free. Every warp stops
-        // here together once any wait of the CTA has given up (a warp that left alone would strand the
-        // others at the barrier).
-        if (named_bar_or(1, 32 * EPI_WARPS, !ok || *abort_flag != 0)) break;
-
+        const float2 s01 = __fadd2_rn(__fadd2_rn(sq[0], sq[1]), __fadd2_rn(sq[2], sq[3]));
+        const float rstd = rsqrtf((s01.x + s01.y) * (1.0f / kC) + 1e-5f);
+        const int j = jt * BM + t;
+        float m = 0.f;
+        if (j < p.N) m = p.mask ? p.mask[i] * p.mask[j] : 1.0f;
+        const unsigned bits = __ballot_sync(0xffffffffu, m != 0.f);
+        // the epilogue of two tiles ago has let go of this buffer
+        if (!warp_wait_bounded(&sempty[sb], sph ^ 1u, p.w, abort_flag, 18)) break;
+        float* st = reinterpret_cast<float*>(sbase + sb * STAT_BUF);
+        st[(t >> 1) * 4 + (t & 1)] = rstd;
+        st[(t >> 1) * 4 + 2 + (t & 1)] = -rstd * mu;
+        if (lane == 0) reinterpret_cast<uint32_t*>(sbase + sb * STAT_BUF + (BM / 2) * 16)[sw] = bits;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sfull[sb]);
+      }
+    } else {
+      // ------------------------------------------------------------ epilogue, thread = channel
+      const int ew = warp - 2 - STAT_WARPS;    // 0..7
+      const int q = warp & 3;                  // TMEM lane quadrant: channels 32q .. 32q+31
+      const int c = q * 32 + lane;
+      const int grp = ew >> 2;                 // staging box: pairs 64*grp .. 64*grp + 63
+      const int pbase = grp * 64;
+      const bool issuer = (ew & 3) == 0 && lane == 0;   // one thread per box issues its TMA store
+      const CUtensorMap* omap = half ? &bmap : &amap;
+      uint8_t* const box = ostg + grp * (int)kBoxProjOut.bytes();
+      const float* cst = p.consts + half * 512;
+      const float2 rsp = make_float2(cst[c], cst[c]), rsg = make_float2(cst[kC + c], cst[kC + c]);
+      const float2 bp = make_float2(cst[256 + c], cst[256 + c]), bg = make_float2(cst[256 + kC + c], cst[256 + kC + c]);
+      const float2 nlog2e = make_float2(-1.4426950408889634f, -1.4426950408889634f);
+      const float2 one2 = make_float2(1.f, 1.f);
+      if (issuer) tma_prefetch_desc(omap);
+      int local = 0;
+      for (long long u = cta; u < p.total_tiles; u += nctas, ++local) {
+        const int i = (int)(u / p.tiles_per_row);
+        const int jt = (int)(u - (long long)i * p.tiles_per_row);
         const int buf = local & 1;
         const uint32_t use = (uint32_t)(local >> 1);
-        ok = warp_wait_bounded(&tfull[buf], use & 1u, p.w, abort_flag, 17);
+        const int sb = local & 1;
+        const uint32_t sph = (uint32_t)(local >> 1) & 1u;
+        // the previous tile's store has finished reading this group's staging box
+        if (issuer) bulk_wait_read<0>();
+        // barrier A (group): the box is free. Every warp of the group stops together once any wait of
+        // the CTA has given up (a warp that left alone would strand the others at the barrier).
+        if (named_bar_or(1 + grp, 128, *abort_flag != 0)) break;
+        bool ok = warp_wait_bounded(&sfull[sb], sph, p.w, abort_flag, 19) &&
+                  warp_wait_bounded(&tfull[buf], use & 1u, p.w, abort_flag, 17);
         if (ok) {
           tc_fence_after();
+          const float4* st = reinterpret_cast<const float4*>(sbase + sb * STAT_BUF);
+          const uint32_t* mw = reinterpret_cast<const uint32_t*>(sbase + sb * STAT_BUF + (BM / 2) * 16);
 #pragma unroll 1
-          for (int cc = 0; cc < 2; ++cc) {
-            const int p0 = pbase + cc * 32;       // first pair column of this chunk
-            uint32_t pr[32], gt[32];
+          for (int cc = 0; cc < 4; ++cc) {
+            const int p0 = pbase + cc * 16;       // first pair column of this 16-pair chunk
+            uint32_t pr[16], gt[16];
             const uint32_t ta = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * 2 * BM + p0);
-            tmem_ld32(ta, pr);
-            tmem_ld32(ta + BM, gt);
+            tmem_ld16(ta, pr);
+            tmem_ld16(ta + BM, gt);
+            const uint32_t mword = mw[p0 >> 5] >> (p0 & 31);
             tmem_ld_wait();
-            uint32_t packed[16];
+            uint32_t packed[8];
 #pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              const float4 s0 = stats[p0 + e];
-              const float4 s1 = stats[p0 + e + 1];
-              const float pre0 = fmaf(s0.x, __uint_as_float(pr[e]), fmaf(s0.y, rs_p, b_p));
-              const float pre1 = fmaf(s1.x, __uint_as_float(pr[e + 1]), fmaf(s1.y, rs_p, b_p));
-              const float g0 = fmaf(s0.x, __uint_as_float(gt[e]), fmaf(s0.y, rs_g, b_g));
-              const float g1 = fmaf(s1.x, __uint_as_float(gt[e + 1]), fmaf(s1.y, rs_g, b_g));
-              packed[e >> 1] = pack_bf16x2(sigmoid_mufu(g0) * pre0 * s0.z, sigmoid_mufu(g1) * pre1 * s1.z);
+            for (int e = 0; e < 16; e += 2) {
+              const float4 sv = st[(p0 + e) >> 1];          // rstd and -rstd*mu of pairs p0+e, p0+e+1
+              const float2 r = make_float2(sv.x, sv.y), n = make_float2(sv.z, sv.w);
+              const float2 pre = __ffma2_rn(r, make_float2(__uint_as_float(pr[e]), __uint_as_float(pr[e + 1])),
+                                            __ffma2_rn(n, rsp, bp));
+              const float2 gpre = __ffma2_rn(r, make_float2(__uint_as_float(gt[e]), __uint_as_float(gt[e + 1])),
+                                             __ffma2_rn(n, rsg, bg));
+              const float2 ga = __fmul2_rn(gpre, nlog2e);
+              float e0, e1, r0, r1;
+              asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(ga.x));
+              asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(ga.y));
+              const float2 den = __fadd2_rn(make_float2(e0, e1), one2);
+              asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r0) : "f"(den.x));
+              asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r1) : "f"(den.y));
+              const float2 v = __fmul2_rn(make_float2(r0, r1), pre);
+              packed[e >> 1] = pack_bf16x2(((mword >> e) & 1u) ? v.x : 0.f, ((mword >> (e + 1)) & 1u) ? v.y : 0.f);
             }
-            // 64 bytes of this channel's row of the staging box: 16-byte units 4cc .. 4cc+3
+            // 32 bytes of this channel's row of the staging box: 16-byte units 2cc, 2cc+1
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              *reinterpret_cast<uint4*>(box + sw128_offset(c, cc * 4 + k)) =
+            for (int k = 0; k < 2; ++k)
+              *reinterpret_cast<uint4*>(box + sw128_offset(c, cc * 2 + k)) =
                   make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
           }
           fence_proxy_async_smem();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&tempty[buf]);
+          if (lane == 0) {
+            mbar_arrive(&tempty[buf]);
+            mbar_arrive(&sempty[sb]);
+          }
         }
-        // barrier 2: the staging boxes are complete, and every warp is done with this tile's statistics
-        // before they are overwritten
-        if (named_bar_or(2, 32 * EPI_WARPS, !ok || *abort_flag != 0)) break;
+        // barrier B (group): the staging box is complete
+        if (named_bar_or(3 + grp, 128, !ok || *abort_flag != 0)) break;
         // pairs past N are clipped by TMA (whole 16-byte granules, inside the row padding of ld)
         if (issuer && jt * BM + pbase < p.N) {
           tma_store_3d(omap, box, jt * BM + pbase, i, 0);
           bulk_commit();
         }
       }
+      if (issuer) bulk_wait_all();   // stores out before the CTA's shared memory goes away
     }
   }
 
-  if (warp >= 2 && lane == 0 && ((warp - 2) & 3) == 0) bulk_wait_all();   // stores out before exit
   __syncthreads();
   if (*abort_flag) {
     const uint64_t t0 = gtimer();
