@@ -68,6 +68,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete sleeps (is
+// woken when the phase completes, or after at most `ns` nanoseconds) instead of
+// spinning and taking issue slots from the warps that do the work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase of `bar` with the given parity to complete. Gives up
 // after w.limit_ns (or when another role of the CTA has given up, *abort != 0),
 // records the failure in the status word and returns false.
@@ -76,15 +91,13 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, con
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = gtimer();
 #pragma unroll 1
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0u) {
-      if (*abort) return false;
-      if (gtimer() - t0 > w.limit_ns) {
-        raise_status(w, ST_TIMEOUT, site);
-        *abort = 1;
-        return false;
-      }
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;   // sleeps up to 0.1 ms per try
+    if (*abort) return false;
+    if (gtimer() - t0 > w.limit_ns) {
+      raise_status(w, ST_TIMEOUT, site);
+      *abort = 1;
+      return false;
     }
   }
 }
