@@ -287,9 +287,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint32_t mword = mw[p0 >> 5] >> (p0 & 31);
             tmem_ld_wait();
             uint32_t packed[8];
-#pragma unroll
-            for (int e = 0; e < 16; e += 2) {
-              const float4 sv = st[(p0 + e) >> 1];          // rstd and -rstd*mu of pairs p0+e, p0+e+1
+            // a, b of pairs p0+e and p0+e+1 for this channel (fp32x2: folded LayerNorm, gate, product)
+            auto pair_values = [&](int e) -> float2 {
+              const float4 sv = st[(p0 + e) >> 1];          // rstd and -rstd*mu of the two pairs
               const float2 r = make_float2(sv.x, sv.y), n = make_float2(sv.z, sv.w);
               const float2 pre = __ffma2_rn(r, make_float2(__uint_as_float(pr[e]), __uint_as_float(pr[e + 1])),
                                             __ffma2_rn(n, rsp, bp));
@@ -302,8 +302,21 @@ __global__ void __launch_bounds__(THREADS, 1)
               const float2 den = __fadd2_rn(make_float2(e0, e1), one2);
               asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r0) : "f"(den.x));
               asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r1) : "f"(den.y));
-              const float2 v = __fmul2_rn(make_float2(r0, r1), pre);
-              packed[e >> 1] = pack_bf16x2(((mword >> e) & 1u) ? v.x : 0.f, ((mword >> (e + 1)) & 1u) ? v.y : 0.f);
+              return __fmul2_rn(make_float2(r0, r1), pre);
+            };
+            if ((mword & 0xFFFFu) == 0xFFFFu) {
+              // all 16 pairs unmasked and inside the grid (warp-uniform): no per-element mask
+#pragma unroll
+              for (int e = 0; e < 16; e += 2) {
+                const float2 v = pair_values(e);
+                packed[e >> 1] = pack_bf16x2(v.x, v.y);
+              }
+            } else {
+#pragma unroll
+              for (int e = 0; e < 16; e += 2) {
+                const float2 v = pair_values(e);
+                packed[e >> 1] = pack_bf16x2(((mword >> e) & 1u) ? v.x : 0.f, ((mword >> (e + 1)) & 1u) ? v.y : 0.f);
+              }
             }
             // 32 bytes of this channel's row of the staging box: 16-byte units 2cc, 2cc+1
 #pragma unroll

@@ -11,15 +11,19 @@
 // Per tile of 128 pairs (one row i, 128 consecutive j of the block):
 //   warp 0      TMA: x tile [128 c][128 j] fp32 (64 KB), z tile (two 64-channel
 //               boxes, 128-byte swizzle); W_o (fp16) and W_g (bf16 hi + lo) once.
-//   warps 2..5  thread = pair. LayerNorm of x over its 128 channels in fp32,
-//               written back as fp16 rows of a K-major operand; LayerNorm
-//               statistics of z. Then, one tile later, the epilogue of the
-//               previous tile from TMEM: gate, product, 16-byte stores of out.
+//   warps 2..5  LayerNorm, thread = pair: three fp32x2 passes over its x column
+//               in shared memory (mean, variance, normalise) write the fp16 rows
+//               of a K-major operand; two passes over its z row give z's
+//               statistics, handed to the epilogue through a double-buffered
+//               shared array behind mbarriers.
 //   warp 1      tcgen05.mma: D[p][0..128) = xh x W_o'^T (kind::f16, fp16),
 //               D[p][128..256) = z x W_g'^T (bf16, hi and lo), two TMEM buffers.
+//   warps 6..13 epilogue, thread = pair: two warps per TMEM lane quadrant split
+//               the 128 output channels; gate, product and 16-byte stores of out.
 // LayerNorm_out's gamma is folded into W_o' = W_o diag(gamma_out) (scaled by a
 // power of two to use fp16's range) and beta into a bias; LayerNorm_in of the
 // gate is folded as in the projection: W_g zh = rstd (W_g' z - mu rowsum) + bias.
+// The per-channel constants travel in the kernel's parameter block.
 #include "tm_kernels.h"
 
 namespace tmk {
@@ -31,8 +35,10 @@ constexpr int XH_BYTES = BM * kC * 2;        // 32 KB fp16, two K-chunks
 constexpr int Z_BYTES = BM * kC * 2;         // 32 KB bf16, two K-chunks
 constexpr int WO_BYTES = kC * kC * 2;        // 32 KB fp16
 constexpr int WG_BYTES = 2 * kC * kC * 2;    // 64 KB bf16 hi + lo
-constexpr int THREADS = 192;
-constexpr int SMEM_BYTES = X_BYTES + XH_BYTES + Z_BYTES + WO_BYTES + WG_BYTES + 3 * kC * 4 + 256;
+constexpr int LN_WARPS = 4, EPI_WARPS = 8;
+constexpr int THREADS = 64 + 32 * (LN_WARPS + EPI_WARPS);
+constexpr int ZST_BYTES = 2 * BM * 8;        // two buffers of float2 (rstd, -rstd*mu) per pair
+constexpr int SMEM_BYTES = X_BYTES + XH_BYTES + Z_BYTES + WO_BYTES + WG_BYTES + ZST_BYTES + 256;
 constexpr int TMEM_COLS = 512;
 
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -40,18 +46,65 @@ static_assert(kBoxFinishX.bytes() == X_BYTES, "x tile = one box");
 static_assert(2 * kBoxFinishZ.bytes() == Z_BYTES, "z tile = two boxes");
 static_assert(2 * kBoxFinishW.bytes() == WO_BYTES && 4 * kBoxFinishW.bytes() == WG_BYTES, "weight boxes");
 
+__device__ __forceinline__ float2 bf2f(uint32_t v) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
+}
+
+// Epilogue of one tile for one thread: pair row of the TMEM accumulator at `tmem_row`, output
+// channels [64*H, 64*H + 64). H is a template parameter so the constant-bank offsets are immediates.
+template <int H>
+__device__ __forceinline__ void finish_pair(const FinishParams& p, uint32_t tmem_row, int buf, float2 zst,
+                                            __nv_bfloat16* dst, bool valid) {
+  const float2 inv = make_float2(p.inv_scale_o, p.inv_scale_o);
+  const float2 r2 = make_float2(zst.x, zst.x), n2 = make_float2(zst.y, zst.y);
+  const float2 nlog2e = make_float2(-1.4426950408889634f, -1.4426950408889634f);
+  const float2 one2 = make_float2(1.f, 1.f);
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    const int o0 = 64 * H + cc * 16;
+    uint32_t yv[16], gv[16];
+    tmem_ld16(tmem_row + (uint32_t)(buf * 2 * kC + o0), yv);
+    tmem_ld16(tmem_row + (uint32_t)(buf * 2 * kC + kC + o0), gv);
+    tmem_ld_wait();
+    uint32_t packed[8];
+#pragma unroll
+    for (int e = 0; e < 16; e += 2) {
+      const int o = o0 + e;
+      const float2 y = __ffma2_rn(make_float2(__uint_as_float(yv[e]), __uint_as_float(yv[e + 1])), inv,
+                                  make_float2(p.cst[2 * kC + o], p.cst[2 * kC + o + 1]));
+      const float2 g = __ffma2_rn(r2, make_float2(__uint_as_float(gv[e]), __uint_as_float(gv[e + 1])),
+                                  __ffma2_rn(n2, make_float2(p.cst[o], p.cst[o + 1]),
+                                             make_float2(p.cst[kC + o], p.cst[kC + o + 1])));
+      const float2 ga = __fmul2_rn(g, nlog2e);
+      float e0, e1, s0, s1;
+      asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(ga.x));
+      asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(ga.y));
+      const float2 den = __fadd2_rn(make_float2(e0, e1), one2);
+      asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(s0) : "f"(den.x));
+      asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(s1) : "f"(den.y));
+      const float2 v = __fmul2_rn(make_float2(s0, s1), y);
+      packed[e >> 1] = pack_bf16x2(v.x, v.y);
+    }
+    if (valid) {
+      uint4* d4 = reinterpret_cast<uint4*>(dst + o0);
+      d4[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+      d4[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    }
+  }
+}
+
 __global__ void __launch_bounds__(THREADS, 1)
     k3_finish(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap zmap,
               const __grid_constant__ CUtensorMap womap, const __grid_constant__ CUtensorMap wgmap,
-              const FinishParams p) {
+              const __grid_constant__ FinishParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* zs = smem;                        // 1024-aligned swizzled tiles first
   uint8_t* xh = zs + Z_BYTES;
   uint8_t* wo = xh + XH_BYTES;
   uint8_t* wg = wo + WO_BYTES;               // hi chunks then lo chunks
   float* xs = reinterpret_cast<float*>(wg + WG_BYTES);
-  float* cst = xs + kC * BM;                 // rowsum_g[128], bias_g[128], bias_o[128]
-  uint64_t* xfull = reinterpret_cast<uint64_t*>(cst + 3 * kC);
+  float2* zst = reinterpret_cast<float2*>(xs + kC * BM);   // [2][128]: rstd_z, -rstd_z * mu_z
+  uint64_t* xfull = reinterpret_cast<uint64_t*>(zst + 2 * BM);
   uint64_t* xempty = xfull + 1;
   uint64_t* zfull = xempty + 1;
   uint64_t* zempty = zfull + 1;
@@ -59,7 +112,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* hempty = hfull + 1;
   uint64_t* tfull = hempty + 1;
   uint64_t* tempty = tfull + 2;
-  uint64_t* wfull = tempty + 2;
+  uint64_t* sfull = tempty + 2;
+  uint64_t* sempty = sfull + 2;
+  uint64_t* wfull = sempty + 2;
   uint64_t* fin = wfull + 1;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(fin + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
@@ -69,21 +124,21 @@ __global__ void __launch_bounds__(THREADS, 1)
     *abort_flag = (smem_u32(smem) & 1023u) ? 1 : 0;
     if (*abort_flag) raise_status(p.w, ST_TIMEOUT, 90);
     mbar_init(xfull, 1);
-    mbar_init(xempty, 4);
+    mbar_init(xempty, LN_WARPS);
     mbar_init(zfull, 1);
     mbar_init(zempty, 1);
-    mbar_init(hfull, 4);
+    mbar_init(hfull, LN_WARPS);
     mbar_init(hempty, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 4);
+      mbar_init(&tempty[b], EPI_WARPS);
+      mbar_init(&sfull[b], LN_WARPS);
+      mbar_init(&sempty[b], EPI_WARPS);
     }
     mbar_init(wfull, 1);
     mbar_init(fin, 1);
     fence_mbar_init();
   }
-  if (threadIdx.x >= 64)
-    for (int t = threadIdx.x - 64; t < 3 * kC; t += THREADS - 64) cst[t] = p.consts[t];
   if (warp == 1) {
     tmem_alloc(tslot, TMEM_COLS);
     tmem_relinquish();
@@ -95,6 +150,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (!*abort_flag) {
     if (warp == 0) {
+      // ------------------------------------------------------------ TMA producer
       if (lane == 0) {
         tma_prefetch_desc(&xmap);
         tma_prefetch_desc(&zmap);
@@ -118,6 +174,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
     } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer
       if (lane == 0) {
         constexpr uint32_t id_y = make_idesc(BM, kC, FMT_F16, false, false);
         constexpr uint32_t id_g = make_idesc(BM, kC, FMT_BF16, false, false);
@@ -154,146 +211,125 @@ __global__ void __launch_bounds__(THREADS, 1)
         mma_commit(fin);
         wait_bounded(fin, 0, p.w, abort_flag, 37);
       }
-    } else {
-      // ------------------------------------------------------------ LayerNorm + epilogue, thread = pair
-      const int q = warp & 3;
-      const int r = q * 32 + lane;
+    } else if (warp < 2 + LN_WARPS) {
+      // ------------------------------------------------------------ LayerNorm, thread = pair
+      const int r = (warp - 2) * 32 + lane;
       uint32_t ph = 0;
       int local = 0;
-      // state of the previous tile, whose epilogue runs after this tile's LayerNorm
-      float pmu = 0.f, prs = 0.f;
-      int pi = -1, pj = 0;
-      bool pvalid = false;
-      bool ok = true;
-      for (long long t = blockIdx.x;; t += gridDim.x, ++local) {
-        const bool have = t < p.total_tiles;
-        float zmu = 0.f, zrs = 0.f;
-        int ci = 0, cj = 0;
-        bool cvalid = false;
-        if (have) {
-          const int il = (int)(t / p.tiles_j);
-          const int jt = (int)(t - (long long)il * p.tiles_j);
-          ci = p.i0 + il;
-          cj = p.j0 + jt * BM + r;
-          cvalid = (jt * BM + r) < p.bj;
-          // statistics of z_ij
-          if (!warp_wait_bounded(zfull, ph, p.w, abort_flag, 38)) {
-            ok = false;
-            break;
-          }
-          {
-            float v[kC];
-#pragma unroll
-            for (int kc = 0; kc < 2; ++kc)
-#pragma unroll
-              for (int uu = 0; uu < 8; ++uu) {
-                const uint4 w4 = *reinterpret_cast<const uint4*>(zs + kc * (Z_BYTES / 2) + sw128_offset(r, uu));
-                const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w4);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const float2 f = __bfloat1622float2(h[e]);
-                  v[kc * 64 + uu * 8 + 2 * e] = f.x;
-                  v[kc * 64 + uu * 8 + 2 * e + 1] = f.y;
-                }
-              }
-            float s0 = 0.f;
-#pragma unroll
-            for (int c = 0; c < kC; ++c) s0 += v[c];
-            zmu = s0 * (1.0f / kC);
-            float s1 = 0.f;
-#pragma unroll
-            for (int c = 0; c < kC; ++c) s1 += (v[c] - zmu) * (v[c] - zmu);
-            zrs = rsqrtf(s1 * (1.0f / kC) + 1e-5f);
-          }
-          // LayerNorm of x_ij over channels -> fp16 operand row
-          if (!warp_wait_bounded(xfull, ph, p.w, abort_flag, 39)) {
-            ok = false;
-            break;
-          }
-          float v[kC];
-#pragma unroll
-          for (int c = 0; c < kC; ++c) v[c] = xs[c * BM + r];
-          __syncwarp();
-          if (lane == 0) mbar_arrive(xempty);
-          float s0 = 0.f;
-#pragma unroll
-          for (int c = 0; c < kC; ++c) s0 += v[c];
-          const float xmu = s0 * (1.0f / kC);
-          float s1 = 0.f;
-#pragma unroll
-          for (int c = 0; c < kC; ++c) s1 += (v[c] - xmu) * (v[c] - xmu);
-          const float xrs = rsqrtf(s1 * (1.0f / kC) + 1e-5f);
-          if (!warp_wait_bounded(hempty, ph ^ 1u, p.w, abort_flag, 40)) {
-            ok = false;
-            break;
-          }
-#pragma unroll
-          for (int kc = 0; kc < 2; ++kc)
-#pragma unroll
-            for (int uu = 0; uu < 8; ++uu) {
-              const int c = kc * 64 + uu * 8;
-              uint4 w4;
-              w4.x = pack_f16x2((v[c + 0] - xmu) * xrs, (v[c + 1] - xmu) * xrs);
-              w4.y = pack_f16x2((v[c + 2] - xmu) * xrs, (v[c + 3] - xmu) * xrs);
-              w4.z = pack_f16x2((v[c + 4] - xmu) * xrs, (v[c + 5] - xmu) * xrs);
-              w4.w = pack_f16x2((v[c + 6] - xmu) * xrs, (v[c + 7] - xmu) * xrs);
-              *reinterpret_cast<uint4*>(xh + kc * (XH_BYTES / 2) + sw128_offset(r, uu)) = w4;
-            }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(hfull);
-          ph ^= 1u;
+      for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++local) {
+        const int sb = local & 1;
+        const uint32_t sph = (uint32_t)(local >> 1) & 1u;
+        // statistics of z_ij over its 128 channels (two passes over the smem row, fp32x2)
+        if (!warp_wait_bounded(zfull, ph, p.w, abort_flag, 38)) break;
+        float2 a0 = make_float2(0.f, 0.f), a1 = a0;
+#pragma unroll 4
+        for (int k = 0; k < 16; ++k) {
+          const uint4 w4 = *reinterpret_cast<const uint4*>(zs + (k >> 3) * (Z_BYTES / 2) + sw128_offset(r, k & 7));
+          a0 = __fadd2_rn(a0, __fadd2_rn(bf2f(w4.x), bf2f(w4.y)));
+          a1 = __fadd2_rn(a1, __fadd2_rn(bf2f(w4.z), bf2f(w4.w)));
         }
-        // epilogue of the previous tile
-        if (local > 0) {
-          const int pl = local - 1;
-          const int buf = pl & 1;
-          const uint32_t use = (uint32_t)(pl >> 1);
-          if (!warp_wait_bounded(&tfull[buf], use & 1u, p.w, abort_flag, 41)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          __nv_bfloat16* dst = p.out + ((size_t)pi * p.N + pj) * kC;
-#pragma unroll 1
-          for (int cc = 0; cc < 4; ++cc) {
-            uint32_t yv[32], gv[32];
-            const uint32_t ta = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * 2 * kC + cc * 32);
-            tmem_ld32(ta, yv);
-            tmem_ld32(ta + kC, gv);
-            tmem_ld_wait();
-            if (pvalid) {
-              uint32_t packed[16];
-#pragma unroll
-              for (int e = 0; e < 32; e += 2) {
-                float o2[2];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                  const int o = cc * 32 + e + h;
-                  const float y = __uint_as_float(yv[e + h]) * p.inv_scale_o + cst[2 * kC + o];
-                  const float g = prs * (__uint_as_float(gv[e + h]) - pmu * cst[o]) + cst[kC + o];
-                  o2[h] = sigmoidf_fast(g) * y;
-                }
-                packed[e / 2] = pack_bf16x2(o2[0], o2[1]);
-              }
-              uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
-#pragma unroll
-              for (int k = 0; k < 4; ++k)
-                d4[k] = make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
-            }
-          }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&tempty[buf]);
+        const float2 as = __fadd2_rn(a0, a1);
+        const float zmu = (as.x + as.y) * (1.0f / kC);
+        const float2 nz = make_float2(-zmu, -zmu);
+        float2 q0 = make_float2(0.f, 0.f), q1 = q0;
+#pragma unroll 4
+        for (int k = 0; k < 16; ++k) {
+          const uint4 w4 = *reinterpret_cast<const uint4*>(zs + (k >> 3) * (Z_BYTES / 2) + sw128_offset(r, k & 7));
+          float2 d;
+          d = __fadd2_rn(bf2f(w4.x), nz);
+          q0 = __ffma2_rn(d, d, q0);
+          d = __fadd2_rn(bf2f(w4.y), nz);
+          q1 = __ffma2_rn(d, d, q1);
+          d = __fadd2_rn(bf2f(w4.z), nz);
+          q0 = __ffma2_rn(d, d, q0);
+          d = __fadd2_rn(bf2f(w4.w), nz);
+          q1 = __ffma2_rn(d, d, q1);
         }
-        if (!have) break;
-        pmu = zmu;
-        prs = zrs;
-        pi = ci;
-        pj = cj;
-        pvalid = cvalid;
+        const float2 qs = __fadd2_rn(q0, q1);
+        const float zrs = rsqrtf((qs.x + qs.y) * (1.0f / kC) + 1e-5f);
+        if (!warp_wait_bounded(&sempty[sb], sph ^ 1u, p.w, abort_flag, 42)) break;
+        zst[sb * BM + r] = make_float2(zrs, -zrs * zmu);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sfull[sb]);
+
+        // LayerNorm of x_ij over its 128 channels: column r of the [c][j] tile, pairs of channels
+        if (!warp_wait_bounded(xfull, ph, p.w, abort_flag, 39)) break;
+        float2 s0 = make_float2(0.f, 0.f), s1 = s0;
+#pragma unroll 8
+        for (int c = 0; c < kC; c += 4) {
+          s0 = __fadd2_rn(s0, make_float2(xs[(c + 0) * BM + r], xs[(c + 1) * BM + r]));
+          s1 = __fadd2_rn(s1, make_float2(xs[(c + 2) * BM + r], xs[(c + 3) * BM + r]));
+        }
+        const float2 ss = __fadd2_rn(s0, s1);
+        const float xmu = (ss.x + ss.y) * (1.0f / kC);
+        const float2 nx = make_float2(-xmu, -xmu);
+        float2 v0 = make_float2(0.f, 0.f), v1 = v0;
+#pragma unroll 8
+        for (int c = 0; c < kC; c += 4) {
+          const float2 d0 = __fadd2_rn(make_float2(xs[(c + 0) * BM + r], xs[(c + 1) * BM + r]), nx);
+          const float2 d1 = __fadd2_rn(make_float2(xs[(c + 2) * BM + r], xs[(c + 3) * BM + r]), nx);
+          v0 = __ffma2_rn(d0, d0, v0);
+          v1 = __ffma2_rn(d1, d1, v1);
+        }
+        const float2 vs = __fadd2_rn(v0, v1);
+        const float xrs = rsqrtf((vs.x + vs.y) * (1.0f / kC) + 1e-5f);
+        const float2 xr2 = make_float2(xrs, xrs), xb2 = make_float2(-xrs * xmu, -xrs * xmu);
+        if (!warp_wait_bounded(hempty, ph ^ 1u, p.w, abort_flag, 40)) break;
+#pragma unroll 2
+        for (int u = 0; u < 16; ++u) {          // 16-byte unit u of the operand row: channels 8u .. 8u+7
+          const int c = u * 8;
+          uint32_t hv[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 xn =
+                __ffma2_rn(make_float2(xs[(c + 2 * k) * BM + r], xs[(c + 2 * k + 1) * BM + r]), xr2, xb2);
+            hv[k] = pack_f16x2(xn.x, xn.y);
+          }
+          *reinterpret_cast<uint4*>(xh + (u >> 3) * (XH_BYTES / 2) + sw128_offset(r, u & 7)) =
+              make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(xempty);
+          mbar_arrive(hfull);
+        }
+        ph ^= 1u;
       }
-      (void)ok;
+    } else {
+      // ------------------------------------------------------------ epilogue, thread = pair
+      const int ew = warp - 2 - LN_WARPS;      // 0..7
+      const int q = warp & 3;                  // TMEM lane quadrant: pairs 32q .. 32q+31
+      const int r = q * 32 + lane;
+      const int hsel = ew >> 2;                // output channels 64*hsel .. 64*hsel + 63
+      const uint32_t tmem_row = tmem_base + ((uint32_t)(q * 32) << 16);
+      int local = 0;
+      for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++local) {
+        const int il = (int)(t / p.tiles_j);
+        const int jt = (int)(t - (long long)il * p.tiles_j);
+        const int buf = local & 1;
+        const uint32_t use = (uint32_t)(local >> 1);
+        const int sb = local & 1;
+        const uint32_t sph = (uint32_t)(local >> 1) & 1u;
+        if (!warp_wait_bounded(&sfull[sb], sph, p.w, abort_flag, 43)) break;
+        if (!warp_wait_bounded(&tfull[buf], use & 1u, p.w, abort_flag, 41)) break;
+        tc_fence_after();
+        const float2 zs2 = zst[sb * BM + r];
+        const int i = p.i0 + il;
+        const int jl = jt * BM + r;
+        const bool valid = jl < p.bj;
+        __nv_bfloat16* dst = p.out + ((size_t)i * p.N + (size_t)(p.j0 + jl)) * kC;
+        if (hsel == 0)
+          finish_pair<0>(p, tmem_row, buf, zs2, dst, valid);
+        else
+          finish_pair<1>(p, tmem_row, buf, zs2, dst, valid);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&tempty[buf]);
+          mbar_arrive(&sempty[sb]);
+        }
+      }
     }
   }
 

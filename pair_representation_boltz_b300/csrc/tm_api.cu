@@ -80,6 +80,7 @@ struct tm_ctx {
   __half* wo16 = nullptr;        // [128][128], scaled
   __nv_bfloat16* wg16 = nullptr; // [hi, lo][128][128]
   float* k3c = nullptr;          // [3][128]
+  float k3c_host[3 * kC] = {};   // the same, passed to the finish kernel in its parameter block
   float inv_scale_o = 1.f;
   CUtensorMap wk1_map, wo_map, wg_map;
   // status word (mapped host memory)
@@ -275,6 +276,7 @@ tm_status prepare_tensor_core_weights(tm_ctx* c, const tm_weights* w) {
     k3c[2 * C + o] = (float)bo;
   }
   c->inv_scale_o = (float)std::ldexp(1.0, -e);
+  std::memcpy(c->k3c_host, k3c.data(), sizeof c->k3c_host);
 
   cudaError_t err;
 #define TM_UP(dst, vec)                                                                       \
@@ -399,7 +401,7 @@ tm_status run_finish_bf16(tm_ctx* c, const float* x, int ldx, const void* z, int
   }
   FinishParams p;
   p.out = reinterpret_cast<__nv_bfloat16*>(out);
-  p.consts = c->k3c;
+  std::memcpy(p.cst, c->k3c_host, sizeof p.cst);
   p.inv_scale_o = c->inv_scale_o;
   p.N = N;
   p.i0 = i0;

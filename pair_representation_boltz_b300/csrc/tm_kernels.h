@@ -43,7 +43,7 @@ struct ContractParams {
 // Output epilogue of one block: out = sigmoid(g) * (W_o LayerNorm(x)).
 struct FinishParams {
   __nv_bfloat16* out;     // [N][N][128]
-  const float* consts;    // [3][128]: rowsum of W_g' (hi+lo), bias W_g beta_in, bias W_o beta_out
+  float cst[3 * kC];      // rowsum of W_g' (hi+lo), bias W_g beta_in, bias W_o beta_out (constant bank)
   float inv_scale_o;      // W_o is stored scaled by a power of two; this undoes it
   int N;
   int i0, j0, bi, bj;
