@@ -25,21 +25,24 @@
 //   warp 1      TMEM (2 x 256 columns) and tcgen05.mma with the channels on
 //               the TMEM lanes: D_proj[c][p] = W'_proj z^T and D_gate[c][p] =
 //               W'_gate z^T (M = 128 channels, N = 128 pairs), hi + lo each.
-//   warps 2..5  LayerNorm statistics, thread = pair, from the z tile in fp32
-//               (packed fp32x2 arithmetic), one tile ahead of the epilogue:
-//               double-buffered in shared memory behind mbarriers, with the
-//               pair mask as one bit per pair (warp ballot).
+//   warps 2..5  LayerNorm statistics, thread = pair: one pass over the z row
+//               (sums of z - z_0 and of its square, fp32x2; the shift by the
+//               row's first value keeps the variance free of cancellation for
+//               rows whose mean is far from zero), the z tile released as soon
+//               as it is read; one tile ahead of the epilogue, double-buffered
+//               in shared memory behind mbarriers, with the pair mask as one
+//               bit per pair (warp ballot).
 //   warps 6..13 epilogue, thread = channel: two warps per TMEM lane quadrant
 //               split the 128 pairs; per-channel folding constants live in
 //               registers; two pairs at a time in fp32x2 arithmetic, the
 //               sigmoid as two MUFU operations, no branch. Results go through
-//               shared memory: each group of four warps fills a 128-channel x
-//               64-pair staging box (128-byte swizzle) that one thread writes
-//               out with a TMA store, so every channel row leaves as a
-//               128-byte line. (Stores straight from the threads, one channel
+//               shared memory: each warp fills its own 32-channel x 64-pair
+//               staging box (128-byte swizzle) that its lane 0 writes out with
+//               one TMA store per tile, so channel rows leave as 128-byte lines
+//               and no warp waits for another; the store drains while the next
+//               tile's MMA runs. (Stores straight from the threads, one channel
 //               row per lane, scatter each warp instruction over 32 DRAM pages
-//               and ran 6x slower.) Two group-local named barriers per tile
-//               fence the staging box.
+//               and ran 6x slower.)
 #include "tm_kernels.h"
 
 namespace tmk {
@@ -52,7 +55,7 @@ constexpr int W_MAT = kC * kC * 2;             // one 128 x 128 bf16 matrix, two
 constexpr int W_BYTES = 4 * W_MAT;             // proj hi, proj lo, gate hi, gate lo
 constexpr int STAT_WARPS = 4, EPI_WARPS = 8;
 constexpr int THREADS = 64 + 32 * (STAT_WARPS + EPI_WARPS);   // TMA, MMA, statistics, epilogue warps
-constexpr int OUT_BYTES = 2 * (int)kBoxProjOut.bytes();        // two staging boxes: pairs 0-63 and 64-127
+constexpr int OUT_BYTES = EPI_WARPS * (int)kBoxProjOut.bytes();      // one staging box per epilogue warp
 constexpr int STAT_BUF = (BM / 2) * 16 + 16;   // float4 {rstd_2k, rstd_2k+1, nmu_2k, nmu_2k+1} + 4 mask words
 constexpr int SMEM_BYTES = STAGES * Z_BYTES + W_BYTES + OUT_BYTES + 2 * STAT_BUF + 256;
 constexpr int TMEM_COLS = 512;
@@ -60,7 +63,8 @@ constexpr int TMEM_COLS = 512;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(2 * kBoxProjZ.bytes() == Z_BYTES, "z tile = two boxes");
 static_assert(2 * kBoxProjW.bytes() == W_MAT, "weight matrix = two boxes");
-static_assert(kBoxProjOut.d0 * 2 == 128, "a staging row is one 128-byte swizzle row");
+static_assert(kBoxProjOut.d0 * 2 == 128 && kBoxProjOut.d2 == 32, "a staging box is 32 channel rows of 128 bytes");
+static_assert(OUT_BYTES == 32768, "staging budget");
 
 __global__ void __launch_bounds__(THREADS, 1)
     k1_project(const __grid_constant__ CUtensorMap zmap, const __grid_constant__ CUtensorMap wmap,
@@ -69,7 +73,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* zs = smem;
   uint8_t* ws = smem + STAGES * Z_BYTES;                  // [proj hi, proj lo, gate hi, gate lo]
-  uint8_t* ostg = ws + W_BYTES;                           // [2 boxes][128 channels][128 B], swizzled
+  uint8_t* ostg = ws + W_BYTES;                           // [epilogue warp][32 channels][128 B], swizzled
   uint8_t* sbase = ostg + OUT_BYTES;                      // [2][STAT_BUF]
   uint64_t* zfull = reinterpret_cast<uint64_t*>(sbase + 2 * STAT_BUF);
   uint64_t* zempty = zfull + STAGES;
@@ -197,38 +201,38 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t sph = (uint32_t)(local >> 1) & 1u;
         if (!warp_wait_bounded(&zfull[s], ph, p.w, abort_flag, 16)) break;
         const uint8_t* zt = zs + s * Z_BYTES;
-        // mean and biased variance over the 128 channels: two passes over the z row in shared memory
-        // (re-read rather than held in registers), fp32x2 arithmetic
-        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll 4
-        for (int k = 0; k < 16; ++k) {
-          const uint4 w4 = *reinterpret_cast<const uint4*>(zt + (k >> 3) * (Z_BYTES / 2) + sw128_offset(t, k & 7));
-          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w4);
+        // one pass over the row: sums of d = z - z_0 and of d^2 (fp32x2), shifted by the row's first
+        // value; the z tile is released as soon as the row is in registers
+        uint4 raw[16];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) acc[e] = __fadd2_rn(acc[e], __bfloat1622float2(h[e]));
-        }
-        const float2 a01 = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
-        const float mu = (a01.x + a01.y) * (1.0f / kC);
-        const float2 mu2 = make_float2(-mu, -mu);
-        float2 sq[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll 4
-        for (int k = 0; k < 16; ++k) {
-          const uint4 w4 = *reinterpret_cast<const uint4*>(zt + (k >> 3) * (Z_BYTES / 2) + sw128_offset(t, k & 7));
-          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w4);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 d = __fadd2_rn(__bfloat1622float2(h[e]), mu2);
-            sq[e] = __ffma2_rn(d, d, sq[e]);
-          }
-        }
+        for (int k = 0; k < 16; ++k)
+          raw[k] = *reinterpret_cast<const uint4*>(zt + (k >> 3) * (Z_BYTES / 2) + sw128_offset(t, k & 7));
         __syncwarp();
         if (lane == 0) mbar_arrive(&zempty[s]);     // this warp has finished reading the z tile
         if (++s == STAGES) {
           s = 0;
           ph ^= 1u;
         }
-        const float2 s01 = __fadd2_rn(__fadd2_rn(sq[0], sq[1]), __fadd2_rn(sq[2], sq[3]));
-        const float rstd = rsqrtf((s01.x + s01.y) * (1.0f / kC) + 1e-5f);
+        const float z0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(&raw[0].x));
+        const float2 nz0 = make_float2(-z0, -z0);
+        float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        float2 sq[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 d = __fadd2_rn(__bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e])), nz0);
+            acc[e & 1] = __fadd2_rn(acc[e & 1], d);
+            sq[e & 1] = __ffma2_rn(d, d, sq[e & 1]);
+          }
+        }
+        const float2 a01 = __fadd2_rn(acc[0], acc[1]);
+        const float2 s01 = __fadd2_rn(sq[0], sq[1]);
+        const float dm = (a01.x + a01.y) * (1.0f / kC);            // mean of d
+        const float mu = z0 + dm;
+        const float var = fmaxf((s01.x + s01.y) * (1.0f / kC) - dm * dm, 0.f);
+        const float rstd = rsqrtf(var + 1e-5f);
         const int j = jt * BM + t;
         float m = 0.f;
         if (j < p.N) m = p.mask ? p.mask[i] * p.mask[j] : 1.0f;
@@ -247,17 +251,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int ew = warp - 2 - STAT_WARPS;    // 0..7
       const int q = warp & 3;                  // TMEM lane quadrant: channels 32q .. 32q+31
       const int c = q * 32 + lane;
-      const int grp = ew >> 2;                 // staging box: pairs 64*grp .. 64*grp + 63
-      const int pbase = grp * 64;
-      const bool issuer = (ew & 3) == 0 && lane == 0;   // one thread per box issues its TMA store
+      const int pbase = (ew >> 2) * 64;        // this warp's 64 pair columns
       const CUtensorMap* omap = half ? &bmap : &amap;
-      uint8_t* const box = ostg + grp * (int)kBoxProjOut.bytes();
+      uint8_t* const box = ostg + ew * (int)kBoxProjOut.bytes();
       const float* cst = p.consts + half * 512;
       const float2 rsp = make_float2(cst[c], cst[c]), rsg = make_float2(cst[kC + c], cst[kC + c]);
       const float2 bp = make_float2(cst[256 + c], cst[256 + c]), bg = make_float2(cst[256 + kC + c], cst[256 + kC + c]);
       const float2 nlog2e = make_float2(-1.4426950408889634f, -1.4426950408889634f);
       const float2 one2 = make_float2(1.f, 1.f);
-      if (issuer) tma_prefetch_desc(omap);
+      if (lane == 0) tma_prefetch_desc(omap);
       int local = 0;
       for (long long u = cta; u < p.total_tiles; u += nctas, ++local) {
         const int i = (int)(u / p.tiles_per_row);
@@ -266,20 +268,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t use = (uint32_t)(local >> 1);
         const int sb = local & 1;
         const uint32_t sph = (uint32_t)(local >> 1) & 1u;
-        // the previous tile's store has finished reading this group's staging box
-        if (issuer) bulk_wait_read<0>();
-        // barrier A (group): the box is free. Every warp of the group stops together once any wait of
-        // the CTA has given up (a warp that left alone would strand the others at the barrier).
-        if (named_bar_or(1 + grp, 128, *abort_flag != 0)) break;
-        bool ok = warp_wait_bounded(&sfull[sb], sph, p.w, abort_flag, 19) &&
-                  warp_wait_bounded(&tfull[buf], use & 1u, p.w, abort_flag, 17);
-        if (ok) {
-          tc_fence_after();
-          const float4* st = reinterpret_cast<const float4*>(sbase + sb * STAT_BUF);
-          const uint32_t* mw = reinterpret_cast<const uint32_t*>(sbase + sb * STAT_BUF + (BM / 2) * 16);
+        if (!warp_wait_bounded(&sfull[sb], sph, p.w, abort_flag, 19)) break;
+        if (!warp_wait_bounded(&tfull[buf], use & 1u, p.w, abort_flag, 17)) break;
+        tc_fence_after();
+        const float4* st = reinterpret_cast<const float4*>(sbase + sb * STAT_BUF);
+        const uint32_t* mw = reinterpret_cast<const uint32_t*>(sbase + sb * STAT_BUF + (BM / 2) * 16);
+        if (lane == 0) bulk_wait_read<0>();     // last tile's store has finished reading the staging box
+        __syncwarp();
+        {
 #pragma unroll 1
-          for (int cc = 0; cc < 4; ++cc) {
-            const int p0 = pbase + cc * 16;       // first pair column of this 16-pair chunk
+          for (int hh = 0; hh < 4; ++hh) {       // four 16-pair TMEM chunks
+            const int p0 = pbase + hh * 16;
             uint32_t pr[16], gt[16];
             const uint32_t ta = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * 2 * BM + p0);
             tmem_ld16(ta, pr);
@@ -318,29 +317,28 @@ __global__ void __launch_bounds__(THREADS, 1)
                 packed[e >> 1] = pack_bf16x2(((mword >> e) & 1u) ? v.x : 0.f, ((mword >> (e + 1)) & 1u) ? v.y : 0.f);
               }
             }
-            // 32 bytes of this channel's row of the staging box: 16-byte units 2cc, 2cc+1
+            // 32 bytes of this channel's 128-byte staging row: 16-byte units 2hh, 2hh+1
 #pragma unroll
             for (int k = 0; k < 2; ++k)
-              *reinterpret_cast<uint4*>(box + sw128_offset(c, cc * 2 + k)) =
+              *reinterpret_cast<uint4*>(box + sw128_offset(lane, hh * 2 + k)) =
                   make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
           }
           fence_proxy_async_smem();
-          tc_fence_before();
           __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&tempty[buf]);
-            mbar_arrive(&sempty[sb]);
+          // pairs past N are clipped by TMA (whole 16-byte granules, inside the row padding of ld)
+          if (lane == 0 && jt * BM + pbase < p.N) {
+            tma_store_3d(omap, box, jt * BM + pbase, i, q * 32);
+            bulk_commit();
           }
         }
-        // barrier B (group): the staging box is complete
-        if (named_bar_or(3 + grp, 128, !ok || *abort_flag != 0)) break;
-        // pairs past N are clipped by TMA (whole 16-byte granules, inside the row padding of ld)
-        if (issuer && jt * BM + pbase < p.N) {
-          tma_store_3d(omap, box, jt * BM + pbase, i, 0);
-          bulk_commit();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&tempty[buf]);
+          mbar_arrive(&sempty[sb]);
         }
       }
-      if (issuer) bulk_wait_all();   // stores out before the CTA's shared memory goes away
+      if (lane == 0) bulk_wait_all();   // stores out before the CTA's shared memory goes away
     }
   }
 

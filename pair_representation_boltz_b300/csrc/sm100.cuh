@@ -266,6 +266,12 @@ __device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t u) {
   return r * 128u + ((u ^ (r & 7u)) << 4);
 }
 
+// Byte offset of the 16-byte unit `u` (0..3) of row `r` inside a 64-byte-swizzled tile of
+// 64-byte rows whose base is 512-byte aligned (the TMA SWIZZLE_64B pattern).
+__device__ __forceinline__ uint32_t sw64_offset(uint32_t r, uint32_t u) {
+  return r * 64u + ((u ^ ((r >> 1) & 3u)) << 4);
+}
+
 // ---------------------------------------------------------------- math helpers
 __device__ __forceinline__ float sigmoidf_fast(float v) {
   // 1 / (1 + e^-v). Clamping v at -80 keeps e^-v below 2^126, where

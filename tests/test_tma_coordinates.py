@@ -55,11 +55,11 @@ def projection_boxes(N):
         yield ("z", kc * 64, 2)
     for kc in (0, 1):
         yield ("w", kc * 64, 2)
-    # stores of a / b: 64 pairs x 128 channels per box, two boxes per 128-pair tile
+    # stores of a / b: 64 pairs x 32 channels per box, two pair-boxes x four channel quadrants per tile
     tiles_per_row = (N + PROJ_J - 1) // PROJ_J
     for jt in range(tiles_per_row):
-        for g in (0, 1):
-            x = jt * PROJ_J + 64 * g
+        for pb in range(0, PROJ_J, 64):
+            x = jt * PROJ_J + pb
             if x < N:
                 yield ("ab-store", x, 2)
 
