@@ -35,7 +35,8 @@
 //   warps 6..13 epilogue, thread = channel: two warps per TMEM lane quadrant
 //               split the 128 pairs; per-channel folding constants live in
 //               registers; two pairs at a time in fp32x2 arithmetic, the
-//               sigmoid as two MUFU operations, no branch. Results go through
+//               two sigmoids with two exponentials and one shared reciprocal
+//               (three MUFU operations), no branch. Results go through
 //               shared memory: each warp fills its own 32-channel x 64-pair
 //               staging box (128-byte swizzle) that its lane 0 writes out with
 //               one TMA store per tile, so channel rows leave as 128-byte lines
@@ -294,14 +295,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                                             __ffma2_rn(n, rsp, bp));
               const float2 gpre = __ffma2_rn(r, make_float2(__uint_as_float(gt[e]), __uint_as_float(gt[e + 1])),
                                              __ffma2_rn(n, rsg, bg));
+              // sigmoid of both gates with one reciprocal: with d = 1 + 2^(-g log2 e),
+              // sigmoid(g0) = d1 / (d0 d1) and sigmoid(g1) = d0 / (d0 d1). The exponent is capped at
+              // 63 so that d0 d1 < 2^127 (a gate below -43 then reads 2^-63 instead of ~0).
               const float2 ga = __fmul2_rn(gpre, nlog2e);
-              float e0, e1, r0, r1;
-              asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(ga.x));
-              asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(ga.y));
+              float e0, e1, rd;
+              asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(fminf(ga.x, 63.f)));
+              asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(fminf(ga.y, 63.f)));
               const float2 den = __fadd2_rn(make_float2(e0, e1), one2);
-              asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r0) : "f"(den.x));
-              asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r1) : "f"(den.y));
-              return __fmul2_rn(make_float2(r0, r1), pre);
+              asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rd) : "f"(den.x * den.y));
+              return __fmul2_rn(__fmul2_rn(make_float2(den.y, den.x), pre), make_float2(rd, rd));
             };
             if ((mword & 0xFFFFu) == 0xFFFFu) {
               // all 16 pairs unmasked and inside the grid (warp-uniform): no per-element mask

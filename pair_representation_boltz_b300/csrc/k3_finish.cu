@@ -11,15 +11,18 @@
 // Per tile of 128 pairs (one row i, 128 consecutive j of the block):
 //   warp 0      TMA: x tile [128 c][128 j] fp32 (64 KB), z tile (two 64-channel
 //               boxes, 128-byte swizzle); W_o (fp16) and W_g (bf16 hi + lo) once.
-//   warps 2..5  LayerNorm, thread = pair: three fp32x2 passes over its x column
-//               in shared memory (mean, variance, normalise) write the fp16 rows
-//               of a K-major operand; two passes over its z row give z's
-//               statistics, handed to the epilogue through a double-buffered
-//               shared array behind mbarriers.
+//   warps 2..5  LayerNorm, two lanes per pair (one per channel half): a shifted
+//               one-pass sum and sum of squares per half, merged across the two
+//               lanes, then a normalising pass that writes the fp16 rows of a
+//               K-major operand; 8-byte loads cover two pairs at a time. z's
+//               statistics the same way, handed to the epilogue through a
+//               double-buffered shared array behind mbarriers. The producer
+//               also prefetches the next two tiles' boxes into L2.
 //   warp 1      tcgen05.mma: D[p][0..128) = xh x W_o'^T (kind::f16, fp16),
 //               D[p][128..256) = z x W_g'^T (bf16, hi and lo), two TMEM buffers.
 //   warps 6..13 epilogue, thread = pair: two warps per TMEM lane quadrant split
-//               the 128 output channels; gate, product and 16-byte stores of out.
+//               the 128 output channels; gate (sigmoid through one tanh), product
+//               and 16-byte stores of out.
 // LayerNorm_out's gamma is folded into W_o' = W_o diag(gamma_out) (scaled by a
 // power of two to use fp16's range) and beta into a bias; LayerNorm_in of the
 // gate is folded as in the projection: W_g zh = rstd (W_g' z - mu rowsum) + bias.
@@ -57,8 +60,6 @@ __device__ __forceinline__ void finish_pair(const FinishParams& p, uint32_t tmem
                                             __nv_bfloat16* dst, bool valid) {
   const float2 inv = make_float2(p.inv_scale_o, p.inv_scale_o);
   const float2 r2 = make_float2(zst.x, zst.x), n2 = make_float2(zst.y, zst.y);
-  const float2 nlog2e = make_float2(-1.4426950408889634f, -1.4426950408889634f);
-  const float2 one2 = make_float2(1.f, 1.f);
 #pragma unroll
   for (int cc = 0; cc < 4; ++cc) {
     const int o0 = 64 * H + cc * 16;
@@ -70,19 +71,14 @@ __device__ __forceinline__ void finish_pair(const FinishParams& p, uint32_t tmem
 #pragma unroll
     for (int e = 0; e < 16; e += 2) {
       const int o = o0 + e;
-      const float2 y = __ffma2_rn(make_float2(__uint_as_float(yv[e]), __uint_as_float(yv[e + 1])), inv,
-                                  make_float2(p.cst[2 * kC + o], p.cst[2 * kC + o + 1]));
-      const float2 g = __ffma2_rn(r2, make_float2(__uint_as_float(gv[e]), __uint_as_float(gv[e + 1])),
-                                  __ffma2_rn(n2, make_float2(p.cst[o], p.cst[o + 1]),
-                                             make_float2(p.cst[kC + o], p.cst[kC + o + 1])));
-      const float2 ga = __fmul2_rn(g, nlog2e);
-      float e0, e1, s0, s1;
-      asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(ga.x));
-      asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(ga.y));
-      const float2 den = __fadd2_rn(make_float2(e0, e1), one2);
-      asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(s0) : "f"(den.x));
-      asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(s1) : "f"(den.y));
-      const float2 v = __fmul2_rn(make_float2(s0, s1), y);
+      // W_o', its bias, W_g' and the gate constants all carry a factor 1/2 (exact), so that
+      // hy = y / 2 and hg = g / 2, and y * sigmoid(g) = hy + hy * tanh(hg): one MUFU operation.
+      const float2 hy = __ffma2_rn(make_float2(__uint_as_float(yv[e]), __uint_as_float(yv[e + 1])), inv,
+                                   make_float2(p.cst[2 * kC + o], p.cst[2 * kC + o + 1]));
+      const float2 hg = __ffma2_rn(r2, make_float2(__uint_as_float(gv[e]), __uint_as_float(gv[e + 1])),
+                                   __ffma2_rn(n2, make_float2(p.cst[o], p.cst[o + 1]),
+                                              make_float2(p.cst[kC + o], p.cst[kC + o + 1])));
+      const float2 v = __ffma2_rn(hy, make_float2(tanh_mufu(hg.x), tanh_mufu(hg.y)), hy);
       packed[e >> 1] = pack_bf16x2(v.x, v.y);
     }
     if (valid) {
@@ -159,6 +155,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int hl = 0; hl < 2; ++hl)
           for (int kc = 0; kc < 2; ++kc)
             tma_load_2d(wg + (hl * 2 + kc) * (WO_BYTES / 2), &wgmap, wfull, kc * 64, hl * kC);
+        // the x and z boxes of the tiles one and two steps ahead are prefetched into L2, so that a
+        // buffer, once free, refills at L2 rather than HBM latency
+        auto prefetch = [&](long long t) {
+          if (t >= p.total_tiles) return;
+          const int il = (int)(t / p.tiles_j);
+          const int jt = (int)(t - (long long)il * p.tiles_j);
+          tma_prefetch_l2_3d(&xmap, jt * BM, il, 0);
+          tma_prefetch_l2_3d(&zmap, 0, p.j0 + jt * BM, p.i0 + il);
+          tma_prefetch_l2_3d(&zmap, 64, p.j0 + jt * BM, p.i0 + il);
+        };
         uint32_t ph = 0;
         for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
           const int il = (int)(t / p.tiles_j);
@@ -170,6 +176,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_expect_tx(zfull, Z_BYTES);
           tma_load_3d(zs, &zmap, zfull, 0, p.j0 + jt * BM, p.i0 + il);
           tma_load_3d(zs + Z_BYTES / 2, &zmap, zfull, 64, p.j0 + jt * BM, p.i0 + il);
+          if (t == blockIdx.x) prefetch(t + gridDim.x);
+          prefetch(t + 2 * (long long)gridDim.x);
           ph ^= 1u;
         }
       }
@@ -212,81 +220,101 @@ __global__ void __launch_bounds__(THREADS, 1)
         wait_bounded(fin, 0, p.w, abort_flag, 37);
       }
     } else if (warp < 2 + LN_WARPS) {
-      // ------------------------------------------------------------ LayerNorm, thread = pair
-      const int r = (warp - 2) * 32 + lane;
+      // ------------------------------------------------------------ LayerNorm, two lanes per pair
+      // Lane l of LayerNorm warp w takes channel half hc = l / 16 of pair group 32w .. 32w+31:
+      // x columns p0 = 32w + 2 (l % 16) and p0 + 1 (8-byte loads along j, fp32x2 math over the two
+      // pairs), z rows 32w + l % 16 and that + 16. Each half gives a shifted one-pass mean and sum of
+      // squared deviations of its 64 channels; the two halves meet through a lane exchange and are
+      // merged with the pairwise update of the mean and the sum of squares (Chan, Golub, LeVeque).
+      const int lw = warp - 2;
+      const int lp = lane & 15, hc = lane >> 4;
+      const int p0 = lw * 32 + 2 * lp;
+      const int zr0 = lw * 32 + lp;
       uint32_t ph = 0;
       int local = 0;
+      // mean and variance of 128 channels from the two halves' (mean, M2) over 64 channels each
+      auto merge = [](float mean_h, float m2_h, float& mean, float& rstd) {
+        const float mean_o = __shfl_xor_sync(0xffffffffu, mean_h, 16);
+        const float m2_o = __shfl_xor_sync(0xffffffffu, m2_h, 16);
+        const float dm = mean_h - mean_o;
+        mean = 0.5f * (mean_h + mean_o);
+        const float var = fmaxf((m2_h + m2_o + 32.0f * dm * dm) * (1.0f / kC), 0.f);
+        rstd = rsqrtf(var + 1e-5f);
+      };
       for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++local) {
         const int sb = local & 1;
         const uint32_t sph = (uint32_t)(local >> 1) & 1u;
-        // statistics of z_ij over its 128 channels (two passes over the smem row, fp32x2)
+        // statistics of z over its 128 channels: rows zr0 and zr0 + 16, K-chunk hc of the tile
         if (!warp_wait_bounded(zfull, ph, p.w, abort_flag, 38)) break;
-        float2 a0 = make_float2(0.f, 0.f), a1 = a0;
-#pragma unroll 4
-        for (int k = 0; k < 16; ++k) {
-          const uint4 w4 = *reinterpret_cast<const uint4*>(zs + (k >> 3) * (Z_BYTES / 2) + sw128_offset(r, k & 7));
-          a0 = __fadd2_rn(a0, __fadd2_rn(bf2f(w4.x), bf2f(w4.y)));
-          a1 = __fadd2_rn(a1, __fadd2_rn(bf2f(w4.z), bf2f(w4.w)));
+        float zmean[2], zrstd[2];
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+          const int row = zr0 + 16 * rr;
+          const uint8_t* zrow = zs + hc * (Z_BYTES / 2);
+          uint4 raw[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) raw[u] = *reinterpret_cast<const uint4*>(zrow + sw128_offset(row, u));
+          const float sh = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(&raw[0].x));
+          const float2 nsh = make_float2(-sh, -sh);
+          float2 a0 = make_float2(0.f, 0.f), a1 = a0, q0 = a0, q1 = a0;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const float2 d0 = __fadd2_rn(bf2f(raw[u].x), nsh), d1 = __fadd2_rn(bf2f(raw[u].y), nsh);
+            const float2 d2 = __fadd2_rn(bf2f(raw[u].z), nsh), d3 = __fadd2_rn(bf2f(raw[u].w), nsh);
+            a0 = __fadd2_rn(a0, __fadd2_rn(d0, d2));
+            a1 = __fadd2_rn(a1, __fadd2_rn(d1, d3));
+            q0 = __ffma2_rn(d0, d0, __ffma2_rn(d2, d2, q0));
+            q1 = __ffma2_rn(d1, d1, __ffma2_rn(d3, d3, q1));
+          }
+          const float2 as = __fadd2_rn(a0, a1), qs = __fadd2_rn(q0, q1);
+          const float sd = as.x + as.y;
+          merge(sh + sd * (1.0f / 64), (qs.x + qs.y) - sd * sd * (1.0f / 64), zmean[rr], zrstd[rr]);
         }
-        const float2 as = __fadd2_rn(a0, a1);
-        const float zmu = (as.x + as.y) * (1.0f / kC);
-        const float2 nz = make_float2(-zmu, -zmu);
-        float2 q0 = make_float2(0.f, 0.f), q1 = q0;
-#pragma unroll 4
-        for (int k = 0; k < 16; ++k) {
-          const uint4 w4 = *reinterpret_cast<const uint4*>(zs + (k >> 3) * (Z_BYTES / 2) + sw128_offset(r, k & 7));
-          float2 d;
-          d = __fadd2_rn(bf2f(w4.x), nz);
-          q0 = __ffma2_rn(d, d, q0);
-          d = __fadd2_rn(bf2f(w4.y), nz);
-          q1 = __ffma2_rn(d, d, q1);
-          d = __fadd2_rn(bf2f(w4.z), nz);
-          q0 = __ffma2_rn(d, d, q0);
-          d = __fadd2_rn(bf2f(w4.w), nz);
-          q1 = __ffma2_rn(d, d, q1);
-        }
-        const float2 qs = __fadd2_rn(q0, q1);
-        const float zrs = rsqrtf((qs.x + qs.y) * (1.0f / kC) + 1e-5f);
         if (!warp_wait_bounded(&sempty[sb], sph ^ 1u, p.w, abort_flag, 42)) break;
-        zst[sb * BM + r] = make_float2(zrs, -zrs * zmu);
+        // lane hc of the two that share the rows writes row zr0 + 16 hc
+        zst[sb * BM + zr0 + 16 * hc] = hc ? make_float2(zrstd[1], -zrstd[1] * zmean[1])
+                                          : make_float2(zrstd[0], -zrstd[0] * zmean[0]);
         __syncwarp();
         if (lane == 0) mbar_arrive(&sfull[sb]);
 
-        // LayerNorm of x_ij over its 128 channels: column r of the [c][j] tile, pairs of channels
+        // LayerNorm of x over its 128 channels: columns p0, p0 + 1 of the [c][j] tile, channels of half hc
         if (!warp_wait_bounded(xfull, ph, p.w, abort_flag, 39)) break;
-        float2 s0 = make_float2(0.f, 0.f), s1 = s0;
+        const float* xcol = xs + (hc * 64) * BM + p0;
+        const float2 xsh = *reinterpret_cast<const float2*>(xcol);
+        const float2 nxsh = make_float2(-xsh.x, -xsh.y);
+        float2 s0 = make_float2(0.f, 0.f), s1 = s0, v0 = s0, v1 = s0;
 #pragma unroll 8
-        for (int c = 0; c < kC; c += 4) {
-          s0 = __fadd2_rn(s0, make_float2(xs[(c + 0) * BM + r], xs[(c + 1) * BM + r]));
-          s1 = __fadd2_rn(s1, make_float2(xs[(c + 2) * BM + r], xs[(c + 3) * BM + r]));
-        }
-        const float2 ss = __fadd2_rn(s0, s1);
-        const float xmu = (ss.x + ss.y) * (1.0f / kC);
-        const float2 nx = make_float2(-xmu, -xmu);
-        float2 v0 = make_float2(0.f, 0.f), v1 = v0;
-#pragma unroll 8
-        for (int c = 0; c < kC; c += 4) {
-          const float2 d0 = __fadd2_rn(make_float2(xs[(c + 0) * BM + r], xs[(c + 1) * BM + r]), nx);
-          const float2 d1 = __fadd2_rn(make_float2(xs[(c + 2) * BM + r], xs[(c + 3) * BM + r]), nx);
+        for (int c = 0; c < 64; c += 2) {
+          const float2 d0 = __fadd2_rn(*reinterpret_cast<const float2*>(xcol + c * BM), nxsh);
+          const float2 d1 = __fadd2_rn(*reinterpret_cast<const float2*>(xcol + (c + 1) * BM), nxsh);
+          s0 = __fadd2_rn(s0, d0);
+          s1 = __fadd2_rn(s1, d1);
           v0 = __ffma2_rn(d0, d0, v0);
           v1 = __ffma2_rn(d1, d1, v1);
         }
-        const float2 vs = __fadd2_rn(v0, v1);
-        const float xrs = rsqrtf((vs.x + vs.y) * (1.0f / kC) + 1e-5f);
-        const float2 xr2 = make_float2(xrs, xrs), xb2 = make_float2(-xrs * xmu, -xrs * xmu);
+        const float2 ss = __fadd2_rn(s0, s1), vs = __fadd2_rn(v0, v1);
+        float xm0, xr0, xm1, xr1;
+        merge(xsh.x + ss.x * (1.0f / 64), vs.x - ss.x * ss.x * (1.0f / 64), xm0, xr0);
+        merge(xsh.y + ss.y * (1.0f / 64), vs.y - ss.y * ss.y * (1.0f / 64), xm1, xr1);
+        const float2 xr2 = make_float2(xr0, xr1), xb2 = make_float2(-xr0 * xm0, -xr1 * xm1);
         if (!warp_wait_bounded(hempty, ph ^ 1u, p.w, abort_flag, 40)) break;
+        uint8_t* xhc = xh + hc * (XH_BYTES / 2);
 #pragma unroll 2
-        for (int u = 0; u < 16; ++u) {          // 16-byte unit u of the operand row: channels 8u .. 8u+7
-          const int c = u * 8;
-          uint32_t hv[4];
+        for (int u = 0; u < 8; ++u) {
+          // 16-byte unit uu (channels 64 hc + 8 uu ..) of rows p0 and p0 + 1; the unit order is
+          // rotated by lane group so that the 16 lanes of a half store to distinct bank groups
+          const int uu = (u + (lp >> 2)) & 7;
+          const float* xc = xcol + (8 * uu) * BM;
+          uint32_t h0[4], h1[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const float2 xn =
-                __ffma2_rn(make_float2(xs[(c + 2 * k) * BM + r], xs[(c + 2 * k + 1) * BM + r]), xr2, xb2);
-            hv[k] = pack_f16x2(xn.x, xn.y);
+            const float2 e0 = __ffma2_rn(*reinterpret_cast<const float2*>(xc + (2 * k) * BM), xr2, xb2);
+            const float2 e1 = __ffma2_rn(*reinterpret_cast<const float2*>(xc + (2 * k + 1) * BM), xr2, xb2);
+            h0[k] = pack_f16x2(e0.x, e1.x);
+            h1[k] = pack_f16x2(e0.y, e1.y);
           }
-          *reinterpret_cast<uint4*>(xh + (u >> 3) * (XH_BYTES / 2) + sw128_offset(r, u & 7)) =
-              make_uint4(hv[0], hv[1], hv[2], hv[3]);
+          *reinterpret_cast<uint4*>(xhc + sw128_offset(p0, uu)) = make_uint4(h0[0], h0[1], h0[2], h0[3]);
+          *reinterpret_cast<uint4*>(xhc + sw128_offset(p0 + 1, uu)) = make_uint4(h1[0], h1[1], h1[2], h1[3]);
         }
         fence_proxy_async_smem();
         __syncwarp();

@@ -263,19 +263,20 @@ tm_status prepare_tensor_core_weights(tm_ctx* c, const tm_weights* w) {
     for (int k = 0; k < C; ++k) {
       wo[(size_t)o * C + k] = __float2half_rn((float)((double)w->w_o[(size_t)o * C + k] * w->ln_out_gamma[k] * sc));
       bo += (double)w->w_o[(size_t)o * C + k] * (double)w->ln_out_beta[k];
-      const double vg = (double)w->w_g[(size_t)o * C + k] * (double)w->ln_in_gamma[k];
+      // the finish kernel's gate reads W_g zh / 2 (sigmoid through tanh of the half argument)
+      const double vg = 0.5 * (double)w->w_g[(size_t)o * C + k] * (double)w->ln_in_gamma[k];
       __nv_bfloat16 hi, lo;
       split_bf16(vg, &hi, &lo);
       wg[(size_t)o * C + k] = hi;
       wg[(size_t)(C + o) * C + k] = lo;
       rs += (double)__bfloat162float(hi) + (double)__bfloat162float(lo);
-      bg += (double)w->w_g[(size_t)o * C + k] * (double)w->ln_in_beta[k];
+      bg += 0.5 * (double)w->w_g[(size_t)o * C + k] * (double)w->ln_in_beta[k];
     }
     k3c[o] = (float)rs;
     k3c[C + o] = (float)bg;
-    k3c[2 * C + o] = (float)bo;
+    k3c[2 * C + o] = (float)(0.5 * bo);     // the output projection is read as y / 2 as well
   }
-  c->inv_scale_o = (float)std::ldexp(1.0, -e);
+  c->inv_scale_o = (float)std::ldexp(1.0, -e - 1);
   std::memcpy(c->k3c_host, k3c.data(), sizeof c->k3c_host);
 
   cudaError_t err;
