@@ -11,42 +11,50 @@
 // context parallelism e quebra barreira de memória da GPU"); here the N x N
 // grid is tiled inside one GPU.
 //
-// Design (one CTA per SM, persistent over (channel, i-tile, j-tile)):
-//   warp 0      TMA producer: 128 x 64 A tile and 256 x 64 B tile per stage,
-//               128-byte swizzle, 4-stage ring of mbarriers.
-//   warp 1      TMEM allocator and single-thread tcgen05.mma issuer
-//               (M = 128, N = 256, K = 16 per instruction, f32 accumulate),
-//               two TMEM accumulators so the epilogue of one tile overlaps the
-//               main loop of the next.
-//   warps 2..5  epilogue: tcgen05.ld 32 columns at a time into a per-warp
-//               128-byte-swizzled staging tile (two per warp), TMA store of
-//               each 32 x 32 float32 sub-tile; TMA clips the block edges.
-//               (Blocks whose origin is not a multiple of 8 fall back to
-//               direct 16-byte stores: a TMA box must not start below zero or
-//               off its 16-byte inner-axis grid.)
-// Incoming reads the same a/b buffers through tensor maps whose box runs
-// along the other pair index ("transposed" boxes), and tells the MMA that A
-// and B are M/N-major; no transpose is ever materialised. k beyond N is
-// zero-filled by TMA.
+// Design: clusters of two CTAs (one per SM), persistent over (channel, i-tile,
+// j-tile) with 256 x 256 output tiles. The pair's tensor cores run one
+// M = 256, N = 256 MMA: each CTA stages its own 128 rows of A and its own 128
+// of the tile's 256 B rows, so that per multiply-add each SM reads half the B
+// bytes a single-CTA 128 x 256 tile would need, from L2 and from shared memory.
+//   warp 0      (both CTAs) TMA producer: 128 x 64 A and 128 x 64 B per stage,
+//               128-byte swizzle, 6-stage ring; completion of both CTAs' copies
+//               is counted on the first CTA's "full" barrier, the stage's
+//               release arrives on both CTAs' "empty" barriers.
+//   warp 1      TMEM (512 columns, two 256-column accumulators, allocated in both
+//               CTAs together); in the first CTA, the single-thread issuer of
+//               tcgen05.mma.cta_group::2 (K = 16 per instruction, f32 accumulate).
+//   warps 2..5  (both CTAs) epilogue of the CTA's 128 rows: tcgen05.ld 32 columns
+//               at a time into a per-warp 128-byte-swizzled staging tile (two per
+//               warp), TMA store of each 32 x 32 float32 sub-tile; TMA clips the
+//               block edges. The accumulator goes back to the MMA issuer when the
+//               warps of both CTAs have arrived on the first CTA's barrier.
+//               (Blocks whose origin is not a multiple of 8 fall back to direct
+//               16-byte stores: a TMA box must not start below zero or off its
+//               16-byte inner-axis grid.)
+// Incoming reads the same a/b buffers through tensor maps whose box runs along
+// the other pair index ("transposed" boxes), and tells the MMA that A and B are
+// M/N-major; no transpose is ever materialised. k beyond N is zero-filled by TMA.
 #include "tm_kernels.h"
 
 namespace tmk {
 namespace {
 
-constexpr int BM = kContractBM, BN = kContractBN, BK = kContractBK;
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;          // 16 KB
-constexpr int B_BYTES = BN * BK * 2;          // 32 KB
+constexpr int BM = kContractBM, BN = kContractBN, BK = kContractBK;   // 256 x 256 tile of the pair
+constexpr int HM = BM / 2, HN = BN / 2;       // rows of A and of B staged by each CTA
+constexpr int STAGES = 6;
+constexpr int A_BYTES = HM * BK * 2;          // 16 KB
+constexpr int B_BYTES = HN * BK * 2;          // 16 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 2 * BN;             // two accumulators
 constexpr int THREADS = 192;
-constexpr int STG_BYTES = 32 * 32 * 4;         // one 32 x 32 float32 staging tile
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 4 * 2 * STG_BYTES + 256;
+constexpr int EPI_WARPS = 4;
+constexpr int STG_BYTES = 32 * 32 * 4;        // one 32 x 32 float32 staging tile
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_WARPS * 2 * STG_BYTES + 256;
 
 static_assert(TMEM_COLS == 512, "two 256-column accumulators fill TMEM");
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(kBoxContractOutA.bytes() == A_BYTES && kBoxContractOutB.bytes() == B_BYTES, "outgoing boxes");
-static_assert(2 * kBoxContractIn.bytes() == A_BYTES && (BN / 64) * kBoxContractIn.bytes() == B_BYTES,
-              "incoming boxes");
+static_assert(2 * kBoxContractIn.bytes() == A_BYTES && 2 * kBoxContractIn.bytes() == B_BYTES, "incoming boxes");
 static_assert(kBoxContractX.bytes() == 32 * 32 * 4, "x store box");
 
 struct Tile {
@@ -63,13 +71,13 @@ __device__ __forceinline__ Tile decode(long long t, const ContractParams& p) {
 }
 
 template <bool INCOMING>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     k2_contract(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap,
                 const __grid_constant__ CUtensorMap xmap, const ContractParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* tiles = smem;
   uint8_t* stg = smem + STAGES * STAGE_BYTES;     // [epilogue warp][2][32 x 32 float32], 1024-aligned
-  uint64_t* full = reinterpret_cast<uint64_t*>(stg + 4 * 2 * STG_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(stg + EPI_WARPS * 2 * STG_BYTES);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
@@ -78,16 +86,18 @@ __global__ void __launch_bounds__(THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();        // 0: issues the MMAs; 1: its peer
+  const long long pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   if (threadIdx.x == 0) {
     *abort_flag = (smem_u32(smem) & 1023u) ? 1 : 0;  // swizzled tiles need 1024-byte alignment
     if (*abort_flag) raise_status(p.w, ST_TIMEOUT, 90);
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&full[s], 1);     // first CTA: its producer's arrival + both CTAs' bytes
+      mbar_init(&empty[s], 1);    // both CTAs: the stage's MMAs have read it
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 4);
+      mbar_init(&tfull[b], 1);                 // both CTAs: the accumulator is complete
+      mbar_init(&tempty[b], 2 * EPI_WARPS);    // first CTA: both CTAs' epilogues are done with it
     }
     mbar_init(fin, 1);
     fence_mbar_init();
@@ -97,41 +107,46 @@ __global__ void __launch_bounds__(THREADS, 1)
     tma_prefetch_desc(&bmap);
   }
   if (warp == 1) {
-    tmem_alloc(tslot, TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(tslot, TMEM_COLS);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();      // both CTAs' barriers are initialised before either signals the other's
   tc_fence_after();
   const uint32_t tmem_base = *tslot;
   const int KB = (p.N + BK - 1) / BK;
-
+  // the first CTA's barriers, as cluster-window addresses (valid from either CTA)
+  const uint32_t full0 = mapa_cluster(smem_u32(full), 0);
+  const uint32_t tempty0 = mapa_cluster(smem_u32(tempty), 0);
   if (!*abort_flag) {
     if (warp == 0) {
-      // ------------------------------------------------------------ TMA producer
+      // ------------------------------------------------------------ TMA producer (both CTAs)
       if (lane == 0) {
         int s = 0;
         uint32_t ph = 0;
-        for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+        for (long long t = pair; t < p.total_tiles; t += npairs) {
           const Tile tl = decode(t, p);
           // ia, jb are multiples of 8: the incoming boxes start there along their inner axis
-          const int ia = p.i_base + tl.ti * BM;
-          const int jb = p.j_base + tl.tj * BN;
+          const int ia = p.i_base + tl.ti * BM + (int)rank * HM;
+          const int jb = p.j_base + tl.tj * BN + (int)rank * HN;
           for (int kb = 0; kb < KB; ++kb) {
             if (!wait_bounded(&empty[s], ph ^ 1u, p.w, abort_flag, 1)) goto producer_done;
             uint8_t* sa = tiles + s * STAGE_BYTES;
             uint8_t* sb = sa + A_BYTES;
-            mbar_expect_tx(&full[s], STAGE_BYTES);
+            // the first CTA's "full" barrier counts the bytes of both CTAs' copies
+            const uint32_t fb = rank == 0 ? smem_u32(&full[s]) : full0 + (uint32_t)(s * 8);
+            if (rank == 0) mbar_expect_tx_u32(fb, 2 * STAGE_BYTES);
             if (!INCOMING) {
               // A_c[i][k] = a_ik: rows i, k contiguous (K-major); B_c[j][k] = b_jk likewise.
-              tma_load_3d(sa, &amap, &full[s], kb * BK, ia, tl.c);
-              tma_load_3d(sb, &bmap, &full[s], kb * BK, jb, tl.c);
+              tma_load_3d_pair(sa, &amap, fb, kb * BK, ia, tl.c);
+              tma_load_3d_pair(sb, &bmap, fb, kb * BK, jb, tl.c);
             } else {
               // a_ki, b_kj: rows k, i (or j) contiguous; 64-wide slabs along i / j (M/N-major).
-              tma_load_3d(sa, &amap, &full[s], ia, kb * BK, tl.c);
-              tma_load_3d(sa + 8192, &amap, &full[s], ia + 64, kb * BK, tl.c);
-#pragma unroll
-              for (int h = 0; h < BN / 64; ++h) tma_load_3d(sb + h * 8192, &bmap, &full[s], jb + 64 * h, kb * BK, tl.c);
+              tma_load_3d_pair(sa, &amap, fb, ia, kb * BK, tl.c);
+              tma_load_3d_pair(sa + 8192, &amap, fb, ia + 64, kb * BK, tl.c);
+              tma_load_3d_pair(sb, &bmap, fb, jb, kb * BK, tl.c);
+              tma_load_3d_pair(sb + 8192, &bmap, fb, jb + 64, kb * BK, tl.c);
             }
             if (++s == STAGES) {
               s = 0;
@@ -142,13 +157,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       producer_done:;
       }
     } else if (warp == 1) {
-      // ------------------------------------------------------------ MMA issuer
-      if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer (first CTA)
+      if (lane == 0 && rank == 0) {
         constexpr uint32_t idesc = make_idesc(BM, BN, FMT_BF16, INCOMING, INCOMING);
         int s = 0;
         uint32_t ph = 0;
         int local = 0;
-        for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++local) {
+        for (long long t = pair; t < p.total_tiles; t += npairs, ++local) {
           const int buf = local & 1;
           const uint32_t use = (uint32_t)(local >> 1);
           if (!wait_bounded(&tempty[buf], (use & 1u) ^ 1u, p.w, abort_flag, 2)) break;
@@ -173,30 +188,30 @@ __global__ void __launch_bounds__(THREADS, 1)
                 ad = make_sdesc_sw128(a0 + ks * 2048, 8192, 1024);
                 bd = make_sdesc_sw128(b0 + ks * 2048, 8192, 1024);
               }
-              mma_f16(d, ad, bd, idesc, (kb | ks) != 0);
+              mma_f16_pair(d, ad, bd, idesc, (kb | ks) != 0);
             }
-            mma_commit(&empty[s]);
+            mma_commit_pair(&empty[s]);
             if (++s == STAGES) {
               s = 0;
               ph ^= 1u;
             }
           }
           if (!ok) break;
-          mma_commit(&tfull[buf]);
+          mma_commit_pair(&tfull[buf]);
         }
         // every MMA issued by this thread has completed before TMEM is released
-        mma_commit(fin);
+        mma_commit_pair(fin);
         wait_bounded(fin, 0, p.w, abort_flag, 4);
       }
     } else {
-      // ------------------------------------------------------------ epilogue
+      // ------------------------------------------------------------ epilogue (both CTAs)
       const int q = warp & 3;  // TMEM lanes 32q .. 32q+31 belong to this warp
       const int r = q * 32 + lane;
       uint8_t* const my_stg = stg + (warp - 2) * 2 * STG_BYTES;
       int sb = 0;
       if (lane == 0 && p.tma_store) tma_prefetch_desc(&xmap);
       int local = 0;
-      for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++local) {
+      for (long long t = pair; t < p.total_tiles; t += npairs, ++local) {
         const Tile tl = decode(t, p);
         const int buf = local & 1;
         const uint32_t use = (uint32_t)(local >> 1);
@@ -204,7 +219,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         if (p.tma_store) {
           // i_base == i0 and j_base == j0 here, so every coordinate is >= 0 and 32-aligned along j
-          const int row0 = tl.ti * BM + q * 32;
+          const int row0 = tl.ti * BM + (int)rank * HM + q * 32;
 #pragma unroll 1
           for (int ch = 0; ch < BN / 32; ++ch) {
             const int col0 = tl.tj * BN + ch * 32;
@@ -230,38 +245,35 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             sb ^= 1;
           }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&tempty[buf]);
-          continue;
-        }
-        // block-local row of this thread's TMEM lane, and block-local column of the tile's first column
-        const int il = p.i_base + tl.ti * BM + r - p.i0;
-        const bool row_ok = il >= 0 && il < p.bi;
-        const int jl0 = p.j_base + tl.tj * BN - p.j0;   // in (-8, bj)
-        float* xrow = p.x + (long long)tl.c * p.chan_stride + (long long)(row_ok ? il : 0) * p.ldx;
+        } else {
+          // block-local row of this thread's TMEM lane, and block-local column of the tile's first column
+          const int il = p.i_base + tl.ti * BM + (int)rank * HM + r - p.i0;
+          const bool row_ok = il >= 0 && il < p.bi;
+          const int jl0 = p.j_base + tl.tj * BN - p.j0;   // in (-8, bj)
+          float* xrow = p.x + (long long)tl.c * p.chan_stride + (long long)(row_ok ? il : 0) * p.ldx;
 #pragma unroll 1
-        for (int ch = 0; ch < BN / 32; ++ch) {
-          uint32_t v[32];
-          tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + ch * 32), v);
-          tmem_ld_wait();
-          const int jc = jl0 + ch * 32;
-          if (row_ok && jc < p.bj && jc + 32 > 0) {
-            if (jc >= 0 && jc + 32 <= p.bj && (jc & 3) == 0) {
-              float* dst = xrow + jc;   // 16-byte aligned: x, ldx and chan_stride are multiples of 4
+          for (int ch = 0; ch < BN / 32; ++ch) {
+            uint32_t v[32];
+            tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + ch * 32), v);
+            tmem_ld_wait();
+            const int jc = jl0 + ch * 32;
+            if (row_ok && jc < p.bj && jc + 32 > 0) {
+              if (jc >= 0 && jc + 32 <= p.bj && (jc & 3) == 0) {
+                float* dst = xrow + jc;   // 16-byte aligned: x, ldx and chan_stride are multiples of 4
 #pragma unroll
-              for (int e = 0; e < 32; e += 4)
-                *reinterpret_cast<uint4*>(dst + e) = make_uint4(v[e], v[e + 1], v[e + 2], v[e + 3]);
-            } else {
+                for (int e = 0; e < 32; e += 4)
+                  *reinterpret_cast<uint4*>(dst + e) = make_uint4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+              } else {
 #pragma unroll
-              for (int e = 0; e < 32; ++e)
-                if (jc + e >= 0 && jc + e < p.bj) xrow[jc + e] = __uint_as_float(v[e]);
+                for (int e = 0; e < 32; ++e)
+                  if (jc + e >= 0 && jc + e < p.bj) xrow[jc + e] = __uint_as_float(v[e]);
+              }
             }
           }
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[buf]);
+        if (lane == 0) mbar_arrive_cluster(tempty0 + (uint32_t)(buf * 8));
       }
       if (lane == 0) bulk_wait_all();   // stores done before the CTA's shared memory goes away
     }
@@ -269,14 +281,16 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   __syncthreads();
   if (*abort_flag) {
-    // give in-flight TMA copies time to land before the CTA's shared memory is released
+    // give in-flight TMA copies (this CTA's and the peer's, which signal this CTA) time to land
     const uint64_t t0 = gtimer();
     while (gtimer() - t0 < 2000000ull) {
     }
   }
+  tc_fence_before();
+  cluster_sync_all();      // the peer's TMEM is written by the first CTA's MMAs: both are done first
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
 }
 
@@ -294,7 +308,10 @@ cudaError_t launch_contract_bf16(bool incoming, const CUtensorMap& amap, const C
     attr_set = true;
   }
   if (p.total_tiles <= 0) return cudaSuccess;
-  const int grid = (int)(p.total_tiles < num_sms ? p.total_tiles : num_sms);
+  long long pairs = num_sms / 2;
+  if (pairs > p.total_tiles) pairs = p.total_tiles;
+  if (pairs < 1) pairs = 1;
+  const int grid = (int)(2 * pairs);
   if (incoming)
     k2_contract<true><<<grid, THREADS, SMEM_BYTES, s>>>(amap, bmap, xmap, p);
   else

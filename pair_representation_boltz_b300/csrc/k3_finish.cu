@@ -21,8 +21,11 @@
 //   warp 1      tcgen05.mma: D[p][0..128) = xh x W_o'^T (kind::f16, fp16),
 //               D[p][128..256) = z x W_g'^T (bf16, hi and lo), two TMEM buffers.
 //   warps 6..13 epilogue, thread = pair: two warps per TMEM lane quadrant split
-//               the 128 output channels; gate (sigmoid through one tanh), product
-//               and 16-byte stores of out.
+//               the 128 output channels; gate (sigmoid through one tanh) and
+//               product, staged in the x-hat buffer (free once the tile's MMA has
+//               read it) and written by one TMA store of 32 pairs x 64 channels
+//               per warp; the buffer goes back to the LayerNorm warps when the
+//               stores have read it.
 // LayerNorm_out's gamma is folded into W_o' = W_o diag(gamma_out) (scaled by a
 // power of two to use fp16's range) and beta into a bias; LayerNorm_in of the
 // gate is folded as in the projection: W_g zh = rstd (W_g' z - mu rowsum) + bias.
@@ -48,16 +51,20 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(kBoxFinishX.bytes() == X_BYTES, "x tile = one box");
 static_assert(2 * kBoxFinishZ.bytes() == Z_BYTES, "z tile = two boxes");
 static_assert(2 * kBoxFinishW.bytes() == WO_BYTES && 4 * kBoxFinishW.bytes() == WG_BYTES, "weight boxes");
+static_assert(EPI_WARPS * kBoxFinishOut.bytes() == XH_BYTES && kBoxFinishOut.d0 * 2 == 128,
+              "out staging: one 32-row box of 128-byte rows per epilogue warp fills the x-hat buffer");
 
 __device__ __forceinline__ float2 bf2f(uint32_t v) {
   return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
 }
 
 // Epilogue of one tile for one thread: pair row of the TMEM accumulator at `tmem_row`, output
-// channels [64*H, 64*H + 64). H is a template parameter so the constant-bank offsets are immediates.
+// channels [64*H, 64*H + 64), written as bf16 into row `r` of the 128-byte-swizzled staging box
+// `stg` (64 channels x 128 pairs, the K-major layout of the x-hat operand whose buffer it reuses).
+// H is a template parameter so the constant-bank offsets are immediates.
 template <int H>
 __device__ __forceinline__ void finish_pair(const FinishParams& p, uint32_t tmem_row, int buf, float2 zst,
-                                            __nv_bfloat16* dst, bool valid) {
+                                            uint8_t* stg, int r) {
   const float2 inv = make_float2(p.inv_scale_o, p.inv_scale_o);
   const float2 r2 = make_float2(zst.x, zst.x), n2 = make_float2(zst.y, zst.y);
 #pragma unroll
@@ -81,18 +88,17 @@ __device__ __forceinline__ void finish_pair(const FinishParams& p, uint32_t tmem
       const float2 v = __ffma2_rn(hy, make_float2(tanh_mufu(hg.x), tanh_mufu(hg.y)), hy);
       packed[e >> 1] = pack_bf16x2(v.x, v.y);
     }
-    if (valid) {
-      uint4* d4 = reinterpret_cast<uint4*>(dst + o0);
-      d4[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-      d4[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-    }
+    // 16-byte units 2cc and 2cc + 1 of this pair's 128-byte staging row
+    *reinterpret_cast<uint4*>(stg + sw128_offset(r, 2 * cc)) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    *reinterpret_cast<uint4*>(stg + sw128_offset(r, 2 * cc + 1)) =
+        make_uint4(packed[4], packed[5], packed[6], packed[7]);
   }
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
     k3_finish(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap zmap,
               const __grid_constant__ CUtensorMap womap, const __grid_constant__ CUtensorMap wgmap,
-              const __grid_constant__ FinishParams p) {
+              const __grid_constant__ CUtensorMap omap, const __grid_constant__ FinishParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* zs = smem;                        // 1024-aligned swizzled tiles first
   uint8_t* xh = zs + Z_BYTES;
@@ -124,7 +130,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(zfull, 1);
     mbar_init(zempty, 1);
     mbar_init(hfull, LN_WARPS);
-    mbar_init(hempty, 1);
+    mbar_init(hempty, EPI_WARPS);         // the epilogue's stores have read their staging rows
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], EPI_WARPS);
@@ -210,7 +216,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                 mma_f16(d + kC, make_sdesc_sw128(z0 + off, 16, 1024),
                         make_sdesc_sw128(g0 + 2 * 16384 + off, 16, 1024), id_g, 1u);
               }
-            mma_commit(hempty);
             mma_commit(zempty);
             mma_commit(&tfull[buf]);
             ph ^= 1u;
@@ -343,21 +348,29 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!warp_wait_bounded(&tfull[buf], use & 1u, p.w, abort_flag, 41)) break;
         tc_fence_after();
         const float2 zs2 = zst[sb * BM + r];
-        const int i = p.i0 + il;
-        const int jl = jt * BM + r;
-        const bool valid = jl < p.bj;
-        __nv_bfloat16* dst = p.out + ((size_t)i * p.N + (size_t)(p.j0 + jl)) * kC;
+        // the x-hat buffer becomes the staging box of out once this tile's MMA has read it (tfull)
+        uint8_t* stg = xh + hsel * (XH_BYTES / 2);
         if (hsel == 0)
-          finish_pair<0>(p, tmem_row, buf, zs2, dst, valid);
+          finish_pair<0>(p, tmem_row, buf, zs2, stg, r);
         else
-          finish_pair<1>(p, tmem_row, buf, zs2, dst, valid);
+          finish_pair<1>(p, tmem_row, buf, zs2, stg, r);
         tc_fence_before();
+        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&tempty[buf]);
           mbar_arrive(&sempty[sb]);
+          // rows 32q .. 32q+31 of the box: one TMA store (pairs past the block's edge are clipped by
+          // the map, whose extents are the block's)
+          if (jt * BM + q * 32 < p.bj) {
+            tma_store_3d(&omap, stg + q * 32 * 128, hsel * 64, jt * BM + q * 32, il);
+            bulk_commit();
+          }
+          bulk_wait_read<0>();
+          mbar_arrive(hempty);
         }
       }
+      if (lane == 0) bulk_wait_all();   // stores out before the CTA's shared memory goes away
     }
   }
 
@@ -376,7 +389,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 }  // namespace
 
 cudaError_t launch_finish_bf16(const CUtensorMap& xmap, const CUtensorMap& zmap, const CUtensorMap& womap,
-                               const CUtensorMap& wgmap, const FinishParams& p, int num_sms, cudaStream_t s) {
+                               const CUtensorMap& wgmap, const CUtensorMap& omap, const FinishParams& p, int num_sms,
+                               cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(k3_finish, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
@@ -385,7 +399,7 @@ cudaError_t launch_finish_bf16(const CUtensorMap& xmap, const CUtensorMap& zmap,
   }
   if (p.total_tiles <= 0) return cudaSuccess;
   const int grid = (int)(p.total_tiles < num_sms ? p.total_tiles : num_sms);
-  k3_finish<<<grid, THREADS, SMEM_BYTES, s>>>(xmap, zmap, womap, wgmap, p);
+  k3_finish<<<grid, THREADS, SMEM_BYTES, s>>>(xmap, zmap, womap, wgmap, omap, p);
   return cudaGetLastError();
 }
 

@@ -400,8 +400,16 @@ tm_status run_finish_bf16(tm_ctx* c, const float* x, int ldx, const void* z, int
     if (!encode(&zmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, z, dims, str, kBoxFinishZ, CU_TENSOR_MAP_SWIZZLE_128B))
       return fail(c, TM_ERR_CUDA, "tensor map (z, finish)");
   }
+  // out of this block: base at (i0, j0), extents (128, bj, bi), so that stores clip at the block's edges
+  CUtensorMap omap;
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)kC, (cuuint64_t)bj, (cuuint64_t)bi};
+    const cuuint64_t str[2] = {(cuuint64_t)kC * 2, (cuuint64_t)N * kC * 2};
+    const void* base = reinterpret_cast<const __nv_bfloat16*>(out) + ((size_t)i0 * N + (size_t)j0) * kC;
+    if (!encode(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, str, kBoxFinishOut, CU_TENSOR_MAP_SWIZZLE_128B))
+      return fail(c, TM_ERR_CUDA, "tensor map (out, finish)");
+  }
   FinishParams p;
-  p.out = reinterpret_cast<__nv_bfloat16*>(out);
   std::memcpy(p.cst, c->k3c_host, sizeof p.cst);
   p.inv_scale_o = c->inv_scale_o;
   p.N = N;
@@ -413,7 +421,7 @@ tm_status run_finish_bf16(tm_ctx* c, const float* x, int ldx, const void* z, int
   p.total_tiles = (long long)bi * p.tiles_j;
   p.w = watch(c, KID_FINISH, opt);
   cudaError_t e = timed(c, 2, (long long)bi * bj, s,
-                        [&] { return launch_finish_bf16(xmap, zmap, c->wo_map, c->wg_map, p, c->num_sms, s); });
+                        [&] { return launch_finish_bf16(xmap, zmap, c->wo_map, c->wg_map, omap, p, c->num_sms, s); });
   return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "finish launch");
 }
 

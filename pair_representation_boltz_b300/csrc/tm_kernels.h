@@ -42,7 +42,6 @@ struct ContractParams {
 
 // Output epilogue of one block: out = sigmoid(g) * (W_o LayerNorm(x)).
 struct FinishParams {
-  __nv_bfloat16* out;     // [N][N][128]
   float cst[3 * kC];      // rowsum of W_g' (hi+lo), bias W_g beta_in, bias W_o beta_out (constant bank)
   float inv_scale_o;      // W_o is stored scaled by a power of two; this undoes it
   int N;
@@ -57,12 +56,13 @@ cudaError_t launch_project_bf16(const CUtensorMap& zmap, const CUtensorMap& wmap
 cudaError_t launch_contract_bf16(bool incoming, const CUtensorMap& amap, const CUtensorMap& bmap,
                                  const CUtensorMap& xmap, const ContractParams& p, int num_sms, cudaStream_t s);
 cudaError_t launch_finish_bf16(const CUtensorMap& xmap, const CUtensorMap& zmap, const CUtensorMap& womap,
-                               const CUtensorMap& wgmap, const FinishParams& p, int num_sms, cudaStream_t s);
+                               const CUtensorMap& wgmap, const CUtensorMap& omap, const FinishParams& p, int num_sms,
+                               cudaStream_t s);
 
 // Tile sizes.
 constexpr int kProjTileJ = 128;     // pairs per projection tile
-constexpr int kContractBM = 128;    // output rows per contraction tile
-constexpr int kContractBN = 256;    // output columns per contraction tile
+constexpr int kContractBM = 256;    // output rows per contraction tile (a CTA pair, 128 rows each)
+constexpr int kContractBN = 256;    // output columns per contraction tile (128 B rows staged by each CTA)
 constexpr int kContractBK = 64;     // k per pipeline stage
 constexpr int kFinishTileJ = 128;   // pairs per finish tile
 
@@ -76,13 +76,14 @@ struct Box {
 constexpr Box kBoxProjZ{64, (uint32_t)kProjTileJ, 1, 2};              // z tile, one 64-channel half
 constexpr Box kBoxProjW{64, 128, 1, 2};                               // one K-half of a 128 x 128 weight
 constexpr Box kBoxProjOut{64, 1, 32, 2};                              // a or b store: 64 pairs x 32 channels
-constexpr Box kBoxContractOutA{(uint32_t)kContractBK, (uint32_t)kContractBM, 1, 2};
-constexpr Box kBoxContractOutB{(uint32_t)kContractBK, (uint32_t)kContractBN, 1, 2};
+constexpr Box kBoxContractOutA{(uint32_t)kContractBK, (uint32_t)kContractBM / 2, 1, 2};   // one CTA's A rows
+constexpr Box kBoxContractOutB{(uint32_t)kContractBK, (uint32_t)kContractBN / 2, 1, 2};   // one CTA's B rows
 constexpr Box kBoxContractIn{64, (uint32_t)kContractBK, 1, 2};        // incoming: 64-wide slab of i or j
 constexpr Box kBoxContractX{32, 32, 1, 4};                            // x store sub-tile
 constexpr Box kBoxFinishX{(uint32_t)kFinishTileJ, 1, (uint32_t)kC, 4};
 constexpr Box kBoxFinishZ{64, (uint32_t)kFinishTileJ, 1, 2};
 constexpr Box kBoxFinishW{64, (uint32_t)kC, 1, 2};                    // W_o (fp16) and W_g (bf16) halves
+constexpr Box kBoxFinishOut{64, 32, 1, 2};                            // out store: 32 pairs x 64 channels
 
 // ----------------------------------------------------------------- float32 CUDA-core path (any c <= 256)
 struct F32Weights {

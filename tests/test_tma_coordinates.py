@@ -10,7 +10,8 @@ import itertools
 
 import pytest
 
-BM, BN, BK = 128, 256, 64          # contraction tile
+BM, BN, BK = 256, 256, 64          # contraction tile of a CTA pair: each CTA stages 128 rows of A and of B
+HM, HN = BM // 2, BN // 2
 PROJ_J = 128                       # projection tile (pairs)
 FIN_J = 128                        # finish tile (pairs)
 
@@ -23,16 +24,17 @@ def contraction_boxes(N, i0, j0, bi, bj, incoming):
     kb_n = (N + BK - 1) // BK
     for ti in range(tiles_i):
         for tj in range(tiles_j):
-            ia, jb = i_base + ti * BM, j_base + tj * BN
-            for kb in range(kb_n):
-                if not incoming:
-                    yield ("a", kb * BK, 2)
-                    yield ("b", kb * BK, 2)
-                else:
-                    yield ("a", ia, 2)
-                    yield ("a", ia + 64, 2)
-                    for h in range(BN // 64):
-                        yield ("b", jb + 64 * h, 2)
+            for rank in (0, 1):
+                ia, jb = i_base + ti * BM + rank * HM, j_base + tj * BN + rank * HN
+                for kb in range(kb_n):
+                    if not incoming:
+                        yield ("a", kb * BK, 2)
+                        yield ("b", kb * BK, 2)
+                    else:
+                        for h in range(HM // 64):
+                            yield ("a", ia + 64 * h, 2)
+                        for h in range(HN // 64):
+                            yield ("b", jb + 64 * h, 2)
 
 
 def contraction_store_boxes(N, i0, j0, bi, bj):
@@ -43,11 +45,12 @@ def contraction_store_boxes(N, i0, j0, bi, bj):
     tiles_j = (bj + BN - 1) // BN
     for ti in range(tiles_i):
         for tj in range(tiles_j):
-            for q in range(4):
-                for ch in range(BN // 32):
-                    row0, col0 = ti * BM + 32 * q, tj * BN + 32 * ch
-                    if row0 < bi and col0 < bj:
-                        yield ("x-store", col0, 4, row0)
+            for rank in (0, 1):
+                for q in range(4):
+                    for ch in range(BN // 32):
+                        row0, col0 = ti * BM + rank * HM + 32 * q, tj * BN + 32 * ch
+                        if row0 < bi and col0 < bj:
+                            yield ("x-store", col0, 4, row0)
 
 
 def projection_boxes(N):
@@ -67,6 +70,11 @@ def projection_boxes(N):
 def finish_boxes(N, i0, j0, bi, bj):
     for jt in range((bj + FIN_J - 1) // FIN_J):
         yield ("x", jt * FIN_J, 4)
+        # out: one 32-pair x 64-channel store per epilogue warp, on a map based at the block origin
+        for q in range(4):
+            if jt * FIN_J + 32 * q < bj:
+                for h in (0, 1):
+                    yield ("out-store", 64 * h, 2)
     for kc in (0, 1):
         yield ("z", kc * 64, 2)
         yield ("w_o", kc * 64, 2)
