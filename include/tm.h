@@ -72,13 +72,25 @@ typedef struct {
   const float *w_o;                        /* [c_z][c_h]   */
 } tm_weights;
 
+/* Storage of the contraction's output x (c_h values per pair of the current
+ * output block) on its way to the output LayerNorm, bf16 path only:
+ *   TM_X_FP16  fp16, every value scaled by one power of two 2^e with
+ *              e = 14 - ceil(log2(N max_c(max|a_c| max|b_c|))) (clamped to
+ *              [-60, 60]); since |x_ij^c| <= N max|a_c| max|b_c|, no value can
+ *              overflow, and LayerNorm (scale-free but for its epsilon, which
+ *              is scaled alike) reads the scaled values as they are;
+ *   TM_X_FP32  float32.
+ * The float32 path always keeps x in float32. */
+typedef enum { TM_X_FP16 = 0, TM_X_FP32 = 1 } tm_x_storage;
+
 typedef struct {
   int block;              /* edge of the square output blocks of the streamed
-                             schedule; 0 = automatic (whole grid while its float32
-                             x fits the workspace limit, else about 2500)          */
+                             schedule; 0 = automatic (whole grid while its x
+                             fits the workspace limit, else about 2500)            */
   int timeout_ms;         /* limit of every device-side wait; 0 = 2000 ms           */
   size_t workspace_limit; /* bytes; 0 = env TM_WORKSPACE_LIMIT, else no limit      */
-  int reserved[8];        /* must be zero                                          */
+  int x_storage;          /* tm_x_storage; 0 = TM_X_FP16                            */
+  int reserved[7];        /* must be zero                                          */
 } tm_options;
 
 /* Create a context on the current CUDA device. Copies and converts the

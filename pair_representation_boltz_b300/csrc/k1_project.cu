@@ -261,6 +261,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       const float2 nlog2e = make_float2(-1.4426950408889634f, -1.4426950408889634f);
       const float2 one2 = make_float2(1.f, 1.f);
       if (lane == 0) tma_prefetch_desc(omap);
+      // running max |value| of this channel over the pairs this warp writes (bf16x2: both halves)
+      __nv_bfloat162 vmax = __floats2bfloat162_rn(0.f, 0.f);
       int local = 0;
       for (long long u = cta; u < p.total_tiles; u += nctas, ++local) {
         const int i = (int)(u / p.tiles_per_row);
@@ -320,6 +322,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 packed[e >> 1] = pack_bf16x2(((mword >> e) & 1u) ? v.x : 0.f, ((mword >> (e + 1)) & 1u) ? v.y : 0.f);
               }
             }
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              vmax = __hmax2(vmax, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&packed[k])));
             // 32 bytes of this channel's 128-byte staging row: 16-byte units 2hh, 2hh+1
 #pragma unroll
             for (int k = 0; k < 2; ++k)
@@ -342,6 +347,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       if (lane == 0) bulk_wait_all();   // stores out before the CTA's shared memory goes away
+      // per-channel maximum for the scale of the fp16 x (non-negative floats order like their bits)
+      if (p.amax) {
+        const float m = fmaxf(__low2float(vmax), __high2float(vmax));
+        atomicMax(p.amax + half * kC + c, __float_as_uint(m));
+      }
     }
   }
 

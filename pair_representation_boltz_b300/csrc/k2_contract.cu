@@ -4,15 +4,17 @@
 //   outgoing: x_ij = sum_k a_ik b_jk   (X_c = A_c B_c^T)
 //   incoming: x_ij = sum_k a_ki b_kj   (X_c = A_c^T B_c)
 //
-// a and b are channel-major bf16 [128][N][ld]; x is float32 [128][bi][ldx]
-// for one output block (i0, j0, bi, bj). This is the O(N^3 c) step that the
+// a and b are channel-major bf16 [128][N][ld]; x is [128][bi][ldx] for one
+// output block (i0, j0, bi, bj), float32 or fp16 scaled by one power of two
+// (x16_exponent: the bound N max|a_c| max|b_c| keeps every value in range). This is the O(N^3 c) step that the
 // 2D block tiling of the pair representation exists for ("2D tiling da pair
 // representation" section of "NVIDIA BioNeMo escala modelagem biomolecular com
 // context parallelism e quebra barreira de memória da GPU"); here the N x N
 // grid is tiled inside one GPU.
 //
 // Design: clusters of two CTAs (one per SM), persistent over (channel, i-tile,
-// j-tile) with 256 x 256 output tiles. The pair's tensor cores run one
+// j-tile) with 256 x 256 output tiles (the last tile column only as wide as the
+// columns it has left, rounded up to 16: a narrower MMA, not wasted work). The pair's tensor cores run one
 // M = 256, N = 256 MMA: each CTA stages its own 128 rows of A and its own 128
 // of the tile's 256 B rows, so that per multiply-add each SM reads half the B
 // bytes a single-CTA 128 x 256 tile would need, from L2 and from shared memory.
@@ -25,8 +27,8 @@
 //               tcgen05.mma.cta_group::2 (K = 16 per instruction, f32 accumulate).
 //   warps 2..5  (both CTAs) epilogue of the CTA's 128 rows: tcgen05.ld 32 columns
 //               at a time into a per-warp 128-byte-swizzled staging tile (two per
-//               warp), TMA store of each 32 x 32 float32 sub-tile; TMA clips the
-//               block edges. The accumulator goes back to the MMA issuer when the
+//               warp), TMA store of each 32 x 32 float32 (or 32 x 64 fp16) sub-tile;
+//               TMA clips the block edges. The accumulator goes back to the MMA issuer when the
 //               warps of both CTAs have arrived on the first CTA's barrier.
 //               (Blocks whose origin is not a multiple of 8 fall back to direct
 //               16-byte stores: a TMA box must not start below zero or off its
@@ -55,7 +57,7 @@ static_assert(TMEM_COLS == 512, "two 256-column accumulators fill TMEM");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(kBoxContractOutA.bytes() == A_BYTES && kBoxContractOutB.bytes() == B_BYTES, "outgoing boxes");
 static_assert(2 * kBoxContractIn.bytes() == A_BYTES && 2 * kBoxContractIn.bytes() == B_BYTES, "incoming boxes");
-static_assert(kBoxContractX.bytes() == 32 * 32 * 4, "x store box");
+static_assert(kBoxContractX.bytes() == STG_BYTES && kBoxContractX16.bytes() == STG_BYTES, "x store boxes");
 
 struct Tile {
   int c, ti, tj;
@@ -70,7 +72,8 @@ __device__ __forceinline__ Tile decode(long long t, const ContractParams& p) {
   return r;
 }
 
-template <bool INCOMING>
+// X16: x leaves as fp16 scaled by 2^e (e = x16_exponent of the projection's maxima), else float32.
+template <bool INCOMING, bool X16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     k2_contract(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap,
                 const __grid_constant__ CUtensorMap xmap, const ContractParams p) {
@@ -127,9 +130,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         uint32_t ph = 0;
         for (long long t = pair; t < p.total_tiles; t += npairs) {
           const Tile tl = decode(t, p);
-          // ia, jb are multiples of 8: the incoming boxes start there along their inner axis
+          // ia, jb are multiples of 8: the incoming boxes start there along their inner axis. The last
+          // tile column runs a narrower MMA (N = last_n), whose second half of B comes from the peer.
+          const int ntile = tl.tj == p.tiles_j - 1 ? p.last_n : BN;
           const int ia = p.i_base + tl.ti * BM + (int)rank * HM;
-          const int jb = p.j_base + tl.tj * BN + (int)rank * HN;
+          const int jb = p.j_base + tl.tj * BN + (int)rank * (ntile / 2);
           for (int kb = 0; kb < KB; ++kb) {
             if (!wait_bounded(&empty[s], ph ^ 1u, p.w, abort_flag, 1)) goto producer_done;
             uint8_t* sa = tiles + s * STAGE_BYTES;
@@ -159,7 +164,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer (first CTA)
       if (lane == 0 && rank == 0) {
-        constexpr uint32_t idesc = make_idesc(BM, BN, FMT_BF16, INCOMING, INCOMING);
+        constexpr uint32_t idesc_full = make_idesc(BM, BN, FMT_BF16, INCOMING, INCOMING);
+        const uint32_t idesc_last = make_idesc(BM, p.last_n, FMT_BF16, INCOMING, INCOMING);
         int s = 0;
         uint32_t ph = 0;
         int local = 0;
@@ -169,6 +175,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           if (!wait_bounded(&tempty[buf], (use & 1u) ^ 1u, p.w, abort_flag, 2)) break;
           tc_fence_after();
           const uint32_t d = tmem_base + (uint32_t)(buf * BN);
+          const uint32_t idesc = decode(t, p).tj == p.tiles_j - 1 ? idesc_last : idesc_full;
           bool ok = true;
           for (int kb = 0; kb < KB; ++kb) {
             if (!wait_bounded(&full[s], ph, p.w, abort_flag, 3)) {
@@ -210,6 +217,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       uint8_t* const my_stg = stg + (warp - 2) * 2 * STG_BYTES;
       int sb = 0;
       if (lane == 0 && p.tma_store) tma_prefetch_desc(&xmap);
+      // fp16 x: every value times 2^e, exact; |x| 2^e < 2^14 by the bound behind e
+      const float xs = X16 ? __int_as_float((127 + x16_exponent(p.amax, p.N)) << 23) : 1.f;
+      // output columns per staged box: 32 float32 or 64 fp16 values (128-byte rows either way)
+      constexpr int BOXW = X16 ? 64 : 32;
       int local = 0;
       for (long long t = pair; t < p.total_tiles; t += npairs, ++local) {
         const Tile tl = decode(t, p);
@@ -217,26 +228,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         const uint32_t use = (uint32_t)(local >> 1);
         if (!warp_wait_bounded(&tfull[buf], use & 1u, p.w, abort_flag, 5)) break;
         tc_fence_after();
+        const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
         if (p.tma_store) {
           // i_base == i0 and j_base == j0 here, so every coordinate is >= 0 and 32-aligned along j
           const int row0 = tl.ti * BM + (int)rank * HM + q * 32;
 #pragma unroll 1
-          for (int ch = 0; ch < BN / 32; ++ch) {
-            const int col0 = tl.tj * BN + ch * 32;
+          for (int ch = 0; ch < BN / BOXW; ++ch) {
+            const int col0 = tl.tj * BN + ch * BOXW;
             // Sub-tiles wholly outside the block are neither staged nor stored (warp-uniform). Every
             // staging write below is followed by exactly one committed store, which is what makes
             // "at most one group still reading" mean "the other buffer's store, not this one's".
             if (row0 >= p.bi || col0 >= p.bj) break;
-            uint32_t v[32];
-            tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + ch * 32), v);
+            uint32_t v[32], w[32];
+            tmem_ld32(trow + (uint32_t)(ch * BOXW), v);
+            if (X16) tmem_ld32(trow + (uint32_t)(ch * BOXW + 32), w);
             tmem_ld_wait();
             uint8_t* sbuf = my_stg + sb * STG_BYTES;
             if (lane == 0) bulk_wait_read<1>();   // the store that last read this buffer is done with it
             __syncwarp();
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-              *reinterpret_cast<uint4*>(sbuf + sw128_offset(lane, u)) =
-                  make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+            for (int u = 0; u < 8; ++u) {
+              uint4 val;
+              if (X16) {
+                const uint32_t* src = u < 4 ? v + 8 * u : w + 8 * (u - 4);
+                val = make_uint4(pack_f16x2(__uint_as_float(src[0]) * xs, __uint_as_float(src[1]) * xs),
+                                 pack_f16x2(__uint_as_float(src[2]) * xs, __uint_as_float(src[3]) * xs),
+                                 pack_f16x2(__uint_as_float(src[4]) * xs, __uint_as_float(src[5]) * xs),
+                                 pack_f16x2(__uint_as_float(src[6]) * xs, __uint_as_float(src[7]) * xs));
+              } else {
+                val = make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+              }
+              *reinterpret_cast<uint4*>(sbuf + sw128_offset(lane, u)) = val;
+            }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -250,19 +273,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           const int il = p.i_base + tl.ti * BM + (int)rank * HM + r - p.i0;
           const bool row_ok = il >= 0 && il < p.bi;
           const int jl0 = p.j_base + tl.tj * BN - p.j0;   // in (-8, bj)
-          float* xrow = p.x + (long long)tl.c * p.chan_stride + (long long)(row_ok ? il : 0) * p.ldx;
+          const long long row_off = (long long)tl.c * p.chan_stride + (long long)(row_ok ? il : 0) * p.ldx;
 #pragma unroll 1
           for (int ch = 0; ch < BN / 32; ++ch) {
             uint32_t v[32];
-            tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + ch * 32), v);
+            tmem_ld32(trow + (uint32_t)(ch * 32), v);
             tmem_ld_wait();
             const int jc = jl0 + ch * 32;
-            if (row_ok && jc < p.bj && jc + 32 > 0) {
+            if (!row_ok || jc >= p.bj || jc + 32 <= 0) continue;
+            if (X16) {
+              __half* xrow = reinterpret_cast<__half*>(p.x) + row_off;
+              if (jc >= 0 && jc + 32 <= p.bj && (jc & 7) == 0) {
+                // 16-byte aligned: x, ldx and chan_stride are multiples of 8 halves
+#pragma unroll
+                for (int e = 0; e < 32; e += 8)
+                  *reinterpret_cast<uint4*>(xrow + jc + e) = make_uint4(
+                      pack_f16x2(__uint_as_float(v[e]) * xs, __uint_as_float(v[e + 1]) * xs),
+                      pack_f16x2(__uint_as_float(v[e + 2]) * xs, __uint_as_float(v[e + 3]) * xs),
+                      pack_f16x2(__uint_as_float(v[e + 4]) * xs, __uint_as_float(v[e + 5]) * xs),
+                      pack_f16x2(__uint_as_float(v[e + 6]) * xs, __uint_as_float(v[e + 7]) * xs));
+              } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                  if (jc + e >= 0 && jc + e < p.bj) xrow[jc + e] = __float2half_rn(__uint_as_float(v[e]) * xs);
+              }
+            } else {
+              float* xrow = reinterpret_cast<float*>(p.x) + row_off;
               if (jc >= 0 && jc + 32 <= p.bj && (jc & 3) == 0) {
-                float* dst = xrow + jc;   // 16-byte aligned: x, ldx and chan_stride are multiples of 4
+                // 16-byte aligned: x, ldx and chan_stride are multiples of 4
 #pragma unroll
                 for (int e = 0; e < 32; e += 4)
-                  *reinterpret_cast<uint4*>(dst + e) = make_uint4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+                  *reinterpret_cast<uint4*>(xrow + jc + e) = make_uint4(v[e], v[e + 1], v[e + 2], v[e + 3]);
               } else {
 #pragma unroll
                 for (int e = 0; e < 32; ++e)
@@ -300,11 +341,12 @@ cudaError_t launch_contract_bf16(bool incoming, const CUtensorMap& amap, const C
                                  const CUtensorMap& xmap, const ContractParams& p, int num_sms, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k2_contract<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k2_contract<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
+    const void* fns[4] = {(const void*)k2_contract<false, false>, (const void*)k2_contract<true, false>,
+                          (const void*)k2_contract<false, true>, (const void*)k2_contract<true, true>};
+    for (const void* f : fns) {
+      cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+      if (e != cudaSuccess) return e;
+    }
     attr_set = true;
   }
   if (p.total_tiles <= 0) return cudaSuccess;
@@ -312,10 +354,17 @@ cudaError_t launch_contract_bf16(bool incoming, const CUtensorMap& amap, const C
   if (pairs > p.total_tiles) pairs = p.total_tiles;
   if (pairs < 1) pairs = 1;
   const int grid = (int)(2 * pairs);
-  if (incoming)
-    k2_contract<true><<<grid, THREADS, SMEM_BYTES, s>>>(amap, bmap, xmap, p);
-  else
-    k2_contract<false><<<grid, THREADS, SMEM_BYTES, s>>>(amap, bmap, xmap, p);
+  if (p.x_f16) {
+    if (incoming)
+      k2_contract<true, true><<<grid, THREADS, SMEM_BYTES, s>>>(amap, bmap, xmap, p);
+    else
+      k2_contract<false, true><<<grid, THREADS, SMEM_BYTES, s>>>(amap, bmap, xmap, p);
+  } else {
+    if (incoming)
+      k2_contract<true, false><<<grid, THREADS, SMEM_BYTES, s>>>(amap, bmap, xmap, p);
+    else
+      k2_contract<false, false><<<grid, THREADS, SMEM_BYTES, s>>>(amap, bmap, xmap, p);
+  }
   return cudaGetLastError();
 }
 

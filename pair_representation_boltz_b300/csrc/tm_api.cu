@@ -79,8 +79,8 @@ struct tm_ctx {
   float* k1c = nullptr;          // [2][512]
   __half* wo16 = nullptr;        // [128][128], scaled
   __nv_bfloat16* wg16 = nullptr; // [hi, lo][128][128]
-  float* k3c = nullptr;          // [3][128]
-  float k3c_host[3 * kC] = {};   // the same, passed to the finish kernel in its parameter block
+  float k3c_host[3 * kC] = {};   // finish-kernel constants, passed in its parameter block
+  unsigned* amax = nullptr;      // [2][128] per-channel max |a|, |b| of the last projection (fp16 x scale)
   float inv_scale_o = 1.f;
   CUtensorMap wk1_map, wo_map, wg_map;
   // status word (mapped host memory)
@@ -289,8 +289,11 @@ tm_status prepare_tensor_core_weights(tm_ctx* c, const tm_weights* w) {
   TM_UP(c->k1c, k1c)
   TM_UP(c->wo16, wo)
   TM_UP(c->wg16, wg)
-  TM_UP(c->k3c, k3c)
 #undef TM_UP
+  err = cudaMalloc(&c->amax, 2 * kC * sizeof(unsigned));
+  if (err != cudaSuccess) return cuda_fail(c, err, "cudaMalloc(channel maxima)");
+  err = cudaMemset(c->amax, 0, 2 * kC * sizeof(unsigned));
+  if (err != cudaSuccess) return cuda_fail(c, err, "cudaMemset(channel maxima)");
 
   {
     const cuuint64_t dims[2] = {(cuuint64_t)C, 1024};
@@ -311,7 +314,7 @@ tm_status prepare_tensor_core_weights(tm_ctx* c, const tm_weights* w) {
 }
 
 // ------------------------------------------------------------------ bf16 stage launchers (arguments checked)
-tm_status run_project_bf16(tm_ctx* c, const void* z, const float* mask, int N, __nv_bfloat16* a,
+tm_status run_project_bf16(tm_ctx* c, const void* z, const float* mask, int N, unsigned* amax, __nv_bfloat16* a,
                            __nv_bfloat16* b, int ld, cudaStream_t s, const tm_options* opt) {
   CUtensorMap zmap;
   const cuuint64_t dims[3] = {(cuuint64_t)kC, (cuuint64_t)N, (cuuint64_t)N};
@@ -331,6 +334,7 @@ tm_status run_project_bf16(tm_ctx* c, const void* z, const float* mask, int N, _
   p.b = b;
   p.mask = mask;
   p.consts = c->k1c;
+  p.amax = amax;
   p.N = N;
   p.ld = ld;
   p.tiles_per_row = (N + kProjTileJ - 1) / kProjTileJ;
@@ -341,8 +345,8 @@ tm_status run_project_bf16(tm_ctx* c, const void* z, const float* mask, int N, _
 }
 
 tm_status run_contract_bf16(tm_ctx* c, const __nv_bfloat16* a, const __nv_bfloat16* b, int N, int ld, bool incoming,
-                            int i0, int j0, int bi, int bj, float* x, int ldx, cudaStream_t s,
-                            const tm_options* opt) {
+                            int i0, int j0, int bi, int bj, void* x, int ldx, XFormat xf, const unsigned* amax,
+                            cudaStream_t s, const tm_options* opt) {
   CUtensorMap amap, bmap;
   const cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)N, (cuuint64_t)kC};
   const cuuint64_t str[2] = {(cuuint64_t)ld * 2, (cuuint64_t)N * ld * 2};
@@ -357,6 +361,8 @@ tm_status run_contract_bf16(tm_ctx* c, const __nv_bfloat16* a, const __nv_bfloat
   }
   ContractParams p;
   p.x = x;
+  p.x_f16 = xf == X_F16 ? 1 : 0;
+  p.amax = amax;
   p.ldx = ldx;
   p.chan_stride = (long long)bi * ldx;
   p.N = N;
@@ -369,15 +375,23 @@ tm_status run_contract_bf16(tm_ctx* c, const __nv_bfloat16* a, const __nv_bfloat
   p.tiles_i = (i0 + bi - p.i_base + kContractBM - 1) / kContractBM;
   p.tiles_j = (j0 + bj - p.j_base + kContractBN - 1) / kContractBN;
   p.total_tiles = (long long)kC * p.tiles_i * p.tiles_j;
+  {
+    const int rest = j0 + bj - p.j_base - (p.tiles_j - 1) * kContractBN;   // in [1, 256]
+    p.last_n = (rest + 15) / 16 * 16;
+  }
   // TMA stores need every box to start at a non-negative, 16-byte-aligned coordinate: block origins on the
   // 8-element grid give i_base == i0 and j_base == j0, so the tiles start at 0 in the block's own x map.
   p.tma_store = ((i0 & 7) == 0 && (j0 & 7) == 0) ? 1 : 0;
   CUtensorMap xmap;
   {
+    const size_t xe = xf == X_F16 ? 2 : 4;
     const cuuint64_t xd[3] = {(cuuint64_t)bj, (cuuint64_t)bi, (cuuint64_t)kC};
-    const cuuint64_t xs[2] = {(cuuint64_t)ldx * 4, (cuuint64_t)bi * ldx * 4};
-    if (!encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, x, xd, xs, kBoxContractX, CU_TENSOR_MAP_SWIZZLE_128B))
-      return fail(c, TM_ERR_CUDA, "tensor map (x, contraction store)");
+    const cuuint64_t xs[2] = {(cuuint64_t)ldx * xe, (cuuint64_t)bi * ldx * xe};
+    const bool ok = xf == X_F16 ? encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, x, xd, xs, kBoxContractX16,
+                                         CU_TENSOR_MAP_SWIZZLE_128B)
+                                : encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, x, xd, xs, kBoxContractX,
+                                         CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!ok) return fail(c, TM_ERR_CUDA, "tensor map (x, contraction store)");
   }
   p.w = watch(c, KID_CONTRACT, opt);
   cudaError_t e = timed(c, 1, (long long)kC * bi * bj, s,
@@ -385,14 +399,18 @@ tm_status run_contract_bf16(tm_ctx* c, const __nv_bfloat16* a, const __nv_bfloat
   return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "contraction launch");
 }
 
-tm_status run_finish_bf16(tm_ctx* c, const float* x, int ldx, const void* z, int N, int i0, int j0, int bi, int bj,
-                          void* out, cudaStream_t s, const tm_options* opt) {
+tm_status run_finish_bf16(tm_ctx* c, const void* x, int ldx, XFormat xf, const unsigned* amax, const void* z, int N,
+                          int i0, int j0, int bi, int bj, void* out, cudaStream_t s, const tm_options* opt) {
   CUtensorMap xmap, zmap;
   {
+    const size_t xe = xf == X_F16 ? 2 : 4;
     const cuuint64_t dims[3] = {(cuuint64_t)bj, (cuuint64_t)bi, (cuuint64_t)kC};
-    const cuuint64_t str[2] = {(cuuint64_t)ldx * 4, (cuuint64_t)bi * ldx * 4};
-    if (!encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, x, dims, str, kBoxFinishX, CU_TENSOR_MAP_SWIZZLE_NONE))
-      return fail(c, TM_ERR_CUDA, "tensor map (x)");
+    const cuuint64_t str[2] = {(cuuint64_t)ldx * xe, (cuuint64_t)bi * ldx * xe};
+    const bool ok = xf == X_F16 ? encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, x, dims, str, kBoxFinishX16,
+                                         CU_TENSOR_MAP_SWIZZLE_NONE)
+                                : encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, x, dims, str, kBoxFinishX,
+                                         CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (!ok) return fail(c, TM_ERR_CUDA, "tensor map (x)");
   }
   {
     const cuuint64_t dims[3] = {(cuuint64_t)kC, (cuuint64_t)N, (cuuint64_t)N};
@@ -410,6 +428,7 @@ tm_status run_finish_bf16(tm_ctx* c, const float* x, int ldx, const void* z, int
       return fail(c, TM_ERR_CUDA, "tensor map (out, finish)");
   }
   FinishParams p;
+  p.amax = amax;
   std::memcpy(p.cst, c->k3c_host, sizeof p.cst);
   p.inv_scale_o = c->inv_scale_o;
   p.N = N;
@@ -421,7 +440,7 @@ tm_status run_finish_bf16(tm_ctx* c, const float* x, int ldx, const void* z, int
   p.total_tiles = (long long)bi * p.tiles_j;
   p.w = watch(c, KID_FINISH, opt);
   cudaError_t e = timed(c, 2, (long long)bi * bj, s,
-                        [&] { return launch_finish_bf16(xmap, zmap, c->wo_map, c->wg_map, omap, p, c->num_sms, s); });
+                        [&] { return launch_finish_bf16(xf == X_F16, xmap, zmap, c->wo_map, c->wg_map, omap, p, c->num_sms, s); });
   return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "finish launch");
 }
 
@@ -438,9 +457,9 @@ tm_status check_common(tm_ctx* c, int N, tm_dtype dtype) {
   return check_device_status(c);
 }
 
-int choose_block(const tm_ctx* c, int N, const tm_options* opt, size_t ab_bytes) {
+int choose_block(const tm_ctx* c, int N, const tm_options* opt, size_t ab_bytes, size_t xe) {
   if (opt && opt->block > 0) return std::min(opt->block, N);
-  const size_t full_x = (size_t)c->c_h * N * align_up(N, 32) * 4;
+  const size_t full_x = (size_t)c->c_h * N * align_up(N, 128 / xe) * xe;
   size_t budget = (size_t)32 << 30;
   const size_t lim = limit_of(c, opt);
   if (lim) budget = lim > ab_bytes ? std::min(budget, lim - ab_bytes) : 0;
@@ -448,7 +467,7 @@ int choose_block(const tm_ctx* c, int N, const tm_options* opt, size_t ab_bytes)
   int nb = (N + 2499) / 2500;
   for (;; ++nb) {
     const int B = (int)align_up((size_t)((N + nb - 1) / nb), 8);   // block origins on the 8-element grid
-    if ((size_t)c->c_h * B * align_up(B, 32) * 4 <= budget || B <= 256) return B;
+    if ((size_t)c->c_h * B * align_up(B, 128 / xe) * xe <= budget || B <= 256) return B;
   }
 }
 
@@ -534,7 +553,7 @@ void tm_destroy(tm_ctx* c) {
   cudaDeviceSynchronize();
   if (c->ws) cudaFree(c->ws);
   if (c->io) cudaFree(c->io);
-  for (void* p : {(void*)c->w32, (void*)c->wk1, (void*)c->k1c, (void*)c->wo16, (void*)c->wg16, (void*)c->k3c})
+  for (void* p : {(void*)c->w32, (void*)c->wk1, (void*)c->k1c, (void*)c->wo16, (void*)c->wg16, (void*)c->amax})
     if (p) cudaFree(p);
   if (c->status_h) cudaFreeHost(c->status_h);
   for (auto& t : c->timed) {
@@ -556,7 +575,7 @@ tm_status tm_project(tm_ctx* c, const void* z, const float* mask, int N, tm_dtyp
   if (ld < N || (dtype == TM_BF16 && ld % 8)) return fail(c, TM_ERR_INVALID, "ld=%d must be >= N (and a multiple of 8 for bf16)", ld);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (dtype == TM_BF16)
-    return run_project_bf16(c, z, mask, N, reinterpret_cast<__nv_bfloat16*>(a), reinterpret_cast<__nv_bfloat16*>(b),
+    return run_project_bf16(c, z, mask, N, nullptr, reinterpret_cast<__nv_bfloat16*>(a), reinterpret_cast<__nv_bfloat16*>(b),
                             ld, s, nullptr);
   cudaError_t e = timed(c, 3, (long long)N * N, s, [&] {
     return launch_project_f32(reinterpret_cast<const float*>(z), mask, c->f32w, reinterpret_cast<float*>(a),
@@ -580,7 +599,7 @@ tm_status tm_contract(tm_ctx* c, const void* a, const void* b, int N, int ld, tm
   const bool inc = dir == TM_INCOMING;
   if (dtype == TM_BF16)
     return run_contract_bf16(c, reinterpret_cast<const __nv_bfloat16*>(a), reinterpret_cast<const __nv_bfloat16*>(b),
-                             N, ld, inc, i0, j0, bi, bj, x, ldx, s, nullptr);
+                             N, ld, inc, i0, j0, bi, bj, x, ldx, X_F32, nullptr, s, nullptr);
   cudaError_t e = timed(c, 3, (long long)c->c_h * bi * bj, s, [&] {
     return launch_contract_f32(inc, reinterpret_cast<const float*>(a), reinterpret_cast<const float*>(b), N, ld,
                                c->c_h, i0, j0, bi, bj, x, ldx, (long long)bi * ldx, s);
@@ -600,7 +619,7 @@ tm_status tm_finish(tm_ctx* c, const float* x, int ldx, const void* z, int N, tm
   const size_t zbytes = (size_t)N * N * c->c_z * (dtype == TM_BF16 ? 2 : 4);
   if (ranges_overlap(z, zbytes, out, zbytes)) return fail(c, TM_ERR_INVALID, "out overlaps z");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (dtype == TM_BF16) return run_finish_bf16(c, x, ldx, z, N, i0, j0, bi, bj, out, s, nullptr);
+  if (dtype == TM_BF16) return run_finish_bf16(c, x, ldx, X_F32, nullptr, z, N, i0, j0, bi, bj, out, s, nullptr);
   cudaError_t e = timed(c, 3, (long long)bi * bj, s, [&] {
     return launch_finish_f32(x, ldx, (long long)bi * ldx, reinterpret_cast<const float*>(z), c->f32w, N, i0, j0, bi,
                              bj, reinterpret_cast<float*>(out), s);
@@ -620,7 +639,12 @@ tm_status tm_forward_ex(tm_ctx* c, const void* z, const float* mask, int N, tm_d
     for (int r : opt->reserved)
       if (r) return fail(c, TM_ERR_INVALID, "tm_options.reserved must be zero");
     if (opt->block < 0 || opt->timeout_ms < 0) return fail(c, TM_ERR_INVALID, "negative option");
+    if (opt->x_storage != TM_X_FP16 && opt->x_storage != TM_X_FP32)
+      return fail(c, TM_ERR_INVALID, "unknown x_storage %d", opt->x_storage);
   }
+  // x between the contraction and the finish: scaled fp16 unless float32 is asked for (the float32
+  // CUDA-core path always keeps float32)
+  const XFormat xf = (dtype == TM_BF16 && !(opt && opt->x_storage == TM_X_FP32)) ? X_F16 : X_F32;
   const size_t esz = dtype == TM_BF16 ? 2 : 4;
   const size_t zbytes = (size_t)N * N * c->c_z * esz;
   if (ranges_overlap(z, zbytes, out, zbytes)) return fail(c, TM_ERR_INVALID, "out overlaps z");
@@ -631,9 +655,10 @@ tm_status tm_forward_ex(tm_ctx* c, const void* z, const float* mask, int N, tm_d
   // (with N = 3605 and 16-byte-aligned rows every 128-byte row segment straddled two lines).
   const int ld = dtype == TM_BF16 ? (int)align_up(N, 64) : N;
   const size_t ab_bytes = align_up((size_t)c->c_h * N * ld * esz, 256);
-  const int B = choose_block(c, N, opt, 2 * ab_bytes);
-  const int ldx = (int)align_up(B, 32);
-  const size_t x_bytes = align_up((size_t)c->c_h * B * ldx * 4, 256);
+  const size_t xe = xf == X_F16 ? 2 : 4;
+  const int B = choose_block(c, N, opt, 2 * ab_bytes, xe);
+  const int ldx = (int)align_up(B, 128 / xe);     // 128-byte rows
+  const size_t x_bytes = align_up((size_t)c->c_h * B * ldx * xe, 256);
   st = ensure_workspace(c, 2 * ab_bytes + x_bytes, s, opt);
   if (st != TM_OK) return st;
   uint8_t* base = reinterpret_cast<uint8_t*>(c->ws);
@@ -642,16 +667,23 @@ tm_status tm_forward_ex(tm_ctx* c, const void* z, const float* mask, int N, tm_d
   float* x = reinterpret_cast<float*>(base + 2 * ab_bytes);
 
   if (dtype == TM_BF16) {
-    st = run_project_bf16(c, z, mask, N, reinterpret_cast<__nv_bfloat16*>(a), reinterpret_cast<__nv_bfloat16*>(b),
+    unsigned* amax = nullptr;
+    if (xf == X_F16) {
+      // the projection leaves the per-channel maxima of a and b that fix the fp16 scale of x
+      amax = c->amax;
+      cudaError_t e = cudaMemsetAsync(amax, 0, 2 * kC * sizeof(unsigned), s);
+      if (e != cudaSuccess) return cuda_fail(c, e, "cudaMemsetAsync(channel maxima)");
+    }
+    st = run_project_bf16(c, z, mask, N, amax, reinterpret_cast<__nv_bfloat16*>(a), reinterpret_cast<__nv_bfloat16*>(b),
                           ld, s, opt);
     if (st != TM_OK) return st;
     for (int i0 = 0; i0 < N; i0 += B)
       for (int j0 = 0; j0 < N; j0 += B) {
         const int bi = std::min(B, N - i0), bj = std::min(B, N - j0);
         st = run_contract_bf16(c, reinterpret_cast<const __nv_bfloat16*>(a), reinterpret_cast<const __nv_bfloat16*>(b),
-                               N, ld, inc, i0, j0, bi, bj, x, ldx, s, opt);
+                               N, ld, inc, i0, j0, bi, bj, x, ldx, xf, amax, s, opt);
         if (st != TM_OK) return st;
-        st = run_finish_bf16(c, x, ldx, z, N, i0, j0, bi, bj, out, s, opt);
+        st = run_finish_bf16(c, x, ldx, xf, amax, z, N, i0, j0, bi, bj, out, s, opt);
         if (st != TM_OK) return st;
       }
     return TM_OK;
@@ -835,9 +867,10 @@ extern "C" tm_status tm_forward_noalloc(tm_ctx* c, const void* z, const float* m
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool timing = c->timing;  // event creation is an allocation too: no timing inside this call
   c->timing = false;
-  st = run_project_bf16(c, z, mask, N, a, b, ld, s, nullptr);
-  if (st == TM_OK) st = run_contract_bf16(c, a, b, N, ld, dir == TM_INCOMING, 0, 0, N, N, x, ldx, s, nullptr);
-  if (st == TM_OK) st = run_finish_bf16(c, x, ldx, z, N, 0, 0, N, N, out, s, nullptr);
+  st = run_project_bf16(c, z, mask, N, nullptr, a, b, ld, s, nullptr);
+  if (st == TM_OK)
+    st = run_contract_bf16(c, a, b, N, ld, dir == TM_INCOMING, 0, 0, N, N, x, ldx, X_F32, nullptr, s, nullptr);
+  if (st == TM_OK) st = run_finish_bf16(c, x, ldx, X_F32, nullptr, z, N, 0, 0, N, N, out, s, nullptr);
   c->timing = timing;
   return st;
 }

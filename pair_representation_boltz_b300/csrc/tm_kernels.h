@@ -5,6 +5,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "sm100.cuh"
 
@@ -19,15 +20,53 @@ struct ProjectParams {
   __nv_bfloat16* b;       // [128][N][ld]
   const float* mask;      // [N] or nullptr
   const float* consts;    // [2 halves][512]: rowsum[256] then bias[256] of the folded LayerNorm
+  unsigned* amax;         // [2 halves][128] max |a|, |b| per channel as float bits (atomicMax; zeroed
+                          // by the caller), or nullptr
   int N, ld;
   int tiles_per_row;      // ceil(N / 128)
   long long total_tiles;  // N * tiles_per_row
   Watch w;
 };
 
+// Storage of the contraction's output x between the contraction and the finish kernels: float32,
+// or fp16 scaled by one power of two 2^e (see x16_exponent).
+enum XFormat : int { X_F32 = 0, X_F16 = 1 };
+
+// Exponent e of the fp16 storage of x: |x_ij^c| = |sum_k a b| <= N max|a_c| max|b_c|, so with
+// e = 14 - ceil(log2(N max_c(max|a_c| max|b_c|))) every scaled value stays below 2^14 (fp16 tops out
+// near 2^16) -- the bound holds for any input, so the store never overflows. e is clamped to
+// [-60, 60]: 2^(2e) (the LayerNorm epsilon in scaled units) stays a normal float.
+// amax: [2][128] float bits of max |a_c| then max |b_c|, as the projection kernel leaves them.
+__host__ __device__ inline int x16_exponent_from_bound(float bound) {
+  if (!(bound > 0.f)) return 0;                                   // all-zero (or NaN) x: any scale
+  if (!(bound < 3.0e38f)) return -60;
+  uint32_t u;
+  memcpy(&u, &bound, 4);
+  const int be = (int)((u >> 23) & 255u);
+  int ce = be - 126;                                              // 2^ce >= bound for normal bound
+  if (be == 0) ce = -126;                                         // subnormal bound: 2^-126 >= it
+  int e = 14 - ce;
+  return e < -60 ? -60 : (e > 60 ? 60 : e);
+}
+
+// The same exponent from the device array, by one whole warp (every lane gets the result): the
+// per-channel products of the maxima, their maximum, times N.
+__device__ __forceinline__ int x16_exponent(const unsigned* amax, int N) {
+  const int lane = threadIdx.x & 31;
+  float m = 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int c = lane * 4 + k;
+    m = fmaxf(m, __uint_as_float(amax[c]) * __uint_as_float(amax[128 + c]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  return x16_exponent_from_bound((float)N * m);
+}
+
 // Contraction of one output block: x[c][i-i0][j-j0] over k in [0, N).
 struct ContractParams {
-  float* x;               // block buffer [128][bi][ldx]
+  void* x;                // block buffer [128][bi][ldx], float32 or fp16 (x_f16)
   long long ldx;          // row stride (elements)
   long long chan_stride;  // channel stride (elements)
   int N;                  // contraction length
@@ -36,12 +75,16 @@ struct ContractParams {
                           // every TMA box starts on a 16-byte boundary along its inner axis
   int tiles_i, tiles_j;   // tiles covering [i_base, i0 + bi) x [j_base, j0 + bj)
   long long total_tiles;  // 128 * tiles_i * tiles_j
+  int last_n;             // MMA N of the last tile column: the columns it still has to cover, rounded up to 16
+  int x_f16;              // 1: x is stored fp16, scaled by 2^e with e = x16_exponent(amax, N)
+  const unsigned* amax;   // the projection's per-channel maxima (x_f16 only)
   int tma_store;          // 1: x leaves through TMA stores (needs i0, j0 multiples of 8); 0: direct stores
   Watch w;
 };
 
 // Output epilogue of one block: out = sigmoid(g) * (W_o LayerNorm(x)).
 struct FinishParams {
+  const unsigned* amax;   // the projection's per-channel maxima (fp16 x only)
   float cst[3 * kC];      // rowsum of W_g' (hi+lo), bias W_g beta_in, bias W_o beta_out (constant bank)
   float inv_scale_o;      // W_o is stored scaled by a power of two; this undoes it
   int N;
@@ -55,9 +98,10 @@ cudaError_t launch_project_bf16(const CUtensorMap& zmap, const CUtensorMap& wmap
                                 const CUtensorMap& bmap, const ProjectParams& p, int num_sms, cudaStream_t s);
 cudaError_t launch_contract_bf16(bool incoming, const CUtensorMap& amap, const CUtensorMap& bmap,
                                  const CUtensorMap& xmap, const ContractParams& p, int num_sms, cudaStream_t s);
-cudaError_t launch_finish_bf16(const CUtensorMap& xmap, const CUtensorMap& zmap, const CUtensorMap& womap,
-                               const CUtensorMap& wgmap, const CUtensorMap& omap, const FinishParams& p, int num_sms,
-                               cudaStream_t s);
+// x16 selects the fp16 x tile (kBoxFinishX16, double-buffered) instead of the float32 one.
+cudaError_t launch_finish_bf16(bool x16, const CUtensorMap& xmap, const CUtensorMap& zmap,
+                               const CUtensorMap& womap, const CUtensorMap& wgmap, const CUtensorMap& omap,
+                               const FinishParams& p, int num_sms, cudaStream_t s);
 
 // Tile sizes.
 constexpr int kProjTileJ = 128;     // pairs per projection tile
@@ -79,8 +123,10 @@ constexpr Box kBoxProjOut{64, 1, 32, 2};                              // a or b 
 constexpr Box kBoxContractOutA{(uint32_t)kContractBK, (uint32_t)kContractBM / 2, 1, 2};   // one CTA's A rows
 constexpr Box kBoxContractOutB{(uint32_t)kContractBK, (uint32_t)kContractBN / 2, 1, 2};   // one CTA's B rows
 constexpr Box kBoxContractIn{64, (uint32_t)kContractBK, 1, 2};        // incoming: 64-wide slab of i or j
-constexpr Box kBoxContractX{32, 32, 1, 4};                            // x store sub-tile
+constexpr Box kBoxContractX{32, 32, 1, 4};                            // x store sub-tile (float32)
+constexpr Box kBoxContractX16{64, 32, 1, 2};                          // x store sub-tile (fp16)
 constexpr Box kBoxFinishX{(uint32_t)kFinishTileJ, 1, (uint32_t)kC, 4};
+constexpr Box kBoxFinishX16{(uint32_t)kFinishTileJ, 1, (uint32_t)kC, 2};
 constexpr Box kBoxFinishZ{64, (uint32_t)kFinishTileJ, 1, 2};
 constexpr Box kBoxFinishW{64, (uint32_t)kC, 1, 2};                    // W_o (fp16) and W_g (bf16) halves
 constexpr Box kBoxFinishOut{64, 32, 1, 2};                            // out store: 32 pairs x 64 channels

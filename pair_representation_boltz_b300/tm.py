@@ -37,9 +37,13 @@ class TmWeights(C.Structure):
     _fields_ = [(n, C.POINTER(C.c_float)) for n in WEIGHT_FIELDS]
 
 
+TM_X_FP16, TM_X_FP32 = 0, 1
+X_STORAGE = {"fp16": TM_X_FP16, "fp32": TM_X_FP32}
+
+
 class TmOptions(C.Structure):
     _fields_ = [("block", C.c_int), ("timeout_ms", C.c_int), ("workspace_limit", C.c_size_t),
-                ("reserved", C.c_int * 8)]
+                ("x_storage", C.c_int), ("reserved", C.c_int * 7)]
 
 
 class TmTiming(C.Structure):
@@ -169,9 +173,10 @@ def tm_destroy(ctx) -> None:
         load_library().tm_destroy(ctx)
 
 
-def tm_forward_ex(ctx, z, mask, direction, out, stream=None, block=0, timeout_ms=0, workspace_limit=0):
+def tm_forward_ex(ctx, z, mask, direction, out, stream=None, block=0, timeout_ms=0, workspace_limit=0,
+                  x_storage="fp16"):
     N = z.shape[0]
-    opt = TmOptions(block, timeout_ms, workspace_limit)
+    opt = TmOptions(block, timeout_ms, workspace_limit, X_STORAGE[x_storage])
     _check(ctx, load_library().tm_forward_ex(ctx, _ptr(z), _ptr(mask), N, _dtype_code(z), _direction(direction),
                                              _ptr(out), _stream(stream), C.byref(opt)))
     return out

@@ -1,4 +1,7 @@
 """Helpers shared by the GPU tests: moving seeded inputs to the device and the parity gates."""
+import json
+import os
+
 import numpy as np
 
 import oracle
@@ -46,6 +49,12 @@ def check_bf16(got, z, m, W, direction, rows=None, cols=None):
     ee = oracle.errors(got, ref_e, "bf16")
     metrics = {"excess_vs_storage_oracle": es["excess"], "rms_rel_vs_exact": ee["rms_rel"],
                "max_rel_vs_exact": ee["max_rel"], "max_rel_vs_storage_oracle": es["max_rel"]}
+    log = os.environ.get("TM_METRICS_LOG")
+    if log:     # one JSON line per check, for the record of the measured precision
+        with open(log, "a") as f:
+            f.write(json.dumps({"test": os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0],
+                                "direction": direction, "n_values": int(np.size(got)),
+                                **{k: float(v) for k, v in metrics.items()}}) + "\n")
     assert np.all(np.isfinite(got))
     assert es["excess"] <= BF16_TOL, metrics
     assert ee["rms_rel"] <= BF16_TOL, metrics

@@ -173,6 +173,37 @@ def test_forward_bf16(tm128, torch_cuda, direction, N, mask):
 
 
 @pytest.mark.parametrize("direction", DIRS)
+@pytest.mark.parametrize("N,mask", [(129, "scatter"), (300, "last10pct")])
+def test_forward_bf16_x_fp32(tm128, torch_cuda, direction, N, mask):
+    """The float32 storage of x (tm_options.x_storage) meets the same gates."""
+    mod, W = tm128
+    z = wl.make_z(N, 128, 51 + N, "bf16")
+    m = wl.make_mask(N, mask, 52)
+    out = mod(z_to_device(z), mask_to_device(m), direction, x_storage="fp32")
+    check_bf16(to_f64(out), z, m, W, direction)
+
+
+@pytest.mark.parametrize("gain", [300.0, 1e-3])
+def test_fp16_x_scale_follows_the_magnitude_of_a_and_b(torch_cuda, gain):
+    """Projections scaled up (x ~ 1e5 times larger) or down (x ~ 1e-6 times): the power-of-two scale of the
+    fp16 x follows, nothing overflows or flushes, and the bf16 gates hold in both directions."""
+    from pair_representation_boltz_b300 import tm
+    W = wl.make_weights(128, 128, 1)
+    for k in ("w_a", "w_b"):
+        W[k] = (W[k] * gain).astype(np.float32)
+    mod = tm.TriMul(128, 128, W)
+    N = 200
+    z = wl.make_z(N, 128, 61, "bf16")
+    m = wl.make_mask(N, "last10pct", 62)
+    for d in DIRS:
+        out = mod(z_to_device(z), mask_to_device(m), d)
+        o = to_f64(out)
+        assert np.isfinite(o).all()
+        check_bf16(o, z, m, W, d)
+    mod.close()
+
+
+@pytest.mark.parametrize("direction", DIRS)
 def test_crop768(tm128, torch_cuda, direction):
     """Boltz-2 training crop: N = 768, last 76 tokens masked, whole grid against the full oracle."""
     mod, W = tm128

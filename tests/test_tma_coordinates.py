@@ -24,8 +24,10 @@ def contraction_boxes(N, i0, j0, bi, bj, incoming):
     kb_n = (N + BK - 1) // BK
     for ti in range(tiles_i):
         for tj in range(tiles_j):
+            rest = j0 + bj - j_base - (tiles_j - 1) * BN
+            ntile = (rest + 15) // 16 * 16 if tj == tiles_j - 1 else BN
             for rank in (0, 1):
-                ia, jb = i_base + ti * BM + rank * HM, j_base + tj * BN + rank * HN
+                ia, jb = i_base + ti * BM + rank * HM, j_base + tj * BN + rank * (ntile // 2)
                 for kb in range(kb_n):
                     if not incoming:
                         yield ("a", kb * BK, 2)
