@@ -79,7 +79,7 @@ struct tm_ctx {
   float* k1c = nullptr;          // [2][512]
   __half* wo16 = nullptr;        // [128][128], scaled
   __nv_bfloat16* wg16 = nullptr; // [hi, lo][128][128]
-  float k3c_host[3 * kC] = {};   // finish-kernel constants, passed in its parameter block
+  float k3c_host[4 * kC] = {};   // finish-kernel constants, passed in its parameter block
   unsigned* amax = nullptr;      // [2][128] per-channel max |a|, |b| of the last projection (fp16 x scale)
   float inv_scale_o = 1.f;
   CUtensorMap wk1_map, wo_map, wg_map;
@@ -257,7 +257,7 @@ tm_status prepare_tensor_core_weights(tm_ctx* c, const tm_weights* w) {
   const double sc = std::ldexp(1.0, e);
   std::vector<__half> wo(C * C);
   std::vector<__nv_bfloat16> wg(2 * C * C);
-  std::vector<float> k3c(3 * C);
+  std::vector<float> k3c(4 * C);
   for (int o = 0; o < C; ++o) {
     double bo = 0, rs = 0, bg = 0;
     for (int k = 0; k < C; ++k) {
@@ -277,6 +277,13 @@ tm_status prepare_tensor_core_weights(tm_ctx* c, const tm_weights* w) {
     k3c[2 * C + o] = (float)(0.5 * bo);     // the output projection is read as y / 2 as well
   }
   c->inv_scale_o = (float)std::ldexp(1.0, -e - 1);
+  // row sums of the stored (scaled fp16) W_o', times the scale that undoes it: the fp16-x finish
+  // kernel applies LayerNorm_out after the MMA, y/2 = inv rstd (W_o' x - mu rowsum W_o') + bias/2
+  for (int o = 0; o < C; ++o) {
+    double rs = 0;
+    for (int k = 0; k < C; ++k) rs += (double)__half2float(wo[(size_t)o * C + k]);
+    k3c[3 * C + o] = (float)(rs * c->inv_scale_o);
+  }
   std::memcpy(c->k3c_host, k3c.data(), sizeof c->k3c_host);
 
   cudaError_t err;
@@ -407,7 +414,7 @@ tm_status run_finish_bf16(tm_ctx* c, const void* x, int ldx, XFormat xf, const u
     const cuuint64_t dims[3] = {(cuuint64_t)bj, (cuuint64_t)bi, (cuuint64_t)kC};
     const cuuint64_t str[2] = {(cuuint64_t)ldx * xe, (cuuint64_t)bi * ldx * xe};
     const bool ok = xf == X_F16 ? encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, x, dims, str, kBoxFinishX16,
-                                         CU_TENSOR_MAP_SWIZZLE_NONE)
+                                         CU_TENSOR_MAP_SWIZZLE_128B)
                                 : encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, x, dims, str, kBoxFinishX,
                                          CU_TENSOR_MAP_SWIZZLE_NONE);
     if (!ok) return fail(c, TM_ERR_CUDA, "tensor map (x)");

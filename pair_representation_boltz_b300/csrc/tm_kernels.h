@@ -85,7 +85,8 @@ struct ContractParams {
 // Output epilogue of one block: out = sigmoid(g) * (W_o LayerNorm(x)).
 struct FinishParams {
   const unsigned* amax;   // the projection's per-channel maxima (fp16 x only)
-  float cst[3 * kC];      // rowsum of W_g' (hi+lo), bias W_g beta_in, bias W_o beta_out (constant bank)
+  float cst[4 * kC];      // rowsum of W_g' (hi+lo), bias W_g beta_in, bias W_o beta_out, rowsum of W_o'
+                          // (times inv_scale_o); all halved for the tanh form (constant bank)
   float inv_scale_o;      // W_o is stored scaled by a power of two; this undoes it
   int N;
   int i0, j0, bi, bj;
@@ -126,7 +127,7 @@ constexpr Box kBoxContractIn{64, (uint32_t)kContractBK, 1, 2};        // incomin
 constexpr Box kBoxContractX{32, 32, 1, 4};                            // x store sub-tile (float32)
 constexpr Box kBoxContractX16{64, 32, 1, 2};                          // x store sub-tile (fp16)
 constexpr Box kBoxFinishX{(uint32_t)kFinishTileJ, 1, (uint32_t)kC, 4};
-constexpr Box kBoxFinishX16{(uint32_t)kFinishTileJ, 1, (uint32_t)kC, 2};
+constexpr Box kBoxFinishX16{64, 1, (uint32_t)kC, 2};                  // fp16 x: 64 pairs x 128 channels
 constexpr Box kBoxFinishZ{64, (uint32_t)kFinishTileJ, 1, 2};
 constexpr Box kBoxFinishW{64, (uint32_t)kC, 1, 2};                    // W_o (fp16) and W_g (bf16) halves
 constexpr Box kBoxFinishOut{64, 32, 1, 2};                            // out store: 32 pairs x 64 channels

@@ -203,6 +203,31 @@ def test_fp16_x_scale_follows_the_magnitude_of_a_and_b(torch_cuda, gain):
     mod.close()
 
 
+def test_forward_large_channel_mean_of_x(torch_cuda):
+    """x with a channel mean several times its spread (a, b share a positive offset in every channel):
+    the output LayerNorm folded into the finish GEMM (W_o' x - mu rowsum W_o') still meets the gates."""
+    from pair_representation_boltz_b300 import tm
+    W = wl.make_weights(128, 128, 1)
+    W["ln_in_beta"] = np.full(128, 3.0, np.float32)
+    for k in ("w_a", "w_b"):     # every row sums to 1/2: a and b get a positive offset in every channel
+        W[k] = (W[k] - W[k].mean(axis=1, keepdims=True) + 0.5 / 128).astype(np.float32)
+    for k in ("w_ga", "w_gb"):   # gates near 1/2 in every channel, so the offset is alike across channels
+        W[k] = (W[k] * 0.05).astype(np.float32)
+    mod = tm.TriMul(128, 128, W)
+    N = 200
+    z = wl.make_z(N, 128, 71, "bf16")
+    m = wl.make_mask(N, "full")
+    zd = z_to_device(z)
+    # the premise: the mean over channels of x dominates its spread
+    import oracle
+    _, _, _, x = oracle.intermediates(wl.as_f64(z), m, W, "outgoing", storage="bf16")
+    ratio = np.abs(x.mean(-1)).mean() / x.std(-1).mean()
+    assert ratio > 4, ratio
+    for d in DIRS:
+        check_bf16(to_f64(mod(zd, mask_to_device(m), d)), z, m, W, d)
+    mod.close()
+
+
 @pytest.mark.parametrize("direction", DIRS)
 def test_crop768(tm128, torch_cuda, direction):
     """Boltz-2 training crop: N = 768, last 76 tokens masked, whole grid against the full oracle."""

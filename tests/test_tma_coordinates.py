@@ -53,6 +53,10 @@ def contraction_store_boxes(N, i0, j0, bi, bj):
                         row0, col0 = ti * BM + rank * HM + 32 * q, tj * BN + 32 * ch
                         if row0 < bi and col0 < bj:
                             yield ("x-store", col0, 4, row0)
+                    for ch in range(BN // 64):        # fp16 x: 64-column boxes
+                        row0, col0 = ti * BM + rank * HM + 32 * q, tj * BN + 64 * ch
+                        if row0 < bi and col0 < bj:
+                            yield ("x16-store", col0, 2, row0)
 
 
 def projection_boxes(N):
@@ -72,6 +76,8 @@ def projection_boxes(N):
 def finish_boxes(N, i0, j0, bi, bj):
     for jt in range((bj + FIN_J - 1) // FIN_J):
         yield ("x", jt * FIN_J, 4)
+        yield ("x16", jt * FIN_J, 2)          # fp16 x: two 64-pair boxes per tile
+        yield ("x16", jt * FIN_J + 64, 2)
         # out: one 32-pair x 64-channel store per epilogue warp, on a map based at the block origin
         for q in range(4):
             if jt * FIN_J + 32 * q < bj:
