@@ -821,8 +821,8 @@ namespace {
 
 constexpr int kNoAllocMaxN = 128;
 constexpr size_t kNoAllocAB = (size_t)kC * kNoAllocMaxN * kNoAllocMaxN * 2;  // a or b, bf16: 4 MiB
-constexpr size_t kNoAllocX = (size_t)kC * kNoAllocMaxN * kNoAllocMaxN * 4;   // x, float32: 8 MiB
-constexpr size_t kNoAllocBytes = 2 * kNoAllocAB + kNoAllocX;                // 16 MiB in all
+constexpr size_t kNoAllocX = (size_t)kC * kNoAllocMaxN * kNoAllocMaxN * 2;   // x, fp16: 4 MiB
+constexpr size_t kNoAllocBytes = 2 * kNoAllocAB + kNoAllocX;                // 12 MiB in all
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
@@ -866,18 +866,26 @@ extern "C" tm_status tm_forward_noalloc(tm_ctx* c, const void* z, const float* m
   if (st != TM_OK) return st;
   // Every scratch byte the kernels read is written earlier in the same call (a and b
   // for every pair of the grid, x for every entry of the block); the row padding of
-  // a/b past N is never read, so nothing has to be cleared between calls.
-  const int ld = (int)align_up(N, 8), ldx = (int)align_up(N, 4);
+  // a/b past N is never read, so nothing has to be cleared between calls. x is kept
+  // as tm_forward keeps it by default (fp16, scaled by the maxima the projection
+  // records in the ctx's small buffer, cleared here by a memset, not an allocation),
+  // so that both give the same result.
+  const int ld = (int)align_up(N, 8), ldx = (int)align_up(N, 64);
   __nv_bfloat16* a = reinterpret_cast<__nv_bfloat16*>(scratch);
   __nv_bfloat16* b = reinterpret_cast<__nv_bfloat16*>(scratch + kNoAllocAB);
-  float* x = reinterpret_cast<float*>(scratch + 2 * kNoAllocAB);
+  void* x = scratch + 2 * kNoAllocAB;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool timing = c->timing;  // event creation is an allocation too: no timing inside this call
   c->timing = false;
-  st = run_project_bf16(c, z, mask, N, nullptr, a, b, ld, s, nullptr);
+  cudaError_t e = cudaMemsetAsync(c->amax, 0, 2 * kC * sizeof(unsigned), s);
+  if (e != cudaSuccess) {
+    c->timing = timing;
+    return cuda_fail(c, e, "cudaMemsetAsync(channel maxima)");
+  }
+  st = run_project_bf16(c, z, mask, N, c->amax, a, b, ld, s, nullptr);
   if (st == TM_OK)
-    st = run_contract_bf16(c, a, b, N, ld, dir == TM_INCOMING, 0, 0, N, N, x, ldx, X_F32, nullptr, s, nullptr);
-  if (st == TM_OK) st = run_finish_bf16(c, x, ldx, X_F32, nullptr, z, N, 0, 0, N, N, out, s, nullptr);
+    st = run_contract_bf16(c, a, b, N, ld, dir == TM_INCOMING, 0, 0, N, N, x, ldx, X_F16, c->amax, s, nullptr);
+  if (st == TM_OK) st = run_finish_bf16(c, x, ldx, X_F16, c->amax, z, N, 0, 0, N, N, out, s, nullptr);
   c->timing = timing;
   return st;
 }
