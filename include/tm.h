@@ -75,10 +75,12 @@ typedef struct {
 /* Storage of the contraction's output x (c_h values per pair of the current
  * output block) on its way to the output LayerNorm, bf16 path only:
  *   TM_X_FP16  fp16, every value scaled by one power of two 2^e with
- *              e = 14 - ceil(log2(N max_c(max|a_c| max|b_c|))) (clamped to
- *              [-60, 60]); since |x_ij^c| <= N max|a_c| max|b_c|, no value can
- *              overflow, and LayerNorm (scale-free but for its epsilon, which
- *              is scaled alike) reads the scaled values as they are;
+ *              e = 14 - ceil(log2(N max_c(A_c B_c))) (clamped to [-60, 60]),
+ *              A_c = sqrt(c_z) ||W_a[c] diag(gamma_in)|| + |(W_a beta_in)_c|
+ *              bounding |a_c| for any input (B_c likewise for b); since
+ *              |x_ij^c| <= N max|a_c| max|b_c|, no value can overflow, and
+ *              LayerNorm (scale-free but for its epsilon, which is scaled
+ *              alike) reads the scaled values as they are;
  *   TM_X_FP32  float32.
  * The float32 path always keeps x in float32. */
 typedef enum { TM_X_FP16 = 0, TM_X_FP32 = 1 } tm_x_storage;

@@ -258,11 +258,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       const float* cst = p.consts + half * 512;
       const float2 rsp = make_float2(cst[c], cst[c]), rsg = make_float2(cst[kC + c], cst[kC + c]);
       const float2 bp = make_float2(cst[256 + c], cst[256 + c]), bg = make_float2(cst[256 + kC + c], cst[256 + kC + c]);
-      const float2 nlog2e = make_float2(-1.4426950408889634f, -1.4426950408889634f);
       const float2 one2 = make_float2(1.f, 1.f);
       if (lane == 0) tma_prefetch_desc(omap);
-      // running max |value| of this channel over the pairs this warp writes (bf16x2: both halves)
-      __nv_bfloat162 vmax = __floats2bfloat162_rn(0.f, 0.f);
       int local = 0;
       for (long long u = cta; u < p.total_tiles; u += nctas, ++local) {
         const int i = (int)(u / p.tiles_per_row);
@@ -297,10 +294,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                                             __ffma2_rn(n, rsp, bp));
               const float2 gpre = __ffma2_rn(r, make_float2(__uint_as_float(gt[e]), __uint_as_float(gt[e + 1])),
                                              __ffma2_rn(n, rsg, bg));
-              // sigmoid of both gates with one reciprocal: with d = 1 + 2^(-g log2 e),
-              // sigmoid(g0) = d1 / (d0 d1) and sigmoid(g1) = d0 / (d0 d1). The exponent is capped at
-              // 63 so that d0 d1 < 2^127 (a gate below -43 then reads 2^-63 instead of ~0).
-              const float2 ga = __fmul2_rn(gpre, nlog2e);
+              // sigmoid of both gates with one reciprocal: the gate rows carry -log2(e), so gpre is
+              // -g log2 e and with d = 1 + 2^gpre, sigmoid(g0) = d1 / (d0 d1), sigmoid(g1) = d0 / (d0 d1).
+              // The exponent is capped at 63 so that d0 d1 < 2^127 (a gate below -43 then reads 2^-63
+              // instead of ~0).
+              const float2 ga = gpre;
               float e0, e1, rd;
               asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(fminf(ga.x, 63.f)));
               asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(fminf(ga.y, 63.f)));
@@ -322,9 +320,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                 packed[e >> 1] = pack_bf16x2(((mword >> e) & 1u) ? v.x : 0.f, ((mword >> (e + 1)) & 1u) ? v.y : 0.f);
               }
             }
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              vmax = __hmax2(vmax, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&packed[k])));
             // 32 bytes of this channel's 128-byte staging row: 16-byte units 2hh, 2hh+1
 #pragma unroll
             for (int k = 0; k < 2; ++k)
@@ -347,11 +342,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       if (lane == 0) bulk_wait_all();   // stores out before the CTA's shared memory goes away
-      // per-channel maximum for the scale of the fp16 x (non-negative floats order like their bits)
-      if (p.amax) {
-        const float m = fmaxf(__low2float(vmax), __high2float(vmax));
-        atomicMax(p.amax + half * kC + c, __float_as_uint(m));
-      }
     }
   }
 

@@ -6,7 +6,7 @@
 //
 // a and b are channel-major bf16 [128][N][ld]; x is [128][bi][ldx] for one
 // output block (i0, j0, bi, bj), float32 or fp16 scaled by one power of two
-// (x16_exponent: the bound N max|a_c| max|b_c| keeps every value in range). This is the O(N^3 c) step that the
+// chosen on the host so that no value can leave fp16's range. This is the O(N^3 c) step that the
 // 2D block tiling of the pair representation exists for ("2D tiling da pair
 // representation" section of "NVIDIA BioNeMo escala modelagem biomolecular com
 // context parallelism e quebra barreira de memória da GPU"); here the N x N
@@ -72,7 +72,7 @@ __device__ __forceinline__ Tile decode(long long t, const ContractParams& p) {
   return r;
 }
 
-// X16: x leaves as fp16 scaled by 2^e (e = x16_exponent of the projection's maxima), else float32.
+// X16: x leaves as fp16 scaled by 2^x_exp, else float32.
 template <bool INCOMING, bool X16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     k2_contract(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap,
@@ -217,8 +217,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       uint8_t* const my_stg = stg + (warp - 2) * 2 * STG_BYTES;
       int sb = 0;
       if (lane == 0 && p.tma_store) tma_prefetch_desc(&xmap);
-      // fp16 x: every value times 2^e, exact; |x| 2^e < 2^14 by the bound behind e
-      const float xs = X16 ? __int_as_float((127 + x16_exponent(p.amax, p.N)) << 23) : 1.f;
+      // fp16 x: every value times 2^x_exp, exact; |x| 2^x_exp <= 2^14 by the bound behind x_exp
+      const float xs = X16 ? __int_as_float((127 + p.x_exp) << 23) : 1.f;
       // output columns per staged box: 32 float32 or 64 fp16 values (128-byte rows either way)
       constexpr int BOXW = X16 ? 64 : 32;
       int local = 0;

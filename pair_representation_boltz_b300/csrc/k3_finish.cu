@@ -17,7 +17,7 @@
 // already stored at the precision the operand needs.
 //
 // Two kernels, one per storage of x:
-//   k3_finish_x16  x fp16 scaled by 2^e (x16_exponent): the x tile is the MMA's
+//   k3_finish_x16  x fp16 scaled by 2^x_exp: the x tile is the MMA's
 //                  A operand directly (M-major, 128-byte swizzle), two tiles in
 //                  flight; LayerNorm is scale-free apart from its epsilon,
 //                  which is scaled to match.
@@ -371,8 +371,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int xoff = (p0 >> 6) * (SLOT / 2) + ((p0 & 7) << 1);
       const uint32_t xunit = (uint32_t)((p0 & 63) >> 3);
       // LayerNorm epsilon in the units x16 = x 2^e is stored in
-      const int e = x16_exponent(p.amax, p.N);
-      const float x_eps = 1e-5f * __int_as_float((127 + 2 * e) << 23);
+      const float x_eps = 1e-5f * __int_as_float((127 + 2 * p.x_exp) << 23);
       uint32_t ph = 0;
       int local = 0;
       for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++local) {

@@ -80,7 +80,7 @@ struct tm_ctx {
   __half* wo16 = nullptr;        // [128][128], scaled
   __nv_bfloat16* wg16 = nullptr; // [hi, lo][128][128]
   float k3c_host[4 * kC] = {};   // finish-kernel constants, passed in its parameter block
-  unsigned* amax = nullptr;      // [2][128] per-channel max |a|, |b| of the last projection (fp16 x scale)
+  double ab_bound = 0;           // max_c of the bounds on |a_c| and |b_c| multiplied (fp16 x scale)
   float inv_scale_o = 1.f;
   CUtensorMap wk1_map, wo_map, wg_map;
   // status word (mapped host memory)
@@ -228,25 +228,36 @@ tm_status prepare_tensor_core_weights(tm_ctx* c, const tm_weights* w) {
   const int C = kC;
   std::vector<__nv_bfloat16> k1(2 * 2 * 256 * C);
   std::vector<float> k1c(2 * 512);
+  // Gate rows carry a factor -log2(e): the projection kernel takes sigmoid(g) = 1 / (1 + 2^(-g log2 e))
+  // straight from its accumulator. Bound on |a_c| (and |b_c|) for the fp16 storage of x: with
+  // W' = W diag(gamma_in), |W zh| = |rstd W'(z - mu) + W beta| <= sqrt(c_z) ||W'_c|| + |(W beta)_c|, since
+  // ||z - mu|| rstd <= sqrt(c_z); the gate and the mask only shrink it.
+  const double kNegLog2e = -1.4426950408889634;
+  double abound[2][kC];
   for (int h = 0; h < 2; ++h) {
     const float* wp = h == 0 ? w->w_a : w->w_b;
     const float* wgt = h == 0 ? w->w_ga : w->w_gb;
     for (int n = 0; n < 256; ++n) {
       const float* src = n < C ? wp + (size_t)n * C : wgt + (size_t)(n - C) * C;
-      double rs = 0, bias = 0;
+      const double f = n < C ? 1.0 : kNegLog2e;
+      double rs = 0, bias = 0, norm2 = 0;
       for (int k = 0; k < C; ++k) {
-        const double v = (double)src[k] * (double)w->ln_in_gamma[k];
+        const double v = f * (double)src[k] * (double)w->ln_in_gamma[k];
+        norm2 += v * v;
         __nv_bfloat16 hi, lo;
         split_bf16(v, &hi, &lo);
         k1[((size_t)(h * 2 + 0) * 256 + n) * C + k] = hi;
         k1[((size_t)(h * 2 + 1) * 256 + n) * C + k] = lo;
         rs += (double)__bfloat162float(hi) + (double)__bfloat162float(lo);
-        bias += (double)src[k] * (double)w->ln_in_beta[k];
+        bias += f * (double)src[k] * (double)w->ln_in_beta[k];
       }
       k1c[h * 512 + n] = (float)rs;
       k1c[h * 512 + 256 + n] = (float)bias;
+      if (n < C) abound[h][n] = std::sqrt((double)C * norm2) + std::fabs(bias);
     }
   }
+  c->ab_bound = 0;
+  for (int n = 0; n < C; ++n) c->ab_bound = std::max(c->ab_bound, abound[0][n] * abound[1][n]);
   // W_o' = W_o diag(gamma_out), scaled by 2^e into fp16's top binades
   double maxabs = 0;
   for (int o = 0; o < C; ++o)
@@ -297,10 +308,6 @@ tm_status prepare_tensor_core_weights(tm_ctx* c, const tm_weights* w) {
   TM_UP(c->wo16, wo)
   TM_UP(c->wg16, wg)
 #undef TM_UP
-  err = cudaMalloc(&c->amax, 2 * kC * sizeof(unsigned));
-  if (err != cudaSuccess) return cuda_fail(c, err, "cudaMalloc(channel maxima)");
-  err = cudaMemset(c->amax, 0, 2 * kC * sizeof(unsigned));
-  if (err != cudaSuccess) return cuda_fail(c, err, "cudaMemset(channel maxima)");
 
   {
     const cuuint64_t dims[2] = {(cuuint64_t)C, 1024};
@@ -321,7 +328,7 @@ tm_status prepare_tensor_core_weights(tm_ctx* c, const tm_weights* w) {
 }
 
 // ------------------------------------------------------------------ bf16 stage launchers (arguments checked)
-tm_status run_project_bf16(tm_ctx* c, const void* z, const float* mask, int N, unsigned* amax, __nv_bfloat16* a,
+tm_status run_project_bf16(tm_ctx* c, const void* z, const float* mask, int N, __nv_bfloat16* a,
                            __nv_bfloat16* b, int ld, cudaStream_t s, const tm_options* opt) {
   CUtensorMap zmap;
   const cuuint64_t dims[3] = {(cuuint64_t)kC, (cuuint64_t)N, (cuuint64_t)N};
@@ -341,7 +348,6 @@ tm_status run_project_bf16(tm_ctx* c, const void* z, const float* mask, int N, u
   p.b = b;
   p.mask = mask;
   p.consts = c->k1c;
-  p.amax = amax;
   p.N = N;
   p.ld = ld;
   p.tiles_per_row = (N + kProjTileJ - 1) / kProjTileJ;
@@ -352,7 +358,7 @@ tm_status run_project_bf16(tm_ctx* c, const void* z, const float* mask, int N, u
 }
 
 tm_status run_contract_bf16(tm_ctx* c, const __nv_bfloat16* a, const __nv_bfloat16* b, int N, int ld, bool incoming,
-                            int i0, int j0, int bi, int bj, void* x, int ldx, XFormat xf, const unsigned* amax,
+                            int i0, int j0, int bi, int bj, void* x, int ldx, XFormat xf, int x_exp,
                             cudaStream_t s, const tm_options* opt) {
   CUtensorMap amap, bmap;
   const cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)N, (cuuint64_t)kC};
@@ -369,7 +375,7 @@ tm_status run_contract_bf16(tm_ctx* c, const __nv_bfloat16* a, const __nv_bfloat
   ContractParams p;
   p.x = x;
   p.x_f16 = xf == X_F16 ? 1 : 0;
-  p.amax = amax;
+  p.x_exp = x_exp;
   p.ldx = ldx;
   p.chan_stride = (long long)bi * ldx;
   p.N = N;
@@ -406,7 +412,7 @@ tm_status run_contract_bf16(tm_ctx* c, const __nv_bfloat16* a, const __nv_bfloat
   return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "contraction launch");
 }
 
-tm_status run_finish_bf16(tm_ctx* c, const void* x, int ldx, XFormat xf, const unsigned* amax, const void* z, int N,
+tm_status run_finish_bf16(tm_ctx* c, const void* x, int ldx, XFormat xf, int x_exp, const void* z, int N,
                           int i0, int j0, int bi, int bj, void* out, cudaStream_t s, const tm_options* opt) {
   CUtensorMap xmap, zmap;
   {
@@ -435,7 +441,7 @@ tm_status run_finish_bf16(tm_ctx* c, const void* x, int ldx, XFormat xf, const u
       return fail(c, TM_ERR_CUDA, "tensor map (out, finish)");
   }
   FinishParams p;
-  p.amax = amax;
+  p.x_exp = x_exp;
   std::memcpy(p.cst, c->k3c_host, sizeof p.cst);
   p.inv_scale_o = c->inv_scale_o;
   p.N = N;
@@ -449,6 +455,18 @@ tm_status run_finish_bf16(tm_ctx* c, const void* x, int ldx, XFormat xf, const u
   cudaError_t e = timed(c, 2, (long long)bi * bj, s,
                         [&] { return launch_finish_bf16(xf == X_F16, xmap, zmap, c->wo_map, c->wg_map, omap, p, c->num_sms, s); });
   return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "finish launch");
+}
+
+// Exponent e of the fp16 storage of x. Every x_ij^c = sum_k a b is bounded by N max|a_c| max|b_c|
+// <= N ab_bound (the bound from the weights alone, prepare_tensor_core_weights), so with
+// e = 14 - ceil(log2(N ab_bound)) every stored value stays below 2^14, four times inside fp16's range:
+// the store cannot overflow for any input. e is clamped to [-60, 60] so that 2^(2e) (the LayerNorm
+// epsilon in stored units) stays a normal float.
+int x16_exponent(const tm_ctx* c, int N) {
+  const double bound = (double)N * c->ab_bound;
+  if (!(bound > 0)) return 0;
+  const int e = 14 - (int)std::ceil(std::log2(bound));
+  return std::min(60, std::max(-60, e));
 }
 
 tm_status check_common(tm_ctx* c, int N, tm_dtype dtype) {
@@ -560,7 +578,7 @@ void tm_destroy(tm_ctx* c) {
   cudaDeviceSynchronize();
   if (c->ws) cudaFree(c->ws);
   if (c->io) cudaFree(c->io);
-  for (void* p : {(void*)c->w32, (void*)c->wk1, (void*)c->k1c, (void*)c->wo16, (void*)c->wg16, (void*)c->amax})
+  for (void* p : {(void*)c->w32, (void*)c->wk1, (void*)c->k1c, (void*)c->wo16, (void*)c->wg16})
     if (p) cudaFree(p);
   if (c->status_h) cudaFreeHost(c->status_h);
   for (auto& t : c->timed) {
@@ -582,7 +600,7 @@ tm_status tm_project(tm_ctx* c, const void* z, const float* mask, int N, tm_dtyp
   if (ld < N || (dtype == TM_BF16 && ld % 8)) return fail(c, TM_ERR_INVALID, "ld=%d must be >= N (and a multiple of 8 for bf16)", ld);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (dtype == TM_BF16)
-    return run_project_bf16(c, z, mask, N, nullptr, reinterpret_cast<__nv_bfloat16*>(a), reinterpret_cast<__nv_bfloat16*>(b),
+    return run_project_bf16(c, z, mask, N, reinterpret_cast<__nv_bfloat16*>(a), reinterpret_cast<__nv_bfloat16*>(b),
                             ld, s, nullptr);
   cudaError_t e = timed(c, 3, (long long)N * N, s, [&] {
     return launch_project_f32(reinterpret_cast<const float*>(z), mask, c->f32w, reinterpret_cast<float*>(a),
@@ -606,7 +624,7 @@ tm_status tm_contract(tm_ctx* c, const void* a, const void* b, int N, int ld, tm
   const bool inc = dir == TM_INCOMING;
   if (dtype == TM_BF16)
     return run_contract_bf16(c, reinterpret_cast<const __nv_bfloat16*>(a), reinterpret_cast<const __nv_bfloat16*>(b),
-                             N, ld, inc, i0, j0, bi, bj, x, ldx, X_F32, nullptr, s, nullptr);
+                             N, ld, inc, i0, j0, bi, bj, x, ldx, X_F32, 0, s, nullptr);
   cudaError_t e = timed(c, 3, (long long)c->c_h * bi * bj, s, [&] {
     return launch_contract_f32(inc, reinterpret_cast<const float*>(a), reinterpret_cast<const float*>(b), N, ld,
                                c->c_h, i0, j0, bi, bj, x, ldx, (long long)bi * ldx, s);
@@ -626,7 +644,7 @@ tm_status tm_finish(tm_ctx* c, const float* x, int ldx, const void* z, int N, tm
   const size_t zbytes = (size_t)N * N * c->c_z * (dtype == TM_BF16 ? 2 : 4);
   if (ranges_overlap(z, zbytes, out, zbytes)) return fail(c, TM_ERR_INVALID, "out overlaps z");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (dtype == TM_BF16) return run_finish_bf16(c, x, ldx, X_F32, nullptr, z, N, i0, j0, bi, bj, out, s, nullptr);
+  if (dtype == TM_BF16) return run_finish_bf16(c, x, ldx, X_F32, 0, z, N, i0, j0, bi, bj, out, s, nullptr);
   cudaError_t e = timed(c, 3, (long long)bi * bj, s, [&] {
     return launch_finish_f32(x, ldx, (long long)bi * ldx, reinterpret_cast<const float*>(z), c->f32w, N, i0, j0, bi,
                              bj, reinterpret_cast<float*>(out), s);
@@ -674,23 +692,17 @@ tm_status tm_forward_ex(tm_ctx* c, const void* z, const float* mask, int N, tm_d
   float* x = reinterpret_cast<float*>(base + 2 * ab_bytes);
 
   if (dtype == TM_BF16) {
-    unsigned* amax = nullptr;
-    if (xf == X_F16) {
-      // the projection leaves the per-channel maxima of a and b that fix the fp16 scale of x
-      amax = c->amax;
-      cudaError_t e = cudaMemsetAsync(amax, 0, 2 * kC * sizeof(unsigned), s);
-      if (e != cudaSuccess) return cuda_fail(c, e, "cudaMemsetAsync(channel maxima)");
-    }
-    st = run_project_bf16(c, z, mask, N, amax, reinterpret_cast<__nv_bfloat16*>(a), reinterpret_cast<__nv_bfloat16*>(b),
+    const int x_exp = x16_exponent(c, N);
+    st = run_project_bf16(c, z, mask, N, reinterpret_cast<__nv_bfloat16*>(a), reinterpret_cast<__nv_bfloat16*>(b),
                           ld, s, opt);
     if (st != TM_OK) return st;
     for (int i0 = 0; i0 < N; i0 += B)
       for (int j0 = 0; j0 < N; j0 += B) {
         const int bi = std::min(B, N - i0), bj = std::min(B, N - j0);
         st = run_contract_bf16(c, reinterpret_cast<const __nv_bfloat16*>(a), reinterpret_cast<const __nv_bfloat16*>(b),
-                               N, ld, inc, i0, j0, bi, bj, x, ldx, xf, amax, s, opt);
+                               N, ld, inc, i0, j0, bi, bj, x, ldx, xf, x_exp, s, opt);
         if (st != TM_OK) return st;
-        st = run_finish_bf16(c, x, ldx, xf, amax, z, N, i0, j0, bi, bj, out, s, opt);
+        st = run_finish_bf16(c, x, ldx, xf, x_exp, z, N, i0, j0, bi, bj, out, s, opt);
         if (st != TM_OK) return st;
       }
     return TM_OK;
@@ -867,9 +879,8 @@ extern "C" tm_status tm_forward_noalloc(tm_ctx* c, const void* z, const float* m
   // Every scratch byte the kernels read is written earlier in the same call (a and b
   // for every pair of the grid, x for every entry of the block); the row padding of
   // a/b past N is never read, so nothing has to be cleared between calls. x is kept
-  // as tm_forward keeps it by default (fp16, scaled by the maxima the projection
-  // records in the ctx's small buffer, cleared here by a memset, not an allocation),
-  // so that both give the same result.
+  // as tm_forward keeps it by default (fp16, scaled by the same power of two), so
+  // that both give the same result.
   const int ld = (int)align_up(N, 8), ldx = (int)align_up(N, 64);
   __nv_bfloat16* a = reinterpret_cast<__nv_bfloat16*>(scratch);
   __nv_bfloat16* b = reinterpret_cast<__nv_bfloat16*>(scratch + kNoAllocAB);
@@ -877,15 +888,11 @@ extern "C" tm_status tm_forward_noalloc(tm_ctx* c, const void* z, const float* m
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool timing = c->timing;  // event creation is an allocation too: no timing inside this call
   c->timing = false;
-  cudaError_t e = cudaMemsetAsync(c->amax, 0, 2 * kC * sizeof(unsigned), s);
-  if (e != cudaSuccess) {
-    c->timing = timing;
-    return cuda_fail(c, e, "cudaMemsetAsync(channel maxima)");
-  }
-  st = run_project_bf16(c, z, mask, N, c->amax, a, b, ld, s, nullptr);
+  const int x_exp = x16_exponent(c, N);
+  st = run_project_bf16(c, z, mask, N, a, b, ld, s, nullptr);
   if (st == TM_OK)
-    st = run_contract_bf16(c, a, b, N, ld, dir == TM_INCOMING, 0, 0, N, N, x, ldx, X_F16, c->amax, s, nullptr);
-  if (st == TM_OK) st = run_finish_bf16(c, x, ldx, X_F16, c->amax, z, N, 0, 0, N, N, out, s, nullptr);
+    st = run_contract_bf16(c, a, b, N, ld, dir == TM_INCOMING, 0, 0, N, N, x, ldx, X_F16, x_exp, s, nullptr);
+  if (st == TM_OK) st = run_finish_bf16(c, x, ldx, X_F16, x_exp, z, N, 0, 0, N, N, out, s, nullptr);
   c->timing = timing;
   return st;
 }

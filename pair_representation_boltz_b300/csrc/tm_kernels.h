@@ -5,7 +5,6 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
-#include <string.h>
 
 #include "sm100.cuh"
 
@@ -20,8 +19,6 @@ struct ProjectParams {
   __nv_bfloat16* b;       // [128][N][ld]
   const float* mask;      // [N] or nullptr
   const float* consts;    // [2 halves][512]: rowsum[256] then bias[256] of the folded LayerNorm
-  unsigned* amax;         // [2 halves][128] max |a|, |b| per channel as float bits (atomicMax; zeroed
-                          // by the caller), or nullptr
   int N, ld;
   int tiles_per_row;      // ceil(N / 128)
   long long total_tiles;  // N * tiles_per_row
@@ -29,40 +26,11 @@ struct ProjectParams {
 };
 
 // Storage of the contraction's output x between the contraction and the finish kernels: float32,
-// or fp16 scaled by one power of two 2^e (see x16_exponent).
+// or fp16 scaled by one power of two 2^e.
 enum XFormat : int { X_F32 = 0, X_F16 = 1 };
 
-// Exponent e of the fp16 storage of x: |x_ij^c| = |sum_k a b| <= N max|a_c| max|b_c|, so with
-// e = 14 - ceil(log2(N max_c(max|a_c| max|b_c|))) every scaled value stays below 2^14 (fp16 tops out
-// near 2^16) -- the bound holds for any input, so the store never overflows. e is clamped to
-// [-60, 60]: 2^(2e) (the LayerNorm epsilon in scaled units) stays a normal float.
-// amax: [2][128] float bits of max |a_c| then max |b_c|, as the projection kernel leaves them.
-__host__ __device__ inline int x16_exponent_from_bound(float bound) {
-  if (!(bound > 0.f)) return 0;                                   // all-zero (or NaN) x: any scale
-  if (!(bound < 3.0e38f)) return -60;
-  uint32_t u;
-  memcpy(&u, &bound, 4);
-  const int be = (int)((u >> 23) & 255u);
-  int ce = be - 126;                                              // 2^ce >= bound for normal bound
-  if (be == 0) ce = -126;                                         // subnormal bound: 2^-126 >= it
-  int e = 14 - ce;
-  return e < -60 ? -60 : (e > 60 ? 60 : e);
-}
-
-// The same exponent from the device array, by one whole warp (every lane gets the result): the
-// per-channel products of the maxima, their maximum, times N.
-__device__ __forceinline__ int x16_exponent(const unsigned* amax, int N) {
-  const int lane = threadIdx.x & 31;
-  float m = 0.f;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int c = lane * 4 + k;
-    m = fmaxf(m, __uint_as_float(amax[c]) * __uint_as_float(amax[128 + c]));
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  return x16_exponent_from_bound((float)N * m);
-}
+// The fp16 storage of x scales every value by 2^e, chosen on the host from a bound on |x| that the
+// weights alone fix (tm_api.cu, x16_exponent).
 
 // Contraction of one output block: x[c][i-i0][j-j0] over k in [0, N).
 struct ContractParams {
@@ -76,17 +44,19 @@ struct ContractParams {
   int tiles_i, tiles_j;   // tiles covering [i_base, i0 + bi) x [j_base, j0 + bj)
   long long total_tiles;  // 128 * tiles_i * tiles_j
   int last_n;             // MMA N of the last tile column: the columns it still has to cover, rounded up to 16
-  int x_f16;              // 1: x is stored fp16, scaled by 2^e with e = x16_exponent(amax, N)
-  const unsigned* amax;   // the projection's per-channel maxima (x_f16 only)
+  int x_f16;              // 1: x is stored fp16, scaled by 2^x_exp
+  int x_exp;
   int tma_store;          // 1: x leaves through TMA stores (needs i0, j0 multiples of 8); 0: direct stores
   Watch w;
 };
 
 // Output epilogue of one block: out = sigmoid(g) * (W_o LayerNorm(x)).
 struct FinishParams {
-  const unsigned* amax;   // the projection's per-channel maxima (fp16 x only)
-  float cst[4 * kC];      // rowsum of W_g' (hi+lo), bias W_g beta_in, bias W_o beta_out, rowsum of W_o'
-                          // (times inv_scale_o); all halved for the tanh form (constant bank)
+  // rowsum of W_g' (hi+lo), bias W_g beta_in, bias W_o beta_out, rowsum of W_o' (times inv_scale_o);
+  // all halved for the tanh form. First and 16-byte aligned: the epilogue reads them two at a time as
+  // 8-byte constant-bank operands.
+  alignas(16) float cst[4 * kC];
+  int x_exp;              // fp16 x is stored times 2^x_exp
   float inv_scale_o;      // W_o is stored scaled by a power of two; this undoes it
   int N;
   int i0, j0, bi, bj;
