@@ -190,7 +190,7 @@ tm_status tm_watchdog_selftest(tm_ctx* ctx, int timeout_ms, void* stream);
  * 1 <= N <= 128, for callers that may not allocate device memory: code whose
  * device memory all belongs to another allocator or to a fixed budget, and code
  * that must not pay a device allocation's host-side stall. The a, b and x
- * scratch lives in one static 12 MiB device array inside libtm, which every
+ * scratch lives in one static 12.1 MiB device array inside libtm, which every
  * GPU that loads the library holds until the process exits; the call itself
  * allocates nothing. The first call on a device looks up that array's device
  * address (once per device, with the device current), so make that first call

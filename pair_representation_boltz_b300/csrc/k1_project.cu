@@ -235,6 +235,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         const float var = fmaxf((s01.x + s01.y) * (1.0f / kC) - dm * dm, 0.f);
         const float rstd = rsqrtf(var + 1e-5f);
         const int j = jt * BM + t;
+        // the finish kernel's gate reads the same LayerNorm_in statistics (one CTA of the pair writes
+        // them: 256 contiguous bytes per warp)
+        if (p.zstat && half == 0 && j < p.N) p.zstat[(size_t)i * p.N + j] = make_float2(rstd, -rstd * mu);
         float m = 0.f;
         if (j < p.N) m = p.mask ? p.mask[i] * p.mask[j] : 1.0f;
         const unsigned bits = __ballot_sync(0xffffffffu, m != 0.f);

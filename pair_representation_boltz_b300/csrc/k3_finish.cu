@@ -32,8 +32,9 @@
 //   warps 2..5  statistics, two lanes per pair (one per channel half): a shifted
 //               one-pass sum and sum of squares per half, merged across the two
 //               lanes (pairwise update of mean and sum of squares, Chan, Golub,
-//               LeVeque), for x and for z; handed to the epilogue through shared
-//               memory behind mbarriers.
+//               LeVeque), of x (and of z for float32 x; with fp16 x the
+//               projection kernel's LayerNorm_in statistics are read instead);
+//               handed to the epilogue through shared memory behind mbarriers.
 //   warps 6..13 epilogue, thread = pair: two warps per TMEM lane quadrant split
 //               the 128 output channels; folded LayerNorms, gate (sigmoid through
 //               one tanh) and product, staged in shared memory and written by one
@@ -202,10 +203,18 @@ __device__ __forceinline__ void epilogue_role(const FinishParams& p, const Smem&
     const int jt = (int)(t - (long long)il * p.tiles_j);
     const int buf = local & 1;
     const uint32_t use = (uint32_t)(local >> 1);
+    // X16: LayerNorm_in statistics of this thread's pair, as the projection kernel left them; the load
+    // is issued before the waits so that its latency hides behind them
+    float2 zst = make_float2(0.f, 0.f);
+    if (X16 && jt * BM + r < p.bj) zst = p.zstat[(size_t)(p.i0 + il) * p.N + (p.j0 + jt * BM + r)];
     if (!warp_wait_bounded(&b.sfull[0], (uint32_t)local & 1u, p.w, abort_flag, 43)) break;
     if (!warp_wait_bounded(&b.tfull[buf], use & 1u, p.w, abort_flag, 41)) break;
     tc_fence_after();
-    const float4 st = sm.st[r];
+    float4 st = sm.st[r];
+    if (X16) {
+      st.x = zst.x;
+      st.y = zst.y;
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(&b.sempty[0]);     // the statistics of this tile have been read
     if (X16) {
@@ -282,9 +291,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   volatile int* abort_flag = &b.abort_flag;
   constexpr int SLOT = XS_BYTES / 2;        // one fp16 x tile: two 64-pair boxes of [128 c][64 j]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // x slots and z are released by the MMA and by the statistics warps; the one statistics buffer
-  // by the epilogue warps once they have read it
-  if (threadIdx.x == 0) init_common(sm, 1 + LN_WARPS, 1 + LN_WARPS, EPI_WARPS, p);
+  // x slots are released by the MMA and the statistics warps, z by the MMA alone (z's LayerNorm
+  // statistics come from the projection kernel); the statistics buffer by the epilogue warps
+  if (threadIdx.x == 0) init_common(sm, 1 + LN_WARPS, 1, EPI_WARPS, p);
   if (warp == 1) {
     tmem_alloc(&b.tslot, TMEM_COLS);
     tmem_relinquish();
@@ -362,17 +371,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else if (warp < 2 + LN_WARPS) {
       // ------------------------------------------------------------ statistics, two lanes per pair
       // Lane l of warp w takes channel half hc = l / 16: x columns p0 = 32w + 2 (l % 16) and p0 + 1
-      // (one 4-byte load covers both; fp32x2 math over the two pairs), z rows 32w + l % 16 and + 16.
+      // (one 4-byte load covers both; fp32x2 math over the two pairs).
       const int lw = warp - 2;
       const int lp = lane & 15, hc = lane >> 4;
       const int p0 = lw * 32 + 2 * lp;
-      const int zr0 = lw * 32 + lp;
       // x16[c][p0], [c][p0 + 1] in a slot: the 64-pair half, 16-byte unit and byte of the pair
       const int xoff = (p0 >> 6) * (SLOT / 2) + ((p0 & 7) << 1);
       const uint32_t xunit = (uint32_t)((p0 & 63) >> 3);
       // LayerNorm epsilon in the units x16 = x 2^e is stored in
       const float x_eps = 1e-5f * __int_as_float((127 + 2 * p.x_exp) << 23);
-      uint32_t ph = 0;
       int local = 0;
       for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++local) {
         const int xsl = local & 1;
@@ -399,23 +406,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         float xm0, xr0, xm1, xr1;
         merge_halves(sh.x + ss.x * (1.0f / 64), vs.x - ss.x * ss.x * (1.0f / 64), x_eps, xm0, xr0);
         merge_halves(sh.y + ss.y * (1.0f / 64), vs.y - ss.y * ss.y * (1.0f / 64), x_eps, xm1, xr1);
-        if (!warp_wait_bounded(&b.zfull, ph, p.w, abort_flag, 38)) break;
-        float zmean[2], zrstd[2];
-        z_stats(sm.zs, zr0, hc, zmean, zrstd);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&b.zempty);        // this warp is done reading the z tile
         // the epilogue has read the previous tile's statistics
         if (!warp_wait_bounded(&b.sempty[0], ((uint32_t)local & 1u) ^ 1u, p.w, abort_flag, 42)) break;
         float2* st2 = reinterpret_cast<float2*>(sm.st);
-        // z: lane hc of the two that share the rows writes row zr0 + 16 hc; x: lane hc writes pair p0 + hc.
-        // rx carries the scale of W_o' (1/2 and its power of two): y/2 = rx acc + nx rowsum' + bias'.
-        st2[2 * (zr0 + 16 * hc)] = hc ? make_float2(zrstd[1], -zrstd[1] * zmean[1])
-                                      : make_float2(zrstd[0], -zrstd[0] * zmean[0]);
+        // lane hc of the two that share the pairs writes pair p0 + hc. rx carries the scale of W_o'
+        // (1/2 and its power of two): y/2 = rx acc + nx rowsum' + bias'.
         st2[2 * (p0 + hc) + 1] = hc ? make_float2(p.inv_scale_o * xr1, -xr1 * xm1)
                                     : make_float2(p.inv_scale_o * xr0, -xr0 * xm0);
         __syncwarp();
         if (lane == 0) mbar_arrive(&b.sfull[0]);
-        ph ^= 1u;
       }
     } else {
       epilogue_role<true>(p, sm, tmem_base, &omap, abort_flag, warp, lane);

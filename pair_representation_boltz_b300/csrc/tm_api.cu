@@ -328,7 +328,7 @@ tm_status prepare_tensor_core_weights(tm_ctx* c, const tm_weights* w) {
 }
 
 // ------------------------------------------------------------------ bf16 stage launchers (arguments checked)
-tm_status run_project_bf16(tm_ctx* c, const void* z, const float* mask, int N, __nv_bfloat16* a,
+tm_status run_project_bf16(tm_ctx* c, const void* z, const float* mask, int N, float2* zstat, __nv_bfloat16* a,
                            __nv_bfloat16* b, int ld, cudaStream_t s, const tm_options* opt) {
   CUtensorMap zmap;
   const cuuint64_t dims[3] = {(cuuint64_t)kC, (cuuint64_t)N, (cuuint64_t)N};
@@ -348,6 +348,7 @@ tm_status run_project_bf16(tm_ctx* c, const void* z, const float* mask, int N, _
   p.b = b;
   p.mask = mask;
   p.consts = c->k1c;
+  p.zstat = zstat;
   p.N = N;
   p.ld = ld;
   p.tiles_per_row = (N + kProjTileJ - 1) / kProjTileJ;
@@ -412,7 +413,7 @@ tm_status run_contract_bf16(tm_ctx* c, const __nv_bfloat16* a, const __nv_bfloat
   return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "contraction launch");
 }
 
-tm_status run_finish_bf16(tm_ctx* c, const void* x, int ldx, XFormat xf, int x_exp, const void* z, int N,
+tm_status run_finish_bf16(tm_ctx* c, const void* x, int ldx, XFormat xf, int x_exp, const float2* zstat, const void* z, int N,
                           int i0, int j0, int bi, int bj, void* out, cudaStream_t s, const tm_options* opt) {
   CUtensorMap xmap, zmap;
   {
@@ -442,6 +443,7 @@ tm_status run_finish_bf16(tm_ctx* c, const void* x, int ldx, XFormat xf, int x_e
   }
   FinishParams p;
   p.x_exp = x_exp;
+  p.zstat = zstat;
   std::memcpy(p.cst, c->k3c_host, sizeof p.cst);
   p.inv_scale_o = c->inv_scale_o;
   p.N = N;
@@ -600,7 +602,7 @@ tm_status tm_project(tm_ctx* c, const void* z, const float* mask, int N, tm_dtyp
   if (ld < N || (dtype == TM_BF16 && ld % 8)) return fail(c, TM_ERR_INVALID, "ld=%d must be >= N (and a multiple of 8 for bf16)", ld);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (dtype == TM_BF16)
-    return run_project_bf16(c, z, mask, N, reinterpret_cast<__nv_bfloat16*>(a), reinterpret_cast<__nv_bfloat16*>(b),
+    return run_project_bf16(c, z, mask, N, nullptr, reinterpret_cast<__nv_bfloat16*>(a), reinterpret_cast<__nv_bfloat16*>(b),
                             ld, s, nullptr);
   cudaError_t e = timed(c, 3, (long long)N * N, s, [&] {
     return launch_project_f32(reinterpret_cast<const float*>(z), mask, c->f32w, reinterpret_cast<float*>(a),
@@ -644,7 +646,7 @@ tm_status tm_finish(tm_ctx* c, const float* x, int ldx, const void* z, int N, tm
   const size_t zbytes = (size_t)N * N * c->c_z * (dtype == TM_BF16 ? 2 : 4);
   if (ranges_overlap(z, zbytes, out, zbytes)) return fail(c, TM_ERR_INVALID, "out overlaps z");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (dtype == TM_BF16) return run_finish_bf16(c, x, ldx, X_F32, 0, z, N, i0, j0, bi, bj, out, s, nullptr);
+  if (dtype == TM_BF16) return run_finish_bf16(c, x, ldx, X_F32, 0, nullptr, z, N, i0, j0, bi, bj, out, s, nullptr);
   cudaError_t e = timed(c, 3, (long long)bi * bj, s, [&] {
     return launch_finish_f32(x, ldx, (long long)bi * ldx, reinterpret_cast<const float*>(z), c->f32w, N, i0, j0, bi,
                              bj, reinterpret_cast<float*>(out), s);
@@ -684,17 +686,20 @@ tm_status tm_forward_ex(tm_ctx* c, const void* z, const float* mask, int N, tm_d
   const int B = choose_block(c, N, opt, 2 * ab_bytes, xe);
   const int ldx = (int)align_up(B, 128 / xe);     // 128-byte rows
   const size_t x_bytes = align_up((size_t)c->c_h * B * ldx * xe, 256);
-  st = ensure_workspace(c, 2 * ab_bytes + x_bytes, s, opt);
+  // LayerNorm_in statistics per pair, from the projection to the fp16-x finish kernel
+  const size_t zst_bytes = xf == X_F16 ? align_up((size_t)N * N * sizeof(float2), 256) : 0;
+  st = ensure_workspace(c, 2 * ab_bytes + x_bytes + zst_bytes, s, opt);
   if (st != TM_OK) return st;
   uint8_t* base = reinterpret_cast<uint8_t*>(c->ws);
   void* a = base;
   void* b = base + ab_bytes;
   float* x = reinterpret_cast<float*>(base + 2 * ab_bytes);
+  float2* zstat = xf == X_F16 ? reinterpret_cast<float2*>(base + 2 * ab_bytes + x_bytes) : nullptr;
 
   if (dtype == TM_BF16) {
     const int x_exp = x16_exponent(c, N);
-    st = run_project_bf16(c, z, mask, N, reinterpret_cast<__nv_bfloat16*>(a), reinterpret_cast<__nv_bfloat16*>(b),
-                          ld, s, opt);
+    st = run_project_bf16(c, z, mask, N, zstat, reinterpret_cast<__nv_bfloat16*>(a),
+                          reinterpret_cast<__nv_bfloat16*>(b), ld, s, opt);
     if (st != TM_OK) return st;
     for (int i0 = 0; i0 < N; i0 += B)
       for (int j0 = 0; j0 < N; j0 += B) {
@@ -702,7 +707,7 @@ tm_status tm_forward_ex(tm_ctx* c, const void* z, const float* mask, int N, tm_d
         st = run_contract_bf16(c, reinterpret_cast<const __nv_bfloat16*>(a), reinterpret_cast<const __nv_bfloat16*>(b),
                                N, ld, inc, i0, j0, bi, bj, x, ldx, xf, x_exp, s, opt);
         if (st != TM_OK) return st;
-        st = run_finish_bf16(c, x, ldx, xf, x_exp, z, N, i0, j0, bi, bj, out, s, opt);
+        st = run_finish_bf16(c, x, ldx, xf, x_exp, zstat, z, N, i0, j0, bi, bj, out, s, opt);
         if (st != TM_OK) return st;
       }
     return TM_OK;
@@ -834,7 +839,8 @@ namespace {
 constexpr int kNoAllocMaxN = 128;
 constexpr size_t kNoAllocAB = (size_t)kC * kNoAllocMaxN * kNoAllocMaxN * 2;  // a or b, bf16: 4 MiB
 constexpr size_t kNoAllocX = (size_t)kC * kNoAllocMaxN * kNoAllocMaxN * 2;   // x, fp16: 4 MiB
-constexpr size_t kNoAllocBytes = 2 * kNoAllocAB + kNoAllocX;                // 12 MiB in all
+constexpr size_t kNoAllocZst = (size_t)kNoAllocMaxN * kNoAllocMaxN * 8;     // LayerNorm_in statistics: 128 KiB
+constexpr size_t kNoAllocBytes = 2 * kNoAllocAB + kNoAllocX + kNoAllocZst;  // 12.125 MiB in all
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
@@ -885,14 +891,15 @@ extern "C" tm_status tm_forward_noalloc(tm_ctx* c, const void* z, const float* m
   __nv_bfloat16* a = reinterpret_cast<__nv_bfloat16*>(scratch);
   __nv_bfloat16* b = reinterpret_cast<__nv_bfloat16*>(scratch + kNoAllocAB);
   void* x = scratch + 2 * kNoAllocAB;
+  float2* zstat = reinterpret_cast<float2*>(scratch + 2 * kNoAllocAB + kNoAllocX);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool timing = c->timing;  // event creation is an allocation too: no timing inside this call
   c->timing = false;
   const int x_exp = x16_exponent(c, N);
-  st = run_project_bf16(c, z, mask, N, a, b, ld, s, nullptr);
+  st = run_project_bf16(c, z, mask, N, zstat, a, b, ld, s, nullptr);
   if (st == TM_OK)
     st = run_contract_bf16(c, a, b, N, ld, dir == TM_INCOMING, 0, 0, N, N, x, ldx, X_F16, x_exp, s, nullptr);
-  if (st == TM_OK) st = run_finish_bf16(c, x, ldx, X_F16, x_exp, z, N, 0, 0, N, N, out, s, nullptr);
+  if (st == TM_OK) st = run_finish_bf16(c, x, ldx, X_F16, x_exp, zstat, z, N, 0, 0, N, N, out, s, nullptr);
   c->timing = timing;
   return st;
 }

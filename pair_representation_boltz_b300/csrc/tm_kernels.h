@@ -19,6 +19,8 @@ struct ProjectParams {
   __nv_bfloat16* b;       // [128][N][ld]
   const float* mask;      // [N] or nullptr
   const float* consts;    // [2 halves][512]: rowsum[256] then bias[256] of the folded LayerNorm
+  float2* zstat;          // [N][N] (rstd, -rstd mu) of LayerNorm_in per pair, written by the a-half CTA
+                          // for the finish kernel; nullptr: not written
   int N, ld;
   int tiles_per_row;      // ceil(N / 128)
   long long total_tiles;  // N * tiles_per_row
@@ -57,6 +59,7 @@ struct FinishParams {
   // 8-byte constant-bank operands.
   alignas(16) float cst[4 * kC];
   int x_exp;              // fp16 x is stored times 2^x_exp
+  const float2* zstat;    // [N][N] (rstd, -rstd mu) of LayerNorm_in per pair (fp16-x kernel)
   float inv_scale_o;      // W_o is stored scaled by a power of two; this undoes it
   int N;
   int i0, j0, bi, bj;
