@@ -92,7 +92,12 @@ typedef struct {
   int timeout_ms;         /* limit of every device-side wait; 0 = 2000 ms           */
   size_t workspace_limit; /* bytes; 0 = env TM_WORKSPACE_LIMIT, else no limit      */
   int x_storage;          /* tm_x_storage; 0 = TM_X_FP16                            */
-  int reserved[7];        /* must be zero                                          */
+  int residual;           /* 1: out = z + update, the residual connection of a
+                             Pairformer block (bf16: one rounding of the sum, as a
+                             bf16 add does); out may then be z itself (in place,
+                             no extra pass) or a separate buffer (z is copied into
+                             it first). 0: out = update, out must not overlap z.  */
+  int reserved[6];        /* must be zero                                          */
 } tm_options;
 
 /* Create a context on the current CUDA device. Copies and converts the
@@ -113,6 +118,18 @@ tm_status tm_forward(tm_ctx* ctx, const void* z, const float* mask, int N, tm_dt
 /* tm_forward with options (NULL = defaults). */
 tm_status tm_forward_ex(tm_ctx* ctx, const void* z, const float* mask, int N, tm_dtype dtype,
                         tm_direction dir, void* out, void* stream, const tm_options* opt);
+
+/* The two triangle multiplicative updates of a Pairformer block, in place:
+ *   z <- z + update_outgoing(z);  z <- z + update_incoming(z)
+ * (the residual connections around the two layers; "outgoing then incoming,
+ * as in one Pairformer block" of the four-chain complex workload). z is
+ * device [N][N][c_z] of dtype and is overwritten; each update is a
+ * tm_forward_ex with residual = 1 and out = z, so the sums are formed where
+ * the finish kernel writes (no extra pass over z). opt as for tm_forward_ex
+ * (residual is ignored; NULL = defaults). Stream-ordered; capturable into a
+ * CUDA graph once a first call has sized the workspace. */
+tm_status tm_pair_update(tm_ctx* ctx, void* z, const float* mask, int N, tm_dtype dtype, void* stream,
+                         const tm_options* opt);
 
 /* tm_forward on HOST buffers: copies z (and mask) host -> device into
  * ctx-owned device buffers, runs the update, and copies out device -> host,

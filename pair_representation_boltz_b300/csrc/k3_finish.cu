@@ -232,8 +232,13 @@ __device__ __forceinline__ void epilogue_role(const FinishParams& p, const Smem&
       mbar_arrive(&b.tempty[buf]);
       // rows 32q .. 32q+31 of the box: one TMA store (pairs past the block's edge are clipped by the
       // map, whose extents are the block's)
+      // (residual: the box is added to out, which holds z: out = z + update, rounded once to bf16 where
+      // it lands)
       if (jt * BM + q * 32 < p.bj) {
-        tma_store_3d(omap, stg + q * 32 * 128, hsel * 64, jt * BM + q * 32, il);
+        if (p.residual)
+          tma_reduce_add_3d(omap, stg + q * 32 * 128, hsel * 64, jt * BM + q * 32, il);
+        else
+          tma_store_3d(omap, stg + q * 32 * 128, hsel * 64, jt * BM + q * 32, il);
         bulk_commit();
       }
       if (!X16) {

@@ -88,8 +88,8 @@ __global__ void k2f_contract(const float* __restrict__ a, const float* __restric
 }
 
 __global__ void k3f_finish(const float* __restrict__ x, long long ldx, long long chan_stride,
-                           const float* __restrict__ z, const F32Weights w, int N, int i0, int j0, int bi, int bj,
-                           float* __restrict__ out) {
+                           const float* z, const F32Weights w, int N, int i0, int j0, int bi, int bj,
+                           float* out, int residual) {
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (long long)bi * bj) return;
   const int il = (int)(idx / bj), jl = (int)(idx - (long long)il * bj);
@@ -115,7 +115,10 @@ __global__ void k3f_finish(const float* __restrict__ x, long long ldx, long long
     const float* rg = w.w_g + (size_t)o * w.c_z;
     for (int c = 0; c < w.c_h; ++c) y = fmaf(ro[c], xv[c], y);
     for (int k = 0; k < w.c_z; ++k) g = fmaf(rg[k], zh[k], g);
-    op[o] = sigmoid_acc(g) * y;
+    // residual: out = z + update; z of this pair and channel is read before it is written (out may be z)
+    // (the product is rounded first, then the sum: the same value as adding z to the plain output)
+    const float zo = residual ? z[pair * w.c_z + o] : 0.f;
+    op[o] = __fadd_rn(zo, __fmul_rn(sigmoid_acc(g), y));
   }
 }
 
@@ -139,10 +142,11 @@ cudaError_t launch_contract_f32(bool incoming, const float* a, const float* b, i
 
 cudaError_t launch_finish_f32(const float* x, long long ldx, long long chan_stride, const float* z,
                               const F32Weights& w, int N, int i0, int j0, int bi, int bj, float* out,
-                              cudaStream_t s) {
+                              bool residual, cudaStream_t s) {
   const long long n = (long long)bi * bj;
   const int th = 128;
-  k3f_finish<<<(unsigned)((n + th - 1) / th), th, 0, s>>>(x, ldx, chan_stride, z, w, N, i0, j0, bi, bj, out);
+  k3f_finish<<<(unsigned)((n + th - 1) / th), th, 0, s>>>(x, ldx, chan_stride, z, w, N, i0, j0, bi, bj, out,
+                                                          residual ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -414,7 +414,8 @@ tm_status run_contract_bf16(tm_ctx* c, const __nv_bfloat16* a, const __nv_bfloat
 }
 
 tm_status run_finish_bf16(tm_ctx* c, const void* x, int ldx, XFormat xf, int x_exp, const float2* zstat, const void* z, int N,
-                          int i0, int j0, int bi, int bj, void* out, cudaStream_t s, const tm_options* opt) {
+                          int i0, int j0, int bi, int bj, void* out, bool residual, cudaStream_t s,
+                          const tm_options* opt) {
   CUtensorMap xmap, zmap;
   {
     const size_t xe = xf == X_F16 ? 2 : 4;
@@ -443,6 +444,7 @@ tm_status run_finish_bf16(tm_ctx* c, const void* x, int ldx, XFormat xf, int x_e
   }
   FinishParams p;
   p.x_exp = x_exp;
+  p.residual = residual ? 1 : 0;
   p.zstat = zstat;
   std::memcpy(p.cst, c->k3c_host, sizeof p.cst);
   p.inv_scale_o = c->inv_scale_o;
@@ -646,10 +648,11 @@ tm_status tm_finish(tm_ctx* c, const float* x, int ldx, const void* z, int N, tm
   const size_t zbytes = (size_t)N * N * c->c_z * (dtype == TM_BF16 ? 2 : 4);
   if (ranges_overlap(z, zbytes, out, zbytes)) return fail(c, TM_ERR_INVALID, "out overlaps z");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (dtype == TM_BF16) return run_finish_bf16(c, x, ldx, X_F32, 0, nullptr, z, N, i0, j0, bi, bj, out, s, nullptr);
+  if (dtype == TM_BF16)
+    return run_finish_bf16(c, x, ldx, X_F32, 0, nullptr, z, N, i0, j0, bi, bj, out, false, s, nullptr);
   cudaError_t e = timed(c, 3, (long long)bi * bj, s, [&] {
     return launch_finish_f32(x, ldx, (long long)bi * ldx, reinterpret_cast<const float*>(z), c->f32w, N, i0, j0, bi,
-                             bj, reinterpret_cast<float*>(out), s);
+                             bj, reinterpret_cast<float*>(out), false, s);
   });
   return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "finish (f32) launch");
 }
@@ -668,13 +671,17 @@ tm_status tm_forward_ex(tm_ctx* c, const void* z, const float* mask, int N, tm_d
     if (opt->block < 0 || opt->timeout_ms < 0) return fail(c, TM_ERR_INVALID, "negative option");
     if (opt->x_storage != TM_X_FP16 && opt->x_storage != TM_X_FP32)
       return fail(c, TM_ERR_INVALID, "unknown x_storage %d", opt->x_storage);
+    if (opt->residual != 0 && opt->residual != 1) return fail(c, TM_ERR_INVALID, "residual must be 0 or 1");
   }
+  const bool residual = opt && opt->residual;
   // x between the contraction and the finish: scaled fp16 unless float32 is asked for (the float32
   // CUDA-core path always keeps float32)
   const XFormat xf = (dtype == TM_BF16 && !(opt && opt->x_storage == TM_X_FP32)) ? X_F16 : X_F32;
   const size_t esz = dtype == TM_BF16 ? 2 : 4;
   const size_t zbytes = (size_t)N * N * c->c_z * esz;
-  if (ranges_overlap(z, zbytes, out, zbytes)) return fail(c, TM_ERR_INVALID, "out overlaps z");
+  const bool in_place = residual && out == z;   // the residual update may overwrite z itself
+  if (!in_place && ranges_overlap(z, zbytes, out, zbytes))
+    return fail(c, TM_ERR_INVALID, residual ? "out overlaps z without being z" : "out overlaps z");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool inc = dir == TM_INCOMING;
 
@@ -701,13 +708,18 @@ tm_status tm_forward_ex(tm_ctx* c, const void* z, const float* mask, int N, tm_d
     st = run_project_bf16(c, z, mask, N, zstat, reinterpret_cast<__nv_bfloat16*>(a),
                           reinterpret_cast<__nv_bfloat16*>(b), ld, s, opt);
     if (st != TM_OK) return st;
+    if (residual && !in_place) {
+      // the finish kernel adds the update to what out holds: give it z first
+      cudaError_t e = cudaMemcpyAsync(out, z, zbytes, cudaMemcpyDeviceToDevice, s);
+      if (e != cudaSuccess) return cuda_fail(c, e, "cudaMemcpyAsync(out <- z)");
+    }
     for (int i0 = 0; i0 < N; i0 += B)
       for (int j0 = 0; j0 < N; j0 += B) {
         const int bi = std::min(B, N - i0), bj = std::min(B, N - j0);
         st = run_contract_bf16(c, reinterpret_cast<const __nv_bfloat16*>(a), reinterpret_cast<const __nv_bfloat16*>(b),
                                N, ld, inc, i0, j0, bi, bj, x, ldx, xf, x_exp, s, opt);
         if (st != TM_OK) return st;
-        st = run_finish_bf16(c, x, ldx, xf, x_exp, zstat, z, N, i0, j0, bi, bj, out, s, opt);
+        st = run_finish_bf16(c, x, ldx, xf, x_exp, zstat, z, N, i0, j0, bi, bj, out, residual, s, opt);
         if (st != TM_OK) return st;
       }
     return TM_OK;
@@ -728,11 +740,21 @@ tm_status tm_forward_ex(tm_ctx* c, const void* z, const float* mask, int N, tm_d
       if (e != cudaSuccess) return cuda_fail(c, e, "contraction (f32) launch");
       e = timed(c, 3, (long long)bi * bj, s, [&] {
         return launch_finish_f32(x, ldx, (long long)bi * ldx, reinterpret_cast<const float*>(z), c->f32w, N, i0, j0,
-                                 bi, bj, reinterpret_cast<float*>(out), s);
+                                 bi, bj, reinterpret_cast<float*>(out), residual, s);
       });
       if (e != cudaSuccess) return cuda_fail(c, e, "finish (f32) launch");
     }
   return TM_OK;
+}
+
+tm_status tm_pair_update(tm_ctx* c, void* z, const float* mask, int N, tm_dtype dtype, void* stream,
+                         const tm_options* opt) {
+  tm_options o{};
+  if (opt) o = *opt;
+  o.residual = 1;
+  tm_status st = tm_forward_ex(c, z, mask, N, dtype, TM_OUTGOING, z, stream, &o);
+  if (st != TM_OK) return st;
+  return tm_forward_ex(c, z, mask, N, dtype, TM_INCOMING, z, stream, &o);
 }
 
 tm_status tm_forward(tm_ctx* c, const void* z, const float* mask, int N, tm_dtype dtype, tm_direction dir, void* out,
@@ -899,7 +921,7 @@ extern "C" tm_status tm_forward_noalloc(tm_ctx* c, const void* z, const float* m
   st = run_project_bf16(c, z, mask, N, zstat, a, b, ld, s, nullptr);
   if (st == TM_OK)
     st = run_contract_bf16(c, a, b, N, ld, dir == TM_INCOMING, 0, 0, N, N, x, ldx, X_F16, x_exp, s, nullptr);
-  if (st == TM_OK) st = run_finish_bf16(c, x, ldx, X_F16, x_exp, zstat, z, N, 0, 0, N, N, out, s, nullptr);
+  if (st == TM_OK) st = run_finish_bf16(c, x, ldx, X_F16, x_exp, zstat, z, N, 0, 0, N, N, out, false, s, nullptr);
   c->timing = timing;
   return st;
 }

@@ -59,6 +59,7 @@ struct FinishParams {
   // 8-byte constant-bank operands.
   alignas(16) float cst[4 * kC];
   int x_exp;              // fp16 x is stored times 2^x_exp
+  int residual;           // 1: out += update (out holds z: a residual connection), else out = update
   const float2* zstat;    // [N][N] (rstd, -rstd mu) of LayerNorm_in per pair (fp16-x kernel)
   float inv_scale_o;      // W_o is stored scaled by a power of two; this undoes it
   int N;
@@ -118,7 +119,7 @@ cudaError_t launch_contract_f32(bool incoming, const float* a, const float* b, i
                                 cudaStream_t s);
 cudaError_t launch_finish_f32(const float* x, long long ldx, long long chan_stride, const float* z,
                               const F32Weights& w, int N, int i0, int j0, int bi, int bj, float* out,
-                              cudaStream_t s);
+                              bool residual, cudaStream_t s);
 
 // ----------------------------------------------------------------- diagnostics
 enum : int { KID_SELFTEST = 9 };

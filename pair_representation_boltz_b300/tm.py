@@ -7,7 +7,7 @@ streams only. There is no fallback: without the built library or without a
 GPU every call raises.
 
 The function names mirror the C ABI: tm_create, tm_forward, tm_forward_ex, tm_forward_host,
-tm_forward_noalloc,
+tm_forward_noalloc, tm_pair_update,
 tm_project, tm_contract, tm_finish, tm_sync_status, tm_watchdog_selftest, tm_set_timing,
 tm_get_timing, tm_launch_count, tm_workspace_bytes, tm_status_string,
 tm_last_error, tm_destroy. ``TriMul`` wraps a context for convenience.
@@ -43,7 +43,7 @@ X_STORAGE = {"fp16": TM_X_FP16, "fp32": TM_X_FP32}
 
 class TmOptions(C.Structure):
     _fields_ = [("block", C.c_int), ("timeout_ms", C.c_int), ("workspace_limit", C.c_size_t),
-                ("x_storage", C.c_int), ("reserved", C.c_int * 7)]
+                ("x_storage", C.c_int), ("residual", C.c_int), ("reserved", C.c_int * 6)]
 
 
 class TmTiming(C.Structure):
@@ -74,6 +74,7 @@ def load_library(path: str = LIB_PATH):
         "tm_forward": (st, [vp, vp, vp, i, i, i, vp, vp]),
         "tm_forward_ex": (st, [vp, vp, vp, i, i, i, vp, vp, C.POINTER(TmOptions)]),
         "tm_forward_host": (st, [vp, vp, vp, i, i, i, vp, vp]),
+        "tm_pair_update": (st, [vp, vp, vp, i, i, vp, C.POINTER(TmOptions)]),
         "tm_forward_noalloc": (st, [vp, vp, vp, i, i, vp, vp]),
         "tm_project": (st, [vp, vp, vp, i, i, vp, vp, i, vp]),
         "tm_contract": (st, [vp, vp, vp, i, i, i, i, i, i, i, i, vp, i, vp]),
@@ -174,12 +175,21 @@ def tm_destroy(ctx) -> None:
 
 
 def tm_forward_ex(ctx, z, mask, direction, out, stream=None, block=0, timeout_ms=0, workspace_limit=0,
-                  x_storage="fp16"):
+                  x_storage="fp16", residual=False):
     N = z.shape[0]
-    opt = TmOptions(block, timeout_ms, workspace_limit, X_STORAGE[x_storage])
+    opt = TmOptions(block, timeout_ms, workspace_limit, X_STORAGE[x_storage], 1 if residual else 0)
     _check(ctx, load_library().tm_forward_ex(ctx, _ptr(z), _ptr(mask), N, _dtype_code(z), _direction(direction),
                                              _ptr(out), _stream(stream), C.byref(opt)))
     return out
+
+
+def tm_pair_update(ctx, z, mask=None, stream=None, block=0, timeout_ms=0, workspace_limit=0, x_storage="fp16"):
+    """z <- z + outgoing(z); z <- z + incoming(z), in place (z: contiguous CUDA tensor [N][N][c_z])."""
+    N = z.shape[0]
+    opt = TmOptions(block, timeout_ms, workspace_limit, X_STORAGE[x_storage], 1)
+    _check(ctx, load_library().tm_pair_update(ctx, _ptr(z), _ptr(mask), N, _dtype_code(z), _stream(stream),
+                                              C.byref(opt)))
+    return z
 
 
 def tm_forward(ctx, z, mask, direction, out, stream=None):

@@ -52,10 +52,11 @@ def test_create_rejects_bad_arguments_before_touching_cuda(libtm):
 
 
 def test_options_struct_layout():
-    # int block; int timeout_ms; size_t workspace_limit; int x_storage; int reserved[7]
-    assert ctypes.sizeof(tm.TmOptions) == 4 + 4 + 8 + 4 + 28
+    # int block; int timeout_ms; size_t workspace_limit; int x_storage; int residual; int reserved[6]
+    assert ctypes.sizeof(tm.TmOptions) == 4 + 4 + 8 + 4 + 4 + 24
     assert tm.TmOptions.workspace_limit.offset == 8
     assert tm.TmOptions.x_storage.offset == 16
+    assert tm.TmOptions.residual.offset == 20
     assert ctypes.sizeof(tm.TmTiming) == 16 + 32 + 32
 
 
