@@ -172,6 +172,49 @@ tm_status tm_contract(tm_ctx* ctx, const void* a, const void* b, int N, int ld, 
 tm_status tm_finish(tm_ctx* ctx, const float* x, int ldx, const void* z, int N, tm_dtype dtype,
                     int i0, int j0, int bi, int bj, void* out, void* stream);
 
+/* Gradients of the layer's parameters: device float32 arrays, each shaped as
+ * the tm_weights member of the same name. A NULL member is not written. */
+typedef struct {
+  float *ln_in_gamma, *ln_in_beta;
+  float *w_a, *w_ga, *w_b, *w_gb;
+  float *w_g;
+  float *ln_out_gamma, *ln_out_beta;
+  float *w_o;
+} tm_grads;
+
+/* Backward pass of one update, for training (the pages call fine-tuning at
+ * larger crops essential: section "A pegadinha" of the BioNeMo context-
+ * parallelism page named above). For the cotangent dout of out = update(z)
+ * (the gradient of a scalar loss L with respect to out) it writes
+ *   dz    = dL/dz   = J_z^T dout,   and
+ *   grads = dL/dW for every parameter (overwritten, not accumulated),
+ * with the chain rule taken through the definition in the header comment:
+ *   dy = dout*g, dgg = dout*y*g(1-g) (g = sigmoid(W_g zh), y = W_o LN_out(x));
+ *   LayerNorm backward over c_h gives dx;
+ *   outgoing: da = dX b, db = dX^T a  /  incoming: da = b dX^T, db = a dX
+ *     (per channel, over the N x N planes);
+ *   the gate backward of a and b (masked like a and b) and W^T products give
+ *   dzh; LayerNorm backward over c_z gives dz.
+ * It recomputes a, b and x from z (no state is kept from a forward call).
+ *   z      device [N][N][c_z] of dtype;
+ *   mask   device float32 [N] or NULL, as for tm_forward;
+ *   dout   device [N][N][c_z] of dtype;
+ *   dz     device [N][N][c_z] of dtype; may be dout itself (dout is fully read
+ *          before dz is written), must not otherwise overlap dout or z;
+ *   grads  device pointers (float32), or NULL to skip every parameter gradient.
+ * Precisions: TM_F32 keeps every intermediate in float32 on the CUDA cores.
+ * TM_BF16 recomputes a and b in bf16 as the forward stores them and x in
+ * float32, and its contractions of the gradient (dX with b and a, the
+ * per-pair W^T products, the parameter sums over N^2 pairs) run on the tensor
+ * cores from bf16 operands with float32 accumulation; dA and dB are float32.
+ * Workspace: about (4 c_h (2 + 4) + 4 c_z) N^2 bytes for TM_BF16
+ * (33 GB at N = 3605) -- beyond the workspace limit it returns TM_ERR_OOM before
+ * any launch. opt: timeout_ms and workspace_limit apply; block, x_storage and
+ * residual must be 0. Stream-ordered like tm_forward. */
+tm_status tm_backward(tm_ctx* ctx, const void* z, const float* mask, int N, tm_dtype dtype,
+                      tm_direction dir, const void* dout, void* dz, const tm_grads* grads,
+                      void* stream, const tm_options* opt);
+
 /* Synchronise `stream` and return the device status word (TM_OK or
  * TM_ERR_TIMEOUT), clearing it. */
 tm_status tm_sync_status(tm_ctx* ctx, void* stream);
@@ -179,9 +222,11 @@ tm_status tm_sync_status(tm_ctx* ctx, void* stream);
 /* Per-kernel timing with CUDA events recorded on the launch stream.
  * enable != 0 starts recording (and clears the totals). */
 typedef struct {
-  int launches[4];     /* projection, contraction, finish, float32 kernels */
-  double ms[4];        /* summed event-measured durations                  */
-  long long units[4];  /* pairs processed (projection, finish) or
+  int launches[8];     /* projection, contraction, finish, float32 kernels,
+                          output backward, projection backward, other
+                          backward kernels (transpose, sums), unused         */
+  double ms[8];        /* summed event-measured durations                  */
+  long long units[8];  /* pairs processed (projection, finish, backward) or
                           channel x output-pair products (contraction)     */
 } tm_timing;
 tm_status tm_set_timing(tm_ctx* ctx, int enable);

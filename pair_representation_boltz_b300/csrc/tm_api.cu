@@ -500,6 +500,98 @@ int choose_block(const tm_ctx* c, int N, const tm_options* opt, size_t ab_bytes,
   }
 }
 
+// ---------------------------------------------------------------------- backward pass
+//
+// Schedule (both precisions): recompute a, b (projection) and x (contraction, float32); the
+// output backward gives dX, its transpose dX^T, and the gate's term of dzh; the two contraction
+// gradients are contractions again, with other operands:
+//   outgoing (X = A B^T):  dA = dX B   = incoming-form contraction of (dX^T, b)
+//                          dB = dX^T A = incoming-form contraction of (dX, a)
+//   incoming (X = A^T B):  dA = B dX^T = outgoing-form contraction of (b, dX)
+//                          dB = A dX   = outgoing-form contraction of (a, dX^T)
+// (the incoming form sums over the first index of both planes, the outgoing form over the second),
+// so the forward's contraction kernels serve unchanged; the projection backward then gives dz.
+// Every parameter gradient is a sum over the N^2 pairs, formed without atomics in fixed order.
+
+tm_status backward_f32(tm_ctx* c, const float* z, const float* mask, int N, bool inc, const float* dout, float* dz,
+                       const tm_grads* g, cudaStream_t s, const tm_options* opt) {
+  const int Cz = c->c_z, Ch = c->c_h;
+  const long long P = (long long)N * N;
+  const int ld = N;
+  const size_t plane = align_up((size_t)Ch * N * ld * 4, 256);
+  const size_t vh = align_up((size_t)Ch * P * 4, 256), vz = align_up((size_t)Cz * P * 4, 256);
+  const size_t part = align_up((size_t)outer_sum_splits(P) * 256 * 256 * 4, 256);
+  // planes a, b, x (then dA), dX, dX^T, dB; vectors: 7 of c_h, 6 of c_z
+  const size_t need = 6 * plane + 7 * vh + 6 * vz + part;
+  tm_status st = ensure_workspace(c, need, s, opt);
+  if (st != TM_OK) return st;
+  uint8_t* q = reinterpret_cast<uint8_t*>(c->ws);
+  auto take = [&](size_t n) { float* r = reinterpret_cast<float*>(q); q += n; return r; };
+  float *a = take(plane), *b = take(plane), *x = take(plane), *dX = take(plane), *dXT = take(plane),
+        *dB = take(plane);
+  BwdF32Vectors v{};
+  v.dX = dX;
+  v.dXT = dXT;
+  v.dA = x;            // x is dead once the output backward has run
+  v.dB = dB;
+  v.ld = ld;
+  v.xh = take(vh);
+  v.q_out_n = take(vh);
+  v.q_out = take(vh);
+  v.dpa = take(vh);
+  v.dga = take(vh);
+  v.dpb = take(vh);
+  v.dgb = take(vh);
+  v.dzh = take(vz);
+  v.zh = take(vz);
+  v.dy = take(vz);
+  v.dgg = take(vz);
+  v.q_in_n = take(vz);
+  v.q_in = take(vz);
+  float* partial = take(part);
+  const F32Weights& w = c->f32w;
+  cudaError_t e;
+#define TM_F32_STEP(what, call)                                         \
+  e = timed(c, 3, P, s, [&] { return call; });                          \
+  if (e != cudaSuccess) return cuda_fail(c, e, what);
+  TM_F32_STEP("projection (f32) launch", launch_project_f32(z, mask, w, a, b, N, ld, s))
+  TM_F32_STEP("contraction (f32) launch",
+              launch_contract_f32(inc, a, b, N, ld, Ch, 0, 0, N, N, x, ld, (long long)N * ld, s))
+  TM_F32_STEP("output backward (f32) launch", launch_bwd_output_f32(x, ld, z, dout, w, N, v, s))
+  float* dA = x;
+  if (!inc) {
+    TM_F32_STEP("dA contraction (f32) launch",
+                launch_contract_f32(true, dXT, b, N, ld, Ch, 0, 0, N, N, dA, ld, (long long)N * ld, s))
+    TM_F32_STEP("dB contraction (f32) launch",
+                launch_contract_f32(true, dX, a, N, ld, Ch, 0, 0, N, N, dB, ld, (long long)N * ld, s))
+  } else {
+    TM_F32_STEP("dA contraction (f32) launch",
+                launch_contract_f32(false, b, dX, N, ld, Ch, 0, 0, N, N, dA, ld, (long long)N * ld, s))
+    TM_F32_STEP("dB contraction (f32) launch",
+                launch_contract_f32(false, a, dXT, N, ld, Ch, 0, 0, N, N, dB, ld, (long long)N * ld, s))
+  }
+  TM_F32_STEP("projection backward (f32) launch", launch_bwd_project_f32(z, mask, w, N, v, dz, s))
+  if (g) {
+    struct Sum { float* out; const float* U; const float* V; int O, K; };
+    const Sum sums[10] = {{g->w_g, v.dgg, v.zh, Cz, Cz},       {g->w_o, v.dy, v.xh, Cz, Ch},
+                          {g->w_a, v.dpa, v.zh, Ch, Cz},       {g->w_ga, v.dga, v.zh, Ch, Cz},
+                          {g->w_b, v.dpb, v.zh, Ch, Cz},       {g->w_gb, v.dgb, v.zh, Ch, Cz},
+                          {g->ln_out_gamma, v.q_out_n, nullptr, Ch, 1}, {g->ln_out_beta, v.q_out, nullptr, Ch, 1},
+                          {g->ln_in_gamma, v.q_in_n, nullptr, Cz, 1},   {g->ln_in_beta, v.q_in, nullptr, Cz, 1}};
+    for (const Sum& t : sums) {
+      if (!t.out) continue;
+      TM_F32_STEP("parameter gradient (f32) launch", launch_outer_sum_f32(t.U, t.V, t.O, t.K, P, partial, t.out, s))
+    }
+  }
+#undef TM_F32_STEP
+  return TM_OK;
+}
+
+tm_status backward_bf16(tm_ctx* c, const void* z, const float* mask, int N, bool inc, const void* dout, void* dz,
+                        const tm_grads* g, cudaStream_t s, const tm_options* opt) {
+  return fail(c, TM_ERR_UNSUPPORTED, "bf16 backward pending");
+}
+
 }  // namespace
 
 // ====================================================================== C ABI
@@ -798,6 +890,40 @@ tm_status tm_forward_host(tm_ctx* c, const void* z_host, const float* mask_host,
   if (st != TM_OK) return st;
   e = cudaMemcpyAsync(out_host, od, zbytes, cudaMemcpyDeviceToHost, s);
   return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "cudaMemcpyAsync(device to host)");
+}
+
+tm_status tm_backward(tm_ctx* c, const void* z, const float* mask, int N, tm_dtype dtype, tm_direction dir,
+                      const void* dout, void* dz, const tm_grads* grads, void* stream, const tm_options* opt) {
+  tm_status st = check_common(c, N, dtype);
+  if (st != TM_OK) return st;
+  if (dir != TM_OUTGOING && dir != TM_INCOMING) return fail(c, TM_ERR_INVALID, "unknown direction %d", (int)dir);
+  if (!z || !dout || !dz || !aligned16(z) || !aligned16(dout) || !aligned16(dz))
+    return fail(c, TM_ERR_INVALID, "z, dout and dz must be non-null and 16-byte aligned");
+  if (mask && (reinterpret_cast<uintptr_t>(mask) & 3u)) return fail(c, TM_ERR_INVALID, "mask must be 4-byte aligned");
+  if (opt) {
+    for (int r : opt->reserved)
+      if (r) return fail(c, TM_ERR_INVALID, "tm_options.reserved must be zero");
+    if (opt->block || opt->x_storage || opt->residual)
+      return fail(c, TM_ERR_INVALID, "tm_backward takes no block, x_storage or residual option");
+    if (opt->timeout_ms < 0) return fail(c, TM_ERR_INVALID, "negative option");
+  }
+  if (grads) {
+    const float* gp[10] = {grads->ln_in_gamma, grads->ln_in_beta, grads->w_a, grads->w_ga, grads->w_b,
+                           grads->w_gb, grads->w_g, grads->ln_out_gamma, grads->ln_out_beta, grads->w_o};
+    for (const float* q : gp)
+      if (q && (reinterpret_cast<uintptr_t>(q) & 15u))
+        return fail(c, TM_ERR_INVALID, "gradient arrays must be 16-byte aligned");
+  }
+  const size_t zbytes = (size_t)N * N * c->c_z * (dtype == TM_BF16 ? 2 : 4);
+  if (ranges_overlap(z, zbytes, dz, zbytes)) return fail(c, TM_ERR_INVALID, "dz overlaps z");
+  if (dz != dout && ranges_overlap(dout, zbytes, dz, zbytes))
+    return fail(c, TM_ERR_INVALID, "dz overlaps dout without being dout");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool inc = dir == TM_INCOMING;
+  if (dtype == TM_F32)
+    return backward_f32(c, reinterpret_cast<const float*>(z), mask, N, inc, reinterpret_cast<const float*>(dout),
+                        reinterpret_cast<float*>(dz), grads, s, opt);
+  return backward_bf16(c, z, mask, N, inc, dout, dz, grads, s, opt);
 }
 
 tm_status tm_sync_status(tm_ctx* c, void* stream) {

@@ -121,6 +121,29 @@ cudaError_t launch_finish_f32(const float* x, long long ldx, long long chan_stri
                               const F32Weights& w, int N, int i0, int j0, int bi, int bj, float* out,
                               bool residual, cudaStream_t s);
 
+// Backward pass (k_f32_backward.cu). Per-pair vectors are channel-major [c][N*N] (pair p = i*N + j);
+// the gradient planes dX, dXT, dA, dB are [c_h][N][ld].
+struct BwdF32Vectors {
+  float *dX, *dXT;                  // dL/dx and its per-channel transpose (output backward)
+  const float *dA, *dB;             // dL/da, dL/db (contraction gradients)
+  int ld;
+  float* dzh;                       // [c_z][P] dL/dzh: the gate's term, then the projections' terms
+  float *zh, *xh, *dy, *dgg;        // [c_z], [c_h], [c_z], [c_z] x [P]
+  float *q_out_n, *q_out;           // [c_h][P] dxh * n_x and dxh
+  float *dpa, *dga, *dpb, *dgb;     // [c_h][P]
+  float *q_in_n, *q_in;             // [c_z][P] dzh * n_z and dzh
+};
+constexpr int kOuterSumMaxSplits = 512;
+cudaError_t launch_bwd_output_f32(const float* x, long long ldx, const float* z, const float* dout,
+                                  const F32Weights& w, int N, const BwdF32Vectors& v, cudaStream_t s);
+cudaError_t launch_bwd_project_f32(const float* z, const float* mask, const F32Weights& w, int N,
+                                   const BwdF32Vectors& v, float* dz, cudaStream_t s);
+// out[o][k] = sum_p U[o][p] V[k][p] (V == nullptr: K = 1, V = 1) through outer_sum_splits(P) fixed-order
+// partial sums in part [splits][O][K].
+int outer_sum_splits(long long P);
+cudaError_t launch_outer_sum_f32(const float* U, const float* V, int O, int K, long long P, float* part,
+                                 float* out, cudaStream_t s);
+
 // ----------------------------------------------------------------- diagnostics
 enum : int { KID_SELFTEST = 9 };
 cudaError_t launch_watchdog_selftest(const Watch& w, cudaStream_t s);

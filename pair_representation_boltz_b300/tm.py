@@ -7,7 +7,7 @@ streams only. There is no fallback: without the built library or without a
 GPU every call raises.
 
 The function names mirror the C ABI: tm_create, tm_forward, tm_forward_ex, tm_forward_host,
-tm_forward_noalloc, tm_pair_update,
+tm_forward_noalloc, tm_pair_update, tm_backward,
 tm_project, tm_contract, tm_finish, tm_sync_status, tm_watchdog_selftest, tm_set_timing,
 tm_get_timing, tm_launch_count, tm_workspace_bytes, tm_status_string,
 tm_last_error, tm_destroy. ``TriMul`` wraps a context for convenience.
@@ -47,7 +47,11 @@ class TmOptions(C.Structure):
 
 
 class TmTiming(C.Structure):
-    _fields_ = [("launches", C.c_int * 4), ("ms", C.c_double * 4), ("units", C.c_longlong * 4)]
+    _fields_ = [("launches", C.c_int * 8), ("ms", C.c_double * 8), ("units", C.c_longlong * 8)]
+
+
+class TmGrads(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in WEIGHT_FIELDS]
 
 
 class TmError(RuntimeError):
@@ -79,6 +83,7 @@ def load_library(path: str = LIB_PATH):
         "tm_project": (st, [vp, vp, vp, i, i, vp, vp, i, vp]),
         "tm_contract": (st, [vp, vp, vp, i, i, i, i, i, i, i, i, vp, i, vp]),
         "tm_finish": (st, [vp, vp, i, vp, i, i, i, i, i, i, vp, vp]),
+        "tm_backward": (st, [vp, vp, vp, i, i, i, vp, vp, C.POINTER(TmGrads), vp, C.POINTER(TmOptions)]),
         "tm_sync_status": (st, [vp, vp]),
         "tm_watchdog_selftest": (st, [vp, i, vp]),
         "tm_set_timing": (st, [vp, i]),
@@ -242,6 +247,27 @@ def tm_finish(ctx, x, ldx, z, i0, j0, bi, bj, out, stream=None):
                                          _stream(stream)))
 
 
+def tm_backward(ctx, z, mask, direction, dout, dz, grads=None, stream=None, timeout_ms=0, workspace_limit=0):
+    """dz = dL/dz and grads[name] = dL/dW for the cotangent dout of out = update(z).
+
+    grads: dict of contiguous float32 CUDA tensors keyed by parameter name (a missing key is not
+    written), or None. dz may be dout itself."""
+    N = z.shape[0]
+    g = None
+    if grads is not None:
+        g = TmGrads(*[_ptr(grads[n]) if n in grads else None for n in WEIGHT_FIELDS])
+        for n, t in grads.items():
+            if n not in WEIGHT_FIELDS:
+                raise KeyError(f"unknown parameter {n!r}")
+            if str(t.dtype) != "torch.float32":
+                raise TypeError(f"gradient {n} must be float32")
+    opt = TmOptions(0, timeout_ms, workspace_limit, 0, 0)
+    _check(ctx, load_library().tm_backward(ctx, _ptr(z), _ptr(mask), N, _dtype_code(z), _direction(direction),
+                                           _ptr(dout), _ptr(dz), C.byref(g) if g is not None else None,
+                                           _stream(stream), C.byref(opt)))
+    return dz
+
+
 def tm_sync_status(ctx, stream=None) -> int:
     return load_library().tm_sync_status(ctx, _stream(stream))
 
@@ -257,7 +283,7 @@ def tm_set_timing(ctx, enable: bool) -> None:
 def tm_get_timing(ctx) -> dict:
     t = TmTiming()
     _check(ctx, load_library().tm_get_timing(ctx, C.byref(t)))
-    names = ("project", "contract", "finish", "f32")
+    names = ("project", "contract", "finish", "f32", "out_backward", "proj_backward", "aux_backward", "unused")
     return {n: {"launches": t.launches[k], "ms": t.ms[k], "units": t.units[k]} for k, n in enumerate(names)}
 
 
@@ -285,6 +311,21 @@ class TriMul:
         if opts:
             return tm_forward_ex(self.ctx, z, mask, direction, out, stream, **opts)
         return tm_forward(self.ctx, z, mask, direction, out, stream)
+
+    def backward(self, z, dout, mask=None, direction="outgoing", dz=None, stream=None, **opts):
+        """(dz, grads): the gradient of sum(dout * self(z, mask, direction)) with respect to z and to
+        every parameter (a dict of float32 CUDA tensors in the parameters' shapes)."""
+        import torch
+        if dz is None:
+            dz = torch.empty_like(z)
+        shapes = {"ln_in_gamma": (self.c_z,), "ln_in_beta": (self.c_z,), "w_a": (self.c_hidden, self.c_z),
+                  "w_ga": (self.c_hidden, self.c_z), "w_b": (self.c_hidden, self.c_z),
+                  "w_gb": (self.c_hidden, self.c_z), "w_g": (self.c_z, self.c_z),
+                  "ln_out_gamma": (self.c_hidden,), "ln_out_beta": (self.c_hidden,),
+                  "w_o": (self.c_z, self.c_hidden)}
+        grads = {n: torch.empty(shp, dtype=torch.float32, device=z.device) for n, shp in shapes.items()}
+        tm_backward(self.ctx, z, mask, direction, dout, dz, grads, stream, **opts)
+        return dz, grads
 
     def close(self):
         if self.ctx:

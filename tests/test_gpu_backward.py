@@ -1,0 +1,126 @@
+"""The backward pass through the C ABI (tm_backward) against the float64 oracle of the gradient.
+
+The metric of each gradient (dz and every parameter) is max|got - ref| / rms(ref) over all of its
+values, with ref the oracle's gradient for the same inputs and cotangent. Bounds:
+  * float32 path: F32_GRAD_TOL. Its arithmetic is the forward's (max_rel ~2e-6) followed by the
+    chain rule in float32 and sums over the N^2 pairs for the parameters; a float32 sum of P terms
+    errs by about sqrt(P) u sum|terms| (u = 2^-24) with independent rounding errors, 3e-6 at
+    P = 2304, and at most P u = 1.4e-4 in the worst case. Measured: <= 9.1e-6 on every gradient;
+    the bound takes five times that;
+  * bf16 path: BF16_GRAD_TOL, from the bf16 operands: a, b (stored bf16, as the forward stores
+    them), dX, the per-pair operands of the gradient's products (zh, x-hat, dy, dgg, dpa, dga, dpb,
+    dgb) are each rounded once to 8 significant bits (relative error <= 2^-9 = 2e-3), and dz is
+    stored bf16; errors of independent roundings add in quadrature in each float32-accumulated
+    product, so a few times 2e-3 bounds the worst element relative to the rms, with the sampled
+    worst case over N^2 c values above the typical one.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from tests.gpu_util import mask_to_device, to_f64, z_to_device
+
+pytestmark = pytest.mark.gpu
+
+F32_GRAD_TOL = 5e-5
+BF16_GRAD_TOL = 3e-2
+
+
+@pytest.fixture(scope="module")
+def torch_tm():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    from pair_representation_boltz_b300 import build, tm
+    build.build()
+    return torch, tm
+
+
+def _metrics(got, ref):
+    out = {}
+    for k, r in ref.items():
+        g = got[k]
+        rms = float(np.sqrt(np.mean(r * r))) or 1.0
+        out[k] = float(np.max(np.abs(g - r)) / rms)
+    return out
+
+
+def _log(name, metrics):
+    log = os.environ.get("TM_METRICS_LOG")
+    if log:
+        with open(log, "a") as f:
+            f.write(json.dumps({"test": name, **metrics}) + "\n")
+
+
+def _run(torch, tm, W, c_z, c_h, z_np, m_np, dout_np, direction, dtype):
+    mod = tm.TriMul(c_z, c_h, W)
+    try:
+        z = z_to_device(z_np)
+        dout = z_to_device(dout_np)
+        m = mask_to_device(m_np) if m_np is not None else None
+        dz, grads = mod.backward(z, dout, m, direction)
+        torch.cuda.synchronize()
+        assert tm.tm_sync_status(mod.ctx) == tm.TM_OK
+        got = {"z": to_f64(dz)}
+        got.update({k: v.double().cpu().numpy() for k, v in grads.items()})
+        return got
+    finally:
+        mod.close()
+
+
+def _dout(N, c, seed, dtype):
+    d = np.random.default_rng(seed).standard_normal((N, N, c)).astype(np.float32)
+    return wl.f32_to_bf16_bits(d) if dtype == "bf16" else d
+
+
+@pytest.mark.parametrize("direction", ("outgoing", "incoming"))
+def test_backward_f32_tiny48(torch_tm, direction):
+    torch, tm = torch_tm
+    w = wl.WORKLOADS["tiny48"]
+    W = wl.make_weights(w.c_z, w.c_h, w.seed_w, ln_random=True)
+    z = wl.make_z(w.N, w.c_z, w.seed_z, "f32")
+    m = wl.make_mask(w.N, w.mask)
+    dout = _dout(w.N, w.c_z, 5, "f32")
+    got = _run(torch, tm, W, w.c_z, w.c_h, z, m, dout, direction, "f32")
+    ref = oracle.full_backward(wl.as_f64(z), m, W, direction, dout.astype(np.float64))
+    met = _metrics(got, ref)
+    _log(f"f32_tiny48_{direction}", met)
+    assert max(met.values()) <= F32_GRAD_TOL, met
+
+
+@pytest.mark.parametrize("direction", ("outgoing", "incoming"))
+def test_backward_f32_c128_ragged(torch_tm, direction):
+    torch, tm = torch_tm
+    N = 37
+    W = wl.make_weights(128, 128, 3, ln_random=True)
+    z = wl.make_z(N, 128, 7, "f32")
+    m = wl.make_mask(N, "scatter", 8)
+    dout = _dout(N, 128, 9, "f32")
+    got = _run(torch, tm, W, 128, 128, z, m, dout, direction, "f32")
+    ref = oracle.full_backward(wl.as_f64(z), m, W, direction, dout.astype(np.float64))
+    met = _metrics(got, ref)
+    _log(f"f32_c128_N37_{direction}", met)
+    assert max(met.values()) <= F32_GRAD_TOL, met
+
+
+def test_backward_in_place_and_without_parameter_gradients(torch_tm):
+    torch, tm = torch_tm
+    N, c = 20, 12
+    W = wl.make_weights(c, 9, 4, ln_random=True)
+    mod = tm.TriMul(c, 9, W)
+    try:
+        z = z_to_device(wl.make_z(N, c, 1, "f32"))
+        dout = z_to_device(_dout(N, c, 2, "f32"))
+        dz, _ = mod.backward(z, dout, None, "incoming")
+        inplace = dout.clone()
+        tm.tm_backward(mod.ctx, z, None, "incoming", inplace, inplace, None)
+        torch.cuda.synchronize()
+        assert torch.equal(inplace, dz)
+        with pytest.raises(tm.TmError):
+            tm.tm_backward(mod.ctx, z, None, "incoming", dout, z, None)      # dz over z
+    finally:
+        mod.close()
