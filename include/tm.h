@@ -207,9 +207,10 @@ typedef struct {
  * float32, and its contractions of the gradient (dX with b and a, the
  * per-pair W^T products, the parameter sums over N^2 pairs) run on the tensor
  * cores from bf16 operands with float32 accumulation; dA and dB are float32.
- * Workspace: about (4 c_h (2 + 4) + 4 c_z) N^2 bytes for TM_BF16
- * (33 GB at N = 3605) -- beyond the workspace limit it returns TM_ERR_OOM before
- * any launch. opt: timeout_ms and workspace_limit apply; block, x_storage and
+ * Workspace for TM_BF16: about 2.6 kB per pair (a, b, dX, dX^T in bf16; x
+ * then dA, and dB in float32; dzh in float32): 33 GB at N = 3605, 109 GB at
+ * N = 6500. Beyond the workspace limit it returns TM_ERR_OOM before any
+ * launch. opt: timeout_ms and workspace_limit apply; block, x_storage and
  * residual must be 0. Stream-ordered like tm_forward. */
 tm_status tm_backward(tm_ctx* ctx, const void* z, const float* mask, int N, tm_dtype dtype,
                       tm_direction dir, const void* dout, void* dz, const tm_grads* grads,

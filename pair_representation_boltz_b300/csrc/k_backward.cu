@@ -1,0 +1,594 @@
+// k_backward.cu -- tensor-core (tcgen05) kernels of the bf16 backward pass, c_z = c_h = 128.
+//
+// The backward pass of the triangle multiplicative update (the layer of the code-sample section of
+// "NVIDIA BioNeMo escala modelagem biomolecular com context parallelism e quebra barreira de
+// memória da GPU", trained at larger crops as that page's section "A pegadinha" asks) is the chain
+// rule through its steps in reverse. Two per-pair stages bracket the contraction gradients:
+//
+//   output backward (k_bwd_output), per pair p = (i, j):
+//     zh = LN_in(z), xh = LN_out(x);  gg = W_g zh, y = W_o xh            [MMA 1: A = zh, xh]
+//     dy = dout sigmoid(gg),  dgg = dout y sigmoid'(gg)
+//     dxh = W_o^T dy,  dzh_g = W_g^T dgg                                  [MMA 2: A = dy, dgg]
+//     dW_g += dgg zh^T,  dW_o += dy xh^T   (summed over the CTA's pairs)   [MMA 3, TMEM-resident]
+//     dx = LN_out backward of dxh -> dX (bf16, channel-major), d(gamma_out), d(beta_out)
+//   projection backward (k_bwd_project), per pair p = (i, k), once for a and once for b:
+//     pv = W_v zh, pg = W_gt zh                                            [MMA 1: A = zh]
+//     dpv = dV sigmoid(pg) m_i m_k,  dpg = dV pv m_i m_k sigmoid'(pg)     (dV = dA or dB)
+//     dzh += W_v^T dpv + W_gt^T dpg                                       [MMA 2]
+//     dW_v += dpv zh^T,  dW_gt += dpg zh^T                                [MMA 3, TMEM-resident]
+//     second launch: dz = LN_in backward of dzh, d(gamma_in), d(beta_in)
+//
+// Layout. One CTA of 128 threads per SM, persistent over tiles of 128 consecutive pairs of the
+// flattened N x N grid; thread t owns pair (tile * 128 + t) and TMEM lane t. Per-pair operands are
+// written by their thread into 128 x 128 bf16 shared-memory tiles in the 128-byte-swizzled K-major
+// layout (pair rows, channel columns). The same bytes serve MMA 1 and 2 as K-major operands (K =
+// channels) and MMA 3 as MN-major operands (K = pairs): a 128-byte row of 64 channels of one pair is
+// one K-major row and, read the other way, one MN-major row of 64 M (or N) elements at one K index.
+// Weights are plain bf16 [out][in] images in the same layout; MMA 1 reads them K-major (B = W,
+// N = out), MMA 2 MN-major (B = W^T, N = in, K = out). TMEM: columns 0..255 hold MMA 1's two
+// results and then MMA 2's; columns 256..511 accumulate the two parameter gradients of MMA 3 over
+// every tile of the CTA, written out once as per-CTA partial sums (added in fixed order later).
+#include "tm_kernels.h"
+
+namespace tmk {
+namespace {
+
+constexpr int BT = 128;                 // pairs per tile = threads per CTA
+constexpr uint32_t TILE = 128 * 128 * 2;  // bytes of one 128 x 128 bf16 operand tile
+constexpr uint32_t SLAB = TILE / 2;       // one 64-channel half
+
+struct alignas(1024) OutSmem {
+  uint8_t zh[TILE], xh[TILE], dy[TILE], dgg[TILE], wg[TILE], wo[TILE];
+  float ln[4 * kC];                     // gamma_in, beta_in, gamma_out, beta_out
+  float red[4][2 * kC];                 // per-warp channel sums, reduced at the end
+  uint64_t bar;
+  uint32_t tmem_slot;
+  int abort_flag;
+};
+
+struct alignas(1024) ProjSmem {
+  uint8_t zh[TILE], dv[TILE], dg[TILE], wv[TILE], wgt[TILE];
+  float ln[2 * kC];                     // gamma_in, beta_in
+  float red[4][2 * kC];
+  uint64_t bar;
+  uint32_t tmem_slot;
+  int abort_flag;
+};
+
+// 8 floats -> one 16-byte unit of row `r` of an operand tile, for channels c0 .. c0+7 (c0 % 8 == 0)
+__device__ __forceinline__ void put8(uint8_t* tile, int r, int c0, const float* v) {
+  const uint4 q = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                             pack_bf16x2(v[6], v[7]));
+  *reinterpret_cast<uint4*>(tile + (c0 >> 6) * SLAB + sw128_offset((uint32_t)r, (uint32_t)((c0 & 63) >> 3))) = q;
+}
+
+__device__ __forceinline__ void bf16x8_to_float(const uint4& q, float* f) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    f[2 * k] = __uint_as_float(w[k] << 16);
+    f[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+  }
+}
+
+// Copy a weight image (already in the tile layout) into shared memory, 128 threads.
+__device__ __forceinline__ void copy_tile(uint8_t* dst, const __nv_bfloat16* src) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll 4
+  for (int k = threadIdx.x; k < (int)(TILE / 16); k += BT) d[k] = s[k];
+}
+
+// Butterfly reduce-scatter over the 32 lanes of a warp: on return lane l holds the sum over the
+// lanes of v[l] (v is consumed).
+__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int half = 16; half >= 1; half >>= 1) {
+    const bool upper = (lane & half) != 0;
+#pragma unroll
+    for (int k = 0; k < half; ++k) {
+      const float keep = upper ? v[k + half] : v[k];
+      const float send = upper ? v[k] : v[k + half];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, half);
+    }
+  }
+  return v[0];
+}
+
+// Issue helpers (one thread). K-major operand of a 128 x 128 tile: K = channels; MN-major operand:
+// K = the tile's rows (pairs, or the out index of a weight image).
+__device__ __forceinline__ uint64_t kdesc(uint32_t base, int ks) {
+  return make_sdesc_sw128(base + (uint32_t)((ks >> 2) * SLAB + (ks & 3) * 32), 16, 1024);
+}
+__device__ __forceinline__ uint64_t mndesc(uint32_t base, int ks) {
+  return make_sdesc_sw128(base + (uint32_t)ks * 2048u, SLAB, 1024);
+}
+constexpr uint32_t ID_KK = make_idesc(128, 128, FMT_BF16, false, false);
+constexpr uint32_t ID_KM = make_idesc(128, 128, FMT_BF16, false, true);
+constexpr uint32_t ID_MM = make_idesc(128, 128, FMT_BF16, true, true);
+
+// D (+)= A B^T over the 128 K of two tiles
+__device__ __forceinline__ void mma_tile(uint32_t d, uint32_t a, bool a_mn, uint32_t b, bool b_mn, uint32_t idesc,
+                                         bool acc) {
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks)
+    mma_f16(d, a_mn ? mndesc(a, ks) : kdesc(a, ks), b_mn ? mndesc(b, ks) : kdesc(b, ks), idesc,
+            (acc || ks != 0) ? 1u : 0u);
+}
+
+// Wait for the MMA barrier with a CTA-uniform outcome.
+__device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, const Watch& w, int* abort_flag, int site) {
+  const bool ok = wait_bounded(bar, parity, w, abort_flag, site);
+  return __syncthreads_and(ok) != 0;
+}
+
+}  // namespace
+
+namespace {
+
+__device__ __forceinline__ void zh_row(uint8_t* tile, const float* ln_g, const float* ln_b, const __nv_bfloat16* z,
+                                       const float2* zstat, long long pr, bool valid) {
+  const float2 st = valid ? zstat[pr] : make_float2(0.f, 0.f);
+  const uint4* zrow = reinterpret_cast<const uint4*>(z + pr * kC);
+#pragma unroll 2
+  for (int u = 0; u < 16; ++u) {
+    float f[8];
+    if (valid) {
+      bf16x8_to_float(zrow[u], f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] = ln_g[8 * u + e] * fmaf(f[e], st.x, st.y) + ln_b[8 * u + e];
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] = 0.f;
+    }
+    put8(tile, threadIdx.x, 8 * u, f);
+  }
+}
+
+__global__ void __launch_bounds__(BT, 1) k_bwd_output(const BwdOutParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  OutSmem& sm = *reinterpret_cast<OutSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    mbar_init(&sm.bar, 1);
+    sm.abort_flag = 0;
+    fence_mbar_init();
+  }
+  for (int k = tid; k < 4 * kC; k += BT) sm.ln[k] = p.ln[k];
+  copy_tile(sm.wg, p.w_g);
+  copy_tile(sm.wo, p.w_o);
+  if (warp == 0) {
+    tmem_alloc(&sm.tmem_slot, 512);
+    tmem_relinquish();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_slot;
+  const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+  const float *g_in = sm.ln, *b_in = sm.ln + kC, *g_out = sm.ln + 2 * kC, *b_out = sm.ln + 3 * kC;
+  const uint32_t a_zh = smem_u32(sm.zh), a_xh = smem_u32(sm.xh), a_dy = smem_u32(sm.dy), a_dgg = smem_u32(sm.dgg);
+  const uint32_t a_wg = smem_u32(sm.wg), a_wo = smem_u32(sm.wo);
+
+  float acc_g[4] = {0.f, 0.f, 0.f, 0.f}, acc_b[4] = {0.f, 0.f, 0.f, 0.f};
+  uint32_t phase = 0;
+  int local = 0;
+  bool ok = true;
+  for (long long t = blockIdx.x; t < p.tiles; t += gridDim.x, ++local) {
+    const long long pr = t * BT + tid;
+    const bool valid = pr < p.P;
+    const int i = valid ? (int)(pr / p.N) : 0;
+    const int j = valid ? (int)(pr - (long long)i * p.N) : 0;
+    const float* xp = p.x + (long long)i * p.ldx + j;
+
+    // ---- operands of MMA 1: zh and xh = LN_out(x) (shifted one-pass statistics of x)
+    zh_row(sm.zh, g_in, b_in, p.z, p.zstat, pr, valid);
+    float mu = 0.f, rx = 0.f;
+    if (valid) {
+      const float k0 = xp[0];
+      float s1 = 0.f, s2 = 0.f;
+#pragma unroll 8
+      for (int c = 0; c < kC; ++c) {
+        const float d = xp[c * p.xplane] - k0;
+        s1 += d;
+        s2 = fmaf(d, d, s2);
+      }
+      const float m1 = s1 * (1.f / kC);
+      mu = k0 + m1;
+      rx = rsqrtf(fmaxf(s2 * (1.f / kC) - m1 * m1, 0.f) + 1e-5f);
+    }
+#pragma unroll 2
+    for (int u = 0; u < 16; ++u) {
+      float f[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int c = 8 * u + e;
+        f[e] = valid ? g_out[c] * ((xp[c * p.xplane] - mu) * rx) + b_out[c] : 0.f;
+      }
+      put8(sm.xh, tid, 8 * u, f);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      mma_tile(tmem, a_zh, false, a_wg, false, ID_KK, false);         // gg = W_g zh
+      mma_tile(tmem + kC, a_xh, false, a_wo, false, ID_KK, false);    // y  = W_o xh
+      mma_commit(&sm.bar);
+    }
+    if (!cta_wait(&sm.bar, phase, p.w, &sm.abort_flag, 1)) { ok = false; break; }
+    phase ^= 1u;
+    tc_fence_after();
+
+    // ---- dy = dout g, dgg = dout y g (1 - g): operands of MMA 2 and 3
+    const uint4* drow = reinterpret_cast<const uint4*>(p.dout + pr * kC);
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {
+      uint32_t rg[32], ry[32];
+      tmem_ld32(trow + 32 * q, rg);
+      tmem_ld32(trow + kC + 32 * q, ry);
+      tmem_ld_wait();
+      float d[32];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (valid) bf16x8_to_float(drow[4 * q + u], d + 8 * u);
+        else
+#pragma unroll
+          for (int e = 0; e < 8; ++e) d[8 * u + e] = 0.f;
+      }
+      float vy[32], vg[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const float s = sigmoid_mufu(__uint_as_float(rg[e]));
+        vy[e] = d[e] * s;
+        vg[e] = d[e] * __uint_as_float(ry[e]) * s * (1.f - s);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        put8(sm.dy, tid, 32 * q + 8 * u, vy + 8 * u);
+        put8(sm.dgg, tid, 32 * q + 8 * u, vg + 8 * u);
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      mma_tile(tmem, a_dy, false, a_wo, true, ID_KM, false);              // dxh   = W_o^T dy
+      mma_tile(tmem + kC, a_dgg, false, a_wg, true, ID_KM, false);        // dzh_g = W_g^T dgg
+      mma_tile(tmem + 2 * kC, a_dgg, true, a_zh, true, ID_MM, local > 0); // dW_g += dgg zh^T
+      mma_tile(tmem + 3 * kC, a_dy, true, a_xh, true, ID_MM, local > 0);  // dW_o += dy xh^T
+      mma_commit(&sm.bar);
+    }
+    if (!cta_wait(&sm.bar, phase, p.w, &sm.abort_flag, 2)) { ok = false; break; }
+    phase ^= 1u;
+    tc_fence_after();
+
+    // ---- dzh_g out; LayerNorm_out backward of dxh -> dX
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {
+      uint32_t r[32];
+      tmem_ld32(trow + kC + 32 * q, r);
+      tmem_ld_wait();
+      if (valid)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) p.dzh[(long long)(32 * q + e) * p.P + pr] = __uint_as_float(r[e]);
+    }
+    float s1 = 0.f, s2 = 0.f;
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {
+      uint32_t r[32];
+      tmem_ld32(trow + 32 * q, r);
+      tmem_ld_wait();
+      float vn[32], vd[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int c = 32 * q + e;
+        const float n = valid ? (xp[c * p.xplane] - mu) * rx : 0.f;
+        const float dxh = valid ? __uint_as_float(r[e]) : 0.f;
+        const float dn = dxh * g_out[c];
+        s1 += dn;
+        s2 = fmaf(dn, n, s2);
+        vn[e] = dxh * n;
+        vd[e] = dxh;
+      }
+      acc_g[q] += reduce_scatter32(vn, lane);
+      acc_b[q] += reduce_scatter32(vd, lane);
+    }
+    s1 *= 1.f / kC;
+    s2 *= 1.f / kC;
+    __nv_bfloat16* dxp = p.dX + (long long)i * p.ld + j;
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {
+      uint32_t r[32];
+      tmem_ld32(trow + 32 * q, r);
+      tmem_ld_wait();
+      if (valid)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int c = 32 * q + e;
+          const float n = (xp[c * p.xplane] - mu) * rx;
+          dxp[c * p.dplane] = __float2bfloat16_rn(rx * (__uint_as_float(r[e]) * g_out[c] - s1 - n * s2));
+        }
+    }
+  }
+
+  // ---- per-CTA partial sums: d(gamma_out), d(beta_out) over the warps; dW_g, dW_o from TMEM
+  if (ok) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      sm.red[warp][32 * q + lane] = acc_g[q];
+      sm.red[warp][kC + 32 * q + lane] = acc_b[q];
+    }
+    __syncthreads();
+    for (int k = tid; k < 2 * kC; k += BT)
+      p.part_ln[(long long)blockIdx.x * 2 * kC + k] = ((sm.red[0][k] + sm.red[1][k]) + sm.red[2][k]) + sm.red[3][k];
+    float* pw = p.part_w + (long long)blockIdx.x * 2 * kC * kC + (long long)tid * kC;
+#pragma unroll 1
+    for (int m = 0; m < 2; ++m)
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        uint32_t r[32];
+        tmem_ld32(trow + (2 + m) * kC + 32 * q, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) pw[m * kC * kC + 32 * q + e] = local > 0 ? __uint_as_float(r[e]) : 0.f;
+      }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+namespace {
+
+__global__ void __launch_bounds__(BT, 1) k_bwd_project(const BwdProjParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  ProjSmem& sm = *reinterpret_cast<ProjSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    mbar_init(&sm.bar, 1);
+    sm.abort_flag = 0;
+    fence_mbar_init();
+  }
+  for (int k = tid; k < 2 * kC; k += BT) sm.ln[k] = p.ln[k];
+  copy_tile(sm.wv, p.w_v);
+  copy_tile(sm.wgt, p.w_gt);
+  if (warp == 0) {
+    tmem_alloc(&sm.tmem_slot, 512);
+    tmem_relinquish();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_slot;
+  const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+  const float *g_in = sm.ln, *b_in = sm.ln + kC;
+  const uint32_t a_zh = smem_u32(sm.zh), a_dv = smem_u32(sm.dv), a_dg = smem_u32(sm.dg);
+  const uint32_t a_wv = smem_u32(sm.wv), a_wgt = smem_u32(sm.wgt);
+
+  float acc_g[4] = {0.f, 0.f, 0.f, 0.f}, acc_b[4] = {0.f, 0.f, 0.f, 0.f};
+  uint32_t phase = 0;
+  int local = 0;
+  bool ok = true;
+  for (long long t = blockIdx.x; t < p.tiles; t += gridDim.x, ++local) {
+    const long long pr = t * BT + tid;
+    const bool valid = pr < p.P;
+    const int i = valid ? (int)(pr / p.N) : 0;
+    const int k2 = valid ? (int)(pr - (long long)i * p.N) : 0;
+
+    zh_row(sm.zh, g_in, b_in, p.z, p.zstat, pr, valid);
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      mma_tile(tmem, a_zh, false, a_wv, false, ID_KK, false);        // pv = W_v zh
+      mma_tile(tmem + kC, a_zh, false, a_wgt, false, ID_KK, false);  // pg = W_gt zh
+      mma_commit(&sm.bar);
+    }
+    if (!cta_wait(&sm.bar, phase, p.w, &sm.abort_flag, 1)) { ok = false; break; }
+    phase ^= 1u;
+    tc_fence_after();
+
+    // ---- gate backward: dpv = dV s m, dpg = dV pv m s (1 - s)
+    const float m = valid ? (p.mask ? p.mask[i] * p.mask[k2] : 1.f) : 0.f;
+    const float* vp = p.dV + (long long)i * p.ldv + k2;
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {
+      uint32_t rv[32], rg[32];
+      tmem_ld32(trow + 32 * q, rv);
+      tmem_ld32(trow + kC + 32 * q, rg);
+      tmem_ld_wait();
+      float fv[32], fg[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const float dv = valid ? vp[(32 * q + e) * p.vplane] * m : 0.f;
+        const float s = sigmoid_mufu(__uint_as_float(rg[e]));
+        fv[e] = dv * s;
+        fg[e] = dv * __uint_as_float(rv[e]) * s * (1.f - s);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        put8(sm.dv, tid, 32 * q + 8 * u, fv + 8 * u);
+        put8(sm.dg, tid, 32 * q + 8 * u, fg + 8 * u);
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      mma_tile(tmem, a_dv, false, a_wv, true, ID_KM, false);               // W_v^T dpv
+      mma_tile(tmem, a_dg, false, a_wgt, true, ID_KM, true);               //  + W_gt^T dpg
+      mma_tile(tmem + 2 * kC, a_dv, true, a_zh, true, ID_MM, local > 0);   // dW_v  += dpv zh^T
+      mma_tile(tmem + 3 * kC, a_dg, true, a_zh, true, ID_MM, local > 0);   // dW_gt += dpg zh^T
+      mma_commit(&sm.bar);
+    }
+    if (!cta_wait(&sm.bar, phase, p.w, &sm.abort_flag, 2)) { ok = false; break; }
+    phase ^= 1u;
+    tc_fence_after();
+
+    if (!p.final_pass) {
+      // dzh += this side's term
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        uint32_t r[32];
+        tmem_ld32(trow + 32 * q, r);
+        tmem_ld_wait();
+        if (valid)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            float* d = p.dzh + (long long)(32 * q + e) * p.P + pr;
+            *d = *d + __uint_as_float(r[e]);
+          }
+      }
+    } else {
+      // dzh (all terms) -> LayerNorm_in backward -> dz; n = z rstd - rstd mu from the statistics
+      const float2 st = valid ? p.zstat[pr] : make_float2(0.f, 0.f);
+      const uint4* zrow = reinterpret_cast<const uint4*>(p.z + pr * kC);
+      float s1 = 0.f, s2 = 0.f;
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        uint32_t r[32];
+        tmem_ld32(trow + 32 * q, r);
+        tmem_ld_wait();
+        float zf[32];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (valid) bf16x8_to_float(zrow[4 * q + u], zf + 8 * u);
+          else
+#pragma unroll
+            for (int e = 0; e < 8; ++e) zf[8 * u + e] = 0.f;
+        }
+        float vn[32], vd[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int c = 32 * q + e;
+          const float dzh = valid ? p.dzh[(long long)c * p.P + pr] + __uint_as_float(r[e]) : 0.f;
+          const float n = fmaf(zf[e], st.x, st.y);
+          const float dn = dzh * g_in[c];
+          s1 += dn;
+          s2 = fmaf(dn, n, s2);
+          vn[e] = dzh * n;
+          vd[e] = dzh;
+        }
+        acc_g[q] += reduce_scatter32(vn, lane);
+        acc_b[q] += reduce_scatter32(vd, lane);
+      }
+      s1 *= 1.f / kC;
+      s2 *= 1.f / kC;
+      uint4* dzrow = reinterpret_cast<uint4*>(p.dz + pr * kC);
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        uint32_t r[32];
+        tmem_ld32(trow + 32 * q, r);
+        tmem_ld_wait();
+        if (!valid) continue;
+        float zf[32], out[32];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) bf16x8_to_float(zrow[4 * q + u], zf + 8 * u);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int c = 32 * q + e;
+          const float dzh = p.dzh[(long long)c * p.P + pr] + __uint_as_float(r[e]);
+          const float n = fmaf(zf[e], st.x, st.y);
+          out[e] = st.x * (dzh * g_in[c] - s1 - n * s2);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          dzrow[4 * q + u] = make_uint4(pack_bf16x2(out[8 * u], out[8 * u + 1]), pack_bf16x2(out[8 * u + 2], out[8 * u + 3]),
+                                        pack_bf16x2(out[8 * u + 4], out[8 * u + 5]), pack_bf16x2(out[8 * u + 6], out[8 * u + 7]));
+      }
+    }
+  }
+
+  if (ok) {
+    if (p.final_pass) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        sm.red[warp][32 * q + lane] = acc_g[q];
+        sm.red[warp][kC + 32 * q + lane] = acc_b[q];
+      }
+      __syncthreads();
+      for (int k = tid; k < 2 * kC; k += BT)
+        p.part_ln[(long long)blockIdx.x * 2 * kC + k] = ((sm.red[0][k] + sm.red[1][k]) + sm.red[2][k]) + sm.red[3][k];
+    }
+    float* pw = p.part_w + (long long)blockIdx.x * 2 * kC * kC + (long long)tid * kC;
+#pragma unroll 1
+    for (int m = 0; m < 2; ++m)
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        uint32_t r[32];
+        tmem_ld32(trow + (2 + m) * kC + 32 * q, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) pw[m * kC * kC + 32 * q + e] = local > 0 ? __uint_as_float(r[e]) : 0.f;
+      }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// out[c][j][i] = in[c][i][j] for i, j < N (bf16 planes [128][N][ld]); 64 x 64 tiles, 2 elements per thread
+__global__ void __launch_bounds__(256) k_transpose_planes(const __nv_bfloat16* __restrict__ in,
+                                                          __nv_bfloat16* __restrict__ out, int N, long long ld,
+                                                          long long plane) {
+  __shared__ __nv_bfloat16 t[64][64 + 2];
+  const int c = blockIdx.z;
+  const int i0 = blockIdx.y * 64, j0 = blockIdx.x * 64;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8
+  const __nv_bfloat16* src = in + c * plane;
+  __nv_bfloat16* dst = out + c * plane;
+  for (int r = ty; r < 64; r += 8) {
+    const int i = i0 + r, j = j0 + 2 * tx;
+    __nv_bfloat16 v0 = __float2bfloat16_rn(0.f), v1 = v0;
+    if (i < N && j < N) v0 = src[(long long)i * ld + j];
+    if (i < N && j + 1 < N) v1 = src[(long long)i * ld + j + 1];
+    t[r][2 * tx] = v0;
+    t[r][2 * tx + 1] = v1;
+  }
+  __syncthreads();
+  for (int r = ty; r < 64; r += 8) {
+    const int j = j0 + r, i = i0 + 2 * tx;
+    if (j < N && i < N) dst[(long long)j * ld + i] = t[2 * tx][r];
+    if (j < N && i + 1 < N) dst[(long long)j * ld + i + 1] = t[2 * tx + 1][r];
+  }
+}
+
+}  // namespace
+
+constexpr size_t kOutSmemBytes = sizeof(OutSmem) + 1024;
+constexpr size_t kProjSmemBytes = sizeof(ProjSmem) + 1024;
+static_assert(kOutSmemBytes <= 232448, "output backward shared memory");
+static_assert(kProjSmemBytes <= 232448, "projection backward shared memory");
+
+int bwd_grid(long long tiles, int num_sms) { return (int)(tiles < num_sms ? tiles : num_sms); }
+
+cudaError_t launch_bwd_output_bf16(const BwdOutParams& p, int grid, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(k_bwd_output, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kOutSmemBytes);
+  if (e != cudaSuccess) return e;
+  k_bwd_output<<<grid, BT, kOutSmemBytes, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_project_bf16(const BwdProjParams& p, int grid, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(k_bwd_project, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kProjSmemBytes);
+  if (e != cudaSuccess) return e;
+  k_bwd_project<<<grid, BT, kProjSmemBytes, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_planes_bf16(const __nv_bfloat16* in, __nv_bfloat16* out, int N, long long ld, int planes,
+                                         cudaStream_t s) {
+  dim3 grid((N + 63) / 64, (N + 63) / 64, planes);
+  k_transpose_planes<<<grid, 256, 0, s>>>(in, out, N, ld, (long long)N * ld);
+  return cudaGetLastError();
+}
+
+}  // namespace tmk

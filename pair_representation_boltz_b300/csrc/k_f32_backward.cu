@@ -11,7 +11,7 @@
 //   projection backward (one thread per pair): the gate backward of a and b, the W^T products
 //     of dzh and LayerNorm_in backward -> dz;
 //   every parameter gradient is a sum over the N^2 pairs of an outer product of two per-pair
-//     vectors that the two per-pair kernels store channel-major: bwd_outer_sum_f32 forms it
+//     vectors that the two per-pair kernels store channel-major: outer_sum_f32 forms it
 //     in fixed-order partial sums (deterministic, no atomics).
 #include "tm_kernels.h"
 
@@ -184,11 +184,12 @@ __global__ void outer_sum_f32(const float* __restrict__ U, const float* __restri
   if (o < O && k < K) part[((long long)blockIdx.z * O + o) * K + k] = acc;
 }
 
-__global__ void sum_parts_f32(const float* __restrict__ part, int S, long long E, float* __restrict__ out) {
+__global__ void sum_parts_f32(const float* __restrict__ part, int S, long long E, long long stride,
+                              float* __restrict__ out) {
   const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= E) return;
   float s = 0.f;
-  for (int q = 0; q < S; ++q) s += part[q * E + e];
+  for (int q = 0; q < S; ++q) s += part[q * stride + e];
   out[e] = s;
 }
 
@@ -223,8 +224,11 @@ cudaError_t launch_outer_sum_f32(const float* U, const float* V, int O, int K, l
   outer_sum_f32<<<grid, block, 0, s>>>(U, V, O, K, P, chunk, part);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const long long E = (long long)O * K;
-  sum_parts_f32<<<(unsigned)((E + 255) / 256), 256, 0, s>>>(part, S, E, out);
+  return launch_sum_parts(part, S, (long long)O * K, (long long)O * K, out, s);
+}
+
+cudaError_t launch_sum_parts(const float* part, int S, long long E, long long stride, float* out, cudaStream_t s) {
+  sum_parts_f32<<<(unsigned)((E + 255) / 256), 256, 0, s>>>(part, S, E, stride, out);
   return cudaGetLastError();
 }
 

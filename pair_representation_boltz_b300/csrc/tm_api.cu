@@ -83,6 +83,9 @@ struct tm_ctx {
   double ab_bound = 0;           // max_c of the bounds on |a_c| and |b_c| multiplied (fp16 x scale)
   float inv_scale_o = 1.f;
   CUtensorMap wk1_map, wo_map, wg_map;
+  // backward pass: bf16 images of W_g, W_o, W_a, W_ga, W_b, W_gb in the 128 x 128 operand-tile layout
+  // of the backward kernels, then gamma_in, beta_in, gamma_out, beta_out (float32)
+  void* wbwd = nullptr;
   // status word (mapped host memory)
   int* status_h = nullptr;
   int* status_d = nullptr;
@@ -308,6 +311,34 @@ tm_status prepare_tensor_core_weights(tm_ctx* c, const tm_weights* w) {
   TM_UP(c->wo16, wo)
   TM_UP(c->wg16, wg)
 #undef TM_UP
+  {
+    // Backward images: W [out][in] as bf16 in the 128-byte-swizzled K-major tile layout the backward
+    // kernels copy straight into shared memory (64-column halves 16 KB apart, 128-byte rows, 16-byte
+    // unit u of row r at unit u ^ (r % 8)).
+    const float* src[6] = {w->w_g, w->w_o, w->w_a, w->w_ga, w->w_b, w->w_gb};
+    std::vector<__nv_bfloat16> img(6 * C * C);
+    for (int m = 0; m < 6; ++m)
+      for (int r = 0; r < C; ++r)
+        for (int k = 0; k < C; ++k) {
+          const int half = k / 64, u = (k % 64) / 8, e = k % 8;
+          const size_t byte = (size_t)half * (C * 64 * 2) + (size_t)r * 128 + (size_t)((u ^ (r & 7)) * 16) + e * 2;
+          img[(size_t)m * C * C + byte / 2] = __float2bfloat16_rn(src[m][(size_t)r * C + k]);
+        }
+    std::vector<float> ln(4 * C);
+    for (int k = 0; k < C; ++k) {
+      ln[k] = w->ln_in_gamma[k];
+      ln[C + k] = w->ln_in_beta[k];
+      ln[2 * C + k] = w->ln_out_gamma[k];
+      ln[3 * C + k] = w->ln_out_beta[k];
+    }
+    const size_t ib = img.size() * sizeof(img[0]);
+    err = cudaMalloc(&c->wbwd, ib + ln.size() * sizeof(float));
+    if (err != cudaSuccess) return cuda_fail(c, err, "cudaMalloc(backward weights)");
+    err = cudaMemcpy(c->wbwd, img.data(), ib, cudaMemcpyHostToDevice);
+    if (err == cudaSuccess)
+      err = cudaMemcpy(reinterpret_cast<uint8_t*>(c->wbwd) + ib, ln.data(), ln.size() * sizeof(float), cudaMemcpyHostToDevice);
+    if (err != cudaSuccess) return cuda_fail(c, err, "cudaMemcpy(backward weights)");
+  }
 
   {
     const cuuint64_t dims[2] = {(cuuint64_t)C, 1024};
@@ -589,7 +620,116 @@ tm_status backward_f32(tm_ctx* c, const float* z, const float* mask, int N, bool
 
 tm_status backward_bf16(tm_ctx* c, const void* z, const float* mask, int N, bool inc, const void* dout, void* dz,
                         const tm_grads* g, cudaStream_t s, const tm_options* opt) {
-  return fail(c, TM_ERR_UNSUPPORTED, "bf16 backward pending");
+  const long long P = (long long)N * N;
+  const int ld = (int)align_up(N, 64);     // bf16 planes a, b, dX, dX^T: 128-byte rows
+  const int ldx = (int)align_up(N, 32);    // float32 planes x (then dA), dB: 128-byte rows
+  const long long tiles = (P + 127) / 128;
+  const int grid = bwd_grid(tiles, c->num_sms);
+  const size_t pb = align_up((size_t)kC * N * ld * 2, 256);
+  const size_t xb = align_up((size_t)kC * N * ldx * 4, 256);
+  const size_t zb = align_up((size_t)P * sizeof(float2), 256);
+  const size_t hb = align_up((size_t)kC * P * 4, 256);
+  const size_t wb = align_up((size_t)grid * 2 * kC * kC * 4, 256);
+  const size_t lb = align_up((size_t)grid * 2 * kC * 4, 256);
+  tm_status st = ensure_workspace(c, 4 * pb + 2 * xb + zb + hb + 3 * wb + 2 * lb, s, opt);
+  if (st != TM_OK) return st;
+  uint8_t* q = reinterpret_cast<uint8_t*>(c->ws);
+  auto take = [&](size_t n) { uint8_t* r = q; q += n; return r; };
+  auto* a = reinterpret_cast<__nv_bfloat16*>(take(pb));
+  auto* b = reinterpret_cast<__nv_bfloat16*>(take(pb));
+  auto* dX = reinterpret_cast<__nv_bfloat16*>(take(pb));
+  auto* dXT = reinterpret_cast<__nv_bfloat16*>(take(pb));
+  float* x = reinterpret_cast<float*>(take(xb));     // x, then dA
+  float* dB = reinterpret_cast<float*>(take(xb));
+  auto* zstat = reinterpret_cast<float2*>(take(zb));
+  float* dzh = reinterpret_cast<float*>(take(hb));
+  float* part_o = reinterpret_cast<float*>(take(wb));
+  float* part_a = reinterpret_cast<float*>(take(wb));
+  float* part_b = reinterpret_cast<float*>(take(wb));
+  float* ln_o = reinterpret_cast<float*>(take(lb));
+  float* ln_i = reinterpret_cast<float*>(take(lb));
+  const auto* wimg = reinterpret_cast<const __nv_bfloat16*>(c->wbwd);
+  const float* ln4 = reinterpret_cast<const float*>(wimg + 6 * kC * kC);
+  auto W = [&](int m) { return wimg + (size_t)m * kC * kC; };   // W_g, W_o, W_a, W_ga, W_b, W_gb
+
+  st = run_project_bf16(c, z, mask, N, zstat, a, b, ld, s, opt);
+  if (st != TM_OK) return st;
+  st = run_contract_bf16(c, a, b, N, ld, inc, 0, 0, N, N, x, ldx, X_F32, 0, s, opt);
+  if (st != TM_OK) return st;
+
+  BwdOutParams po{};
+  po.z = reinterpret_cast<const __nv_bfloat16*>(z);
+  po.zstat = zstat;
+  po.x = x;
+  po.ldx = ldx;
+  po.xplane = (long long)N * ldx;
+  po.dout = reinterpret_cast<const __nv_bfloat16*>(dout);
+  po.dX = dX;
+  po.ld = ld;
+  po.dplane = (long long)N * ld;
+  po.dzh = dzh;
+  po.part_w = part_o;
+  po.part_ln = ln_o;
+  po.w_g = W(0);
+  po.w_o = W(1);
+  po.ln = ln4;
+  po.N = N;
+  po.P = P;
+  po.tiles = tiles;
+  po.w = watch(c, KID_BWD_OUTPUT, opt);
+  cudaError_t e = timed(c, 4, P, s, [&] { return launch_bwd_output_bf16(po, grid, s); });
+  if (e != cudaSuccess) return cuda_fail(c, e, "output backward launch");
+  e = timed(c, 6, P, s, [&] { return launch_transpose_planes_bf16(dX, dXT, N, ld, kC, s); });
+  if (e != cudaSuccess) return cuda_fail(c, e, "transpose launch");
+
+  float* dA = x;   // x is dead once the output backward has run
+  if (!inc) {
+    st = run_contract_bf16(c, dXT, b, N, ld, true, 0, 0, N, N, dA, ldx, X_F32, 0, s, opt);
+    if (st == TM_OK) st = run_contract_bf16(c, dX, a, N, ld, true, 0, 0, N, N, dB, ldx, X_F32, 0, s, opt);
+  } else {
+    st = run_contract_bf16(c, b, dX, N, ld, false, 0, 0, N, N, dA, ldx, X_F32, 0, s, opt);
+    if (st == TM_OK) st = run_contract_bf16(c, a, dXT, N, ld, false, 0, 0, N, N, dB, ldx, X_F32, 0, s, opt);
+  }
+  if (st != TM_OK) return st;
+
+  for (int side = 0; side < 2; ++side) {
+    BwdProjParams pp{};
+    pp.z = po.z;
+    pp.zstat = zstat;
+    pp.mask = mask;
+    pp.dV = side == 0 ? dA : dB;
+    pp.ldv = ldx;
+    pp.vplane = (long long)N * ldx;
+    pp.dzh = dzh;
+    pp.dz = reinterpret_cast<__nv_bfloat16*>(dz);
+    pp.final_pass = side;
+    pp.part_w = side == 0 ? part_a : part_b;
+    pp.part_ln = ln_i;
+    pp.w_v = W(2 + 2 * side);
+    pp.w_gt = W(3 + 2 * side);
+    pp.ln = ln4;
+    pp.N = N;
+    pp.P = P;
+    pp.tiles = tiles;
+    pp.w = watch(c, KID_BWD_PROJECT, opt);
+    e = timed(c, 5, P, s, [&] { return launch_bwd_project_bf16(pp, grid, s); });
+    if (e != cudaSuccess) return cuda_fail(c, e, "projection backward launch");
+  }
+  if (g) {
+    struct Sum { float* out; const float* part; long long E, stride; };
+    const long long WW = (long long)kC * kC;
+    const Sum sums[10] = {{g->w_g, part_o, WW, 2 * WW},       {g->w_o, part_o + WW, WW, 2 * WW},
+                          {g->w_a, part_a, WW, 2 * WW},       {g->w_ga, part_a + WW, WW, 2 * WW},
+                          {g->w_b, part_b, WW, 2 * WW},       {g->w_gb, part_b + WW, WW, 2 * WW},
+                          {g->ln_out_gamma, ln_o, kC, 2 * kC}, {g->ln_out_beta, ln_o + kC, kC, 2 * kC},
+                          {g->ln_in_gamma, ln_i, kC, 2 * kC},  {g->ln_in_beta, ln_i + kC, kC, 2 * kC}};
+    for (const Sum& t : sums) {
+      if (!t.out) continue;
+      e = timed(c, 6, 0, s, [&] { return launch_sum_parts(t.part, grid, t.E, t.stride, t.out, s); });
+      if (e != cudaSuccess) return cuda_fail(c, e, "parameter gradient sum launch");
+    }
+  }
+  return TM_OK;
 }
 
 }  // namespace
@@ -674,7 +814,7 @@ void tm_destroy(tm_ctx* c) {
   cudaDeviceSynchronize();
   if (c->ws) cudaFree(c->ws);
   if (c->io) cudaFree(c->io);
-  for (void* p : {(void*)c->w32, (void*)c->wk1, (void*)c->k1c, (void*)c->wo16, (void*)c->wg16})
+  for (void* p : {(void*)c->w32, (void*)c->wk1, (void*)c->k1c, (void*)c->wo16, (void*)c->wg16, c->wbwd})
     if (p) cudaFree(p);
   if (c->status_h) cudaFreeHost(c->status_h);
   for (auto& t : c->timed) {

@@ -144,6 +144,50 @@ int outer_sum_splits(long long P);
 cudaError_t launch_outer_sum_f32(const float* U, const float* V, int O, int K, long long P, float* part,
                                  float* out, cudaStream_t s);
 
+// Backward pass, bf16 tensor-core path (k_backward.cu). Pairs are taken in tiles of 128 consecutive
+// entries of the flattened grid (p = i * N + j); per-pair vectors are channel-major [128][N * N].
+struct BwdOutParams {
+  const __nv_bfloat16* z;         // [N][N][128]
+  const float2* zstat;            // [N][N] (rstd, -rstd mu) of LayerNorm_in (projection kernel)
+  const float* x;                 // [128][N][ldx] float32 (contraction kernel)
+  long long ldx, xplane;          // row and channel strides of x
+  const __nv_bfloat16* dout;      // [N][N][128]
+  __nv_bfloat16* dX;              // [128][N][ld] dL/dx
+  long long ld, dplane;
+  float* dzh;                     // [128][N*N] written: the gate's term of dL/dzh
+  float* part_w;                  // [grid][2][128][128] per-CTA sums of dW_g, dW_o
+  float* part_ln;                 // [grid][256] per-CTA sums of d(gamma_out), d(beta_out)
+  const __nv_bfloat16 *w_g, *w_o; // bf16 weight images in the 128-byte-swizzled tile layout
+  const float* ln;                // gamma_in, beta_in, gamma_out, beta_out (float32, 4 x 128)
+  int N;
+  long long P, tiles;
+  Watch w;
+};
+struct BwdProjParams {
+  const __nv_bfloat16* z;
+  const float2* zstat;
+  const float* mask;              // [N] or nullptr
+  const float* dV;                // [128][N][ldv] float32: dL/da or dL/db
+  long long ldv, vplane;
+  float* dzh;                     // [128][N*N], accumulated
+  __nv_bfloat16* dz;              // [N][N][128] (final pass)
+  int final_pass;                 // 1: add this side's term, then LayerNorm_in backward into dz
+  float* part_w;                  // [grid][2][128][128] per-CTA sums of dW_v, dW_gt
+  float* part_ln;                 // [grid][256] per-CTA sums of d(gamma_in), d(beta_in) (final pass)
+  const __nv_bfloat16 *w_v, *w_gt;
+  const float* ln;                // gamma_in, beta_in
+  int N;
+  long long P, tiles;
+  Watch w;
+};
+int bwd_grid(long long tiles, int num_sms);
+cudaError_t launch_bwd_output_bf16(const BwdOutParams& p, int grid, cudaStream_t s);
+cudaError_t launch_bwd_project_bf16(const BwdProjParams& p, int grid, cudaStream_t s);
+cudaError_t launch_transpose_planes_bf16(const __nv_bfloat16* in, __nv_bfloat16* out, int N, long long ld, int planes,
+                                         cudaStream_t s);
+// out[e] = sum over q < S of part[q * stride + e], e < E, in order q = 0, 1, ...
+cudaError_t launch_sum_parts(const float* part, int S, long long E, long long stride, float* out, cudaStream_t s);
+
 // ----------------------------------------------------------------- diagnostics
 enum : int { KID_SELFTEST = 9 };
 cudaError_t launch_watchdog_selftest(const Watch& w, cudaStream_t s);
