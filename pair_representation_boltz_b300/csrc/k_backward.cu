@@ -18,10 +18,13 @@
 //     dW_v += dpv zh^T,  dW_gt += dpg zh^T                                [MMA 3, TMEM-resident]
 //     second launch: dz = LN_in backward of dzh, d(gamma_in), d(beta_in)
 //
-// Layout. One CTA of 128 threads per SM, persistent over tiles of 128 consecutive pairs of the
-// flattened N x N grid; thread t owns pair (tile * 128 + t) and TMEM lane t. Per-pair operands are
-// written by their thread into 128 x 128 bf16 shared-memory tiles in the 128-byte-swizzled K-major
-// layout (pair rows, channel columns). The same bytes serve MMA 1 and 2 as K-major operands (K =
+// Layout. One CTA of 512 threads per SM, persistent over tiles of 128 consecutive pairs of the
+// flattened N x N grid. Warp w serves the 32 pairs of TMEM lane quarter w % 4 (the lanes it may
+// read) and channel quarter w / 4: each pair is handled by four threads of 32 channels each, so
+// that every warp's loads of a channel cover 32 consecutive pairs, and the LayerNorm statistics of a
+// pair are combined from its four quarters through shared memory. Per-pair operands are written
+// into 128 x 128 bf16 shared-memory tiles in the 128-byte-swizzled K-major layout (pair rows,
+// channel columns). The same bytes serve MMA 1 and 2 as K-major operands (K =
 // channels) and MMA 3 as MN-major operands (K = pairs): a 128-byte row of 64 channels of one pair is
 // one K-major row and, read the other way, one MN-major row of 64 M (or N) elements at one K index.
 // Weights are plain bf16 [out][in] images in the same layout; MMA 1 reads them K-major (B = W,
@@ -33,14 +36,17 @@
 namespace tmk {
 namespace {
 
-constexpr int BT = 128;                 // pairs per tile = threads per CTA
+constexpr int BT = 128;                 // pairs per tile
+constexpr int NT = 512;                 // threads per CTA: 4 per pair, 32 channels each
 constexpr uint32_t TILE = 128 * 128 * 2;  // bytes of one 128 x 128 bf16 operand tile
 constexpr uint32_t SLAB = TILE / 2;       // one 64-channel half
 
 struct alignas(1024) OutSmem {
   uint8_t zh[TILE], xh[TILE], dy[TILE], dgg[TILE], wg[TILE], wo[TILE];
   float ln[4 * kC];                     // gamma_in, beta_in, gamma_out, beta_out
-  float red[4][2 * kC];                 // per-warp channel sums, reduced at the end
+  float red[4][2 * kC];                 // channel sums of each lane quarter, reduced at the end
+  float2 xst[4][BT];                    // per channel quarter and pair: (mean, M2) of x
+  float2 sst[4][BT];                    // per channel quarter and pair: sums of the LayerNorm backward
   uint64_t bar;
   uint32_t tmem_slot;
   int abort_flag;
@@ -50,6 +56,7 @@ struct alignas(1024) ProjSmem {
   uint8_t zh[TILE], dv[TILE], dg[TILE], wv[TILE], wgt[TILE];
   float ln[2 * kC];                     // gamma_in, beta_in
   float red[4][2 * kC];
+  float2 sst[4][BT];
   uint64_t bar;
   uint32_t tmem_slot;
   int abort_flag;
@@ -71,12 +78,22 @@ __device__ __forceinline__ void bf16x8_to_float(const uint4& q, float* f) {
   }
 }
 
-// Copy a weight image (already in the tile layout) into shared memory, 128 threads.
+// Copy a weight image (already in the tile layout) into shared memory, all threads.
 __device__ __forceinline__ void copy_tile(uint8_t* dst, const __nv_bfloat16* src) {
   const uint4* s = reinterpret_cast<const uint4*>(src);
   uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll 4
-  for (int k = threadIdx.x; k < (int)(TILE / 16); k += BT) d[k] = s[k];
+  for (int k = threadIdx.x; k < (int)(TILE / 16); k += NT) d[k] = s[k];
+}
+
+// 32 bf16 values (64 bytes) -> floats
+__device__ __forceinline__ void load32_bf16(const __nv_bfloat16* src, float* f) {
+  const uint4* q = reinterpret_cast<const uint4*>(src);
+  uint4 v[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) v[u] = q[u];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) bf16x8_to_float(v[u], f + 8 * u);
 }
 
 // Butterfly reduce-scatter over the 32 lanes of a warp: on return lane l holds the sum over the
@@ -124,37 +141,40 @@ __device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, const W
 
 }  // namespace
 
+
 namespace {
 
-__device__ __forceinline__ void zh_row(uint8_t* tile, const float* ln_g, const float* ln_b, const __nv_bfloat16* z,
-                                       const float2* zstat, long long pr, bool valid) {
-  const float2 st = valid ? zstat[pr] : make_float2(0.f, 0.f);
-  const uint4* zrow = reinterpret_cast<const uint4*>(z + pr * kC);
-#pragma unroll 2
-  for (int u = 0; u < 16; ++u) {
-    float f[8];
-    if (valid) {
-      bf16x8_to_float(zrow[u], f);
+// The 32 channels [32 h, 32 h + 32) of zh for pair `pr` (LayerNorm_in from the stored statistics) into
+// row r of an operand tile; zeros for a pair past the grid.
+__device__ __forceinline__ void zh_quarter(uint8_t* tile, const float* ln_g, const float* ln_b,
+                                           const __nv_bfloat16* z, const float2* zstat, long long pr, bool valid,
+                                           int r, int h) {
+  float f[32];
+  if (valid) {
+    const float2 st = zstat[pr];
+    load32_bf16(z + pr * kC + 32 * h, f);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) f[e] = ln_g[8 * u + e] * fmaf(f[e], st.x, st.y) + ln_b[8 * u + e];
-    } else {
+    for (int e = 0; e < 32; ++e) f[e] = ln_g[32 * h + e] * fmaf(f[e], st.x, st.y) + ln_b[32 * h + e];
+  } else {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) f[e] = 0.f;
-    }
-    put8(tile, threadIdx.x, 8 * u, f);
+    for (int e = 0; e < 32; ++e) f[e] = 0.f;
   }
+#pragma unroll
+  for (int u = 0; u < 4; ++u) put8(tile, r, 32 * h + 8 * u, f + 8 * u);
 }
 
-__global__ void __launch_bounds__(BT, 1) k_bwd_output(const BwdOutParams p) {
+__global__ void __launch_bounds__(NT, 1) k_bwd_output(const BwdOutParams p) {
   extern __shared__ uint8_t smem_raw[];
   OutSmem& sm = *reinterpret_cast<OutSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int lq = warp & 3, h = warp >> 2;          // TMEM lane quarter, channel quarter
+  const int r = 32 * lq + lane;                    // pair row of the tile
   if (tid == 0) {
     mbar_init(&sm.bar, 1);
     sm.abort_flag = 0;
     fence_mbar_init();
   }
-  for (int k = tid; k < 4 * kC; k += BT) sm.ln[k] = p.ln[k];
+  for (int k = tid; k < 4 * kC; k += NT) sm.ln[k] = p.ln[k];
   copy_tile(sm.wg, p.w_g);
   copy_tile(sm.wo, p.w_o);
   if (warp == 0) {
@@ -166,47 +186,53 @@ __global__ void __launch_bounds__(BT, 1) k_bwd_output(const BwdOutParams p) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_slot;
-  const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+  const uint32_t trow = tmem + ((uint32_t)(32 * lq) << 16);
   const float *g_in = sm.ln, *b_in = sm.ln + kC, *g_out = sm.ln + 2 * kC, *b_out = sm.ln + 3 * kC;
   const uint32_t a_zh = smem_u32(sm.zh), a_xh = smem_u32(sm.xh), a_dy = smem_u32(sm.dy), a_dgg = smem_u32(sm.dgg);
   const uint32_t a_wg = smem_u32(sm.wg), a_wo = smem_u32(sm.wo);
+  const int c0 = 32 * h;                           // this thread's first channel
 
-  float acc_g[4] = {0.f, 0.f, 0.f, 0.f}, acc_b[4] = {0.f, 0.f, 0.f, 0.f};
+  float acc_g = 0.f, acc_b = 0.f;                  // channel c0 + lane: sums of dxh n and dxh
   uint32_t phase = 0;
   int local = 0;
   bool ok = true;
   for (long long t = blockIdx.x; t < p.tiles; t += gridDim.x, ++local) {
-    const long long pr = t * BT + tid;
+    const long long pr = t * BT + r;
     const bool valid = pr < p.P;
     const int i = valid ? (int)(pr / p.N) : 0;
     const int j = valid ? (int)(pr - (long long)i * p.N) : 0;
-    const float* xp = p.x + (long long)i * p.ldx + j;
+    const float* xp = p.x + (long long)i * p.ldx + j + (long long)c0 * p.xplane;
 
-    // ---- operands of MMA 1: zh and xh = LN_out(x) (shifted one-pass statistics of x)
-    zh_row(sm.zh, g_in, b_in, p.z, p.zstat, pr, valid);
-    float mu = 0.f, rx = 0.f;
-    if (valid) {
-      const float k0 = xp[0];
-      float s1 = 0.f, s2 = 0.f;
-#pragma unroll 8
-      for (int c = 0; c < kC; ++c) {
-        const float d = xp[c * p.xplane] - k0;
-        s1 += d;
-        s2 = fmaf(d, d, s2);
-      }
-      const float m1 = s1 * (1.f / kC);
-      mu = k0 + m1;
-      rx = rsqrtf(fmaxf(s2 * (1.f / kC) - m1 * m1, 0.f) + 1e-5f);
-    }
-#pragma unroll 2
-    for (int u = 0; u < 16; ++u) {
-      float f[8];
+    // ---- zh; x of this quarter: (mean, M2), combined over the four quarters (Chan et al.)
+    zh_quarter(sm.zh, g_in, b_in, p.z, p.zstat, pr, valid, r, h);
+    float xv[32];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int c = 8 * u + e;
-        f[e] = valid ? g_out[c] * ((xp[c * p.xplane] - mu) * rx) + b_out[c] : 0.f;
-      }
-      put8(sm.xh, tid, 8 * u, f);
+    for (int e = 0; e < 32; ++e) xv[e] = valid ? xp[e * p.xplane] : 0.f;
+    {
+      float s = 0.f;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) s += xv[e];
+      const float m = s * (1.f / 32);
+      float m2 = 0.f;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) m2 = fmaf(xv[e] - m, xv[e] - m, m2);
+      sm.xst[h][r] = make_float2(m, m2);
+    }
+    __syncthreads();
+    float mu, rx;
+    {
+      const float2 q0 = sm.xst[0][r], q1 = sm.xst[1][r], q2 = sm.xst[2][r], q3 = sm.xst[3][r];
+      mu = ((q0.x + q1.x) + (q2.x + q3.x)) * 0.25f;
+      const float d0 = q0.x - mu, d1 = q1.x - mu, d2 = q2.x - mu, d3 = q3.x - mu;
+      const float m2 = ((q0.y + q1.y) + (q2.y + q3.y)) + 32.f * ((d0 * d0 + d1 * d1) + (d2 * d2 + d3 * d3));
+      rx = rsqrtf(m2 * (1.f / kC) + 1e-5f);
+    }
+    {
+      float f[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) f[e] = valid ? g_out[c0 + e] * ((xv[e] - mu) * rx) + b_out[c0 + e] : 0.f;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) put8(sm.xh, r, c0 + 8 * u, f + 8 * u);
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -221,33 +247,34 @@ __global__ void __launch_bounds__(BT, 1) k_bwd_output(const BwdOutParams p) {
     phase ^= 1u;
     tc_fence_after();
 
-    // ---- dy = dout g, dgg = dout y g (1 - g): operands of MMA 2 and 3
-    const uint4* drow = reinterpret_cast<const uint4*>(p.dout + pr * kC);
+    // ---- dy = dout g, dgg = dout y g (1 - g), channels [c0, c0 + 32), in two halves of 16
 #pragma unroll 1
-    for (int q = 0; q < 4; ++q) {
-      uint32_t rg[32], ry[32];
-      tmem_ld32(trow + 32 * q, rg);
-      tmem_ld32(trow + kC + 32 * q, ry);
-      tmem_ld_wait();
-      float d[32];
+    for (int hh = 0; hh < 2; ++hh) {
+      uint32_t rg[16], ry[16];
+      tmem_ld16(trow + c0 + 16 * hh, rg);
+      tmem_ld16(trow + kC + c0 + 16 * hh, ry);
+      float d[16];
+      if (valid) {
+        const uint4* q = reinterpret_cast<const uint4*>(p.dout + pr * kC + c0 + 16 * hh);
+        const uint4 q0 = q[0], q1 = q[1];
+        bf16x8_to_float(q0, d);
+        bf16x8_to_float(q1, d + 8);
+      } else {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        if (valid) bf16x8_to_float(drow[4 * q + u], d + 8 * u);
-        else
-#pragma unroll
-          for (int e = 0; e < 8; ++e) d[8 * u + e] = 0.f;
+        for (int e = 0; e < 16; ++e) d[e] = 0.f;
       }
-      float vy[32], vg[32];
+      tmem_ld_wait();
+      float vy[16], vg[16];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
+      for (int e = 0; e < 16; ++e) {
         const float s = sigmoid_mufu(__uint_as_float(rg[e]));
         vy[e] = d[e] * s;
         vg[e] = d[e] * __uint_as_float(ry[e]) * s * (1.f - s);
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        put8(sm.dy, tid, 32 * q + 8 * u, vy + 8 * u);
-        put8(sm.dgg, tid, 32 * q + 8 * u, vg + 8 * u);
+      for (int u = 0; u < 2; ++u) {
+        put8(sm.dy, r, c0 + 16 * hh + 8 * u, vy + 8 * u);
+        put8(sm.dgg, r, c0 + 16 * hh + 8 * u, vg + 8 * u);
       }
     }
     fence_proxy_async_smem();
@@ -266,75 +293,66 @@ __global__ void __launch_bounds__(BT, 1) k_bwd_output(const BwdOutParams p) {
     tc_fence_after();
 
     // ---- dzh_g out; LayerNorm_out backward of dxh -> dX
-#pragma unroll 1
-    for (int q = 0; q < 4; ++q) {
-      uint32_t r[32];
-      tmem_ld32(trow + kC + 32 * q, r);
+    {
+      uint32_t rz[32];
+      tmem_ld32(trow + kC + c0, rz);
       tmem_ld_wait();
       if (valid)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) p.dzh[(long long)(32 * q + e) * p.P + pr] = __uint_as_float(r[e]);
+        for (int e = 0; e < 32; ++e) p.dzh[(long long)(c0 + e) * p.P + pr] = __uint_as_float(rz[e]);
     }
+    uint32_t rd[32];
+    tmem_ld32(trow + c0, rd);
+    tmem_ld_wait();
     float s1 = 0.f, s2 = 0.f;
-#pragma unroll 1
-    for (int q = 0; q < 4; ++q) {
-      uint32_t r[32];
-      tmem_ld32(trow + 32 * q, r);
-      tmem_ld_wait();
-      float vn[32], vd[32];
+    {
+      float v[32];
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
-        const int c = 32 * q + e;
-        const float n = valid ? (xp[c * p.xplane] - mu) * rx : 0.f;
-        const float dxh = valid ? __uint_as_float(r[e]) : 0.f;
-        const float dn = dxh * g_out[c];
+        xv[e] = valid ? (xv[e] - mu) * rx : 0.f;                  // n, the normalised x
+        const float dxh = valid ? __uint_as_float(rd[e]) : 0.f;
+        rd[e] = __float_as_uint(dxh);
+        const float dn = dxh * g_out[c0 + e];
         s1 += dn;
-        s2 = fmaf(dn, n, s2);
-        vn[e] = dxh * n;
-        vd[e] = dxh;
+        s2 = fmaf(dn, xv[e], s2);
+        v[e] = dxh * xv[e];
       }
-      acc_g[q] += reduce_scatter32(vn, lane);
-      acc_b[q] += reduce_scatter32(vd, lane);
-    }
-    s1 *= 1.f / kC;
-    s2 *= 1.f / kC;
-    __nv_bfloat16* dxp = p.dX + (long long)i * p.ld + j;
-#pragma unroll 1
-    for (int q = 0; q < 4; ++q) {
-      uint32_t r[32];
-      tmem_ld32(trow + 32 * q, r);
-      tmem_ld_wait();
-      if (valid)
+      acc_g += reduce_scatter32(v, lane);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int c = 32 * q + e;
-          const float n = (xp[c * p.xplane] - mu) * rx;
-          dxp[c * p.dplane] = __float2bfloat16_rn(rx * (__uint_as_float(r[e]) * g_out[c] - s1 - n * s2));
-        }
+      for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(rd[e]);
+      acc_b += reduce_scatter32(v, lane);
+    }
+    sm.sst[h][r] = make_float2(s1, s2);
+    __syncthreads();
+    {
+      const float2 q0 = sm.sst[0][r], q1 = sm.sst[1][r], q2 = sm.sst[2][r], q3 = sm.sst[3][r];
+      s1 = ((q0.x + q1.x) + (q2.x + q3.x)) * (1.f / kC);
+      s2 = ((q0.y + q1.y) + (q2.y + q3.y)) * (1.f / kC);
+    }
+    if (valid) {
+      __nv_bfloat16* dxp = p.dX + (long long)i * p.ld + j + (long long)c0 * p.dplane;
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        dxp[e * p.dplane] = __float2bfloat16_rn(rx * (__uint_as_float(rd[e]) * g_out[c0 + e] - s1 - xv[e] * s2));
     }
   }
 
-  // ---- per-CTA partial sums: d(gamma_out), d(beta_out) over the warps; dW_g, dW_o from TMEM
+  // ---- per-CTA partial sums: d(gamma_out), d(beta_out) over the lane quarters; dW_g, dW_o from TMEM
   if (ok) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      sm.red[warp][32 * q + lane] = acc_g[q];
-      sm.red[warp][kC + 32 * q + lane] = acc_b[q];
-    }
+    sm.red[lq][c0 + lane] = acc_g;
+    sm.red[lq][kC + c0 + lane] = acc_b;
     __syncthreads();
-    for (int k = tid; k < 2 * kC; k += BT)
+    for (int k = tid; k < 2 * kC; k += NT)
       p.part_ln[(long long)blockIdx.x * 2 * kC + k] = ((sm.red[0][k] + sm.red[1][k]) + sm.red[2][k]) + sm.red[3][k];
-    float* pw = p.part_w + (long long)blockIdx.x * 2 * kC * kC + (long long)tid * kC;
+    float* pw = p.part_w + (long long)blockIdx.x * 2 * kC * kC + (long long)r * kC + c0;
 #pragma unroll 1
-    for (int m = 0; m < 2; ++m)
-#pragma unroll 1
-      for (int q = 0; q < 4; ++q) {
-        uint32_t r[32];
-        tmem_ld32(trow + (2 + m) * kC + 32 * q, r);
-        tmem_ld_wait();
+    for (int m = 0; m < 2; ++m) {
+      uint32_t rr[32];
+      tmem_ld32(trow + (2 + m) * kC + c0, rr);
+      tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) pw[m * kC * kC + 32 * q + e] = local > 0 ? __uint_as_float(r[e]) : 0.f;
-      }
+      for (int e = 0; e < 32; ++e) pw[m * kC * kC + e] = local > 0 ? __uint_as_float(rr[e]) : 0.f;
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -345,16 +363,18 @@ __global__ void __launch_bounds__(BT, 1) k_bwd_output(const BwdOutParams p) {
 
 namespace {
 
-__global__ void __launch_bounds__(BT, 1) k_bwd_project(const BwdProjParams p) {
+__global__ void __launch_bounds__(NT, 1) k_bwd_project(const BwdProjParams p) {
   extern __shared__ uint8_t smem_raw[];
   ProjSmem& sm = *reinterpret_cast<ProjSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int lq = warp & 3, h = warp >> 2;
+  const int r = 32 * lq + lane;
   if (tid == 0) {
     mbar_init(&sm.bar, 1);
     sm.abort_flag = 0;
     fence_mbar_init();
   }
-  for (int k = tid; k < 2 * kC; k += BT) sm.ln[k] = p.ln[k];
+  for (int k = tid; k < 2 * kC; k += NT) sm.ln[k] = p.ln[k];
   copy_tile(sm.wv, p.w_v);
   copy_tile(sm.wgt, p.w_gt);
   if (warp == 0) {
@@ -366,22 +386,31 @@ __global__ void __launch_bounds__(BT, 1) k_bwd_project(const BwdProjParams p) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_slot;
-  const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+  const uint32_t trow = tmem + ((uint32_t)(32 * lq) << 16);
   const float *g_in = sm.ln, *b_in = sm.ln + kC;
   const uint32_t a_zh = smem_u32(sm.zh), a_dv = smem_u32(sm.dv), a_dg = smem_u32(sm.dg);
   const uint32_t a_wv = smem_u32(sm.wv), a_wgt = smem_u32(sm.wgt);
+  const int c0 = 32 * h;
 
-  float acc_g[4] = {0.f, 0.f, 0.f, 0.f}, acc_b[4] = {0.f, 0.f, 0.f, 0.f};
+  float acc_g = 0.f, acc_b = 0.f;
   uint32_t phase = 0;
   int local = 0;
   bool ok = true;
   for (long long t = blockIdx.x; t < p.tiles; t += gridDim.x, ++local) {
-    const long long pr = t * BT + tid;
+    const long long pr = t * BT + r;
     const bool valid = pr < p.P;
     const int i = valid ? (int)(pr / p.N) : 0;
     const int k2 = valid ? (int)(pr - (long long)i * p.N) : 0;
 
-    zh_row(sm.zh, g_in, b_in, p.z, p.zstat, pr, valid);
+    zh_quarter(sm.zh, g_in, b_in, p.z, p.zstat, pr, valid, r, h);
+    // this quarter of dV (issued before the MMA, consumed after it)
+    const float m = valid ? (p.mask ? p.mask[i] * p.mask[k2] : 1.f) : 0.f;
+    float dv[32];
+    {
+      const float* vp = p.dV + (long long)i * p.ldv + k2 + (long long)c0 * p.vplane;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) dv[e] = valid ? vp[e * p.vplane] * m : 0.f;
+    }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -396,26 +425,24 @@ __global__ void __launch_bounds__(BT, 1) k_bwd_project(const BwdProjParams p) {
     tc_fence_after();
 
     // ---- gate backward: dpv = dV s m, dpg = dV pv m s (1 - s)
-    const float m = valid ? (p.mask ? p.mask[i] * p.mask[k2] : 1.f) : 0.f;
-    const float* vp = p.dV + (long long)i * p.ldv + k2;
 #pragma unroll 1
-    for (int q = 0; q < 4; ++q) {
-      uint32_t rv[32], rg[32];
-      tmem_ld32(trow + 32 * q, rv);
-      tmem_ld32(trow + kC + 32 * q, rg);
+    for (int hh = 0; hh < 2; ++hh) {
+      uint32_t rv[16], rg[16];
+      tmem_ld16(trow + c0 + 16 * hh, rv);
+      tmem_ld16(trow + kC + c0 + 16 * hh, rg);
       tmem_ld_wait();
-      float fv[32], fg[32];
+      float fv[16], fg[16];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const float dv = valid ? vp[(32 * q + e) * p.vplane] * m : 0.f;
+      for (int e = 0; e < 16; ++e) {
+        const float d = dv[16 * hh + e];
         const float s = sigmoid_mufu(__uint_as_float(rg[e]));
-        fv[e] = dv * s;
-        fg[e] = dv * __uint_as_float(rv[e]) * s * (1.f - s);
+        fv[e] = d * s;
+        fg[e] = d * __uint_as_float(rv[e]) * s * (1.f - s);
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        put8(sm.dv, tid, 32 * q + 8 * u, fv + 8 * u);
-        put8(sm.dg, tid, 32 * q + 8 * u, fg + 8 * u);
+      for (int u = 0; u < 2; ++u) {
+        put8(sm.dv, r, c0 + 16 * hh + 8 * u, fv + 8 * u);
+        put8(sm.dg, r, c0 + 16 * hh + 8 * u, fg + 8 * u);
       }
     }
     fence_proxy_async_smem();
@@ -429,106 +456,90 @@ __global__ void __launch_bounds__(BT, 1) k_bwd_project(const BwdProjParams p) {
       mma_tile(tmem + 3 * kC, a_dg, true, a_zh, true, ID_MM, local > 0);   // dW_gt += dpg zh^T
       mma_commit(&sm.bar);
     }
+    // the earlier terms of dzh, read while the MMA runs
+    float dzh[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) dzh[e] = valid ? p.dzh[(long long)(c0 + e) * p.P + pr] : 0.f;
     if (!cta_wait(&sm.bar, phase, p.w, &sm.abort_flag, 2)) { ok = false; break; }
     phase ^= 1u;
     tc_fence_after();
-
+    {
+      uint32_t rr[32];
+      tmem_ld32(trow + c0, rr);
+      tmem_ld_wait();
+#pragma unroll
+      for (int e = 0; e < 32; ++e) dzh[e] = valid ? dzh[e] + __uint_as_float(rr[e]) : 0.f;
+    }
     if (!p.final_pass) {
-      // dzh += this side's term
-#pragma unroll 1
-      for (int q = 0; q < 4; ++q) {
-        uint32_t r[32];
-        tmem_ld32(trow + 32 * q, r);
-        tmem_ld_wait();
-        if (valid)
+      if (valid)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            float* d = p.dzh + (long long)(32 * q + e) * p.P + pr;
-            *d = *d + __uint_as_float(r[e]);
-          }
-      }
+        for (int e = 0; e < 32; ++e) p.dzh[(long long)(c0 + e) * p.P + pr] = dzh[e];
     } else {
-      // dzh (all terms) -> LayerNorm_in backward -> dz; n = z rstd - rstd mu from the statistics
-      const float2 st = valid ? p.zstat[pr] : make_float2(0.f, 0.f);
-      const uint4* zrow = reinterpret_cast<const uint4*>(p.z + pr * kC);
-      float s1 = 0.f, s2 = 0.f;
-#pragma unroll 1
-      for (int q = 0; q < 4; ++q) {
-        uint32_t r[32];
-        tmem_ld32(trow + 32 * q, r);
-        tmem_ld_wait();
-        float zf[32];
+      // LayerNorm_in backward: n = z rstd - rstd mu from the stored statistics
+      float n[32];
+      float rstd = 0.f;
+      if (valid) {
+        const float2 st = p.zstat[pr];
+        rstd = st.x;
+        load32_bf16(p.z + pr * kC + c0, n);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if (valid) bf16x8_to_float(zrow[4 * q + u], zf + 8 * u);
-          else
+        for (int e = 0; e < 32; ++e) n[e] = fmaf(n[e], st.x, st.y);
+      } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) zf[8 * u + e] = 0.f;
-        }
-        float vn[32], vd[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int c = 32 * q + e;
-          const float dzh = valid ? p.dzh[(long long)c * p.P + pr] + __uint_as_float(r[e]) : 0.f;
-          const float n = fmaf(zf[e], st.x, st.y);
-          const float dn = dzh * g_in[c];
-          s1 += dn;
-          s2 = fmaf(dn, n, s2);
-          vn[e] = dzh * n;
-          vd[e] = dzh;
-        }
-        acc_g[q] += reduce_scatter32(vn, lane);
-        acc_b[q] += reduce_scatter32(vd, lane);
+        for (int e = 0; e < 32; ++e) n[e] = 0.f;
       }
-      s1 *= 1.f / kC;
-      s2 *= 1.f / kC;
-      uint4* dzrow = reinterpret_cast<uint4*>(p.dz + pr * kC);
-#pragma unroll 1
-      for (int q = 0; q < 4; ++q) {
-        uint32_t r[32];
-        tmem_ld32(trow + 32 * q, r);
-        tmem_ld_wait();
-        if (!valid) continue;
-        float zf[32], out[32];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) bf16x8_to_float(zrow[4 * q + u], zf + 8 * u);
+      float s1 = 0.f, s2 = 0.f;
+      {
+        float v[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const int c = 32 * q + e;
-          const float dzh = p.dzh[(long long)c * p.P + pr] + __uint_as_float(r[e]);
-          const float n = fmaf(zf[e], st.x, st.y);
-          out[e] = st.x * (dzh * g_in[c] - s1 - n * s2);
+          const float dn = dzh[e] * g_in[c0 + e];
+          s1 += dn;
+          s2 = fmaf(dn, n[e], s2);
+          v[e] = dzh[e] * n[e];
         }
+        acc_g += reduce_scatter32(v, lane);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = dzh[e];
+        acc_b += reduce_scatter32(v, lane);
+      }
+      sm.sst[h][r] = make_float2(s1, s2);
+      __syncthreads();
+      {
+        const float2 q0 = sm.sst[0][r], q1 = sm.sst[1][r], q2 = sm.sst[2][r], q3 = sm.sst[3][r];
+        s1 = ((q0.x + q1.x) + (q2.x + q3.x)) * (1.f / kC);
+        s2 = ((q0.y + q1.y) + (q2.y + q3.y)) * (1.f / kC);
+      }
+      if (valid) {
+        float o[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = rstd * (dzh[e] * g_in[c0 + e] - s1 - n[e] * s2);
+        uint4* dzp = reinterpret_cast<uint4*>(p.dz + pr * kC + c0);
 #pragma unroll
         for (int u = 0; u < 4; ++u)
-          dzrow[4 * q + u] = make_uint4(pack_bf16x2(out[8 * u], out[8 * u + 1]), pack_bf16x2(out[8 * u + 2], out[8 * u + 3]),
-                                        pack_bf16x2(out[8 * u + 4], out[8 * u + 5]), pack_bf16x2(out[8 * u + 6], out[8 * u + 7]));
+          dzp[u] = make_uint4(pack_bf16x2(o[8 * u], o[8 * u + 1]), pack_bf16x2(o[8 * u + 2], o[8 * u + 3]),
+                              pack_bf16x2(o[8 * u + 4], o[8 * u + 5]), pack_bf16x2(o[8 * u + 6], o[8 * u + 7]));
       }
     }
   }
 
   if (ok) {
     if (p.final_pass) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        sm.red[warp][32 * q + lane] = acc_g[q];
-        sm.red[warp][kC + 32 * q + lane] = acc_b[q];
-      }
+      sm.red[lq][c0 + lane] = acc_g;
+      sm.red[lq][kC + c0 + lane] = acc_b;
       __syncthreads();
-      for (int k = tid; k < 2 * kC; k += BT)
+      for (int k = tid; k < 2 * kC; k += NT)
         p.part_ln[(long long)blockIdx.x * 2 * kC + k] = ((sm.red[0][k] + sm.red[1][k]) + sm.red[2][k]) + sm.red[3][k];
     }
-    float* pw = p.part_w + (long long)blockIdx.x * 2 * kC * kC + (long long)tid * kC;
+    float* pw = p.part_w + (long long)blockIdx.x * 2 * kC * kC + (long long)r * kC + c0;
 #pragma unroll 1
-    for (int m = 0; m < 2; ++m)
-#pragma unroll 1
-      for (int q = 0; q < 4; ++q) {
-        uint32_t r[32];
-        tmem_ld32(trow + (2 + m) * kC + 32 * q, r);
-        tmem_ld_wait();
+    for (int mm = 0; mm < 2; ++mm) {
+      uint32_t rr[32];
+      tmem_ld32(trow + (2 + mm) * kC + c0, rr);
+      tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) pw[m * kC * kC + 32 * q + e] = local > 0 ? __uint_as_float(r[e]) : 0.f;
-      }
+      for (int e = 0; e < 32; ++e) pw[mm * kC * kC + e] = local > 0 ? __uint_as_float(rr[e]) : 0.f;
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -573,14 +584,14 @@ int bwd_grid(long long tiles, int num_sms) { return (int)(tiles < num_sms ? tile
 cudaError_t launch_bwd_output_bf16(const BwdOutParams& p, int grid, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(k_bwd_output, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kOutSmemBytes);
   if (e != cudaSuccess) return e;
-  k_bwd_output<<<grid, BT, kOutSmemBytes, s>>>(p);
+  k_bwd_output<<<grid, NT, kOutSmemBytes, s>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_project_bf16(const BwdProjParams& p, int grid, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(k_bwd_project, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kProjSmemBytes);
   if (e != cudaSuccess) return e;
-  k_bwd_project<<<grid, BT, kProjSmemBytes, s>>>(p);
+  k_bwd_project<<<grid, NT, kProjSmemBytes, s>>>(p);
   return cudaGetLastError();
 }
 
