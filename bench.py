@@ -327,6 +327,49 @@ def run_ours(args, w):
                "d2h_bytes_per_step": len(w.directions) * zbytes, "steps": k_e2e,
                "ms_per_step": ms_e2e / k_e2e}
 
+    # backward pass (training): tm_backward per direction on the same z, a seeded bf16 cotangent
+    bwd = None
+    if not args.no_backward and w.dtype == "bf16" and not w.block:
+        gen = torch.Generator(device="cuda").manual_seed(5)
+        dout = torch.randn(z.shape, device="cuda", generator=gen).to(torch.bfloat16)
+        dz = torch.empty_like(z)
+        shapes = {"ln_in_gamma": (w.c_z,), "ln_in_beta": (w.c_z,), "w_a": (w.c_h, w.c_z), "w_ga": (w.c_h, w.c_z),
+                  "w_b": (w.c_h, w.c_z), "w_gb": (w.c_h, w.c_z), "w_g": (w.c_z, w.c_z),
+                  "ln_out_gamma": (w.c_h,), "ln_out_beta": (w.c_h,), "w_o": (w.c_z, w.c_h)}
+        grads = {n: torch.empty(sh, dtype=torch.float32, device="cuda") for n, sh in shapes.items()}
+
+        def bstep():
+            for d in w.directions:
+                tm.tm_backward(mod.ctx, z, mask, d, dout, dz, grads)
+
+        bstep()                             # sizes the workspace
+        barrier()
+        k_b = max(1, min(args.steps, 3))
+        b_l0 = tm.tm_launch_count(mod.ctx)
+        tm.tm_set_timing(mod.ctx, True)
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record()
+        for _ in range(k_b):
+            bstep()
+        b1.record()
+        barrier()
+        ms_b = b0.elapsed_time(b1) / (k_b * len(w.directions))
+        bt = tm.tm_get_timing(mod.ctx)
+        tm.tm_set_timing(mod.ctx, False)
+        if tm.tm_sync_status(mod.ctx) != tm.TM_OK:
+            raise RuntimeError("device status after the backward: " + tm.tm_last_error(mod.ctx))
+        # the gradient's own work: the contractions dA = dX b-side and dB (2 x 2 N^3 c_h) and 12 per-pair
+        # 128 x 128 products (W^T products and parameter sums of both per-pair stages); the recomputed
+        # forward (projection, x) is not counted
+        gflops = 4.0 * float(w.N) ** 3 * w.c_h + 12 * 2 * 128 * 128 * float(w.N) ** 2
+        btot = sum(v["ms"] for v in bt.values()) or 1.0
+        bwd = {"ms_per_update": ms_b, "grad_tflops": gflops / (ms_b / 1e3) / 1e12,
+               "grad_flops_per_update": gflops, "gpu_launches": tm.tm_launch_count(mod.ctx) - b_l0,
+               "kernels": {n: {"launches": v["launches"], "ms_per_update": v["ms"] / (k_b * len(w.directions)),
+                               "share": v["ms"] / btot}
+                           for n, v in bt.items() if v["launches"]}}
+        del dout, dz, grads
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         dt, tf, desc = oracle_sample(z_np, m_np, W, w, args.cpu_rows, args.cpu_rows, 7)
@@ -342,7 +385,7 @@ def run_ours(args, w):
             "ms_per_update": ms_total / args.steps / len(w.directions),
             "frac_of_bf16_peak": value / world / peaks["bf16_tflops"],
             "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": launches, "clocks": clk,
+            "gpu_launches": launches, "clocks": clk, "backward": bwd,
         }
         print(json.dumps(line), flush=True)
     mod.close()
@@ -361,6 +404,7 @@ def main():
     ap.add_argument("--workload", default="complex3605")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-backward", action="store_true", help="skip the backward-pass measurement")
     ap.add_argument("--cpu-rows", type=int, default=48, help="side of the oracle's sampled grid")
     ap.add_argument("--N", type=int, default=0, help="override the workload's token count (profiling runs)")
     args = ap.parse_args()

@@ -133,6 +133,23 @@ __device__ __forceinline__ void mma_tile(uint32_t d, uint32_t a, bool a_mn, uint
             (acc || ks != 0) ? 1u : 0u);
 }
 
+// L2 prefetch of bytes [b0, b1) of a buffer, widened to 16-byte bounds (the caller keeps the
+// widened range inside the buffer's allocation).
+__device__ __forceinline__ void prefetch_range(const void* base, long long b0, long long b1) {
+  const long long a0 = b0 & ~15ll, a1 = (b1 + 15) & ~15ll;
+  if (a1 > a0) prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(base) + a0, (uint32_t)(a1 - a0));
+}
+
+// Prefetch, for the pairs [p0, p1) of a tile (N >= 128: at most two grid rows), channel c of a float32
+// plane [128][N][ld] whose rows are 16-byte multiples.
+__device__ __forceinline__ void prefetch_plane_rows(const float* plane, long long ld, int N, long long p0,
+                                                    long long p1) {
+  const int i = (int)(p0 / N), j0 = (int)(p0 - (long long)i * N);
+  const int n1 = (int)((p1 - p0) < (long long)(N - j0) ? (p1 - p0) : (long long)(N - j0));
+  prefetch_range(plane + (long long)i * ld, 4ll * j0, 4ll * (j0 + n1));
+  if (p0 + n1 < p1) prefetch_range(plane + (long long)(i + 1) * ld, 0, 4ll * (p1 - p0 - n1));
+}
+
 // Wait for the MMA barrier with a CTA-uniform outcome.
 __device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, const Watch& w, int* abort_flag, int site) {
   const bool ok = wait_bounded(bar, parity, w, abort_flag, site);
@@ -202,6 +219,18 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_output(const BwdOutParams p) {
     const int i = valid ? (int)(pr / p.N) : 0;
     const int j = valid ? (int)(pr - (long long)i * p.N) : 0;
     const float* xp = p.x + (long long)i * p.ldx + j + (long long)c0 * p.xplane;
+    {
+      // L2 prefetch of what the next tile of this CTA reads: x (one channel per thread of the first
+      // 128), z, dout and the LayerNorm_in statistics
+      const long long tn = t + gridDim.x;
+      if (tn < p.tiles && p.N >= BT) {
+        const long long q0 = tn * BT, q1 = (q0 + BT < p.P) ? q0 + BT : p.P;
+        if (tid < kC) prefetch_plane_rows(p.x + (long long)tid * p.xplane, p.ldx, p.N, q0, q1);
+        else if (tid == kC) prefetch_range(p.z, q0 * 2 * kC, q1 * 2 * kC);
+        else if (tid == kC + 1) prefetch_range(p.dout, q0 * 2 * kC, q1 * 2 * kC);
+        else if (tid == kC + 2) prefetch_range(p.zstat, q0 * 8, q1 * 8);
+      }
+    }
 
     // ---- zh; x of this quarter: (mean, M2), combined over the four quarters (Chan et al.)
     zh_quarter(sm.zh, g_in, b_in, p.z, p.zstat, pr, valid, r, h);
@@ -401,6 +430,17 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_project(const BwdProjParams p) {
     const bool valid = pr < p.P;
     const int i = valid ? (int)(pr / p.N) : 0;
     const int k2 = valid ? (int)(pr - (long long)i * p.N) : 0;
+    {
+      // L2 prefetch of the next tile's dV (threads 0..127), dzh (128..255), z and statistics
+      const long long tn = t + gridDim.x;
+      if (tn < p.tiles && p.N >= BT) {
+        const long long q0 = tn * BT, q1 = (q0 + BT < p.P) ? q0 + BT : p.P;
+        if (tid < kC) prefetch_plane_rows(p.dV + (long long)tid * p.vplane, p.ldv, p.N, q0, q1);
+        else if (tid < 2 * kC) prefetch_range(p.dzh, ((tid - kC) * p.P + q0) * 4, ((tid - kC) * p.P + q1) * 4);
+        else if (tid == 2 * kC) prefetch_range(p.z, q0 * 2 * kC, q1 * 2 * kC);
+        else if (tid == 2 * kC + 1) prefetch_range(p.zstat, q0 * 8, q1 * 8);
+      }
+    }
 
     zh_quarter(sm.zh, g_in, b_in, p.z, p.zstat, pr, valid, r, h);
     // this quarter of dV (issued before the MMA, consumed after it)

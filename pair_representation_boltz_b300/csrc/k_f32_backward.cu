@@ -227,6 +227,31 @@ cudaError_t launch_outer_sum_f32(const float* U, const float* V, int O, int K, l
   return launch_sum_parts(part, S, (long long)O * K, (long long)O * K, out, s);
 }
 
+namespace {
+// One launch for several partial-sum jobs (blockIdx.y = job); the loads of a thread are independent,
+// the sum runs over q = 0, 1, ... in order.
+__global__ void sum_parts_multi(const SumJobs j, int S) {
+  const int k = blockIdx.y;
+  const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= j.E[k] || !j.out[k]) return;
+  const float* src = j.part[k] + e;
+  const long long st = j.stride[k];
+  float s = 0.f;
+#pragma unroll 8
+  for (int q = 0; q < S; ++q) s += src[q * st];
+  j.out[k][e] = s;
+}
+}  // namespace
+
+cudaError_t launch_sum_parts_multi(const SumJobs& j, int S, cudaStream_t s) {
+  long long emax = 0;
+  for (int k = 0; k < j.n; ++k) emax = j.E[k] > emax ? j.E[k] : emax;
+  if (j.n == 0 || emax == 0) return cudaSuccess;
+  dim3 grid((unsigned)((emax + 127) / 128), (unsigned)j.n);
+  sum_parts_multi<<<grid, 128, 0, s>>>(j, S);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_sum_parts(const float* part, int S, long long E, long long stride, float* out, cudaStream_t s) {
   sum_parts_f32<<<(unsigned)((E + 255) / 256), 256, 0, s>>>(part, S, E, stride, out);
   return cudaGetLastError();

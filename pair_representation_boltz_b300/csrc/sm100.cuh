@@ -162,6 +162,12 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* m, int c0,
                : "memory");
 }
 
+// Bulk prefetch of [p, p + bytes) into L2 (p and bytes multiples of 16; no completion to wait for).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+               : "memory");
+}
+
 // ---------------------------------------------------------------- CTA pairs (clusters of two)
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;

@@ -723,11 +723,16 @@ tm_status backward_bf16(tm_ctx* c, const void* z, const float* mask, int N, bool
                           {g->w_b, part_b, WW, 2 * WW},       {g->w_gb, part_b + WW, WW, 2 * WW},
                           {g->ln_out_gamma, ln_o, kC, 2 * kC}, {g->ln_out_beta, ln_o + kC, kC, 2 * kC},
                           {g->ln_in_gamma, ln_i, kC, 2 * kC},  {g->ln_in_beta, ln_i + kC, kC, 2 * kC}};
+    SumJobs jobs{};
     for (const Sum& t : sums) {
-      if (!t.out) continue;
-      e = timed(c, 6, 0, s, [&] { return launch_sum_parts(t.part, grid, t.E, t.stride, t.out, s); });
-      if (e != cudaSuccess) return cuda_fail(c, e, "parameter gradient sum launch");
+      jobs.part[jobs.n] = t.part;
+      jobs.out[jobs.n] = t.out;
+      jobs.E[jobs.n] = t.E;
+      jobs.stride[jobs.n] = t.stride;
+      ++jobs.n;
     }
+    e = timed(c, 6, 0, s, [&] { return launch_sum_parts_multi(jobs, grid, s); });
+    if (e != cudaSuccess) return cuda_fail(c, e, "parameter gradient sum launch");
   }
   return TM_OK;
 }

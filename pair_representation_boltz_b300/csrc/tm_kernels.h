@@ -187,6 +187,14 @@ cudaError_t launch_transpose_planes_bf16(const __nv_bfloat16* in, __nv_bfloat16*
                                          cudaStream_t s);
 // out[e] = sum over q < S of part[q * stride + e], e < E, in order q = 0, 1, ...
 cudaError_t launch_sum_parts(const float* part, int S, long long E, long long stride, float* out, cudaStream_t s);
+// The same for up to 10 jobs in one launch (a job whose out is nullptr is skipped).
+struct SumJobs {
+  const float* part[10];
+  float* out[10];
+  long long E[10], stride[10];
+  int n;
+};
+cudaError_t launch_sum_parts_multi(const SumJobs& j, int S, cudaStream_t s);
 
 // ----------------------------------------------------------------- diagnostics
 enum : int { KID_SELFTEST = 9 };
