@@ -8,3 +8,4 @@ from .trimul import (LN_EPS, DIRECTIONS, sigmoid, layer_norm, round_to_bf16, nor
                      half_ulp_bf16, errors)
 from .trimul_backward import (WEIGHT_NAMES, layer_norm_backward, contract_backward,  # noqa: F401
                               gated_projection_backward, output_backward, full_backward)
+from . import triangle_attention  # noqa: F401
