@@ -216,6 +216,50 @@ tm_status tm_backward(tm_ctx* ctx, const void* z, const float* mask, int N, tm_d
                       tm_direction dir, const void* dout, void* dz, const tm_grads* grads,
                       void* stream, const tm_options* opt);
 
+/* ------------------------------------------------------------------ triangle attention
+ * The other O(N^3) operation of the pair stack: the BioIR page ("BioIR da Nvidia
+ * acelera previsão de proteínas em 2,9x com PyTorch puro") names triangle
+ * operations and pairwise attention among the Pairformer parts its kernels
+ * target, without their arithmetic. libtm computes the AlphaFold3/Boltz
+ * triangle attention over z [N][N][c_z] with H heads of dimension c:
+ *
+ *   zh = LayerNorm(z);  q, k, v = W_q zh, W_k zh, W_v zh;  g = sigmoid(W_g zh)
+ *   b_jk^h = (W_b zh_jk)^h                                        (pair bias)
+ *   starting node: o_ij^h = g_ij^h * sum_k softmax_k(q_ij^h.k_ik^h/sqrt(c) + b_jk^h) v_ik^h
+ *                  over keys k with m_i m_k = 1
+ *   ending node:   the same on the transposed grid (keys k_kj, v_kj, bias b_ki)
+ *   out_ij = W_o [o_ij^1 .. o_ij^H]
+ *
+ * Linear layers have no bias; a query row with no valid key (a masked token's
+ * row for the starting node, column for the ending node) gives o = 0.
+ * Supported: bf16, c_z = 128, H = 4, c = 32; q, k, v, g, b and P are bf16
+ * operands of tcgen05 products with float32 accumulation, the softmax runs
+ * in float32 (online, one pass over the keys). */
+typedef enum { TM_ATTN_STARTING = 0, TM_ATTN_ENDING = 1 } tm_attn_node;
+
+/* Host float32 arrays, Linear layout [out][in]. */
+typedef struct {
+  const float *ln_gamma, *ln_beta;         /* [c_z]         */
+  const float *w_q, *w_k, *w_v, *w_g;      /* [H c][c_z]    */
+  const float *w_b;                        /* [H][c_z]      */
+  const float *w_o;                        /* [c_z][H c]    */
+} tm_attn_weights;
+
+/* A context holding one triangle attention layer (freed by tm_destroy; the
+ * update's calls reject it with TM_ERR_INVALID). Returns TM_ERR_INVALID for a
+ * NULL argument, TM_ERR_UNSUPPORTED for any shape but c_z = 128, H = 4,
+ * c = 32. Synchronous; the caller may free its arrays afterwards. */
+tm_status tm_attn_create(int c_z, int heads, int c_head, const tm_attn_weights* w, tm_ctx** out_ctx);
+
+/* out = triangle attention of the given node over z.
+ *   z     device bf16 [N][N][c_z]; mask device float32 [N] or NULL;
+ *   out   device bf16 [N][N][c_z], must not overlap z.
+ * Workspace: about 1.3 kB per pair (q, k, v, g, o and the bias, bf16).
+ * opt: timeout_ms and workspace_limit apply, other fields must be 0. dtype
+ * TM_F32 returns TM_ERR_UNSUPPORTED. Stream-ordered like tm_forward. */
+tm_status tm_attn_forward(tm_ctx* ctx, const void* z, const float* mask, int N, tm_dtype dtype,
+                          tm_attn_node node, void* out, void* stream, const tm_options* opt);
+
 /* Synchronise `stream` and return the device status word (TM_OK or
  * TM_ERR_TIMEOUT), clearing it. */
 tm_status tm_sync_status(tm_ctx* ctx, void* stream);
@@ -223,12 +267,15 @@ tm_status tm_sync_status(tm_ctx* ctx, void* stream);
 /* Per-kernel timing with CUDA events recorded on the launch stream.
  * enable != 0 starts recording (and clears the totals). */
 typedef struct {
-  int launches[8];     /* projection, contraction, finish, float32 kernels,
+  int launches[12];    /* projection, contraction, finish, float32 kernels,
                           output backward, projection backward, other
-                          backward kernels (transpose, sums), unused         */
-  double ms[8];        /* summed event-measured durations                  */
-  long long units[8];  /* pairs processed (projection, finish, backward) or
-                          channel x output-pair products (contraction)     */
+                          backward kernels (transpose, sums), unused,
+                          attention projection, attention, attention
+                          output, unused                                    */
+  double ms[12];       /* summed event-measured durations                  */
+  long long units[12]; /* pairs processed (projection, finish, backward,
+                          attention) or channel x output-pair products
+                          (contraction)                                     */
 } tm_timing;
 tm_status tm_set_timing(tm_ctx* ctx, int enable);
 /* Synchronises the recorded events and fills *t. */

@@ -1,0 +1,477 @@
+// k_attention.cu -- triangle attention (starting and ending node) on the tensor cores, c_z = 128,
+// H = 4 heads of c = 32.
+//
+// The BioIR page ("BioIR da Nvidia acelera previsão de proteínas em 2,9x com PyTorch puro") names
+// triangle operations and pairwise attention among the Pairformer parts its kernels target; the
+// arithmetic is the AlphaFold3 / Boltz triangle attention around the starting node:
+//   zh = LN(z);  q, k, v, g = W_q zh, W_k zh, W_v zh, sigmoid(W_g zh);  b^h_jk = W_b^h zh_jk
+//   o_ij^h = g_ij^h * sum_k softmax_k(q_ij^h . k_ik^h / sqrt(c) + b_jk^h) v_ik^h  over keys m_i m_k = 1
+//   out_ij = W_o [o_ij^1 .. o_ij^H]
+// and the ending node is the same on the transposed grid (z_ji in, out_ji written).
+//
+// Two kernels.
+//   k_ta_project: per tile of 128 pairs (512 threads, four per pair), LayerNorm statistics from the
+//     pair's four channel quarters, zh into a 128 x 128 bf16 tile, one MMA each for q, k, v, g
+//     (TMEM columns 0..511), b on the CUDA cores. q, k and g are stored pair-major like z; v is stored
+//     per (row, head, channel) with the key index innermost, so that it is the K-major operand of the
+//     P V product; b per (head, j) with k innermost.
+//   k_ta_attend: per (row i, block of 128 queries j), heads one after another, keys in blocks of 128:
+//     S = Q K^T (tcgen05, TMEM), + bias tile, key mask, online softmax in registers (one thread per
+//     query row), P (bf16) into shared memory, O_blk = P V (tcgen05) added into the row's running
+//     output; the gated o of all heads forms a 128 x 128 tile and one more MMA applies W_o.
+#include "pair_tile.cuh"
+
+namespace tmk {
+namespace {
+
+using namespace pt;
+
+constexpr int kHeads = 4, kHd = 32;
+
+struct alignas(1024) TaProjSmem {
+  uint8_t zh[TILE], wq[TILE], wk[TILE], wv[TILE], wg[TILE];
+  float ln[2 * kC];                    // gamma, beta
+  float wb[kHeads * kC];               // W_b, float32
+  float2 zst[4][BT];                   // per channel quarter and pair: (mean, M2) of z
+  float bpart[4][kHeads][BT];          // per channel quarter: partial W_b zh
+  uint64_t bar;
+  uint32_t tmem_slot;
+  int abort_flag;
+};
+
+__global__ void __launch_bounds__(NT, 1) k_ta_project(const TaProjectParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  TaProjSmem& sm = *reinterpret_cast<TaProjSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int lq = warp & 3, h = warp >> 2;   // TMEM lane quarter; channel quarter = head
+  const int r = 32 * lq + lane;
+  const int c0 = 32 * h;
+  if (tid == 0) {
+    mbar_init(&sm.bar, 1);
+    sm.abort_flag = 0;
+    fence_mbar_init();
+  }
+  for (int k = tid; k < 2 * kC; k += NT) sm.ln[k] = p.ln[k];
+  for (int k = tid; k < kHeads * kC; k += NT) sm.wb[k] = p.w_b[k];
+  copy_tile(sm.wq, p.w_q);
+  copy_tile(sm.wk, p.w_k);
+  copy_tile(sm.wv, p.w_v);
+  copy_tile(sm.wg, p.w_g);
+  if (warp == 0) {
+    tmem_alloc(&sm.tmem_slot, 512);
+    tmem_relinquish();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_slot;
+  const uint32_t trow = tmem + ((uint32_t)(32 * lq) << 16);
+  const uint32_t a_zh = smem_u32(sm.zh);
+
+  uint32_t phase = 0;
+  for (long long t = blockIdx.x; t < p.tiles; t += gridDim.x) {
+    const long long pr = t * BT + r;          // pair (i, j) of the (possibly transposed) grid
+    const bool valid = pr < p.P;
+    const int i = valid ? (int)(pr / p.N) : 0;
+    const int j = valid ? (int)(pr - (long long)i * p.N) : 0;
+    const long long zp = p.transpose ? (long long)j * p.N + i : pr;   // the z pair it reads
+
+    // ---- LayerNorm of z: quarter statistics combined over the pair's four threads
+    float f[32];
+    if (valid) load32_bf16(p.z + zp * kC + c0, f);
+    else
+#pragma unroll
+      for (int e = 0; e < 32; ++e) f[e] = 0.f;
+    {
+      float s = 0.f;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) s += f[e];
+      const float m = s * (1.f / 32);
+      float m2 = 0.f;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) m2 = fmaf(f[e] - m, f[e] - m, m2);
+      sm.zst[h][r] = make_float2(m, m2);
+    }
+    __syncthreads();
+    float mu, rs;
+    {
+      const float2 q0 = sm.zst[0][r], q1 = sm.zst[1][r], q2 = sm.zst[2][r], q3 = sm.zst[3][r];
+      mu = ((q0.x + q1.x) + (q2.x + q3.x)) * 0.25f;
+      const float d0 = q0.x - mu, d1 = q1.x - mu, d2 = q2.x - mu, d3 = q3.x - mu;
+      const float m2 = ((q0.y + q1.y) + (q2.y + q3.y)) + 32.f * ((d0 * d0 + d1 * d1) + (d2 * d2 + d3 * d3));
+      rs = rsqrtf(m2 * (1.f / kC) + 1e-5f);
+    }
+    float bp[kHeads] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      f[e] = valid ? sm.ln[c0 + e] * ((f[e] - mu) * rs) + sm.ln[kC + c0 + e] : 0.f;
+#pragma unroll
+      for (int hh = 0; hh < kHeads; ++hh) bp[hh] = fmaf(sm.wb[hh * kC + c0 + e], f[e], bp[hh]);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) put8(sm.zh, r, c0 + 8 * u, f + 8 * u);
+#pragma unroll
+    for (int hh = 0; hh < kHeads; ++hh) sm.bpart[h][hh][r] = bp[hh];
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      mma_tile(tmem, a_zh, false, smem_u32(sm.wq), false, ID_KK, false);
+      mma_tile(tmem + kC, a_zh, false, smem_u32(sm.wk), false, ID_KK, false);
+      mma_tile(tmem + 2 * kC, a_zh, false, smem_u32(sm.wv), false, ID_KK, false);
+      mma_tile(tmem + 3 * kC, a_zh, false, smem_u32(sm.wg), false, ID_KK, false);
+      mma_commit(&sm.bar);
+    }
+    // b of head h for this pair: the four quarters' partial sums
+    if (valid) {
+      const float bsum = ((sm.bpart[0][h][r] + sm.bpart[1][h][r]) + sm.bpart[2][h][r]) + sm.bpart[3][h][r];
+      p.b[((long long)h * p.N + i) * p.ldb + j] = __float2bfloat16_rn(bsum);
+    }
+    if (!cta_wait(&sm.bar, phase, p.w, &sm.abort_flag, 1)) break;
+    phase ^= 1u;
+    tc_fence_after();
+
+    // ---- q, k, g pair-major (this head's 32 channels); v per (row, head, channel), key innermost
+#pragma unroll 1
+    for (int m = 0; m < 4; ++m) {
+      uint32_t rr[32];
+      tmem_ld32(trow + m * kC + c0, rr);
+      tmem_ld_wait();
+      if (!valid) continue;
+      float o[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) o[e] = m == 3 ? sigmoid_mufu(__uint_as_float(rr[e])) : __uint_as_float(rr[e]);
+      if (m == 2) {
+        __nv_bfloat16* vp = p.vt + ((long long)i * kC + c0) * p.ldv + j;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) vp[(long long)e * p.ldv] = __float2bfloat16_rn(o[e]);
+      } else {
+        __nv_bfloat16* dst = (m == 0 ? p.q : m == 1 ? p.k : p.g) + pr * kC + c0;
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          d4[u] = make_uint4(pack_bf16x2(o[8 * u], o[8 * u + 1]), pack_bf16x2(o[8 * u + 2], o[8 * u + 3]),
+                             pack_bf16x2(o[8 * u + 4], o[8 * u + 5]), pack_bf16x2(o[8 * u + 6], o[8 * u + 7]));
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+namespace {
+
+constexpr uint32_t kQBytes = 64 * 128 * 2;      // Q box: 64 channels (a head pair) x 128 queries
+constexpr uint32_t kKBytes = 64 * 128 * 2;      // K box: 64 channels x 128 keys
+constexpr uint32_t kVBytes = 64 * 32 * 2;       // one v box: 64 keys x 32 channels of one head
+constexpr uint32_t kBBytes = 64 * 128 * 2;      // one bias box: 64 keys x 128 queries
+
+static_assert(kBoxTaQK.bytes() == kQBytes && kBoxTaQK.bytes() == kKBytes, "Q/K box fills its slot");
+static_assert(kBoxTaV.bytes() == kVBytes, "v box fills its slot");
+static_assert(kBoxTaBias.bytes() == kBBytes, "bias box fills its slot");
+
+struct alignas(1024) TaAttSmem {
+  uint8_t q[kQBytes];
+  uint8_t k[kKBytes];
+  uint8_t b[2][kBBytes];                        // keys 0..63 and 64..127 of the block
+  uint8_t p[TILE];                              // P: 128 queries x 128 keys, bf16, K-major
+  uint8_t v[2][kVBytes];                        // keys 0..63 and 64..127, rows = channels
+  float kmask[BT];
+  uint64_t tma_bar, mma_bar;
+  uint32_t tmem_slot;
+  int abort_flag;
+};
+
+__global__ void __launch_bounds__(BT, 2) k_ta_attend(const __grid_constant__ CUtensorMap qmap,
+                                                     const __grid_constant__ CUtensorMap kmap,
+                                                     const __grid_constant__ CUtensorMap vmap,
+                                                     const __grid_constant__ CUtensorMap bmap,
+                                                     const TaAttendParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  TaAttSmem& sm = *reinterpret_cast<TaAttSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int i = (int)(blockIdx.x / p.jblocks);
+  const int jb = (int)(blockIdx.x - (long long)i * p.jblocks);
+  const int j = jb * BT + tid;
+  const bool jvalid = j < p.N;
+  __nv_bfloat16* orow = p.o + ((long long)i * p.N + j) * kC;
+  if (p.mask && p.mask[i] == 0.f) {
+    // no valid key in this row: o = 0
+    if (jvalid) {
+      uint4* d = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+      for (int u = 0; u < 16; ++u) d[u] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    return;
+  }
+  if (tid == 0) {
+    mbar_init(&sm.tma_bar, 1);
+    mbar_init(&sm.mma_bar, 1);
+    sm.abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&qmap);
+    tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&vmap);
+    tma_prefetch_desc(&bmap);
+  }
+  if (warp == 0) {
+    tmem_alloc(&sm.tmem_slot, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_slot;
+  const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
+  constexpr uint32_t ID_S = make_idesc(128, 128, FMT_BF16, false, false);
+  constexpr uint32_t ID_O = make_idesc(128, kHd, FMT_BF16, false, false);
+  const float kscale = 1.4426950408889634f * 0.17677669529663687f;   // log2(e) / sqrt(32)
+  const float klog2e = 1.4426950408889634f;
+  const int kblocks = (p.N + BT - 1) / BT;
+  uint32_t tph = 0, mph = 0;
+  bool ok = true;
+
+  for (int hp = 0; hp < 2 && ok; ++hp) {
+    for (int hh = 0; hh < 2 && ok; ++hh) {
+      const int h = 2 * hp + hh;
+      float m_run = -INFINITY, l_run = 0.f;
+      float acc[kHd];
+#pragma unroll
+      for (int e = 0; e < kHd; ++e) acc[e] = 0.f;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        // ---- loads of this key block (and of Q at the start of a head pair)
+        if (tid == 0) {
+          const bool with_q = hh == 0 && kb == 0;
+          mbar_expect_tx(&sm.tma_bar, kKBytes + 2 * kVBytes + 2 * kBBytes + (with_q ? kQBytes : 0u));
+          if (with_q) tma_load_3d(sm.q, &qmap, &sm.tma_bar, 64 * hp, jb * BT, i);
+          tma_load_3d(sm.k, &kmap, &sm.tma_bar, 64 * hp, kb * BT, i);
+          tma_load_3d(sm.v[0], &vmap, &sm.tma_bar, kb * BT, kHd * h, i);
+          tma_load_3d(sm.v[1], &vmap, &sm.tma_bar, kb * BT + 64, kHd * h, i);
+          tma_load_3d(sm.b[0], &bmap, &sm.tma_bar, kb * BT, jb * BT, h);
+          tma_load_3d(sm.b[1], &bmap, &sm.tma_bar, kb * BT + 64, jb * BT, h);
+        }
+        {
+          const int kk = kb * BT + tid;
+          sm.kmask[tid] = kk < p.N ? (p.mask ? p.mask[kk] : 1.f) : 0.f;
+        }
+        if (!cta_wait(&sm.tma_bar, tph, p.w, &sm.abort_flag, 1)) { ok = false; break; }
+        tph ^= 1u;
+        if (tid == 0) {
+          tc_fence_after();
+          const uint32_t q0 = smem_u32(sm.q) + 64 * hh, k0 = smem_u32(sm.k) + 64 * hh;
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks)
+            mma_f16(tmem, make_sdesc_sw128(q0 + 32 * ks, 16, 1024), make_sdesc_sw128(k0 + 32 * ks, 16, 1024), ID_S,
+                    ks ? 1u : 0u);
+          mma_commit(&sm.mma_bar);
+        }
+        if (!cta_wait(&sm.mma_bar, mph, p.w, &sm.abort_flag, 2)) { ok = false; break; }
+        mph ^= 1u;
+        tc_fence_after();
+
+        // ---- logits in the log2 domain: S log2(e)/sqrt(c) + b log2(e); masked keys -> -inf
+        float bmax = -INFINITY;
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t rs[32];
+          tmem_ld32(trow + 32 * ch, rs);
+          tmem_ld_wait();
+          const uint8_t* brow = sm.b[ch >> 1];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            float bv[8];
+            bf16x8_to_float(*reinterpret_cast<const uint4*>(brow + sw128_offset((uint32_t)tid, (uint32_t)((ch & 1) * 4 + u))), bv);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int kk = 32 * ch + 8 * u + e;
+              const float s = sm.kmask[kk] != 0.f ? fmaf(__uint_as_float(rs[8 * u + e]), kscale, bv[e] * klog2e) : -INFINITY;
+              bmax = fmaxf(bmax, s);
+            }
+          }
+        }
+        const float m_new = fmaxf(m_run, bmax);
+        const float alpha = m_new == -INFINITY ? 1.f : exp2f(m_run - m_new);
+        float lsum = 0.f;
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t rs[32];
+          tmem_ld32(trow + 32 * ch, rs);
+          tmem_ld_wait();
+          const uint8_t* brow = sm.b[ch >> 1];
+          float pv[32];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            float bv[8];
+            bf16x8_to_float(*reinterpret_cast<const uint4*>(brow + sw128_offset((uint32_t)tid, (uint32_t)((ch & 1) * 4 + u))), bv);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int kk = 32 * ch + 8 * u + e;
+              const float s = fmaf(__uint_as_float(rs[8 * u + e]), kscale, bv[e] * klog2e);
+              const float pe = (sm.kmask[kk] != 0.f && m_new != -INFINITY) ? exp2f(s - m_new) : 0.f;
+              pv[8 * u + e] = pe;
+              lsum += pe;
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) put8(sm.p, tid, 32 * ch + 8 * u, pv + 8 * u);
+        }
+        l_run = l_run * alpha + lsum;
+        m_run = m_new;
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+          tc_fence_after();
+          const uint32_t p0 = smem_u32(sm.p), v0 = smem_u32(sm.v[0]);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_f16(tmem + BT, make_sdesc_sw128(p0 + (ks >> 2) * SLAB + (ks & 3) * 32, 16, 1024),
+                    make_sdesc_sw128(v0 + (ks >> 2) * kVBytes + (ks & 3) * 32, 16, 1024), ID_O, ks ? 1u : 0u);
+          mma_commit(&sm.mma_bar);
+        }
+        if (!cta_wait(&sm.mma_bar, mph, p.w, &sm.abort_flag, 3)) { ok = false; break; }
+        mph ^= 1u;
+        tc_fence_after();
+        {
+          uint32_t ro[32];
+          tmem_ld32(trow + BT, ro);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < kHd; ++e) acc[e] = fmaf(acc[e], alpha, __uint_as_float(ro[e]));
+        }
+      }
+      if (!ok) break;
+      // ---- o = g * acc / l for this head
+      if (jvalid) {
+        float gv[kHd];
+        load32_bf16(p.g + ((long long)i * p.N + j) * kC + kHd * h, gv);
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        float o[kHd];
+#pragma unroll
+        for (int e = 0; e < kHd; ++e) o[e] = gv[e] * acc[e] * inv;
+        uint4* d4 = reinterpret_cast<uint4*>(orow + kHd * h);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          d4[u] = make_uint4(pack_bf16x2(o[8 * u], o[8 * u + 1]), pack_bf16x2(o[8 * u + 2], o[8 * u + 3]),
+                             pack_bf16x2(o[8 * u + 4], o[8 * u + 5]), pack_bf16x2(o[8 * u + 6], o[8 * u + 7]));
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+// out = W_o o per pair (512 threads, tiles of 128 pairs); for the ending node the pair (i, j) of the
+// transposed grid is written at (j, i).
+struct alignas(1024) TaOutSmem {
+  uint8_t o[TILE], wo[TILE];
+  uint64_t bar;
+  uint32_t tmem_slot;
+  int abort_flag;
+};
+
+__global__ void __launch_bounds__(NT, 1) k_ta_out(const TaOutParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  TaOutSmem& sm = *reinterpret_cast<TaOutSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int lq = warp & 3, h = warp >> 2;
+  const int r = 32 * lq + lane;
+  const int c0 = 32 * h;
+  if (tid == 0) {
+    mbar_init(&sm.bar, 1);
+    sm.abort_flag = 0;
+    fence_mbar_init();
+  }
+  copy_tile(sm.wo, p.w_o);
+  if (warp == 0) {
+    tmem_alloc(&sm.tmem_slot, 128);
+    tmem_relinquish();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_slot;
+  const uint32_t trow = tmem + ((uint32_t)(32 * lq) << 16);
+  uint32_t phase = 0;
+  for (long long t = blockIdx.x; t < p.tiles; t += gridDim.x) {
+    const long long pr = t * BT + r;
+    const bool valid = pr < p.P;
+    const int i = valid ? (int)(pr / p.N) : 0;
+    const int j = valid ? (int)(pr - (long long)i * p.N) : 0;
+    float f[32];
+    if (valid) load32_bf16(p.o + pr * kC + c0, f);
+    else
+#pragma unroll
+      for (int e = 0; e < 32; ++e) f[e] = 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) put8(sm.o, r, c0 + 8 * u, f + 8 * u);
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      mma_tile(tmem, smem_u32(sm.o), false, smem_u32(sm.wo), false, ID_KK, false);
+      mma_commit(&sm.bar);
+    }
+    if (!cta_wait(&sm.bar, phase, p.w, &sm.abort_flag, 1)) break;
+    phase ^= 1u;
+    tc_fence_after();
+    uint32_t rr[32];
+    tmem_ld32(trow + c0, rr);
+    tmem_ld_wait();
+    if (valid) {
+      const long long op = p.transpose ? (long long)j * p.N + i : pr;
+      uint4* d4 = reinterpret_cast<uint4*>(p.out + op * kC + c0);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        d4[u] = make_uint4(pack_bf16x2(__uint_as_float(rr[8 * u]), __uint_as_float(rr[8 * u + 1])),
+                           pack_bf16x2(__uint_as_float(rr[8 * u + 2]), __uint_as_float(rr[8 * u + 3])),
+                           pack_bf16x2(__uint_as_float(rr[8 * u + 4]), __uint_as_float(rr[8 * u + 5])),
+                           pack_bf16x2(__uint_as_float(rr[8 * u + 6]), __uint_as_float(rr[8 * u + 7])));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 128);
+}
+
+}  // namespace
+
+constexpr size_t kTaProjSmem = sizeof(TaProjSmem) + 1024;
+constexpr size_t kTaAttSmem = sizeof(TaAttSmem) + 1024;
+constexpr size_t kTaOutSmem = sizeof(TaOutSmem) + 1024;
+static_assert(kTaProjSmem <= 232448, "attention projection shared memory");
+static_assert(2 * kTaAttSmem <= 233472, "two attention CTAs per SM");
+static_assert(kTaOutSmem <= 232448, "attention output shared memory");
+
+cudaError_t launch_ta_project(const TaProjectParams& p, int grid, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(k_ta_project, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTaProjSmem);
+  if (e != cudaSuccess) return e;
+  k_ta_project<<<grid, NT, kTaProjSmem, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ta_attend(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                             const CUtensorMap& bmap, const TaAttendParams& p, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(k_ta_attend, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTaAttSmem);
+  if (e != cudaSuccess) return e;
+  const long long grid = (long long)p.N * p.jblocks;
+  k_ta_attend<<<(unsigned)grid, BT, kTaAttSmem, s>>>(qmap, kmap, vmap, bmap, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ta_out(const TaOutParams& p, int grid, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(k_ta_out, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTaOutSmem);
+  if (e != cudaSuccess) return e;
+  k_ta_out<<<grid, NT, kTaOutSmem, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace tmk

@@ -31,15 +31,12 @@
 // N = out), MMA 2 MN-major (B = W^T, N = in, K = out). TMEM: columns 0..255 hold MMA 1's two
 // results and then MMA 2's; columns 256..511 accumulate the two parameter gradients of MMA 3 over
 // every tile of the CTA, written out once as per-CTA partial sums (added in fixed order later).
-#include "tm_kernels.h"
+#include "pair_tile.cuh"
 
 namespace tmk {
 namespace {
 
-constexpr int BT = 128;                 // pairs per tile
-constexpr int NT = 512;                 // threads per CTA: 4 per pair, 32 channels each
-constexpr uint32_t TILE = 128 * 128 * 2;  // bytes of one 128 x 128 bf16 operand tile
-constexpr uint32_t SLAB = TILE / 2;       // one 64-channel half
+using namespace pt;
 
 struct alignas(1024) OutSmem {
   uint8_t zh[TILE], xh[TILE], dy[TILE], dgg[TILE], wg[TILE], wo[TILE];
@@ -62,77 +59,6 @@ struct alignas(1024) ProjSmem {
   int abort_flag;
 };
 
-// 8 floats -> one 16-byte unit of row `r` of an operand tile, for channels c0 .. c0+7 (c0 % 8 == 0)
-__device__ __forceinline__ void put8(uint8_t* tile, int r, int c0, const float* v) {
-  const uint4 q = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
-                             pack_bf16x2(v[6], v[7]));
-  *reinterpret_cast<uint4*>(tile + (c0 >> 6) * SLAB + sw128_offset((uint32_t)r, (uint32_t)((c0 & 63) >> 3))) = q;
-}
-
-__device__ __forceinline__ void bf16x8_to_float(const uint4& q, float* f) {
-  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    f[2 * k] = __uint_as_float(w[k] << 16);
-    f[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
-  }
-}
-
-// Copy a weight image (already in the tile layout) into shared memory, all threads.
-__device__ __forceinline__ void copy_tile(uint8_t* dst, const __nv_bfloat16* src) {
-  const uint4* s = reinterpret_cast<const uint4*>(src);
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll 4
-  for (int k = threadIdx.x; k < (int)(TILE / 16); k += NT) d[k] = s[k];
-}
-
-// 32 bf16 values (64 bytes) -> floats
-__device__ __forceinline__ void load32_bf16(const __nv_bfloat16* src, float* f) {
-  const uint4* q = reinterpret_cast<const uint4*>(src);
-  uint4 v[4];
-#pragma unroll
-  for (int u = 0; u < 4; ++u) v[u] = q[u];
-#pragma unroll
-  for (int u = 0; u < 4; ++u) bf16x8_to_float(v[u], f + 8 * u);
-}
-
-// Butterfly reduce-scatter over the 32 lanes of a warp: on return lane l holds the sum over the
-// lanes of v[l] (v is consumed).
-__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
-#pragma unroll
-  for (int half = 16; half >= 1; half >>= 1) {
-    const bool upper = (lane & half) != 0;
-#pragma unroll
-    for (int k = 0; k < half; ++k) {
-      const float keep = upper ? v[k + half] : v[k];
-      const float send = upper ? v[k] : v[k + half];
-      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, half);
-    }
-  }
-  return v[0];
-}
-
-// Issue helpers (one thread). K-major operand of a 128 x 128 tile: K = channels; MN-major operand:
-// K = the tile's rows (pairs, or the out index of a weight image).
-__device__ __forceinline__ uint64_t kdesc(uint32_t base, int ks) {
-  return make_sdesc_sw128(base + (uint32_t)((ks >> 2) * SLAB + (ks & 3) * 32), 16, 1024);
-}
-__device__ __forceinline__ uint64_t mndesc(uint32_t base, int ks) {
-  return make_sdesc_sw128(base + (uint32_t)ks * 2048u, SLAB, 1024);
-}
-constexpr uint32_t ID_KK = make_idesc(128, 128, FMT_BF16, false, false);
-constexpr uint32_t ID_KM = make_idesc(128, 128, FMT_BF16, false, true);
-constexpr uint32_t ID_MM = make_idesc(128, 128, FMT_BF16, true, true);
-
-// D (+)= A B^T over the 128 K of two tiles
-__device__ __forceinline__ void mma_tile(uint32_t d, uint32_t a, bool a_mn, uint32_t b, bool b_mn, uint32_t idesc,
-                                         bool acc) {
-#pragma unroll
-  for (int ks = 0; ks < 8; ++ks)
-    mma_f16(d, a_mn ? mndesc(a, ks) : kdesc(a, ks), b_mn ? mndesc(b, ks) : kdesc(b, ks), idesc,
-            (acc || ks != 0) ? 1u : 0u);
-}
-
 // L2 prefetch of bytes [b0, b1) of a buffer, widened to 16-byte bounds (the caller keeps the
 // widened range inside the buffer's allocation).
 __device__ __forceinline__ void prefetch_range(const void* base, long long b0, long long b1) {
@@ -148,12 +74,6 @@ __device__ __forceinline__ void prefetch_plane_rows(const float* plane, long lon
   const int n1 = (int)((p1 - p0) < (long long)(N - j0) ? (p1 - p0) : (long long)(N - j0));
   prefetch_range(plane + (long long)i * ld, 4ll * j0, 4ll * (j0 + n1));
   if (p0 + n1 < p1) prefetch_range(plane + (long long)(i + 1) * ld, 0, 4ll * (p1 - p0 - n1));
-}
-
-// Wait for the MMA barrier with a CTA-uniform outcome.
-__device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, const Watch& w, int* abort_flag, int site) {
-  const bool ok = wait_bounded(bar, parity, w, abort_flag, site);
-  return __syncthreads_and(ok) != 0;
 }
 
 }  // namespace

@@ -15,7 +15,8 @@ namespace tmk {
 // The host maps a small int array into device memory: [0] status code,
 // [1] kernel id, [2] wait site, [3] block index of the first failure.
 enum : int { ST_OK = 0, ST_TIMEOUT = 5 };
-enum : int { KID_PROJECT = 1, KID_CONTRACT = 2, KID_FINISH = 3, KID_BWD_OUTPUT = 4, KID_BWD_PROJECT = 5 };
+enum : int { KID_PROJECT = 1, KID_CONTRACT = 2, KID_FINISH = 3, KID_BWD_OUTPUT = 4, KID_BWD_PROJECT = 5,
+             KID_TA_PROJECT = 6, KID_TA_ATTEND = 7, KID_TA_OUT = 8 };
 
 struct Watch {
   int* status;                    // device-visible status word (mapped host memory)

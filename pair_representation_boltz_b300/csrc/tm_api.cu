@@ -68,6 +68,7 @@ struct TimedLaunch {
 }  // namespace
 
 struct tm_ctx {
+  int layer = 0;                 // 0: triangle multiplicative update, 1: triangle attention
   int device = 0, num_sms = 0;
   int c_z = 0, c_h = 0;
   // float32 weights (device), one allocation
@@ -86,6 +87,8 @@ struct tm_ctx {
   // backward pass: bf16 images of W_g, W_o, W_a, W_ga, W_b, W_gb in the 128 x 128 operand-tile layout
   // of the backward kernels, then gamma_in, beta_in, gamma_out, beta_out (float32)
   void* wbwd = nullptr;
+  // triangle attention: bf16 images of W_q, W_k, W_v, W_g, W_o, then gamma, beta and W_b (float32)
+  void* ta_w = nullptr;
   // status word (mapped host memory)
   int* status_h = nullptr;
   int* status_d = nullptr;
@@ -227,6 +230,18 @@ inline void split_bf16(double v, __nv_bfloat16* hi, __nv_bfloat16* lo) {
   *lo = __float2bfloat16_rn((float)(v - (double)__bfloat162float(*hi)));
 }
 
+// W [128][128] (row-major [out][in]) as bf16 in the 128-byte-swizzled K-major tile layout of the
+// per-pair kernels (64-column halves 16 KB apart, 128-byte rows, 16-byte unit u of row r at u ^ (r % 8)).
+void make_tile_image(const float* W, __nv_bfloat16* img) {
+  const int C = kC;
+  for (int r = 0; r < C; ++r)
+    for (int k = 0; k < C; ++k) {
+      const int half = k / 64, u = (k % 64) / 8, e = k % 8;
+      const size_t byte = (size_t)half * (C * 64 * 2) + (size_t)r * 128 + (size_t)((u ^ (r & 7)) * 16) + e * 2;
+      img[byte / 2] = __float2bfloat16_rn(W[(size_t)r * C + k]);
+    }
+}
+
 tm_status prepare_tensor_core_weights(tm_ctx* c, const tm_weights* w) {
   const int C = kC;
   std::vector<__nv_bfloat16> k1(2 * 2 * 256 * C);
@@ -317,13 +332,7 @@ tm_status prepare_tensor_core_weights(tm_ctx* c, const tm_weights* w) {
     // unit u of row r at unit u ^ (r % 8)).
     const float* src[6] = {w->w_g, w->w_o, w->w_a, w->w_ga, w->w_b, w->w_gb};
     std::vector<__nv_bfloat16> img(6 * C * C);
-    for (int m = 0; m < 6; ++m)
-      for (int r = 0; r < C; ++r)
-        for (int k = 0; k < C; ++k) {
-          const int half = k / 64, u = (k % 64) / 8, e = k % 8;
-          const size_t byte = (size_t)half * (C * 64 * 2) + (size_t)r * 128 + (size_t)((u ^ (r & 7)) * 16) + e * 2;
-          img[(size_t)m * C * C + byte / 2] = __float2bfloat16_rn(src[m][(size_t)r * C + k]);
-        }
+    for (int m = 0; m < 6; ++m) make_tile_image(src[m], img.data() + (size_t)m * C * C);
     std::vector<float> ln(4 * C);
     for (int k = 0; k < C; ++k) {
       ln[k] = w->ln_in_gamma[k];
@@ -507,6 +516,7 @@ int x16_exponent(const tm_ctx* c, int N) {
 tm_status check_common(tm_ctx* c, int N, tm_dtype dtype) {
   if (!c) return TM_ERR_INVALID;
   c->err.clear();
+  if (c->layer != 0) return fail(c, TM_ERR_INVALID, "this ctx holds a triangle attention layer (tm_attn_forward)");
   if (N < 1 || N > 65535) return fail(c, TM_ERR_INVALID, "N=%d outside [1, 65535]", N);
   if (dtype != TM_F32 && dtype != TM_BF16) return fail(c, TM_ERR_INVALID, "unknown dtype %d", (int)dtype);
   if (dtype == TM_BF16 && !c->tc)
@@ -819,7 +829,7 @@ void tm_destroy(tm_ctx* c) {
   cudaDeviceSynchronize();
   if (c->ws) cudaFree(c->ws);
   if (c->io) cudaFree(c->io);
-  for (void* p : {(void*)c->w32, (void*)c->wk1, (void*)c->k1c, (void*)c->wo16, (void*)c->wg16, c->wbwd})
+  for (void* p : {(void*)c->w32, (void*)c->wk1, (void*)c->k1c, (void*)c->wo16, (void*)c->wg16, c->wbwd, c->ta_w})
     if (p) cudaFree(p);
   if (c->status_h) cudaFreeHost(c->status_h);
   for (auto& t : c->timed) {
@@ -1069,6 +1079,166 @@ tm_status tm_backward(tm_ctx* c, const void* z, const float* mask, int N, tm_dty
     return backward_f32(c, reinterpret_cast<const float*>(z), mask, N, inc, reinterpret_cast<const float*>(dout),
                         reinterpret_cast<float*>(dz), grads, s, opt);
   return backward_bf16(c, z, mask, N, inc, dout, dz, grads, s, opt);
+}
+
+// ---------------------------------------------------------------------- triangle attention
+tm_status tm_attn_create(int c_z, int heads, int c_head, const tm_attn_weights* w, tm_ctx** out_ctx) {
+  if (!w || !out_ctx) return TM_ERR_INVALID;
+  const float* req[] = {w->ln_gamma, w->ln_beta, w->w_q, w->w_k, w->w_v, w->w_b, w->w_g, w->w_o};
+  for (const float* q : req)
+    if (!q) return TM_ERR_INVALID;
+  if (c_z < 1 || heads < 1 || c_head < 1) return TM_ERR_INVALID;
+  if (c_z != kC || heads != 4 || c_head != 32) return TM_ERR_UNSUPPORTED;
+  tm_ctx* c = new tm_ctx();
+  c->layer = 1;
+  cudaError_t e = cudaGetDevice(&c->device);
+  if (e != cudaSuccess) {
+    delete c;
+    cudaGetLastError();
+    return TM_ERR_CUDA;
+  }
+  cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
+  c->c_z = c_z;
+  c->c_h = heads * c_head;
+  if (const char* env = std::getenv("TM_WORKSPACE_LIMIT")) c->env_limit = (size_t)std::strtoull(env, nullptr, 10);
+  e = cudaHostAlloc(reinterpret_cast<void**>(&c->status_h), 64, cudaHostAllocMapped);
+  if (e != cudaSuccess) {
+    tm_destroy(c);
+    cudaGetLastError();
+    return TM_ERR_CUDA;
+  }
+  std::memset(c->status_h, 0, 64);
+  cudaHostGetDevicePointer(reinterpret_cast<void**>(&c->status_d), c->status_h, 0);
+  // bf16 tile images of W_q, W_k, W_v, W_g, W_o, then gamma, beta, W_b as float32
+  const size_t T = (size_t)kC * kC;
+  std::vector<__nv_bfloat16> img(5 * T);
+  const float* mats[5] = {w->w_q, w->w_k, w->w_v, w->w_g, w->w_o};
+  for (int m = 0; m < 5; ++m) make_tile_image(mats[m], img.data() + m * T);
+  std::vector<float> f(2 * kC + 4 * kC);
+  for (int k = 0; k < kC; ++k) {
+    f[k] = w->ln_gamma[k];
+    f[kC + k] = w->ln_beta[k];
+  }
+  for (int k = 0; k < 4 * kC; ++k) f[2 * kC + k] = w->w_b[k];
+  const size_t ib = img.size() * sizeof(img[0]);
+  e = cudaMalloc(&c->ta_w, ib + f.size() * sizeof(float));
+  if (e == cudaSuccess) e = cudaMemcpy(c->ta_w, img.data(), ib, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(reinterpret_cast<uint8_t*>(c->ta_w) + ib, f.data(), f.size() * sizeof(float), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    tm_destroy(c);
+    cudaGetLastError();
+    return TM_ERR_CUDA;
+  }
+  *out_ctx = c;
+  return TM_OK;
+}
+
+tm_status tm_attn_forward(tm_ctx* c, const void* z, const float* mask, int N, tm_dtype dtype, tm_attn_node node,
+                          void* out, void* stream, const tm_options* opt) {
+  if (!c) return TM_ERR_INVALID;
+  c->err.clear();
+  if (c->layer != 1) return fail(c, TM_ERR_INVALID, "this ctx holds a triangle multiplicative update (tm_forward)");
+  if (N < 1 || N > 65535) return fail(c, TM_ERR_INVALID, "N=%d outside [1, 65535]", N);
+  if (dtype != TM_BF16) return fail(c, dtype == TM_F32 ? TM_ERR_UNSUPPORTED : TM_ERR_INVALID, "triangle attention runs in bf16");
+  if (node != TM_ATTN_STARTING && node != TM_ATTN_ENDING) return fail(c, TM_ERR_INVALID, "unknown node %d", (int)node);
+  if (!z || !out || !aligned16(z) || !aligned16(out))
+    return fail(c, TM_ERR_INVALID, "z and out must be non-null and 16-byte aligned");
+  if (mask && (reinterpret_cast<uintptr_t>(mask) & 3u)) return fail(c, TM_ERR_INVALID, "mask must be 4-byte aligned");
+  if (opt) {
+    for (int r : opt->reserved)
+      if (r) return fail(c, TM_ERR_INVALID, "tm_options.reserved must be zero");
+    if (opt->block || opt->x_storage || opt->residual || opt->timeout_ms < 0)
+      return fail(c, TM_ERR_INVALID, "tm_attn_forward takes only timeout_ms and workspace_limit");
+  }
+  int dev = -1;
+  cudaGetDevice(&dev);
+  if (dev != c->device) return fail(c, TM_ERR_INVALID, "current device %d is not the ctx's device %d", dev, c->device);
+  tm_status st = check_device_status(c);
+  if (st != TM_OK) return st;
+  const size_t zbytes = (size_t)N * N * kC * 2;
+  if (ranges_overlap(z, zbytes, out, zbytes)) return fail(c, TM_ERR_INVALID, "out overlaps z");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool tr = node == TM_ATTN_ENDING;
+  const long long P = (long long)N * N;
+  const long long ldv = (long long)align_up(N, 64), ldb = ldv;
+  const size_t pb = align_up(zbytes, 256);
+  const size_t vb = align_up((size_t)N * kC * ldv * 2, 256);
+  const size_t bb = align_up((size_t)4 * N * ldb * 2, 256);
+  st = ensure_workspace(c, 4 * pb + vb + bb, s, opt);
+  if (st != TM_OK) return st;
+  uint8_t* q8 = reinterpret_cast<uint8_t*>(c->ws);
+  auto* q = reinterpret_cast<__nv_bfloat16*>(q8);
+  auto* k = reinterpret_cast<__nv_bfloat16*>(q8 + pb);
+  auto* g = reinterpret_cast<__nv_bfloat16*>(q8 + 2 * pb);
+  auto* o = reinterpret_cast<__nv_bfloat16*>(q8 + 3 * pb);
+  auto* vt = reinterpret_cast<__nv_bfloat16*>(q8 + 4 * pb);
+  auto* bias = reinterpret_cast<__nv_bfloat16*>(q8 + 4 * pb + vb);
+  const auto* wimg = reinterpret_cast<const __nv_bfloat16*>(c->ta_w);
+  const float* wf = reinterpret_cast<const float*>(wimg + 5 * kC * kC);
+  const long long tiles = (P + 127) / 128;
+  const int grid = (int)std::min<long long>(tiles, c->num_sms);
+
+  TaProjectParams pp{};
+  pp.z = reinterpret_cast<const __nv_bfloat16*>(z);
+  pp.transpose = tr ? 1 : 0;
+  pp.ln = wf;
+  pp.w_b = wf + 2 * kC;
+  pp.w_q = wimg;
+  pp.w_k = wimg + kC * kC;
+  pp.w_v = wimg + 2 * kC * kC;
+  pp.w_g = wimg + 3 * kC * kC;
+  pp.q = q;
+  pp.k = k;
+  pp.g = g;
+  pp.vt = vt;
+  pp.b = bias;
+  pp.ldv = ldv;
+  pp.ldb = ldb;
+  pp.N = N;
+  pp.P = P;
+  pp.tiles = tiles;
+  pp.w = watch(c, KID_TA_PROJECT, opt);
+  cudaError_t e = timed(c, 8, P, s, [&] { return launch_ta_project(pp, grid, s); });
+  if (e != cudaSuccess) return cuda_fail(c, e, "attention projection launch");
+
+  CUtensorMap qmap, kmap, vmap, bmap;
+  {
+    const cuuint64_t d[3] = {(cuuint64_t)kC, (cuuint64_t)N, (cuuint64_t)N};
+    const cuuint64_t st2[2] = {(cuuint64_t)kC * 2, (cuuint64_t)N * kC * 2};
+    if (!encode(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, d, st2, kBoxTaQK, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, k, d, st2, kBoxTaQK, CU_TENSOR_MAP_SWIZZLE_128B))
+      return fail(c, TM_ERR_CUDA, "tensor map (q/k)");
+    const cuuint64_t dv[3] = {(cuuint64_t)N, (cuuint64_t)kC, (cuuint64_t)N};
+    const cuuint64_t sv[2] = {(cuuint64_t)ldv * 2, (cuuint64_t)kC * ldv * 2};
+    if (!encode(&vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, vt, dv, sv, kBoxTaV, CU_TENSOR_MAP_SWIZZLE_128B))
+      return fail(c, TM_ERR_CUDA, "tensor map (v)");
+    const cuuint64_t db[3] = {(cuuint64_t)N, (cuuint64_t)N, 4};
+    const cuuint64_t sb[2] = {(cuuint64_t)ldb * 2, (cuuint64_t)N * ldb * 2};
+    if (!encode(&bmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, bias, db, sb, kBoxTaBias, CU_TENSOR_MAP_SWIZZLE_128B))
+      return fail(c, TM_ERR_CUDA, "tensor map (bias)");
+  }
+  TaAttendParams pa{};
+  pa.mask = mask;
+  pa.g = g;
+  pa.o = o;
+  pa.N = N;
+  pa.jblocks = (N + 127) / 128;
+  pa.w = watch(c, KID_TA_ATTEND, opt);
+  e = timed(c, 9, P, s, [&] { return launch_ta_attend(qmap, kmap, vmap, bmap, pa, s); });
+  if (e != cudaSuccess) return cuda_fail(c, e, "attention launch");
+
+  TaOutParams po{};
+  po.o = o;
+  po.w_o = wimg + 4 * kC * kC;
+  po.out = reinterpret_cast<__nv_bfloat16*>(out);
+  po.transpose = tr ? 1 : 0;
+  po.N = N;
+  po.P = P;
+  po.tiles = tiles;
+  po.w = watch(c, KID_TA_OUT, opt);
+  e = timed(c, 10, P, s, [&] { return launch_ta_out(po, grid, s); });
+  return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "attention output launch");
 }
 
 tm_status tm_sync_status(tm_ctx* c, void* stream) {

@@ -196,6 +196,47 @@ struct SumJobs {
 };
 cudaError_t launch_sum_parts_multi(const SumJobs& j, int S, cudaStream_t s);
 
+// Triangle attention, bf16 tensor-core path (k_attention.cu): c_z = 128, 4 heads of 32. The grid may be
+// the transposed one (ending node): pair (i, j) then reads z at (j, i) and writes out at (j, i).
+struct TaProjectParams {
+  const __nv_bfloat16* z;           // [N][N][128]
+  int transpose;
+  const float* ln;                  // gamma, beta (float32, 2 x 128)
+  const float* w_b;                 // [4][128] float32
+  const __nv_bfloat16 *w_q, *w_k, *w_v, *w_g;   // bf16 tile images
+  __nv_bfloat16 *q, *k, *g;         // [N][N][128] pair-major
+  __nv_bfloat16* vt;                // [N][128][ldv]: row i, (head, channel), key
+  __nv_bfloat16* b;                 // [4][N][ldb]: head, j, k
+  long long ldv, ldb;
+  int N;
+  long long P, tiles;
+  Watch w;
+};
+struct TaAttendParams {
+  const float* mask;                // [N] or nullptr
+  const __nv_bfloat16* g;           // [N][N][128]
+  __nv_bfloat16* o;                 // [N][N][128]: gated attention output of every head
+  int N, jblocks;
+  Watch w;
+};
+struct TaOutParams {
+  const __nv_bfloat16* o;
+  const __nv_bfloat16* w_o;         // bf16 tile image of W_o [128][128]
+  __nv_bfloat16* out;               // [N][N][128]
+  int transpose;
+  int N;
+  long long P, tiles;
+  Watch w;
+};
+cudaError_t launch_ta_project(const TaProjectParams& p, int grid, cudaStream_t s);
+cudaError_t launch_ta_attend(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                             const CUtensorMap& bmap, const TaAttendParams& p, cudaStream_t s);
+cudaError_t launch_ta_out(const TaOutParams& p, int grid, cudaStream_t s);
+// Box shapes of the attention kernel's tensor maps (elements innermost first, 128-byte swizzle).
+constexpr Box kBoxTaQK{64, 128, 1, 2};     // 64 channels (a head pair) x 128 positions of one row
+constexpr Box kBoxTaV{64, 32, 1, 2};       // 64 keys x 32 channels of one head of one row
+constexpr Box kBoxTaBias{64, 128, 1, 2};   // 64 keys x 128 queries of one head
+
 // ----------------------------------------------------------------- diagnostics
 enum : int { KID_SELFTEST = 9 };
 cudaError_t launch_watchdog_selftest(const Watch& w, cudaStream_t s);

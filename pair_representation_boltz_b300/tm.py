@@ -7,7 +7,7 @@ streams only. There is no fallback: without the built library or without a
 GPU every call raises.
 
 The function names mirror the C ABI: tm_create, tm_forward, tm_forward_ex, tm_forward_host,
-tm_forward_noalloc, tm_pair_update, tm_backward,
+tm_forward_noalloc, tm_pair_update, tm_backward, tm_attn_create, tm_attn_forward,
 tm_project, tm_contract, tm_finish, tm_sync_status, tm_watchdog_selftest, tm_set_timing,
 tm_get_timing, tm_launch_count, tm_workspace_bytes, tm_status_string,
 tm_last_error, tm_destroy. ``TriMul`` wraps a context for convenience.
@@ -47,7 +47,15 @@ class TmOptions(C.Structure):
 
 
 class TmTiming(C.Structure):
-    _fields_ = [("launches", C.c_int * 8), ("ms", C.c_double * 8), ("units", C.c_longlong * 8)]
+    _fields_ = [("launches", C.c_int * 12), ("ms", C.c_double * 12), ("units", C.c_longlong * 12)]
+
+
+ATTN_WEIGHT_FIELDS = ("ln_gamma", "ln_beta", "w_q", "w_k", "w_v", "w_g", "w_b", "w_o")
+ATTN_NODES = {"starting": 0, "ending": 1}
+
+
+class TmAttnWeights(C.Structure):
+    _fields_ = [(n, C.POINTER(C.c_float)) for n in ATTN_WEIGHT_FIELDS]
 
 
 class TmGrads(C.Structure):
@@ -84,6 +92,8 @@ def load_library(path: str = LIB_PATH):
         "tm_contract": (st, [vp, vp, vp, i, i, i, i, i, i, i, i, vp, i, vp]),
         "tm_finish": (st, [vp, vp, i, vp, i, i, i, i, i, i, vp, vp]),
         "tm_backward": (st, [vp, vp, vp, i, i, i, vp, vp, C.POINTER(TmGrads), vp, C.POINTER(TmOptions)]),
+        "tm_attn_create": (st, [i, i, i, C.POINTER(TmAttnWeights), C.POINTER(vp)]),
+        "tm_attn_forward": (st, [vp, vp, vp, i, i, i, vp, vp, C.POINTER(TmOptions)]),
         "tm_sync_status": (st, [vp, vp]),
         "tm_watchdog_selftest": (st, [vp, i, vp]),
         "tm_set_timing": (st, [vp, i]),
@@ -268,6 +278,26 @@ def tm_backward(ctx, z, mask, direction, dout, dz, grads=None, stream=None, time
     return dz
 
 
+def tm_attn_create(c_z: int, heads: int, c_head: int, weights: dict):
+    """A triangle attention context from host float32 weights (dict of numpy arrays, [out][in])."""
+    lib = load_library()
+    arrays = {k: np.ascontiguousarray(weights[k], dtype=np.float32) for k in ATTN_WEIGHT_FIELDS}
+    w = TmAttnWeights(*[arrays[k].ctypes.data_as(C.POINTER(C.c_float)) for k in ATTN_WEIGHT_FIELDS])
+    ctx = C.c_void_p()
+    _check(None, lib.tm_attn_create(c_z, heads, c_head, C.byref(w), C.byref(ctx)))
+    return ctx
+
+
+def tm_attn_forward(ctx, z, mask, node, out, stream=None, timeout_ms=0, workspace_limit=0):
+    """out = triangle attention ("starting" or "ending" node) of bf16 z [N][N][128]."""
+    N = z.shape[0]
+    opt = TmOptions(0, timeout_ms, workspace_limit, 0, 0)
+    _check(ctx, load_library().tm_attn_forward(ctx, _ptr(z), _ptr(mask), N, _dtype_code(z),
+                                               ATTN_NODES[node] if isinstance(node, str) else int(node),
+                                               _ptr(out), _stream(stream), C.byref(opt)))
+    return out
+
+
 def tm_sync_status(ctx, stream=None) -> int:
     return load_library().tm_sync_status(ctx, _stream(stream))
 
@@ -283,7 +313,8 @@ def tm_set_timing(ctx, enable: bool) -> None:
 def tm_get_timing(ctx) -> dict:
     t = TmTiming()
     _check(ctx, load_library().tm_get_timing(ctx, C.byref(t)))
-    names = ("project", "contract", "finish", "f32", "out_backward", "proj_backward", "aux_backward", "unused")
+    names = ("project", "contract", "finish", "f32", "out_backward", "proj_backward", "aux_backward", "unused7",
+             "attn_project", "attn_attend", "attn_out", "unused11")
     return {n: {"launches": t.launches[k], "ms": t.ms[k], "units": t.units[k]} for k, n in enumerate(names)}
 
 
@@ -295,7 +326,31 @@ def tm_workspace_bytes(ctx) -> int:
     return load_library().tm_workspace_bytes(ctx)
 
 
-# ------------------------------------------------------------------ convenience wrapper
+# ------------------------------------------------------------------ convenience wrappers
+
+class TriangleAttention:
+    """A libtm triangle attention layer: ``TriangleAttention(weights)(z, mask, "starting")``."""
+
+    def __init__(self, weights: dict, c_z: int = 128, heads: int = 4, c_head: int = 32):
+        self.ctx = tm_attn_create(c_z, heads, c_head, weights)
+
+    def __call__(self, z, mask=None, node="starting", out=None, stream=None, **opts):
+        import torch
+        if out is None:
+            out = torch.empty_like(z)
+        return tm_attn_forward(self.ctx, z, mask, node, out, stream, **opts)
+
+    def close(self):
+        if self.ctx:
+            tm_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
 
 class TriMul:
     """A libtm context: ``TriMul(c_z, c_hidden, weights)(z, mask, "outgoing")``."""

@@ -1,0 +1,76 @@
+"""Precision floor of the bf16 triangle attention: the oracle's arithmetic with bf16 rounding at the
+values the bf16 path stores in bf16, against the exact float64 result.
+
+A model of the path's storage, not of its code: zh (the operand of the projections), the weights
+W_q, W_k, W_v, W_g, W_o, the stored q, k, v, g and pair bias b, the softmax numerator's weights P
+(a bf16 operand of the P V product; the denominator sums them unrounded), the gated output o and
+the result are each rounded once to bf16; everything else is exact.
+
+Run as a script to print the floor of the test cases: python -m tests.bf16_attention_floor
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+import oracle
+import oracle.triangle_attention as TA
+import workloads as wl
+
+r16 = oracle.round_to_bf16
+
+
+def emulated(z, mask, W, node, heads=4, c=32):
+    if node == "ending":
+        return np.swapaxes(emulated(np.swapaxes(z, 0, 1), mask, W, "starting", heads, c), 0, 1)
+    W = {k: np.asarray(v, np.float64) for k, v in W.items()}
+    N = z.shape[0]
+    m = np.asarray(mask, np.float64)
+    zh = oracle.layer_norm(z, W["ln_gamma"], W["ln_beta"])
+    zb = r16(zh)
+    q = r16(zb @ r16(W["w_q"]).T).reshape(N, N, heads, c)
+    k = r16(zb @ r16(W["w_k"]).T).reshape(N, N, heads, c)
+    v = r16(zb @ r16(W["w_v"]).T).reshape(N, N, heads, c)
+    g = r16(oracle.sigmoid(zb @ r16(W["w_g"]).T)).reshape(N, N, heads, c)
+    b = r16(np.moveaxis(zh @ W["w_b"].T, -1, 0))
+    s = np.einsum("ijhc,ikhc->ihjk", q, k) / math.sqrt(c) + b[None]
+    valid = (np.outer(m, m) != 0)[:, None, None, :]
+    s = np.where(valid, s, -np.inf)
+    smax = np.max(s, axis=-1, keepdims=True)
+    smax = np.where(np.isfinite(smax), smax, 0.0)
+    e = np.where(valid, np.exp(s - smax), 0.0)
+    den = e.sum(axis=-1, keepdims=True)
+    num = np.einsum("ihjk,ikhc->ijhc", r16(e), v)
+    den = np.moveaxis(den, 1, 2)                               # [i][j][h][1]
+    o = r16(g * np.where(den > 0, num / np.where(den > 0, den, 1.0), 0.0))
+    return r16(o.reshape(N, N, heads * c) @ r16(W["w_o"]).T)
+
+
+def attention_weights(seed=1):
+    """The weights of the GPU tests: N(0, 1/fan_in), random LayerNorm affine."""
+    rng = np.random.default_rng(seed)
+    W = {k: (rng.standard_normal(s) / math.sqrt(s[-1])).astype(np.float32)
+         for k, s in TA.weight_shapes(128, 4, 32).items()}
+    W["ln_gamma"] = (1.0 + 0.3 * rng.standard_normal(128)).astype(np.float32)
+    W["ln_beta"] = (0.3 * rng.standard_normal(128)).astype(np.float32)
+    return W
+
+
+def floor(N, mask, node, seed_z, seed_m=12, rms=False):
+    """max|model - exact| / rms(exact) for the inputs of the GPU test case (with rms=True, also
+    rms(model - exact) / rms(exact))."""
+    W = attention_weights()
+    z = wl.as_f64(wl.make_z(N, 128, seed_z, "bf16"))
+    m = wl.make_mask(N, mask, seed_m)
+    ex = TA.full(z, m, W, node)
+    em = emulated(z, m, W, node)
+    r = np.sqrt(np.mean(ex ** 2))
+    mx = float(np.max(np.abs(em - ex)) / r)
+    return (mx, float(np.sqrt(np.mean((em - ex) ** 2)) / r)) if rms else mx
+
+
+if __name__ == "__main__":
+    for N, mask in ((64, "scatter"), (129, "last10pct"), (200, "scatter")):
+        for node in TA.NODES:
+            print(N, mask, node, f"{floor(N, mask, node, 31 + N):.4f}")

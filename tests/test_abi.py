@@ -57,7 +57,7 @@ def test_options_struct_layout():
     assert tm.TmOptions.workspace_limit.offset == 8
     assert tm.TmOptions.x_storage.offset == 16
     assert tm.TmOptions.residual.offset == 20
-    assert ctypes.sizeof(tm.TmTiming) == 32 + 64 + 64
+    assert ctypes.sizeof(tm.TmTiming) == 48 + 96 + 96
     assert ctypes.sizeof(tm.TmGrads) == 10 * 8
 
 
