@@ -126,8 +126,10 @@ __global__ void __launch_bounds__(NT, 1) k_ta_project(const TaProjectParams p) {
     }
     // b of head h for this pair: the four quarters' partial sums
     if (valid) {
+      // the bias of query i and key j; a masked key j gets -inf, which removes it from every softmax
       const float bsum = ((sm.bpart[0][h][r] + sm.bpart[1][h][r]) + sm.bpart[2][h][r]) + sm.bpart[3][h][r];
-      p.b[((long long)h * p.N + i) * p.ldb + j] = __float2bfloat16_rn(bsum);
+      const bool kmasked = p.mask && p.mask[j] == 0.f;
+      p.b[((long long)h * p.N + i) * p.ldb + j] = __float2bfloat16_rn(kmasked ? -INFINITY : bsum);
     }
     if (!cta_wait(&sm.bar, phase, p.w, &sm.abort_flag, 1)) break;
     phase ^= 1u;
@@ -181,31 +183,42 @@ struct alignas(1024) TaAttSmem {
   uint8_t b[2][kBBytes];                        // keys 0..63 and 64..127 of the block
   uint8_t p[TILE];                              // P: 128 queries x 128 keys, bf16, K-major
   uint8_t v[2][kVBytes];                        // keys 0..63 and 64..127, rows = channels
-  float kmask[BT];
+  float xmax[2][BT];                            // per key half and query: block maximum
+  float xl[2][BT];                              // per key half and query: softmax denominator
   uint64_t tma_bar, mma_bar;
   uint32_t tmem_slot;
   int abort_flag;
 };
 
-__global__ void __launch_bounds__(BT, 2) k_ta_attend(const __grid_constant__ CUtensorMap qmap,
-                                                     const __grid_constant__ CUtensorMap kmap,
-                                                     const __grid_constant__ CUtensorMap vmap,
-                                                     const __grid_constant__ CUtensorMap bmap,
-                                                     const TaAttendParams p) {
+constexpr int kAttThreads = 256;   // two threads per query row, 64 keys of each block each
+
+__device__ __forceinline__ float ex2_approx(float v) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+__global__ void __launch_bounds__(kAttThreads, 2) k_ta_attend(const __grid_constant__ CUtensorMap qmap,
+                                                              const __grid_constant__ CUtensorMap kmap,
+                                                              const __grid_constant__ CUtensorMap vmap,
+                                                              const __grid_constant__ CUtensorMap bmap,
+                                                              const TaAttendParams p) {
   extern __shared__ uint8_t smem_raw[];
   TaAttSmem& sm = *reinterpret_cast<TaAttSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int row = 32 * (warp & 3) + lane;      // query row of the block (TMEM lane)
+  const int kh = warp >> 2;                    // key half of every block; output channels 16 kh ..
   const int i = (int)(blockIdx.x / p.jblocks);
   const int jb = (int)(blockIdx.x - (long long)i * p.jblocks);
-  const int j = jb * BT + tid;
+  const int j = jb * BT + row;
   const bool jvalid = j < p.N;
   __nv_bfloat16* orow = p.o + ((long long)i * p.N + j) * kC;
   if (p.mask && p.mask[i] == 0.f) {
     // no valid key in this row: o = 0
     if (jvalid) {
-      uint4* d = reinterpret_cast<uint4*>(orow);
+      uint4* d = reinterpret_cast<uint4*>(orow) + 8 * kh;
 #pragma unroll
-      for (int u = 0; u < 16; ++u) d[u] = make_uint4(0u, 0u, 0u, 0u);
+      for (int u = 0; u < 8; ++u) d[u] = make_uint4(0u, 0u, 0u, 0u);
     }
     return;
   }
@@ -227,7 +240,7 @@ __global__ void __launch_bounds__(BT, 2) k_ta_attend(const __grid_constant__ CUt
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_slot;
-  const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
+  const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
   constexpr uint32_t ID_S = make_idesc(128, 128, FMT_BF16, false, false);
   constexpr uint32_t ID_O = make_idesc(128, kHd, FMT_BF16, false, false);
   const float kscale = 1.4426950408889634f * 0.17677669529663687f;   // log2(e) / sqrt(32)
@@ -240,9 +253,9 @@ __global__ void __launch_bounds__(BT, 2) k_ta_attend(const __grid_constant__ CUt
     for (int hh = 0; hh < 2 && ok; ++hh) {
       const int h = 2 * hp + hh;
       float m_run = -INFINITY, l_run = 0.f;
-      float acc[kHd];
+      float acc[16];
 #pragma unroll
-      for (int e = 0; e < kHd; ++e) acc[e] = 0.f;
+      for (int e = 0; e < 16; ++e) acc[e] = 0.f;
       for (int kb = 0; kb < kblocks; ++kb) {
         // ---- loads of this key block (and of Q at the start of a head pair)
         if (tid == 0) {
@@ -254,10 +267,6 @@ __global__ void __launch_bounds__(BT, 2) k_ta_attend(const __grid_constant__ CUt
           tma_load_3d(sm.v[1], &vmap, &sm.tma_bar, kb * BT + 64, kHd * h, i);
           tma_load_3d(sm.b[0], &bmap, &sm.tma_bar, kb * BT, jb * BT, h);
           tma_load_3d(sm.b[1], &bmap, &sm.tma_bar, kb * BT + 64, jb * BT, h);
-        }
-        {
-          const int kk = kb * BT + tid;
-          sm.kmask[tid] = kk < p.N ? (p.mask ? p.mask[kk] : 1.f) : 0.f;
         }
         if (!cta_wait(&sm.tma_bar, tph, p.w, &sm.abort_flag, 1)) { ok = false; break; }
         tph ^= 1u;
@@ -274,51 +283,50 @@ __global__ void __launch_bounds__(BT, 2) k_ta_attend(const __grid_constant__ CUt
         mph ^= 1u;
         tc_fence_after();
 
-        // ---- logits in the log2 domain: S log2(e)/sqrt(c) + b log2(e); masked keys -> -inf
-        float bmax = -INFINITY;
-#pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {
-          uint32_t rs[32];
-          tmem_ld32(trow + 32 * ch, rs);
+        // ---- this thread's 64 logits, log2 domain: S log2(e)/sqrt(c) + b log2(e) (b is -inf at masked
+        // keys); keys past the grid (last block only) -> -inf
+        float sv[64];
+        {
+          uint32_t r0[32], r1[32];
+          tmem_ld32(trow + 64 * kh, r0);
+          tmem_ld32(trow + 64 * kh + 32, r1);
           tmem_ld_wait();
-          const uint8_t* brow = sm.b[ch >> 1];
+          const uint8_t* brow = sm.b[kh];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
+          for (int u = 0; u < 8; ++u) {
             float bv[8];
-            bf16x8_to_float(*reinterpret_cast<const uint4*>(brow + sw128_offset((uint32_t)tid, (uint32_t)((ch & 1) * 4 + u))), bv);
+            bf16x8_to_float(*reinterpret_cast<const uint4*>(brow + sw128_offset((uint32_t)row, (uint32_t)u)), bv);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-              const int kk = 32 * ch + 8 * u + e;
-              const float s = sm.kmask[kk] != 0.f ? fmaf(__uint_as_float(rs[8 * u + e]), kscale, bv[e] * klog2e) : -INFINITY;
-              bmax = fmaxf(bmax, s);
+              const uint32_t raw = u < 4 ? r0[8 * u + e] : r1[8 * (u - 4) + e];
+              sv[8 * u + e] = fmaf(__uint_as_float(raw), kscale, bv[e] * klog2e);
             }
           }
         }
-        const float m_new = fmaxf(m_run, bmax);
-        const float alpha = m_new == -INFINITY ? 1.f : exp2f(m_run - m_new);
+        if (kb == kblocks - 1) {
+          const int kbase = kb * BT + 64 * kh;
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (kbase + e >= p.N) sv[e] = -INFINITY;
+        }
+        float bmax = sv[0];
+#pragma unroll
+        for (int e = 1; e < 64; ++e) bmax = fmaxf(bmax, sv[e]);
+        sm.xmax[kh][row] = bmax;
+        __syncthreads();
+        const float m_new = fmaxf(m_run, fmaxf(sm.xmax[0][row], sm.xmax[1][row]));
+        const float mref = m_new == -INFINITY ? 0.f : m_new;
+        const float alpha = ex2_approx(m_run - mref);
         float lsum = 0.f;
-#pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {
-          uint32_t rs[32];
-          tmem_ld32(trow + 32 * ch, rs);
-          tmem_ld_wait();
-          const uint8_t* brow = sm.b[ch >> 1];
-          float pv[32];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            float bv[8];
-            bf16x8_to_float(*reinterpret_cast<const uint4*>(brow + sw128_offset((uint32_t)tid, (uint32_t)((ch & 1) * 4 + u))), bv);
+        for (int u = 0; u < 8; ++u) {
+          float pv[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int kk = 32 * ch + 8 * u + e;
-              const float s = fmaf(__uint_as_float(rs[8 * u + e]), kscale, bv[e] * klog2e);
-              const float pe = (sm.kmask[kk] != 0.f && m_new != -INFINITY) ? exp2f(s - m_new) : 0.f;
-              pv[8 * u + e] = pe;
-              lsum += pe;
-            }
+          for (int e = 0; e < 8; ++e) {
+            pv[e] = ex2_approx(sv[8 * u + e] - mref);
+            lsum += pv[e];
           }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) put8(sm.p, tid, 32 * ch + 8 * u, pv + 8 * u);
+          put8(sm.p, row, 64 * kh + 8 * u, pv);
         }
         l_run = l_run * alpha + lsum;
         m_run = m_new;
@@ -338,25 +346,34 @@ __global__ void __launch_bounds__(BT, 2) k_ta_attend(const __grid_constant__ CUt
         mph ^= 1u;
         tc_fence_after();
         {
-          uint32_t ro[32];
-          tmem_ld32(trow + BT, ro);
+          uint32_t ro[16];
+          tmem_ld16(trow + BT + 16 * kh, ro);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < kHd; ++e) acc[e] = fmaf(acc[e], alpha, __uint_as_float(ro[e]));
+          for (int e = 0; e < 16; ++e) acc[e] = fmaf(acc[e], alpha, __uint_as_float(ro[e]));
         }
       }
       if (!ok) break;
-      // ---- o = g * acc / l for this head
+      // ---- the denominator is the sum of both key halves; o = g * acc / l for 16 channels of this head
+      sm.xl[kh][row] = l_run;
+      __syncthreads();
+      const float l_tot = sm.xl[0][row] + sm.xl[1][row];
       if (jvalid) {
-        float gv[kHd];
-        load32_bf16(p.g + ((long long)i * p.N + j) * kC + kHd * h, gv);
-        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-        float o[kHd];
+        const int cb = kHd * h + 16 * kh;
+        float gv[16];
+        {
+          const uint4* gq = reinterpret_cast<const uint4*>(p.g + ((long long)i * p.N + j) * kC + cb);
+          const uint4 g0 = gq[0], g1 = gq[1];
+          bf16x8_to_float(g0, gv);
+          bf16x8_to_float(g1, gv + 8);
+        }
+        const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+        float o[16];
 #pragma unroll
-        for (int e = 0; e < kHd; ++e) o[e] = gv[e] * acc[e] * inv;
-        uint4* d4 = reinterpret_cast<uint4*>(orow + kHd * h);
+        for (int e = 0; e < 16; ++e) o[e] = gv[e] * acc[e] * inv;
+        uint4* d4 = reinterpret_cast<uint4*>(orow + cb);
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
+        for (int u = 0; u < 2; ++u)
           d4[u] = make_uint4(pack_bf16x2(o[8 * u], o[8 * u + 1]), pack_bf16x2(o[8 * u + 2], o[8 * u + 3]),
                              pack_bf16x2(o[8 * u + 4], o[8 * u + 5]), pack_bf16x2(o[8 * u + 6], o[8 * u + 7]));
       }
@@ -463,7 +480,7 @@ cudaError_t launch_ta_attend(const CUtensorMap& qmap, const CUtensorMap& kmap, c
   cudaError_t e = cudaFuncSetAttribute(k_ta_attend, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTaAttSmem);
   if (e != cudaSuccess) return e;
   const long long grid = (long long)p.N * p.jblocks;
-  k_ta_attend<<<(unsigned)grid, BT, kTaAttSmem, s>>>(qmap, kmap, vmap, bmap, p);
+  k_ta_attend<<<(unsigned)grid, kAttThreads, kTaAttSmem, s>>>(qmap, kmap, vmap, bmap, p);
   return cudaGetLastError();
 }
 

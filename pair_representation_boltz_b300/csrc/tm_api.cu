@@ -1181,6 +1181,7 @@ tm_status tm_attn_forward(tm_ctx* c, const void* z, const float* mask, int N, tm
 
   TaProjectParams pp{};
   pp.z = reinterpret_cast<const __nv_bfloat16*>(z);
+  pp.mask = mask;
   pp.transpose = tr ? 1 : 0;
   pp.ln = wf;
   pp.w_b = wf + 2 * kC;

@@ -200,6 +200,7 @@ cudaError_t launch_sum_parts_multi(const SumJobs& j, int S, cudaStream_t s);
 // the transposed one (ending node): pair (i, j) then reads z at (j, i) and writes out at (j, i).
 struct TaProjectParams {
   const __nv_bfloat16* z;           // [N][N][128]
+  const float* mask;                // [N] or nullptr: keys j with mask 0 get a bias of -inf
   int transpose;
   const float* ln;                  // gamma, beta (float32, 2 x 128)
   const float* w_b;                 // [4][128] float32
