@@ -370,6 +370,43 @@ def run_ours(args, w):
                            for n, v in bt.items() if v["launches"]}}
         del dout, dz, grads
 
+    # triangle attention (starting and ending node) on the same z
+    attn = None
+    if not args.no_attention and w.dtype == "bf16" and not w.block:
+        amod = tm.TriangleAttention(wl.make_attention_weights())
+        aout = torch.empty_like(z)
+        nodes = ("starting", "ending")
+        for nd in nodes:
+            amod(z, mask, nd, out=aout)
+        barrier()
+        k_a = max(1, min(args.steps, 2))
+        a_l0 = tm.tm_launch_count(amod.ctx)
+        tm.tm_set_timing(amod.ctx, True)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record()
+        for _ in range(k_a):
+            for nd in nodes:
+                amod(z, mask, nd, out=aout)
+        a1.record()
+        barrier()
+        ms_a = a0.elapsed_time(a1) / (k_a * len(nodes))
+        at = tm.tm_get_timing(amod.ctx)
+        tm.tm_set_timing(amod.ctx, False)
+        if tm.tm_sync_status(amod.ctx) != tm.TM_OK:
+            raise RuntimeError("device status after the attention: " + tm.tm_last_error(amod.ctx))
+        # algorithmic FLOPs: the two attention products 4 N^3 H c, and per pair the q, k, v, g, b
+        # projections and the output (2 c_z (4 H c + H) + 2 H c c_z)
+        hc = 128
+        aflops = 4.0 * float(w.N) ** 3 * hc + float(w.N) ** 2 * (2 * 128 * (4 * hc + 4) + 2 * hc * 128)
+        atot = sum(v["ms"] for v in at.values()) or 1.0
+        attn = {"heads": 4, "head_dim": 32, "ms_per_node": ms_a, "tflops": aflops / (ms_a / 1e3) / 1e12,
+                "flops_per_node": aflops, "gpu_launches": tm.tm_launch_count(amod.ctx) - a_l0,
+                "kernels": {n: {"launches": v["launches"], "ms_per_node": v["ms"] / (k_a * len(nodes)),
+                                "share": v["ms"] / atot}
+                            for n, v in at.items() if v["launches"]}}
+        amod.close()
+        del aout
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         dt, tf, desc = oracle_sample(z_np, m_np, W, w, args.cpu_rows, args.cpu_rows, 7)
@@ -386,6 +423,7 @@ def run_ours(args, w):
             "frac_of_bf16_peak": value / world / peaks["bf16_tflops"],
             "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches, "clocks": clk, "backward": bwd,
+            "triangle_attention": attn,
         }
         print(json.dumps(line), flush=True)
     mod.close()
@@ -405,6 +443,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-backward", action="store_true", help="skip the backward-pass measurement")
+    ap.add_argument("--no-attention", action="store_true", help="skip the triangle-attention measurement")
     ap.add_argument("--cpu-rows", type=int, default=48, help="side of the oracle's sampled grid")
     ap.add_argument("--N", type=int, default=0, help="override the workload's token count (profiling runs)")
     args = ap.parse_args()

@@ -9,16 +9,20 @@
 //   out_ij = W_o [o_ij^1 .. o_ij^H]
 // and the ending node is the same on the transposed grid (z_ji in, out_ji written).
 //
-// Two kernels.
+// Three kernels.
 //   k_ta_project: per tile of 128 pairs (512 threads, four per pair), LayerNorm statistics from the
 //     pair's four channel quarters, zh into a 128 x 128 bf16 tile, one MMA each for q, k, v, g
 //     (TMEM columns 0..511), b on the CUDA cores. q, k and g are stored pair-major like z; v is stored
 //     per (row, head, channel) with the key index innermost, so that it is the K-major operand of the
 //     P V product; b per (head, j) with k innermost.
 //   k_ta_attend: per (row i, block of 128 queries j), heads one after another, keys in blocks of 128:
-//     S = Q K^T (tcgen05, TMEM), + bias tile, key mask, online softmax in registers (one thread per
-//     query row), P (bf16) into shared memory, O_blk = P V (tcgen05) added into the row's running
-//     output; the gated o of all heads forms a 128 x 128 tile and one more MMA applies W_o.
+//     S = Q K^T (tcgen05, TMEM; q stored times log2(e)/sqrt(c), the bias times log2(e), so the softmax
+//     runs in base 2), + bias tile (-inf at masked keys), online softmax in registers (two threads per
+//     query row, 64 keys each), P (bf16) into shared memory, O_blk = P V (tcgen05) added into the
+//     row's running output, the gate at the end of each head. Loads and products are pipelined one
+//     block ahead: the next block's K and bias are fetched once this block's S and bias are in
+//     registers, its S is issued together with this block's P V, and its v once P V is done.
+//   k_ta_out: out = W_o o per pair (the ending node writes the transposed pair).
 #include "pair_tile.cuh"
 
 namespace tmk {
@@ -27,6 +31,8 @@ namespace {
 using namespace pt;
 
 constexpr int kHeads = 4, kHd = 32;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kQScale = 1.4426950408889634f * 0.17677669529663687f;   // log2(e) / sqrt(32)
 
 struct alignas(1024) TaProjSmem {
   uint8_t zh[TILE], wq[TILE], wk[TILE], wv[TILE], wg[TILE];
@@ -129,7 +135,7 @@ __global__ void __launch_bounds__(NT, 1) k_ta_project(const TaProjectParams p) {
       // the bias of query i and key j; a masked key j gets -inf, which removes it from every softmax
       const float bsum = ((sm.bpart[0][h][r] + sm.bpart[1][h][r]) + sm.bpart[2][h][r]) + sm.bpart[3][h][r];
       const bool kmasked = p.mask && p.mask[j] == 0.f;
-      p.b[((long long)h * p.N + i) * p.ldb + j] = __float2bfloat16_rn(kmasked ? -INFINITY : bsum);
+      p.b[((long long)h * p.N + i) * p.ldb + j] = __float2bfloat16_rn(kmasked ? -INFINITY : bsum * kLog2e);
     }
     if (!cta_wait(&sm.bar, phase, p.w, &sm.abort_flag, 1)) break;
     phase ^= 1u;
@@ -144,7 +150,11 @@ __global__ void __launch_bounds__(NT, 1) k_ta_project(const TaProjectParams p) {
       if (!valid) continue;
       float o[32];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) o[e] = m == 3 ? sigmoid_mufu(__uint_as_float(rr[e])) : __uint_as_float(rr[e]);
+      for (int e = 0; e < 32; ++e) {
+        const float x = __uint_as_float(rr[e]);
+        // q carries log2(e)/sqrt(c), so that q . k is the logit in the base-2 exponent of the softmax
+        o[e] = m == 3 ? sigmoid_mufu(x) : m == 0 ? x * kQScale : x;
+      }
       if (m == 2) {
         __nv_bfloat16* vp = p.vt + ((long long)i * kC + c0) * p.ldv + j;
 #pragma unroll
@@ -185,7 +195,7 @@ struct alignas(1024) TaAttSmem {
   uint8_t v[2][kVBytes];                        // keys 0..63 and 64..127, rows = channels
   float xmax[2][BT];                            // per key half and query: block maximum
   float xl[2][BT];                              // per key half and query: softmax denominator
-  uint64_t tma_bar, mma_bar;
+  uint64_t kb_bar, v_bar, s_bar, pv_bar;
   uint32_t tmem_slot;
   int abort_flag;
 };
@@ -222,15 +232,49 @@ __global__ void __launch_bounds__(kAttThreads, 2) k_ta_attend(const __grid_const
     }
     return;
   }
+  const int kblocks = (p.N + BT - 1) / BT;
+  const int total = kHeads * kblocks;          // iterations: heads in order, key blocks within a head
+  // loads of iteration t: K and bias (and Q at the start of a head pair) on kb_bar, v on v_bar
+  auto load_kb = [&](int t) {
+    const int h = t / kblocks, kb = t - h * kblocks;
+    const bool with_q = kb == 0 && (h & 1) == 0;
+    mbar_expect_tx(&sm.kb_bar, kKBytes + 2 * kBBytes + (with_q ? kQBytes : 0u));
+    if (with_q) tma_load_3d(sm.q, &qmap, &sm.kb_bar, 64 * (h >> 1), jb * BT, i);
+    tma_load_3d(sm.k, &kmap, &sm.kb_bar, 64 * (h >> 1), kb * BT, i);
+    tma_load_3d(sm.b[0], &bmap, &sm.kb_bar, kb * BT, jb * BT, h);
+    tma_load_3d(sm.b[1], &bmap, &sm.kb_bar, kb * BT + 64, jb * BT, h);
+  };
+  auto load_v = [&](int t) {
+    const int h = t / kblocks, kb = t - h * kblocks;
+    mbar_expect_tx(&sm.v_bar, 2 * kVBytes);
+    tma_load_3d(sm.v[0], &vmap, &sm.v_bar, kb * BT, kHd * h, i);
+    tma_load_3d(sm.v[1], &vmap, &sm.v_bar, kb * BT + 64, kHd * h, i);
+  };
+  constexpr uint32_t ID_S = make_idesc(128, 128, FMT_BF16, false, false);
+  constexpr uint32_t ID_O = make_idesc(128, kHd, FMT_BF16, false, false);
+  auto issue_s = [&](uint32_t tmem, int t) {     // S = Q_h K_h^T (q is stored pre-scaled by log2(e)/sqrt(c))
+    const int hh = (t / kblocks) & 1;
+    const uint32_t q0 = smem_u32(sm.q) + 64 * hh, k0 = smem_u32(sm.k) + 64 * hh;
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks)
+      mma_f16(tmem, make_sdesc_sw128(q0 + 32 * ks, 16, 1024), make_sdesc_sw128(k0 + 32 * ks, 16, 1024), ID_S,
+              ks ? 1u : 0u);
+    mma_commit(&sm.s_bar);
+  };
+
   if (tid == 0) {
-    mbar_init(&sm.tma_bar, 1);
-    mbar_init(&sm.mma_bar, 1);
+    mbar_init(&sm.kb_bar, 1);
+    mbar_init(&sm.v_bar, 1);
+    mbar_init(&sm.s_bar, 1);
+    mbar_init(&sm.pv_bar, 1);
     sm.abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&qmap);
     tma_prefetch_desc(&kmap);
     tma_prefetch_desc(&vmap);
     tma_prefetch_desc(&bmap);
+    load_kb(0);
+    load_v(0);
   }
   if (warp == 0) {
     tmem_alloc(&sm.tmem_slot, 256);
@@ -241,120 +285,117 @@ __global__ void __launch_bounds__(kAttThreads, 2) k_ta_attend(const __grid_const
   tc_fence_after();
   const uint32_t tmem = sm.tmem_slot;
   const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-  constexpr uint32_t ID_S = make_idesc(128, 128, FMT_BF16, false, false);
-  constexpr uint32_t ID_O = make_idesc(128, kHd, FMT_BF16, false, false);
-  const float kscale = 1.4426950408889634f * 0.17677669529663687f;   // log2(e) / sqrt(32)
-  const float klog2e = 1.4426950408889634f;
-  const int kblocks = (p.N + BT - 1) / BT;
-  uint32_t tph = 0, mph = 0;
+  uint32_t kph = 0, vph = 0, sph = 0, pph = 0;   // phases (kb/v: thread 0 only)
   bool ok = true;
+  if (tid == 0) {
+    if (wait_bounded(&sm.kb_bar, kph, p.w, &sm.abort_flag, 1)) {
+      tc_fence_after();
+      issue_s(tmem, 0);
+    }
+    kph ^= 1u;
+  }
 
-  for (int hp = 0; hp < 2 && ok; ++hp) {
-    for (int hh = 0; hh < 2 && ok; ++hh) {
-      const int h = 2 * hp + hh;
-      float m_run = -INFINITY, l_run = 0.f;
-      float acc[16];
+  float m_run = -INFINITY, l_run = 0.f;
+  float acc[16];
+  for (int t = 0; t < total; ++t) {
+    const int h = t / kblocks, kb = t - h * kblocks;
+    if (kb == 0) {
+      m_run = -INFINITY;
+      l_run = 0.f;
 #pragma unroll
       for (int e = 0; e < 16; ++e) acc[e] = 0.f;
-      for (int kb = 0; kb < kblocks; ++kb) {
-        // ---- loads of this key block (and of Q at the start of a head pair)
-        if (tid == 0) {
-          const bool with_q = hh == 0 && kb == 0;
-          mbar_expect_tx(&sm.tma_bar, kKBytes + 2 * kVBytes + 2 * kBBytes + (with_q ? kQBytes : 0u));
-          if (with_q) tma_load_3d(sm.q, &qmap, &sm.tma_bar, 64 * hp, jb * BT, i);
-          tma_load_3d(sm.k, &kmap, &sm.tma_bar, 64 * hp, kb * BT, i);
-          tma_load_3d(sm.v[0], &vmap, &sm.tma_bar, kb * BT, kHd * h, i);
-          tma_load_3d(sm.v[1], &vmap, &sm.tma_bar, kb * BT + 64, kHd * h, i);
-          tma_load_3d(sm.b[0], &bmap, &sm.tma_bar, kb * BT, jb * BT, h);
-          tma_load_3d(sm.b[1], &bmap, &sm.tma_bar, kb * BT + 64, jb * BT, h);
-        }
-        if (!cta_wait(&sm.tma_bar, tph, p.w, &sm.abort_flag, 1)) { ok = false; break; }
-        tph ^= 1u;
-        if (tid == 0) {
-          tc_fence_after();
-          const uint32_t q0 = smem_u32(sm.q) + 64 * hh, k0 = smem_u32(sm.k) + 64 * hh;
-#pragma unroll
-          for (int ks = 0; ks < 2; ++ks)
-            mma_f16(tmem, make_sdesc_sw128(q0 + 32 * ks, 16, 1024), make_sdesc_sw128(k0 + 32 * ks, 16, 1024), ID_S,
-                    ks ? 1u : 0u);
-          mma_commit(&sm.mma_bar);
-        }
-        if (!cta_wait(&sm.mma_bar, mph, p.w, &sm.abort_flag, 2)) { ok = false; break; }
-        mph ^= 1u;
-        tc_fence_after();
+    }
+    if (!cta_wait(&sm.s_bar, sph, p.w, &sm.abort_flag, 2)) { ok = false; break; }
+    sph ^= 1u;
+    tc_fence_after();
 
-        // ---- this thread's 64 logits, log2 domain: S log2(e)/sqrt(c) + b log2(e) (b is -inf at masked
-        // keys); keys past the grid (last block only) -> -inf
-        float sv[64];
-        {
-          uint32_t r0[32], r1[32];
-          tmem_ld32(trow + 64 * kh, r0);
-          tmem_ld32(trow + 64 * kh + 32, r1);
-          tmem_ld_wait();
-          const uint8_t* brow = sm.b[kh];
+    // ---- this thread's 64 logits (log2 domain): S + b, b stored times log2(e) and -inf at masked keys;
+    // keys past the grid (last block only) -> -inf
+    // every thread observes the completion of this block's bias copy before reading it (load t is the
+    // t-th completion of kb_bar; load t + 1 is issued only after all threads are past this point)
+    if (!wait_bounded(&sm.kb_bar, (uint32_t)(t & 1), p.w, &sm.abort_flag, 8)) ok = false;
+    float sv[64];
+    {
+      uint32_t r0[32], r1[32];
+      tmem_ld32(trow + 64 * kh, r0);
+      tmem_ld32(trow + 64 * kh + 32, r1);
+      tmem_ld_wait();
+      const uint8_t* brow = sm.b[kh];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            float bv[8];
-            bf16x8_to_float(*reinterpret_cast<const uint4*>(brow + sw128_offset((uint32_t)row, (uint32_t)u)), bv);
+      for (int u = 0; u < 8; ++u) {
+        float bv[8];
+        bf16x8_to_float(*reinterpret_cast<const uint4*>(brow + sw128_offset((uint32_t)row, (uint32_t)u)), bv);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const uint32_t raw = u < 4 ? r0[8 * u + e] : r1[8 * (u - 4) + e];
-              sv[8 * u + e] = fmaf(__uint_as_float(raw), kscale, bv[e] * klog2e);
-            }
-          }
-        }
-        if (kb == kblocks - 1) {
-          const int kbase = kb * BT + 64 * kh;
-#pragma unroll
-          for (int e = 0; e < 64; ++e)
-            if (kbase + e >= p.N) sv[e] = -INFINITY;
-        }
-        float bmax = sv[0];
-#pragma unroll
-        for (int e = 1; e < 64; ++e) bmax = fmaxf(bmax, sv[e]);
-        sm.xmax[kh][row] = bmax;
-        __syncthreads();
-        const float m_new = fmaxf(m_run, fmaxf(sm.xmax[0][row], sm.xmax[1][row]));
-        const float mref = m_new == -INFINITY ? 0.f : m_new;
-        const float alpha = ex2_approx(m_run - mref);
-        float lsum = 0.f;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          float pv[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            pv[e] = ex2_approx(sv[8 * u + e] - mref);
-            lsum += pv[e];
-          }
-          put8(sm.p, row, 64 * kh + 8 * u, pv);
-        }
-        l_run = l_run * alpha + lsum;
-        m_run = m_new;
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
-          tc_fence_after();
-          const uint32_t p0 = smem_u32(sm.p), v0 = smem_u32(sm.v[0]);
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            mma_f16(tmem + BT, make_sdesc_sw128(p0 + (ks >> 2) * SLAB + (ks & 3) * 32, 16, 1024),
-                    make_sdesc_sw128(v0 + (ks >> 2) * kVBytes + (ks & 3) * 32, 16, 1024), ID_O, ks ? 1u : 0u);
-          mma_commit(&sm.mma_bar);
-        }
-        if (!cta_wait(&sm.mma_bar, mph, p.w, &sm.abort_flag, 3)) { ok = false; break; }
-        mph ^= 1u;
-        tc_fence_after();
-        {
-          uint32_t ro[16];
-          tmem_ld16(trow + BT + 16 * kh, ro);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 16; ++e) acc[e] = fmaf(acc[e], alpha, __uint_as_float(ro[e]));
-        }
+        for (int e = 0; e < 8; ++e) sv[8 * u + e] = __uint_as_float(u < 4 ? r0[8 * u + e] : r1[8 * (u - 4) + e]) + bv[e];
       }
-      if (!ok) break;
-      // ---- the denominator is the sum of both key halves; o = g * acc / l for 16 channels of this head
+    }
+    if (kb == kblocks - 1) {
+      const int kbase = kb * BT + 64 * kh;
+#pragma unroll
+      for (int e = 0; e < 64; ++e)
+        if (kbase + e >= p.N) sv[e] = -INFINITY;
+    }
+    float bmax = sv[0];
+#pragma unroll
+    for (int e = 1; e < 64; ++e) bmax = fmaxf(bmax, sv[e]);
+    sm.xmax[kh][row] = bmax;
+    tc_fence_before();
+    __syncthreads();
+    // S, K and the bias of this block have been read: the next block's K and bias can come in
+    if (tid == 0 && t + 1 < total) load_kb(t + 1);
+    const float m_new = fmaxf(m_run, fmaxf(sm.xmax[0][row], sm.xmax[1][row]));
+    const float mref = m_new == -INFINITY ? 0.f : m_new;
+    const float alpha = ex2_approx(m_run - mref);
+    float lsum = 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      float pv[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        pv[e] = ex2_approx(sv[8 * u + e] - mref);
+        lsum += pv[e];
+      }
+      put8(sm.p, row, 64 * kh + 8 * u, pv);
+    }
+    l_run = l_run * alpha + lsum;
+    m_run = m_new;
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      // P V of this block, then S of the next one (different TMEM columns, different operands)
+      if (wait_bounded(&sm.v_bar, vph, p.w, &sm.abort_flag, 3)) {
+        const uint32_t p0 = smem_u32(sm.p), v0 = smem_u32(sm.v[0]);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          mma_f16(tmem + BT, make_sdesc_sw128(p0 + (ks >> 2) * SLAB + (ks & 3) * 32, 16, 1024),
+                  make_sdesc_sw128(v0 + (ks >> 2) * kVBytes + (ks & 3) * 32, 16, 1024), ID_O, ks ? 1u : 0u);
+        mma_commit(&sm.pv_bar);
+      }
+      vph ^= 1u;
+      if (t + 1 < total) {
+        if (wait_bounded(&sm.kb_bar, kph, p.w, &sm.abort_flag, 4)) {
+          tc_fence_after();
+          issue_s(tmem, t + 1);
+        }
+        kph ^= 1u;
+      }
+    }
+    if (!cta_wait(&sm.pv_bar, pph, p.w, &sm.abort_flag, 5)) { ok = false; break; }
+    pph ^= 1u;
+    tc_fence_after();
+    // P V has read v: the next block's v can come in
+    if (tid == 0 && t + 1 < total) load_v(t + 1);
+    {
+      uint32_t ro[16];
+      tmem_ld16(trow + BT + 16 * kh, ro);
+      tmem_ld_wait();
+#pragma unroll
+      for (int e = 0; e < 16; ++e) acc[e] = fmaf(acc[e], alpha, __uint_as_float(ro[e]));
+    }
+    if (kb == kblocks - 1) {
+      // ---- the denominator is the sum of both key halves; o = g * acc / l for 16 channels of head h
       sm.xl[kh][row] = l_run;
       __syncthreads();
       const float l_tot = sm.xl[0][row] + sm.xl[1][row];
@@ -378,6 +419,11 @@ __global__ void __launch_bounds__(kAttThreads, 2) k_ta_attend(const __grid_const
                              pack_bf16x2(o[8 * u + 4], o[8 * u + 5]), pack_bf16x2(o[8 * u + 6], o[8 * u + 7]));
       }
     }
+  }
+  if (!ok && tid == 0) {
+    // a wait ran out: let copies still in flight land before the shared memory is released
+    wait_bounded(&sm.kb_bar, kph, p.w, &sm.abort_flag, 6);
+    wait_bounded(&sm.v_bar, vph, p.w, &sm.abort_flag, 7);
   }
   tc_fence_before();
   __syncthreads();

@@ -2,7 +2,8 @@
 values the bf16 path stores in bf16, against the exact float64 result.
 
 A model of the path's storage, not of its code: zh (the operand of the projections), the weights
-W_q, W_k, W_v, W_g, W_o, the stored q, k, v, g and pair bias b, the softmax numerator's weights P
+W_q, W_k, W_v, W_g, W_o, the stored q (times log2(e)/sqrt(c)), k, v, g and pair bias b (times
+log2(e): the path's softmax runs in base 2), the softmax numerator's weights P
 (a bf16 operand of the P V product; the denominator sums them unrounded), the gated output o and
 the result are each rounded once to bf16; everything else is exact.
 
@@ -29,17 +30,18 @@ def emulated(z, mask, W, node, heads=4, c=32):
     m = np.asarray(mask, np.float64)
     zh = oracle.layer_norm(z, W["ln_gamma"], W["ln_beta"])
     zb = r16(zh)
-    q = r16(zb @ r16(W["w_q"]).T).reshape(N, N, heads, c)
+    log2e = 1.0 / math.log(2.0)
+    q = r16((zb @ r16(W["w_q"]).T) * (log2e / math.sqrt(c))).reshape(N, N, heads, c)
     k = r16(zb @ r16(W["w_k"]).T).reshape(N, N, heads, c)
     v = r16(zb @ r16(W["w_v"]).T).reshape(N, N, heads, c)
     g = r16(oracle.sigmoid(zb @ r16(W["w_g"]).T)).reshape(N, N, heads, c)
-    b = r16(np.moveaxis(zh @ W["w_b"].T, -1, 0))
-    s = np.einsum("ijhc,ikhc->ihjk", q, k) / math.sqrt(c) + b[None]
+    b = r16(np.moveaxis(zh @ W["w_b"].T, -1, 0) * log2e)
+    s = np.einsum("ijhc,ikhc->ihjk", q, k) + b[None]            # logits in base 2
     valid = (np.outer(m, m) != 0)[:, None, None, :]
     s = np.where(valid, s, -np.inf)
     smax = np.max(s, axis=-1, keepdims=True)
     smax = np.where(np.isfinite(smax), smax, 0.0)
-    e = np.where(valid, np.exp(s - smax), 0.0)
+    e = np.where(valid, np.exp2(s - smax), 0.0)
     den = e.sum(axis=-1, keepdims=True)
     num = np.einsum("ihjk,ikhc->ijhc", r16(e), v)
     den = np.moveaxis(den, 1, 2)                               # [i][j][h][1]

@@ -101,6 +101,25 @@ def make_weights(c_z: int, c_h: int, seed: int = 1, ln_random: bool = False) -> 
     return out
 
 
+def attention_weight_shapes(c_z: int = 128, heads: int = 4, c: int = 32) -> dict:
+    """Shapes of a triangle attention layer's parameters, Linear layout [out][in]."""
+    hc = heads * c
+    return {"ln_gamma": (c_z,), "ln_beta": (c_z,), "w_q": (hc, c_z), "w_k": (hc, c_z), "w_v": (hc, c_z),
+            "w_b": (heads, c_z), "w_g": (hc, c_z), "w_o": (c_z, hc)}
+
+
+def make_attention_weights(c_z: int = 128, heads: int = 4, c: int = 32, seed: int = 1) -> dict:
+    """float32 parameters of a triangle attention layer: W ~ N(0, 1/fan_in); LayerNorm gamma=1, beta=0."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 104729]))
+    out = {}
+    for name, shp in attention_weight_shapes(c_z, heads, c).items():
+        if name.startswith("w_"):
+            out[name] = (rng.standard_normal(shp) / np.sqrt(shp[1])).astype(np.float32)
+        else:
+            out[name] = (np.ones(shp) if name.endswith("gamma") else np.zeros(shp)).astype(np.float32)
+    return out
+
+
 # --------------------------------------------------------------------------- masks
 
 def make_mask(N: int, kind: str, seed: int = 3) -> np.ndarray:
