@@ -153,6 +153,40 @@ def oracle_sample(z, m, W, w, n_rows, n_cols, seed):
 
 # --------------------------------------------------------------------------- reference arm (CPU oracle)
 
+def oracle_backward_sample(n):
+    """The float64 backward oracle on the whole grid at N = n (bf16 z, c = 128): its gradient work
+    (4 n^3 c + 12 per-pair 128 x 128 products) per second. Every dz entry depends on the whole grid, so the
+    oracle has no sampled form of the backward; a small full case stands in."""
+    import numpy as np
+    import oracle
+    import workloads as wl
+    z = wl.make_z(n, 128, 3, "bf16")
+    W = wl.make_weights(128, 128, 1)
+    dout = wl.make_z(n, 128, 4, "bf16")
+    t0 = time.perf_counter()
+    oracle.full_backward(z, np.ones(n), W, "outgoing", dout, storage="bf16")
+    dt = time.perf_counter() - t0
+    f = 4.0 * n ** 3 * 128 + 12 * 2 * 128 * 128 * float(n) ** 2
+    return {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
+            "sample": f"full float64 backward at N={n}, outgoing", "seconds": dt}
+
+
+def oracle_attention_sample(n):
+    """The float64 triangle-attention oracle on the whole grid at N = n (starting node): algorithmic
+    work per second."""
+    import oracle.triangle_attention as TA
+    import workloads as wl
+    z = wl.make_z(n, 128, 3, "bf16")
+    W = wl.make_attention_weights()
+    m = wl.make_mask(n, "full")
+    t0 = time.perf_counter()
+    TA.full(z, m, W, "starting")
+    dt = time.perf_counter() - t0
+    f = 4.0 * n ** 3 * 128 + float(n) ** 2 * (2 * 128 * (4 * 128 + 4) + 2 * 128 * 128)
+    return {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
+            "sample": f"full float64 triangle attention at N={n}, starting node", "seconds": dt}
+
+
 def run_reference(args, w):
     world, rank, _ = dist_setup()
     if rank != 0:
@@ -368,6 +402,20 @@ def run_ours(args, w):
                "kernels": {n: {"launches": v["launches"], "ms_per_update": v["ms"] / (k_b * len(w.directions)),
                                "share": v["ms"] / btot}
                            for n, v in bt.items() if v["launches"]}}
+        # roofline of the dominant kernel (the contractions: recomputed x, dA, dB; 2 N FLOP per channel
+        # and output pair), and the per-pair backward kernels' algorithmic bandwidth (1800 B per pair each)
+        bc = bt["contract"]
+        if bc["ms"] > 0:
+            c_tf = 2.0 * w.N * bc["units"] / (bc["ms"] / 1e3) / 1e12
+            bwd["roofline"] = {"bound": "tensor", "kernel": "k2_contract (x, dA, dB)", "achieved": c_tf,
+                               "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": c_tf / peaks["bf16_tflops"],
+                               "traffic": None, "peak_source": f"bf16 burst, {peak_src}"}
+        for n in ("out_backward", "proj_backward"):
+            v = bt[n]
+            if v["ms"] > 0:
+                bwd["kernels"][n]["gbs"] = v["units"] * 1800 / (v["ms"] / 1e3) / 1e9
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            bwd["cpu_baseline"] = oracle_backward_sample(192)
         del dout, dz, grads
 
     # triangle attention (starting and ending node) on the same z
@@ -404,6 +452,18 @@ def run_ours(args, w):
                 "kernels": {n: {"launches": v["launches"], "ms_per_node": v["ms"] / (k_a * len(nodes)),
                                 "share": v["ms"] / atot}
                             for n, v in at.items() if v["launches"]}}
+        # the attention kernel is bound by its exponentials: one ex2 per logit (N^3 H per node) on the
+        # special-function pipe, 16 per clock per SM, at the maximum SM clock
+        ta = at["attn_attend"]
+        if ta["ms"] > 0:
+            logits = float(w.N) ** 3 * 4 * ta["launches"]
+            ach = logits / (ta["ms"] / 1e3) / 1e12
+            pk = 16 * 148 * 2032e6 / 1e12
+            attn["roofline"] = {"bound": "alu", "kernel": "k_ta_attend", "achieved": ach, "peak": pk,
+                                "unit": "Tera-ex2/s", "frac": ach / pk, "traffic": None,
+                                "peak_source": "16 ex2 per clock per SM x 148 SMs x 2032 MHz (nominal)"}
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            attn["cpu_baseline"] = oracle_attention_sample(256)
         amod.close()
         del aout
 

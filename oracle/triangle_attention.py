@@ -56,7 +56,7 @@ def attention_rows(q, k, v, bias, key_valid):
     booleans. A row without any valid key gives 0. Returns o [N][N][H][c] before the gate.
     """
     c = q.shape[-1]
-    s = np.einsum("ijhc,ikhc->ihjk", q, k) / np.sqrt(c) + bias[None, :, :, :]
+    s = np.einsum("ijhc,ikhc->ihjk", q, k, optimize=True) / np.sqrt(c) + bias[None, :, :, :]
     valid = key_valid[:, None, None, :]                       # [i][1][1][k]
     s = np.where(valid, s, -np.inf)
     smax = np.max(s, axis=-1, keepdims=True)
@@ -64,7 +64,7 @@ def attention_rows(q, k, v, bias, key_valid):
     e = np.where(valid, np.exp(s - smax), 0.0)
     den = e.sum(axis=-1, keepdims=True)
     a = np.where(den > 0, e / np.where(den > 0, den, 1.0), 0.0)
-    return np.einsum("ihjk,ikhc->ijhc", a, v)
+    return np.einsum("ihjk,ikhc->ijhc", a, v, optimize=True)
 
 
 def starting_node(z, mask, W, heads=4, c=32):
@@ -98,3 +98,44 @@ def flops(N: int, c_z: int = 128, heads: int = 4, c: int = 32) -> float:
     the per-pair projections q, k, v, g, b and the output (2 c_z (4 H c + H) + 2 H c c_z per pair)."""
     hc = heads * c
     return 4.0 * N ** 3 * hc + float(N) ** 2 * (2 * c_z * (4 * hc + heads) + 2 * hc * c_z)
+
+
+def pair_bias(z, W, heads=4, chunk=32):
+    """b[h][j][k] = (W_b LayerNorm(z_jk))^h for every pair, computed in row chunks (float64)."""
+    W = T._w64(W)
+    N = z.shape[0]
+    b = np.empty((heads, N, N))
+    for j0 in range(0, N, chunk):
+        zh = T.layer_norm(T._to_f64(z[j0:j0 + chunk]), W["ln_gamma"], W["ln_beta"])
+        b[:, j0:j0 + chunk, :] = np.moveaxis(zh @ W["w_b"].T, -1, 0)
+    return b
+
+
+def sampled(z, mask, W, node, lines, heads=4, c=32, bias=None):
+    """Whole lines of the output, exactly: out[i, :, :] for i in ``lines`` (starting node) or
+    out[:, j, :] for j in ``lines`` (ending node), returned as [len(lines)][N][c_z].
+
+    A starting-node row i needs z[i, :] (its q, k, v, g) and the pair bias of every pair (j, k); the
+    ending node is the starting node of the transposed grid. ``bias`` may pass in pair_bias of the
+    (transposed, for the ending node) grid to share it between calls. ``z`` may be float32 or uint16
+    bf16 bits, indexable like [N][N][c_z].
+    """
+    _check_node(node)
+    W = T._w64(W)
+    m = np.asarray(mask, np.float64)
+    N = z.shape[0]
+    lines = np.asarray(lines, np.int64)
+    if bias is None:
+        bias = pair_bias(z if node == "starting" else np.swapaxes(z, 0, 1), W, heads)
+    out = np.empty((len(lines), N, W["w_o"].shape[0]))
+    for n, i in enumerate(lines):
+        zi = T._to_f64(z[i, :, :] if node == "starting" else z[:, i, :])      # [N][c_z]: pairs (i, .)
+        zh = T.layer_norm(zi, W["ln_gamma"], W["ln_beta"])
+        q = (zh @ W["w_q"].T).reshape(1, N, heads, c)
+        k = (zh @ W["w_k"].T).reshape(1, N, heads, c)
+        v = (zh @ W["w_v"].T).reshape(1, N, heads, c)
+        g = T.sigmoid(zh @ W["w_g"].T).reshape(1, N, heads, c)
+        key_valid = (m[i] * m != 0)[None, :]
+        o = g * attention_rows(q, k, v, bias, key_valid)
+        out[n] = o.reshape(N, heads * c) @ W["w_o"].T
+    return out

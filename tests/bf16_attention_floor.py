@@ -76,3 +76,36 @@ if __name__ == "__main__":
     for N, mask in ((64, "scatter"), (129, "last10pct"), (200, "scatter")):
         for node in TA.NODES:
             print(N, mask, node, f"{floor(N, mask, node, 31 + N):.4f}")
+
+
+def emulated_lines(z, mask, W, node, lines, bias, heads=4, c=32):
+    """``emulated`` restricted to whole output lines (rows i of the starting node, columns j of the
+    ending node), for grids too large to model whole; ``bias`` is the exact pair bias of the
+    (transposed, for the ending node) grid, as oracle.triangle_attention.pair_bias gives it. Returns
+    [len(lines)][N][c_z]."""
+    if node == "ending":
+        return emulated_lines(np.swapaxes(z, 0, 1), mask, W, "starting", lines, bias, heads, c)
+    W = {k: np.asarray(v, np.float64) for k, v in W.items()}
+    N = z.shape[0]
+    m = np.asarray(mask, np.float64)
+    log2e = 1.0 / math.log(2.0)
+    b = r16(bias * log2e)
+    out = np.empty((len(lines), N, W["w_o"].shape[0]))
+    for n, i in enumerate(lines):
+        zh = oracle.layer_norm(wl.as_f64(np.ascontiguousarray(z[i])), W["ln_gamma"], W["ln_beta"])
+        zb = r16(zh)
+        q = r16((zb @ r16(W["w_q"]).T) * (log2e / math.sqrt(c))).reshape(N, heads, c)
+        k = r16(zb @ r16(W["w_k"]).T).reshape(N, heads, c)
+        v = r16(zb @ r16(W["w_v"]).T).reshape(N, heads, c)
+        g = r16(oracle.sigmoid(zb @ r16(W["w_g"]).T)).reshape(N, heads, c)
+        s = np.einsum("jhc,khc->hjk", q, k, optimize=True) + b
+        valid = (m[i] * m != 0)[None, None, :]
+        s = np.where(valid, s, -np.inf)
+        smax = np.max(s, axis=-1, keepdims=True)
+        smax = np.where(np.isfinite(smax), smax, 0.0)
+        e = np.where(valid, np.exp2(s - smax), 0.0)
+        den = np.moveaxis(e.sum(axis=-1, keepdims=True), 0, 1)          # [j][h][1]
+        num = np.einsum("hjk,khc->jhc", r16(e), v, optimize=True)
+        o = r16(g * np.where(den > 0, num / np.where(den > 0, den, 1.0), 0.0))
+        out[n] = r16(o.reshape(N, heads * c) @ r16(W["w_o"]).T)
+    return out

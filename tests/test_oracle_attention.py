@@ -170,6 +170,18 @@ def test_masked_tokens(node):
         assert np.all(out[:, dead, :] == 0.0)
 
 
+@pytest.mark.parametrize("node", NODES)
+def test_sampled_lines_equal_full(node):
+    N, c_z, H, c = 11, 6, 2, 3
+    z, m, W = _inputs(N, c_z, H, c, seed=13)
+    m[4] = 0.0
+    full = TA.full(z, m, W, node, H, c)
+    lines = [0, 4, 10]
+    got = TA.sampled(z, m, W, node, lines, H, c)
+    ref = full[lines] if node == "starting" else np.swapaxes(full[:, lines], 0, 1)
+    assert np.max(np.abs(got - ref)) < 1e-12
+
+
 # --------------------------------------------------------------------------- planted mistakes
 
 def _rows_no_scale(q, k, v, bias, key_valid):
