@@ -18,8 +18,9 @@
 //   k_ta_attend: per (row i, block of 128 queries j), heads one after another, keys in blocks of 128:
 //     S = Q K^T (tcgen05, TMEM; q stored times log2(e)/sqrt(c), the bias times log2(e), so the softmax
 //     runs in base 2), + bias tile (-inf at masked keys), online softmax in registers (two threads per
-//     query row, 64 keys each), P (bf16) into shared memory, O_blk = P V (tcgen05) added into the
-//     row's running output, the gate at the end of each head. Loads and products are pipelined one
+//     query row, 64 keys each), P (bf16) into shared memory, O_blk = P V (tcgen05, with a row of ones
+//     appended to v so that the product also gives the row sum of P, the softmax denominator) added
+//     into the row's running output, the gate at the end of each head. Loads and products are pipelined one
 //     block ahead: the next block's K and bias are fetched once this block's S and bias are in
 //     registers, its S is issued together with this block's P V, and its v once P V is done.
 //   k_ta_out: out = W_o o per pair (the ending node writes the transposed pair).
@@ -181,6 +182,8 @@ namespace {
 constexpr uint32_t kQBytes = 64 * 128 * 2;      // Q box: 64 channels (a head pair) x 128 queries
 constexpr uint32_t kKBytes = 64 * 128 * 2;      // K box: 64 channels x 128 keys
 constexpr uint32_t kVBytes = 64 * 32 * 2;       // one v box: 64 keys x 32 channels of one head
+constexpr uint32_t kVSlot = 64 * 48 * 2;        // its slot: 32 rows of v, a row of ones, 15 rows of zeros
+constexpr int kPvN = 48;                        // N of the P V product: 32 channels, the row sum, padding
 constexpr uint32_t kBBytes = 64 * 128 * 2;      // one bias box: 64 keys x 128 queries
 
 static_assert(kBoxTaQK.bytes() == kQBytes && kBoxTaQK.bytes() == kKBytes, "Q/K box fills its slot");
@@ -192,9 +195,8 @@ struct alignas(1024) TaAttSmem {
   uint8_t k[kKBytes];
   uint8_t b[2][kBBytes];                        // keys 0..63 and 64..127 of the block
   uint8_t p[TILE];                              // P: 128 queries x 128 keys, bf16, K-major
-  uint8_t v[2][kVBytes];                        // keys 0..63 and 64..127, rows = channels
+  uint8_t v[2][kVSlot];                         // keys 0..63 and 64..127, rows = channels (+ ones row)
   float xmax[2][BT];                            // per key half and query: block maximum
-  float xl[2][BT];                              // per key half and query: softmax denominator
   uint64_t kb_bar, v_bar, s_bar, pv_bar;
   uint32_t tmem_slot;
   int abort_flag;
@@ -251,7 +253,7 @@ __global__ void __launch_bounds__(kAttThreads, 2) k_ta_attend(const __grid_const
     tma_load_3d(sm.v[1], &vmap, &sm.v_bar, kb * BT + 64, kHd * h, i);
   };
   constexpr uint32_t ID_S = make_idesc(128, 128, FMT_BF16, false, false);
-  constexpr uint32_t ID_O = make_idesc(128, kHd, FMT_BF16, false, false);
+  constexpr uint32_t ID_O = make_idesc(128, kPvN, FMT_BF16, false, false);
   auto issue_s = [&](uint32_t tmem, int t) {     // S = Q_h K_h^T (q is stored pre-scaled by log2(e)/sqrt(c))
     const int hh = (t / kblocks) & 1;
     const uint32_t q0 = smem_u32(sm.q) + 64 * hh, k0 = smem_u32(sm.k) + 64 * hh;
@@ -280,6 +282,13 @@ __global__ void __launch_bounds__(kAttThreads, 2) k_ta_attend(const __grid_const
     tmem_alloc(&sm.tmem_slot, 256);
     tmem_relinquish();
   }
+  // rows 32..47 of both v slots, which no copy overwrites: a row of ones (the P V product's column 32
+  // is then the row sum of the bf16 P, the softmax denominator) and zeros
+  for (int x = tid; x < 2 * (kVSlot - kVBytes) / 4; x += kAttThreads) {
+    const int half = x / ((kVSlot - kVBytes) / 4), w4 = x % ((kVSlot - kVBytes) / 4);
+    reinterpret_cast<uint32_t*>(sm.v[half] + kVBytes)[w4] = w4 < 32 ? 0x3F803F80u : 0u;
+  }
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -346,18 +355,13 @@ __global__ void __launch_bounds__(kAttThreads, 2) k_ta_attend(const __grid_const
     const float m_new = fmaxf(m_run, fmaxf(sm.xmax[0][row], sm.xmax[1][row]));
     const float mref = m_new == -INFINITY ? 0.f : m_new;
     const float alpha = ex2_approx(m_run - mref);
-    float lsum = 0.f;
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       float pv[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        pv[e] = ex2_approx(sv[8 * u + e] - mref);
-        lsum += pv[e];
-      }
+      for (int e = 0; e < 8; ++e) pv[e] = ex2_approx(sv[8 * u + e] - mref);
       put8(sm.p, row, 64 * kh + 8 * u, pv);
     }
-    l_run = l_run * alpha + lsum;
     m_run = m_new;
     fence_proxy_async_smem();
     tc_fence_before();
@@ -370,7 +374,7 @@ __global__ void __launch_bounds__(kAttThreads, 2) k_ta_attend(const __grid_const
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
           mma_f16(tmem + BT, make_sdesc_sw128(p0 + (ks >> 2) * SLAB + (ks & 3) * 32, 16, 1024),
-                  make_sdesc_sw128(v0 + (ks >> 2) * kVBytes + (ks & 3) * 32, 16, 1024), ID_O, ks ? 1u : 0u);
+                  make_sdesc_sw128(v0 + (ks >> 2) * kVSlot + (ks & 3) * 32, 16, 1024), ID_O, ks ? 1u : 0u);
         mma_commit(&sm.pv_bar);
       }
       vph ^= 1u;
@@ -390,15 +394,15 @@ __global__ void __launch_bounds__(kAttThreads, 2) k_ta_attend(const __grid_const
     {
       uint32_t ro[16];
       tmem_ld16(trow + BT + 16 * kh, ro);
+      const uint32_t rl = tmem_ld1(trow + BT + kHd);     // the row sum of this block's P
       tmem_ld_wait();
 #pragma unroll
       for (int e = 0; e < 16; ++e) acc[e] = fmaf(acc[e], alpha, __uint_as_float(ro[e]));
+      l_run = fmaf(l_run, alpha, __uint_as_float(rl));
     }
     if (kb == kblocks - 1) {
-      // ---- the denominator is the sum of both key halves; o = g * acc / l for 16 channels of head h
-      sm.xl[kh][row] = l_run;
-      __syncthreads();
-      const float l_tot = sm.xl[0][row] + sm.xl[1][row];
+      // ---- o = g * acc / l for 16 channels of head h (l: the running sum of the bf16 P over all keys)
+      const float l_tot = l_run;
       if (jvalid) {
         const int cb = kHd * h + 16 * kh;
         float gv[16];

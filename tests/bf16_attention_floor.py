@@ -4,7 +4,8 @@ values the bf16 path stores in bf16, against the exact float64 result.
 A model of the path's storage, not of its code: zh (the operand of the projections), the weights
 W_q, W_k, W_v, W_g, W_o, the stored q (times log2(e)/sqrt(c)), k, v, g and pair bias b (times
 log2(e): the path's softmax runs in base 2), the softmax numerator's weights P
-(a bf16 operand of the P V product; the denominator sums them unrounded), the gated output o and
+(a bf16 operand of the P V product, whose extra column of ones also gives the denominator, so both sum
+the rounded weights), the gated output o and
 the result are each rounded once to bf16; everything else is exact.
 
 Run as a script to print the floor of the test cases: python -m tests.bf16_attention_floor
@@ -41,9 +42,9 @@ def emulated(z, mask, W, node, heads=4, c=32):
     s = np.where(valid, s, -np.inf)
     smax = np.max(s, axis=-1, keepdims=True)
     smax = np.where(np.isfinite(smax), smax, 0.0)
-    e = np.where(valid, np.exp2(s - smax), 0.0)
+    e = r16(np.where(valid, np.exp2(s - smax), 0.0))
     den = e.sum(axis=-1, keepdims=True)
-    num = np.einsum("ihjk,ikhc->ijhc", r16(e), v)
+    num = np.einsum("ihjk,ikhc->ijhc", e, v)
     den = np.moveaxis(den, 1, 2)                               # [i][j][h][1]
     o = r16(g * np.where(den > 0, num / np.where(den > 0, den, 1.0), 0.0))
     return r16(o.reshape(N, N, heads * c) @ r16(W["w_o"]).T)
@@ -103,9 +104,9 @@ def emulated_lines(z, mask, W, node, lines, bias, heads=4, c=32):
         s = np.where(valid, s, -np.inf)
         smax = np.max(s, axis=-1, keepdims=True)
         smax = np.where(np.isfinite(smax), smax, 0.0)
-        e = np.where(valid, np.exp2(s - smax), 0.0)
+        e = r16(np.where(valid, np.exp2(s - smax), 0.0))
         den = np.moveaxis(e.sum(axis=-1, keepdims=True), 0, 1)          # [j][h][1]
-        num = np.einsum("hjk,khc->jhc", r16(e), v, optimize=True)
+        num = np.einsum("hjk,khc->jhc", e, v, optimize=True)
         o = r16(g * np.where(den > 0, num / np.where(den > 0, den, 1.0), 0.0))
         out[n] = r16(o.reshape(N, heads * c) @ r16(W["w_o"]).T)
     return out
