@@ -4,7 +4,9 @@ A tiled TMA copy must start at an inner-axis coordinate whose byte offset is a
 multiple of 16 (8 elements for bf16/fp16, 4 for fp32). This test replays the
 coordinate arithmetic of the projection, contraction and finish kernels for
 every workload and block schedule the tests and the benchmark use, including
-unaligned block origins, and asserts that rule for each box.
+unaligned block origins, and asserts that rule for each box; the same for the
+triangle-attention kernel's copies (with the bytes each barrier expects), and
+the alignment and bounds of the backward kernels' L2 prefetch ranges.
 """
 import itertools
 
@@ -126,3 +128,93 @@ def test_unaligned_block_origins_are_covered():
         tiles_j = (j0 + bj - j_base + BN - 1) // BN
         assert i_base + tiles_i * BM >= i0 + bi and j_base + tiles_j * BN >= j0 + bj
         assert 0 <= i0 - i_base < 8 and 0 <= j0 - j_base < 8
+
+
+# --------------------------------------------------------------------------- triangle attention
+
+def _box(name):
+    """A Box constant {d0, d1, d2, esz} from the kernels' header, so the replay uses the real shapes."""
+    import os
+    import re
+    hdr = open(os.path.join(os.path.dirname(__file__), "..", "pair_representation_boltz_b300", "csrc",
+                            "tm_kernels.h")).read()
+    m = re.search(r"constexpr Box " + name + r"\{(\d+), (\d+), (\d+), (\d+)\}", hdr)
+    assert m, name
+    return tuple(int(g) for g in m.groups())
+
+
+def attention_boxes(N, i, jb):
+    """Yield (tensor, barrier, (x, y, z) start, box) for every copy of one attention CTA (row i, query
+    block jb), in the order the kernel issues them: per iteration t (head t // kblocks, key block
+    t % kblocks) K and bias (and Q at the first block of a head pair) on kb_bar, v on v_bar."""
+    qk, vb, bb = _box("kBoxTaQK"), _box("kBoxTaV"), _box("kBoxTaBias")
+    kblocks = (N + 127) // 128
+    for t in range(4 * kblocks):
+        h, kb = divmod(t, kblocks)
+        if kb == 0 and h % 2 == 0:
+            yield ("q", "kb", t, (64 * (h // 2), jb * 128, i), qk)
+        yield ("k", "kb", t, (64 * (h // 2), kb * 128, i), qk)
+        yield ("bias", "kb", t, (kb * 128, jb * 128, h), bb)
+        yield ("bias", "kb", t, (kb * 128 + 64, jb * 128, h), bb)
+        yield ("v", "v", t, (kb * 128, 32 * h, i), vb)
+        yield ("v", "v", t, (kb * 128 + 64, 32 * h, i), vb)
+
+
+@pytest.mark.parametrize("N", [1, 7, 64, 127, 128, 129, 200, 300, 768, 1025, 3605])
+def test_attention_boxes(N):
+    """Every attention copy starts at a non-negative, 16-byte-aligned inner coordinate, and the bytes each
+    barrier expects per iteration equal the boxes it receives (a load past the grid still moves a whole,
+    zero-filled box)."""
+    expect_kb = {"k": 64 * 128 * 2, "q": 64 * 128 * 2, "bias": 2 * 64 * 128 * 2}   # kKBytes, kQBytes, 2 kBBytes
+    expect_v = 2 * 64 * 32 * 2                                                     # 2 kVBytes
+    jblocks = (N + 127) // 128
+    rows = sorted({0, N // 2, N - 1})
+    for i in rows:
+        for jb in sorted({0, jblocks - 1}):
+            got_kb, got_v = {}, {}
+            for name, bar, t, (x, y, z), (d0, d1, d2, esz) in attention_boxes(N, i, jb):
+                assert x >= 0 and y >= 0 and z >= 0 and (x * esz) % 16 == 0, (N, name, x)
+                nbytes = d0 * d1 * d2 * esz
+                (got_kb if bar == "kb" else got_v)[t] = (got_kb if bar == "kb" else got_v).get(t, 0) + nbytes
+            kblocks = (N + 127) // 128
+            for t in range(4 * kblocks):
+                h, kb = divmod(t, kblocks)
+                want = expect_kb["k"] + expect_kb["bias"] + (expect_kb["q"] if kb == 0 and h % 2 == 0 else 0)
+                assert got_kb[t] == want and got_v[t] == expect_v, (N, t)
+
+
+# --------------------------------------------------------------------------- backward L2 prefetch ranges
+
+def _up(v, a):
+    return (v + a - 1) // a * a
+
+
+def _prefetch(base, b0, b1, alloc):
+    a0, a1 = b0 & ~15, (b1 + 15) & ~15
+    if a1 > a0:
+        assert (base + a0) % 16 == 0 and base + a0 >= 0 and base + a1 <= alloc, (base, a0, a1, alloc)
+
+
+@pytest.mark.parametrize("N", [128, 129, 200, 255, 256, 257, 511, 768, 1023, 1025, 3605])
+def test_backward_prefetch_ranges_stay_aligned_and_inside(N):
+    """The per-pair backward kernels prefetch, for the next tile of 128 flattened pairs, row segments of the
+    float32 planes x / dA / dB ([128][N][ldx], ldx a multiple of 32), the matching span of each channel of
+    dzh ([128][N*N]), and the tile's span of z and of the LayerNorm statistics. Every widened range must
+    start on 16 bytes and end inside its allocation."""
+    P, ldx = N * N, _up(N, 32)
+    xplane, xalloc = N * ldx, _up(128 * N * ldx * 4, 256)
+    hb, zst, zb = _up(128 * P * 4, 256), _up(P * 8, 256), P * 256
+    tiles = (P + 127) // 128
+    for tn in sorted(set(range(0, tiles, max(1, tiles // 97))) | {tiles - 1}):
+        q0, q1 = tn * 128, min(tn * 128 + 128, P)
+        i, j0 = divmod(q0, N)
+        n1 = min(q1 - q0, N - j0)
+        for c in (0, 1, 63, 127):
+            base = c * xplane * 4
+            _prefetch(base + i * ldx * 4, 4 * j0, 4 * (j0 + n1), xalloc)
+            if q0 + n1 < q1:
+                assert i + 1 < N
+                _prefetch(base + (i + 1) * ldx * 4, 0, 4 * (q1 - q0 - n1), xalloc)
+            _prefetch(0, (c * P + q0) * 4, (c * P + q1) * 4, hb)
+        _prefetch(0, q0 * 256, q1 * 256, zb)
+        _prefetch(0, q0 * 8, q1 * 8, zst)
