@@ -506,7 +506,9 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_project(const BwdProjParams p) {
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-// out[c][j][i] = in[c][i][j] for i, j < N (bf16 planes [128][N][ld]); 64 x 64 tiles, 2 elements per thread
+// out[c][j][i] = in[c][i][j] for i, j < N (bf16 planes [128][N][ld], ld a multiple of 64); 64 x 64 tiles,
+// two elements per thread: rows start 128-byte aligned and every thread takes an even column pair, so a
+// pair inside the grid moves as one 4-byte load and one 4-byte store (scalar at the grid's ragged edge)
 __global__ void __launch_bounds__(256) k_transpose_planes(const __nv_bfloat16* __restrict__ in,
                                                           __nv_bfloat16* __restrict__ out, int N, long long ld,
                                                           long long plane) {
@@ -516,19 +518,32 @@ __global__ void __launch_bounds__(256) k_transpose_planes(const __nv_bfloat16* _
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8
   const __nv_bfloat16* src = in + c * plane;
   __nv_bfloat16* dst = out + c * plane;
+  const __nv_bfloat16 zero = __float2bfloat16_rn(0.f);
   for (int r = ty; r < 64; r += 8) {
     const int i = i0 + r, j = j0 + 2 * tx;
-    __nv_bfloat16 v0 = __float2bfloat16_rn(0.f), v1 = v0;
-    if (i < N && j < N) v0 = src[(long long)i * ld + j];
-    if (i < N && j + 1 < N) v1 = src[(long long)i * ld + j + 1];
-    t[r][2 * tx] = v0;
-    t[r][2 * tx + 1] = v1;
+    __nv_bfloat162 v;
+    v.x = zero;
+    v.y = zero;
+    if (i < N && j + 1 < N) {
+      v = *reinterpret_cast<const __nv_bfloat162*>(src + (long long)i * ld + j);
+    } else if (i < N && j < N) {
+      v.x = src[(long long)i * ld + j];
+    }
+    t[r][2 * tx] = v.x;
+    t[r][2 * tx + 1] = v.y;
   }
   __syncthreads();
   for (int r = ty; r < 64; r += 8) {
     const int j = j0 + r, i = i0 + 2 * tx;
-    if (j < N && i < N) dst[(long long)j * ld + i] = t[2 * tx][r];
-    if (j < N && i + 1 < N) dst[(long long)j * ld + i + 1] = t[2 * tx + 1][r];
+    if (j >= N || i >= N) continue;
+    if (i + 1 < N) {
+      __nv_bfloat162 v;
+      v.x = t[2 * tx][r];
+      v.y = t[2 * tx + 1][r];
+      *reinterpret_cast<__nv_bfloat162*>(dst + (long long)j * ld + i) = v;
+    } else {
+      dst[(long long)j * ld + i] = t[2 * tx][r];
+    }
   }
 }
 
