@@ -361,6 +361,29 @@ def run_ours(args, w):
                "d2h_bytes_per_step": len(w.directions) * zbytes, "steps": k_e2e,
                "ms_per_step": ms_e2e / k_e2e}
 
+    # the Pairformer's own chain: z <- z + outgoing(z); z <- z + incoming(z), in place (tm_pair_update,
+    # the residual add fused into the finish kernel), on a copy of z
+    pair = None
+    if w.dtype == "bf16" and not w.block and len(w.directions) == 2:
+        zc = z.clone()
+        for _ in range(2):
+            tm.tm_pair_update(mod.ctx, zc, mask)
+        barrier()
+        k_p = max(1, min(args.steps, 5))
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        p0.record()
+        for _ in range(k_p):
+            tm.tm_pair_update(mod.ctx, zc, mask)
+        p1.record()
+        barrier()
+        if tm.tm_sync_status(mod.ctx) != tm.TM_OK:
+            raise RuntimeError("device status after the pair update: " + tm.tm_last_error(mod.ctx))
+        ms_p = p0.elapsed_time(p1) / k_p
+        pair = {"ms_per_step": ms_p, "ms_per_update": ms_p / 2,
+                "tflops": 2 * flops_update(w.N, w.c_z, w.c_h) / (ms_p / 1e3) / 1e12, "steps": k_p,
+                "note": "outgoing then incoming on the updated z, residual adds fused, in place"}
+        del zc
+
     # backward pass (training): tm_backward per direction on the same z, a seeded bf16 cotangent
     bwd = None
     if not args.no_backward and w.dtype == "bf16" and not w.block:
@@ -483,7 +506,7 @@ def run_ours(args, w):
             "frac_of_bf16_peak": value / world / peaks["bf16_tflops"],
             "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches, "clocks": clk, "backward": bwd,
-            "triangle_attention": attn,
+            "triangle_attention": attn, "pair_update": pair,
         }
         print(json.dumps(line), flush=True)
     mod.close()

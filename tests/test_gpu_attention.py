@@ -88,3 +88,16 @@ def test_attention_is_deterministic_and_checks_arguments(env):
             tm.tm_forward(mod.ctx, z, None, "outgoing", torch.empty_like(z))
     finally:
         upd.close()
+
+
+def test_attention_refuses_a_workspace_over_the_limit(env):
+    torch, tm, mod, W = env
+    z = z_to_device(wl.make_z(200, 128, 3, "bf16"))
+    launches = tm.tm_launch_count(mod.ctx)
+    with pytest.raises(tm.TmError) as err:
+        tm.tm_attn_forward(mod.ctx, z, None, "starting", torch.empty_like(z), workspace_limit=1 << 20)
+    assert err.value.status == tm.TM_ERR_OOM
+    assert tm.tm_launch_count(mod.ctx) == launches
+    mod(z, None, "starting")
+    torch.cuda.synchronize()
+    assert tm.tm_sync_status(mod.ctx) == tm.TM_OK

@@ -169,3 +169,25 @@ def test_backward_bf16_is_deterministic_and_in_place(torch_tm):
             assert torch.equal(g1[k], g2[k]), k
     finally:
         mod.close()
+
+
+def test_backward_refuses_a_workspace_over_the_limit(torch_tm):
+    """Beyond tm_options.workspace_limit the backward returns TM_ERR_OOM before any launch, and the ctx
+    keeps working."""
+    torch, tm = torch_tm
+    N = 200
+    mod = tm.TriMul(128, 128, wl.make_weights(128, 128, 1))
+    try:
+        z = z_to_device(wl.make_z(N, 128, 1, "bf16"))
+        dout = z_to_device(_dout(N, 128, 2, "bf16"))
+        dz = torch.empty_like(z)
+        launches = tm.tm_launch_count(mod.ctx)
+        with pytest.raises(tm.TmError) as err:
+            tm.tm_backward(mod.ctx, z, None, "outgoing", dout, dz, None, workspace_limit=1 << 20)
+        assert err.value.status == tm.TM_ERR_OOM
+        assert tm.tm_launch_count(mod.ctx) == launches
+        tm.tm_backward(mod.ctx, z, None, "outgoing", dout, dz, None)
+        torch.cuda.synchronize()
+        assert tm.tm_sync_status(mod.ctx) == tm.TM_OK
+    finally:
+        mod.close()
