@@ -277,13 +277,20 @@ def run_ours(args, w):
     launches0 = tm.tm_launch_count(mod.ctx)
     tm.tm_set_timing(mod.ctx, True)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ev0.record()
-    for _ in range(args.steps):
+    for k in range(args.steps):
         step()
+        step_ev[k].record()             # one event per step: the distribution of step times
     ev1.record()
     barrier()
     clk = clocks.stop()
     ms_total = ev0.elapsed_time(ev1)
+    per_step = sorted([ev0.elapsed_time(step_ev[0])] +
+                      [step_ev[k - 1].elapsed_time(step_ev[k]) for k in range(1, args.steps)])
+    def pct(q):
+        return per_step[min(len(per_step) - 1, int(round(q * (len(per_step) - 1))))]
+    step_stats = {"median": statistics.median(per_step), "p10": pct(0.1), "p90": pct(0.9), "n": len(per_step)}
     launches = tm.tm_launch_count(mod.ctx) - launches0
     ktime = tm.tm_get_timing(mod.ctx)
     tm.tm_set_timing(mod.ctx, False)
@@ -360,6 +367,31 @@ def run_ours(args, w):
                "h2d_bytes_per_step": len(w.directions) * (zbytes + m_np.nbytes),
                "d2h_bytes_per_step": len(w.directions) * zbytes, "steps": k_e2e,
                "ms_per_step": ms_e2e / k_e2e}
+
+    # reference point for the contraction: cuBLAS (torch.bmm) over the 128 channel planes, bf16 in, bf16 out.
+    # Timed at N rounded up to a multiple of 64 (the row padding the library's own a and b use): at N = 3605 a
+    # bf16 row is 7210 bytes, not a multiple of 16, which keeps cuBLAS off its fast paths. Rates compare.
+    cublas = None
+    if w.dtype == "bf16" and not w.block:
+        nb = (w.N + 63) // 64 * 64
+        gen = torch.Generator(device="cuda").manual_seed(9)
+        A = torch.randn(w.c_h, nb, nb, device="cuda", generator=gen).to(torch.bfloat16)
+        B = torch.randn(w.c_h, nb, nb, device="cuda", generator=gen).to(torch.bfloat16)
+        C = torch.empty_like(A)
+        for _ in range(2):
+            torch.bmm(A, B.transpose(1, 2), out=C)
+        barrier()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record()
+        for _ in range(5):
+            torch.bmm(A, B.transpose(1, 2), out=C)
+        c1.record()
+        barrier()
+        ms_c = c0.elapsed_time(c1) / 5
+        tf_c = 2.0 * nb ** 3 * w.c_h / (ms_c / 1e3) / 1e12
+        cublas = {"ms": ms_c, "N": nb, "tflops": tf_c, "k2_over_cublas": (k2_tflops / tf_c) if k2_tflops else None,
+                  "op": f"torch.bmm(A, B^T), [{w.c_h}][{nb}][{nb}] bf16, outgoing form"}
+        del A, B, C
 
     # the Pairformer's own chain: z <- z + outgoing(z); z <- z + incoming(z), in place (tm_pair_update,
     # the residual add fused into the finish kernel), on a copy of z
@@ -506,7 +538,8 @@ def run_ours(args, w):
             "frac_of_bf16_peak": value / world / peaks["bf16_tflops"],
             "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches, "clocks": clk, "backward": bwd,
-            "triangle_attention": attn, "pair_update": pair,
+            "triangle_attention": attn, "pair_update": pair, "step_ms": step_stats,
+            "cublas_bmm_reference": cublas,
         }
         print(json.dumps(line), flush=True)
     mod.close()

@@ -506,6 +506,8 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_project(const BwdProjParams p) {
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
+constexpr int kTransposePlanes = 16;   // channel planes per block (the same 64 x 64 tile of each)
+
 // out[c][j][i] = in[c][i][j] for i, j < N (bf16 planes [128][N][ld], ld a multiple of 64); 64 x 64 tiles,
 // two elements per thread: rows start 128-byte aligned and every thread takes an even column pair, so a
 // pair inside the grid moves as one 4-byte load and one 4-byte store (scalar at the grid's ragged edge)
@@ -513,12 +515,13 @@ __global__ void __launch_bounds__(256) k_transpose_planes(const __nv_bfloat16* _
                                                           __nv_bfloat16* __restrict__ out, int N, long long ld,
                                                           long long plane) {
   __shared__ __nv_bfloat16 t[64][64 + 2];
-  const int c = blockIdx.z;
   const int i0 = blockIdx.y * 64, j0 = blockIdx.x * 64;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8
+  const __nv_bfloat16 zero = __float2bfloat16_rn(0.f);
+  for (int c = blockIdx.z * kTransposePlanes; c < (blockIdx.z + 1) * kTransposePlanes; ++c) {
   const __nv_bfloat16* src = in + c * plane;
   __nv_bfloat16* dst = out + c * plane;
-  const __nv_bfloat16 zero = __float2bfloat16_rn(0.f);
+  if (c > blockIdx.z * kTransposePlanes) __syncthreads();   // the previous plane's tile has been written out
   for (int r = ty; r < 64; r += 8) {
     const int i = i0 + r, j = j0 + 2 * tx;
     __nv_bfloat162 v;
@@ -544,6 +547,7 @@ __global__ void __launch_bounds__(256) k_transpose_planes(const __nv_bfloat16* _
     } else {
       dst[(long long)j * ld + i] = t[2 * tx][r];
     }
+  }
   }
 }
 
@@ -572,7 +576,8 @@ cudaError_t launch_bwd_project_bf16(const BwdProjParams& p, int grid, cudaStream
 
 cudaError_t launch_transpose_planes_bf16(const __nv_bfloat16* in, __nv_bfloat16* out, int N, long long ld, int planes,
                                          cudaStream_t s) {
-  dim3 grid((N + 63) / 64, (N + 63) / 64, planes);
+  if (planes % kTransposePlanes) return cudaErrorInvalidValue;
+  dim3 grid((N + 63) / 64, (N + 63) / 64, planes / kTransposePlanes);
   k_transpose_planes<<<grid, 256, 0, s>>>(in, out, N, ld, (long long)N * ld);
   return cudaGetLastError();
 }
