@@ -1,6 +1,8 @@
 // tm_api.cu -- the C ABI of libtm (declared in include/tm.h): argument
 // checking, weight preparation, the workspace, TMA tensor maps and the
-// block-streamed schedule of the triangle multiplicative update.
+// block-streamed schedule of the triangle multiplicative update. The backward
+// pass's host side is in tm_backward_api.cu, triangle attention's in
+// tm_attention_api.cu; what they share with this file is in tm_internal.h.
 //
 // Schedule of one bf16 update (tm_forward):
 //   projection       z -> a, b                    (one launch, whole grid)
@@ -27,19 +29,19 @@
 #include <string>
 #include <vector>
 
-#include "tm.h"
-#include "tm_kernels.h"
+#include "tm_internal.h"
 
 using namespace tmk;
 
-namespace {
+using namespace tmk;
+using namespace tmh;
 
+namespace {
 const char* kStatusText[] = {"ok", "invalid argument", "unsupported configuration", "out of workspace memory",
                              "CUDA error", "device wait timed out"};
+}  // namespace
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+namespace tmh {
 
 // The driver's tensor-map encoder, looked up once per process (contexts on different host threads may
 // ask for it at the same time).
@@ -56,60 +58,6 @@ EncodeTiledFn encode_fn() {
   });
   return fn;
 }
-
-inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
-inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-struct TimedLaunch {
-  cudaEvent_t start, stop;
-  int kind;
-  long long units;
-};
-
-}  // namespace
-
-struct tm_ctx {
-  int layer = 0;                 // 0: triangle multiplicative update, 1: triangle attention
-  int device = 0, num_sms = 0;
-  int c_z = 0, c_h = 0;
-  // float32 weights (device), one allocation
-  float* w32 = nullptr;
-  F32Weights f32w{};
-  // tensor-core path (c_z = c_h = 128)
-  bool tc = false;
-  __nv_bfloat16* wk1 = nullptr;  // [2 halves][hi, lo][256][128]
-  float* k1c = nullptr;          // [2][512]
-  __half* wo16 = nullptr;        // [128][128], scaled
-  __nv_bfloat16* wg16 = nullptr; // [hi, lo][128][128]
-  float k3c_host[4 * kC] = {};   // finish-kernel constants, passed in its parameter block
-  double ab_bound = 0;           // max_c of the bounds on |a_c| and |b_c| multiplied (fp16 x scale)
-  float inv_scale_o = 1.f;
-  CUtensorMap wk1_map, wo_map, wg_map;
-  // backward pass: bf16 images of W_g, W_o, W_a, W_ga, W_b, W_gb in the 128 x 128 operand-tile layout
-  // of the backward kernels, then gamma_in, beta_in, gamma_out, beta_out (float32)
-  void* wbwd = nullptr;
-  // triangle attention: bf16 images of W_q, W_k, W_v, W_g, W_o, then gamma, beta and W_b (float32)
-  void* ta_w = nullptr;
-  // status word (mapped host memory)
-  int* status_h = nullptr;
-  int* status_d = nullptr;
-  // workspace
-  void* ws = nullptr;
-  size_t ws_bytes = 0;
-  cudaStream_t ws_stream = nullptr;
-  size_t env_limit = 0;
-  // device staging of tm_forward_host
-  void* io = nullptr;
-  size_t io_bytes = 0;
-  // instrumentation
-  bool timing = false;
-  std::vector<TimedLaunch> timed;
-  std::vector<cudaEvent_t> event_pool;
-  long long launches = 0;
-  std::string err;
-};
-
-namespace {
 
 tm_status fail(tm_ctx* c, tm_status s, const char* fmt, ...) {
   if (c) {
@@ -161,25 +109,6 @@ cudaEvent_t take_event(tm_ctx* c) {
   return e;
 }
 
-// Launch wrapper: counts launches and, when timing is on, brackets the launch with events on `s`.
-template <typename F>
-cudaError_t timed(tm_ctx* c, int kind, long long units, cudaStream_t s, F&& launch) {
-  TimedLaunch tl{};
-  if (c->timing) {
-    tl.start = take_event(c);
-    tl.stop = take_event(c);
-    tl.kind = kind;
-    tl.units = units;
-    cudaEventRecord(tl.start, s);
-  }
-  cudaError_t e = launch();
-  if (e == cudaSuccess) ++c->launches;
-  if (c->timing) {
-    cudaEventRecord(tl.stop, s);
-    c->timed.push_back(tl);
-  }
-  return e;
-}
 
 tm_status check_device_status(tm_ctx* c) {
   volatile int* st = c->status_h;
@@ -542,213 +471,8 @@ int choose_block(const tm_ctx* c, int N, const tm_options* opt, size_t ab_bytes,
   }
 }
 
-// ---------------------------------------------------------------------- backward pass
-//
-// Schedule (both precisions): recompute a, b (projection) and x (contraction, float32); the
-// output backward gives dX, its transpose dX^T, and the gate's term of dzh; the two contraction
-// gradients are contractions again, with other operands:
-//   outgoing (X = A B^T):  dA = dX B   = incoming-form contraction of (dX^T, b)
-//                          dB = dX^T A = incoming-form contraction of (dX, a)
-//   incoming (X = A^T B):  dA = B dX^T = outgoing-form contraction of (b, dX)
-//                          dB = A dX   = outgoing-form contraction of (a, dX^T)
-// (the incoming form sums over the first index of both planes, the outgoing form over the second),
-// so the forward's contraction kernels serve unchanged; the projection backward then gives dz.
-// Every parameter gradient is a sum over the N^2 pairs, formed without atomics in fixed order.
+}  // namespace tmh
 
-tm_status backward_f32(tm_ctx* c, const float* z, const float* mask, int N, bool inc, const float* dout, float* dz,
-                       const tm_grads* g, cudaStream_t s, const tm_options* opt) {
-  const int Cz = c->c_z, Ch = c->c_h;
-  const long long P = (long long)N * N;
-  const int ld = N;
-  const size_t plane = align_up((size_t)Ch * N * ld * 4, 256);
-  const size_t vh = align_up((size_t)Ch * P * 4, 256), vz = align_up((size_t)Cz * P * 4, 256);
-  const size_t part = align_up((size_t)outer_sum_splits(P) * 256 * 256 * 4, 256);
-  // planes a, b, x (then dA), dX, dX^T, dB; vectors: 7 of c_h, 6 of c_z
-  const size_t need = 6 * plane + 7 * vh + 6 * vz + part;
-  tm_status st = ensure_workspace(c, need, s, opt);
-  if (st != TM_OK) return st;
-  uint8_t* q = reinterpret_cast<uint8_t*>(c->ws);
-  auto take = [&](size_t n) { float* r = reinterpret_cast<float*>(q); q += n; return r; };
-  float *a = take(plane), *b = take(plane), *x = take(plane), *dX = take(plane), *dXT = take(plane),
-        *dB = take(plane);
-  BwdF32Vectors v{};
-  v.dX = dX;
-  v.dXT = dXT;
-  v.dA = x;            // x is dead once the output backward has run
-  v.dB = dB;
-  v.ld = ld;
-  v.xh = take(vh);
-  v.q_out_n = take(vh);
-  v.q_out = take(vh);
-  v.dpa = take(vh);
-  v.dga = take(vh);
-  v.dpb = take(vh);
-  v.dgb = take(vh);
-  v.dzh = take(vz);
-  v.zh = take(vz);
-  v.dy = take(vz);
-  v.dgg = take(vz);
-  v.q_in_n = take(vz);
-  v.q_in = take(vz);
-  float* partial = take(part);
-  const F32Weights& w = c->f32w;
-  cudaError_t e;
-#define TM_F32_STEP(what, call)                                         \
-  e = timed(c, 3, P, s, [&] { return call; });                          \
-  if (e != cudaSuccess) return cuda_fail(c, e, what);
-  TM_F32_STEP("projection (f32) launch", launch_project_f32(z, mask, w, a, b, N, ld, s))
-  TM_F32_STEP("contraction (f32) launch",
-              launch_contract_f32(inc, a, b, N, ld, Ch, 0, 0, N, N, x, ld, (long long)N * ld, s))
-  TM_F32_STEP("output backward (f32) launch", launch_bwd_output_f32(x, ld, z, dout, w, N, v, s))
-  float* dA = x;
-  if (!inc) {
-    TM_F32_STEP("dA contraction (f32) launch",
-                launch_contract_f32(true, dXT, b, N, ld, Ch, 0, 0, N, N, dA, ld, (long long)N * ld, s))
-    TM_F32_STEP("dB contraction (f32) launch",
-                launch_contract_f32(true, dX, a, N, ld, Ch, 0, 0, N, N, dB, ld, (long long)N * ld, s))
-  } else {
-    TM_F32_STEP("dA contraction (f32) launch",
-                launch_contract_f32(false, b, dX, N, ld, Ch, 0, 0, N, N, dA, ld, (long long)N * ld, s))
-    TM_F32_STEP("dB contraction (f32) launch",
-                launch_contract_f32(false, a, dXT, N, ld, Ch, 0, 0, N, N, dB, ld, (long long)N * ld, s))
-  }
-  TM_F32_STEP("projection backward (f32) launch", launch_bwd_project_f32(z, mask, w, N, v, dz, s))
-  if (g) {
-    struct Sum { float* out; const float* U; const float* V; int O, K; };
-    const Sum sums[10] = {{g->w_g, v.dgg, v.zh, Cz, Cz},       {g->w_o, v.dy, v.xh, Cz, Ch},
-                          {g->w_a, v.dpa, v.zh, Ch, Cz},       {g->w_ga, v.dga, v.zh, Ch, Cz},
-                          {g->w_b, v.dpb, v.zh, Ch, Cz},       {g->w_gb, v.dgb, v.zh, Ch, Cz},
-                          {g->ln_out_gamma, v.q_out_n, nullptr, Ch, 1}, {g->ln_out_beta, v.q_out, nullptr, Ch, 1},
-                          {g->ln_in_gamma, v.q_in_n, nullptr, Cz, 1},   {g->ln_in_beta, v.q_in, nullptr, Cz, 1}};
-    for (const Sum& t : sums) {
-      if (!t.out) continue;
-      TM_F32_STEP("parameter gradient (f32) launch", launch_outer_sum_f32(t.U, t.V, t.O, t.K, P, partial, t.out, s))
-    }
-  }
-#undef TM_F32_STEP
-  return TM_OK;
-}
-
-tm_status backward_bf16(tm_ctx* c, const void* z, const float* mask, int N, bool inc, const void* dout, void* dz,
-                        const tm_grads* g, cudaStream_t s, const tm_options* opt) {
-  const long long P = (long long)N * N;
-  const int ld = (int)align_up(N, 64);     // bf16 planes a, b, dX, dX^T: 128-byte rows
-  const int ldx = (int)align_up(N, 32);    // float32 planes x (then dA), dB: 128-byte rows
-  const long long tiles = (P + 127) / 128;
-  const int grid = bwd_grid(tiles, c->num_sms);
-  const size_t pb = align_up((size_t)kC * N * ld * 2, 256);
-  const size_t xb = align_up((size_t)kC * N * ldx * 4, 256);
-  const size_t zb = align_up((size_t)P * sizeof(float2), 256);
-  const size_t hb = align_up((size_t)kC * P * 4, 256);
-  const size_t wb = align_up((size_t)grid * 2 * kC * kC * 4, 256);
-  const size_t lb = align_up((size_t)grid * 2 * kC * 4, 256);
-  tm_status st = ensure_workspace(c, 4 * pb + 2 * xb + zb + hb + 3 * wb + 2 * lb, s, opt);
-  if (st != TM_OK) return st;
-  uint8_t* q = reinterpret_cast<uint8_t*>(c->ws);
-  auto take = [&](size_t n) { uint8_t* r = q; q += n; return r; };
-  auto* a = reinterpret_cast<__nv_bfloat16*>(take(pb));
-  auto* b = reinterpret_cast<__nv_bfloat16*>(take(pb));
-  auto* dX = reinterpret_cast<__nv_bfloat16*>(take(pb));
-  auto* dXT = reinterpret_cast<__nv_bfloat16*>(take(pb));
-  float* x = reinterpret_cast<float*>(take(xb));     // x, then dA
-  float* dB = reinterpret_cast<float*>(take(xb));
-  auto* zstat = reinterpret_cast<float2*>(take(zb));
-  float* dzh = reinterpret_cast<float*>(take(hb));
-  float* part_o = reinterpret_cast<float*>(take(wb));
-  float* part_a = reinterpret_cast<float*>(take(wb));
-  float* part_b = reinterpret_cast<float*>(take(wb));
-  float* ln_o = reinterpret_cast<float*>(take(lb));
-  float* ln_i = reinterpret_cast<float*>(take(lb));
-  const auto* wimg = reinterpret_cast<const __nv_bfloat16*>(c->wbwd);
-  const float* ln4 = reinterpret_cast<const float*>(wimg + 6 * kC * kC);
-  auto W = [&](int m) { return wimg + (size_t)m * kC * kC; };   // W_g, W_o, W_a, W_ga, W_b, W_gb
-
-  st = run_project_bf16(c, z, mask, N, zstat, a, b, ld, s, opt);
-  if (st != TM_OK) return st;
-  st = run_contract_bf16(c, a, b, N, ld, inc, 0, 0, N, N, x, ldx, X_F32, 0, s, opt);
-  if (st != TM_OK) return st;
-
-  BwdOutParams po{};
-  po.z = reinterpret_cast<const __nv_bfloat16*>(z);
-  po.zstat = zstat;
-  po.x = x;
-  po.ldx = ldx;
-  po.xplane = (long long)N * ldx;
-  po.dout = reinterpret_cast<const __nv_bfloat16*>(dout);
-  po.dX = dX;
-  po.ld = ld;
-  po.dplane = (long long)N * ld;
-  po.dzh = dzh;
-  po.part_w = part_o;
-  po.part_ln = ln_o;
-  po.w_g = W(0);
-  po.w_o = W(1);
-  po.ln = ln4;
-  po.N = N;
-  po.P = P;
-  po.tiles = tiles;
-  po.w = watch(c, KID_BWD_OUTPUT, opt);
-  cudaError_t e = timed(c, 4, P, s, [&] { return launch_bwd_output_bf16(po, grid, s); });
-  if (e != cudaSuccess) return cuda_fail(c, e, "output backward launch");
-  e = timed(c, 6, P, s, [&] { return launch_transpose_planes_bf16(dX, dXT, N, ld, kC, s); });
-  if (e != cudaSuccess) return cuda_fail(c, e, "transpose launch");
-
-  float* dA = x;   // x is dead once the output backward has run
-  if (!inc) {
-    st = run_contract_bf16(c, dXT, b, N, ld, true, 0, 0, N, N, dA, ldx, X_F32, 0, s, opt);
-    if (st == TM_OK) st = run_contract_bf16(c, dX, a, N, ld, true, 0, 0, N, N, dB, ldx, X_F32, 0, s, opt);
-  } else {
-    st = run_contract_bf16(c, b, dX, N, ld, false, 0, 0, N, N, dA, ldx, X_F32, 0, s, opt);
-    if (st == TM_OK) st = run_contract_bf16(c, a, dXT, N, ld, false, 0, 0, N, N, dB, ldx, X_F32, 0, s, opt);
-  }
-  if (st != TM_OK) return st;
-
-  for (int side = 0; side < 2; ++side) {
-    BwdProjParams pp{};
-    pp.z = po.z;
-    pp.zstat = zstat;
-    pp.mask = mask;
-    pp.dV = side == 0 ? dA : dB;
-    pp.ldv = ldx;
-    pp.vplane = (long long)N * ldx;
-    pp.dzh = dzh;
-    pp.dz = reinterpret_cast<__nv_bfloat16*>(dz);
-    pp.final_pass = side;
-    pp.part_w = side == 0 ? part_a : part_b;
-    pp.part_ln = ln_i;
-    pp.w_v = W(2 + 2 * side);
-    pp.w_gt = W(3 + 2 * side);
-    pp.ln = ln4;
-    pp.N = N;
-    pp.P = P;
-    pp.tiles = tiles;
-    pp.w = watch(c, KID_BWD_PROJECT, opt);
-    e = timed(c, 5, P, s, [&] { return launch_bwd_project_bf16(pp, grid, s); });
-    if (e != cudaSuccess) return cuda_fail(c, e, "projection backward launch");
-  }
-  if (g) {
-    struct Sum { float* out; const float* part; long long E, stride; };
-    const long long WW = (long long)kC * kC;
-    const Sum sums[10] = {{g->w_g, part_o, WW, 2 * WW},       {g->w_o, part_o + WW, WW, 2 * WW},
-                          {g->w_a, part_a, WW, 2 * WW},       {g->w_ga, part_a + WW, WW, 2 * WW},
-                          {g->w_b, part_b, WW, 2 * WW},       {g->w_gb, part_b + WW, WW, 2 * WW},
-                          {g->ln_out_gamma, ln_o, kC, 2 * kC}, {g->ln_out_beta, ln_o + kC, kC, 2 * kC},
-                          {g->ln_in_gamma, ln_i, kC, 2 * kC},  {g->ln_in_beta, ln_i + kC, kC, 2 * kC}};
-    SumJobs jobs{};
-    for (const Sum& t : sums) {
-      jobs.part[jobs.n] = t.part;
-      jobs.out[jobs.n] = t.out;
-      jobs.E[jobs.n] = t.E;
-      jobs.stride[jobs.n] = t.stride;
-      ++jobs.n;
-    }
-    e = timed(c, 6, 0, s, [&] { return launch_sum_parts_multi(jobs, grid, s); });
-    if (e != cudaSuccess) return cuda_fail(c, e, "parameter gradient sum launch");
-  }
-  return TM_OK;
-}
-
-}  // namespace
 
 // ====================================================================== C ABI
 
@@ -1046,201 +770,6 @@ tm_status tm_forward_host(tm_ctx* c, const void* z_host, const float* mask_host,
   if (st != TM_OK) return st;
   e = cudaMemcpyAsync(out_host, od, zbytes, cudaMemcpyDeviceToHost, s);
   return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "cudaMemcpyAsync(device to host)");
-}
-
-tm_status tm_backward(tm_ctx* c, const void* z, const float* mask, int N, tm_dtype dtype, tm_direction dir,
-                      const void* dout, void* dz, const tm_grads* grads, void* stream, const tm_options* opt) {
-  tm_status st = check_common(c, N, dtype);
-  if (st != TM_OK) return st;
-  if (dir != TM_OUTGOING && dir != TM_INCOMING) return fail(c, TM_ERR_INVALID, "unknown direction %d", (int)dir);
-  if (!z || !dout || !dz || !aligned16(z) || !aligned16(dout) || !aligned16(dz))
-    return fail(c, TM_ERR_INVALID, "z, dout and dz must be non-null and 16-byte aligned");
-  if (mask && (reinterpret_cast<uintptr_t>(mask) & 3u)) return fail(c, TM_ERR_INVALID, "mask must be 4-byte aligned");
-  if (opt) {
-    for (int r : opt->reserved)
-      if (r) return fail(c, TM_ERR_INVALID, "tm_options.reserved must be zero");
-    if (opt->block || opt->x_storage || opt->residual)
-      return fail(c, TM_ERR_INVALID, "tm_backward takes no block, x_storage or residual option");
-    if (opt->timeout_ms < 0) return fail(c, TM_ERR_INVALID, "negative option");
-  }
-  if (grads) {
-    const float* gp[10] = {grads->ln_in_gamma, grads->ln_in_beta, grads->w_a, grads->w_ga, grads->w_b,
-                           grads->w_gb, grads->w_g, grads->ln_out_gamma, grads->ln_out_beta, grads->w_o};
-    for (const float* q : gp)
-      if (q && (reinterpret_cast<uintptr_t>(q) & 15u))
-        return fail(c, TM_ERR_INVALID, "gradient arrays must be 16-byte aligned");
-  }
-  const size_t zbytes = (size_t)N * N * c->c_z * (dtype == TM_BF16 ? 2 : 4);
-  if (ranges_overlap(z, zbytes, dz, zbytes)) return fail(c, TM_ERR_INVALID, "dz overlaps z");
-  if (dz != dout && ranges_overlap(dout, zbytes, dz, zbytes))
-    return fail(c, TM_ERR_INVALID, "dz overlaps dout without being dout");
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const bool inc = dir == TM_INCOMING;
-  if (dtype == TM_F32)
-    return backward_f32(c, reinterpret_cast<const float*>(z), mask, N, inc, reinterpret_cast<const float*>(dout),
-                        reinterpret_cast<float*>(dz), grads, s, opt);
-  return backward_bf16(c, z, mask, N, inc, dout, dz, grads, s, opt);
-}
-
-// ---------------------------------------------------------------------- triangle attention
-tm_status tm_attn_create(int c_z, int heads, int c_head, const tm_attn_weights* w, tm_ctx** out_ctx) {
-  if (!w || !out_ctx) return TM_ERR_INVALID;
-  const float* req[] = {w->ln_gamma, w->ln_beta, w->w_q, w->w_k, w->w_v, w->w_b, w->w_g, w->w_o};
-  for (const float* q : req)
-    if (!q) return TM_ERR_INVALID;
-  if (c_z < 1 || heads < 1 || c_head < 1) return TM_ERR_INVALID;
-  if (c_z != kC || heads != 4 || c_head != 32) return TM_ERR_UNSUPPORTED;
-  tm_ctx* c = new tm_ctx();
-  c->layer = 1;
-  cudaError_t e = cudaGetDevice(&c->device);
-  if (e != cudaSuccess) {
-    delete c;
-    cudaGetLastError();
-    return TM_ERR_CUDA;
-  }
-  cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
-  c->c_z = c_z;
-  c->c_h = heads * c_head;
-  if (const char* env = std::getenv("TM_WORKSPACE_LIMIT")) c->env_limit = (size_t)std::strtoull(env, nullptr, 10);
-  e = cudaHostAlloc(reinterpret_cast<void**>(&c->status_h), 64, cudaHostAllocMapped);
-  if (e != cudaSuccess) {
-    tm_destroy(c);
-    cudaGetLastError();
-    return TM_ERR_CUDA;
-  }
-  std::memset(c->status_h, 0, 64);
-  cudaHostGetDevicePointer(reinterpret_cast<void**>(&c->status_d), c->status_h, 0);
-  // bf16 tile images of W_q, W_k, W_v, W_g, W_o, then gamma, beta, W_b as float32
-  const size_t T = (size_t)kC * kC;
-  std::vector<__nv_bfloat16> img(5 * T);
-  const float* mats[5] = {w->w_q, w->w_k, w->w_v, w->w_g, w->w_o};
-  for (int m = 0; m < 5; ++m) make_tile_image(mats[m], img.data() + m * T);
-  std::vector<float> f(2 * kC + 4 * kC);
-  for (int k = 0; k < kC; ++k) {
-    f[k] = w->ln_gamma[k];
-    f[kC + k] = w->ln_beta[k];
-  }
-  for (int k = 0; k < 4 * kC; ++k) f[2 * kC + k] = w->w_b[k];
-  const size_t ib = img.size() * sizeof(img[0]);
-  e = cudaMalloc(&c->ta_w, ib + f.size() * sizeof(float));
-  if (e == cudaSuccess) e = cudaMemcpy(c->ta_w, img.data(), ib, cudaMemcpyHostToDevice);
-  if (e == cudaSuccess)
-    e = cudaMemcpy(reinterpret_cast<uint8_t*>(c->ta_w) + ib, f.data(), f.size() * sizeof(float), cudaMemcpyHostToDevice);
-  if (e != cudaSuccess) {
-    tm_destroy(c);
-    cudaGetLastError();
-    return TM_ERR_CUDA;
-  }
-  *out_ctx = c;
-  return TM_OK;
-}
-
-tm_status tm_attn_forward(tm_ctx* c, const void* z, const float* mask, int N, tm_dtype dtype, tm_attn_node node,
-                          void* out, void* stream, const tm_options* opt) {
-  if (!c) return TM_ERR_INVALID;
-  c->err.clear();
-  if (c->layer != 1) return fail(c, TM_ERR_INVALID, "this ctx holds a triangle multiplicative update (tm_forward)");
-  if (N < 1 || N > 65535) return fail(c, TM_ERR_INVALID, "N=%d outside [1, 65535]", N);
-  if (dtype != TM_BF16) return fail(c, dtype == TM_F32 ? TM_ERR_UNSUPPORTED : TM_ERR_INVALID, "triangle attention runs in bf16");
-  if (node != TM_ATTN_STARTING && node != TM_ATTN_ENDING) return fail(c, TM_ERR_INVALID, "unknown node %d", (int)node);
-  if (!z || !out || !aligned16(z) || !aligned16(out))
-    return fail(c, TM_ERR_INVALID, "z and out must be non-null and 16-byte aligned");
-  if (mask && (reinterpret_cast<uintptr_t>(mask) & 3u)) return fail(c, TM_ERR_INVALID, "mask must be 4-byte aligned");
-  if (opt) {
-    for (int r : opt->reserved)
-      if (r) return fail(c, TM_ERR_INVALID, "tm_options.reserved must be zero");
-    if (opt->block || opt->x_storage || opt->residual || opt->timeout_ms < 0)
-      return fail(c, TM_ERR_INVALID, "tm_attn_forward takes only timeout_ms and workspace_limit");
-  }
-  int dev = -1;
-  cudaGetDevice(&dev);
-  if (dev != c->device) return fail(c, TM_ERR_INVALID, "current device %d is not the ctx's device %d", dev, c->device);
-  tm_status st = check_device_status(c);
-  if (st != TM_OK) return st;
-  const size_t zbytes = (size_t)N * N * kC * 2;
-  if (ranges_overlap(z, zbytes, out, zbytes)) return fail(c, TM_ERR_INVALID, "out overlaps z");
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const bool tr = node == TM_ATTN_ENDING;
-  const long long P = (long long)N * N;
-  const long long ldv = (long long)align_up(N, 64), ldb = ldv;
-  const size_t pb = align_up(zbytes, 256);
-  const size_t vb = align_up((size_t)N * kC * ldv * 2, 256);
-  const size_t bb = align_up((size_t)4 * N * ldb * 2, 256);
-  st = ensure_workspace(c, 4 * pb + vb + bb, s, opt);
-  if (st != TM_OK) return st;
-  uint8_t* q8 = reinterpret_cast<uint8_t*>(c->ws);
-  auto* q = reinterpret_cast<__nv_bfloat16*>(q8);
-  auto* k = reinterpret_cast<__nv_bfloat16*>(q8 + pb);
-  auto* g = reinterpret_cast<__nv_bfloat16*>(q8 + 2 * pb);
-  auto* o = reinterpret_cast<__nv_bfloat16*>(q8 + 3 * pb);
-  auto* vt = reinterpret_cast<__nv_bfloat16*>(q8 + 4 * pb);
-  auto* bias = reinterpret_cast<__nv_bfloat16*>(q8 + 4 * pb + vb);
-  const auto* wimg = reinterpret_cast<const __nv_bfloat16*>(c->ta_w);
-  const float* wf = reinterpret_cast<const float*>(wimg + 5 * kC * kC);
-  const long long tiles = (P + 127) / 128;
-  const int grid = (int)std::min<long long>(tiles, c->num_sms);
-
-  TaProjectParams pp{};
-  pp.z = reinterpret_cast<const __nv_bfloat16*>(z);
-  pp.mask = mask;
-  pp.transpose = tr ? 1 : 0;
-  pp.ln = wf;
-  pp.w_b = wf + 2 * kC;
-  pp.w_q = wimg;
-  pp.w_k = wimg + kC * kC;
-  pp.w_v = wimg + 2 * kC * kC;
-  pp.w_g = wimg + 3 * kC * kC;
-  pp.q = q;
-  pp.k = k;
-  pp.g = g;
-  pp.vt = vt;
-  pp.b = bias;
-  pp.ldv = ldv;
-  pp.ldb = ldb;
-  pp.N = N;
-  pp.P = P;
-  pp.tiles = tiles;
-  pp.w = watch(c, KID_TA_PROJECT, opt);
-  cudaError_t e = timed(c, 8, P, s, [&] { return launch_ta_project(pp, grid, s); });
-  if (e != cudaSuccess) return cuda_fail(c, e, "attention projection launch");
-
-  CUtensorMap qmap, kmap, vmap, bmap;
-  {
-    const cuuint64_t d[3] = {(cuuint64_t)kC, (cuuint64_t)N, (cuuint64_t)N};
-    const cuuint64_t st2[2] = {(cuuint64_t)kC * 2, (cuuint64_t)N * kC * 2};
-    if (!encode(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, d, st2, kBoxTaQK, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, k, d, st2, kBoxTaQK, CU_TENSOR_MAP_SWIZZLE_128B))
-      return fail(c, TM_ERR_CUDA, "tensor map (q/k)");
-    const cuuint64_t dv[3] = {(cuuint64_t)N, (cuuint64_t)kC, (cuuint64_t)N};
-    const cuuint64_t sv[2] = {(cuuint64_t)ldv * 2, (cuuint64_t)kC * ldv * 2};
-    if (!encode(&vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, vt, dv, sv, kBoxTaV, CU_TENSOR_MAP_SWIZZLE_128B))
-      return fail(c, TM_ERR_CUDA, "tensor map (v)");
-    const cuuint64_t db[3] = {(cuuint64_t)N, (cuuint64_t)N, 4};
-    const cuuint64_t sb[2] = {(cuuint64_t)ldb * 2, (cuuint64_t)N * ldb * 2};
-    if (!encode(&bmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, bias, db, sb, kBoxTaBias, CU_TENSOR_MAP_SWIZZLE_128B))
-      return fail(c, TM_ERR_CUDA, "tensor map (bias)");
-  }
-  TaAttendParams pa{};
-  pa.mask = mask;
-  pa.g = g;
-  pa.o = o;
-  pa.N = N;
-  pa.jblocks = (N + 127) / 128;
-  pa.w = watch(c, KID_TA_ATTEND, opt);
-  e = timed(c, 9, P, s, [&] { return launch_ta_attend(qmap, kmap, vmap, bmap, pa, s); });
-  if (e != cudaSuccess) return cuda_fail(c, e, "attention launch");
-
-  TaOutParams po{};
-  po.o = o;
-  po.w_o = wimg + 4 * kC * kC;
-  po.out = reinterpret_cast<__nv_bfloat16*>(out);
-  po.transpose = tr ? 1 : 0;
-  po.N = N;
-  po.P = P;
-  po.tiles = tiles;
-  po.w = watch(c, KID_TA_OUT, opt);
-  e = timed(c, 10, P, s, [&] { return launch_ta_out(po, grid, s); });
-  return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "attention output launch");
 }
 
 tm_status tm_sync_status(tm_ctx* c, void* stream) {

@@ -1,0 +1,121 @@
+// tm_internal.h -- what the host files of libtm share: the context behind the opaque tm_ctx of the C ABI
+// and the helpers that check arguments, encode tensor maps, time launches, hold the workspace and launch
+// the update's three bf16 stages. Not part of the public interface (include/tm.h is).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "tm.h"
+#include "tm_kernels.h"
+
+namespace tmh {
+
+using namespace tmk;
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn();
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct TimedLaunch {
+  cudaEvent_t start, stop;
+  int kind;
+  long long units;
+};
+
+}  // namespace tmh
+
+struct tm_ctx {
+  int layer = 0;                 // 0: triangle multiplicative update, 1: triangle attention
+  int device = 0, num_sms = 0;
+  int c_z = 0, c_h = 0;
+  // float32 weights (device), one allocation
+  float* w32 = nullptr;
+  tmk::F32Weights f32w{};
+  // tensor-core path (c_z = c_h = 128)
+  bool tc = false;
+  __nv_bfloat16* wk1 = nullptr;  // [2 halves][hi, lo][256][128]
+  float* k1c = nullptr;          // [2][512]
+  __half* wo16 = nullptr;        // [128][128], scaled
+  __nv_bfloat16* wg16 = nullptr; // [hi, lo][128][128]
+  float k3c_host[4 * tmk::kC] = {};  // finish-kernel constants, passed in its parameter block
+  double ab_bound = 0;           // max_c of the bounds on |a_c| and |b_c| multiplied (fp16 x scale)
+  float inv_scale_o = 1.f;
+  CUtensorMap wk1_map, wo_map, wg_map;
+  // backward pass: bf16 images of W_g, W_o, W_a, W_ga, W_b, W_gb in the 128 x 128 operand-tile layout
+  // of the backward kernels, then gamma_in, beta_in, gamma_out, beta_out (float32)
+  void* wbwd = nullptr;
+  // triangle attention: bf16 images of W_q, W_k, W_v, W_g, W_o, then gamma, beta and W_b (float32)
+  void* ta_w = nullptr;
+  // status word (mapped host memory)
+  int* status_h = nullptr;
+  int* status_d = nullptr;
+  // workspace
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  cudaStream_t ws_stream = nullptr;
+  size_t env_limit = 0;
+  // device staging of tm_forward_host
+  void* io = nullptr;
+  size_t io_bytes = 0;
+  // instrumentation
+  bool timing = false;
+  std::vector<tmh::TimedLaunch> timed;
+  std::vector<cudaEvent_t> event_pool;
+  long long launches = 0;
+  std::string err;
+};
+
+namespace tmh {
+
+tm_status fail(tm_ctx* c, tm_status s, const char* fmt, ...);
+tm_status cuda_fail(tm_ctx* c, cudaError_t e, const char* what);
+bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const cuuint64_t* dims,
+            const cuuint64_t* strides, const Box& b, CUtensorMapSwizzle sw);
+Watch watch(const tm_ctx* c, int kernel, const tm_options* opt);
+cudaEvent_t take_event(tm_ctx* c);
+tm_status check_device_status(tm_ctx* c);
+size_t limit_of(const tm_ctx* c, const tm_options* opt);
+tm_status ensure_workspace(tm_ctx* c, size_t bytes, cudaStream_t s, const tm_options* opt);
+bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb);
+void make_tile_image(const float* W, __nv_bfloat16* img);
+tm_status run_project_bf16(tm_ctx* c, const void* z, const float* mask, int N, float2* zstat, __nv_bfloat16* a,
+                           __nv_bfloat16* b, int ld, cudaStream_t s, const tm_options* opt);
+tm_status run_contract_bf16(tm_ctx* c, const __nv_bfloat16* a, const __nv_bfloat16* b, int N, int ld, bool incoming,
+                            int i0, int j0, int bi, int bj, void* x, int ldx, XFormat xf, int x_exp,
+                            cudaStream_t s, const tm_options* opt);
+tm_status run_finish_bf16(tm_ctx* c, const void* x, int ldx, XFormat xf, int x_exp, const float2* zstat, const void* z, int N,
+                          int i0, int j0, int bi, int bj, void* out, bool residual, cudaStream_t s,
+                          const tm_options* opt);
+int x16_exponent(const tm_ctx* c, int N);
+tm_status check_common(tm_ctx* c, int N, tm_dtype dtype);
+int choose_block(const tm_ctx* c, int N, const tm_options* opt, size_t ab_bytes, size_t xe);
+
+// Launch wrapper: counts launches and, when timing is on, brackets the launch with events on `s`.
+template <typename F>
+cudaError_t timed(tm_ctx* c, int kind, long long units, cudaStream_t s, F&& launch) {
+  TimedLaunch tl{};
+  if (c->timing) {
+    tl.start = take_event(c);
+    tl.stop = take_event(c);
+    tl.kind = kind;
+    tl.units = units;
+    cudaEventRecord(tl.start, s);
+  }
+  cudaError_t e = launch();
+  if (e == cudaSuccess) ++c->launches;
+  if (c->timing) {
+    cudaEventRecord(tl.stop, s);
+    c->timed.push_back(tl);
+  }
+  return e;
+}
+
+}  // namespace tmh
