@@ -119,6 +119,24 @@ def dist_setup():
     return world, rank, local
 
 
+def max_over_ranks(ms, device):
+    """The largest of ms over the ranks of the default process group (a job ends with its slowest rank);
+    ms itself when there is no group or a single rank."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms
+    import torch
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world, units_per_rank, ms):
+    """Whole-job throughput: the units every rank processed, summed over the ranks, over the slowest
+    rank's time in ms (each rank runs its own replica of the workload: weak scaling)."""
+    return world * units_per_rank / (ms / 1e3)
+
+
 def host_cores():
     try:
         from threadpoolctl import threadpool_info
@@ -296,14 +314,10 @@ def run_ours(args, w):
     tm.tm_set_timing(mod.ctx, False)
     if tm.tm_sync_status(mod.ctx) != tm.TM_OK:
         raise RuntimeError("device status after the timed region: " + tm.tm_last_error(mod.ctx))
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms_total], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, "cuda")
 
     flops_step = len(w.directions) * flops_update(w.N, w.c_z, w.c_h)
-    value = world * args.steps * flops_step / (ms_total / 1e3) / 1e12
+    value = job_rate(world, args.steps * flops_step, ms_total) / 1e12
     peaks, peak_src = read_peaks()
 
     # dominant kernel: the contraction. FLOPs per launch = 2 * N(k) * channels * output pairs.
@@ -356,14 +370,9 @@ def run_ours(args, w):
             step_host()
         e1.record()
         barrier()
-        ms_e2e = e0.elapsed_time(e1)
-        if world > 1:
-            import torch.distributed as dist
-            t = torch.tensor([ms_e2e], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms_e2e = float(t.item())
+        ms_e2e = max_over_ranks(e0.elapsed_time(e1), "cuda")
         zbytes = z_np.nbytes
-        e2e = {"value": world * k_e2e * flops_step / (ms_e2e / 1e3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": job_rate(world, k_e2e * flops_step, ms_e2e) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": len(w.directions) * (zbytes + m_np.nbytes),
                "d2h_bytes_per_step": len(w.directions) * zbytes, "steps": k_e2e,
                "ms_per_step": ms_e2e / k_e2e}
