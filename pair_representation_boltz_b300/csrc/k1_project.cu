@@ -364,12 +364,11 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 cudaError_t launch_project_bf16(const CUtensorMap& zmap, const CUtensorMap& wmap, const CUtensorMap& amap,
                                 const CUtensorMap& bmap, const ProjectParams& p, int num_sms, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k1_project, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static bool attr_set[kMaxDevices] = {};
+  cudaError_t e = once_per_device(attr_set, [] {
+    return cudaFuncSetAttribute(k1_project, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  });
+  if (e != cudaSuccess) return e;
   if (p.total_tiles <= 0) return cudaSuccess;
   long long pairs = num_sms / 2;
   if (pairs > p.total_tiles) pairs = p.total_tiles;

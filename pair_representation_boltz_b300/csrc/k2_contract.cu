@@ -339,16 +339,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
 cudaError_t launch_contract_bf16(bool incoming, const CUtensorMap& amap, const CUtensorMap& bmap,
                                  const CUtensorMap& xmap, const ContractParams& p, int num_sms, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
+  static bool attr_set[kMaxDevices] = {};
+  cudaError_t err = once_per_device(attr_set, [] {
     const void* fns[4] = {(const void*)k2_contract<false, false>, (const void*)k2_contract<true, false>,
                           (const void*)k2_contract<false, true>, (const void*)k2_contract<true, true>};
     for (const void* f : fns) {
       cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
       if (e != cudaSuccess) return e;
     }
-    attr_set = true;
-  }
+    return cudaSuccess;
+  });
+  if (err != cudaSuccess) return err;
   if (p.total_tiles <= 0) return cudaSuccess;
   long long pairs = num_sms / 2;
   if (pairs > p.total_tiles) pairs = p.total_tiles;

@@ -583,14 +583,13 @@ __global__ void __launch_bounds__(THREADS, 1)
 cudaError_t launch_finish_bf16(bool x16, const CUtensorMap& xmap, const CUtensorMap& zmap,
                                const CUtensorMap& womap, const CUtensorMap& wgmap, const CUtensorMap& omap,
                                const FinishParams& p, int num_sms, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
+  static bool attr_set[kMaxDevices] = {};
+  cudaError_t err = once_per_device(attr_set, [] {
     cudaError_t e = cudaFuncSetAttribute(k3_finish_x16, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k3_finish_x32, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+    return cudaFuncSetAttribute(k3_finish_x32, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  });
+  if (err != cudaSuccess) return err;
   if (p.total_tiles <= 0) return cudaSuccess;
   const int grid = (int)(p.total_tiles < num_sms ? p.total_tiles : num_sms);
   if (x16)

@@ -238,6 +238,22 @@ constexpr Box kBoxTaQK{64, 128, 1, 2};     // 64 channels (a head pair) x 128 po
 constexpr Box kBoxTaV{64, 32, 1, 2};       // 64 keys x 32 channels of one head of one row
 constexpr Box kBoxTaBias{64, 128, 1, 2};   // 64 keys x 128 queries of one head
 
+// The dynamic shared-memory limit of a kernel is a property of the kernel's instance on one device
+// (cudaFuncSetAttribute acts on the current device), so the launchers raise it once per device rather
+// than once per process; later launches, including those recorded into a CUDA graph, find it set.
+constexpr int kMaxDevices = 64;
+template <typename F>
+cudaError_t once_per_device(bool (&done)[kMaxDevices], F&& set) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (done[dev]) return cudaSuccess;
+  e = set();
+  if (e == cudaSuccess) done[dev] = true;
+  return e;
+}
+
 // ----------------------------------------------------------------- diagnostics
 enum : int { KID_SELFTEST = 9 };
 cudaError_t launch_watchdog_selftest(const Watch& w, cudaStream_t s);
