@@ -265,12 +265,12 @@ def tm_backward(ctx, z, mask, direction, dout, dz, grads=None, stream=None, time
     N = z.shape[0]
     g = None
     if grads is not None:
-        g = TmGrads(*[_ptr(grads[n]) if n in grads else None for n in WEIGHT_FIELDS])
         for n, t in grads.items():
             if n not in WEIGHT_FIELDS:
                 raise KeyError(f"unknown parameter {n!r}")
             if str(t.dtype) != "torch.float32":
                 raise TypeError(f"gradient {n} must be float32")
+        g = TmGrads(*[_ptr(grads[n]) if n in grads else None for n in WEIGHT_FIELDS])
     opt = TmOptions(0, timeout_ms, workspace_limit, 0, 0)
     _check(ctx, load_library().tm_backward(ctx, _ptr(z), _ptr(mask), N, _dtype_code(z), _direction(direction),
                                            _ptr(dout), _ptr(dz), C.byref(g) if g is not None else None,

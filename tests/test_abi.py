@@ -65,3 +65,13 @@ def test_library_is_built_for_sm_103a(libtm):
     # the build command pins the architecture; check the flag list rather than the binary
     assert "arch=compute_103a,code=sm_103a" in " ".join(build.ARCH)
     assert os.path.getsize(tm.LIB_PATH) > 0
+
+
+def test_backward_binding_checks_the_gradient_dict_first():
+    """A misnamed or non-float32 gradient is reported by name, before any tensor is handed to libtm."""
+    import torch
+    z = torch.zeros(4, 4, 16)
+    with pytest.raises(KeyError, match="w_typo"):
+        tm.tm_backward(None, z, None, "outgoing", z, z, {"w_typo": torch.zeros(16, 16)})
+    with pytest.raises(TypeError, match="w_g"):
+        tm.tm_backward(None, z, None, "outgoing", z, z, {"w_g": torch.zeros(16, 16, dtype=torch.float64)})
