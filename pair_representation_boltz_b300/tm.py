@@ -10,7 +10,8 @@ The function names mirror the C ABI: tm_create, tm_forward, tm_forward_ex, tm_fo
 tm_forward_noalloc, tm_pair_update, tm_backward, tm_attn_create, tm_attn_forward,
 tm_project, tm_contract, tm_finish, tm_sync_status, tm_watchdog_selftest, tm_set_timing,
 tm_get_timing, tm_launch_count, tm_workspace_bytes, tm_status_string,
-tm_last_error, tm_destroy. ``TriMul`` wraps a context for convenience.
+tm_last_error, tm_destroy. ``TriMul`` (the update, with ``backward``) and ``TriangleAttention`` wrap a
+context for convenience.
 """
 from __future__ import annotations
 
