@@ -55,12 +55,21 @@ def profiled_traffic():
     if not os.path.exists(K2_PROFILE):
         return None
     text = open(K2_PROFILE).read()
-    h = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    h = re.search(r"device_code_sha256:\s*([0-9a-f]{64})", text)
     t = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
     if not h or not t:
         return None
-    cur = hashlib.sha256(open(K2_SOURCE, "rb").read()).hexdigest()
+    cur = device_code_sha256(K2_SOURCE)
     return float(t.group(1)) if cur == h.group(1) else None
+
+
+def device_code_sha256(path: str) -> str:
+    """sha256 of a kernel file's device code: the text before its first host launcher definition
+    ("cudaError_t launch_"), so that edits to the host-side launcher alone keep a profile's counters
+    attached to the kernel they were taken from."""
+    text = open(path, "rb").read()
+    cut = text.find(b"\ncudaError_t launch_")
+    return hashlib.sha256(text if cut < 0 else text[:cut]).hexdigest()
 
 
 class ClockSampler:
@@ -137,6 +146,25 @@ def job_rate(world, units_per_rank, ms):
     return world * units_per_rank / (ms / 1e3)
 
 
+# Algorithmic bytes per pair of the bandwidth-bound passes (c = 128): the projection reads z (256 B)
+# and writes a and b (512 B); the finish reads x in its default fp16 storage (128 channels x 2 B) and z,
+# and writes out (256 B each).
+PROJECT_BYTES_PER_PAIR = 256 + 512
+FINISH_BYTES_PER_PAIR = 128 * 2 + 256 + 256
+
+
+def add_kernel_bandwidth(kernels, ktime, peaks):
+    """GB/s of the projection and finish kernels over their algorithmic bytes, and its fraction of the
+    measured copy bandwidth."""
+    for name, per_pair in (("project", PROJECT_BYTES_PER_PAIR), ("finish", FINISH_BYTES_PER_PAIR)):
+        v = ktime[name]
+        if v["ms"] > 0 and name in kernels:
+            gbs = v["units"] * per_pair / (v["ms"] / 1e3) / 1e9
+            kernels[name]["gbs"] = gbs
+            kernels[name]["frac_of_hbm"] = gbs / peaks["hbm_gbs"]
+            kernels[name]["bytes_per_pair"] = per_pair
+
+
 def host_cores():
     try:
         from threadpoolctl import threadpool_info
@@ -203,6 +231,78 @@ def oracle_attention_sample(n):
     f = 4.0 * n ** 3 * 128 + float(n) ** 2 * (2 * 128 * (4 * 128 + 4) + 2 * 128 * 128)
     return {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
             "sample": f"full float64 triangle attention at N={n}, starting node", "seconds": dt}
+
+
+def measure_config(tm, torch, name, steps, warmup, peaks, barrier):
+    """ms per update, per-kernel ms and the contraction's fraction of bf16 peak for another workload of
+    the metric, in this run. z is drawn on the device (seeded normal values rounded to bf16), the mask
+    and weights are the workload's own; every step runs the workload's directions once each."""
+    import numpy as np
+    import workloads as wl
+    w = wl.WORKLOADS[name]
+    gen = torch.Generator(device="cuda").manual_seed(w.seed_z)
+    z = torch.randn((w.N, w.N, w.c_z), device="cuda", generator=gen).to(torch.bfloat16)
+    mask = torch.from_numpy(np.ascontiguousarray(wl.make_mask(w.N, w.mask))).cuda()
+    mod = tm.TriMul(w.c_z, w.c_h, wl.make_weights(w.c_z, w.c_h, w.seed_w))
+    out = torch.empty_like(z)
+    opts = {"block": w.block} if w.block else {}
+
+    def step():
+        for d in w.directions:
+            tm.tm_forward_ex(mod.ctx, z, mask, d, out, **opts)
+
+    for _ in range(warmup):
+        step()
+    barrier()
+    tm.tm_set_timing(mod.ctx, True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    l0 = tm.tm_launch_count(mod.ctx)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    barrier()
+    ms = e0.elapsed_time(e1)
+    kt = tm.tm_get_timing(mod.ctx)
+    tm.tm_set_timing(mod.ctx, False)
+    if tm.tm_sync_status(mod.ctx) != tm.TM_OK:
+        raise RuntimeError(f"device status after {name}: " + tm.tm_last_error(mod.ctx))
+    launches = tm.tm_launch_count(mod.ctx) - l0
+    updates = steps * len(w.directions)
+    kernels = {k: {"launches": v["launches"], "ms_per_launch": v["ms"] / v["launches"]}
+               for k, v in kt.items() if v["launches"]}
+    add_kernel_bandwidth(kernels, kt, peaks)
+    kc = kt["contract"]
+    k2 = 2.0 * w.N * kc["units"] / (kc["ms"] / 1e3) / 1e12 if kc["ms"] > 0 else None
+    res = {"workload": f"{name}: N={w.N} {w.mask} mask, {' + '.join(w.directions)}"
+                       + (f", {w.block}x{w.block} output blocks" if w.block else ""),
+           "N": w.N, "steps": steps, "warmup": warmup, "ms_per_update": ms / updates,
+           "tflops": flops_update(w.N, w.c_z, w.c_h) * updates / (ms / 1e3) / 1e12, "gpu_launches": launches,
+           "kernels": kernels, "contraction_tflops": k2,
+           "contraction_frac_of_bf16_peak": k2 / peaks["bf16_tflops"] if k2 else None,
+           "contraction_frac_of_sustained": k2 / peaks["bf16_tflops_sustained"] if k2 else None,
+           "z": "torch.randn on the device (seeded), rounded to bf16"}
+    mod.close()
+    del z, out, mask
+    torch.cuda.empty_cache()
+    return res
+
+
+def oracle_full_timing(name, directions):
+    """The plain float64 oracle over a whole workload grid (every entry), timed on the host cores."""
+    import oracle
+    import workloads as wl
+    w = wl.WORKLOADS[name]
+    z, m, W = wl.make_inputs(w)
+    storage = "bf16" if w.dtype == "bf16" else "exact"
+    t0 = time.perf_counter()
+    for d in directions:
+        oracle.full(z, m, W, d, storage=storage)
+    dt = time.perf_counter() - t0
+    fl = len(directions) * flops_update(w.N, w.c_z, w.c_h)
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
+            "sample": f"whole grid of {name} (N={w.N}, {w.dtype}), {' + '.join(directions)}, full float64 oracle",
+            "seconds": dt, "ms_per_update": 1e3 * dt / len(directions)}
 
 
 def run_reference(args, w):
@@ -340,14 +440,7 @@ def run_ours(args, w):
         if v["launches"]:
             kernels[name] = {"launches": v["launches"], "ms_per_launch": v["ms"] / v["launches"],
                              "share": v["ms"] / tot}
-    # HBM-bound passes: algorithmic bytes per pair (projection: z read + a, b written; finish: x fp32 +
-    # z read + out written)
-    pairs = float(w.N) ** 2
-    kp, kf = ktime["project"], ktime["finish"]
-    if kp["ms"] > 0:
-        kernels["project"]["gbs"] = (kp["units"] * (256 + 512)) / (kp["ms"] / 1e3) / 1e9
-    if kf["ms"] > 0:
-        kernels["finish"]["gbs"] = (kf["units"] * (512 + 256 + 256)) / (kf["ms"] / 1e3) / 1e9
+    add_kernel_bandwidth(kernels, ktime, peaks)
 
     # e2e: the same step through the C ABI on host buffers (pinned), copies inside the timed region
     e2e = None
@@ -531,11 +624,24 @@ def run_ours(args, w):
         amod.close()
         del aout
 
+    # the metric's other workloads, measured in the same run (the step above is the four-chain complex)
+    others = None
+    if not args.no_other_configs and not args.N and w.name == "complex3605":
+        del outs
+        torch.cuda.empty_cache()
+        others = {}
+        for name, k in (("crop768", 50), ("ppi6500", 3), ("n10000", 2)):
+            others[name] = measure_config(tm, torch, name, k, 3, peaks, barrier)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         dt, tf, desc = oracle_sample(z_np, m_np, W, w, args.cpu_rows, args.cpu_rows, 7)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle", "sample": desc,
                "seconds": dt}
+        # the full oracle on the workloads it finishes within minutes: the tiny fp32 case (both
+        # directions) and the training crop (one direction, about half a minute on 16 cores)
+        cpu["full_oracle"] = {"tiny48": oracle_full_timing("tiny48", ("outgoing", "incoming")),
+                              "crop768": oracle_full_timing("crop768", ("outgoing",))}
 
     if rank == 0:
         line = {
@@ -548,7 +654,7 @@ def run_ours(args, w):
             "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches, "clocks": clk, "backward": bwd,
             "triangle_attention": attn, "pair_update": pair, "step_ms": step_stats,
-            "cublas_bmm_reference": cublas,
+            "cublas_bmm_reference": cublas, "other_configs": others,
         }
         print(json.dumps(line), flush=True)
     mod.close()
@@ -569,6 +675,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-backward", action="store_true", help="skip the backward-pass measurement")
     ap.add_argument("--no-attention", action="store_true", help="skip the triangle-attention measurement")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="skip the crop768, ppi6500 and n10000 measurements beside the step")
     ap.add_argument("--cpu-rows", type=int, default=48, help="side of the oracle's sampled grid")
     ap.add_argument("--N", type=int, default=0, help="override the workload's token count (profiling runs)")
     args = ap.parse_args()

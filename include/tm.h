@@ -21,10 +21,12 @@
  * uses the biased variance.
  *
  * Precisions. TM_BF16: z and out are bf16, a and b are stored as bf16
- * channel-major [c_h][N][ld], x is float32; every contraction accumulates in
- * float32 on the tensor cores (tcgen05); c_z = c_h = 128 only. TM_F32: z, out
- * and every intermediate are float32, computed with FP32 FMA on the CUDA
- * cores; any 1 <= c_z, c_h <= 256.
+ * channel-major [c_h][N][ld]; x, on its way from the contraction to the output
+ * LayerNorm, is fp16 scaled by one power of two 2^e by default (tm_x_storage
+ * below) and float32 with TM_X_FP32; every contraction accumulates in float32
+ * on the tensor cores (tcgen05); c_z = c_h = 128 only. TM_F32: z, out and every
+ * intermediate are float32, computed with FP32 FMA on the CUDA cores; any
+ * 1 <= c_z, c_h <= 256.
  *
  * Conventions for every call below.
  *  - Pointers named "device" are device memory of the ctx's GPU; "host" ones
@@ -143,7 +145,11 @@ tm_status tm_pair_update(tm_ctx* ctx, void* z, const float* mask, int N, tm_dtyp
 tm_status tm_forward_host(tm_ctx* ctx, const void* z_host, const float* mask_host, int N,
                           tm_dtype dtype, tm_direction dir, void* out_host, void* stream);
 
-/* The three steps of tm_forward, for callers that keep intermediates.
+/* The three steps of tm_forward, for callers that keep intermediates. The
+ * plain forms (tm_project, tm_contract, tm_finish) run the float32-x variant
+ * (tm_forward_ex with x_storage = TM_X_FP32); the _ex forms also run the
+ * default fp16 x, and tm_project_ex -> tm_contract_ex -> tm_finish_ex over the
+ * whole grid with TM_X_FP16 gives tm_forward's result bit for bit.
  *
  * tm_project: a, b = gated, masked projections of LayerNorm(z).
  *   a, b  device, channel-major [c_h][N][ld] of dtype (bf16 or float32);
@@ -151,6 +157,18 @@ tm_status tm_forward_host(tm_ctx* ctx, const void* z_host, const float* mask_hos
  */
 tm_status tm_project(tm_ctx* ctx, const void* z, const float* mask, int N, tm_dtype dtype,
                      void* a, void* b, int ld, void* stream);
+
+/* tm_project that also writes, per pair, the LayerNorm_in statistics that the
+ * fp16-x finish step reads:
+ *   zstat  device float32 [N][N][2] = (rstd, -rstd * mean) of z_ij over c_z, or
+ *          NULL (not written); 8-byte aligned; TM_BF16 only. */
+tm_status tm_project_ex(tm_ctx* ctx, const void* z, const float* mask, int N, tm_dtype dtype,
+                        void* a, void* b, int ld, float* zstat, void* stream);
+
+/* The exponent e of the fp16 storage of x for a grid of N tokens: every x value
+ * is stored times 2^e (the bound in the tm_x_storage comment). 0 for a NULL ctx
+ * or one without the bf16 path. */
+int tm_x_exponent(const tm_ctx* ctx, int N);
 
 /* tm_contract: the per-channel contraction over one output block.
  *   a, b    device, [c_h][N][ld] of dtype, as written by tm_project;
@@ -164,6 +182,14 @@ tm_status tm_contract(tm_ctx* ctx, const void* a, const void* b, int N, int ld, 
                       tm_direction dir, int i0, int j0, int bi, int bj, float* x, int ldx,
                       void* stream);
 
+/* tm_contract with the storage of x chosen: x_storage TM_X_FP32 as tm_contract;
+ * TM_X_FP16 (TM_BF16 only) writes x as fp16 times 2^tm_x_exponent(ctx, N) into
+ * x [c_h][bi][ldx] with ldx >= bj and a multiple of 8; only columns < bj of
+ * each row are written. */
+tm_status tm_contract_ex(tm_ctx* ctx, const void* a, const void* b, int N, int ld, tm_dtype dtype,
+                         tm_direction dir, int i0, int j0, int bi, int bj, void* x, int ldx,
+                         int x_storage, void* stream);
+
 /* tm_finish: out over one block from its x block and z.
  *   x    device float32 [c_h][bi][ldx] (as tm_contract writes it);
  *   z    device [N][N][c_z] of dtype;
@@ -171,6 +197,13 @@ tm_status tm_contract(tm_ctx* ctx, const void* a, const void* b, int N, int ld, 
  */
 tm_status tm_finish(tm_ctx* ctx, const float* x, int ldx, const void* z, int N, tm_dtype dtype,
                     int i0, int j0, int bi, int bj, void* out, void* stream);
+
+/* tm_finish with the storage of x chosen: x as tm_contract_ex wrote it with the
+ * same x_storage; TM_X_FP16 also needs zstat as tm_project_ex wrote it for the
+ * same z (TM_ERR_INVALID without it). */
+tm_status tm_finish_ex(tm_ctx* ctx, const void* x, int ldx, int x_storage, const float* zstat,
+                       const void* z, int N, tm_dtype dtype, int i0, int j0, int bi, int bj,
+                       void* out, void* stream);
 
 /* Gradients of the layer's parameters: device float32 arrays, each shaped as
  * the tm_weights member of the same name. A NULL member is not written. */
@@ -286,6 +319,13 @@ long long tm_launch_count(const tm_ctx* ctx);
 
 /* Bytes of workspace currently held by the ctx. */
 size_t tm_workspace_bytes(const tm_ctx* ctx);
+
+/* The shape a ctx was created with: *c_z, *c_hidden, and *layer = 0 for a
+ * triangle multiplicative update (tm_create), 1 for triangle attention
+ * (tm_attn_create; c_hidden is then heads * c_head). NULL outputs are skipped.
+ * TM_ERR_INVALID for a NULL ctx. Lets a binding check tensor shapes before it
+ * hands pointers to a call that cannot see the buffers' sizes. */
+tm_status tm_ctx_info(const tm_ctx* ctx, int* c_z, int* c_hidden, int* layer);
 
 /* Watchdog self-test: launches one small kernel whose wait on an mbarrier
  * that nothing arrives at runs out after timeout_ms (1..10000) and records

@@ -16,6 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libtm.so")
+OBJ_DIR = os.path.join(PKG, "_build")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
@@ -42,21 +43,38 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(d) <= t for d in deps)
 
 
-def build(verbose: bool = False, force: bool = False, extra: list[str] | None = None) -> str:
-    """Compile every .cu under csrc/ into one shared library; returns its path."""
-    if not force and up_to_date():
-        return LIB_PATH
-    os.makedirs(LIB_DIR, exist_ok=True)
-    tmp = LIB_PATH + ".tmp"
-    cmd = [nvcc(), *ARCH, *FLAGS, "-shared", "-I", INCLUDE, "-I", CSRC, *(extra or []),
-           "-o", tmp, *sources()]
+def _compile(src: str, obj: str, extra: list[str], verbose: bool) -> None:
+    cmd = [nvcc(), *ARCH, *FLAGS, "-c", "-I", INCLUDE, "-I", CSRC, *extra, "-o", obj + ".tmp", src]
     if verbose:
         print(" ".join(cmd))
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
-        raise RuntimeError(f"nvcc failed ({r.returncode}):\n{r.stdout}\n{r.stderr}")
+        raise RuntimeError(f"nvcc failed on {os.path.basename(src)} ({r.returncode}):\n{r.stdout}\n{r.stderr}")
     if verbose and (r.stdout or r.stderr):
         print(r.stdout, r.stderr)
+    os.replace(obj + ".tmp", obj)
+
+
+def build(verbose: bool = False, force: bool = False, extra: list[str] | None = None) -> str:
+    """Compile every .cu under csrc/ (one nvcc per file, in parallel) and link them into one shared
+    library; returns its path."""
+    if not force and up_to_date():
+        return LIB_PATH
+    from concurrent.futures import ThreadPoolExecutor
+    os.makedirs(OBJ_DIR, exist_ok=True)
+    srcs = sources()
+    objs = [os.path.join(OBJ_DIR, os.path.basename(src)[:-3] + ".o") for src in srcs]
+    with ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 1)) as ex:
+        for f in [ex.submit(_compile, src, obj, list(extra or []), verbose) for src, obj in zip(srcs, objs)]:
+            f.result()
+    os.makedirs(LIB_DIR, exist_ok=True)
+    tmp = LIB_PATH + ".tmp"
+    cmd = [nvcc(), *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", tmp, *objs]
+    if verbose:
+        print(" ".join(cmd))
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc link failed ({r.returncode}):\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB_PATH)
     return LIB_PATH
 

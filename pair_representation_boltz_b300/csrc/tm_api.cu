@@ -566,18 +566,33 @@ void tm_destroy(tm_ctx* c) {
   delete c;
 }
 
-tm_status tm_project(tm_ctx* c, const void* z, const float* mask, int N, tm_dtype dtype, void* a, void* b, int ld,
-                     void* stream) {
+tm_status tm_ctx_info(const tm_ctx* c, int* c_z, int* c_hidden, int* layer) {
+  if (!c) return TM_ERR_INVALID;
+  if (c_z) *c_z = c->c_z;
+  if (c_hidden) *c_hidden = c->c_h;
+  if (layer) *layer = c->layer;
+  return TM_OK;
+}
+
+int tm_x_exponent(const tm_ctx* c, int N) {
+  if (!c || !c->tc || N < 1) return 0;
+  return x16_exponent(c, N);
+}
+
+tm_status tm_project_ex(tm_ctx* c, const void* z, const float* mask, int N, tm_dtype dtype, void* a, void* b, int ld,
+                        float* zstat, void* stream) {
   tm_status st = check_common(c, N, dtype);
   if (st != TM_OK) return st;
   if (!z || !a || !b || !aligned16(z) || !aligned16(a) || !aligned16(b))
     return fail(c, TM_ERR_INVALID, "z, a, b must be non-null and 16-byte aligned");
   if (mask && (reinterpret_cast<uintptr_t>(mask) & 3u)) return fail(c, TM_ERR_INVALID, "mask must be 4-byte aligned");
   if (ld < N || (dtype == TM_BF16 && ld % 8)) return fail(c, TM_ERR_INVALID, "ld=%d must be >= N (and a multiple of 8 for bf16)", ld);
+  if (zstat && dtype != TM_BF16) return fail(c, TM_ERR_INVALID, "zstat is written by the bf16 projection only");
+  if (zstat && (reinterpret_cast<uintptr_t>(zstat) & 7u)) return fail(c, TM_ERR_INVALID, "zstat must be 8-byte aligned");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (dtype == TM_BF16)
-    return run_project_bf16(c, z, mask, N, nullptr, reinterpret_cast<__nv_bfloat16*>(a), reinterpret_cast<__nv_bfloat16*>(b),
-                            ld, s, nullptr);
+    return run_project_bf16(c, z, mask, N, reinterpret_cast<float2*>(zstat), reinterpret_cast<__nv_bfloat16*>(a),
+                            reinterpret_cast<__nv_bfloat16*>(b), ld, s, nullptr);
   cudaError_t e = timed(c, 3, (long long)N * N, s, [&] {
     return launch_project_f32(reinterpret_cast<const float*>(z), mask, c->f32w, reinterpret_cast<float*>(a),
                               reinterpret_cast<float*>(b), N, ld, s);
@@ -585,8 +600,13 @@ tm_status tm_project(tm_ctx* c, const void* z, const float* mask, int N, tm_dtyp
   return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "projection (f32) launch");
 }
 
-tm_status tm_contract(tm_ctx* c, const void* a, const void* b, int N, int ld, tm_dtype dtype, tm_direction dir,
-                      int i0, int j0, int bi, int bj, float* x, int ldx, void* stream) {
+tm_status tm_project(tm_ctx* c, const void* z, const float* mask, int N, tm_dtype dtype, void* a, void* b, int ld,
+                     void* stream) {
+  return tm_project_ex(c, z, mask, N, dtype, a, b, ld, nullptr, stream);
+}
+
+tm_status tm_contract_ex(tm_ctx* c, const void* a, const void* b, int N, int ld, tm_dtype dtype, tm_direction dir,
+                         int i0, int j0, int bi, int bj, void* x, int ldx, int x_storage, void* stream) {
   tm_status st = check_common(c, N, dtype);
   if (st != TM_OK) return st;
   if (dir != TM_OUTGOING && dir != TM_INCOMING) return fail(c, TM_ERR_INVALID, "unknown direction %d", (int)dir);
@@ -595,38 +615,61 @@ tm_status tm_contract(tm_ctx* c, const void* a, const void* b, int N, int ld, tm
   if (ld < N || (dtype == TM_BF16 && ld % 8)) return fail(c, TM_ERR_INVALID, "bad ld=%d", ld);
   if (i0 < 0 || j0 < 0 || bi < 1 || bj < 1 || i0 + bi > N || j0 + bj > N)
     return fail(c, TM_ERR_INVALID, "block (%d,%d)+(%d,%d) outside the %d x %d grid", i0, j0, bi, bj, N, N);
-  if (ldx < bj || ldx % 4) return fail(c, TM_ERR_INVALID, "ldx=%d must be >= bj and a multiple of 4", ldx);
+  if (x_storage != TM_X_FP16 && x_storage != TM_X_FP32) return fail(c, TM_ERR_INVALID, "unknown x_storage %d", x_storage);
+  const bool x16 = x_storage == TM_X_FP16;
+  if (x16 && dtype != TM_BF16) return fail(c, TM_ERR_INVALID, "fp16 x is a storage of the bf16 path only");
+  if (ldx < bj || ldx % (x16 ? 8 : 4))
+    return fail(c, TM_ERR_INVALID, "ldx=%d must be >= bj and a multiple of %d", ldx, x16 ? 8 : 4);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool inc = dir == TM_INCOMING;
   if (dtype == TM_BF16)
     return run_contract_bf16(c, reinterpret_cast<const __nv_bfloat16*>(a), reinterpret_cast<const __nv_bfloat16*>(b),
-                             N, ld, inc, i0, j0, bi, bj, x, ldx, X_F32, 0, s, nullptr);
+                             N, ld, inc, i0, j0, bi, bj, x, ldx, x16 ? X_F16 : X_F32, x16 ? x16_exponent(c, N) : 0, s,
+                             nullptr);
   cudaError_t e = timed(c, 3, (long long)c->c_h * bi * bj, s, [&] {
     return launch_contract_f32(inc, reinterpret_cast<const float*>(a), reinterpret_cast<const float*>(b), N, ld,
-                               c->c_h, i0, j0, bi, bj, x, ldx, (long long)bi * ldx, s);
+                               c->c_h, i0, j0, bi, bj, reinterpret_cast<float*>(x), ldx, (long long)bi * ldx, s);
   });
   return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "contraction (f32) launch");
 }
 
-tm_status tm_finish(tm_ctx* c, const float* x, int ldx, const void* z, int N, tm_dtype dtype, int i0, int j0, int bi,
-                    int bj, void* out, void* stream) {
+tm_status tm_contract(tm_ctx* c, const void* a, const void* b, int N, int ld, tm_dtype dtype, tm_direction dir,
+                      int i0, int j0, int bi, int bj, float* x, int ldx, void* stream) {
+  return tm_contract_ex(c, a, b, N, ld, dtype, dir, i0, j0, bi, bj, x, ldx, TM_X_FP32, stream);
+}
+
+tm_status tm_finish_ex(tm_ctx* c, const void* x, int ldx, int x_storage, const float* zstat, const void* z, int N,
+                       tm_dtype dtype, int i0, int j0, int bi, int bj, void* out, void* stream) {
   tm_status st = check_common(c, N, dtype);
   if (st != TM_OK) return st;
   if (!x || !z || !out || !aligned16(x) || !aligned16(z) || !aligned16(out))
     return fail(c, TM_ERR_INVALID, "x, z, out must be non-null and 16-byte aligned");
   if (i0 < 0 || j0 < 0 || bi < 1 || bj < 1 || i0 + bi > N || j0 + bj > N)
     return fail(c, TM_ERR_INVALID, "block outside the grid");
-  if (ldx < bj || ldx % 4) return fail(c, TM_ERR_INVALID, "ldx=%d must be >= bj and a multiple of 4", ldx);
+  if (x_storage != TM_X_FP16 && x_storage != TM_X_FP32) return fail(c, TM_ERR_INVALID, "unknown x_storage %d", x_storage);
+  const bool x16 = x_storage == TM_X_FP16;
+  if (x16 && dtype != TM_BF16) return fail(c, TM_ERR_INVALID, "fp16 x is a storage of the bf16 path only");
+  if (x16 && (!zstat || (reinterpret_cast<uintptr_t>(zstat) & 7u)))
+    return fail(c, TM_ERR_INVALID, "fp16 x needs the projection's zstat (8-byte aligned)");
+  if (ldx < bj || ldx % (x16 ? 8 : 4))
+    return fail(c, TM_ERR_INVALID, "ldx=%d must be >= bj and a multiple of %d", ldx, x16 ? 8 : 4);
   const size_t zbytes = (size_t)N * N * c->c_z * (dtype == TM_BF16 ? 2 : 4);
   if (ranges_overlap(z, zbytes, out, zbytes)) return fail(c, TM_ERR_INVALID, "out overlaps z");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (dtype == TM_BF16)
-    return run_finish_bf16(c, x, ldx, X_F32, 0, nullptr, z, N, i0, j0, bi, bj, out, false, s, nullptr);
+    return run_finish_bf16(c, x, ldx, x16 ? X_F16 : X_F32, x16 ? x16_exponent(c, N) : 0,
+                           reinterpret_cast<const float2*>(zstat), z, N, i0, j0, bi, bj, out, false, s, nullptr);
   cudaError_t e = timed(c, 3, (long long)bi * bj, s, [&] {
-    return launch_finish_f32(x, ldx, (long long)bi * ldx, reinterpret_cast<const float*>(z), c->f32w, N, i0, j0, bi,
-                             bj, reinterpret_cast<float*>(out), false, s);
+    return launch_finish_f32(reinterpret_cast<const float*>(x), ldx, (long long)bi * ldx,
+                             reinterpret_cast<const float*>(z), c->f32w, N, i0, j0, bi, bj,
+                             reinterpret_cast<float*>(out), false, s);
   });
   return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "finish (f32) launch");
+}
+
+tm_status tm_finish(tm_ctx* c, const float* x, int ldx, const void* z, int N, tm_dtype dtype, int i0, int j0, int bi,
+                    int bj, void* out, void* stream) {
+  return tm_finish_ex(c, x, ldx, TM_X_FP32, nullptr, z, N, dtype, i0, j0, bi, bj, out, stream);
 }
 
 tm_status tm_forward_ex(tm_ctx* c, const void* z, const float* mask, int N, tm_dtype dtype, tm_direction dir,

@@ -8,10 +8,14 @@ GPU every call raises.
 
 The function names mirror the C ABI: tm_create, tm_forward, tm_forward_ex, tm_forward_host,
 tm_forward_noalloc, tm_pair_update, tm_backward, tm_attn_create, tm_attn_forward,
-tm_project, tm_contract, tm_finish, tm_sync_status, tm_watchdog_selftest, tm_set_timing,
-tm_get_timing, tm_launch_count, tm_workspace_bytes, tm_status_string,
-tm_last_error, tm_destroy. ``TriMul`` (the update, with ``backward``) and ``TriangleAttention`` wrap a
-context for convenience.
+tm_project, tm_project_ex, tm_x_exponent, tm_contract, tm_contract_ex, tm_finish, tm_finish_ex,
+tm_sync_status, tm_watchdog_selftest, tm_set_timing, tm_get_timing, tm_launch_count,
+tm_workspace_bytes, tm_ctx_info, tm_status_string, tm_last_error, tm_destroy.
+
+The C calls see raw pointers only, not the sizes of the buffers behind them, so every wrapper
+checks the tensors it is given (shape, dtype, element count) against the ctx's shape
+(tm_ctx_info) before any pointer is handed over. ``TriMul`` (the update, with ``backward``) and
+``TriangleAttention`` wrap a context for convenience.
 """
 from __future__ import annotations
 
@@ -90,8 +94,13 @@ def load_library(path: str = LIB_PATH):
         "tm_pair_update": (st, [vp, vp, vp, i, i, vp, C.POINTER(TmOptions)]),
         "tm_forward_noalloc": (st, [vp, vp, vp, i, i, vp, vp]),
         "tm_project": (st, [vp, vp, vp, i, i, vp, vp, i, vp]),
+        "tm_project_ex": (st, [vp, vp, vp, i, i, vp, vp, i, vp, vp]),
+        "tm_x_exponent": (i, [vp, i]),
         "tm_contract": (st, [vp, vp, vp, i, i, i, i, i, i, i, i, vp, i, vp]),
+        "tm_contract_ex": (st, [vp, vp, vp, i, i, i, i, i, i, i, i, vp, i, i, vp]),
         "tm_finish": (st, [vp, vp, i, vp, i, i, i, i, i, i, vp, vp]),
+        "tm_finish_ex": (st, [vp, vp, i, i, vp, vp, i, i, i, i, i, i, vp, vp]),
+        "tm_ctx_info": (st, [vp, C.POINTER(i), C.POINTER(i), C.POINTER(i)]),
         "tm_backward": (st, [vp, vp, vp, i, i, i, vp, vp, C.POINTER(TmGrads), vp, C.POINTER(TmOptions)]),
         "tm_attn_create": (st, [i, i, i, C.POINTER(TmAttnWeights), C.POINTER(vp)]),
         "tm_attn_forward": (st, [vp, vp, vp, i, i, i, vp, vp, C.POINTER(TmOptions)]),
@@ -165,6 +174,69 @@ def _direction(d):
     return int(d)
 
 
+# ------------------------------------------------------------------ argument checks
+# libtm's calls receive raw pointers and cannot see how large the buffers behind them are, so the
+# wrappers check every tensor against the sizes the call will touch before handing it over.
+
+def _ctx_dims(ctx):
+    """(c_z, c_hidden, layer) of a ctx (tm_ctx_info)."""
+    if not ctx:
+        raise TmError(TM_ERR_INVALID, "no ctx")
+    cz, ch, layer = C.c_int(), C.c_int(), C.c_int()
+    _check(ctx, load_library().tm_ctx_info(ctx, C.byref(cz), C.byref(ch), C.byref(layer)))
+    return cz.value, ch.value, layer.value
+
+
+def check_pair_tensor(name, t, c, N=None):
+    """t must be a [N][N][c] tensor (N = t.shape[0] unless given); returns N."""
+    if t.dim() != 3 or t.shape[0] != t.shape[1] or t.shape[2] != c or (N is not None and t.shape[0] != N):
+        want = f"[{N if N is not None else 'N'}][{N if N is not None else 'N'}][{c}]"
+        raise ValueError(f"{name} must have shape {want}, got {tuple(t.shape)}")
+    return int(t.shape[0])
+
+
+def check_like(name, t, ref, ref_name="z"):
+    """t must have ref's shape and dtype."""
+    if tuple(t.shape) != tuple(ref.shape) or t.dtype != ref.dtype:
+        raise ValueError(f"{name} must match {ref_name} ({tuple(ref.shape)}, {ref.dtype}), "
+                         f"got {tuple(t.shape)}, {t.dtype}")
+
+
+def check_mask(mask, N):
+    """mask: None, or a float32 vector of N token-mask values."""
+    if mask is None:
+        return
+    if mask.dim() != 1 or mask.shape[0] != N or str(mask.dtype) != "torch.float32":
+        raise ValueError(f"mask must be a float32 vector of N={N} values, got {tuple(mask.shape)}, {mask.dtype}")
+
+
+def check_min_numel(name, t, n, dtype=None):
+    """t must hold at least n elements (of dtype, when given)."""
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.numel() < n:
+        raise ValueError(f"{name} holds {t.numel()} elements; the call touches {n}")
+
+
+def grad_shapes(c_z, c_h):
+    """Shape of every parameter (and of its gradient), keyed by the tm_weights member name."""
+    return {"ln_in_gamma": (c_z,), "ln_in_beta": (c_z,), "w_a": (c_h, c_z), "w_ga": (c_h, c_z),
+            "w_b": (c_h, c_z), "w_gb": (c_h, c_z), "w_g": (c_z, c_z), "ln_out_gamma": (c_h,),
+            "ln_out_beta": (c_h,), "w_o": (c_z, c_h)}
+
+
+def check_grads(grads, c_z, c_h):
+    """grads: dict of float32 tensors keyed by parameter name, each in its parameter's shape."""
+    shapes = grad_shapes(c_z, c_h)
+    for n, t in grads.items():
+        if n not in shapes:
+            raise KeyError(f"unknown parameter {n!r}")
+        if str(t.dtype) != "torch.float32":
+            raise TypeError(f"gradient {n} must be float32")
+        if tuple(t.shape) != shapes[n]:
+            raise ValueError(f"gradient {n} must have shape {shapes[n]}, got {tuple(t.shape)}")
+
+
 # ------------------------------------------------------------------ C-ABI mirrors
 
 def tm_status_string(status: int) -> str:
@@ -190,9 +262,17 @@ def tm_destroy(ctx) -> None:
         load_library().tm_destroy(ctx)
 
 
+def _check_forward(ctx, z, mask, out):
+    c_z, _, _ = _ctx_dims(ctx)
+    N = check_pair_tensor("z", z, c_z)
+    check_like("out", out, z)
+    check_mask(mask, N)
+    return N
+
+
 def tm_forward_ex(ctx, z, mask, direction, out, stream=None, block=0, timeout_ms=0, workspace_limit=0,
                   x_storage="fp16", residual=False):
-    N = z.shape[0]
+    N = _check_forward(ctx, z, mask, out)
     opt = TmOptions(block, timeout_ms, workspace_limit, X_STORAGE[x_storage], 1 if residual else 0)
     _check(ctx, load_library().tm_forward_ex(ctx, _ptr(z), _ptr(mask), N, _dtype_code(z), _direction(direction),
                                              _ptr(out), _stream(stream), C.byref(opt)))
@@ -201,7 +281,7 @@ def tm_forward_ex(ctx, z, mask, direction, out, stream=None, block=0, timeout_ms
 
 def tm_pair_update(ctx, z, mask=None, stream=None, block=0, timeout_ms=0, workspace_limit=0, x_storage="fp16"):
     """z <- z + outgoing(z); z <- z + incoming(z), in place (z: contiguous CUDA tensor [N][N][c_z])."""
-    N = z.shape[0]
+    N = _check_forward(ctx, z, mask, z)
     opt = TmOptions(block, timeout_ms, workspace_limit, X_STORAGE[x_storage], 1)
     _check(ctx, load_library().tm_pair_update(ctx, _ptr(z), _ptr(mask), N, _dtype_code(z), _stream(stream),
                                               C.byref(opt)))
@@ -209,7 +289,7 @@ def tm_pair_update(ctx, z, mask=None, stream=None, block=0, timeout_ms=0, worksp
 
 
 def tm_forward(ctx, z, mask, direction, out, stream=None):
-    N = z.shape[0]
+    N = _check_forward(ctx, z, mask, out)
     _check(ctx, load_library().tm_forward(ctx, _ptr(z), _ptr(mask), N, _dtype_code(z), _direction(direction),
                                           _ptr(out), _stream(stream)))
     return out
@@ -223,7 +303,7 @@ def tm_forward_host(ctx, z, mask, direction, out, stream=None):
         if t.is_cuda or not t.is_contiguous():
             raise ValueError("tm_forward_host takes contiguous host tensors")
     code = TM_BF16 if z.dtype == torch.bfloat16 else TM_F32
-    N = z.shape[0]
+    N = _check_forward(ctx, z, mask, out)
     _check(ctx, load_library().tm_forward_host(ctx, C.c_void_p(z.data_ptr()),
                                                C.c_void_p(mask.data_ptr()) if mask is not None else None, N, code,
                                                _direction(direction), C.c_void_p(out.data_ptr()), _stream(stream)))
@@ -233,29 +313,96 @@ def tm_forward_host(ctx, z, mask, direction, out, stream=None):
 def tm_forward_noalloc(ctx, z, mask, direction, out, stream=None):
     """tm_forward for bf16 z with N <= 128 whose scratch is a static array inside libtm: the call
     allocates no device memory (for callers that may not allocate; see include/tm.h)."""
-    N = z.shape[0]
     if _dtype_code(z) != TM_BF16:
         raise TypeError("tm_forward_noalloc takes bf16 z")
+    N = _check_forward(ctx, z, mask, out)
     _check(ctx, load_library().tm_forward_noalloc(ctx, _ptr(z), _ptr(mask), N, _direction(direction), _ptr(out),
                                                   _stream(stream)))
     return out
 
 
+def _check_project(ctx, z, mask, a, b, ld):
+    c_z, c_h, _ = _ctx_dims(ctx)
+    N = check_pair_tensor("z", z, c_z)
+    check_mask(mask, N)
+    for name, t in (("a", a), ("b", b)):
+        check_min_numel(name, t, c_h * N * ld, z.dtype)
+    return N
+
+
 def tm_project(ctx, z, mask, a, b, ld, stream=None):
-    N = z.shape[0]
+    N = _check_project(ctx, z, mask, a, b, ld)
     _check(ctx, load_library().tm_project(ctx, _ptr(z), _ptr(mask), N, _dtype_code(z), _ptr(a), _ptr(b), ld,
                                           _stream(stream)))
 
 
+def tm_project_ex(ctx, z, mask, a, b, ld, zstat=None, stream=None):
+    """tm_project that also writes the per-pair LayerNorm_in statistics zstat (float32 [N][N][2]) that
+    the fp16-x finish step reads."""
+    N = _check_project(ctx, z, mask, a, b, ld)
+    if zstat is not None:
+        import torch
+        check_min_numel("zstat", zstat, 2 * N * N, torch.float32)
+    _check(ctx, load_library().tm_project_ex(ctx, _ptr(z), _ptr(mask), N, _dtype_code(z), _ptr(a), _ptr(b), ld,
+                                             _ptr(zstat), _stream(stream)))
+
+
+def tm_x_exponent(ctx, N: int) -> int:
+    """e of the fp16 storage of x (every value stored times 2^e) for a grid of N tokens."""
+    return load_library().tm_x_exponent(ctx, N)
+
+
+def _check_contract(ctx, a, b, N, ld, bi, ldx, x, x_dtype):
+    _, c_h, _ = _ctx_dims(ctx)
+    for name, t in (("a", a), ("b", b)):
+        check_min_numel(name, t, c_h * N * ld, a.dtype)
+    check_min_numel("x", x, c_h * bi * ldx, x_dtype)
+
+
 def tm_contract(ctx, a, b, N, ld, direction, i0, j0, bi, bj, x, ldx, stream=None):
+    import torch
+    _check_contract(ctx, a, b, N, ld, bi, ldx, x, torch.float32)
     _check(ctx, load_library().tm_contract(ctx, _ptr(a), _ptr(b), N, ld, _dtype_code(a), _direction(direction),
                                            i0, j0, bi, bj, _ptr(x), ldx, _stream(stream)))
 
 
+def tm_contract_ex(ctx, a, b, N, ld, direction, i0, j0, bi, bj, x, ldx, x_storage="fp16", stream=None):
+    """tm_contract with x stored as fp16 times 2^tm_x_exponent(N) ("fp16", x: torch.float16) or float32."""
+    import torch
+    _check_contract(ctx, a, b, N, ld, bi, ldx, x, torch.float16 if x_storage == "fp16" else torch.float32)
+    _check(ctx, load_library().tm_contract_ex(ctx, _ptr(a), _ptr(b), N, ld, _dtype_code(a), _direction(direction),
+                                              i0, j0, bi, bj, _ptr(x), ldx, X_STORAGE[x_storage], _stream(stream)))
+
+
+def _check_finish(ctx, x, ldx, z, bi, out, x_dtype):
+    c_z, c_h, _ = _ctx_dims(ctx)
+    N = check_pair_tensor("z", z, c_z)
+    check_like("out", out, z)
+    check_min_numel("x", x, c_h * bi * ldx, x_dtype)
+    return N
+
+
 def tm_finish(ctx, x, ldx, z, i0, j0, bi, bj, out, stream=None):
-    N = z.shape[0]
+    import torch
+    N = _check_finish(ctx, x, ldx, z, bi, out, torch.float32)
     _check(ctx, load_library().tm_finish(ctx, _ptr(x), ldx, _ptr(z), N, _dtype_code(z), i0, j0, bi, bj, _ptr(out),
                                          _stream(stream)))
+
+
+def tm_finish_ex(ctx, x, ldx, z, i0, j0, bi, bj, out, x_storage="fp16", zstat=None, stream=None):
+    """tm_finish of an x block stored as tm_contract_ex wrote it; fp16 x needs tm_project_ex's zstat."""
+    import torch
+    N = _check_finish(ctx, x, ldx, z, bi, out, torch.float16 if x_storage == "fp16" else torch.float32)
+    if zstat is not None:
+        check_min_numel("zstat", zstat, 2 * N * N, torch.float32)
+    _check(ctx, load_library().tm_finish_ex(ctx, _ptr(x), ldx, X_STORAGE[x_storage], _ptr(zstat), _ptr(z), N,
+                                            _dtype_code(z), i0, j0, bi, bj, _ptr(out), _stream(stream)))
+
+
+def tm_ctx_info(ctx) -> dict:
+    """{"c_z", "c_hidden", "layer"} of a ctx (layer 0: update, 1: triangle attention)."""
+    c_z, c_h, layer = _ctx_dims(ctx)
+    return {"c_z": c_z, "c_hidden": c_h, "layer": layer}
 
 
 def tm_backward(ctx, z, mask, direction, dout, dz, grads=None, stream=None, timeout_ms=0, workspace_limit=0):
@@ -263,14 +410,15 @@ def tm_backward(ctx, z, mask, direction, dout, dz, grads=None, stream=None, time
 
     grads: dict of contiguous float32 CUDA tensors keyed by parameter name (a missing key is not
     written), or None. dz may be dout itself."""
-    N = z.shape[0]
     g = None
+    c_z, c_h, _ = _ctx_dims(ctx)
     if grads is not None:
-        for n, t in grads.items():
-            if n not in WEIGHT_FIELDS:
-                raise KeyError(f"unknown parameter {n!r}")
-            if str(t.dtype) != "torch.float32":
-                raise TypeError(f"gradient {n} must be float32")
+        check_grads(grads, c_z, c_h)
+    N = check_pair_tensor("z", z, c_z)
+    check_like("dout", dout, z)
+    check_like("dz", dz, z)
+    check_mask(mask, N)
+    if grads is not None:
         g = TmGrads(*[_ptr(grads[n]) if n in grads else None for n in WEIGHT_FIELDS])
     opt = TmOptions(0, timeout_ms, workspace_limit, 0, 0)
     _check(ctx, load_library().tm_backward(ctx, _ptr(z), _ptr(mask), N, _dtype_code(z), _direction(direction),
@@ -291,7 +439,7 @@ def tm_attn_create(c_z: int, heads: int, c_head: int, weights: dict):
 
 def tm_attn_forward(ctx, z, mask, node, out, stream=None, timeout_ms=0, workspace_limit=0):
     """out = triangle attention ("starting" or "ending" node) of bf16 z [N][N][128]."""
-    N = z.shape[0]
+    N = _check_forward(ctx, z, mask, out)
     opt = TmOptions(0, timeout_ms, workspace_limit, 0, 0)
     _check(ctx, load_library().tm_attn_forward(ctx, _ptr(z), _ptr(mask), N, _dtype_code(z),
                                                ATTN_NODES[node] if isinstance(node, str) else int(node),
@@ -374,11 +522,7 @@ class TriMul:
         import torch
         if dz is None:
             dz = torch.empty_like(z)
-        shapes = {"ln_in_gamma": (self.c_z,), "ln_in_beta": (self.c_z,), "w_a": (self.c_hidden, self.c_z),
-                  "w_ga": (self.c_hidden, self.c_z), "w_b": (self.c_hidden, self.c_z),
-                  "w_gb": (self.c_hidden, self.c_z), "w_g": (self.c_z, self.c_z),
-                  "ln_out_gamma": (self.c_hidden,), "ln_out_beta": (self.c_hidden,),
-                  "w_o": (self.c_z, self.c_hidden)}
+        shapes = grad_shapes(self.c_z, self.c_hidden)
         grads = {n: torch.empty(shp, dtype=torch.float32, device=z.device) for n, shp in shapes.items()}
         tm_backward(self.ctx, z, mask, direction, dout, dz, grads, stream, **opts)
         return dz, grads

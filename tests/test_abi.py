@@ -17,7 +17,8 @@ def libtm():
 def test_header_declares_the_boundary():
     names = tm.header_functions()
     for required in ("tm_create", "tm_forward", "tm_forward_ex", "tm_destroy", "tm_sync_status",
-                     "tm_status_string", "tm_project", "tm_contract", "tm_finish"):
+                     "tm_status_string", "tm_project", "tm_contract", "tm_finish", "tm_project_ex",
+                     "tm_contract_ex", "tm_finish_ex", "tm_x_exponent", "tm_ctx_info"):
         assert required in names
 
 
@@ -49,6 +50,8 @@ def test_create_rejects_bad_arguments_before_touching_cuda(libtm):
     assert not ctx.value
     libtm.tm_destroy(None)                  # no-op
     assert libtm.tm_launch_count(None) == 0
+    assert libtm.tm_ctx_info(None, None, None, None) == tm.TM_ERR_INVALID
+    assert libtm.tm_x_exponent(None, 100) == 0
 
 
 def test_options_struct_layout():
@@ -65,13 +68,3 @@ def test_library_is_built_for_sm_103a(libtm):
     # the build command pins the architecture; check the flag list rather than the binary
     assert "arch=compute_103a,code=sm_103a" in " ".join(build.ARCH)
     assert os.path.getsize(tm.LIB_PATH) > 0
-
-
-def test_backward_binding_checks_the_gradient_dict_first():
-    """A misnamed or non-float32 gradient is reported by name, before any tensor is handed to libtm."""
-    import torch
-    z = torch.zeros(4, 4, 16)
-    with pytest.raises(KeyError, match="w_typo"):
-        tm.tm_backward(None, z, None, "outgoing", z, z, {"w_typo": torch.zeros(16, 16)})
-    with pytest.raises(TypeError, match="w_g"):
-        tm.tm_backward(None, z, None, "outgoing", z, z, {"w_g": torch.zeros(16, 16, dtype=torch.float64)})

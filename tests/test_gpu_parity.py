@@ -160,6 +160,42 @@ def test_finish_bf16(tm128, torch_cuda, N):
     assert e["excess"] <= BF16_TOL / 2, e
 
 
+@pytest.mark.parametrize("direction", DIRS)
+@pytest.mark.parametrize("N,mask,ld_pad", [(77, "scatter", 8), (300, "last10pct", 64)])
+def test_three_steps_reproduce_forward_bit_for_bit(tm128, torch_cuda, direction, N, mask, ld_pad):
+    """tm_project_ex -> tm_contract_ex -> tm_finish_ex with the default fp16 x, over the whole grid, is
+    tm_forward: the same kernels on the same values, so the outputs agree bit for bit whatever the
+    row padding of the caller's buffers."""
+    from pair_representation_boltz_b300 import tm
+    torch = torch_cuda
+    mod, W = tm128
+    z = z_to_device(wl.make_z(N, 128, 61 + N, "bf16"))
+    m = mask_to_device(wl.make_mask(N, mask, 62))
+    ref = mod(z, m, direction)
+    ld = (N + ld_pad - 1) // ld_pad * ld_pad
+    a = torch.empty((128, N, ld), dtype=torch.bfloat16, device="cuda")
+    b = torch.empty_like(a)
+    zstat = torch.empty((N, N, 2), dtype=torch.float32, device="cuda")
+    tm.tm_project_ex(mod.ctx, z, m, a, b, ld, zstat)
+    ldx = (N + 7) // 8 * 8
+    x = torch.empty((128, N, ldx), dtype=torch.float16, device="cuda")
+    tm.tm_contract_ex(mod.ctx, a, b, N, ld, direction, 0, 0, N, N, x, ldx, "fp16")
+    out = torch.full_like(z, float("nan"))
+    tm.tm_finish_ex(mod.ctx, x, ldx, z, 0, 0, N, N, out, "fp16", zstat)
+    torch.cuda.synchronize()
+    assert tm.tm_sync_status(mod.ctx) == tm.TM_OK
+    assert torch.equal(out, ref)
+    # the stored x is the float32 contraction times 2^e, rounded once to fp16
+    e = tm.tm_x_exponent(mod.ctx, N)
+    x32 = torch.empty((128, N, ldx), dtype=torch.float32, device="cuda")
+    tm.tm_contract_ex(mod.ctx, a, b, N, ld, direction, 0, 0, N, N, x32, ldx, "fp32")
+    torch.cuda.synchronize()
+    assert torch.equal(x[:, :, :N], (x32[:, :, :N] * 2.0 ** e).to(torch.float16))
+    # fp16 x without the projection's statistics is refused before any launch
+    with pytest.raises(tm.TmError):
+        tm.tm_finish_ex(mod.ctx, x, ldx, z, 0, 0, N, N, out, "fp16", None)
+
+
 # --------------------------------------------------------------------------- whole update, bf16
 
 @pytest.mark.parametrize("direction", DIRS)
