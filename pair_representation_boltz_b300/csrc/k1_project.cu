@@ -67,6 +67,10 @@ static_assert(2 * kBoxProjW.bytes() == W_MAT, "weight matrix = two boxes");
 static_assert(kBoxProjOut.d0 * 2 == 128 && kBoxProjOut.d2 == 32, "a staging box is 32 channel rows of 128 bytes");
 static_assert(OUT_BYTES == 32768, "staging budget");
 
+// F16OUT: a and b leave as fp16, each value rounded to bf16 first (the storage the update defines)
+// and multiplied by the power of two p.out_scale[half], an exact step that the fp16 form of a
+// normal-range bf16 value keeps exactly: the backward pass's contractions take fp16 operands.
+template <bool F16OUT>
 __global__ void __launch_bounds__(THREADS, 1)
     k1_project(const __grid_constant__ CUtensorMap zmap, const __grid_constant__ CUtensorMap wmap,
                const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap,
@@ -262,6 +266,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const float2 rsp = make_float2(cst[c], cst[c]), rsg = make_float2(cst[kC + c], cst[kC + c]);
       const float2 bp = make_float2(cst[256 + c], cst[256 + c]), bg = make_float2(cst[256 + kC + c], cst[256 + kC + c]);
       const float2 one2 = make_float2(1.f, 1.f);
+      const float osc = p.out_scale[half];
       if (lane == 0) tma_prefetch_desc(omap);
       int local = 0;
       for (long long u = cta; u < p.total_tiles; u += nctas, ++local) {
@@ -309,18 +314,24 @@ __global__ void __launch_bounds__(THREADS, 1)
               asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rd) : "f"(den.x * den.y));
               return __fmul2_rn(__fmul2_rn(make_float2(den.y, den.x), pre), make_float2(rd, rd));
             };
+            // bf16 a, b (or their fp16 form, scaled by a power of two, for the backward pass)
+            auto pack = [&](float x, float y) -> uint32_t {
+              if (!F16OUT) return pack_bf16x2(x, y);
+              const float2 r = __bfloat1622float2(__floats2bfloat162_rn(x, y));
+              return pack_f16x2(r.x * osc, r.y * osc);
+            };
             if ((mword & 0xFFFFu) == 0xFFFFu) {
               // all 16 pairs unmasked and inside the grid (warp-uniform): no per-element mask
 #pragma unroll
               for (int e = 0; e < 16; e += 2) {
                 const float2 v = pair_values(e);
-                packed[e >> 1] = pack_bf16x2(v.x, v.y);
+                packed[e >> 1] = pack(v.x, v.y);
               }
             } else {
 #pragma unroll
               for (int e = 0; e < 16; e += 2) {
                 const float2 v = pair_values(e);
-                packed[e >> 1] = pack_bf16x2(((mword >> e) & 1u) ? v.x : 0.f, ((mword >> (e + 1)) & 1u) ? v.y : 0.f);
+                packed[e >> 1] = pack(((mword >> e) & 1u) ? v.x : 0.f, ((mword >> (e + 1)) & 1u) ? v.y : 0.f);
               }
             }
             // 32 bytes of this channel's 128-byte staging row: 16-byte units 2hh, 2hh+1
@@ -366,14 +377,20 @@ cudaError_t launch_project_bf16(const CUtensorMap& zmap, const CUtensorMap& wmap
                                 const CUtensorMap& bmap, const ProjectParams& p, int num_sms, cudaStream_t s) {
   static bool attr_set[kMaxDevices] = {};
   cudaError_t e = once_per_device(attr_set, [] {
-    return cudaFuncSetAttribute(k1_project, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t r = cudaFuncSetAttribute(k1_project<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(k1_project<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    return r;
   });
   if (e != cudaSuccess) return e;
   if (p.total_tiles <= 0) return cudaSuccess;
   long long pairs = num_sms / 2;
   if (pairs > p.total_tiles) pairs = p.total_tiles;
   if (pairs < 1) pairs = 1;
-  k1_project<<<(int)(2 * pairs), THREADS, SMEM_BYTES, s>>>(zmap, wmap, amap, bmap, p);
+  if (p.out_f16)
+    k1_project<true><<<(int)(2 * pairs), THREADS, SMEM_BYTES, s>>>(zmap, wmap, amap, bmap, p);
+  else
+    k1_project<false><<<(int)(2 * pairs), THREADS, SMEM_BYTES, s>>>(zmap, wmap, amap, bmap, p);
   return cudaGetLastError();
 }
 

@@ -164,8 +164,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer (first CTA)
       if (lane == 0 && rank == 0) {
-        constexpr uint32_t idesc_full = make_idesc(BM, BN, FMT_BF16, INCOMING, INCOMING);
-        const uint32_t idesc_last = make_idesc(BM, p.last_n, FMT_BF16, INCOMING, INCOMING);
+        // bf16 operands (the update's a and b) or fp16 ones (the backward pass's)
+        const uint32_t fmt = p.ab_f16 ? FMT_F16 : FMT_BF16;
+        const uint32_t idesc_full = make_idesc(BM, BN, fmt, INCOMING, INCOMING);
+        const uint32_t idesc_last = make_idesc(BM, p.last_n, fmt, INCOMING, INCOMING);
         int s = 0;
         uint32_t ph = 0;
         int local = 0;

@@ -9,16 +9,25 @@
 //   out_ij = W_o [o_ij^1 .. o_ij^H]
 // and the ending node is the same on the transposed grid (z_ji in, out_ji written).
 //
+// Every intermediate (zh, q, k, v, g, the bias, the softmax weights P and the gated output o) is
+// stored as fp16, whose 11 significant bits keep the path's error well inside the bf16 tolerance of
+// the result (bf16 intermediates, 8 bits, cost several times more). zh and v (and with it o) are
+// stored times powers of two that the host derives from bounds the weights fix, so that their
+// largest possible values sit near 2^14 and small ones stay normal; q, k and the bias enter the
+// logits, whose precision is absolute, and are stored as they are (the host refuses weights that
+// could push them past 2^15).
+//
 // Three kernels.
 //   k_ta_project: per tile of 128 pairs (512 threads, four per pair), LayerNorm statistics from the
-//     pair's four channel quarters, zh into a 128 x 128 bf16 tile, one MMA each for q, k, v, g
-//     (TMEM columns 0..511), b on the CUDA cores. q, k and g are stored pair-major like z; v is stored
-//     per (row, head, channel) with the key index innermost, so that it is the K-major operand of the
-//     P V product; b per (head, j) with k innermost.
+//     pair's four channel quarters, zh into a 128 x 128 fp16 tile, one MMA each for q, k, v, g
+//     (TMEM columns 0..511; weights as fp16 images scaled by a power of two each), b on the CUDA
+//     cores. q, k and g are stored pair-major like z; v is stored per (row, head, channel) with the
+//     key index innermost, so that it is the K-major operand of the P V product; b per (head, j) with
+//     k innermost.
 //   k_ta_attend: per (row i, block of 128 queries j), heads one after another, keys in blocks of 128:
 //     S = Q K^T (tcgen05, TMEM; q stored times log2(e)/sqrt(c), the bias times log2(e), so the softmax
 //     runs in base 2), + bias tile (-inf at masked keys), online softmax in registers (two threads per
-//     query row, 64 keys each), P (bf16) into shared memory, O_blk = P V (tcgen05, with a row of ones
+//     query row, 64 keys each), P (fp16) into shared memory, O_blk = P V (tcgen05, with a row of ones
 //     appended to v so that the product also gives the row sum of P, the softmax denominator) added
 //     into the row's running output, the gate at the end of each head. Loads and products are pipelined one
 //     block ahead: the next block's K and bias are fetched once this block's S and bias are in
@@ -117,7 +126,7 @@ __global__ void __launch_bounds__(NT, 1) k_ta_project(const TaProjectParams p) {
       for (int hh = 0; hh < kHeads; ++hh) bp[hh] = fmaf(sm.wb[hh * kC + c0 + e], f[e], bp[hh]);
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) put8(sm.zh, r, c0 + 8 * u, f + 8 * u);
+    for (int u = 0; u < 4; ++u) put8h(sm.zh, r, c0 + 8 * u, f + 8 * u);
 #pragma unroll
     for (int hh = 0; hh < kHeads; ++hh) sm.bpart[h][hh][r] = bp[hh];
     fence_proxy_async_smem();
@@ -125,10 +134,10 @@ __global__ void __launch_bounds__(NT, 1) k_ta_project(const TaProjectParams p) {
     __syncthreads();
     if (tid == 0) {
       tc_fence_after();
-      mma_tile(tmem, a_zh, false, smem_u32(sm.wq), false, ID_KK, false);
-      mma_tile(tmem + kC, a_zh, false, smem_u32(sm.wk), false, ID_KK, false);
-      mma_tile(tmem + 2 * kC, a_zh, false, smem_u32(sm.wv), false, ID_KK, false);
-      mma_tile(tmem + 3 * kC, a_zh, false, smem_u32(sm.wg), false, ID_KK, false);
+      mma_tile(tmem, a_zh, false, smem_u32(sm.wq), false, ID_KK_H, false);
+      mma_tile(tmem + kC, a_zh, false, smem_u32(sm.wk), false, ID_KK_H, false);
+      mma_tile(tmem + 2 * kC, a_zh, false, smem_u32(sm.wv), false, ID_KK_H, false);
+      mma_tile(tmem + 3 * kC, a_zh, false, smem_u32(sm.wg), false, ID_KK_H, false);
       mma_commit(&sm.bar);
     }
     // b of head h for this pair: the four quarters' partial sums
@@ -136,7 +145,7 @@ __global__ void __launch_bounds__(NT, 1) k_ta_project(const TaProjectParams p) {
       // the bias of query i and key j; a masked key j gets -inf, which removes it from every softmax
       const float bsum = ((sm.bpart[0][h][r] + sm.bpart[1][h][r]) + sm.bpart[2][h][r]) + sm.bpart[3][h][r];
       const bool kmasked = p.mask && p.mask[j] == 0.f;
-      p.b[((long long)h * p.N + i) * p.ldb + j] = __float2bfloat16_rn(kmasked ? -INFINITY : bsum * kLog2e);
+      p.b[((long long)h * p.N + i) * p.ldb + j] = __float2half_rn(kmasked ? -INFINITY : bsum * p.bscale);
     }
     if (!cta_wait(&sm.bar, phase, p.w, &sm.abort_flag, 1)) break;
     phase ^= 1u;
@@ -150,23 +159,23 @@ __global__ void __launch_bounds__(NT, 1) k_ta_project(const TaProjectParams p) {
       tmem_ld_wait();
       if (!valid) continue;
       float o[32];
+      // undoes the weight image's power-of-two scale; q's also carries log2(e)/sqrt(c), so that q . k is
+      // the logit in the base-2 exponent of the softmax
+      const float sc = p.wscale[m];
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
-        const float x = __uint_as_float(rr[e]);
-        // q carries log2(e)/sqrt(c), so that q . k is the logit in the base-2 exponent of the softmax
-        o[e] = m == 3 ? sigmoid_mufu(x) : m == 0 ? x * kQScale : x;
+        const float x = __uint_as_float(rr[e]) * sc;
+        o[e] = m == 3 ? sigmoid_mufu(x) : x;
       }
       if (m == 2) {
-        __nv_bfloat16* vp = p.vt + ((long long)i * kC + c0) * p.ldv + j;
+        __half* vp = p.vt + ((long long)i * kC + c0) * p.ldv + j;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) vp[(long long)e * p.ldv] = __float2bfloat16_rn(o[e]);
+        for (int e = 0; e < 32; ++e) vp[(long long)e * p.ldv] = __float2half_rn(o[e]);
       } else {
-        __nv_bfloat16* dst = (m == 0 ? p.q : m == 1 ? p.k : p.g) + pr * kC + c0;
+        __half* dst = (m == 0 ? p.q : m == 1 ? p.k : p.g) + pr * kC + c0;
         uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          d4[u] = make_uint4(pack_bf16x2(o[8 * u], o[8 * u + 1]), pack_bf16x2(o[8 * u + 2], o[8 * u + 3]),
-                             pack_bf16x2(o[8 * u + 4], o[8 * u + 5]), pack_bf16x2(o[8 * u + 6], o[8 * u + 7]));
+        for (int u = 0; u < 4; ++u) d4[u] = pack8h(o + 8 * u);
       }
     }
   }
@@ -194,7 +203,7 @@ struct alignas(1024) TaAttSmem {
   uint8_t q[kQBytes];
   uint8_t k[kKBytes];
   uint8_t b[2][kBBytes];                        // keys 0..63 and 64..127 of the block
-  uint8_t p[TILE];                              // P: 128 queries x 128 keys, bf16, K-major
+  uint8_t p[TILE];                              // P: 128 queries x 128 keys, fp16, K-major
   uint8_t v[2][kVSlot];                         // keys 0..63 and 64..127, rows = channels (+ ones row)
   float xmax[2][BT];                            // per key half and query: block maximum
   uint64_t kb_bar, v_bar, s_bar, pv_bar;
@@ -224,7 +233,7 @@ __global__ void __launch_bounds__(kAttThreads, 2) k_ta_attend(const __grid_const
   const int jb = (int)(blockIdx.x - (long long)i * p.jblocks);
   const int j = jb * BT + row;
   const bool jvalid = j < p.N;
-  __nv_bfloat16* orow = p.o + ((long long)i * p.N + j) * kC;
+  __half* orow = p.o + ((long long)i * p.N + j) * kC;
   if (p.mask && p.mask[i] == 0.f) {
     // no valid key in this row: o = 0
     if (jvalid) {
@@ -252,8 +261,8 @@ __global__ void __launch_bounds__(kAttThreads, 2) k_ta_attend(const __grid_const
     tma_load_3d(sm.v[0], &vmap, &sm.v_bar, kb * BT, kHd * h, i);
     tma_load_3d(sm.v[1], &vmap, &sm.v_bar, kb * BT + 64, kHd * h, i);
   };
-  constexpr uint32_t ID_S = make_idesc(128, 128, FMT_BF16, false, false);
-  constexpr uint32_t ID_O = make_idesc(128, kPvN, FMT_BF16, false, false);
+  constexpr uint32_t ID_S = make_idesc(128, 128, FMT_F16, false, false);
+  constexpr uint32_t ID_O = make_idesc(128, kPvN, FMT_F16, false, false);
   auto issue_s = [&](uint32_t tmem, int t) {     // S = Q_h K_h^T (q is stored pre-scaled by log2(e)/sqrt(c))
     const int hh = (t / kblocks) & 1;
     const uint32_t q0 = smem_u32(sm.q) + 64 * hh, k0 = smem_u32(sm.k) + 64 * hh;
@@ -286,7 +295,7 @@ __global__ void __launch_bounds__(kAttThreads, 2) k_ta_attend(const __grid_const
   // is then the row sum of the bf16 P, the softmax denominator) and zeros
   for (int x = tid; x < 2 * (kVSlot - kVBytes) / 4; x += kAttThreads) {
     const int half = x / ((kVSlot - kVBytes) / 4), w4 = x % ((kVSlot - kVBytes) / 4);
-    reinterpret_cast<uint32_t*>(sm.v[half] + kVBytes)[w4] = w4 < 32 ? 0x3F803F80u : 0u;
+    reinterpret_cast<uint32_t*>(sm.v[half] + kVBytes)[w4] = w4 < 32 ? 0x3C003C00u : 0u;   // fp16 1.0 pairs
   }
   fence_proxy_async_smem();
   tc_fence_before();
@@ -333,7 +342,7 @@ __global__ void __launch_bounds__(kAttThreads, 2) k_ta_attend(const __grid_const
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         float bv[8];
-        bf16x8_to_float(*reinterpret_cast<const uint4*>(brow + sw128_offset((uint32_t)row, (uint32_t)u)), bv);
+        f16x8_to_float(*reinterpret_cast<const uint4*>(brow + sw128_offset((uint32_t)row, (uint32_t)u)), bv);
 #pragma unroll
         for (int e = 0; e < 8; ++e) sv[8 * u + e] = __uint_as_float(u < 4 ? r0[8 * u + e] : r1[8 * (u - 4) + e]) + bv[e];
       }
@@ -360,7 +369,7 @@ __global__ void __launch_bounds__(kAttThreads, 2) k_ta_attend(const __grid_const
       float pv[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) pv[e] = ex2_approx(sv[8 * u + e] - mref);
-      put8(sm.p, row, 64 * kh + 8 * u, pv);
+      put8h(sm.p, row, 64 * kh + 8 * u, pv);
     }
     m_run = m_new;
     fence_proxy_async_smem();
@@ -409,8 +418,8 @@ __global__ void __launch_bounds__(kAttThreads, 2) k_ta_attend(const __grid_const
         {
           const uint4* gq = reinterpret_cast<const uint4*>(p.g + ((long long)i * p.N + j) * kC + cb);
           const uint4 g0 = gq[0], g1 = gq[1];
-          bf16x8_to_float(g0, gv);
-          bf16x8_to_float(g1, gv + 8);
+          f16x8_to_float(g0, gv);
+          f16x8_to_float(g1, gv + 8);
         }
         const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
         float o[16];
@@ -418,9 +427,7 @@ __global__ void __launch_bounds__(kAttThreads, 2) k_ta_attend(const __grid_const
         for (int e = 0; e < 16; ++e) o[e] = gv[e] * acc[e] * inv;
         uint4* d4 = reinterpret_cast<uint4*>(orow + cb);
 #pragma unroll
-        for (int u = 0; u < 2; ++u)
-          d4[u] = make_uint4(pack_bf16x2(o[8 * u], o[8 * u + 1]), pack_bf16x2(o[8 * u + 2], o[8 * u + 3]),
-                             pack_bf16x2(o[8 * u + 4], o[8 * u + 5]), pack_bf16x2(o[8 * u + 6], o[8 * u + 7]));
+        for (int u = 0; u < 2; ++u) d4[u] = pack8h(o + 8 * u);
       }
     }
   }
@@ -434,8 +441,8 @@ __global__ void __launch_bounds__(kAttThreads, 2) k_ta_attend(const __grid_const
   if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
-// out = W_o o per pair (512 threads, tiles of 128 pairs); for the ending node the pair (i, j) of the
-// transposed grid is written at (j, i).
+// out = W_o o per pair (512 threads, tiles of 128 pairs; o and the W_o image fp16); for the ending
+// node the pair (i, j) of the transposed grid is written at (j, i).
 struct alignas(1024) TaOutSmem {
   uint8_t o[TILE], wo[TILE];
   uint64_t bar;
@@ -473,18 +480,18 @@ __global__ void __launch_bounds__(NT, 1) k_ta_out(const TaOutParams p) {
     const int i = valid ? (int)(pr / p.N) : 0;
     const int j = valid ? (int)(pr - (long long)i * p.N) : 0;
     float f[32];
-    if (valid) load32_bf16(p.o + pr * kC + c0, f);
+    if (valid) load32_f16(p.o + pr * kC + c0, f);
     else
 #pragma unroll
       for (int e = 0; e < 32; ++e) f[e] = 0.f;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) put8(sm.o, r, c0 + 8 * u, f + 8 * u);
+    for (int u = 0; u < 4; ++u) put8h(sm.o, r, c0 + 8 * u, f + 8 * u);
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     if (tid == 0) {
       tc_fence_after();
-      mma_tile(tmem, smem_u32(sm.o), false, smem_u32(sm.wo), false, ID_KK, false);
+      mma_tile(tmem, smem_u32(sm.o), false, smem_u32(sm.wo), false, ID_KK_H, false);
       mma_commit(&sm.bar);
     }
     if (!cta_wait(&sm.bar, phase, p.w, &sm.abort_flag, 1)) break;
@@ -496,12 +503,13 @@ __global__ void __launch_bounds__(NT, 1) k_ta_out(const TaOutParams p) {
     if (valid) {
       const long long op = p.transpose ? (long long)j * p.N + i : pr;
       uint4* d4 = reinterpret_cast<uint4*>(p.out + op * kC + c0);
+      const float sc = p.oscale;    // undoes the power-of-two scale of the W_o image
 #pragma unroll
       for (int u = 0; u < 4; ++u)
-        d4[u] = make_uint4(pack_bf16x2(__uint_as_float(rr[8 * u]), __uint_as_float(rr[8 * u + 1])),
-                           pack_bf16x2(__uint_as_float(rr[8 * u + 2]), __uint_as_float(rr[8 * u + 3])),
-                           pack_bf16x2(__uint_as_float(rr[8 * u + 4]), __uint_as_float(rr[8 * u + 5])),
-                           pack_bf16x2(__uint_as_float(rr[8 * u + 6]), __uint_as_float(rr[8 * u + 7])));
+        d4[u] = make_uint4(pack_bf16x2(__uint_as_float(rr[8 * u]) * sc, __uint_as_float(rr[8 * u + 1]) * sc),
+                           pack_bf16x2(__uint_as_float(rr[8 * u + 2]) * sc, __uint_as_float(rr[8 * u + 3]) * sc),
+                           pack_bf16x2(__uint_as_float(rr[8 * u + 4]) * sc, __uint_as_float(rr[8 * u + 5]) * sc),
+                           pack_bf16x2(__uint_as_float(rr[8 * u + 6]) * sc, __uint_as_float(rr[8 * u + 7]) * sc));
     }
   }
   tc_fence_before();

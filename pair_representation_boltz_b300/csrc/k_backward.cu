@@ -10,24 +10,33 @@
 //     dy = dout sigmoid(gg),  dgg = dout y sigmoid'(gg)
 //     dxh = W_o^T dy,  dzh_g = W_g^T dgg                                  [MMA 2: A = dy, dgg]
 //     dW_g += dgg zh^T,  dW_o += dy xh^T   (summed over the CTA's pairs)   [MMA 3, TMEM-resident]
-//     dx = LN_out backward of dxh -> dX (bf16, channel-major), d(gamma_out), d(beta_out)
+//     dx = LN_out backward of dxh -> dX (float32, over x in place), d(gamma_out), d(beta_out)
 //   projection backward (k_bwd_project), per pair p = (i, k), once for a and once for b:
 //     pv = W_v zh, pg = W_gt zh                                            [MMA 1: A = zh]
 //     dpv = dV sigmoid(pg) m_i m_k,  dpg = dV pv m_i m_k sigmoid'(pg)     (dV = dA or dB)
-//     dzh += W_v^T dpv + W_gt^T dpg                                       [MMA 2]
+//     dzh += W_v^T dpv + W_gt^T dpg                                       [MMA 2, two accumulators]
 //     dW_v += dpv zh^T,  dW_gt += dpg zh^T                                [MMA 3, TMEM-resident]
 //     second launch: dz = LN_in backward of dzh, d(gamma_in), d(beta_in)
+//
+// Precision. Every tensor-core operand is fp16 (11 significant bits; bf16's 8 would cost several
+// times the bf16 tolerance of the gradients), each stored times a power of two that keeps it inside
+// fp16's normal range: the weight images and zh, xh by factors the weights fix (host), dy and dgg by
+// factors from the largest |dout| (k_absmax_bf16, read here from device memory), the per-pair dpv and
+// dpg by factors that bound them from the fp16 contraction operands. Every product's epilogue
+// multiplies its float32 result by the exact inverse of the scales it carries, so all stored
+// gradients (dzh, dX, the parameter partials) are in true units. dX is written as float32 over x
+// and its largest magnitude is recorded, so that k_convert_transpose can scale it into fp16.
 //
 // Layout. One CTA of 512 threads per SM, persistent over tiles of 128 consecutive pairs of the
 // flattened N x N grid. Warp w serves the 32 pairs of TMEM lane quarter w % 4 (the lanes it may
 // read) and channel quarter w / 4: each pair is handled by four threads of 32 channels each, so
 // that every warp's loads of a channel cover 32 consecutive pairs, and the LayerNorm statistics of a
 // pair are combined from its four quarters through shared memory. Per-pair operands are written
-// into 128 x 128 bf16 shared-memory tiles in the 128-byte-swizzled K-major layout (pair rows,
+// into 128 x 128 fp16 shared-memory tiles in the 128-byte-swizzled K-major layout (pair rows,
 // channel columns). The same bytes serve MMA 1 and 2 as K-major operands (K =
 // channels) and MMA 3 as MN-major operands (K = pairs): a 128-byte row of 64 channels of one pair is
 // one K-major row and, read the other way, one MN-major row of 64 M (or N) elements at one K index.
-// Weights are plain bf16 [out][in] images in the same layout; MMA 1 reads them K-major (B = W,
+// Weights are fp16 [out][in] images in the same layout; MMA 1 reads them K-major (B = W,
 // N = out), MMA 2 MN-major (B = W^T, N = in, K = out). TMEM: columns 0..255 hold MMA 1's two
 // results and then MMA 2's; columns 256..511 accumulate the two parameter gradients of MMA 3 over
 // every tile of the CTA, written out once as per-CTA partial sums (added in fixed order later).
@@ -47,6 +56,7 @@ struct alignas(1024) OutSmem {
   uint64_t bar;
   uint32_t tmem_slot;
   int abort_flag;
+  float amax;                           // largest |dX| the CTA wrote
 };
 
 struct alignas(1024) ProjSmem {
@@ -81,9 +91,9 @@ __device__ __forceinline__ void prefetch_plane_rows(const float* plane, long lon
 
 namespace {
 
-// The 32 channels [32 h, 32 h + 32) of zh for pair `pr` (LayerNorm_in from the stored statistics) into
-// row r of an operand tile; zeros for a pair past the grid.
-__device__ __forceinline__ void zh_quarter(uint8_t* tile, const float* ln_g, const float* ln_b,
+// The 32 channels [32 h, 32 h + 32) of zh (times sz) for pair `pr` (LayerNorm_in from the stored
+// statistics) into row r of an fp16 operand tile; zeros for a pair past the grid.
+__device__ __forceinline__ void zh_quarter(uint8_t* tile, const float* ln_g, const float* ln_b, float sz,
                                            const __nv_bfloat16* z, const float2* zstat, long long pr, bool valid,
                                            int r, int h) {
   float f[32];
@@ -91,13 +101,20 @@ __device__ __forceinline__ void zh_quarter(uint8_t* tile, const float* ln_g, con
     const float2 st = zstat[pr];
     load32_bf16(z + pr * kC + 32 * h, f);
 #pragma unroll
-    for (int e = 0; e < 32; ++e) f[e] = ln_g[32 * h + e] * fmaf(f[e], st.x, st.y) + ln_b[32 * h + e];
+    for (int e = 0; e < 32; ++e) f[e] = (ln_g[32 * h + e] * fmaf(f[e], st.x, st.y) + ln_b[32 * h + e]) * sz;
   } else {
 #pragma unroll
     for (int e = 0; e < 32; ++e) f[e] = 0.f;
   }
 #pragma unroll
-  for (int u = 0; u < 4; ++u) put8(tile, r, 32 * h + 8 * u, f + 8 * u);
+  for (int u = 0; u < 4; ++u) put8h(tile, r, 32 * h + 8 * u, f + 8 * u);
+}
+
+// Largest |value| of a warp's lanes as a float (non-negative, so its bits order like integers).
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
 }
 
 __global__ void __launch_bounds__(NT, 1) k_bwd_output(const BwdOutParams p) {
@@ -109,6 +126,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_output(const BwdOutParams p) {
   if (tid == 0) {
     mbar_init(&sm.bar, 1);
     sm.abort_flag = 0;
+    sm.amax = 0.f;
     fence_mbar_init();
   }
   for (int k = tid; k < 4 * kC; k += NT) sm.ln[k] = p.ln[k];
@@ -128,8 +146,14 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_output(const BwdOutParams p) {
   const uint32_t a_zh = smem_u32(sm.zh), a_xh = smem_u32(sm.xh), a_dy = smem_u32(sm.dy), a_dgg = smem_u32(sm.dgg);
   const uint32_t a_wg = smem_u32(sm.wg), a_wo = smem_u32(sm.wo);
   const int c0 = 32 * h;                           // this thread's first channel
+  // dy and dgg are stored times d1 and d2: powers of two that bring the largest |dout| to just below
+  // 2^14, and its product with the bound on |y| / 4 likewise
+  const float dmax = __uint_as_float(p.amax[0]);
+  const float d1 = pow2_scale(dmax, 14), d2 = pow2_scale(dmax * p.y_bound4, 14);
+  const float u_dxh = p.u_dxh / d1, u_dzh = p.u_dzh / d2, u_wg = p.u_wg / d2, u_wo = p.u_wo / d1;
 
   float acc_g = 0.f, acc_b = 0.f;                  // channel c0 + lane: sums of dxh n and dxh
+  float dx_max = 0.f;                              // largest |dX| this thread writes
   uint32_t phase = 0;
   int local = 0;
   bool ok = true;
@@ -138,7 +162,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_output(const BwdOutParams p) {
     const bool valid = pr < p.P;
     const int i = valid ? (int)(pr / p.N) : 0;
     const int j = valid ? (int)(pr - (long long)i * p.N) : 0;
-    const float* xp = p.x + (long long)i * p.ldx + j + (long long)c0 * p.xplane;
+    float* xp = p.x + (long long)i * p.ldx + j + (long long)c0 * p.xplane;
     {
       // L2 prefetch of what the next tile of this CTA reads: x (one channel per thread of the first
       // 128), z, dout and the LayerNorm_in statistics
@@ -152,11 +176,12 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_output(const BwdOutParams p) {
       }
     }
 
-    // ---- zh; x of this quarter: (mean, M2), combined over the four quarters (Chan et al.)
-    zh_quarter(sm.zh, g_in, b_in, p.z, p.zstat, pr, valid, r, h);
+    // ---- zh; x of this quarter (the contraction's output times x_unscale): (mean, M2), combined over
+    // the four quarters (Chan et al.)
+    zh_quarter(sm.zh, g_in, b_in, p.sz, p.z, p.zstat, pr, valid, r, h);
     float xv[32];
 #pragma unroll
-    for (int e = 0; e < 32; ++e) xv[e] = valid ? xp[e * p.xplane] : 0.f;
+    for (int e = 0; e < 32; ++e) xv[e] = valid ? xp[e * p.xplane] * p.x_unscale : 0.f;
     {
       float s = 0.f;
 #pragma unroll
@@ -172,24 +197,24 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_output(const BwdOutParams p) {
     {
       const float2 q0 = sm.xst[0][r], q1 = sm.xst[1][r], q2 = sm.xst[2][r], q3 = sm.xst[3][r];
       mu = ((q0.x + q1.x) + (q2.x + q3.x)) * 0.25f;
-      const float d0 = q0.x - mu, d1 = q1.x - mu, d2 = q2.x - mu, d3 = q3.x - mu;
-      const float m2 = ((q0.y + q1.y) + (q2.y + q3.y)) + 32.f * ((d0 * d0 + d1 * d1) + (d2 * d2 + d3 * d3));
+      const float d0 = q0.x - mu, dd1 = q1.x - mu, dd2 = q2.x - mu, d3 = q3.x - mu;
+      const float m2 = ((q0.y + q1.y) + (q2.y + q3.y)) + 32.f * ((d0 * d0 + dd1 * dd1) + (dd2 * dd2 + d3 * d3));
       rx = rsqrtf(m2 * (1.f / kC) + 1e-5f);
     }
     {
       float f[32];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) f[e] = valid ? g_out[c0 + e] * ((xv[e] - mu) * rx) + b_out[c0 + e] : 0.f;
+      for (int e = 0; e < 32; ++e) f[e] = valid ? (g_out[c0 + e] * ((xv[e] - mu) * rx) + b_out[c0 + e]) * p.sx : 0.f;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) put8(sm.xh, r, c0 + 8 * u, f + 8 * u);
+      for (int u = 0; u < 4; ++u) put8h(sm.xh, r, c0 + 8 * u, f + 8 * u);
     }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     if (tid == 0) {
       tc_fence_after();
-      mma_tile(tmem, a_zh, false, a_wg, false, ID_KK, false);         // gg = W_g zh
-      mma_tile(tmem + kC, a_xh, false, a_wo, false, ID_KK, false);    // y  = W_o xh
+      mma_tile(tmem, a_zh, false, a_wg, false, ID_KK_H, false);         // gg = W_g zh
+      mma_tile(tmem + kC, a_xh, false, a_wo, false, ID_KK_H, false);    // y  = W_o xh
       mma_commit(&sm.bar);
     }
     if (!cta_wait(&sm.bar, phase, p.w, &sm.abort_flag, 1)) { ok = false; break; }
@@ -216,14 +241,14 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_output(const BwdOutParams p) {
       float vy[16], vg[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
-        const float s = sigmoid_mufu(__uint_as_float(rg[e]));
-        vy[e] = d[e] * s;
-        vg[e] = d[e] * __uint_as_float(ry[e]) * s * (1.f - s);
+        const float s = sigmoid_mufu(__uint_as_float(rg[e]) * p.u_gg);
+        vy[e] = d[e] * s * d1;
+        vg[e] = d[e] * (__uint_as_float(ry[e]) * p.u_y) * s * (1.f - s) * d2;
       }
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        put8(sm.dy, r, c0 + 16 * hh + 8 * u, vy + 8 * u);
-        put8(sm.dgg, r, c0 + 16 * hh + 8 * u, vg + 8 * u);
+        put8h(sm.dy, r, c0 + 16 * hh + 8 * u, vy + 8 * u);
+        put8h(sm.dgg, r, c0 + 16 * hh + 8 * u, vg + 8 * u);
       }
     }
     fence_proxy_async_smem();
@@ -231,10 +256,10 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_output(const BwdOutParams p) {
     __syncthreads();
     if (tid == 0) {
       tc_fence_after();
-      mma_tile(tmem, a_dy, false, a_wo, true, ID_KM, false);              // dxh   = W_o^T dy
-      mma_tile(tmem + kC, a_dgg, false, a_wg, true, ID_KM, false);        // dzh_g = W_g^T dgg
-      mma_tile(tmem + 2 * kC, a_dgg, true, a_zh, true, ID_MM, local > 0); // dW_g += dgg zh^T
-      mma_tile(tmem + 3 * kC, a_dy, true, a_xh, true, ID_MM, local > 0);  // dW_o += dy xh^T
+      mma_tile(tmem, a_dy, false, a_wo, true, ID_KM_H, false);              // dxh   = W_o^T dy
+      mma_tile(tmem + kC, a_dgg, false, a_wg, true, ID_KM_H, false);        // dzh_g = W_g^T dgg
+      mma_tile(tmem + 2 * kC, a_dgg, true, a_zh, true, ID_MM_H, local > 0); // dW_g += dgg zh^T
+      mma_tile(tmem + 3 * kC, a_dy, true, a_xh, true, ID_MM_H, local > 0);  // dW_o += dy xh^T
       mma_commit(&sm.bar);
     }
     if (!cta_wait(&sm.bar, phase, p.w, &sm.abort_flag, 2)) { ok = false; break; }
@@ -248,7 +273,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_output(const BwdOutParams p) {
       tmem_ld_wait();
       if (valid)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) p.dzh[(long long)(c0 + e) * p.P + pr] = __uint_as_float(rz[e]);
+        for (int e = 0; e < 32; ++e) p.dzh[(long long)(c0 + e) * p.P + pr] = __uint_as_float(rz[e]) * u_dzh;
     }
     uint32_t rd[32];
     tmem_ld32(trow + c0, rd);
@@ -259,7 +284,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_output(const BwdOutParams p) {
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
         xv[e] = valid ? (xv[e] - mu) * rx : 0.f;                  // n, the normalised x
-        const float dxh = valid ? __uint_as_float(rd[e]) : 0.f;
+        const float dxh = valid ? __uint_as_float(rd[e]) * u_dxh : 0.f;
         rd[e] = __float_as_uint(dxh);
         const float dn = dxh * g_out[c0 + e];
         s1 += dn;
@@ -279,12 +304,21 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_output(const BwdOutParams p) {
       s2 = ((q0.y + q1.y) + (q2.y + q3.y)) * (1.f / kC);
     }
     if (valid) {
-      __nv_bfloat16* dxp = p.dX + (long long)i * p.ld + j + (long long)c0 * p.dplane;
+      // over x, in place: this thread has read these 32 values (and no other thread reads them)
 #pragma unroll
-      for (int e = 0; e < 32; ++e)
-        dxp[e * p.dplane] = __float2bfloat16_rn(rx * (__uint_as_float(rd[e]) * g_out[c0 + e] - s1 - xv[e] * s2));
+      for (int e = 0; e < 32; ++e) {
+        const float dx = rx * (__uint_as_float(rd[e]) * g_out[c0 + e] - s1 - xv[e] * s2);
+        dx_max = fmaxf(dx_max, fabsf(dx));
+        xp[e * p.xplane] = dx;
+      }
     }
   }
+
+  // ---- the largest |dX| of the CTA, for the fp16 scale of dX
+  dx_max = warp_max(dx_max);
+  if (lane == 0) atomicMax(reinterpret_cast<unsigned*>(&sm.amax), __float_as_uint(dx_max));
+  __syncthreads();
+  if (tid == 0) atomicMax(p.amax + 1, __float_as_uint(sm.amax));
 
   // ---- per-CTA partial sums: d(gamma_out), d(beta_out) over the lane quarters; dW_g, dW_o from TMEM
   if (ok) {
@@ -299,8 +333,9 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_output(const BwdOutParams p) {
       uint32_t rr[32];
       tmem_ld32(trow + (2 + m) * kC + c0, rr);
       tmem_ld_wait();
+      const float u = m == 0 ? u_wg : u_wo;
 #pragma unroll
-      for (int e = 0; e < 32; ++e) pw[m * kC * kC + e] = local > 0 ? __uint_as_float(rr[e]) : 0.f;
+      for (int e = 0; e < 32; ++e) pw[m * kC * kC + e] = local > 0 ? __uint_as_float(rr[e]) * u : 0.f;
     }
   }
   tc_fence_before();
@@ -340,6 +375,10 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_project(const BwdProjParams p) {
   const uint32_t a_zh = smem_u32(sm.zh), a_dv = smem_u32(sm.dv), a_dg = smem_u32(sm.dg);
   const uint32_t a_wv = smem_u32(sm.wv), a_wgt = smem_u32(sm.wgt);
   const int c0 = 32 * h;
+  // dV arrives times sx (the fp16 scale of dX, from its recorded maximum) and times the fp16 scale of
+  // its contraction partner (in the host factors below)
+  const float ix = 1.f / pow2_scale(__uint_as_float(p.amax[1]), 14);
+  const float u1 = p.u_dzh_v * ix, u2 = p.u_dzh_g * ix, u3 = p.u_wv * ix, u4 = p.u_wgt * ix;
 
   float acc_g = 0.f, acc_b = 0.f;
   uint32_t phase = 0;
@@ -362,7 +401,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_project(const BwdProjParams p) {
       }
     }
 
-    zh_quarter(sm.zh, g_in, b_in, p.z, p.zstat, pr, valid, r, h);
+    zh_quarter(sm.zh, g_in, b_in, p.sz, p.z, p.zstat, pr, valid, r, h);
     // this quarter of dV (issued before the MMA, consumed after it)
     const float m = valid ? (p.mask ? p.mask[i] * p.mask[k2] : 1.f) : 0.f;
     float dv[32];
@@ -376,15 +415,15 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_project(const BwdProjParams p) {
     __syncthreads();
     if (tid == 0) {
       tc_fence_after();
-      mma_tile(tmem, a_zh, false, a_wv, false, ID_KK, false);        // pv = W_v zh
-      mma_tile(tmem + kC, a_zh, false, a_wgt, false, ID_KK, false);  // pg = W_gt zh
+      mma_tile(tmem, a_zh, false, a_wv, false, ID_KK_H, false);        // pv = W_v zh
+      mma_tile(tmem + kC, a_zh, false, a_wgt, false, ID_KK_H, false);  // pg = W_gt zh
       mma_commit(&sm.bar);
     }
     if (!cta_wait(&sm.bar, phase, p.w, &sm.abort_flag, 1)) { ok = false; break; }
     phase ^= 1u;
     tc_fence_after();
 
-    // ---- gate backward: dpv = dV s m, dpg = dV pv m s (1 - s)
+    // ---- gate backward: dpv = dV s m, dpg = dV pv m s (1 - s), stored times q1, q2 (with dV's scale)
 #pragma unroll 1
     for (int hh = 0; hh < 2; ++hh) {
       uint32_t rv[16], rg[16];
@@ -395,14 +434,14 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_project(const BwdProjParams p) {
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const float d = dv[16 * hh + e];
-        const float s = sigmoid_mufu(__uint_as_float(rg[e]));
-        fv[e] = d * s;
-        fg[e] = d * __uint_as_float(rv[e]) * s * (1.f - s);
+        const float s = sigmoid_mufu(__uint_as_float(rg[e]) * p.u_pg);
+        fv[e] = d * s * p.q1;
+        fg[e] = d * (__uint_as_float(rv[e]) * p.u_pv) * s * (1.f - s) * p.q2;
       }
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        put8(sm.dv, r, c0 + 16 * hh + 8 * u, fv + 8 * u);
-        put8(sm.dg, r, c0 + 16 * hh + 8 * u, fg + 8 * u);
+        put8h(sm.dv, r, c0 + 16 * hh + 8 * u, fv + 8 * u);
+        put8h(sm.dg, r, c0 + 16 * hh + 8 * u, fg + 8 * u);
       }
     }
     fence_proxy_async_smem();
@@ -410,10 +449,11 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_project(const BwdProjParams p) {
     __syncthreads();
     if (tid == 0) {
       tc_fence_after();
-      mma_tile(tmem, a_dv, false, a_wv, true, ID_KM, false);               // W_v^T dpv
-      mma_tile(tmem, a_dg, false, a_wgt, true, ID_KM, true);               //  + W_gt^T dpg
-      mma_tile(tmem + 2 * kC, a_dv, true, a_zh, true, ID_MM, local > 0);   // dW_v  += dpv zh^T
-      mma_tile(tmem + 3 * kC, a_dg, true, a_zh, true, ID_MM, local > 0);   // dW_gt += dpg zh^T
+      // the two terms of dzh carry different scales: one accumulator each
+      mma_tile(tmem, a_dv, false, a_wv, true, ID_KM_H, false);               // W_v^T dpv
+      mma_tile(tmem + kC, a_dg, false, a_wgt, true, ID_KM_H, false);         // W_gt^T dpg
+      mma_tile(tmem + 2 * kC, a_dv, true, a_zh, true, ID_MM_H, local > 0);   // dW_v  += dpv zh^T
+      mma_tile(tmem + 3 * kC, a_dg, true, a_zh, true, ID_MM_H, local > 0);   // dW_gt += dpg zh^T
       mma_commit(&sm.bar);
     }
     // the earlier terms of dzh, read while the MMA runs
@@ -424,11 +464,13 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_project(const BwdProjParams p) {
     phase ^= 1u;
     tc_fence_after();
     {
-      uint32_t rr[32];
-      tmem_ld32(trow + c0, rr);
+      uint32_t ra[32], rb[32];
+      tmem_ld32(trow + c0, ra);
+      tmem_ld32(trow + kC + c0, rb);
       tmem_ld_wait();
 #pragma unroll
-      for (int e = 0; e < 32; ++e) dzh[e] = valid ? dzh[e] + __uint_as_float(rr[e]) : 0.f;
+      for (int e = 0; e < 32; ++e)
+        dzh[e] = valid ? dzh[e] + (__uint_as_float(ra[e]) * u1 + __uint_as_float(rb[e]) * u2) : 0.f;
     }
     if (!p.final_pass) {
       if (valid)
@@ -497,8 +539,9 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_project(const BwdProjParams p) {
       uint32_t rr[32];
       tmem_ld32(trow + (2 + mm) * kC + c0, rr);
       tmem_ld_wait();
+      const float u = mm == 0 ? u3 : u4;
 #pragma unroll
-      for (int e = 0; e < 32; ++e) pw[mm * kC * kC + e] = local > 0 ? __uint_as_float(rr[e]) : 0.f;
+      for (int e = 0; e < 32; ++e) pw[mm * kC * kC + e] = local > 0 ? __uint_as_float(rr[e]) * u : 0.f;
     }
   }
   tc_fence_before();
@@ -506,48 +549,79 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_project(const BwdProjParams p) {
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
+// Largest |value| of a bf16 tensor of n elements (n a multiple of 8, 16-byte aligned), merged into
+// *out with an atomic maximum on the float's bits (non-negative floats order like their bits).
+__global__ void __launch_bounds__(256) k_absmax_bf16(const __nv_bfloat16* __restrict__ v, long long n,
+                                                      unsigned* out) {
+  __shared__ unsigned red[8];
+  uint32_t mx = 0;   // largest |bf16| as its bits (sign cleared)
+  const uint4* q = reinterpret_cast<const uint4*>(v);
+  for (long long k = blockIdx.x * (long long)blockDim.x + threadIdx.x; k < n / 8; k += (long long)gridDim.x * blockDim.x) {
+    const uint4 w = q[k];
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) mx = max(mx, max(ws[e] & 0x7fffu, (ws[e] >> 16) & 0x7fffu));
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) mx = max(mx, red[w]);
+    atomicMax(out, mx << 16);   // the bf16 bits are the upper half of the float's
+  }
+}
+
 constexpr int kTransposePlanes = 16;   // channel planes per block (the same 64 x 64 tile of each)
 
-// out[c][j][i] = in[c][i][j] for i, j < N (bf16 planes [128][N][ld], ld a multiple of 64); 64 x 64 tiles,
-// two elements per thread: rows start 128-byte aligned and every thread takes an even column pair, so a
-// pair inside the grid moves as one 4-byte load and one 4-byte store (scalar at the grid's ragged edge)
-__global__ void __launch_bounds__(256) k_transpose_planes(const __nv_bfloat16* __restrict__ in,
-                                                          __nv_bfloat16* __restrict__ out, int N, long long ld,
-                                                          long long plane) {
-  __shared__ __nv_bfloat16 t[64][64 + 2];
+// dX (float32 planes [128][N][ldx], over x) -> fp16 dX and its per-channel transpose dX^T (planes
+// [128][N][ld]), every value times sx = the power of two that brings the largest |dX| (recorded by
+// the output backward) to just below 2^14. 64 x 64 tiles, 16 channel planes per block, two elements
+// per thread: rows start 128-byte aligned and every thread takes an even column pair, so a pair
+// inside the grid moves as one 8-byte load and one 4-byte store (scalar at the grid's ragged edge).
+__global__ void __launch_bounds__(256) k_convert_transpose(const float* __restrict__ in, long long ldx,
+                                                           long long in_plane, const unsigned* __restrict__ amax,
+                                                           __half* __restrict__ out, __half* __restrict__ outT,
+                                                           int N, long long ld, long long plane) {
+  __shared__ __half t[64][64 + 2];
   const int i0 = blockIdx.y * 64, j0 = blockIdx.x * 64;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8
-  const __nv_bfloat16 zero = __float2bfloat16_rn(0.f);
+  const float sx = pow2_scale(__uint_as_float(*amax), 14);
+  const __half zero = __float2half_rn(0.f);
   for (int c = blockIdx.z * kTransposePlanes; c < (blockIdx.z + 1) * kTransposePlanes; ++c) {
-  const __nv_bfloat16* src = in + c * plane;
-  __nv_bfloat16* dst = out + c * plane;
-  if (c > blockIdx.z * kTransposePlanes) __syncthreads();   // the previous plane's tile has been written out
-  for (int r = ty; r < 64; r += 8) {
-    const int i = i0 + r, j = j0 + 2 * tx;
-    __nv_bfloat162 v;
-    v.x = zero;
-    v.y = zero;
-    if (i < N && j + 1 < N) {
-      v = *reinterpret_cast<const __nv_bfloat162*>(src + (long long)i * ld + j);
-    } else if (i < N && j < N) {
-      v.x = src[(long long)i * ld + j];
+    const float* src = in + c * in_plane;
+    __half* dst = out + c * plane;
+    __half* dstT = outT + c * plane;
+    if (c > blockIdx.z * kTransposePlanes) __syncthreads();   // the previous plane's tile has been written out
+    for (int r = ty; r < 64; r += 8) {
+      const int i = i0 + r, j = j0 + 2 * tx;
+      __half2 v;
+      v.x = zero;
+      v.y = zero;
+      if (i < N && j + 1 < N) {
+        const float2 f = *reinterpret_cast<const float2*>(src + (long long)i * ldx + j);
+        v = __floats2half2_rn(f.x * sx, f.y * sx);
+        *reinterpret_cast<__half2*>(dst + (long long)i * ld + j) = v;
+      } else if (i < N && j < N) {
+        v.x = __float2half_rn(src[(long long)i * ldx + j] * sx);
+        dst[(long long)i * ld + j] = v.x;
+      }
+      t[r][2 * tx] = v.x;
+      t[r][2 * tx + 1] = v.y;
     }
-    t[r][2 * tx] = v.x;
-    t[r][2 * tx + 1] = v.y;
-  }
-  __syncthreads();
-  for (int r = ty; r < 64; r += 8) {
-    const int j = j0 + r, i = i0 + 2 * tx;
-    if (j >= N || i >= N) continue;
-    if (i + 1 < N) {
-      __nv_bfloat162 v;
-      v.x = t[2 * tx][r];
-      v.y = t[2 * tx + 1][r];
-      *reinterpret_cast<__nv_bfloat162*>(dst + (long long)j * ld + i) = v;
-    } else {
-      dst[(long long)j * ld + i] = t[2 * tx][r];
+    __syncthreads();
+    for (int r = ty; r < 64; r += 8) {
+      const int j = j0 + r, i = i0 + 2 * tx;
+      if (j >= N || i >= N) continue;
+      if (i + 1 < N) {
+        __half2 v;
+        v.x = t[2 * tx][r];
+        v.y = t[2 * tx + 1][r];
+        *reinterpret_cast<__half2*>(dstT + (long long)j * ld + i) = v;
+      } else {
+        dstT[(long long)j * ld + i] = t[2 * tx][r];
+      }
     }
-  }
   }
 }
 
@@ -574,11 +648,21 @@ cudaError_t launch_bwd_project_bf16(const BwdProjParams& p, int grid, cudaStream
   return cudaGetLastError();
 }
 
-cudaError_t launch_transpose_planes_bf16(const __nv_bfloat16* in, __nv_bfloat16* out, int N, long long ld, int planes,
-                                         cudaStream_t s) {
+cudaError_t launch_convert_transpose(const float* in, long long ldx, const unsigned* amax, __half* out, __half* outT,
+                                    int N, long long ld, int planes, cudaStream_t s) {
   if (planes % kTransposePlanes) return cudaErrorInvalidValue;
   dim3 grid((N + 63) / 64, (N + 63) / 64, planes / kTransposePlanes);
-  k_transpose_planes<<<grid, 256, 0, s>>>(in, out, N, ld, (long long)N * ld);
+  k_convert_transpose<<<grid, 256, 0, s>>>(in, ldx, (long long)N * ldx, amax, out, outT, N, ld, (long long)N * ld);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_absmax_bf16(const __nv_bfloat16* v, long long n, unsigned* out, int num_sms, cudaStream_t s) {
+  if (n % 8) return cudaErrorInvalidValue;
+  long long blocks = (n / 8 + 255) / 256;
+  const long long cap = 8LL * num_sms;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  k_absmax_bf16<<<(int)blocks, 256, 0, s>>>(v, n, out);
   return cudaGetLastError();
 }
 

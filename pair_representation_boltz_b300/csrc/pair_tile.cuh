@@ -14,11 +14,32 @@ constexpr uint32_t TILE = 128 * 128 * 2;  // bytes of one 128 x 128 bf16 operand
 constexpr uint32_t SLAB = TILE / 2;       // one 64-channel half
 
 
-// 8 floats -> one 16-byte unit of row `r` of an operand tile, for channels c0 .. c0+7 (c0 % 8 == 0)
+// 8 floats -> one 16-byte unit of row `r` of an operand tile, for channels c0 .. c0+7 (c0 % 8 == 0),
+// as bf16 (put8) or fp16 (put8h)
 __device__ __forceinline__ void put8(uint8_t* tile, int r, int c0, const float* v) {
   const uint4 q = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
                              pack_bf16x2(v[6], v[7]));
   *reinterpret_cast<uint4*>(tile + (c0 >> 6) * SLAB + sw128_offset((uint32_t)r, (uint32_t)((c0 & 63) >> 3))) = q;
+}
+__device__ __forceinline__ void put8h(uint8_t* tile, int r, int c0, const float* v) {
+  const uint4 q = make_uint4(pack_f16x2(v[0], v[1]), pack_f16x2(v[2], v[3]), pack_f16x2(v[4], v[5]),
+                             pack_f16x2(v[6], v[7]));
+  *reinterpret_cast<uint4*>(tile + (c0 >> 6) * SLAB + sw128_offset((uint32_t)r, (uint32_t)((c0 & 63) >> 3))) = q;
+}
+
+__device__ __forceinline__ void f16x8_to_float(const uint4& q, float* f) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+    f[2 * k] = t.x;
+    f[2 * k + 1] = t.y;
+  }
+}
+
+// 8 floats as fp16 in one 16-byte word
+__device__ __forceinline__ uint4 pack8h(const float* v) {
+  return make_uint4(pack_f16x2(v[0], v[1]), pack_f16x2(v[2], v[3]), pack_f16x2(v[4], v[5]), pack_f16x2(v[6], v[7]));
 }
 
 __device__ __forceinline__ void bf16x8_to_float(const uint4& q, float* f) {
@@ -30,8 +51,8 @@ __device__ __forceinline__ void bf16x8_to_float(const uint4& q, float* f) {
   }
 }
 
-// Copy a weight image (already in the tile layout) into shared memory, all threads.
-__device__ __forceinline__ void copy_tile(uint8_t* dst, const __nv_bfloat16* src) {
+// Copy a weight image (already in the tile layout, 16-bit elements) into shared memory, all threads.
+__device__ __forceinline__ void copy_tile(uint8_t* dst, const void* src) {
   const uint4* s = reinterpret_cast<const uint4*>(src);
   uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll 4
@@ -46,6 +67,16 @@ __device__ __forceinline__ void load32_bf16(const __nv_bfloat16* src, float* f) 
   for (int u = 0; u < 4; ++u) v[u] = q[u];
 #pragma unroll
   for (int u = 0; u < 4; ++u) bf16x8_to_float(v[u], f + 8 * u);
+}
+
+// 32 fp16 values (64 bytes) -> floats
+__device__ __forceinline__ void load32_f16(const __half* src, float* f) {
+  const uint4* q = reinterpret_cast<const uint4*>(src);
+  uint4 v[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) v[u] = q[u];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) f16x8_to_float(v[u], f + 8 * u);
 }
 
 // Butterfly reduce-scatter over the 32 lanes of a warp: on return lane l holds the sum over the
@@ -75,6 +106,10 @@ __device__ __forceinline__ uint64_t mndesc(uint32_t base, int ks) {
 constexpr uint32_t ID_KK = make_idesc(128, 128, FMT_BF16, false, false);
 constexpr uint32_t ID_KM = make_idesc(128, 128, FMT_BF16, false, true);
 constexpr uint32_t ID_MM = make_idesc(128, 128, FMT_BF16, true, true);
+// the same products on fp16 operand tiles (both operands fp16)
+constexpr uint32_t ID_KK_H = make_idesc(128, 128, FMT_F16, false, false);
+constexpr uint32_t ID_KM_H = make_idesc(128, 128, FMT_F16, false, true);
+constexpr uint32_t ID_MM_H = make_idesc(128, 128, FMT_F16, true, true);
 
 // D (+)= A B^T over the 128 K of two tiles
 __device__ __forceinline__ void mma_tile(uint32_t d, uint32_t a, bool a_mn, uint32_t b, bool b_mn, uint32_t idesc,

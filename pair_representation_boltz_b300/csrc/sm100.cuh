@@ -392,6 +392,17 @@ __device__ __forceinline__ float tanh_mufu(float v) {
   return r;
 }
 
+// The power of two 2^(target - E) for the exponent E with 2^(E-1) <= amax < 2^E, so that every value
+// of magnitude at most amax, multiplied by it, stays below 2^target; 1 when amax is 0, subnormal, or
+// not finite. The exponent is clamped so that the result is a normal float.
+__device__ __forceinline__ float pow2_scale(float amax, int target) {
+  const uint32_t be = (__float_as_uint(amax) >> 23) & 255u;
+  if (be == 0u || be == 255u) return 1.f;
+  int ex = target - ((int)be - 126);
+  ex = ex < -126 ? -126 : (ex > 127 ? 127 : ex);
+  return __uint_as_float((uint32_t)(127 + ex) << 23);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);

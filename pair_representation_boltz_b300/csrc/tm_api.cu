@@ -172,6 +172,26 @@ void make_tile_image(const float* W, __nv_bfloat16* img) {
     }
 }
 
+// The same image in fp16, every weight multiplied by `scale` (a power of two) first.
+void make_tile_image_h(const float* W, double scale, __half* img) {
+  const int C = kC;
+  for (int r = 0; r < C; ++r)
+    for (int k = 0; k < C; ++k) {
+      const int half = k / 64, u = (k % 64) / 8, e = k % 8;
+      const size_t byte = (size_t)half * (C * 64 * 2) + (size_t)r * 128 + (size_t)((u ^ (r & 7)) * 16) + e * 2;
+      img[byte / 2] = __float2half_rn((float)((double)W[(size_t)r * C + k] * scale));
+    }
+}
+
+// Power-of-two exponent s that brings the largest |W| of a 128 x 128 matrix into [2^13, 2^14), so that
+// its fp16 image keeps every entry normal down to 2^-27 of the largest.
+int fp16_image_exponent(const float* W) {
+  double mx = 0;
+  for (int i = 0; i < kC * kC; ++i) mx = std::max(mx, std::fabs((double)W[i]));
+  if (!(mx > 0)) return 0;
+  return 13 - (int)std::floor(std::log2(mx));
+}
+
 tm_status prepare_tensor_core_weights(tm_ctx* c, const tm_weights* w) {
   const int C = kC;
   std::vector<__nv_bfloat16> k1(2 * 2 * 256 * C);
@@ -205,7 +225,12 @@ tm_status prepare_tensor_core_weights(tm_ctx* c, const tm_weights* w) {
     }
   }
   c->ab_bound = 0;
-  for (int n = 0; n < C; ++n) c->ab_bound = std::max(c->ab_bound, abound[0][n] * abound[1][n]);
+  c->pv_bound[0] = c->pv_bound[1] = 0;
+  for (int n = 0; n < C; ++n) {
+    c->ab_bound = std::max(c->ab_bound, abound[0][n] * abound[1][n]);
+    c->pv_bound[0] = std::max(c->pv_bound[0], abound[0][n]);
+    c->pv_bound[1] = std::max(c->pv_bound[1], abound[1][n]);
+  }
   // W_o' = W_o diag(gamma_out), scaled by 2^e into fp16's top binades
   double maxabs = 0;
   for (int o = 0; o < C; ++o)
@@ -257,12 +282,34 @@ tm_status prepare_tensor_core_weights(tm_ctx* c, const tm_weights* w) {
   TM_UP(c->wg16, wg)
 #undef TM_UP
   {
-    // Backward images: W [out][in] as bf16 in the 128-byte-swizzled K-major tile layout the backward
-    // kernels copy straight into shared memory (64-column halves 16 KB apart, 128-byte rows, 16-byte
-    // unit u of row r at unit u ^ (r % 8)).
+    // Backward images: W [out][in] as fp16, times a power of two each, in the 128-byte-swizzled K-major
+    // tile layout the backward kernels copy straight into shared memory (64-column halves 16 KB apart,
+    // 128-byte rows, 16-byte unit u of row r at unit u ^ (r % 8)). Bounds for the fp16 scales of the
+    // backward's per-pair operands: |zh_k| <= sqrt(c_z) |gamma_in,k| + |beta_in,k|, |xh_k| likewise
+    // with the output LayerNorm, |(W_o xh)_c| <= sqrt(c_h) ||W_o[c] diag(gamma_out)|| + |(W_o beta_out)_c|.
     const float* src[6] = {w->w_g, w->w_o, w->w_a, w->w_ga, w->w_b, w->w_gb};
-    std::vector<__nv_bfloat16> img(6 * C * C);
-    for (int m = 0; m < 6; ++m) make_tile_image(src[m], img.data() + (size_t)m * C * C);
+    std::vector<__half> img(6 * C * C);
+    for (int m = 0; m < 6; ++m) {
+      c->bwd_wexp[m] = fp16_image_exponent(src[m]);
+      make_tile_image_h(src[m], std::ldexp(1.0, c->bwd_wexp[m]), img.data() + (size_t)m * C * C);
+    }
+    double zb = 0, xb = 0, yb = 0;
+    for (int k = 0; k < C; ++k) {
+      zb = std::max(zb, std::sqrt((double)C) * std::fabs((double)w->ln_in_gamma[k]) + std::fabs((double)w->ln_in_beta[k]));
+      xb = std::max(xb, std::sqrt((double)C) * std::fabs((double)w->ln_out_gamma[k]) + std::fabs((double)w->ln_out_beta[k]));
+    }
+    for (int o = 0; o < C; ++o) {
+      double n2 = 0, b = 0;
+      for (int k = 0; k < C; ++k) {
+        const double v = (double)w->w_o[(size_t)o * C + k];
+        n2 += v * v * (double)w->ln_out_gamma[k] * (double)w->ln_out_gamma[k];
+        b += v * (double)w->ln_out_beta[k];
+      }
+      yb = std::max(yb, std::sqrt((double)C * n2) + std::fabs(b));
+    }
+    c->zh_bound = zb;
+    c->xh_bound = xb;
+    c->y_bound = yb;
     std::vector<float> ln(4 * C);
     for (int k = 0; k < C; ++k) {
       ln[k] = w->ln_in_gamma[k];
@@ -298,8 +345,17 @@ tm_status prepare_tensor_core_weights(tm_ctx* c, const tm_weights* w) {
 }
 
 // ------------------------------------------------------------------ bf16 stage launchers (arguments checked)
-tm_status run_project_bf16(tm_ctx* c, const void* z, const float* mask, int N, float2* zstat, __nv_bfloat16* a,
-                           __nv_bfloat16* b, int ld, cudaStream_t s, const tm_options* opt) {
+double pow2_scale_host(double bound, int target) {
+  if (!(bound > 0) || !std::isfinite(bound)) return 1.0;
+  int e = 0;
+  std::frexp(bound, &e);   // bound = m 2^e, 0.5 <= m < 1
+  const int ex = std::min(127, std::max(-126, target - e));
+  return std::ldexp(1.0, ex);
+}
+
+tm_status run_project_bf16(tm_ctx* c, const void* z, const float* mask, int N, float2* zstat, void* a,
+                           void* b, int ld, cudaStream_t s, const tm_options* opt, bool out_f16, float scale_a,
+                           float scale_b) {
   CUtensorMap zmap;
   const cuuint64_t dims[3] = {(cuuint64_t)kC, (cuuint64_t)N, (cuuint64_t)N};
   const cuuint64_t str[2] = {(cuuint64_t)kC * 2, (cuuint64_t)N * kC * 2};
@@ -314,8 +370,11 @@ tm_status run_project_bf16(tm_ctx* c, const void* z, const float* mask, int N, f
       return fail(c, TM_ERR_CUDA, "tensor map (a/b, projection store)");
   }
   ProjectParams p;
-  p.a = a;
-  p.b = b;
+  p.a = reinterpret_cast<__nv_bfloat16*>(a);
+  p.b = reinterpret_cast<__nv_bfloat16*>(b);
+  p.out_f16 = out_f16 ? 1 : 0;
+  p.out_scale[0] = scale_a;
+  p.out_scale[1] = scale_b;
   p.mask = mask;
   p.consts = c->k1c;
   p.zstat = zstat;
@@ -328,9 +387,9 @@ tm_status run_project_bf16(tm_ctx* c, const void* z, const float* mask, int N, f
   return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "projection launch");
 }
 
-tm_status run_contract_bf16(tm_ctx* c, const __nv_bfloat16* a, const __nv_bfloat16* b, int N, int ld, bool incoming,
+tm_status run_contract_bf16(tm_ctx* c, const void* a, const void* b, int N, int ld, bool incoming,
                             int i0, int j0, int bi, int bj, void* x, int ldx, XFormat xf, int x_exp,
-                            cudaStream_t s, const tm_options* opt) {
+                            cudaStream_t s, const tm_options* opt, bool ab_f16) {
   CUtensorMap amap, bmap;
   const cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)N, (cuuint64_t)kC};
   const cuuint64_t str[2] = {(cuuint64_t)ld * 2, (cuuint64_t)N * ld * 2};
@@ -345,6 +404,7 @@ tm_status run_contract_bf16(tm_ctx* c, const __nv_bfloat16* a, const __nv_bfloat
   }
   ContractParams p;
   p.x = x;
+  p.ab_f16 = ab_f16 ? 1 : 0;
   p.x_f16 = xf == X_F16 ? 1 : 0;
   p.x_exp = x_exp;
   p.ldx = ldx;
@@ -623,9 +683,8 @@ tm_status tm_contract_ex(tm_ctx* c, const void* a, const void* b, int N, int ld,
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool inc = dir == TM_INCOMING;
   if (dtype == TM_BF16)
-    return run_contract_bf16(c, reinterpret_cast<const __nv_bfloat16*>(a), reinterpret_cast<const __nv_bfloat16*>(b),
-                             N, ld, inc, i0, j0, bi, bj, x, ldx, x16 ? X_F16 : X_F32, x16 ? x16_exponent(c, N) : 0, s,
-                             nullptr);
+    return run_contract_bf16(c, a, b, N, ld, inc, i0, j0, bi, bj, x, ldx, x16 ? X_F16 : X_F32,
+                             x16 ? x16_exponent(c, N) : 0, s, nullptr);
   cudaError_t e = timed(c, 3, (long long)c->c_h * bi * bj, s, [&] {
     return launch_contract_f32(inc, reinterpret_cast<const float*>(a), reinterpret_cast<const float*>(b), N, ld,
                                c->c_h, i0, j0, bi, bj, reinterpret_cast<float*>(x), ldx, (long long)bi * ldx, s);

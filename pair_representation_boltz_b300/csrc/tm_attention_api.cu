@@ -2,8 +2,10 @@
 // include/tm.h): the layer's weight images, argument checks, the workspace, the tensor maps and the
 // three launches.
 #include <algorithm>
+#include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <vector>
 
 #include "tm_internal.h"
 
@@ -39,15 +41,61 @@ tm_status tm_attn_create(int c_z, int heads, int c_head, const tm_attn_weights* 
   }
   std::memset(c->status_h, 0, 64);
   cudaHostGetDevicePointer(reinterpret_cast<void**>(&c->status_d), c->status_h, 0);
-  // bf16 tile images of W_q, W_k, W_v, W_g, W_o, then gamma, beta, W_b as float32
+  // Every intermediate of the path is stored as fp16 (normal values 2^-14 .. 65504). The weights bound
+  // each one for any input: with zh = gamma (z - mu) rstd + beta and ||(z - mu) rstd|| <= sqrt(c_z),
+  // |zh_k| <= sqrt(c_z) |gamma_k| + |beta_k| and |(W zh)_c| <= sqrt(c_z) ||W[c] diag(gamma)|| + |(W beta)_c|.
+  // zh and v are stored times powers of two 2^sz, 2^sv that put those bounds near 2^14 (o, a gated
+  // average of v, shares v's); the products undo the scales in their epilogues, exactly. q (which
+  // carries log2(e)/sqrt(c)), k and the bias (times log2(e)) set the logits, whose error is absolute,
+  // and are stored unscaled: weights that could push them past 2^15 are refused.
+  const double kLog2e = 1.4426950408889634, kQ = kLog2e / std::sqrt(32.0);
+  int sz = 0, sv = 0;
+  {
+    double zb = 0;
+    for (int k = 0; k < kC; ++k) zb = std::max(zb, std::sqrt((double)kC) * std::fabs((double)w->ln_gamma[k]) +
+                                                       std::fabs((double)w->ln_beta[k]));
+    auto bound = [&](const float* W, int rows) {
+      double mx = 0;
+      for (int r = 0; r < rows; ++r) {
+        double n2 = 0, b = 0;
+        for (int k = 0; k < kC; ++k) {
+          const double v = (double)W[(size_t)r * kC + k];
+          n2 += v * v * (double)w->ln_gamma[k] * (double)w->ln_gamma[k];
+          b += v * (double)w->ln_beta[k];
+        }
+        mx = std::max(mx, std::sqrt((double)kC * n2) + std::fabs(b));
+      }
+      return mx;
+    };
+    const double lim = 32768.0;
+    const double bq = kQ * bound(w->w_q, kC), bk = bound(w->w_k, kC), bv = bound(w->w_v, kC),
+                 bb = kLog2e * bound(w->w_b, 4);
+    if (!(bq < lim && bk < lim && bb < lim) || !std::isfinite(zb) || !std::isfinite(bv)) {
+      tm_destroy(c);
+      return TM_ERR_UNSUPPORTED;
+    }
+    auto expo = [](double b) { return b > 0 ? std::min(60, std::max(-60, 14 - (int)std::ceil(std::log2(b)))) : 0; };
+    sz = expo(zb);
+    sv = expo(bv);
+  }
   const size_t T = (size_t)kC * kC;
-  std::vector<__nv_bfloat16> img(5 * T);
+  std::vector<__half> img(5 * T);
   const float* mats[5] = {w->w_q, w->w_k, w->w_v, w->w_g, w->w_o};
-  for (int m = 0; m < 5; ++m) make_tile_image(mats[m], img.data() + m * T);
+  for (int m = 0; m < 5; ++m) {
+    const int ex = fp16_image_exponent(mats[m]);
+    make_tile_image_h(mats[m], std::ldexp(1.0, ex), img.data() + m * T);
+    if (m < 4) {
+      const double sc = std::ldexp(1.0, -ex - sz + (m == 2 ? sv : 0));
+      c->ta_wscale[m] = (float)(m == 0 ? sc * kQ : sc);
+    } else {
+      c->ta_oscale = (float)std::ldexp(1.0, -ex - sv);
+    }
+  }
+  c->ta_bscale = (float)(kLog2e * std::ldexp(1.0, -sz));
   std::vector<float> f(2 * kC + 4 * kC);
   for (int k = 0; k < kC; ++k) {
-    f[k] = w->ln_gamma[k];
-    f[kC + k] = w->ln_beta[k];
+    f[k] = (float)std::ldexp((double)w->ln_gamma[k], sz);
+    f[kC + k] = (float)std::ldexp((double)w->ln_beta[k], sz);
   }
   for (int k = 0; k < 4 * kC; ++k) f[2 * kC + k] = w->w_b[k];
   const size_t ib = img.size() * sizeof(img[0]);
@@ -98,13 +146,13 @@ tm_status tm_attn_forward(tm_ctx* c, const void* z, const float* mask, int N, tm
   st = ensure_workspace(c, 4 * pb + vb + bb, s, opt);
   if (st != TM_OK) return st;
   uint8_t* q8 = reinterpret_cast<uint8_t*>(c->ws);
-  auto* q = reinterpret_cast<__nv_bfloat16*>(q8);
-  auto* k = reinterpret_cast<__nv_bfloat16*>(q8 + pb);
-  auto* g = reinterpret_cast<__nv_bfloat16*>(q8 + 2 * pb);
-  auto* o = reinterpret_cast<__nv_bfloat16*>(q8 + 3 * pb);
-  auto* vt = reinterpret_cast<__nv_bfloat16*>(q8 + 4 * pb);
-  auto* bias = reinterpret_cast<__nv_bfloat16*>(q8 + 4 * pb + vb);
-  const auto* wimg = reinterpret_cast<const __nv_bfloat16*>(c->ta_w);
+  auto* q = reinterpret_cast<__half*>(q8);
+  auto* k = reinterpret_cast<__half*>(q8 + pb);
+  auto* g = reinterpret_cast<__half*>(q8 + 2 * pb);
+  auto* o = reinterpret_cast<__half*>(q8 + 3 * pb);
+  auto* vt = reinterpret_cast<__half*>(q8 + 4 * pb);
+  auto* bias = reinterpret_cast<__half*>(q8 + 4 * pb + vb);
+  const auto* wimg = reinterpret_cast<const __half*>(c->ta_w);
   const float* wf = reinterpret_cast<const float*>(wimg + 5 * kC * kC);
   const long long tiles = (P + 127) / 128;
   const int grid = (int)std::min<long long>(tiles, c->num_sms);
@@ -119,6 +167,8 @@ tm_status tm_attn_forward(tm_ctx* c, const void* z, const float* mask, int N, tm
   pp.w_k = wimg + kC * kC;
   pp.w_v = wimg + 2 * kC * kC;
   pp.w_g = wimg + 3 * kC * kC;
+  for (int m = 0; m < 4; ++m) pp.wscale[m] = c->ta_wscale[m];
+  pp.bscale = c->ta_bscale;
   pp.q = q;
   pp.k = k;
   pp.g = g;
@@ -137,16 +187,16 @@ tm_status tm_attn_forward(tm_ctx* c, const void* z, const float* mask, int N, tm
   {
     const cuuint64_t d[3] = {(cuuint64_t)kC, (cuuint64_t)N, (cuuint64_t)N};
     const cuuint64_t st2[2] = {(cuuint64_t)kC * 2, (cuuint64_t)N * kC * 2};
-    if (!encode(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, d, st2, kBoxTaQK, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, k, d, st2, kBoxTaQK, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!encode(&qmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, q, d, st2, kBoxTaQK, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode(&kmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, k, d, st2, kBoxTaQK, CU_TENSOR_MAP_SWIZZLE_128B))
       return fail(c, TM_ERR_CUDA, "tensor map (q/k)");
     const cuuint64_t dv[3] = {(cuuint64_t)N, (cuuint64_t)kC, (cuuint64_t)N};
     const cuuint64_t sv[2] = {(cuuint64_t)ldv * 2, (cuuint64_t)kC * ldv * 2};
-    if (!encode(&vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, vt, dv, sv, kBoxTaV, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!encode(&vmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, vt, dv, sv, kBoxTaV, CU_TENSOR_MAP_SWIZZLE_128B))
       return fail(c, TM_ERR_CUDA, "tensor map (v)");
     const cuuint64_t db[3] = {(cuuint64_t)N, (cuuint64_t)N, 4};
     const cuuint64_t sb[2] = {(cuuint64_t)ldb * 2, (cuuint64_t)N * ldb * 2};
-    if (!encode(&bmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, bias, db, sb, kBoxTaBias, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!encode(&bmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, bias, db, sb, kBoxTaBias, CU_TENSOR_MAP_SWIZZLE_128B))
       return fail(c, TM_ERR_CUDA, "tensor map (bias)");
   }
   TaAttendParams pa{};
@@ -162,6 +212,7 @@ tm_status tm_attn_forward(tm_ctx* c, const void* z, const float* mask, int N, tm
   TaOutParams po{};
   po.o = o;
   po.w_o = wimg + 4 * kC * kC;
+  po.oscale = c->ta_oscale;
   po.out = reinterpret_cast<__nv_bfloat16*>(out);
   po.transpose = tr ? 1 : 0;
   po.N = N;

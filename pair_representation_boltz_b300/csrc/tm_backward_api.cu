@@ -1,6 +1,7 @@
 // tm_backward_api.cu -- host side of the backward pass of the triangle multiplicative update
 // (tm_backward in include/tm.h): the workspace of each precision and the schedule of its kernels.
 #include <algorithm>
+#include <cmath>
 
 #include "tm_internal.h"
 
@@ -99,8 +100,8 @@ tm_status backward_f32(tm_ctx* c, const float* z, const float* mask, int N, bool
 tm_status backward_bf16(tm_ctx* c, const void* z, const float* mask, int N, bool inc, const void* dout, void* dz,
                         const tm_grads* g, cudaStream_t s, const tm_options* opt) {
   const long long P = (long long)N * N;
-  const int ld = (int)align_up(N, 64);     // bf16 planes a, b, dX, dX^T: 128-byte rows
-  const int ldx = (int)align_up(N, 32);    // float32 planes x (then dA), dB: 128-byte rows
+  const int ld = (int)align_up(N, 64);     // fp16 planes a, b, dX, dX^T: 128-byte rows
+  const int ldx = (int)align_up(N, 32);    // float32 planes x (then dX, then dA), dB: 128-byte rows
   const long long tiles = (P + 127) / 128;
   const int grid = bwd_grid(tiles, c->num_sms);
   const size_t pb = align_up((size_t)kC * N * ld * 2, 256);
@@ -109,15 +110,15 @@ tm_status backward_bf16(tm_ctx* c, const void* z, const float* mask, int N, bool
   const size_t hb = align_up((size_t)kC * P * 4, 256);
   const size_t wb = align_up((size_t)grid * 2 * kC * kC * 4, 256);
   const size_t lb = align_up((size_t)grid * 2 * kC * 4, 256);
-  tm_status st = ensure_workspace(c, 4 * pb + 2 * xb + zb + hb + 3 * wb + 2 * lb, s, opt);
+  tm_status st = ensure_workspace(c, 4 * pb + 2 * xb + zb + hb + 3 * wb + 2 * lb + 256, s, opt);
   if (st != TM_OK) return st;
   uint8_t* q = reinterpret_cast<uint8_t*>(c->ws);
   auto take = [&](size_t n) { uint8_t* r = q; q += n; return r; };
-  auto* a = reinterpret_cast<__nv_bfloat16*>(take(pb));
-  auto* b = reinterpret_cast<__nv_bfloat16*>(take(pb));
-  auto* dX = reinterpret_cast<__nv_bfloat16*>(take(pb));
-  auto* dXT = reinterpret_cast<__nv_bfloat16*>(take(pb));
-  float* x = reinterpret_cast<float*>(take(xb));     // x, then dA
+  auto* a = reinterpret_cast<__half*>(take(pb));
+  auto* b = reinterpret_cast<__half*>(take(pb));
+  auto* dX = reinterpret_cast<__half*>(take(pb));
+  auto* dXT = reinterpret_cast<__half*>(take(pb));
+  float* x = reinterpret_cast<float*>(take(xb));     // x, then dX (float32), then dA
   float* dB = reinterpret_cast<float*>(take(xb));
   auto* zstat = reinterpret_cast<float2*>(take(zb));
   float* dzh = reinterpret_cast<float*>(take(hb));
@@ -126,13 +127,25 @@ tm_status backward_bf16(tm_ctx* c, const void* z, const float* mask, int N, bool
   float* part_b = reinterpret_cast<float*>(take(wb));
   float* ln_o = reinterpret_cast<float*>(take(lb));
   float* ln_i = reinterpret_cast<float*>(take(lb));
-  const auto* wimg = reinterpret_cast<const __nv_bfloat16*>(c->wbwd);
+  auto* amax = reinterpret_cast<unsigned*>(take(256));   // [0] largest |dout|, [1] largest |dX| (float bits)
+  const auto* wimg = reinterpret_cast<const __half*>(c->wbwd);
   const float* ln4 = reinterpret_cast<const float*>(wimg + 6 * kC * kC);
   auto W = [&](int m) { return wimg + (size_t)m * kC * kC; };   // W_g, W_o, W_a, W_ga, W_b, W_gb
+  auto SW = [&](int m) { return std::ldexp(1.0, c->bwd_wexp[m]); };
 
-  st = run_project_bf16(c, z, mask, N, zstat, a, b, ld, s, opt);
+  // fp16 scales fixed by the weights: a and b (|a_c| <= the bound on |W_a zh|), zh, xh
+  const double sa = pow2_scale_host(c->pv_bound[0], 14), sb = pow2_scale_host(c->pv_bound[1], 14);
+  const double sz = pow2_scale_host(c->zh_bound, 14), sx = pow2_scale_host(c->xh_bound, 14);
+
+  cudaError_t e = cudaMemsetAsync(amax, 0, 256, s);
+  if (e != cudaSuccess) return cuda_fail(c, e, "cudaMemsetAsync(maxima)");
+  e = timed(c, 6, P, s, [&] {
+    return launch_absmax_bf16(reinterpret_cast<const __nv_bfloat16*>(dout), P * kC, amax, c->num_sms, s);
+  });
+  if (e != cudaSuccess) return cuda_fail(c, e, "maximum of dout launch");
+  st = run_project_bf16(c, z, mask, N, zstat, a, b, ld, s, opt, true, (float)sa, (float)sb);
   if (st != TM_OK) return st;
-  st = run_contract_bf16(c, a, b, N, ld, inc, 0, 0, N, N, x, ldx, X_F32, 0, s, opt);
+  st = run_contract_bf16(c, a, b, N, ld, inc, 0, 0, N, N, x, ldx, X_F32, 0, s, opt, true);
   if (st != TM_OK) return st;
 
   BwdOutParams po{};
@@ -141,10 +154,18 @@ tm_status backward_bf16(tm_ctx* c, const void* z, const float* mask, int N, bool
   po.x = x;
   po.ldx = ldx;
   po.xplane = (long long)N * ldx;
+  po.x_unscale = (float)(1.0 / (sa * sb));
   po.dout = reinterpret_cast<const __nv_bfloat16*>(dout);
-  po.dX = dX;
-  po.ld = ld;
-  po.dplane = (long long)N * ld;
+  po.amax = amax;
+  po.y_bound4 = (float)(c->y_bound / 4);
+  po.sz = (float)sz;
+  po.sx = (float)sx;
+  po.u_gg = (float)(1.0 / (SW(0) * sz));
+  po.u_y = (float)(1.0 / (SW(1) * sx));
+  po.u_dxh = (float)(1.0 / SW(1));
+  po.u_dzh = (float)(1.0 / SW(0));
+  po.u_wg = (float)(1.0 / sz);
+  po.u_wo = (float)(1.0 / sx);
   po.dzh = dzh;
   po.part_w = part_o;
   po.part_ln = ln_o;
@@ -155,22 +176,29 @@ tm_status backward_bf16(tm_ctx* c, const void* z, const float* mask, int N, bool
   po.P = P;
   po.tiles = tiles;
   po.w = watch(c, KID_BWD_OUTPUT, opt);
-  cudaError_t e = timed(c, 4, P, s, [&] { return launch_bwd_output_bf16(po, grid, s); });
+  e = timed(c, 4, P, s, [&] { return launch_bwd_output_bf16(po, grid, s); });
   if (e != cudaSuccess) return cuda_fail(c, e, "output backward launch");
-  e = timed(c, 6, P, s, [&] { return launch_transpose_planes_bf16(dX, dXT, N, ld, kC, s); });
-  if (e != cudaSuccess) return cuda_fail(c, e, "transpose launch");
+  e = timed(c, 6, P, s, [&] { return launch_convert_transpose(x, ldx, amax + 1, dX, dXT, N, ld, kC, s); });
+  if (e != cudaSuccess) return cuda_fail(c, e, "dX conversion launch");
 
-  float* dA = x;   // x is dead once the output backward has run
+  float* dA = x;   // the float32 dX is dead once converted
   if (!inc) {
-    st = run_contract_bf16(c, dXT, b, N, ld, true, 0, 0, N, N, dA, ldx, X_F32, 0, s, opt);
-    if (st == TM_OK) st = run_contract_bf16(c, dX, a, N, ld, true, 0, 0, N, N, dB, ldx, X_F32, 0, s, opt);
+    st = run_contract_bf16(c, dXT, b, N, ld, true, 0, 0, N, N, dA, ldx, X_F32, 0, s, opt, true);
+    if (st == TM_OK) st = run_contract_bf16(c, dX, a, N, ld, true, 0, 0, N, N, dB, ldx, X_F32, 0, s, opt, true);
   } else {
-    st = run_contract_bf16(c, b, dX, N, ld, false, 0, 0, N, N, dA, ldx, X_F32, 0, s, opt);
-    if (st == TM_OK) st = run_contract_bf16(c, a, dXT, N, ld, false, 0, 0, N, N, dB, ldx, X_F32, 0, s, opt);
+    st = run_contract_bf16(c, b, dX, N, ld, false, 0, 0, N, N, dA, ldx, X_F32, 0, s, opt, true);
+    if (st == TM_OK) st = run_contract_bf16(c, a, dXT, N, ld, false, 0, 0, N, N, dB, ldx, X_F32, 0, s, opt, true);
   }
   if (st != TM_OK) return st;
 
   for (int side = 0; side < 2; ++side) {
+    // dA = (dX sx)(b sb) / (sx sb): dV carries dX's scale (device) and its partner's (sb for dA, sa for dB).
+    // |dV raw| <= N 2^14 2^14 (both fp16 operands below 2^14), so q1 = 2^(14 - 28 - ceil(log2 N)) keeps
+    // dpv's fp16 values below 2^14; dpg also carries |pv| <= the bound and sigmoid' <= 1/4.
+    const double sp = side == 0 ? sb : sa;
+    const double raw = (double)N * 16384.0 * 16384.0;
+    const double q1 = pow2_scale_host(raw, 14), q2 = pow2_scale_host(raw * c->pv_bound[side] / 4, 14);
+    const double swv = SW(2 + 2 * side), swg = SW(3 + 2 * side);
     BwdProjParams pp{};
     pp.z = po.z;
     pp.zstat = zstat;
@@ -178,6 +206,16 @@ tm_status backward_bf16(tm_ctx* c, const void* z, const float* mask, int N, bool
     pp.dV = side == 0 ? dA : dB;
     pp.ldv = ldx;
     pp.vplane = (long long)N * ldx;
+    pp.amax = amax;
+    pp.sz = (float)sz;
+    pp.u_pv = (float)(1.0 / (swv * sz));
+    pp.u_pg = (float)(1.0 / (swg * sz));
+    pp.q1 = (float)q1;
+    pp.q2 = (float)q2;
+    pp.u_dzh_v = (float)(1.0 / (swv * sp * q1));
+    pp.u_dzh_g = (float)(1.0 / (swg * sp * q2));
+    pp.u_wv = (float)(1.0 / (sp * q1 * sz));
+    pp.u_wgt = (float)(1.0 / (sp * q2 * sz));
     pp.dzh = dzh;
     pp.dz = reinterpret_cast<__nv_bfloat16*>(dz);
     pp.final_pass = side;

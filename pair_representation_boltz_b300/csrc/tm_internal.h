@@ -49,11 +49,20 @@ struct tm_ctx {
   double ab_bound = 0;           // max_c of the bounds on |a_c| and |b_c| multiplied (fp16 x scale)
   float inv_scale_o = 1.f;
   CUtensorMap wk1_map, wo_map, wg_map;
-  // backward pass: bf16 images of W_g, W_o, W_a, W_ga, W_b, W_gb in the 128 x 128 operand-tile layout
-  // of the backward kernels, then gamma_in, beta_in, gamma_out, beta_out (float32)
+  // backward pass: fp16 images of W_g, W_o, W_a, W_ga, W_b, W_gb (times 2^bwd_wexp[m]) in the
+  // 128 x 128 operand-tile layout of the backward kernels, then gamma_in, beta_in, gamma_out, beta_out
+  // (float32); bounds on |W_a zh|, |W_b zh| (pv_bound), |zh|, |xh| and |W_o xh| that fix the fp16
+  // scales of the backward's operands
   void* wbwd = nullptr;
-  // triangle attention: bf16 images of W_q, W_k, W_v, W_g, W_o, then gamma, beta and W_b (float32)
+  int bwd_wexp[6] = {};
+  double pv_bound[2] = {}, zh_bound = 0, xh_bound = 0, y_bound = 0;
+  // triangle attention: fp16 images of W_q, W_k, W_v, W_g, W_o (each scaled by a power of two), then
+  // gamma and beta (times the power of two zh is stored with) and W_b (float32); the factors that undo
+  // the scales
   void* ta_w = nullptr;
+  float ta_wscale[4] = {1.f, 1.f, 1.f, 1.f};
+  float ta_oscale = 1.f;
+  float ta_bscale = 1.f;
   // status word (mapped host memory)
   int* status_h = nullptr;
   int* status_d = nullptr;
@@ -86,11 +95,19 @@ size_t limit_of(const tm_ctx* c, const tm_options* opt);
 tm_status ensure_workspace(tm_ctx* c, size_t bytes, cudaStream_t s, const tm_options* opt);
 bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb);
 void make_tile_image(const float* W, __nv_bfloat16* img);
-tm_status run_project_bf16(tm_ctx* c, const void* z, const float* mask, int N, float2* zstat, __nv_bfloat16* a,
-                           __nv_bfloat16* b, int ld, cudaStream_t s, const tm_options* opt);
-tm_status run_contract_bf16(tm_ctx* c, const __nv_bfloat16* a, const __nv_bfloat16* b, int N, int ld, bool incoming,
+void make_tile_image_h(const float* W, double scale, __half* img);
+int fp16_image_exponent(const float* W);
+// out_f16: a and b leave as fp16 of their bf16 values times scale_a, scale_b (powers of two), for the
+// backward pass; ab_f16: the contraction's operands are such fp16 planes.
+tm_status run_project_bf16(tm_ctx* c, const void* z, const float* mask, int N, float2* zstat, void* a,
+                           void* b, int ld, cudaStream_t s, const tm_options* opt, bool out_f16 = false,
+                           float scale_a = 1.f, float scale_b = 1.f);
+tm_status run_contract_bf16(tm_ctx* c, const void* a, const void* b, int N, int ld, bool incoming,
                             int i0, int j0, int bi, int bj, void* x, int ldx, XFormat xf, int x_exp,
-                            cudaStream_t s, const tm_options* opt);
+                            cudaStream_t s, const tm_options* opt, bool ab_f16 = false);
+// 2^(target - E) for the exponent E with 2^(E-1) <= bound < 2^E (bound > 0), else 1: the power of two
+// that keeps values bounded by `bound` below 2^target.
+double pow2_scale_host(double bound, int target);
 tm_status run_finish_bf16(tm_ctx* c, const void* x, int ldx, XFormat xf, int x_exp, const float2* zstat, const void* z, int N,
                           int i0, int j0, int bi, int bj, void* out, bool residual, cudaStream_t s,
                           const tm_options* opt);

@@ -24,6 +24,8 @@ struct ProjectParams {
   int N, ld;
   int tiles_per_row;      // ceil(N / 128)
   long long total_tiles;  // N * tiles_per_row
+  int out_f16;            // 1: a, b stored as fp16 of their bf16 values times out_scale[half] (backward)
+  float out_scale[2];
   Watch w;
 };
 
@@ -48,6 +50,7 @@ struct ContractParams {
   int last_n;             // MMA N of the last tile column: the columns it still has to cover, rounded up to 16
   int x_f16;              // 1: x is stored fp16, scaled by 2^x_exp
   int x_exp;
+  int ab_f16;             // 1: a and b are fp16 (the backward pass's operands), else bf16
   int tma_store;          // 1: x leaves through TMA stores (needs i0, j0 multiples of 8); 0: direct stores
   Watch w;
 };
@@ -145,19 +148,27 @@ cudaError_t launch_outer_sum_f32(const float* U, const float* V, int O, int K, l
                                  float* out, cudaStream_t s);
 
 // Backward pass, bf16 tensor-core path (k_backward.cu). Pairs are taken in tiles of 128 consecutive
-// entries of the flattened grid (p = i * N + j); per-pair vectors are channel-major [128][N * N].
+// entries of the flattened grid (p = i * N + j); per-pair vectors are channel-major [128][N * N]. Every
+// tensor-core operand is fp16, stored times a power of two; the u_* factors undo, in each product's
+// epilogue, the scales its operands carry (the host's part; a part set by a recorded maximum, amax, is
+// computed on the device).
 struct BwdOutParams {
   const __nv_bfloat16* z;         // [N][N][128]
   const float2* zstat;            // [N][N] (rstd, -rstd mu) of LayerNorm_in (projection kernel)
-  const float* x;                 // [128][N][ldx] float32 (contraction kernel)
+  float* x;                       // [128][N][ldx] float32: the contraction's x times 1 / x_unscale in,
+                                  // dL/dx out (in place)
   long long ldx, xplane;          // row and channel strides of x
+  float x_unscale;
   const __nv_bfloat16* dout;      // [N][N][128]
-  __nv_bfloat16* dX;              // [128][N][ld] dL/dx
-  long long ld, dplane;
+  unsigned* amax;                 // [0] largest |dout| (read), [1] largest |dX| (merged in), float bits
+  float y_bound4;                 // bound on |W_o xh| / 4 (dgg's scale)
+  float sz, sx;                   // zh, xh are stored times sz, sx
+  float u_gg, u_y;                // gg = MMA * u_gg, y = MMA * u_y
+  float u_dxh, u_dzh, u_wg, u_wo; // dxh, dzh_g, dW_g, dW_o: host parts of the unscale
   float* dzh;                     // [128][N*N] written: the gate's term of dL/dzh
   float* part_w;                  // [grid][2][128][128] per-CTA sums of dW_g, dW_o
   float* part_ln;                 // [grid][256] per-CTA sums of d(gamma_out), d(beta_out)
-  const __nv_bfloat16 *w_g, *w_o; // bf16 weight images in the 128-byte-swizzled tile layout
+  const __half *w_g, *w_o;        // fp16 weight images (times powers of two) in the swizzled tile layout
   const float* ln;                // gamma_in, beta_in, gamma_out, beta_out (float32, 4 x 128)
   int N;
   long long P, tiles;
@@ -167,14 +178,19 @@ struct BwdProjParams {
   const __nv_bfloat16* z;
   const float2* zstat;
   const float* mask;              // [N] or nullptr
-  const float* dV;                // [128][N][ldv] float32: dL/da or dL/db
+  const float* dV;                // [128][N][ldv] float32: dL/da or dL/db times (dX's scale x partner's)
   long long ldv, vplane;
+  const unsigned* amax;           // [1]: largest |dX| (float bits), which fixes dX's scale
+  float sz;                       // zh is stored times sz
+  float u_pv, u_pg;               // pv = MMA * u_pv, pg = MMA * u_pg
+  float q1, q2;                   // dpv, dpg stored times dV's scale x q1, q2
+  float u_dzh_v, u_dzh_g, u_wv, u_wgt;   // host parts of the unscales of the W^T products and dW
   float* dzh;                     // [128][N*N], accumulated
   __nv_bfloat16* dz;              // [N][N][128] (final pass)
   int final_pass;                 // 1: add this side's term, then LayerNorm_in backward into dz
   float* part_w;                  // [grid][2][128][128] per-CTA sums of dW_v, dW_gt
   float* part_ln;                 // [grid][256] per-CTA sums of d(gamma_in), d(beta_in) (final pass)
-  const __nv_bfloat16 *w_v, *w_gt;
+  const __half *w_v, *w_gt;
   const float* ln;                // gamma_in, beta_in
   int N;
   long long P, tiles;
@@ -183,8 +199,12 @@ struct BwdProjParams {
 int bwd_grid(long long tiles, int num_sms);
 cudaError_t launch_bwd_output_bf16(const BwdOutParams& p, int grid, cudaStream_t s);
 cudaError_t launch_bwd_project_bf16(const BwdProjParams& p, int grid, cudaStream_t s);
-cudaError_t launch_transpose_planes_bf16(const __nv_bfloat16* in, __nv_bfloat16* out, int N, long long ld, int planes,
-                                         cudaStream_t s);
+// fp16 dX and dX^T planes [planes][N][ld] from the float32 dX planes [planes][N][ldx], times the power of
+// two set by the recorded maximum *amax
+cudaError_t launch_convert_transpose(const float* in, long long ldx, const unsigned* amax, __half* out, __half* outT,
+                                    int N, long long ld, int planes, cudaStream_t s);
+// *out = max(*out, bits of the largest |v|) over n bf16 values
+cudaError_t launch_absmax_bf16(const __nv_bfloat16* v, long long n, unsigned* out, int num_sms, cudaStream_t s);
 // out[e] = sum over q < S of part[q * stride + e], e < E, in order q = 0, 1, ...
 cudaError_t launch_sum_parts(const float* part, int S, long long E, long long stride, float* out, cudaStream_t s);
 // The same for up to 10 jobs in one launch (a job whose out is nullptr is skipped).
@@ -196,18 +216,22 @@ struct SumJobs {
 };
 cudaError_t launch_sum_parts_multi(const SumJobs& j, int S, cudaStream_t s);
 
-// Triangle attention, bf16 tensor-core path (k_attention.cu): c_z = 128, 4 heads of 32. The grid may be
+// Triangle attention, tensor-core path (k_attention.cu): bf16 z and out, fp16 intermediates, c_z = 128,
+// 4 heads of 32. The grid may be
 // the transposed one (ending node): pair (i, j) then reads z at (j, i) and writes out at (j, i).
 struct TaProjectParams {
   const __nv_bfloat16* z;           // [N][N][128]
   const float* mask;                // [N] or nullptr: keys j with mask 0 get a bias of -inf
   int transpose;
-  const float* ln;                  // gamma, beta (float32, 2 x 128)
+  const float* ln;                  // gamma, beta (float32, 2 x 128), both times 2^sz (zh is stored scaled)
   const float* w_b;                 // [4][128] float32
-  const __nv_bfloat16 *w_q, *w_k, *w_v, *w_g;   // bf16 tile images
-  __nv_bfloat16 *q, *k, *g;         // [N][N][128] pair-major
-  __nv_bfloat16* vt;                // [N][128][ldv]: row i, (head, channel), key
-  __nv_bfloat16* b;                 // [4][N][ldb]: head, j, k
+  const __half *w_q, *w_k, *w_v, *w_g;   // fp16 tile images, each scaled by a power of two
+  float wscale[4];                  // per product: undoes the image's and zh's scales; q's also carries
+                                    // log2(e)/sqrt(c), v's the power of two v is stored times
+  float bscale;                     // log2(e) 2^-sz: the bias of the scaled zh in base-2 logit units
+  __half *q, *k, *g;                // [N][N][128] pair-major
+  __half* vt;                       // [N][128][ldv]: row i, (head, channel), key
+  __half* b;                        // [4][N][ldb]: head, j, k (times log2(e); -inf at masked keys)
   long long ldv, ldb;
   int N;
   long long P, tiles;
@@ -215,14 +239,15 @@ struct TaProjectParams {
 };
 struct TaAttendParams {
   const float* mask;                // [N] or nullptr
-  const __nv_bfloat16* g;           // [N][N][128]
-  __nv_bfloat16* o;                 // [N][N][128]: gated attention output of every head
+  const __half* g;                  // [N][N][128]
+  __half* o;                        // [N][N][128]: gated attention output of every head
   int N, jblocks;
   Watch w;
 };
 struct TaOutParams {
-  const __nv_bfloat16* o;
-  const __nv_bfloat16* w_o;         // bf16 tile image of W_o [128][128]
+  const __half* o;
+  const __half* w_o;                // fp16 tile image of W_o [128][128], scaled by a power of two
+  float oscale;                     // undoes that scale and the scale of the stored o (that of v)
   __nv_bfloat16* out;               // [N][N][128]
   int transpose;
   int N;

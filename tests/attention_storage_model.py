@@ -1,14 +1,16 @@
-"""Precision floor of the bf16 triangle attention: the oracle's arithmetic with bf16 rounding at the
-values the bf16 path stores in bf16, against the exact float64 result.
+"""Storage model of the triangle attention path: the oracle's arithmetic with rounding at the values
+the path stores, against the exact float64 result. A diagnostic that the GPU tests log beside the
+path's own error; the parity gates themselves are fixed numbers against the float64 oracle.
 
 A model of the path's storage, not of its code: zh (the operand of the projections), the weights
 W_q, W_k, W_v, W_g, W_o, the stored q (times log2(e)/sqrt(c)), k, v, g and pair bias b (times
-log2(e): the path's softmax runs in base 2), the softmax numerator's weights P
-(a bf16 operand of the P V product, whose extra column of ones also gives the denominator, so both sum
-the rounded weights), the gated output o and
-the result are each rounded once to bf16; everything else is exact.
+log2(e): the path's softmax runs in base 2), the softmax numerator's weights P (an operand of the
+P V product, whose extra column of ones also gives the denominator, so both sum the rounded weights)
+and the gated output o are each rounded once to fp16 (rh), and the result to bf16 (rb); everything
+else is exact. The weight images are scaled by powers of two before their rounding, which leaves the
+relative rounding of every normal value unchanged.
 
-Run as a script to print the floor of the test cases: python -m tests.bf16_attention_floor
+Run as a script to print the model's error for the test cases: python -m tests.attention_storage_model
 """
 from __future__ import annotations
 
@@ -20,7 +22,12 @@ import oracle
 import oracle.triangle_attention as TA
 import workloads as wl
 
-r16 = oracle.round_to_bf16
+rb = oracle.round_to_bf16
+
+
+def rh(v):
+    """Round float64 values to the nearest fp16 value (ties to even), through numpy's float16."""
+    return np.asarray(v, np.float64).astype(np.float16).astype(np.float64)
 
 
 def emulated(z, mask, W, node, heads=4, c=32):
@@ -30,24 +37,24 @@ def emulated(z, mask, W, node, heads=4, c=32):
     N = z.shape[0]
     m = np.asarray(mask, np.float64)
     zh = oracle.layer_norm(z, W["ln_gamma"], W["ln_beta"])
-    zb = r16(zh)
+    zb = rh(zh)
     log2e = 1.0 / math.log(2.0)
-    q = r16((zb @ r16(W["w_q"]).T) * (log2e / math.sqrt(c))).reshape(N, N, heads, c)
-    k = r16(zb @ r16(W["w_k"]).T).reshape(N, N, heads, c)
-    v = r16(zb @ r16(W["w_v"]).T).reshape(N, N, heads, c)
-    g = r16(oracle.sigmoid(zb @ r16(W["w_g"]).T)).reshape(N, N, heads, c)
-    b = r16(np.moveaxis(zh @ W["w_b"].T, -1, 0) * log2e)
+    q = rh((zb @ rh(W["w_q"]).T) * (log2e / math.sqrt(c))).reshape(N, N, heads, c)
+    k = rh(zb @ rh(W["w_k"]).T).reshape(N, N, heads, c)
+    v = rh(zb @ rh(W["w_v"]).T).reshape(N, N, heads, c)
+    g = rh(oracle.sigmoid(zb @ rh(W["w_g"]).T)).reshape(N, N, heads, c)
+    b = rh(np.moveaxis(zh @ W["w_b"].T, -1, 0) * log2e)
     s = np.einsum("ijhc,ikhc->ihjk", q, k) + b[None]            # logits in base 2
     valid = (np.outer(m, m) != 0)[:, None, None, :]
     s = np.where(valid, s, -np.inf)
     smax = np.max(s, axis=-1, keepdims=True)
     smax = np.where(np.isfinite(smax), smax, 0.0)
-    e = r16(np.where(valid, np.exp2(s - smax), 0.0))
+    e = rh(np.where(valid, np.exp2(s - smax), 0.0))
     den = e.sum(axis=-1, keepdims=True)
     num = np.einsum("ihjk,ikhc->ijhc", e, v)
     den = np.moveaxis(den, 1, 2)                               # [i][j][h][1]
-    o = r16(g * np.where(den > 0, num / np.where(den > 0, den, 1.0), 0.0))
-    return r16(o.reshape(N, N, heads * c) @ r16(W["w_o"]).T)
+    o = rh(g * np.where(den > 0, num / np.where(den > 0, den, 1.0), 0.0))
+    return rb(o.reshape(N, N, heads * c) @ rh(W["w_o"]).T)
 
 
 def attention_weights(seed=1):
@@ -61,7 +68,7 @@ def attention_weights(seed=1):
 
 
 def floor(N, mask, node, seed_z, seed_m=12, rms=False):
-    """max|model - exact| / rms(exact) for the inputs of the GPU test case (with rms=True, also
+    """max|model - exact| / rms(exact) for the inputs of a GPU test case (with rms=True, also
     rms(model - exact) / rms(exact))."""
     W = attention_weights()
     z = wl.as_f64(wl.make_z(N, 128, seed_z, "bf16"))
@@ -90,23 +97,23 @@ def emulated_lines(z, mask, W, node, lines, bias, heads=4, c=32):
     N = z.shape[0]
     m = np.asarray(mask, np.float64)
     log2e = 1.0 / math.log(2.0)
-    b = r16(bias * log2e)
+    b = rh(bias * log2e)
     out = np.empty((len(lines), N, W["w_o"].shape[0]))
     for n, i in enumerate(lines):
         zh = oracle.layer_norm(wl.as_f64(np.ascontiguousarray(z[i])), W["ln_gamma"], W["ln_beta"])
-        zb = r16(zh)
-        q = r16((zb @ r16(W["w_q"]).T) * (log2e / math.sqrt(c))).reshape(N, heads, c)
-        k = r16(zb @ r16(W["w_k"]).T).reshape(N, heads, c)
-        v = r16(zb @ r16(W["w_v"]).T).reshape(N, heads, c)
-        g = r16(oracle.sigmoid(zb @ r16(W["w_g"]).T)).reshape(N, heads, c)
+        zb = rh(zh)
+        q = rh((zb @ rh(W["w_q"]).T) * (log2e / math.sqrt(c))).reshape(N, heads, c)
+        k = rh(zb @ rh(W["w_k"]).T).reshape(N, heads, c)
+        v = rh(zb @ rh(W["w_v"]).T).reshape(N, heads, c)
+        g = rh(oracle.sigmoid(zb @ rh(W["w_g"]).T)).reshape(N, heads, c)
         s = np.einsum("jhc,khc->hjk", q, k, optimize=True) + b
         valid = (m[i] * m != 0)[None, None, :]
         s = np.where(valid, s, -np.inf)
         smax = np.max(s, axis=-1, keepdims=True)
         smax = np.where(np.isfinite(smax), smax, 0.0)
-        e = r16(np.where(valid, np.exp2(s - smax), 0.0))
+        e = rh(np.where(valid, np.exp2(s - smax), 0.0))
         den = np.moveaxis(e.sum(axis=-1, keepdims=True), 0, 1)          # [j][h][1]
         num = np.einsum("hjk,khc->jhc", e, v, optimize=True)
-        o = r16(g * np.where(den > 0, num / np.where(den > 0, den, 1.0), 0.0))
-        out[n] = r16(o.reshape(N, heads * c) @ r16(W["w_o"]).T)
+        o = rh(g * np.where(den > 0, num / np.where(den > 0, den, 1.0), 0.0))
+        out[n] = rb(o.reshape(N, heads * c) @ rh(W["w_o"]).T)
     return out

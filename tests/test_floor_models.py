@@ -1,9 +1,10 @@
-"""The bf16 storage models that set the bf16 parity gates are the oracles' arithmetic plus rounding.
+"""The storage models logged beside the GPU paths' errors are the oracles' arithmetic plus rounding.
 
-tests/bf16_backward_floor.py and tests/bf16_attention_floor.py round values to bf16 where the bf16 path
-stores them. With that rounding replaced by the identity each model must reproduce its float64 oracle
-exactly; a slip in a model (a dropped term, a wrong index) would otherwise loosen or tighten the gates
-without notice. With the rounding in place the models must differ from the oracles by a bf16-sized amount.
+tests/backward_storage_model.py and tests/attention_storage_model.py round values where the paths store
+them. With that rounding replaced by the identity each model must reproduce its float64 oracle
+exactly; a slip in a model (a dropped term, a wrong index) would otherwise misreport what the storage
+costs. With the rounding in place the models must differ from the oracles by an amount the size of
+that rounding.
 """
 import math
 
@@ -13,8 +14,8 @@ import pytest
 import oracle
 import oracle.triangle_attention as TA
 import workloads as wl
-from tests import bf16_attention_floor as AF
-from tests import bf16_backward_floor as BF
+from tests import attention_storage_model as AF
+from tests import backward_storage_model as BF
 
 
 def _small_attention_case(N=9, seed=3):
@@ -31,7 +32,8 @@ def _small_attention_case(N=9, seed=3):
 @pytest.mark.parametrize("node", TA.NODES)
 def test_attention_model_without_rounding_is_the_oracle(monkeypatch, node):
     z, m, W = _small_attention_case()
-    monkeypatch.setattr(AF, "r16", lambda v: np.asarray(v, np.float64))
+    monkeypatch.setattr(AF, "rh", lambda v: np.asarray(v, np.float64))
+    monkeypatch.setattr(AF, "rb", lambda v: np.asarray(v, np.float64))
     ref = TA.full(z, m, W, node)
     assert np.max(np.abs(AF.emulated(z, m, W, node) - ref)) < 1e-10
     lines = [0, 2, 8]
@@ -42,11 +44,18 @@ def test_attention_model_without_rounding_is_the_oracle(monkeypatch, node):
 
 
 @pytest.mark.parametrize("node", TA.NODES)
-def test_attention_model_rounding_is_bf16_sized(node):
+def test_attention_model_rounding_is_fp16_sized(monkeypatch, node):
     z, m, W = _small_attention_case()
     ref = TA.full(z, m, W, node)
-    d = np.max(np.abs(AF.emulated(z, m, W, node) - ref)) / np.sqrt(np.mean(ref ** 2))
-    assert 1e-4 < d < 0.1
+    rms = np.sqrt(np.mean(ref ** 2))
+    # the fp16 intermediates alone (result unrounded): errors of order 2^-11
+    monkeypatch.setattr(AF, "rb", lambda v: np.asarray(v, np.float64))
+    d = np.max(np.abs(AF.emulated(z, m, W, node) - ref)) / rms
+    assert 1e-5 < d < 5e-3
+    # fp16 rounding pinned against numpy's own half-precision conversion of exactly representable and
+    # halfway values
+    assert AF.rh(1.0 + 2.0 ** -11) == 1.0 and AF.rh(1.0 + 3 * 2.0 ** -11) == 1.0 + 2.0 ** -9
+    assert AF.rh(65504.0) == 65504.0 and AF.rh(2.0 ** -24) == 2.0 ** -24
 
 
 def test_backward_model_without_rounding_is_the_oracle(monkeypatch):
@@ -56,20 +65,22 @@ def test_backward_model_without_rounding_is_the_oracle(monkeypatch):
     m = wl.make_mask(N, "scatter", 6)
     dout = wl.as_f64(wl.make_z(N, 128, 7, "bf16"))
     ref = oracle.full_backward(z, m, W, "outgoing", dout, storage="bf16")
-    monkeypatch.setattr(BF, "r16", lambda v: np.asarray(v, np.float64))
+    monkeypatch.setattr(BF, "rh", lambda v: np.asarray(v, np.float64))
+    monkeypatch.setattr(BF, "rb", lambda v: np.asarray(v, np.float64))
     got = BF.emulated_backward(z, m, W, "outgoing", dout)
     for k in ref:
         scale = max(np.max(np.abs(ref[k])), 1e-30)
         assert np.max(np.abs(got[k] - ref[k])) / scale < 1e-10, k
 
 
-def test_backward_model_rounding_is_bf16_sized():
+def test_backward_model_rounding_is_fp16_sized(monkeypatch):
     N = 10
     W = wl.make_weights(128, 128, 4, ln_random=True)
     z = wl.as_f64(wl.make_z(N, 128, 5, "bf16"))
     m = wl.make_mask(N, "scatter", 6)
     dout = wl.as_f64(wl.make_z(N, 128, 7, "bf16"))
     ref = oracle.full_backward(z, m, W, "outgoing", dout, storage="bf16")
+    monkeypatch.setattr(BF, "rb", lambda v: np.asarray(v, np.float64))   # dz unrounded: fp16 operands alone
     got = BF.emulated_backward(z, m, W, "outgoing", dout)
     worst = max(np.max(np.abs(got[k] - ref[k])) / np.sqrt(np.mean(ref[k] ** 2)) for k in ref)
-    assert 1e-4 < worst < 0.1
+    assert 1e-5 < worst < 1e-2

@@ -1,11 +1,13 @@
 """Triangle attention through the C ABI (tm_attn_forward) against the float64 oracle.
 
-Metric: max|got - ref| / rms(ref) over the whole grid, ref the exact float64 oracle. The bf16 path
-stores zh, the weights, q, k, v, g, the pair bias, the softmax weights P, the gated output o and the
-result in bf16; tests/bf16_attention_floor.py applies exactly those roundings to the oracle's
-arithmetic and gives the error they alone cause (0.040-0.056 of rms for these cases). The path must
-stay within FLOOR_FACTOR times that floor (plus FLOOR_SLACK) and within ABS_TOL, about twice the
-largest floor; its rms error must stay within FLOOR_FACTOR times the model's rms error.
+The gates are fixed numbers against the exact float64 oracle, the bf16 tolerance of the update read
+the same way (tests/gpu_util.py): the result is stored as bf16, so the half-ulp rounding of each
+output element is not counted, and the error beyond it must stay within BF16_TOL of rms(ref)
+("excess"); rms|delta|/rms(ref) within BF16_TOL; the literal max|delta|/rms(ref) within
+BF16_LITERAL_BOUND. The path keeps every intermediate in fp16 (zh, the weights, q, k, v, g, the
+pair bias, the softmax weights P and the gated output o); tests/attention_storage_model.py, which
+applies exactly those roundings to the oracle's arithmetic, is logged beside the path's error as a
+diagnostic only (it predicts excess ~5e-3 and rms ~2e-3 for these cases).
 """
 import json
 import os
@@ -13,16 +15,23 @@ import os
 import numpy as np
 import pytest
 
+import oracle
 import oracle.triangle_attention as TA
 import workloads as wl
-from tests.bf16_attention_floor import attention_weights, floor as attn_floor
-from tests.gpu_util import mask_to_device, to_f64, z_to_device
+from tests.attention_storage_model import attention_weights, floor as model_error
+from tests.gpu_util import BF16_LITERAL_BOUND, BF16_TOL, mask_to_device, to_f64, z_to_device
 
 pytestmark = pytest.mark.gpu
 
-FLOOR_FACTOR = 1.5
-FLOOR_SLACK = 3e-3
-ABS_TOL = 0.12
+
+def gate(got, ref):
+    """The attention's parity gates; returns the metrics."""
+    e = oracle.errors(got, ref, "bf16")
+    assert np.all(np.isfinite(got))
+    assert e["excess"] <= BF16_TOL, e
+    assert e["rms_rel"] <= BF16_TOL, e
+    assert e["max_rel"] <= BF16_LITERAL_BOUND, e
+    return e
 
 
 @pytest.fixture(scope="module")
@@ -49,19 +58,14 @@ def test_attention_bf16(env, node, N, mask):
     assert tm.tm_sync_status(mod.ctx) == tm.TM_OK
     got = to_f64(out)
     ref = TA.full(wl.as_f64(z_np), m_np, W, node)
-    rms_ref = np.sqrt(np.mean(ref ** 2))
-    err = float(np.max(np.abs(got - ref)) / rms_ref)
-    err_rms = float(np.sqrt(np.mean((got - ref) ** 2)) / rms_ref)
-    fl, fl_rms = attn_floor(N, mask, node, 31 + N, rms=True)
+    fl, fl_rms = model_error(N, mask, node, 31 + N, rms=True)
+    e = oracle.errors(got, ref, "bf16")
     log = os.environ.get("TM_METRICS_LOG")
     if log:
         with open(log, "a") as f:
-            f.write(json.dumps({"test": f"attn_{node}_N{N}_{mask}", "max_rel": err, "floor": fl,
-                                "rms_rel": err_rms, "floor_rms": fl_rms}) + "\n")
-    assert np.all(np.isfinite(got))
-    assert err <= ABS_TOL, (err, fl)
-    assert err <= FLOOR_FACTOR * fl + FLOOR_SLACK, (err, fl)
-    assert err_rms <= FLOOR_FACTOR * fl_rms + 1e-4, (err_rms, fl_rms)
+            f.write(json.dumps({"test": f"attn_{node}_N{N}_{mask}", "max_rel": e["max_rel"], "excess": e["excess"],
+                                "rms_rel": e["rms_rel"], "model_max_rel": fl, "model_rms_rel": fl_rms}) + "\n")
+    gate(got, ref)
     # rows (starting) or columns (ending) of masked tokens have no valid key: exactly 0
     dead = np.flatnonzero(m_np == 0)
     if dead.size:
@@ -101,3 +105,24 @@ def test_attention_refuses_a_workspace_over_the_limit(env):
     mod(z, None, "starting")
     torch.cuda.synchronize()
     assert tm.tm_sync_status(mod.ctx) == tm.TM_OK
+
+
+def test_attention_refuses_weights_that_could_overflow_fp16(env):
+    """Weights whose bound on a stored intermediate exceeds fp16's range are refused at creation."""
+    torch, tm, mod, W = env
+    big = dict(W)
+    big["w_v"] = W["w_v"] * 1e5
+    with pytest.raises(tm.TmError) as err:
+        tm.TriangleAttention(big)
+    assert err.value.status == tm.TM_ERR_UNSUPPORTED
+    small = dict(W)
+    for k in ("w_q", "w_k", "w_v", "w_g", "w_o"):
+        small[k] = W[k] * 2.0 ** -20      # tiny weights keep their precision (power-of-two image scales)
+    att = tm.TriangleAttention(small)
+    try:
+        N = 40
+        z_np = wl.make_z(N, 128, 9, "bf16")
+        got = to_f64(att(z_to_device(z_np), None, "starting"))
+        gate(got, TA.full(wl.as_f64(z_np), np.ones(N), small, "starting"))
+    finally:
+        att.close()

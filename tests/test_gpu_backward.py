@@ -7,13 +7,13 @@ values, with ref the oracle's gradient for the same inputs and cotangent. Bounds
     errs by about sqrt(P) u sum|terms| (u = 2^-24) with independent rounding errors, 3e-6 at
     P = 2304, and at most P u = 1.4e-4 in the worst case. Measured: <= 9.1e-6 on every gradient;
     the bound takes five times that;
-  * bf16 path: the path stores a, b, the six weights, zh, x-hat, dy, dgg, dX, the gate gradients
-    of a and b, and dz in bf16 (8 significant bits). tests/bf16_backward_floor.py models exactly
-    that storage on the oracle's chain rule (each of those values rounded once, everything else
-    exact) and gives the error that storage alone causes: 0.007-0.042 of rms depending on the
-    gradient and the case (the worst is dz, whose own bf16 rounding is half a bf16 step of its
-    largest element). Each gradient must stay within BF16_FLOOR_FACTOR times its modelled floor
-    (plus BF16_FLOOR_SLACK), and every gradient within BF16_GRAD_TOL, twice the worst floor.
+  * bf16 path: fixed gates against the oracle's gradient of the update as the bf16 path defines it
+    (a and b stored as bf16; storage="bf16"), the bf16 tolerance of the update read the same way
+    (tests/gpu_util.py): every parameter gradient (float32) within BF16_TOL in max|delta|/rms, dz
+    (stored as bf16) within BF16_TOL beyond its own bf16 rounding ("excess"), and every gradient
+    within BF16_TOL in rms|delta|/rms. The path's tensor-core operands are fp16;
+    tests/backward_storage_model.py applies those roundings to the oracle's chain rule and is logged
+    beside the path's error as a diagnostic (it predicts <= 5e-3 for these cases).
 """
 import json
 import os
@@ -23,15 +23,12 @@ import pytest
 
 import oracle
 import workloads as wl
-from tests.bf16_backward_floor import floor as bf16_floor
-from tests.gpu_util import mask_to_device, to_f64, z_to_device
+from tests.backward_storage_model import floor as storage_model_error
+from tests.gpu_util import BF16_TOL, mask_to_device, to_f64, z_to_device
 
 pytestmark = pytest.mark.gpu
 
 F32_GRAD_TOL = 5e-5
-BF16_GRAD_TOL = 0.08
-BF16_FLOOR_FACTOR = 1.5
-BF16_FLOOR_SLACK = 3e-3
 
 
 @pytest.fixture(scope="module")
@@ -141,14 +138,23 @@ def test_backward_bf16(torch_tm, direction, N, mask):
     dout = _dout(N, 128, 13 + N, "bf16")
     got = _run(torch, tm, W, 128, 128, z, m, dout, direction, "bf16")
     ref = oracle.full_backward(wl.as_f64(z), m, W, direction, wl.as_f64(dout), storage="bf16")
-    met = _metrics(got, ref)
-    fl = bf16_floor(N, mask, direction, 11 + N, 13 + N)
-    _log(f"bf16_N{N}_{mask}_{direction}", {**met, **{"floor_" + k: v for k, v in fl.items()}})
-    for k, v in got.items():
-        assert np.all(np.isfinite(v)), k
-    assert max(met.values()) <= BF16_GRAD_TOL, met
-    for k in met:
-        assert met[k] <= BF16_FLOOR_FACTOR * fl[k] + BF16_FLOOR_SLACK, (k, met[k], fl[k])
+    met = bf16_gate(got, ref)
+    fl = storage_model_error(N, mask, direction, 11 + N, 13 + N)
+    _log(f"bf16_N{N}_{mask}_{direction}", {**met, **{"model_" + k: v for k, v in fl.items()}})
+
+
+def bf16_gate(got, ref):
+    """The bf16 backward's gates; returns the metrics (per gradient: excess for dz, max_rel for the
+    float32 parameter gradients, and rms_rel)."""
+    met = {}
+    for k, r in ref.items():
+        assert np.all(np.isfinite(got[k])), k
+        e = oracle.errors(got[k], r, "bf16" if k == "z" else None)
+        met[k] = e["excess"]
+        met[k + "_rms"] = e["rms_rel"]
+        assert e["excess"] <= BF16_TOL, (k, e)
+        assert e["rms_rel"] <= BF16_TOL, (k, e)
+    return met
 
 
 def test_backward_bf16_is_deterministic_and_in_place(torch_tm):

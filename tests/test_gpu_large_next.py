@@ -2,8 +2,7 @@
 full mask), in the launch configuration the benchmark times.
 
 * triangle attention: whole output lines (rows of the starting node, columns of the ending node) against
-  the float64 oracle's sampled lines and against the bf16 storage model of the same lines, with the
-  gates of tests/test_gpu_attention.py;
+  the float64 oracle's sampled lines, with the fixed gates of tests/test_gpu_attention.py;
 * backward: the gradient is linear in the cotangent and every stored rounding commutes with a factor
   of two, so tm_backward(2 dout) must equal 2 tm_backward(dout) bit for bit, for dz and every parameter;
   all values finite.
@@ -13,9 +12,9 @@ import pytest
 
 import oracle.triangle_attention as TA
 import workloads as wl
-from tests.bf16_attention_floor import attention_weights, emulated_lines
+from tests.attention_storage_model import attention_weights
 from tests.gpu_util import mask_to_device, to_f64, z_to_device
-from tests.test_gpu_attention import ABS_TOL, FLOOR_FACTOR, FLOOR_SLACK
+from tests.test_gpu_attention import gate
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -53,14 +52,7 @@ def test_attention_complex3605_sampled_lines(big, node):
         mod.close()
     bias = TA.pair_bias(z_np if node == "starting" else np.swapaxes(z_np, 0, 1), W)
     ref = TA.sampled(z_np, m_np, W, node, LINES, bias=bias)
-    model = emulated_lines(z_np, m_np, W, node, LINES, bias)
-    rms = np.sqrt(np.mean(ref ** 2))
-    err, err_rms = np.max(np.abs(got - ref)) / rms, np.sqrt(np.mean((got - ref) ** 2)) / rms
-    fl, fl_rms = np.max(np.abs(model - ref)) / rms, np.sqrt(np.mean((model - ref) ** 2)) / rms
-    assert np.all(np.isfinite(got))
-    assert err <= ABS_TOL, (err, fl)
-    assert err <= FLOOR_FACTOR * fl + FLOOR_SLACK, (err, fl)
-    assert err_rms <= FLOOR_FACTOR * fl_rms + 1e-4, (err_rms, fl_rms)
+    gate(got, ref)
 
 
 @pytest.mark.parametrize("direction", ("outgoing", "incoming"))
