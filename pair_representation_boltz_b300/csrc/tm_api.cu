@@ -327,12 +327,6 @@ tm_status prepare_tensor_core_weights(tm_ctx* c, const tm_weights* w) {
   }
 
   {
-    const cuuint64_t dims[2] = {(cuuint64_t)C, 1024};
-    const cuuint64_t str[1] = {(cuuint64_t)C * 2};
-    if (!encode(&c->wk1_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c->wk1, dims, str, kBoxProjW, CU_TENSOR_MAP_SWIZZLE_128B))
-      return fail(c, TM_ERR_CUDA, "tensor map (projection weights)");
-  }
-  {
     const cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)C};
     const cuuint64_t str[1] = {(cuuint64_t)C * 2};
     if (!encode(&c->wo_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, c->wo16, dims, str, kBoxFinishW, CU_TENSOR_MAP_SWIZZLE_128B))
@@ -377,13 +371,14 @@ tm_status run_project_bf16(tm_ctx* c, const void* z, const float* mask, int N, f
   p.out_scale[1] = scale_b;
   p.mask = mask;
   p.consts = c->k1c;
+  p.w_tc = c->wk1;
   p.zstat = zstat;
   p.N = N;
   p.ld = ld;
   p.tiles_per_row = (N + kProjTileJ - 1) / kProjTileJ;
   p.total_tiles = (long long)N * p.tiles_per_row;
   p.w = watch(c, KID_PROJECT, opt);
-  cudaError_t e = timed(c, 0, (long long)N * N, s, [&] { return launch_project_bf16(zmap, c->wk1_map, amap, bmap, p, c->num_sms, s); });
+  cudaError_t e = timed(c, 0, (long long)N * N, s, [&] { return launch_project_bf16(zmap, amap, bmap, p, c->num_sms, s); });
   return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "projection launch");
 }
 
