@@ -205,6 +205,32 @@ tm_status tm_finish_ex(tm_ctx* ctx, const void* x, int ldx, int x_storage, const
                        const void* z, int N, tm_dtype dtype, int i0, int j0, int bi, int bj,
                        void* out, void* stream);
 
+/* The steps of the update on one block of a pair representation that is split into square blocks
+ * across devices (the 2D tiling of the "2D tiling da pair representation" section of the BioNeMo
+ * context-parallelism page named above; pair_representation_boltz_b300/ring2d.py schedules them). A block
+ * covers B row tokens I and B column tokens K; its token masks differ between rows and columns.
+ *
+ * tm_project_block: a, b of the block: a_ik = sigmoid(W_ga zh_ik) (W_a zh_ik) m_i m_k over i in I, k in K.
+ *   z          device bf16 [B][B][c_z], the block;
+ *   mask_rows  device float32 [B] token mask of I, or NULL (ones);
+ *   mask_cols  device float32 [B] token mask of K, or NULL (ones);
+ *   a, b       device bf16 [c_h][B][ld], ld >= B and a multiple of 8;
+ *   zstat      as for tm_project_ex, or NULL.
+ * TM_BF16 (c_z = c_h = 128) only. */
+tm_status tm_project_block(tm_ctx* ctx, const void* z, const float* mask_rows, const float* mask_cols, int B,
+                           void* a, void* b, int ld, float* zstat, void* stream);
+
+/* The contraction of one pair of B x B operand blocks into a float32 x block:
+ *   TM_OUTGOING  x[c][i][j] (+)= sum_k a[c][i][k] b[c][j][k]
+ *   TM_INCOMING  x[c][i][j] (+)= sum_k a[c][k][i] b[c][k][j]
+ *   a, b        device bf16 [c_h][B][ld] (ld >= B, a multiple of 8);
+ *   x           device float32 [c_h][B][ldx], ldx >= B and a multiple of 4; columns < B are written;
+ *   accumulate  0: x is overwritten; 1: the product is added to x (TMA reduce-add: each sum is formed and
+ *               rounded to float32 where it lands). The blocks of a split grid's k axis are added one
+ *               after another into the same x. */
+tm_status tm_contract_block(tm_ctx* ctx, const void* a, const void* b, int B, int ld, tm_direction dir,
+                            float* x, int ldx, int accumulate, void* stream);
+
 /* Gradients of the layer's parameters: device float32 arrays, each shaped as
  * the tm_weights member of the same name. A NULL member is not written. */
 typedef struct {

@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // them: 256 contiguous bytes per warp)
         if (p.zstat && half == 0 && j < p.N) p.zstat[(size_t)i * p.N + j] = make_float2(rstd, -rstd * mu);
         float m = 0.f;
-        if (j < p.N) m = p.mask ? p.mask[i] * p.mask[j] : 1.0f;
+        if (j < p.N) m = (p.mask ? p.mask[i] : 1.0f) * (p.mask_col ? p.mask_col[j] : 1.0f);
         const unsigned bits = __ballot_sync(0xffffffffu, m != 0.f);
         // the epilogue of two tiles ago has let go of this buffer
         if (!warp_wait_bounded(&sempty[sb], sph ^ 1u, p.w, abort_flag, 18)) break;

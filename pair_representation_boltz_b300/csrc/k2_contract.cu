@@ -265,7 +265,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_3d(&xmap, sbuf, col0, row0, tl.c);
+              if (!X16 && p.accumulate) tma_reduce_add_3d(&xmap, sbuf, col0, row0, tl.c);   // x += product
+              else tma_store_3d(&xmap, sbuf, col0, row0, tl.c);
               bulk_commit();
             }
             sb ^= 1;

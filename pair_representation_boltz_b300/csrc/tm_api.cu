@@ -349,7 +349,7 @@ double pow2_scale_host(double bound, int target) {
 
 tm_status run_project_bf16(tm_ctx* c, const void* z, const float* mask, int N, float2* zstat, void* a,
                            void* b, int ld, cudaStream_t s, const tm_options* opt, bool out_f16, float scale_a,
-                           float scale_b) {
+                           float scale_b, const float* mask_col, bool separate_col_mask) {
   CUtensorMap zmap;
   const cuuint64_t dims[3] = {(cuuint64_t)kC, (cuuint64_t)N, (cuuint64_t)N};
   const cuuint64_t str[2] = {(cuuint64_t)kC * 2, (cuuint64_t)N * kC * 2};
@@ -366,6 +366,7 @@ tm_status run_project_bf16(tm_ctx* c, const void* z, const float* mask, int N, f
   ProjectParams p;
   p.a = reinterpret_cast<__nv_bfloat16*>(a);
   p.b = reinterpret_cast<__nv_bfloat16*>(b);
+  p.mask_col = separate_col_mask ? mask_col : mask;
   p.out_f16 = out_f16 ? 1 : 0;
   p.out_scale[0] = scale_a;
   p.out_scale[1] = scale_b;
@@ -384,7 +385,7 @@ tm_status run_project_bf16(tm_ctx* c, const void* z, const float* mask, int N, f
 
 tm_status run_contract_bf16(tm_ctx* c, const void* a, const void* b, int N, int ld, bool incoming,
                             int i0, int j0, int bi, int bj, void* x, int ldx, XFormat xf, int x_exp,
-                            cudaStream_t s, const tm_options* opt, bool ab_f16) {
+                            cudaStream_t s, const tm_options* opt, bool ab_f16, bool accumulate) {
   CUtensorMap amap, bmap;
   const cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)N, (cuuint64_t)kC};
   const cuuint64_t str[2] = {(cuuint64_t)ld * 2, (cuuint64_t)N * ld * 2};
@@ -400,6 +401,7 @@ tm_status run_contract_bf16(tm_ctx* c, const void* a, const void* b, int N, int 
   ContractParams p;
   p.x = x;
   p.ab_f16 = ab_f16 ? 1 : 0;
+  p.accumulate = accumulate ? 1 : 0;
   p.x_f16 = xf == X_F16 ? 1 : 0;
   p.x_exp = x_exp;
   p.ldx = ldx;
@@ -421,6 +423,8 @@ tm_status run_contract_bf16(tm_ctx* c, const void* a, const void* b, int N, int 
   // TMA stores need every box to start at a non-negative, 16-byte-aligned coordinate: block origins on the
   // 8-element grid give i_base == i0 and j_base == j0, so the tiles start at 0 in the block's own x map.
   p.tma_store = ((i0 & 7) == 0 && (j0 & 7) == 0) ? 1 : 0;
+  if (accumulate && (!p.tma_store || xf != X_F32))
+    return fail(c, TM_ERR_INVALID, "an accumulating contraction needs float32 x and a block on the 8-element grid");
   CUtensorMap xmap;
   {
     const size_t xe = xf == X_F16 ? 2 : 4;
@@ -724,6 +728,35 @@ tm_status tm_finish_ex(tm_ctx* c, const void* x, int ldx, int x_storage, const f
 tm_status tm_finish(tm_ctx* c, const float* x, int ldx, const void* z, int N, tm_dtype dtype, int i0, int j0, int bi,
                     int bj, void* out, void* stream) {
   return tm_finish_ex(c, x, ldx, TM_X_FP32, nullptr, z, N, dtype, i0, j0, bi, bj, out, stream);
+}
+
+tm_status tm_project_block(tm_ctx* c, const void* z, const float* mask_rows, const float* mask_cols, int B, void* a,
+                           void* b, int ld, float* zstat, void* stream) {
+  tm_status st = check_common(c, B, TM_BF16);
+  if (st != TM_OK) return st;
+  if (!z || !a || !b || !aligned16(z) || !aligned16(a) || !aligned16(b))
+    return fail(c, TM_ERR_INVALID, "z, a, b must be non-null and 16-byte aligned");
+  if ((mask_rows && (reinterpret_cast<uintptr_t>(mask_rows) & 3u)) ||
+      (mask_cols && (reinterpret_cast<uintptr_t>(mask_cols) & 3u)))
+    return fail(c, TM_ERR_INVALID, "masks must be 4-byte aligned");
+  if (ld < B || ld % 8) return fail(c, TM_ERR_INVALID, "ld=%d must be >= B and a multiple of 8", ld);
+  if (zstat && (reinterpret_cast<uintptr_t>(zstat) & 7u)) return fail(c, TM_ERR_INVALID, "zstat must be 8-byte aligned");
+  return run_project_bf16(c, z, mask_rows, B, reinterpret_cast<float2*>(zstat), a, b, ld,
+                          reinterpret_cast<cudaStream_t>(stream), nullptr, false, 1.f, 1.f, mask_cols, true);
+}
+
+tm_status tm_contract_block(tm_ctx* c, const void* a, const void* b, int B, int ld, tm_direction dir, float* x,
+                            int ldx, int accumulate, void* stream) {
+  tm_status st = check_common(c, B, TM_BF16);
+  if (st != TM_OK) return st;
+  if (dir != TM_OUTGOING && dir != TM_INCOMING) return fail(c, TM_ERR_INVALID, "unknown direction %d", (int)dir);
+  if (!a || !b || !x || !aligned16(a) || !aligned16(b) || !aligned16(x))
+    return fail(c, TM_ERR_INVALID, "a, b, x must be non-null and 16-byte aligned");
+  if (ld < B || ld % 8) return fail(c, TM_ERR_INVALID, "ld=%d must be >= B and a multiple of 8", ld);
+  if (ldx < B || ldx % 4) return fail(c, TM_ERR_INVALID, "ldx=%d must be >= B and a multiple of 4", ldx);
+  if (accumulate != 0 && accumulate != 1) return fail(c, TM_ERR_INVALID, "accumulate must be 0 or 1");
+  return run_contract_bf16(c, a, b, B, ld, dir == TM_INCOMING, 0, 0, B, B, x, ldx, X_F32, 0,
+                           reinterpret_cast<cudaStream_t>(stream), nullptr, false, accumulate == 1);
 }
 
 tm_status tm_forward_ex(tm_ctx* c, const void* z, const float* mask, int N, tm_dtype dtype, tm_direction dir,

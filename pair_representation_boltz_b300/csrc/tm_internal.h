@@ -99,12 +99,15 @@ void make_tile_image_h(const float* W, double scale, __half* img);
 int fp16_image_exponent(const float* W);
 // out_f16: a and b leave as fp16 of their bf16 values times scale_a, scale_b (powers of two), for the
 // backward pass; ab_f16: the contraction's operands are such fp16 planes.
+// mask_col: the token mask of the columns when it differs from the rows' (a block of a grid split into
+// blocks); by default the grid's own mask serves both.
 tm_status run_project_bf16(tm_ctx* c, const void* z, const float* mask, int N, float2* zstat, void* a,
                            void* b, int ld, cudaStream_t s, const tm_options* opt, bool out_f16 = false,
-                           float scale_a = 1.f, float scale_b = 1.f);
+                           float scale_a = 1.f, float scale_b = 1.f, const float* mask_col = nullptr,
+                           bool separate_col_mask = false);
 tm_status run_contract_bf16(tm_ctx* c, const void* a, const void* b, int N, int ld, bool incoming,
                             int i0, int j0, int bi, int bj, void* x, int ldx, XFormat xf, int x_exp,
-                            cudaStream_t s, const tm_options* opt, bool ab_f16 = false);
+                            cudaStream_t s, const tm_options* opt, bool ab_f16 = false, bool accumulate = false);
 // 2^(target - E) for the exponent E with 2^(E-1) <= bound < 2^E (bound > 0), else 1: the power of two
 // that keeps values bounded by `bound` below 2^target.
 double pow2_scale_host(double bound, int target);

@@ -17,7 +17,8 @@ constexpr int kC = 128;  // channels of z and of the hidden a/b/x on the tensor-
 struct ProjectParams {
   __nv_bfloat16* a;       // [128][N][ld]
   __nv_bfloat16* b;       // [128][N][ld]
-  const float* mask;      // [N] or nullptr
+  const float* mask;      // [N] token mask of the rows i, or nullptr (ones)
+  const float* mask_col;  // [N] token mask of the columns j, or nullptr (ones); the whole grid's is mask
   const float* consts;    // [2 halves][512]: rowsum[256] then bias[256] of the folded LayerNorm
   const __nv_bfloat16* w_tc;  // [2 halves][hi, lo][256][128] bf16: projection rows then gate rows
   float2* zstat;          // [N][N] (rstd, -rstd mu) of LayerNorm_in per pair, written by the a-half CTA
@@ -52,6 +53,7 @@ struct ContractParams {
   int x_f16;              // 1: x is stored fp16, scaled by 2^x_exp
   int x_exp;
   int ab_f16;             // 1: a and b are fp16 (the backward pass's operands), else bf16
+  int accumulate;         // 1: float32 x += the product (TMA reduce-add; needs tma_store), else x = it
   int tma_store;          // 1: x leaves through TMA stores (needs i0, j0 multiples of 8); 0: direct stores
   Watch w;
 };

@@ -9,8 +9,9 @@ GPU every call raises.
 The function names mirror the C ABI: tm_create, tm_forward, tm_forward_ex, tm_forward_host,
 tm_forward_noalloc, tm_pair_update, tm_backward, tm_attn_create, tm_attn_forward,
 tm_project, tm_project_ex, tm_x_exponent, tm_contract, tm_contract_ex, tm_finish, tm_finish_ex,
-tm_sync_status, tm_watchdog_selftest, tm_set_timing, tm_get_timing, tm_launch_count,
-tm_workspace_bytes, tm_ctx_info, tm_status_string, tm_last_error, tm_destroy.
+tm_project_block, tm_contract_block, tm_sync_status, tm_watchdog_selftest, tm_set_timing,
+tm_get_timing, tm_launch_count, tm_workspace_bytes, tm_ctx_info, tm_status_string, tm_last_error,
+tm_destroy.
 
 The C calls see raw pointers only, not the sizes of the buffers behind them, so every wrapper
 checks the tensors it is given (shape, dtype, element count) against the ctx's shape
@@ -101,6 +102,8 @@ def load_library(path: str = LIB_PATH):
         "tm_finish": (st, [vp, vp, i, vp, i, i, i, i, i, i, vp, vp]),
         "tm_finish_ex": (st, [vp, vp, i, i, vp, vp, i, i, i, i, i, i, vp, vp]),
         "tm_ctx_info": (st, [vp, C.POINTER(i), C.POINTER(i), C.POINTER(i)]),
+        "tm_project_block": (st, [vp, vp, vp, vp, i, vp, vp, i, vp, vp]),
+        "tm_contract_block": (st, [vp, vp, vp, i, i, i, vp, i, i, vp]),
         "tm_backward": (st, [vp, vp, vp, i, i, i, vp, vp, C.POINTER(TmGrads), vp, C.POINTER(TmOptions)]),
         "tm_attn_create": (st, [i, i, i, C.POINTER(TmAttnWeights), C.POINTER(vp)]),
         "tm_attn_forward": (st, [vp, vp, vp, i, i, i, vp, vp, C.POINTER(TmOptions)]),
@@ -397,6 +400,33 @@ def tm_finish_ex(ctx, x, ldx, z, i0, j0, bi, bj, out, x_storage="fp16", zstat=No
         check_min_numel("zstat", zstat, 2 * N * N, torch.float32)
     _check(ctx, load_library().tm_finish_ex(ctx, _ptr(x), ldx, X_STORAGE[x_storage], _ptr(zstat), _ptr(z), N,
                                             _dtype_code(z), i0, j0, bi, bj, _ptr(out), _stream(stream)))
+
+
+def tm_project_block(ctx, z, mask_rows, mask_cols, a, b, ld, zstat=None, stream=None):
+    """a, b of one B x B block of a pair representation split into blocks (row and column token masks
+    of the block; None = ones)."""
+    import torch
+    c_z, c_h, _ = _ctx_dims(ctx)
+    B = check_pair_tensor("z", z, c_z)
+    check_mask(mask_rows, B)
+    check_mask(mask_cols, B)
+    for name, t in (("a", a), ("b", b)):
+        check_min_numel(name, t, c_h * B * ld, z.dtype)
+    if zstat is not None:
+        check_min_numel("zstat", zstat, 2 * B * B, torch.float32)
+    _check(ctx, load_library().tm_project_block(ctx, _ptr(z), _ptr(mask_rows), _ptr(mask_cols), B, _ptr(a),
+                                                _ptr(b), ld, _ptr(zstat), _stream(stream)))
+
+
+def tm_contract_block(ctx, a, b, B, ld, direction, x, ldx, accumulate=False, stream=None):
+    """x (+)= the contraction of one pair of B x B operand blocks (float32 x [c_h][B][ldx])."""
+    import torch
+    _, c_h, _ = _ctx_dims(ctx)
+    for name, t in (("a", a), ("b", b)):
+        check_min_numel(name, t, c_h * B * ld, a.dtype)
+    check_min_numel("x", x, c_h * B * ldx, torch.float32)
+    _check(ctx, load_library().tm_contract_block(ctx, _ptr(a), _ptr(b), B, ld, _direction(direction), _ptr(x),
+                                                 ldx, 1 if accumulate else 0, _stream(stream)))
 
 
 def tm_ctx_info(ctx) -> dict:
