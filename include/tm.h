@@ -134,14 +134,21 @@ tm_status tm_pair_update(tm_ctx* ctx, void* z, const float* mask, int N, tm_dtyp
                          const tm_options* opt);
 
 /* tm_forward on HOST buffers: copies z (and mask) host -> device into
- * ctx-owned device buffers, runs the update, and copies out device -> host,
- * all stream-ordered on `stream`; returns after enqueueing (synchronise the
- * stream before reading out).
+ * ctx-owned device buffers, runs the update, and copies out device -> host;
+ * returns after enqueueing (synchronise `stream` before reading out).
  *   z_host     host [N][N][c_z] of dtype (page-locked memory lets the copies
  *              run asynchronously; pageable memory works but blocks);
  *   mask_host  host float32 [N] or NULL;
  *   out_host   host [N][N][c_z] of dtype.
- * The device copies of z and out are owned by the ctx and freed by tm_destroy. */
+ * The copies run on two streams of the ctx, ordered against `stream` by
+ * events: the copy in starts once the previous call's kernels are done with
+ * the device copy of z (it may overlap that call's copy back), the kernels run
+ * on `stream` after it, and for bf16 the output leaves in strips of 512 rows,
+ * each as soon as its rows are finished, while the next strip computes; at the
+ * end `stream` waits for the copy back. z_host must hold its values when the
+ * call is made (a z_host that overlaps the previous call's out_host is copied
+ * after that call's copy back). The device copies of z and out are owned by the
+ * ctx and freed by tm_destroy. */
 tm_status tm_forward_host(tm_ctx* ctx, const void* z_host, const float* mask_host, int N,
                           tm_dtype dtype, tm_direction dir, void* out_host, void* stream);
 

@@ -19,19 +19,12 @@
 //
 // One CTA per SM. CTA parity selects the half it computes (a: W_a | W_ga, or
 // b: W_b | W_gb), so the two CTAs of a pair read each z tile once from HBM and
-// once from L2. The half's four weight matrices (projection and gate, hi and
-// lo) live in TMEM for the whole kernel, as the A operand of every MMA (the
-// channels on the TMEM lanes): the tensor cores then read only the z tile from
-// shared memory, half the bytes per multiply-add of two shared-memory operands,
-// which leaves shared-memory bandwidth for the copies, the statistics and the
-// output staging that share it. Per tile of 128 pairs (one row i, 128
-// consecutive j), in two sub-tiles of 64 pairs:
-//   warp 0      TMA: z tile (two 64-channel boxes, 128-byte swizzle), 4 stages.
-//   warp 1      TMEM (512 columns: the weights in 0..255, two accumulators of
-//               proj + gate x 64 pairs in 256..511) and tcgen05.mma with A in
-//               TMEM: D_proj[c][p] = W'_proj z^T, D_gate[c][p] = W'_gate z^T
-//               (M = 128 channels, N = 64 pairs, K = 16 per instruction), hi +
-//               lo each; sub-tile s of every tile goes to accumulator s.
+// once from L2. Per tile of 128 pairs (one row i, 128 consecutive j):
+//   warp 0      TMA: z tile (two 64-channel boxes, 128-byte swizzle), 2 stages;
+//               the hi and lo weights of the half once at start (128 KB).
+//   warp 1      TMEM (2 x 256 columns) and tcgen05.mma with the channels on
+//               the TMEM lanes: D_proj[c][p] = W'_proj z^T and D_gate[c][p] =
+//               W'_gate z^T (M = 128 channels, N = 128 pairs), hi + lo each.
 //   warps 2..5  LayerNorm statistics, thread = pair: one pass over the z row
 //               (sums of z - z_0 and of its square, fp32x2; the shift by the
 //               row's first value keeps the variance free of cancellation for
@@ -39,53 +32,56 @@
 //               as it is read; one tile ahead of the epilogue, double-buffered
 //               in shared memory behind mbarriers, with the pair mask as one
 //               bit per pair (warp ballot).
-//   warps 6..13 epilogue, thread = channel, two groups of four warps (one warp
-//               per TMEM lane quadrant): group g takes sub-tile g of every
-//               tile, 64 pairs x 32 channels per warp, in chunks of 16 pairs
-//               whose TMEM loads are issued one chunk ahead. Per-channel folding
-//               constants live in registers; two pairs at a time in fp32x2
-//               arithmetic, the two sigmoids with two exponentials and one shared
-//               reciprocal (three MUFU operations), no branch. Results go through
-//               shared memory: each warp fills a 32-channel x 64-pair staging box
-//               (128-byte swizzle, two per warp in turn) that its lane 0 writes
-//               out with one TMA store, so channel rows leave as 128-byte lines
-//               and no warp waits for another. The group-0 warps also load the
-//               weights into TMEM at the start (tcgen05.st, one row per thread).
+//   warps 6..13 epilogue, thread = channel: two warps per TMEM lane quadrant
+//               split the 128 pairs; per-channel folding constants live in
+//               registers; two pairs at a time in fp32x2 arithmetic, the
+//               two sigmoids with two exponentials and one shared reciprocal
+//               (three MUFU operations), no branch. Results go through
+//               shared memory: each warp fills its own 32-channel x 64-pair
+//               staging box (128-byte swizzle) that its lane 0 writes out with
+//               one TMA store per tile, so channel rows leave as 128-byte lines
+//               and no warp waits for another; the store drains while the next
+//               tile's MMA runs. The TMEM loads of each 16-pair chunk are issued
+//               while the chunk before it is computed, and the wait for the last
+//               store to have read the staging box comes after the first chunk's
+//               arithmetic. (Stores straight from the threads, one channel
+//               row per lane, scatter each warp instruction over 32 DRAM pages
+//               and ran 6x slower.)
 #include "tm_kernels.h"
 
 namespace tmk {
 namespace {
 
-constexpr int BM = kProjTileJ;                 // pairs per tile (one z copy)
-constexpr int SUB = BM / 2;                    // pairs per MMA sub-tile
-constexpr int STAGES = 4;
+constexpr int BM = kProjTileJ;                 // pairs per tile
+constexpr int STAGES = 2;
 constexpr int Z_BYTES = BM * kC * 2;           // 32 KB (two 16 KB K-chunks)
+constexpr int W_MAT = kC * kC * 2;             // one 128 x 128 bf16 matrix, two K-chunks: 32 KB
+constexpr int W_BYTES = 4 * W_MAT;             // proj hi, proj lo, gate hi, gate lo
 constexpr int STAT_WARPS = 4, EPI_WARPS = 8;
 constexpr int THREADS = 64 + 32 * (STAT_WARPS + EPI_WARPS);   // TMA, MMA, statistics, epilogue warps
-constexpr int BOX_BYTES = (int)kBoxProjOut.bytes();            // one staging box: 32 channels x 64 pairs
-constexpr int OUT_BYTES = EPI_WARPS * 2 * BOX_BYTES;           // two boxes per epilogue warp
+constexpr int OUT_BYTES = EPI_WARPS * (int)kBoxProjOut.bytes();      // one staging box per epilogue warp
 constexpr int STAT_BUF = (BM / 2) * 16 + 16;   // float4 {rstd_2k, rstd_2k+1, nmu_2k, nmu_2k+1} + 4 mask words
-constexpr int SMEM_BYTES = STAGES * Z_BYTES + OUT_BYTES + 2 * STAT_BUF + 256;
+constexpr int SMEM_BYTES = STAGES * Z_BYTES + W_BYTES + OUT_BYTES + 2 * STAT_BUF + 256;
 constexpr int TMEM_COLS = 512;
-constexpr uint32_t W_COLS = 64;                // one 128 x 128 bf16 matrix as the TMEM A operand
-constexpr uint32_t ACC0 = 4 * W_COLS;          // accumulator s: proj at ACC0 + 128 s, gate 64 columns on
 
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(2 * kBoxProjZ.bytes() == Z_BYTES, "z tile = two boxes");
-static_assert(kBoxProjOut.d0 == SUB && kBoxProjOut.d0 * 2 == 128 && kBoxProjOut.d2 == 32,
-              "a staging box is 32 channel rows of 64 pairs (128 bytes)");
-static_assert(ACC0 + 2 * 2 * SUB == TMEM_COLS, "weights and two accumulators fill TMEM");
+static_assert(2 * kBoxProjW.bytes() == W_MAT, "weight matrix = two boxes");
+static_assert(kBoxProjOut.d0 * 2 == 128 && kBoxProjOut.d2 == 32, "a staging box is 32 channel rows of 128 bytes");
+static_assert(OUT_BYTES == 32768, "staging budget");
 
 // F16OUT: a and b leave as fp16, each value rounded to bf16 first (the storage the update defines)
 // and multiplied by the power of two p.out_scale[half], an exact step that the fp16 form of a
 // normal-range bf16 value keeps exactly: the backward pass's contractions take fp16 operands.
 template <bool F16OUT>
 __global__ void __launch_bounds__(THREADS, 1)
-    k1_project(const __grid_constant__ CUtensorMap zmap, const __grid_constant__ CUtensorMap amap,
-               const __grid_constant__ CUtensorMap bmap, const ProjectParams p) {
+    k1_project(const __grid_constant__ CUtensorMap zmap, const __grid_constant__ CUtensorMap wmap,
+               const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap,
+               const ProjectParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* zs = smem;
-  uint8_t* ostg = smem + STAGES * Z_BYTES;                // [epilogue warp][2][32 channels][128 B], swizzled
+  uint8_t* ws = smem + STAGES * Z_BYTES;                  // [proj hi, proj lo, gate hi, gate lo]
+  uint8_t* ostg = ws + W_BYTES;                           // [epilogue warp][32 channels][128 B], swizzled
   uint8_t* sbase = ostg + OUT_BYTES;                      // [2][STAT_BUF]
   uint64_t* zfull = reinterpret_cast<uint64_t*>(sbase + 2 * STAT_BUF);
   uint64_t* zempty = zfull + STAGES;
@@ -93,8 +89,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* tempty = tfull + 2;
   uint64_t* sfull = tempty + 2;
   uint64_t* sempty = sfull + 2;
-  uint64_t* wready = sempty + 2;
-  uint64_t* fin = wready + 1;
+  uint64_t* wfull = sempty + 2;
+  uint64_t* fin = wfull + 1;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(fin + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
 
@@ -112,11 +108,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], EPI_WARPS / 2);   // the four warps of the group that reads accumulator b
+      mbar_init(&tempty[b], EPI_WARPS);
       mbar_init(&sfull[b], STAT_WARPS);
       mbar_init(&sempty[b], EPI_WARPS);
     }
-    mbar_init(wready, EPI_WARPS / 2);
+    mbar_init(wfull, 1);
     mbar_init(fin, 1);
     fence_mbar_init();
   }
@@ -134,6 +130,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       // ------------------------------------------------------------ TMA producer
       if (lane == 0) {
         tma_prefetch_desc(&zmap);
+        tma_prefetch_desc(&wmap);
+        // weights: rows (half*2 + hl)*256 + {0: projection, 128: gate} of the [2][2][256][128] array
+        mbar_expect_tx(wfull, W_BYTES);
+        for (int m = 0; m < 4; ++m) {
+          const int hl = m & 1, gate = m >> 1;
+          for (int kc = 0; kc < 2; ++kc)
+            tma_load_2d(ws + m * W_MAT + kc * (W_MAT / 2), &wmap, wfull, kc * 64, (half * 2 + hl) * 256 + gate * 128);
+        }
         int s = 0;
         uint32_t ph = 0;
         for (long long u = cta; u < p.total_tiles; u += nctas) {
@@ -153,43 +157,35 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer
       if (lane == 0) {
-        constexpr uint32_t idesc = make_idesc(kC, SUB, FMT_BF16, false, false);
+        constexpr uint32_t idesc = make_idesc(kC, BM, FMT_BF16, false, false);
         int s = 0;
         uint32_t ph = 0;
         int local = 0;
-        if (wait_bounded(wready, 0, p.w, abort_flag, 12)) {
-          tc_fence_after();
+        if (wait_bounded(wfull, 0, p.w, abort_flag, 12)) {
+          const uint32_t w0 = smem_u32(ws);
           for (long long u = cta; u < p.total_tiles; u += nctas, ++local) {
+            const int buf = local & 1;
+            const uint32_t use = (uint32_t)(local >> 1);
+            if (!wait_bounded(&tempty[buf], (use & 1u) ^ 1u, p.w, abort_flag, 13)) break;
             if (!wait_bounded(&zfull[s], ph, p.w, abort_flag, 14)) break;
+            tc_fence_after();
+            const uint32_t d = tmem_base + (uint32_t)(buf * 2 * BM);
             const uint32_t z0 = smem_u32(zs + s * Z_BYTES);
-            bool ok = true;
-#pragma unroll 1
-            for (int sub = 0; sub < 2; ++sub) {
-              if (!wait_bounded(&tempty[sub], ((uint32_t)local & 1u) ^ 1u, p.w, abort_flag, 13)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              const uint32_t d = tmem_base + ACC0 + (uint32_t)(sub * 2 * SUB);
 #pragma unroll
-              for (int kc = 0; kc < 2; ++kc) {
+            for (int kc = 0; kc < 2; ++kc) {
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                  // B: the sub-tile's 64 pair rows (8 KB into each K-chunk), 16 channels at a time;
-                  // A: 8 TMEM columns (16 bf16 channels) of each weight matrix
-                  const uint64_t bd = make_sdesc_sw128(z0 + kc * (Z_BYTES / 2) + sub * (SUB * 128) + ks * 32, 16, 1024);
-                  const uint32_t ka = (uint32_t)(kc * 4 + ks) * 8u;
-                  const uint32_t acc = (kc | ks) != 0;
-                  mma_f16_ts(d, tmem_base + 0 * W_COLS + ka, bd, idesc, acc);
-                  mma_f16_ts(d, tmem_base + 1 * W_COLS + ka, bd, idesc, 1u);
-                  mma_f16_ts(d + SUB, tmem_base + 2 * W_COLS + ka, bd, idesc, acc);
-                  mma_f16_ts(d + SUB, tmem_base + 3 * W_COLS + ka, bd, idesc, 1u);
-                }
+              for (int ks = 0; ks < 4; ++ks) {
+                const uint32_t off = kc * (W_MAT / 2) + ks * 32;
+                const uint64_t bd = make_sdesc_sw128(z0 + kc * (Z_BYTES / 2) + ks * 32, 16, 1024);
+                const uint32_t acc = (kc | ks) != 0;
+                mma_f16(d, make_sdesc_sw128(w0 + 0 * W_MAT + off, 16, 1024), bd, idesc, acc);
+                mma_f16(d, make_sdesc_sw128(w0 + 1 * W_MAT + off, 16, 1024), bd, idesc, 1u);
+                mma_f16(d + BM, make_sdesc_sw128(w0 + 2 * W_MAT + off, 16, 1024), bd, idesc, acc);
+                mma_f16(d + BM, make_sdesc_sw128(w0 + 3 * W_MAT + off, 16, 1024), bd, idesc, 1u);
               }
-              mma_commit(&tfull[sub]);
             }
-            if (!ok) break;
             mma_commit(&zempty[s]);
+            mma_commit(&tfull[buf]);
             if (++s == STAGES) {
               s = 0;
               ph ^= 1u;
@@ -264,64 +260,31 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else {
       // ------------------------------------------------------------ epilogue, thread = channel
       const int ew = warp - 2 - STAT_WARPS;    // 0..7
-      const int grp = ew >> 2;                 // the sub-tile (and accumulator) of every tile it takes
       const int q = warp & 3;                  // TMEM lane quadrant: channels 32q .. 32q+31
       const int c = q * 32 + lane;
-      const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16);
-      if (grp == 0) {
-        // this quadrant's 32 rows of the half's four weight matrices into TMEM, one row per thread:
-        // rows (half * 2 + hl) * 256 + {0: projection, 128: gate} + c of the [2][2][256][128] bf16 array,
-        // two channels per 32-bit column
-#pragma unroll 1
-        for (int m = 0; m < 4; ++m) {
-          const int hl = m & 1, gate = m >> 1;
-          const uint4* src = reinterpret_cast<const uint4*>(p.w_tc + ((size_t)((half * 2 + hl) * 256 + gate * 128 + c)) * kC);
-          uint32_t v[64];
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const uint4 w4 = src[k];
-            v[4 * k] = w4.x;
-            v[4 * k + 1] = w4.y;
-            v[4 * k + 2] = w4.z;
-            v[4 * k + 3] = w4.w;
-          }
-          tmem_st32(trow + (uint32_t)m * W_COLS, v);
-          tmem_st32(trow + (uint32_t)m * W_COLS + 32u, v + 32);
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(wready);
-      }
+      const int pbase = (ew >> 2) * 64;        // this warp's 64 pair columns
       const CUtensorMap* omap = half ? &bmap : &amap;
+      uint8_t* const box = ostg + ew * (int)kBoxProjOut.bytes();
       const float* cst = p.consts + half * 512;
       const float2 rsp = make_float2(cst[c], cst[c]), rsg = make_float2(cst[kC + c], cst[kC + c]);
       const float2 bp = make_float2(cst[256 + c], cst[256 + c]), bg = make_float2(cst[256 + kC + c], cst[256 + kC + c]);
       const float2 one2 = make_float2(1.f, 1.f);
       const float osc = p.out_scale[half];
       if (lane == 0) tma_prefetch_desc(omap);
-      bool prev_stored = true;
       int local = 0;
       for (long long u = cta; u < p.total_tiles; u += nctas, ++local) {
         const int i = (int)(u / p.tiles_per_row);
         const int jt = (int)(u - (long long)i * p.tiles_per_row);
+        const int buf = local & 1;
+        const uint32_t use = (uint32_t)(local >> 1);
         const int sb = local & 1;
-        const uint32_t ph1 = (uint32_t)local & 1u;
         const uint32_t sph = (uint32_t)(local >> 1) & 1u;
         if (!warp_wait_bounded(&sfull[sb], sph, p.w, abort_flag, 19)) break;
-        if (!warp_wait_bounded(&tfull[grp], ph1, p.w, abort_flag, 17)) break;
+        if (!warp_wait_bounded(&tfull[buf], use & 1u, p.w, abort_flag, 17)) break;
         tc_fence_after();
         const float4* st = reinterpret_cast<const float4*>(sbase + sb * STAT_BUF);
         const uint32_t* mw = reinterpret_cast<const uint32_t*>(sbase + sb * STAT_BUF + (BM / 2) * 16);
-        uint8_t* const box = ostg + (ew * 2 + (local & 1)) * BOX_BYTES;
-        // the store that last read this box (two tiles ago) is done with it: when the last tile stored
-        // into the other box, that store may still be reading; when it stored nothing, none may
-        if (lane == 0) {
-          if (prev_stored) bulk_wait_read<1>();
-          else bulk_wait_read<0>();
-        }
-        __syncwarp();
-        const uint32_t ta = trow + ACC0 + (uint32_t)(grp * 2 * SUB);
+        const uint32_t ta = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * 2 * BM + pbase);
         // a, b of pairs p0+e and p0+e+1 for this channel (fp32x2: folded LayerNorm, gate, product)
         auto pair_values = [&](int p0, int e, const uint32_t* pr, const uint32_t* gt) -> float2 {
           const float4 sv = st[(p0 + e) >> 1];          // rstd and -rstd*mu of the two pairs
@@ -347,18 +310,18 @@ __global__ void __launch_bounds__(THREADS, 1)
           const float2 r2 = __bfloat1622float2(__floats2bfloat162_rn(x, y));
           return pack_f16x2(r2.x * osc, r2.y * osc);
         };
-        // four chunks of 16 pairs; the TMEM loads of chunk hh + 1 are in flight while chunk hh is computed
+        // four 16-pair TMEM chunks; the loads of chunk hh + 1 are in flight while chunk hh is computed
         uint32_t pr[2][16], gt[2][16];
         tmem_ld16(ta, pr[0]);
-        tmem_ld16(ta + SUB, gt[0]);
+        tmem_ld16(ta + BM, gt[0]);
 #pragma unroll
         for (int hh = 0; hh < 4; ++hh) {
           tmem_ld_wait();
           if (hh < 3) {
             tmem_ld16(ta + (uint32_t)((hh + 1) * 16), pr[(hh + 1) & 1]);
-            tmem_ld16(ta + SUB + (uint32_t)((hh + 1) * 16), gt[(hh + 1) & 1]);
+            tmem_ld16(ta + BM + (uint32_t)((hh + 1) * 16), gt[(hh + 1) & 1]);
           }
-          const int p0 = grp * SUB + hh * 16;          // first pair of the chunk in the tile
+          const int p0 = pbase + hh * 16;
           const uint32_t mword = mw[p0 >> 5] >> (p0 & 31);
           const uint32_t* prc = pr[hh & 1];
           const uint32_t* gtc = gt[hh & 1];
@@ -377,27 +340,30 @@ __global__ void __launch_bounds__(THREADS, 1)
               packed[e >> 1] = pack(((mword >> e) & 1u) ? v.x : 0.f, ((mword >> (e + 1)) & 1u) ? v.y : 0.f);
             }
           }
+          if (hh == 0) {
+            // the last tile's store has finished reading the staging box (waited for only now, after the
+            // first chunk's arithmetic)
+            if (lane == 0) bulk_wait_read<0>();
+            __syncwarp();
+          }
           // 32 bytes of this channel's 128-byte staging row: 16-byte units 2hh, 2hh+1
 #pragma unroll
           for (int k = 0; k < 2; ++k)
             *reinterpret_cast<uint4*>(box + sw128_offset(lane, hh * 2 + k)) =
                 make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
         }
-        // the accumulator is free for the MMA of the tile after next
+        // the accumulator and the statistics buffer are free (every TMEM load has been waited for)
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[grp]);
         fence_proxy_async_smem();
         __syncwarp();
-        // pairs past N are clipped by TMA (whole 16-byte granules, inside the row padding of ld); a
-        // sub-tile wholly past N is not stored (warp-uniform)
-        prev_stored = jt * BM + grp * SUB < p.N;
         if (lane == 0) {
-          if (prev_stored) {
-            tma_store_3d(omap, box, jt * BM + grp * SUB, i, q * 32);
+          mbar_arrive(&tempty[buf]);
+          mbar_arrive(&sempty[sb]);
+          // pairs past N are clipped by TMA (whole 16-byte granules, inside the row padding of ld)
+          if (jt * BM + pbase < p.N) {
+            tma_store_3d(omap, box, jt * BM + pbase, i, q * 32);
             bulk_commit();
           }
-          mbar_arrive(&sempty[sb]);
         }
       }
       if (lane == 0) bulk_wait_all();   // stores out before the CTA's shared memory goes away
@@ -418,8 +384,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 }  // namespace
 
-cudaError_t launch_project_bf16(const CUtensorMap& zmap, const CUtensorMap& amap, const CUtensorMap& bmap,
-                                const ProjectParams& p, int num_sms, cudaStream_t s) {
+cudaError_t launch_project_bf16(const CUtensorMap& zmap, const CUtensorMap& wmap, const CUtensorMap& amap,
+                                const CUtensorMap& bmap, const ProjectParams& p, int num_sms, cudaStream_t s) {
   static bool attr_set[kMaxDevices] = {};
   cudaError_t e = once_per_device(attr_set, [] {
     cudaError_t r = cudaFuncSetAttribute(k1_project<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
@@ -433,9 +399,9 @@ cudaError_t launch_project_bf16(const CUtensorMap& zmap, const CUtensorMap& amap
   if (pairs > p.total_tiles) pairs = p.total_tiles;
   if (pairs < 1) pairs = 1;
   if (p.out_f16)
-    k1_project<true><<<(int)(2 * pairs), THREADS, SMEM_BYTES, s>>>(zmap, amap, bmap, p);
+    k1_project<true><<<(int)(2 * pairs), THREADS, SMEM_BYTES, s>>>(zmap, wmap, amap, bmap, p);
   else
-    k1_project<false><<<(int)(2 * pairs), THREADS, SMEM_BYTES, s>>>(zmap, amap, bmap, p);
+    k1_project<false><<<(int)(2 * pairs), THREADS, SMEM_BYTES, s>>>(zmap, wmap, amap, bmap, p);
   return cudaGetLastError();
 }
 

@@ -327,6 +327,12 @@ tm_status prepare_tensor_core_weights(tm_ctx* c, const tm_weights* w) {
   }
 
   {
+    const cuuint64_t dims[2] = {(cuuint64_t)C, 1024};
+    const cuuint64_t str[1] = {(cuuint64_t)C * 2};
+    if (!encode(&c->wk1_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c->wk1, dims, str, kBoxProjW, CU_TENSOR_MAP_SWIZZLE_128B))
+      return fail(c, TM_ERR_CUDA, "tensor map (projection weights)");
+  }
+  {
     const cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)C};
     const cuuint64_t str[1] = {(cuuint64_t)C * 2};
     if (!encode(&c->wo_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, c->wo16, dims, str, kBoxFinishW, CU_TENSOR_MAP_SWIZZLE_128B))
@@ -372,14 +378,13 @@ tm_status run_project_bf16(tm_ctx* c, const void* z, const float* mask, int N, f
   p.out_scale[1] = scale_b;
   p.mask = mask;
   p.consts = c->k1c;
-  p.w_tc = c->wk1;
   p.zstat = zstat;
   p.N = N;
   p.ld = ld;
   p.tiles_per_row = (N + kProjTileJ - 1) / kProjTileJ;
   p.total_tiles = (long long)N * p.tiles_per_row;
   p.w = watch(c, KID_PROJECT, opt);
-  cudaError_t e = timed(c, 0, (long long)N * N, s, [&] { return launch_project_bf16(zmap, amap, bmap, p, c->num_sms, s); });
+  cudaError_t e = timed(c, 0, (long long)N * N, s, [&] { return launch_project_bf16(zmap, c->wk1_map, amap, bmap, p, c->num_sms, s); });
   return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "projection launch");
 }
 
@@ -613,6 +618,11 @@ void tm_destroy(tm_ctx* c) {
   cudaDeviceSynchronize();
   if (c->ws) cudaFree(c->ws);
   if (c->io) cudaFree(c->io);
+  if (c->io_in) cudaStreamDestroy(c->io_in);
+  if (c->io_out) cudaStreamDestroy(c->io_out);
+  for (cudaEvent_t ev : {c->ev_zfree, c->ev_in, c->ev_out})
+    if (ev) cudaEventDestroy(ev);
+  for (cudaEvent_t ev : c->ev_strip) cudaEventDestroy(ev);
   for (void* p : {(void*)c->w32, (void*)c->wk1, (void*)c->k1c, (void*)c->wo16, (void*)c->wg16, c->wbwd, c->ta_w})
     if (p) cudaFree(p);
   if (c->status_h) cudaFreeHost(c->status_h);
@@ -868,38 +878,115 @@ tm_status tm_forward_host(tm_ctx* c, const void* z_host, const float* mask_host,
                           tm_direction dir, void* out_host, void* stream) {
   tm_status st = check_common(c, N, dtype);
   if (st != TM_OK) return st;
+  if (dir != TM_OUTGOING && dir != TM_INCOMING) return fail(c, TM_ERR_INVALID, "unknown direction %d", (int)dir);
   if (!z_host || !out_host) return fail(c, TM_ERR_INVALID, "z_host and out_host must be non-null");
   const size_t esz = dtype == TM_BF16 ? 2 : 4;
   const size_t zbytes = (size_t)N * N * c->c_z * esz;
   if (ranges_overlap(z_host, zbytes, out_host, zbytes)) return fail(c, TM_ERR_INVALID, "out_host overlaps z_host");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  // the ctx's copy streams and their events, made on first use
+  if (!c->io_in) {
+    e = cudaStreamCreateWithFlags(&c->io_in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->io_out, cudaStreamNonBlocking);
+    for (cudaEvent_t* ev : {&c->ev_zfree, &c->ev_in, &c->ev_out})
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(c, e, "copy streams");
+  }
   const size_t zb = align_up(zbytes, 256), mb = align_up((size_t)N * 4, 256);
   const size_t need = 2 * zb + mb;
   if (c->io_bytes < need) {
-    if (c->io) {
-      cudaError_t e = cudaFreeAsync(c->io, s);
-      if (e != cudaSuccess) return cuda_fail(c, e, "cudaFreeAsync(io)");
-      c->io = nullptr;
-      c->io_bytes = 0;
-    }
-    cudaError_t e = cudaMallocAsync(&c->io, need, s);
+    // nothing of an earlier call may still use the staging buffers when they are replaced
+    e = cudaStreamSynchronize(c->io_in);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(c->io_out);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess && c->io) e = cudaFree(c->io);
+    if (e != cudaSuccess) return cuda_fail(c, e, "replacing the host-buffer staging");
+    c->io = nullptr;
+    c->io_bytes = 0;
+    e = cudaMalloc(&c->io, need);
     if (e != cudaSuccess) {
       cudaGetLastError();
       c->io = nullptr;
-      return fail(c, TM_ERR_OOM, "cudaMallocAsync(%zu bytes) for host-buffer staging", need);
+      return fail(c, TM_ERR_OOM, "cudaMalloc(%zu bytes) for host-buffer staging", need);
     }
     c->io_bytes = need;
   }
   uint8_t* zd = reinterpret_cast<uint8_t*>(c->io);
   uint8_t* od = zd + zb;
   float* md = mask_host ? reinterpret_cast<float*>(zd + 2 * zb) : nullptr;
-  cudaError_t e = cudaMemcpyAsync(zd, z_host, zbytes, cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess && md) e = cudaMemcpyAsync(md, mask_host, (size_t)N * 4, cudaMemcpyHostToDevice, s);
-  if (e != cudaSuccess) return cuda_fail(c, e, "cudaMemcpyAsync(host to device)");
-  st = tm_forward_ex(c, zd, md, N, dtype, dir, od, stream, nullptr);
+
+  // z (and mask) host -> device on io_in, once the last call's kernels are done with the device copy of
+  // z (and, when this z is that call's output, once its copy back has landed)
+  e = cudaStreamWaitEvent(c->io_in, c->ev_zfree, 0);
+  if (e == cudaSuccess && c->last_out_host && ranges_overlap(z_host, zbytes, c->last_out_host, c->last_out_bytes))
+    e = cudaStreamWaitEvent(c->io_in, c->ev_out, 0);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(zd, z_host, zbytes, cudaMemcpyHostToDevice, c->io_in);
+  if (e == cudaSuccess && md) e = cudaMemcpyAsync(md, mask_host, (size_t)N * 4, cudaMemcpyHostToDevice, c->io_in);
+  if (e == cudaSuccess) e = cudaEventRecord(c->ev_in, c->io_in);
+  // the update on `stream`, after the copy in; what writes the device copy of out also waits for the
+  // last call's copy back, which reads it
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, c->ev_in, 0);
+  if (e != cudaSuccess) return cuda_fail(c, e, "host-to-device copy");
+
+  if (dtype != TM_BF16) {
+    if ((e = cudaStreamWaitEvent(s, c->ev_out, 0)) != cudaSuccess) return cuda_fail(c, e, "event");
+    st = tm_forward_ex(c, zd, md, N, dtype, dir, od, stream, nullptr);
+    if (st != TM_OK) return st;
+    if ((e = cudaEventRecord(c->ev_zfree, s)) != cudaSuccess) return cuda_fail(c, e, "event");
+    e = cudaMemcpyAsync(out_host, od, zbytes, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaEventRecord(c->ev_out, s);
+    return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "device-to-host copy");
+  }
+
+  // bf16: the projection over the whole grid, then strips of kStrip rows (contraction, finish), each
+  // strip's rows of out copied back on io_out while the next strip computes
+  constexpr int kStrip = 512;
+  const int ld = (int)align_up(N, 64);
+  const int R = std::min(N, kStrip);
+  const int ldx = (int)align_up(N, 64);
+  const size_t ab_bytes = align_up((size_t)kC * N * ld * 2, 256);
+  const size_t x_bytes = align_up((size_t)kC * R * ldx * 2, 256);
+  const size_t zst_bytes = align_up((size_t)N * N * sizeof(float2), 256);
+  st = ensure_workspace(c, 2 * ab_bytes + x_bytes + zst_bytes, s, nullptr);
   if (st != TM_OK) return st;
-  e = cudaMemcpyAsync(out_host, od, zbytes, cudaMemcpyDeviceToHost, s);
-  return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "cudaMemcpyAsync(device to host)");
+  uint8_t* base = reinterpret_cast<uint8_t*>(c->ws);
+  void* a = base;
+  void* b = base + ab_bytes;
+  void* x = base + 2 * ab_bytes;
+  float2* zstat = reinterpret_cast<float2*>(base + 2 * ab_bytes + x_bytes);
+  const int x_exp = x16_exponent(c, N);
+  st = run_project_bf16(c, zd, md, N, zstat, a, b, ld, s, nullptr);
+  if (st != TM_OK) return st;
+  const int strips = (N + R - 1) / R;
+  while ((int)c->ev_strip.size() < strips) {
+    cudaEvent_t ev;
+    if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess) return cuda_fail(c, e, "event");
+    c->ev_strip.push_back(ev);
+  }
+  const size_t row_bytes = (size_t)N * kC * 2;
+  for (int k = 0; k < strips; ++k) {
+    const int i0 = k * R, bi = std::min(R, N - i0);
+    st = run_contract_bf16(c, a, b, N, ld, dir == TM_INCOMING, i0, 0, bi, N, x, ldx, X_F16, x_exp, s, nullptr);
+    if (st == TM_OK && k == 0 && (e = cudaStreamWaitEvent(s, c->ev_out, 0)) != cudaSuccess)
+      return cuda_fail(c, e, "event");
+    if (st == TM_OK) st = run_finish_bf16(c, x, ldx, X_F16, x_exp, zstat, zd, N, i0, 0, bi, N, od, false, s, nullptr);
+    if (st != TM_OK) return st;
+    e = cudaEventRecord(c->ev_strip[k], s);
+    if (e == cudaSuccess && k == strips - 1) e = cudaEventRecord(c->ev_zfree, s);   // the last reader of z
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(c->io_out, c->ev_strip[k], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(reinterpret_cast<uint8_t*>(out_host) + (size_t)i0 * row_bytes, od + (size_t)i0 * row_bytes,
+                          (size_t)bi * row_bytes, cudaMemcpyDeviceToHost, c->io_out);
+    if (e != cudaSuccess) return cuda_fail(c, e, "device-to-host copy");
+  }
+  // `stream` waits for the copy back: synchronising it covers out_host
+  e = cudaEventRecord(c->ev_out, c->io_out);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, c->ev_out, 0);
+  if (e != cudaSuccess) return cuda_fail(c, e, "event");
+  c->last_out_host = out_host;
+  c->last_out_bytes = zbytes;
+  return TM_OK;
 }
 
 tm_status tm_sync_status(tm_ctx* c, void* stream) {

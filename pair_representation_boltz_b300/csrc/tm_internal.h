@@ -48,7 +48,7 @@ struct tm_ctx {
   float k3c_host[4 * tmk::kC] = {};  // finish-kernel constants, passed in its parameter block
   double ab_bound = 0;           // max_c of the bounds on |a_c| and |b_c| multiplied (fp16 x scale)
   float inv_scale_o = 1.f;
-  CUtensorMap wo_map, wg_map;
+  CUtensorMap wk1_map, wo_map, wg_map;
   // backward pass: fp16 images of W_g, W_o, W_a, W_ga, W_b, W_gb (times 2^bwd_wexp[m]) in the
   // 128 x 128 operand-tile layout of the backward kernels, then gamma_in, beta_in, gamma_out, beta_out
   // (float32); bounds on |W_a zh|, |W_b zh| (pv_bound), |zh|, |xh| and |W_o xh| that fix the fp16
@@ -71,9 +71,15 @@ struct tm_ctx {
   size_t ws_bytes = 0;
   cudaStream_t ws_stream = nullptr;
   size_t env_limit = 0;
-  // device staging of tm_forward_host
+  // device staging of tm_forward_host, its copy streams and events: z in on io_in, out back on io_out
+  // (row strips, overlapped with the strips still computing and with the next call's copy in)
   void* io = nullptr;
   size_t io_bytes = 0;
+  cudaStream_t io_in = nullptr, io_out = nullptr;
+  cudaEvent_t ev_zfree = nullptr, ev_in = nullptr, ev_out = nullptr;
+  std::vector<cudaEvent_t> ev_strip;
+  const void* last_out_host = nullptr;
+  size_t last_out_bytes = 0;
   // instrumentation
   bool timing = false;
   std::vector<tmh::TimedLaunch> timed;

@@ -20,7 +20,6 @@ struct ProjectParams {
   const float* mask;      // [N] token mask of the rows i, or nullptr (ones)
   const float* mask_col;  // [N] token mask of the columns j, or nullptr (ones); the whole grid's is mask
   const float* consts;    // [2 halves][512]: rowsum[256] then bias[256] of the folded LayerNorm
-  const __nv_bfloat16* w_tc;  // [2 halves][hi, lo][256][128] bf16: projection rows then gate rows
   float2* zstat;          // [N][N] (rstd, -rstd mu) of LayerNorm_in per pair, written by the a-half CTA
                           // for the finish kernel; nullptr: not written
   int N, ld;
@@ -75,8 +74,8 @@ struct FinishParams {
   Watch w;
 };
 
-cudaError_t launch_project_bf16(const CUtensorMap& zmap, const CUtensorMap& amap, const CUtensorMap& bmap,
-                                const ProjectParams& p, int num_sms, cudaStream_t s);
+cudaError_t launch_project_bf16(const CUtensorMap& zmap, const CUtensorMap& wmap, const CUtensorMap& amap,
+                                const CUtensorMap& bmap, const ProjectParams& p, int num_sms, cudaStream_t s);
 cudaError_t launch_contract_bf16(bool incoming, const CUtensorMap& amap, const CUtensorMap& bmap,
                                  const CUtensorMap& xmap, const ContractParams& p, int num_sms, cudaStream_t s);
 // x16 selects the fp16 x tile (kBoxFinishX16, double-buffered) instead of the float32 one.
@@ -99,6 +98,7 @@ struct Box {
   __host__ __device__ constexpr uint32_t bytes() const { return d0 * d1 * d2 * esz; }
 };
 constexpr Box kBoxProjZ{64, (uint32_t)kProjTileJ, 1, 2};              // z tile, one 64-channel half
+constexpr Box kBoxProjW{64, 128, 1, 2};                               // one K-half of a 128 x 128 weight
 constexpr Box kBoxProjOut{64, 1, 32, 2};                              // a or b store: 64 pairs x 32 channels
 constexpr Box kBoxContractOutA{(uint32_t)kContractBK, (uint32_t)kContractBM / 2, 1, 2};   // one CTA's A rows
 constexpr Box kBoxContractOutB{(uint32_t)kContractBK, (uint32_t)kContractBN / 2, 1, 2};   // one CTA's B rows

@@ -107,22 +107,31 @@ def test_attention_refuses_a_workspace_over_the_limit(env):
     assert tm.tm_sync_status(mod.ctx) == tm.TM_OK
 
 
-def test_attention_refuses_weights_that_could_overflow_fp16(env):
-    """Weights whose bound on a stored intermediate exceeds fp16's range are refused at creation."""
+@pytest.mark.parametrize("name", ["w_q", "w_k", "w_b"])
+def test_attention_refuses_logit_weights_that_could_overflow_fp16(env, name):
+    """q, k and the pair bias enter the logits unscaled: weights whose bound on them reaches 2^15 are
+    refused at creation."""
     torch, tm, mod, W = env
     big = dict(W)
-    big["w_v"] = W["w_v"] * 1e5
+    big[name] = W[name] * 1e5
     with pytest.raises(tm.TmError) as err:
         tm.TriangleAttention(big)
     assert err.value.status == tm.TM_ERR_UNSUPPORTED
-    small = dict(W)
-    for k in ("w_q", "w_k", "w_v", "w_g", "w_o"):
-        small[k] = W[k] * 2.0 ** -20      # tiny weights keep their precision (power-of-two image scales)
-    att = tm.TriangleAttention(small)
+
+
+@pytest.mark.parametrize("gain", [1e5, 2.0 ** -20])
+def test_attention_scales_v_and_the_weight_images(env, gain):
+    """v (and o) are stored times a power of two set by the bound on |v|, and every weight image by its
+    own: very large or very small W_v, W_g, W_o meet the same gates."""
+    torch, tm, mod, W = env
+    scaled = dict(W)
+    for k in ("w_v", "w_g", "w_o"):
+        scaled[k] = W[k] * gain
+    att = tm.TriangleAttention(scaled)
     try:
         N = 40
         z_np = wl.make_z(N, 128, 9, "bf16")
         got = to_f64(att(z_to_device(z_np), None, "starting"))
-        gate(got, TA.full(wl.as_f64(z_np), np.ones(N), small, "starting"))
+        gate(got, TA.full(wl.as_f64(z_np), np.ones(N), scaled, "starting"))
     finally:
         att.close()

@@ -64,8 +64,9 @@ def contraction_store_boxes(N, i0, j0, bi, bj):
 def projection_boxes(N):
     for kc in (0, 1):
         yield ("z", kc * 64, 2)
-    # stores of a / b: 64 pairs x 32 channels per box, one per 64-pair sub-tile x four channel quadrants per
-    # tile; a sub-tile wholly past N is not stored
+    for kc in (0, 1):
+        yield ("w", kc * 64, 2)
+    # stores of a / b: 64 pairs x 32 channels per box, two pair-boxes x four channel quadrants per tile
     tiles_per_row = (N + PROJ_J - 1) // PROJ_J
     for jt in range(tiles_per_row):
         for pb in range(0, PROJ_J, 64):
