@@ -199,19 +199,26 @@ static_assert(kBoxTaQK.bytes() == kQBytes && kBoxTaQK.bytes() == kKBytes, "Q/K b
 static_assert(kBoxTaV.bytes() == kVBytes, "v box fills its slot");
 static_assert(kBoxTaBias.bytes() == kBBytes, "bias box fills its slot");
 
+constexpr int kGroups = 2;            // query tiles per CTA, one softmax group each
+constexpr int kStages = 2;            // K, v and bias stages in flight
+constexpr int kAttThreads = 64 + 32 * 4 * kGroups;   // TMA warp, MMA warp, four softmax warps per group
+constexpr uint32_t kStageBytes = kKBytes + kGroups * 2 * kBBytes + 2 * kVBytes;   // what one stage receives
+
 struct alignas(1024) TaAttSmem {
-  uint8_t q[kQBytes];
-  uint8_t k[kKBytes];
-  uint8_t b[2][kBBytes];                        // keys 0..63 and 64..127 of the block
-  uint8_t p[TILE];                              // P: 128 queries x 128 keys, fp16, K-major
-  uint8_t v[2][kVSlot];                         // keys 0..63 and 64..127, rows = channels (+ ones row)
-  float xmax[2][BT];                            // per key half and query: block maximum
-  uint64_t kb_bar, v_bar, s_bar, pv_bar;
+  uint8_t q[kGroups][kQBytes];                  // per group: 64 channels (a head pair) x 128 queries
+  uint8_t k[kStages][kKBytes];                  // 64 channels x 128 keys
+  uint8_t b[kStages][kGroups][2][kBBytes];      // bias: per group, keys 0..63 and 64..127 of the block
+  uint8_t v[kStages][2][kVSlot];                // keys 0..63 and 64..127, rows = channels (+ ones row)
+  uint64_t q_full, q_free, fin;
+  uint64_t kv_full[kStages], kv_empty[kStages];
+  uint64_t s_full[kGroups], s_free[kGroups], p_full[kGroups], pv_done[kGroups];
   uint32_t tmem_slot;
   int abort_flag;
 };
 
-constexpr int kAttThreads = 256;   // two threads per query row, 64 keys of each block each
+// TMEM columns of group g: S (128 keys, float32) at 256 g, P (128 keys as packed fp16 pairs) at
+// 256 g + 128, the P V product (32 channels, the row sum, padding) at 256 g + 192.
+constexpr uint32_t kTmS = 0, kTmP = 128, kTmPV = 192, kTmGroup = 256;
 
 __device__ __forceinline__ float ex2_approx(float v) {
   float r;
@@ -219,7 +226,22 @@ __device__ __forceinline__ float ex2_approx(float v) {
   return r;
 }
 
-__global__ void __launch_bounds__(kAttThreads, 2) k_ta_attend(const __grid_constant__ CUtensorMap qmap,
+// Triangle attention of one CTA: row i of the grid, query tiles 2 jp and 2 jp + 1 (one per softmax
+// group), heads in turn, keys in blocks of 128. Roles:
+//   warp 0        TMA: per block, K (the head pair's 64 channels), the bias tiles of both groups and
+//                 v (with a row of ones beside it) into one of two stages; Q of both groups per head pair.
+//   warp 1        tcgen05.mma: S_g = Q_g K^T into TMEM (M = 128 queries, N = 128 keys, K = 32), then,
+//                 once group g has stored its P into TMEM, O_g = P_g v (A = P from TMEM, B = v from
+//                 shared memory, N = 48: 32 channels, the row sum from the ones row, padding).
+//   warps 2..9    softmax, thread = query row, group g = the four warps of one query tile: S row and
+//                 bias row -> logits (base 2), block maximum with a lazy running reference (the
+//                 reference moves only when the maximum exceeds it by more than 8, so P <= 2^8 stays
+//                 inside fp16 and most blocks need no rescale of the running output), P = 2^(s - m)
+//                 into TMEM as fp16. The running output O (and its row sum) accumulates in TMEM
+//                 across a head's blocks; when the reference moves, the thread rescales its row of O
+//                 once the block before has been added, before this block's P is released. Each
+//                 group's work overlaps the other group's and the tensor core's.
+__global__ void __launch_bounds__(kAttThreads, 1) k_ta_attend(const __grid_constant__ CUtensorMap qmap,
                                                               const __grid_constant__ CUtensorMap kmap,
                                                               const __grid_constant__ CUtensorMap vmap,
                                                               const __grid_constant__ CUtensorMap bmap,
@@ -227,218 +249,262 @@ __global__ void __launch_bounds__(kAttThreads, 2) k_ta_attend(const __grid_const
   extern __shared__ uint8_t smem_raw[];
   TaAttSmem& sm = *reinterpret_cast<TaAttSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int row = 32 * (warp & 3) + lane;      // query row of the block (TMEM lane)
-  const int kh = warp >> 2;                    // key half of every block; output channels 16 kh ..
-  const int i = (int)(blockIdx.x / p.jblocks);
-  const int jb = (int)(blockIdx.x - (long long)i * p.jblocks);
-  const int j = jb * BT + row;
-  const bool jvalid = j < p.N;
-  __half* orow = p.o + ((long long)i * p.N + j) * kC;
+  const int i = (int)(blockIdx.x / p.jpairs);
+  const int jp = (int)(blockIdx.x - (long long)i * p.jpairs);
   if (p.mask && p.mask[i] == 0.f) {
-    // no valid key in this row: o = 0
-    if (jvalid) {
-      uint4* d = reinterpret_cast<uint4*>(orow) + 8 * kh;
-#pragma unroll
-      for (int u = 0; u < 8; ++u) d[u] = make_uint4(0u, 0u, 0u, 0u);
+    // no valid key in this row: o = 0 for every query of both tiles
+    for (int u = tid; u < kGroups * BT * (kC / 8); u += kAttThreads) {
+      const int jq = jp * kGroups * BT + u / (kC / 8);
+      if (jq < p.N) reinterpret_cast<uint4*>(p.o + ((long long)i * p.N + jq) * kC)[u % (kC / 8)] = make_uint4(0u, 0u, 0u, 0u);
     }
     return;
   }
-  const int kblocks = (p.N + BT - 1) / BT;
-  const int total = kHeads * kblocks;          // iterations: heads in order, key blocks within a head
-  // loads of iteration t: K and bias (and Q at the start of a head pair) on kb_bar, v on v_bar
-  auto load_kb = [&](int t) {
-    const int h = t / kblocks, kb = t - h * kblocks;
-    const bool with_q = kb == 0 && (h & 1) == 0;
-    mbar_expect_tx(&sm.kb_bar, kKBytes + 2 * kBBytes + (with_q ? kQBytes : 0u));
-    if (with_q) tma_load_3d(sm.q, &qmap, &sm.kb_bar, 64 * (h >> 1), jb * BT, i);
-    tma_load_3d(sm.k, &kmap, &sm.kb_bar, 64 * (h >> 1), kb * BT, i);
-    tma_load_3d(sm.b[0], &bmap, &sm.kb_bar, kb * BT, jb * BT, h);
-    tma_load_3d(sm.b[1], &bmap, &sm.kb_bar, kb * BT + 64, jb * BT, h);
-  };
-  auto load_v = [&](int t) {
-    const int h = t / kblocks, kb = t - h * kblocks;
-    mbar_expect_tx(&sm.v_bar, 2 * kVBytes);
-    tma_load_3d(sm.v[0], &vmap, &sm.v_bar, kb * BT, kHd * h, i);
-    tma_load_3d(sm.v[1], &vmap, &sm.v_bar, kb * BT + 64, kHd * h, i);
-  };
-  constexpr uint32_t ID_S = make_idesc(128, 128, FMT_F16, false, false);
-  constexpr uint32_t ID_O = make_idesc(128, kPvN, FMT_F16, false, false);
-  auto issue_s = [&](uint32_t tmem, int t) {     // S = Q_h K_h^T (q is stored pre-scaled by log2(e)/sqrt(c))
-    const int hh = (t / kblocks) & 1;
-    const uint32_t q0 = smem_u32(sm.q) + 64 * hh, k0 = smem_u32(sm.k) + 64 * hh;
-#pragma unroll
-    for (int ks = 0; ks < 2; ++ks)
-      mma_f16(tmem, make_sdesc_sw128(q0 + 32 * ks, 16, 1024), make_sdesc_sw128(k0 + 32 * ks, 16, 1024), ID_S,
-              ks ? 1u : 0u);
-    mma_commit(&sm.s_bar);
-  };
+  const int KB = (p.N + BT - 1) / BT;
+  const int T = 4 * KB;                          // iterations: heads in order, key blocks within a head
 
   if (tid == 0) {
-    mbar_init(&sm.kb_bar, 1);
-    mbar_init(&sm.v_bar, 1);
-    mbar_init(&sm.s_bar, 1);
-    mbar_init(&sm.pv_bar, 1);
+    mbar_init(&sm.q_full, 1);
+    mbar_init(&sm.q_free, 1);
+    mbar_init(&sm.fin, 1);
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(&sm.kv_full[st], 1);
+      mbar_init(&sm.kv_empty[st], 1 + 4 * kGroups);   // the MMA's commit + every softmax warp (bias read)
+    }
+    for (int g = 0; g < kGroups; ++g) {
+      mbar_init(&sm.s_full[g], 1);
+      mbar_init(&sm.s_free[g], 4);
+      mbar_init(&sm.p_full[g], 4);
+      mbar_init(&sm.pv_done[g], 1);
+    }
     sm.abort_flag = 0;
     fence_mbar_init();
-    tma_prefetch_desc(&qmap);
-    tma_prefetch_desc(&kmap);
-    tma_prefetch_desc(&vmap);
-    tma_prefetch_desc(&bmap);
-    load_kb(0);
-    load_v(0);
   }
-  if (warp == 0) {
-    tmem_alloc(&sm.tmem_slot, 256);
+  if (warp == 1) {
+    tmem_alloc(&sm.tmem_slot, 512);
     tmem_relinquish();
   }
-  // rows 32..47 of both v slots, which no copy overwrites: a row of ones (the P V product's column 32
-  // is then the row sum of the bf16 P, the softmax denominator) and zeros
-  for (int x = tid; x < 2 * (kVSlot - kVBytes) / 4; x += kAttThreads) {
-    const int half = x / ((kVSlot - kVBytes) / 4), w4 = x % ((kVSlot - kVBytes) / 4);
-    reinterpret_cast<uint32_t*>(sm.v[half] + kVBytes)[w4] = w4 < 32 ? 0x3C003C00u : 0u;   // fp16 1.0 pairs
+  // rows 32..47 of every v slot, which no copy overwrites: a row of ones (the P V product's column 32
+  // is then the row sum of the fp16 P, the softmax denominator) and zeros
+  for (int x = tid; x < kStages * 2 * (int)((kVSlot - kVBytes) / 4); x += kAttThreads) {
+    const int slot = x / (int)((kVSlot - kVBytes) / 4), w4 = x % (int)((kVSlot - kVBytes) / 4);
+    reinterpret_cast<uint32_t*>(sm.v[slot >> 1][slot & 1] + kVBytes)[w4] = w4 < 32 ? 0x3C003C00u : 0u;
   }
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_slot;
-  const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-  uint32_t kph = 0, vph = 0, sph = 0, pph = 0;   // phases (kb/v: thread 0 only)
-  bool ok = true;
-  if (tid == 0) {
-    if (wait_bounded(&sm.kb_bar, kph, p.w, &sm.abort_flag, 1)) {
-      tc_fence_after();
-      issue_s(tmem, 0);
-    }
-    kph ^= 1u;
-  }
+  int* abort_flag = &sm.abort_flag;
 
-  float m_run = -INFINITY, l_run = 0.f;
-  float acc[16];
-  for (int t = 0; t < total; ++t) {
-    const int h = t / kblocks, kb = t - h * kblocks;
-    if (kb == 0) {
-      m_run = -INFINITY;
-      l_run = 0.f;
-#pragma unroll
-      for (int e = 0; e < 16; ++e) acc[e] = 0.f;
-    }
-    if (!cta_wait(&sm.s_bar, sph, p.w, &sm.abort_flag, 2)) { ok = false; break; }
-    sph ^= 1u;
-    tc_fence_after();
-
-    // ---- this thread's 64 logits (log2 domain): S + b, b stored times log2(e) and -inf at masked keys;
-    // keys past the grid (last block only) -> -inf
-    // every thread observes the completion of this block's bias copy before reading it (load t is the
-    // t-th completion of kb_bar; load t + 1 is issued only after all threads are past this point)
-    if (!wait_bounded(&sm.kb_bar, (uint32_t)(t & 1), p.w, &sm.abort_flag, 8)) ok = false;
-    float sv[64];
-    {
-      uint32_t r0[32], r1[32];
-      tmem_ld32(trow + 64 * kh, r0);
-      tmem_ld32(trow + 64 * kh + 32, r1);
-      tmem_ld_wait();
-      const uint8_t* brow = sm.b[kh];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        float bv[8];
-        f16x8_to_float(*reinterpret_cast<const uint4*>(brow + sw128_offset((uint32_t)row, (uint32_t)u)), bv);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) sv[8 * u + e] = __uint_as_float(u < 4 ? r0[8 * u + e] : r1[8 * (u - 4) + e]) + bv[e];
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&qmap);
+      tma_prefetch_desc(&kmap);
+      tma_prefetch_desc(&vmap);
+      tma_prefetch_desc(&bmap);
+      for (int t = 0; t < T; ++t) {
+        const int h = t / KB, kb = t - h * KB, st = t & 1;
+        if (kb == 0 && (h & 1) == 0) {
+          // Q of the head pair; the second pair's replaces the first once every S of heads 0, 1 is done
+          if (h == 2 && !wait_bounded(&sm.q_free, 0, p.w, abort_flag, 11)) break;
+          mbar_expect_tx(&sm.q_full, kGroups * kQBytes);
+          for (int g = 0; g < kGroups; ++g)
+            tma_load_3d(sm.q[g], &qmap, &sm.q_full, 64 * (h >> 1), (jp * kGroups + g) * BT, i);
+        }
+        if (t >= kStages && !wait_bounded(&sm.kv_empty[st], (uint32_t)((t >> 1) - 1) & 1u, p.w, abort_flag, 12)) break;
+        mbar_expect_tx(&sm.kv_full[st], kStageBytes);
+        tma_load_3d(sm.k[st], &kmap, &sm.kv_full[st], 64 * (h >> 1), kb * BT, i);
+        for (int g = 0; g < kGroups; ++g)
+          for (int hf = 0; hf < 2; ++hf)
+            tma_load_3d(sm.b[st][g][hf], &bmap, &sm.kv_full[st], kb * BT + 64 * hf, (jp * kGroups + g) * BT, h);
+        for (int hf = 0; hf < 2; ++hf)
+          tma_load_3d(sm.v[st][hf], &vmap, &sm.kv_full[st], kb * BT + 64 * hf, kHd * h, i);
       }
     }
-    if (kb == kblocks - 1) {
-      const int kbase = kb * BT + 64 * kh;
-#pragma unroll
-      for (int e = 0; e < 64; ++e)
-        if (kbase + e >= p.N) sv[e] = -INFINITY;
-    }
-    float bmax = sv[0];
-#pragma unroll
-    for (int e = 1; e < 64; ++e) bmax = fmaxf(bmax, sv[e]);
-    sm.xmax[kh][row] = bmax;
-    tc_fence_before();
-    __syncthreads();
-    // S, K and the bias of this block have been read: the next block's K and bias can come in
-    if (tid == 0 && t + 1 < total) load_kb(t + 1);
-    const float m_new = fmaxf(m_run, fmaxf(sm.xmax[0][row], sm.xmax[1][row]));
-    const float mref = m_new == -INFINITY ? 0.f : m_new;
-    const float alpha = ex2_approx(m_run - mref);
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      float pv[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) pv[e] = ex2_approx(sv[8 * u + e] - mref);
-      put8h(sm.p, row, 64 * kh + 8 * u, pv);
-    }
-    m_run = m_new;
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-      tc_fence_after();
-      // P V of this block, then S of the next one (different TMEM columns, different operands)
-      if (wait_bounded(&sm.v_bar, vph, p.w, &sm.abort_flag, 3)) {
-        const uint32_t p0 = smem_u32(sm.p), v0 = smem_u32(sm.v[0]);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          mma_f16(tmem + BT, make_sdesc_sw128(p0 + (ks >> 2) * SLAB + (ks & 3) * 32, 16, 1024),
-                  make_sdesc_sw128(v0 + (ks >> 2) * kVSlot + (ks & 3) * 32, 16, 1024), ID_O, ks ? 1u : 0u);
-        mma_commit(&sm.pv_bar);
-      }
-      vph ^= 1u;
-      if (t + 1 < total) {
-        if (wait_bounded(&sm.kb_bar, kph, p.w, &sm.abort_flag, 4)) {
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t ID_S = make_idesc(128, 128, FMT_F16, false, false);
+      constexpr uint32_t ID_O = make_idesc(128, kPvN, FMT_F16, false, false);
+      bool ok = true;
+      auto issue_pv = [&](int t) -> bool {   // O_g (+)= P_g v for block t, both groups
+        const int st = t & 1;
+        const bool first = (t % KB) == 0;    // a head's first block starts its running output
+        const uint32_t v0 = smem_u32(sm.v[st][0]);
+        for (int g = 0; g < kGroups; ++g) {
+          if (!wait_bounded(&sm.p_full[g], (uint32_t)t & 1u, p.w, abort_flag, 23)) return false;
           tc_fence_after();
-          issue_s(tmem, t + 1);
+          const uint32_t tg = tmem + (uint32_t)g * kTmGroup;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_f16_ts(tg + kTmPV, tg + kTmP + (uint32_t)ks * 8u,
+                       make_sdesc_sw128(v0 + (ks >> 2) * kVSlot + (ks & 3) * 32, 16, 1024), ID_O,
+                       (ks || !first) ? 1u : 0u);
+          mma_commit(&sm.pv_done[g]);
         }
-        kph ^= 1u;
+        mma_commit(&sm.kv_empty[st]);      // K and v of this stage have been read
+        return true;
+      };
+      for (int t = 0; t < T && ok; ++t) {
+        const int h = t / KB, kb = t - h * KB, st = t & 1;
+        if (kb == 0 && (h & 1) == 0 && !wait_bounded(&sm.q_full, (uint32_t)(h >> 1) & 1u, p.w, abort_flag, 20)) break;
+        if (!wait_bounded(&sm.kv_full[st], (uint32_t)(t >> 1) & 1u, p.w, abort_flag, 21)) break;
+        for (int g = 0; g < kGroups; ++g) {
+          // S_g = Q_g K^T of head h (q is stored pre-scaled by log2(e)/sqrt(c)), once group g has read S_g
+          if (t >= 1 && !wait_bounded(&sm.s_free[g], (uint32_t)(t - 1) & 1u, p.w, abort_flag, 22)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t q0 = smem_u32(sm.q[g]) + 64 * (h & 1), k0 = smem_u32(sm.k[st]) + 64 * (h & 1);
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks)
+            mma_f16(tmem + (uint32_t)g * kTmGroup + kTmS, make_sdesc_sw128(q0 + 32 * ks, 16, 1024),
+                    make_sdesc_sw128(k0 + 32 * ks, 16, 1024), ID_S, ks ? 1u : 0u);
+          mma_commit(&sm.s_full[g]);
+        }
+        if (!ok) break;
+        if (t == 2 * KB - 1) mma_commit(&sm.q_free);   // every S of heads 0, 1 issued: Q may be replaced
+        if (t >= 1 && !issue_pv(t - 1)) ok = false;
       }
+      if (ok) issue_pv(T - 1);
+      mma_commit(&sm.fin);
+      wait_bounded(&sm.fin, 0, p.w, abort_flag, 24);
     }
-    if (!cta_wait(&sm.pv_bar, pph, p.w, &sm.abort_flag, 5)) { ok = false; break; }
-    pph ^= 1u;
-    tc_fence_after();
-    // P V has read v: the next block's v can come in
-    if (tid == 0 && t + 1 < total) load_v(t + 1);
-    {
-      uint32_t ro[16];
-      tmem_ld16(trow + BT + 16 * kh, ro);
-      const uint32_t rl = tmem_ld1(trow + BT + kHd);     // the row sum of this block's P
+  } else {
+    // ------------------------------------------------------------ softmax, thread = query row
+    const int g = (warp - 2) >> 2;             // the group's query tile: 2 jp + g
+    const int lq = warp & 3;                   // TMEM lane quarter
+    const int row = 32 * lq + lane;
+    const int j = (jp * kGroups + g) * BT + row;
+    const bool jvalid = j < p.N;
+    const uint32_t trow = tmem + ((uint32_t)(32 * lq) << 16) + (uint32_t)g * kTmGroup;
+    float m_run = -INFINITY;
+    // o = g * O / l for head hf, from the running output in TMEM (l: its column of the row sums of the fp16 P)
+    auto finalize = [&](int hf) {
+      uint32_t ro[32];
+      tmem_ld32(trow + kTmPV, ro);
+      const uint32_t rl = tmem_ld1(trow + kTmPV + kHd);
       tmem_ld_wait();
+      if (!jvalid) return;
+      const __half* gp = p.g + ((long long)i * p.N + j) * kC + kHd * hf;
+      float gv[kHd];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) acc[e] = fmaf(acc[e], alpha, __uint_as_float(ro[e]));
-      l_run = fmaf(l_run, alpha, __uint_as_float(rl));
-    }
-    if (kb == kblocks - 1) {
-      // ---- o = g * acc / l for 16 channels of head h (l: the running sum of the bf16 P over all keys)
-      const float l_tot = l_run;
-      if (jvalid) {
-        const int cb = kHd * h + 16 * kh;
-        float gv[16];
-        {
-          const uint4* gq = reinterpret_cast<const uint4*>(p.g + ((long long)i * p.N + j) * kC + cb);
-          const uint4 g0 = gq[0], g1 = gq[1];
-          f16x8_to_float(g0, gv);
-          f16x8_to_float(g1, gv + 8);
-        }
-        const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
-        float o[16];
+      for (int u = 0; u < 4; ++u) f16x8_to_float(reinterpret_cast<const uint4*>(gp)[u], gv + 8 * u);
+      const float l = __uint_as_float(rl);
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      float o[kHd];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) o[e] = gv[e] * acc[e] * inv;
-        uint4* d4 = reinterpret_cast<uint4*>(orow + cb);
+      for (int e = 0; e < kHd; ++e) o[e] = gv[e] * __uint_as_float(ro[e]) * inv;
+      uint4* d4 = reinterpret_cast<uint4*>(p.o + ((long long)i * p.N + j) * kC + kHd * hf);
 #pragma unroll
-        for (int u = 0; u < 2; ++u) d4[u] = pack8h(o + 8 * u);
+      for (int u = 0; u < 4; ++u) d4[u] = pack8h(o + 8 * u);
+    };
+    bool ok = true;
+    for (int t = 0; t < T; ++t) {
+      const int h = t / KB, kb = t - h * KB, st = t & 1;
+      // ---- at a head's first block, the running output holds the head before's, complete
+      if (t >= 1 && kb == 0) {
+        if (!warp_wait_bounded(&sm.pv_done[g], (uint32_t)(t - 1) & 1u, p.w, abort_flag, 32)) { ok = false; break; }
+        tc_fence_after();
+        finalize(h - 1);
       }
+      // ---- S row of this block -> registers; the TMEM buffer goes back to the MMA
+      if (!warp_wait_bounded(&sm.s_full[g], (uint32_t)t & 1u, p.w, abort_flag, 30)) { ok = false; break; }
+      tc_fence_after();
+      float sv[BT];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r0[32];
+        tmem_ld32(trow + kTmS + 32 * c, r0);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) sv[32 * c + e] = __uint_as_float(r0[e]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.s_free[g]);
+      // ---- + bias (times log2(e), -inf at masked keys) of this group's queries; every thread observes the
+      // completion of the stage's copies before reading them
+      if (!warp_wait_bounded(&sm.kv_full[st], (uint32_t)(t >> 1) & 1u, p.w, abort_flag, 31)) { ok = false; break; }
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const uint8_t* brow = sm.b[st][g][hf];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          float bv[8];
+          f16x8_to_float(*reinterpret_cast<const uint4*>(brow + sw128_offset((uint32_t)row, (uint32_t)u)), bv);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) sv[64 * hf + 8 * u + e] += bv[e];
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.kv_empty[st]);
+      if (kb == KB - 1) {
+        // keys past the grid (last block only)
+#pragma unroll
+        for (int e = 0; e < BT; ++e)
+          if (kb * BT + e >= p.N) sv[e] = -INFINITY;
+      }
+      float mx = sv[0];
+#pragma unroll
+      for (int e = 1; e < BT; ++e) mx = fmaxf(mx, sv[e]);
+      if (kb == 0) m_run = -INFINITY;
+      // lazy reference: kept while this block's maximum stays within 8 of it (P <= 2^8)
+      const float m_new = (mx > m_run + 8.f) ? mx : m_run;
+      const float mref = m_new == -INFINITY ? 0.f : m_new;
+      // ---- the block before has been added into the running output: its P buffer is free
+      if (t >= 1 && kb != 0) {
+        if (!warp_wait_bounded(&sm.pv_done[g], (uint32_t)(t - 1) & 1u, p.w, abort_flag, 33)) { ok = false; break; }
+        tc_fence_after();
+      }
+      // ---- P into TMEM for the P V product, 64 keys at a time
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          pk[e] = pack_f16x2(ex2_approx(sv[64 * hf + 2 * e] - mref), ex2_approx(sv[64 * hf + 2 * e + 1] - mref));
+        tmem_st32(trow + kTmP + 32 * hf, pk);
+      }
+      // ---- the reference moved: rescale this row's running output before this block's product adds in
+      if (kb != 0 && __any_sync(0xffffffffu, m_new != m_run)) {
+        const float alpha = ex2_approx(m_run - mref);
+        uint32_t ro[32];
+        tmem_ld32(trow + kTmPV, ro);
+        const uint32_t rl = tmem_ld1(trow + kTmPV + kHd);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < kHd; ++e) ro[e] = __float_as_uint(__uint_as_float(ro[e]) * alpha);
+        tmem_st32(trow + kTmPV, ro);
+        tmem_st1(trow + kTmPV + kHd, __float_as_uint(__uint_as_float(rl) * alpha));
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.p_full[g]);
+      m_run = m_new;
+    }
+    if (ok && warp_wait_bounded(&sm.pv_done[g], (uint32_t)(T - 1) & 1u, p.w, abort_flag, 34)) {
+      tc_fence_after();
+      finalize(3);
     }
   }
-  if (!ok && tid == 0) {
+
+  __syncthreads();
+  if (*abort_flag) {
     // a wait ran out: let copies still in flight land before the shared memory is released
-    wait_bounded(&sm.kb_bar, kph, p.w, &sm.abort_flag, 6);
-    wait_bounded(&sm.v_bar, vph, p.w, &sm.abort_flag, 7);
+    const uint64_t t0 = gtimer();
+    while (gtimer() - t0 < 2000000ull) {
+    }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 256);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
 }
 
 // out = W_o o per pair (512 threads, tiles of 128 pairs; o and the W_o image fp16); for the ending
@@ -523,7 +589,7 @@ constexpr size_t kTaProjSmem = sizeof(TaProjSmem) + 1024;
 constexpr size_t kTaAttSmem = sizeof(TaAttSmem) + 1024;
 constexpr size_t kTaOutSmem = sizeof(TaOutSmem) + 1024;
 static_assert(kTaProjSmem <= 232448, "attention projection shared memory");
-static_assert(2 * kTaAttSmem <= 233472, "two attention CTAs per SM");
+static_assert(kTaAttSmem <= 232448, "attention shared memory");
 static_assert(kTaOutSmem <= 232448, "attention output shared memory");
 
 cudaError_t launch_ta_project(const TaProjectParams& p, int grid, cudaStream_t s) {
@@ -537,7 +603,7 @@ cudaError_t launch_ta_attend(const CUtensorMap& qmap, const CUtensorMap& kmap, c
                              const CUtensorMap& bmap, const TaAttendParams& p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(k_ta_attend, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTaAttSmem);
   if (e != cudaSuccess) return e;
-  const long long grid = (long long)p.N * p.jblocks;
+  const long long grid = (long long)p.N * p.jpairs;
   k_ta_attend<<<(unsigned)grid, kAttThreads, kTaAttSmem, s>>>(qmap, kmap, vmap, bmap, p);
   return cudaGetLastError();
 }

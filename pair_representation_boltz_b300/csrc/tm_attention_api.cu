@@ -204,7 +204,7 @@ tm_status tm_attn_forward(tm_ctx* c, const void* z, const float* mask, int N, tm
   pa.g = g;
   pa.o = o;
   pa.N = N;
-  pa.jblocks = (N + 127) / 128;
+  pa.jpairs = ((N + 127) / 128 + 1) / 2;
   pa.w = watch(c, KID_TA_ATTEND, opt);
   e = timed(c, 9, P, s, [&] { return launch_ta_attend(qmap, kmap, vmap, bmap, pa, s); });
   if (e != cudaSuccess) return cuda_fail(c, e, "attention launch");

@@ -243,7 +243,7 @@ struct TaAttendParams {
   const float* mask;                // [N] or nullptr
   const __half* g;                  // [N][N][128]
   __half* o;                        // [N][N][128]: gated attention output of every head
-  int N, jblocks;
+  int N, jpairs;                    // jpairs: pairs of 128-query tiles per row, ceil(ceil(N / 128) / 2)
   Watch w;
 };
 struct TaOutParams {

@@ -143,44 +143,45 @@ def _box(name):
     return tuple(int(g) for g in m.groups())
 
 
-def attention_boxes(N, i, jb):
-    """Yield (tensor, barrier, (x, y, z) start, box) for every copy of one attention CTA (row i, query
-    block jb), in the order the kernel issues them: per iteration t (head t // kblocks, key block
-    t % kblocks) K and bias (and Q at the first block of a head pair) on kb_bar, v on v_bar."""
+def attention_boxes(N, i, jp):
+    """Yield (tensor, barrier, iteration, (x, y, z) start, box) for every copy of one attention CTA (row i,
+    query tiles 2 jp and 2 jp + 1), in the order the kernel issues them: Q of both tiles at the first block
+    of each head pair on q_full; per iteration t (head t // kblocks, key block t % kblocks) K, the bias
+    tiles of both query tiles and v on the stage's barrier."""
     qk, vb, bb = _box("kBoxTaQK"), _box("kBoxTaV"), _box("kBoxTaBias")
     kblocks = (N + 127) // 128
     for t in range(4 * kblocks):
         h, kb = divmod(t, kblocks)
         if kb == 0 and h % 2 == 0:
-            yield ("q", "kb", t, (64 * (h // 2), jb * 128, i), qk)
-        yield ("k", "kb", t, (64 * (h // 2), kb * 128, i), qk)
-        yield ("bias", "kb", t, (kb * 128, jb * 128, h), bb)
-        yield ("bias", "kb", t, (kb * 128 + 64, jb * 128, h), bb)
-        yield ("v", "v", t, (kb * 128, 32 * h, i), vb)
-        yield ("v", "v", t, (kb * 128 + 64, 32 * h, i), vb)
+            for g in range(2):
+                yield ("q", "q", h, (64 * (h // 2), (2 * jp + g) * 128, i), qk)
+        yield ("k", "kv", t, (64 * (h // 2), kb * 128, i), qk)
+        for g in range(2):
+            for hf in range(2):
+                yield ("bias", "kv", t, (kb * 128 + 64 * hf, (2 * jp + g) * 128, h), bb)
+        for hf in range(2):
+            yield ("v", "kv", t, (kb * 128 + 64 * hf, 32 * h, i), vb)
 
 
 @pytest.mark.parametrize("N", [1, 7, 64, 127, 128, 129, 200, 300, 768, 1025, 3605])
 def test_attention_boxes(N):
     """Every attention copy starts at a non-negative, 16-byte-aligned inner coordinate, and the bytes each
-    barrier expects per iteration equal the boxes it receives (a load past the grid still moves a whole,
-    zero-filled box)."""
-    expect_kb = {"k": 64 * 128 * 2, "q": 64 * 128 * 2, "bias": 2 * 64 * 128 * 2}   # kKBytes, kQBytes, 2 kBBytes
-    expect_v = 2 * 64 * 32 * 2                                                     # 2 kVBytes
-    jblocks = (N + 127) // 128
+    barrier expects per phase equal the boxes it receives (a load past the grid still moves a whole,
+    zero-filled box): 2 Q boxes per head pair; per block K, four bias boxes and two v boxes."""
+    kq, kk, kb_, kv = 64 * 128 * 2, 64 * 128 * 2, 64 * 128 * 2, 64 * 32 * 2   # kQBytes, kKBytes, kBBytes, kVBytes
+    expect_q = 2 * kq
+    expect_kv = kk + 2 * 2 * kb_ + 2 * kv                                      # kStageBytes
+    jpairs = ((N + 127) // 128 + 1) // 2
     rows = sorted({0, N // 2, N - 1})
     for i in rows:
-        for jb in sorted({0, jblocks - 1}):
-            got_kb, got_v = {}, {}
-            for name, bar, t, (x, y, z), (d0, d1, d2, esz) in attention_boxes(N, i, jb):
+        for jp in sorted({0, jpairs - 1}):
+            got = {"q": {}, "kv": {}}
+            for name, bar, t, (x, y, z), (d0, d1, d2, esz) in attention_boxes(N, i, jp):
                 assert x >= 0 and y >= 0 and z >= 0 and (x * esz) % 16 == 0, (N, name, x)
-                nbytes = d0 * d1 * d2 * esz
-                (got_kb if bar == "kb" else got_v)[t] = (got_kb if bar == "kb" else got_v).get(t, 0) + nbytes
+                got[bar][t] = got[bar].get(t, 0) + d0 * d1 * d2 * esz
             kblocks = (N + 127) // 128
-            for t in range(4 * kblocks):
-                h, kb = divmod(t, kblocks)
-                want = expect_kb["k"] + expect_kb["bias"] + (expect_kb["q"] if kb == 0 and h % 2 == 0 else 0)
-                assert got_kb[t] == want and got_v[t] == expect_v, (N, t)
+            assert got["q"] == {0: expect_q, 2: expect_q}, (N, got["q"])
+            assert got["kv"] == {t: expect_kv for t in range(4 * kblocks)}, N
 
 
 # --------------------------------------------------------------------------- backward L2 prefetch ranges
