@@ -141,14 +141,14 @@ tm_status tm_pair_update(tm_ctx* ctx, void* z, const float* mask, int N, tm_dtyp
  *   mask_host  host float32 [N] or NULL;
  *   out_host   host [N][N][c_z] of dtype.
  * The copies run on two streams of the ctx, ordered against `stream` by
- * events: the copy in starts once the previous call's kernels are done with
- * the device copy of z (it may overlap that call's copy back), the kernels run
- * on `stream` after it, and for bf16 the output leaves in strips of 512 rows,
- * each as soon as its rows are finished, while the next strip computes; at the
- * end `stream` waits for the copy back. z_host must hold its values when the
- * call is made (a z_host that overlaps the previous call's out_host is copied
- * after that call's copy back). The device copies of z and out are owned by the
- * ctx and freed by tm_destroy. */
+ * events, through two device staging slots that calls use in turn: a call's
+ * copy in may run while the call before it still computes or copies back, the
+ * kernels run on `stream` after the copy in, and for bf16 the output leaves in
+ * strips of 512 rows, each as soon as its rows are finished, while the next
+ * strip computes; at the end `stream` waits for the copy back. z_host must
+ * hold its values when the call is made (a z_host that overlaps the previous
+ * call's out_host is copied after that call's copy back). The device staging
+ * (twice z and out) is owned by the ctx and freed by tm_destroy. */
 tm_status tm_forward_host(tm_ctx* ctx, const void* z_host, const float* mask_host, int N,
                           tm_dtype dtype, tm_direction dir, void* out_host, void* stream);
 

@@ -414,13 +414,21 @@ __global__ void __launch_bounds__(kAttThreads, 1) k_ta_attend(const __grid_const
       if (!warp_wait_bounded(&sm.s_full[g], (uint32_t)t & 1u, p.w, abort_flag, 30)) { ok = false; break; }
       tc_fence_after();
       float sv[BT];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r0[32];
-        tmem_ld32(trow + kTmS + 32 * c, r0);
+      {
+        // four loads in flight, one wait
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        tmem_ld32(trow + kTmS, r0);
+        tmem_ld32(trow + kTmS + 32, r1);
+        tmem_ld32(trow + kTmS + 64, r2);
+        tmem_ld32(trow + kTmS + 96, r3);
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) sv[32 * c + e] = __uint_as_float(r0[e]);
+        for (int e = 0; e < 32; ++e) {
+          sv[e] = __uint_as_float(r0[e]);
+          sv[32 + e] = __uint_as_float(r1[e]);
+          sv[64 + e] = __uint_as_float(r2[e]);
+          sv[96 + e] = __uint_as_float(r3[e]);
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -447,9 +455,20 @@ __global__ void __launch_bounds__(kAttThreads, 1) k_ta_attend(const __grid_const
         for (int e = 0; e < BT; ++e)
           if (kb * BT + e >= p.N) sv[e] = -INFINITY;
       }
-      float mx = sv[0];
+      // block maximum as a tree (16 independent chains, then pairwise): short dependency chains
+      float mx;
+      {
+        float t16[16];
 #pragma unroll
-      for (int e = 1; e < BT; ++e) mx = fmaxf(mx, sv[e]);
+        for (int e = 0; e < 16; ++e) t16[e] = sv[e];
+#pragma unroll
+        for (int e = 16; e < BT; ++e) t16[e & 15] = fmaxf(t16[e & 15], sv[e]);
+#pragma unroll
+        for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+          for (int e = 0; e < w; ++e) t16[e] = fmaxf(t16[e], t16[e + w]);
+        mx = t16[0];
+      }
       if (kb == 0) m_run = -INFINITY;
       // lazy reference: kept while this block's maximum stays within 8 of it (P <= 2^8)
       const float m_new = (mx > m_run + 8.f) ? mx : m_run;

@@ -620,7 +620,7 @@ void tm_destroy(tm_ctx* c) {
   if (c->io) cudaFree(c->io);
   if (c->io_in) cudaStreamDestroy(c->io_in);
   if (c->io_out) cudaStreamDestroy(c->io_out);
-  for (cudaEvent_t ev : {c->ev_zfree, c->ev_in, c->ev_out})
+  for (cudaEvent_t ev : {c->ev_zfree[0], c->ev_zfree[1], c->ev_in, c->ev_out[0], c->ev_out[1]})
     if (ev) cudaEventDestroy(ev);
   for (cudaEvent_t ev : c->ev_strip) cudaEventDestroy(ev);
   for (void* p : {(void*)c->w32, (void*)c->wk1, (void*)c->k1c, (void*)c->wo16, (void*)c->wg16, c->wbwd, c->ta_w})
@@ -884,18 +884,20 @@ tm_status tm_forward_host(tm_ctx* c, const void* z_host, const float* mask_host,
   const size_t zbytes = (size_t)N * N * c->c_z * esz;
   if (ranges_overlap(z_host, zbytes, out_host, zbytes)) return fail(c, TM_ERR_INVALID, "out_host overlaps z_host");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e;
+  cudaError_t e = cudaSuccess;
   // the ctx's copy streams and their events, made on first use
   if (!c->io_in) {
     e = cudaStreamCreateWithFlags(&c->io_in, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->io_out, cudaStreamNonBlocking);
-    for (cudaEvent_t* ev : {&c->ev_zfree, &c->ev_in, &c->ev_out})
+    for (cudaEvent_t* ev : {&c->ev_zfree[0], &c->ev_zfree[1], &c->ev_in, &c->ev_out[0], &c->ev_out[1]})
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
     if (e != cudaSuccess) return cuda_fail(c, e, "copy streams");
   }
+  // two staging slots (z, out, mask), used by calls in turn: a call's copy in may then run while the call
+  // before it still computes from the other slot
   const size_t zb = align_up(zbytes, 256), mb = align_up((size_t)N * 4, 256);
-  const size_t need = 2 * zb + mb;
-  if (c->io_bytes < need) {
+  const size_t slot_bytes = 2 * zb + mb;
+  if (c->io_bytes < 2 * slot_bytes) {
     // nothing of an earlier call may still use the staging buffers when they are replaced
     e = cudaStreamSynchronize(c->io_in);
     if (e == cudaSuccess) e = cudaStreamSynchronize(c->io_out);
@@ -904,88 +906,90 @@ tm_status tm_forward_host(tm_ctx* c, const void* z_host, const float* mask_host,
     if (e != cudaSuccess) return cuda_fail(c, e, "replacing the host-buffer staging");
     c->io = nullptr;
     c->io_bytes = 0;
-    e = cudaMalloc(&c->io, need);
+    e = cudaMalloc(&c->io, 2 * slot_bytes);
     if (e != cudaSuccess) {
       cudaGetLastError();
       c->io = nullptr;
-      return fail(c, TM_ERR_OOM, "cudaMalloc(%zu bytes) for host-buffer staging", need);
+      return fail(c, TM_ERR_OOM, "cudaMalloc(%zu bytes) for host-buffer staging", 2 * slot_bytes);
     }
-    c->io_bytes = need;
+    c->io_bytes = 2 * slot_bytes;
   }
-  uint8_t* zd = reinterpret_cast<uint8_t*>(c->io);
+  const int slot = c->io_slot;
+  uint8_t* zd = reinterpret_cast<uint8_t*>(c->io) + (size_t)slot * slot_bytes;
   uint8_t* od = zd + zb;
   float* md = mask_host ? reinterpret_cast<float*>(zd + 2 * zb) : nullptr;
 
-  // z (and mask) host -> device on io_in, once the last call's kernels are done with the device copy of
-  // z (and, when this z is that call's output, once its copy back has landed)
-  e = cudaStreamWaitEvent(c->io_in, c->ev_zfree, 0);
+  // z (and mask) host -> device on io_in, once the kernels of the call that last used this slot are done
+  // with it (and, when this z is the last call's output, once that output has landed)
+  e = cudaStreamWaitEvent(c->io_in, c->ev_zfree[slot], 0);
   if (e == cudaSuccess && c->last_out_host && ranges_overlap(z_host, zbytes, c->last_out_host, c->last_out_bytes))
-    e = cudaStreamWaitEvent(c->io_in, c->ev_out, 0);
+    e = cudaStreamWaitEvent(c->io_in, c->ev_out[slot ^ 1], 0);
   if (e == cudaSuccess) e = cudaMemcpyAsync(zd, z_host, zbytes, cudaMemcpyHostToDevice, c->io_in);
   if (e == cudaSuccess && md) e = cudaMemcpyAsync(md, mask_host, (size_t)N * 4, cudaMemcpyHostToDevice, c->io_in);
   if (e == cudaSuccess) e = cudaEventRecord(c->ev_in, c->io_in);
-  // the update on `stream`, after the copy in; what writes the device copy of out also waits for the
-  // last call's copy back, which reads it
+  // the update on `stream`, after the copy in; what writes this slot's device copy of out also waits for the
+  // copy back of the call that last used the slot
   if (e == cudaSuccess) e = cudaStreamWaitEvent(s, c->ev_in, 0);
   if (e != cudaSuccess) return cuda_fail(c, e, "host-to-device copy");
 
   if (dtype != TM_BF16) {
-    if ((e = cudaStreamWaitEvent(s, c->ev_out, 0)) != cudaSuccess) return cuda_fail(c, e, "event");
+    if ((e = cudaStreamWaitEvent(s, c->ev_out[slot], 0)) != cudaSuccess) return cuda_fail(c, e, "event");
     st = tm_forward_ex(c, zd, md, N, dtype, dir, od, stream, nullptr);
     if (st != TM_OK) return st;
-    if ((e = cudaEventRecord(c->ev_zfree, s)) != cudaSuccess) return cuda_fail(c, e, "event");
-    e = cudaMemcpyAsync(out_host, od, zbytes, cudaMemcpyDeviceToHost, s);
-    if (e == cudaSuccess) e = cudaEventRecord(c->ev_out, s);
-    return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "device-to-host copy");
-  }
-
-  // bf16: the projection over the whole grid, then strips of kStrip rows (contraction, finish), each
-  // strip's rows of out copied back on io_out while the next strip computes
-  constexpr int kStrip = 512;
-  const int ld = (int)align_up(N, 64);
-  const int R = std::min(N, kStrip);
-  const int ldx = (int)align_up(N, 64);
-  const size_t ab_bytes = align_up((size_t)kC * N * ld * 2, 256);
-  const size_t x_bytes = align_up((size_t)kC * R * ldx * 2, 256);
-  const size_t zst_bytes = align_up((size_t)N * N * sizeof(float2), 256);
-  st = ensure_workspace(c, 2 * ab_bytes + x_bytes + zst_bytes, s, nullptr);
-  if (st != TM_OK) return st;
-  uint8_t* base = reinterpret_cast<uint8_t*>(c->ws);
-  void* a = base;
-  void* b = base + ab_bytes;
-  void* x = base + 2 * ab_bytes;
-  float2* zstat = reinterpret_cast<float2*>(base + 2 * ab_bytes + x_bytes);
-  const int x_exp = x16_exponent(c, N);
-  st = run_project_bf16(c, zd, md, N, zstat, a, b, ld, s, nullptr);
-  if (st != TM_OK) return st;
-  const int strips = (N + R - 1) / R;
-  while ((int)c->ev_strip.size() < strips) {
-    cudaEvent_t ev;
-    if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess) return cuda_fail(c, e, "event");
-    c->ev_strip.push_back(ev);
-  }
-  const size_t row_bytes = (size_t)N * kC * 2;
-  for (int k = 0; k < strips; ++k) {
-    const int i0 = k * R, bi = std::min(R, N - i0);
-    st = run_contract_bf16(c, a, b, N, ld, dir == TM_INCOMING, i0, 0, bi, N, x, ldx, X_F16, x_exp, s, nullptr);
-    if (st == TM_OK && k == 0 && (e = cudaStreamWaitEvent(s, c->ev_out, 0)) != cudaSuccess)
-      return cuda_fail(c, e, "event");
-    if (st == TM_OK) st = run_finish_bf16(c, x, ldx, X_F16, x_exp, zstat, zd, N, i0, 0, bi, N, od, false, s, nullptr);
-    if (st != TM_OK) return st;
-    e = cudaEventRecord(c->ev_strip[k], s);
-    if (e == cudaSuccess && k == strips - 1) e = cudaEventRecord(c->ev_zfree, s);   // the last reader of z
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(c->io_out, c->ev_strip[k], 0);
-    if (e == cudaSuccess)
-      e = cudaMemcpyAsync(reinterpret_cast<uint8_t*>(out_host) + (size_t)i0 * row_bytes, od + (size_t)i0 * row_bytes,
-                          (size_t)bi * row_bytes, cudaMemcpyDeviceToHost, c->io_out);
+    e = cudaEventRecord(c->ev_zfree[slot], s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(out_host, od, zbytes, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaEventRecord(c->ev_out[slot], s);
     if (e != cudaSuccess) return cuda_fail(c, e, "device-to-host copy");
+  } else {
+    // bf16: the projection over the whole grid, then strips of kStrip rows (contraction, finish), each
+    // strip's rows of out copied back on io_out while the next strip computes
+    constexpr int kStrip = 512;
+    const int ld = (int)align_up(N, 64);
+    const int R = std::min(N, kStrip);
+    const int ldx = (int)align_up(N, 64);
+    const size_t ab_bytes = align_up((size_t)kC * N * ld * 2, 256);
+    const size_t x_bytes = align_up((size_t)kC * R * ldx * 2, 256);
+    const size_t zst_bytes = align_up((size_t)N * N * sizeof(float2), 256);
+    st = ensure_workspace(c, 2 * ab_bytes + x_bytes + zst_bytes, s, nullptr);
+    if (st != TM_OK) return st;
+    uint8_t* base = reinterpret_cast<uint8_t*>(c->ws);
+    void* a = base;
+    void* b = base + ab_bytes;
+    void* x = base + 2 * ab_bytes;
+    float2* zstat = reinterpret_cast<float2*>(base + 2 * ab_bytes + x_bytes);
+    const int x_exp = x16_exponent(c, N);
+    st = run_project_bf16(c, zd, md, N, zstat, a, b, ld, s, nullptr);
+    if (st != TM_OK) return st;
+    const int strips = (N + R - 1) / R;
+    while ((int)c->ev_strip.size() < strips) {
+      cudaEvent_t ev;
+      if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess) return cuda_fail(c, e, "event");
+      c->ev_strip.push_back(ev);
+    }
+    const size_t row_bytes = (size_t)N * kC * 2;
+    for (int k = 0; k < strips; ++k) {
+      const int i0 = k * R, bi = std::min(R, N - i0);
+      st = run_contract_bf16(c, a, b, N, ld, dir == TM_INCOMING, i0, 0, bi, N, x, ldx, X_F16, x_exp, s, nullptr);
+      if (st == TM_OK && k == 0 && (e = cudaStreamWaitEvent(s, c->ev_out[slot], 0)) != cudaSuccess)
+        return cuda_fail(c, e, "event");
+      if (st == TM_OK) st = run_finish_bf16(c, x, ldx, X_F16, x_exp, zstat, zd, N, i0, 0, bi, N, od, false, s, nullptr);
+      if (st != TM_OK) return st;
+      e = cudaEventRecord(c->ev_strip[k], s);
+      if (e == cudaSuccess && k == strips - 1) e = cudaEventRecord(c->ev_zfree[slot], s);   // the last reader of z
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(c->io_out, c->ev_strip[k], 0);
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync(reinterpret_cast<uint8_t*>(out_host) + (size_t)i0 * row_bytes, od + (size_t)i0 * row_bytes,
+                            (size_t)bi * row_bytes, cudaMemcpyDeviceToHost, c->io_out);
+      if (e != cudaSuccess) return cuda_fail(c, e, "device-to-host copy");
+    }
+    e = cudaEventRecord(c->ev_out[slot], c->io_out);
+    if (e != cudaSuccess) return cuda_fail(c, e, "event");
   }
   // `stream` waits for the copy back: synchronising it covers out_host
-  e = cudaEventRecord(c->ev_out, c->io_out);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, c->ev_out, 0);
-  if (e != cudaSuccess) return cuda_fail(c, e, "event");
+  if ((e = cudaStreamWaitEvent(s, c->ev_out[slot], 0)) != cudaSuccess) return cuda_fail(c, e, "event");
   c->last_out_host = out_host;
   c->last_out_bytes = zbytes;
+  c->io_slot = slot ^ 1;
   return TM_OK;
 }
 

@@ -71,12 +71,14 @@ struct tm_ctx {
   size_t ws_bytes = 0;
   cudaStream_t ws_stream = nullptr;
   size_t env_limit = 0;
-  // device staging of tm_forward_host, its copy streams and events: z in on io_in, out back on io_out
-  // (row strips, overlapped with the strips still computing and with the next call's copy in)
+  // device staging of tm_forward_host (two slots, used by calls in turn), its copy streams and events:
+  // z in on io_in, out back on io_out (row strips, overlapped with the strips still computing and with
+  // the next call's copy in)
   void* io = nullptr;
   size_t io_bytes = 0;
+  int io_slot = 0;
   cudaStream_t io_in = nullptr, io_out = nullptr;
-  cudaEvent_t ev_zfree = nullptr, ev_in = nullptr, ev_out = nullptr;
+  cudaEvent_t ev_zfree[2] = {nullptr, nullptr}, ev_in = nullptr, ev_out[2] = {nullptr, nullptr};
   std::vector<cudaEvent_t> ev_strip;
   const void* last_out_host = nullptr;
   size_t last_out_bytes = 0;
