@@ -410,64 +410,46 @@ __global__ void __launch_bounds__(kAttThreads, 1) k_ta_attend(const __grid_const
         tc_fence_after();
         finalize(h - 1);
       }
-      // ---- S row of this block -> registers; the TMEM buffer goes back to the MMA
+      // ---- two passes over the block's S row in TMEM, 32 keys at a time (S is read twice rather than held
+      // in 128 registers): the maximum of S + bias, then P = 2^(S + bias - reference) into TMEM
       if (!warp_wait_bounded(&sm.s_full[g], (uint32_t)t & 1u, p.w, abort_flag, 30)) { ok = false; break; }
-      tc_fence_after();
-      float sv[BT];
-      {
-        // four loads in flight, one wait
-        uint32_t r0[32], r1[32], r2[32], r3[32];
-        tmem_ld32(trow + kTmS, r0);
-        tmem_ld32(trow + kTmS + 32, r1);
-        tmem_ld32(trow + kTmS + 64, r2);
-        tmem_ld32(trow + kTmS + 96, r3);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          sv[e] = __uint_as_float(r0[e]);
-          sv[32 + e] = __uint_as_float(r1[e]);
-          sv[64 + e] = __uint_as_float(r2[e]);
-          sv[96 + e] = __uint_as_float(r3[e]);
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.s_free[g]);
-      // ---- + bias (times log2(e), -inf at masked keys) of this group's queries; every thread observes the
-      // completion of the stage's copies before reading them
+      // every thread observes the completion of the stage's copies (the bias) before reading them
       if (!warp_wait_bounded(&sm.kv_full[st], (uint32_t)(t >> 1) & 1u, p.w, abort_flag, 31)) { ok = false; break; }
+      tc_fence_after();
+      const int nvalid = p.N - kb * BT;          // keys of the block inside the grid (all of them but in the last)
+      // logits of keys 32 c .. 32 c + 31 (base 2): S + bias (times log2(e), -inf at masked keys), -inf past N
+      auto logits = [&](int c, const uint32_t (&r)[32], float (&x)[32]) {
+        const uint8_t* brow = sm.b[st][g][c >> 1];
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const uint8_t* brow = sm.b[st][g][hf];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < 4; ++u) {
           float bv[8];
-          f16x8_to_float(*reinterpret_cast<const uint4*>(brow + sw128_offset((uint32_t)row, (uint32_t)u)), bv);
+          f16x8_to_float(*reinterpret_cast<const uint4*>(brow + sw128_offset((uint32_t)row, (uint32_t)(4 * (c & 1) + u))),
+                         bv);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) sv[64 * hf + 8 * u + e] += bv[e];
+          for (int e = 0; e < 8; ++e) x[8 * u + e] = __uint_as_float(r[8 * u + e]) + bv[e];
         }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.kv_empty[st]);
-      if (kb == KB - 1) {
-        // keys past the grid (last block only)
+        if (nvalid < BT) {
 #pragma unroll
-        for (int e = 0; e < BT; ++e)
-          if (kb * BT + e >= p.N) sv[e] = -INFINITY;
-      }
-      // block maximum as a tree (16 independent chains, then pairwise): short dependency chains
-      float mx;
+          for (int e = 0; e < 32; ++e)
+            if (32 * c + e >= nvalid) x[e] = -INFINITY;
+        }
+      };
+      float mx = -INFINITY;
       {
-        float t16[16];
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld32(trow + kTmS + 32 * c, r);
+          tmem_ld_wait();
+          float x[32];
+          logits(c, r, x);
+          float m8[8];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) t16[e] = sv[e];
+          for (int e = 0; e < 8; ++e) m8[e] = fmaxf(fmaxf(x[e], x[e + 8]), fmaxf(x[e + 16], x[e + 24]));
 #pragma unroll
-        for (int e = 16; e < BT; ++e) t16[e & 15] = fmaxf(t16[e & 15], sv[e]);
-#pragma unroll
-        for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-          for (int e = 0; e < w; ++e) t16[e] = fmaxf(t16[e], t16[e + w]);
-        mx = t16[0];
+          for (int e = 0; e < 4; ++e) m8[e] = fmaxf(m8[e], m8[e + 4]);
+          mx = fmaxf(mx, fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])));
+        }
       }
       if (kb == 0) m_run = -INFINITY;
       // lazy reference: kept while this block's maximum stays within 8 of it (P <= 2^8)
@@ -478,14 +460,26 @@ __global__ void __launch_bounds__(kAttThreads, 1) k_ta_attend(const __grid_const
         if (!warp_wait_bounded(&sm.pv_done[g], (uint32_t)(t - 1) & 1u, p.w, abort_flag, 33)) { ok = false; break; }
         tc_fence_after();
       }
-      // ---- P into TMEM for the P V product, 64 keys at a time
+      {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld32(trow + kTmS + 32 * c, r);
+          tmem_ld_wait();
+          float x[32];
+          logits(c, r, x);
+          uint32_t pk[16];
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e)
-          pk[e] = pack_f16x2(ex2_approx(sv[64 * hf + 2 * e] - mref), ex2_approx(sv[64 * hf + 2 * e + 1] - mref));
-        tmem_st32(trow + kTmP + 32 * hf, pk);
+          for (int e = 0; e < 16; ++e) pk[e] = pack_f16x2(ex2_approx(x[2 * e] - mref), ex2_approx(x[2 * e + 1] - mref));
+          tmem_st16(trow + kTmP + 16 * c, pk);
+        }
+      }
+      // S and the stage's bias have been read: both go back
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&sm.s_free[g]);
+        mbar_arrive(&sm.kv_empty[st]);
       }
       // ---- the reference moved: rescale this row's running output before this block's product adds in
       if (kb != 0 && __any_sync(0xffffffffu, m_new != m_run)) {
