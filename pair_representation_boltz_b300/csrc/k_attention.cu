@@ -24,14 +24,15 @@
 //     cores. q, k and g are stored pair-major like z; v is stored per (row, head, channel) with the
 //     key index innermost, so that it is the K-major operand of the P V product; b per (head, j) with
 //     k innermost.
-//   k_ta_attend: per (row i, block of 128 queries j), heads one after another, keys in blocks of 128:
-//     S = Q K^T (tcgen05, TMEM; q stored times log2(e)/sqrt(c), the bias times log2(e), so the softmax
-//     runs in base 2), + bias tile (-inf at masked keys), online softmax in registers (two threads per
-//     query row, 64 keys each), P (fp16) into shared memory, O_blk = P V (tcgen05, with a row of ones
-//     appended to v so that the product also gives the row sum of P, the softmax denominator) added
-//     into the row's running output, the gate at the end of each head. Loads and products are pipelined one
-//     block ahead: the next block's K and bias are fetched once this block's S and bias are in
-//     registers, its S is issued together with this block's P V, and its v once P V is done.
+//   k_ta_attend: per (row i, two tiles of 128 queries j), heads one after another, keys in blocks of
+//     128, warp-specialised: a TMA warp, an MMA warp and one softmax thread per query row. S = Q K^T
+//     (tcgen05, TMEM; q stored times log2(e)/sqrt(c), the bias times log2(e), so the softmax runs in
+//     base 2); the softmax thread reads its S row in 32-key chunks, adds the bias row (-inf at masked
+//     keys), and forms P = 2^(x - reference) as fp16 back into TMEM against a lazy running reference,
+//     checking the block maximum on the way (a second pass only when it moved by more than 8); O += P v
+//     (A = P from TMEM, v with a row of ones appended so that the product also gives the row sum of P,
+//     the softmax denominator) accumulates across a head's blocks in TMEM, and the gate is applied at
+//     the end of each head.
 //   k_ta_out: out = W_o o per pair (the ending node writes the transposed pair).
 #include "pair_tile.cuh"
 
@@ -226,6 +227,13 @@ __device__ __forceinline__ float ex2_approx(float v) {
   return r;
 }
 
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // Triangle attention of one CTA: row i of the grid, query tiles 2 jp and 2 jp + 1 (one per softmax
 // group), heads in turn, keys in blocks of 128. Roles:
 //   warp 0        TMA: per block, K (the head pair's 64 channels), the bias tiles of both groups and
@@ -233,14 +241,16 @@ __device__ __forceinline__ float ex2_approx(float v) {
 //   warp 1        tcgen05.mma: S_g = Q_g K^T into TMEM (M = 128 queries, N = 128 keys, K = 32), then,
 //                 once group g has stored its P into TMEM, O_g = P_g v (A = P from TMEM, B = v from
 //                 shared memory, N = 48: 32 channels, the row sum from the ones row, padding).
-//   warps 2..9    softmax, thread = query row, group g = the four warps of one query tile: S row and
-//                 bias row -> logits (base 2), block maximum with a lazy running reference (the
-//                 reference moves only when the maximum exceeds it by more than 8, so P <= 2^8 stays
-//                 inside fp16 and most blocks need no rescale of the running output), P = 2^(s - m)
-//                 into TMEM as fp16. The running output O (and its row sum) accumulates in TMEM
-//                 across a head's blocks; when the reference moves, the thread rescales its row of O
-//                 once the block before has been added, before this block's P is released. Each
-//                 group's work overlaps the other group's and the tensor core's.
+//   warps 2..9    softmax, thread = query row, group g = the four warps of one query tile: S row +
+//                 bias row -> logits (base 2), and P = 2^(x - m) into TMEM as fp16 against the row's
+//                 running reference m, in one pass that also takes the block maximum. The reference
+//                 is lazy: it moves only when the maximum exceeds it by more than 8 (then P is formed
+//                 again, against the new maximum; always at a head's first block), so P <= 2^8 stays
+//                 inside fp16 and most blocks need one pass and no rescale of the running output. The
+//                 running output O (and its row sum) accumulates in TMEM across a head's blocks; when
+//                 the reference moves, the thread rescales its row of O once the block before has been
+//                 added, before this block's P is released. Each group's work overlaps the other
+//                 group's and the tensor core's.
 __global__ void __launch_bounds__(kAttThreads, 1) k_ta_attend(const __grid_constant__ CUtensorMap qmap,
                                                               const __grid_constant__ CUtensorMap kmap,
                                                               const __grid_constant__ CUtensorMap vmap,
@@ -401,6 +411,55 @@ __global__ void __launch_bounds__(kAttThreads, 1) k_ta_attend(const __grid_const
 #pragma unroll
       for (int u = 0; u < 4; ++u) d4[u] = pack8h(o + 8 * u);
     };
+    // One pass over the block's S row in TMEM, 32 keys at a time (the next chunk's load in flight while
+    // one is computed): logits x = S + bias (base 2), their maximum, and P = 2^(x - ref) into TMEM as
+    // fp16 against the reference ref. pmax: the maximum of the logits.
+    auto pass = [&](int st, int nvalid, bool write_p, float ref, float& pmax) {
+      const float2 nref = make_float2(-ref, -ref);
+      float mx = -INFINITY;
+      uint32_t r[2][32];
+      tmem_ld32(trow + kTmS, r[0]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        tmem_ld_wait();
+        if (c < 3) tmem_ld32(trow + kTmS + 32 * (c + 1), r[(c + 1) & 1]);
+        const uint8_t* brow = sm.b[st][g][c >> 1];
+        float x[32];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          float bv[8];
+          f16x8_to_float(*reinterpret_cast<const uint4*>(brow + sw128_offset((uint32_t)row, (uint32_t)(4 * (c & 1) + u))),
+                         bv);
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            const float2 v = __fadd2_rn(make_float2(__uint_as_float(r[c & 1][8 * u + e]), __uint_as_float(r[c & 1][8 * u + e + 1])),
+                                        make_float2(bv[e], bv[e + 1]));
+            x[8 * u + e] = v.x;
+            x[8 * u + e + 1] = v.y;
+          }
+        }
+        if (nvalid < BT) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (32 * c + e >= nvalid) x[e] = -INFINITY;
+        }
+        float m3[11];
+#pragma unroll
+        for (int e = 0; e < 10; ++e) m3[e] = max3f(x[3 * e], x[3 * e + 1], x[3 * e + 2]);
+        m3[10] = max3f(x[30], x[31], mx);
+        mx = max3f(max3f(m3[0], m3[1], m3[2]), max3f(m3[3], m3[4], m3[5]), max3f(max3f(m3[6], m3[7], m3[8]), m3[9], m3[10]));
+        if (write_p) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float2 d = __fadd2_rn(make_float2(x[2 * e], x[2 * e + 1]), nref);
+            pk[e] = pack_f16x2(ex2_approx(d.x), ex2_approx(d.y));
+          }
+          tmem_st16(trow + kTmP + 16 * c, pk);
+        }
+      }
+      pmax = mx;
+    };
     bool ok = true;
     for (int t = 0; t < T; ++t) {
       const int h = t / KB, kb = t - h * KB, st = t & 1;
@@ -410,70 +469,27 @@ __global__ void __launch_bounds__(kAttThreads, 1) k_ta_attend(const __grid_const
         tc_fence_after();
         finalize(h - 1);
       }
-      // ---- two passes over the block's S row in TMEM, 32 keys at a time (S is read twice rather than held
-      // in 128 registers): the maximum of S + bias, then P = 2^(S + bias - reference) into TMEM
       if (!warp_wait_bounded(&sm.s_full[g], (uint32_t)t & 1u, p.w, abort_flag, 30)) { ok = false; break; }
       // every thread observes the completion of the stage's copies (the bias) before reading them
       if (!warp_wait_bounded(&sm.kv_full[st], (uint32_t)(t >> 1) & 1u, p.w, abort_flag, 31)) { ok = false; break; }
-      tc_fence_after();
-      const int nvalid = p.N - kb * BT;          // keys of the block inside the grid (all of them but in the last)
-      // logits of keys 32 c .. 32 c + 31 (base 2): S + bias (times log2(e), -inf at masked keys), -inf past N
-      auto logits = [&](int c, const uint32_t (&r)[32], float (&x)[32]) {
-        const uint8_t* brow = sm.b[st][g][c >> 1];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          float bv[8];
-          f16x8_to_float(*reinterpret_cast<const uint4*>(brow + sw128_offset((uint32_t)row, (uint32_t)(4 * (c & 1) + u))),
-                         bv);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) x[8 * u + e] = __uint_as_float(r[8 * u + e]) + bv[e];
-        }
-        if (nvalid < BT) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (32 * c + e >= nvalid) x[e] = -INFINITY;
-        }
-      };
-      float mx = -INFINITY;
-      {
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld32(trow + kTmS + 32 * c, r);
-          tmem_ld_wait();
-          float x[32];
-          logits(c, r, x);
-          float m8[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) m8[e] = fmaxf(fmaxf(x[e], x[e + 8]), fmaxf(x[e + 16], x[e + 24]));
-#pragma unroll
-          for (int e = 0; e < 4; ++e) m8[e] = fmaxf(m8[e], m8[e + 4]);
-          mx = fmaxf(mx, fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])));
-        }
-      }
-      if (kb == 0) m_run = -INFINITY;
-      // lazy reference: kept while this block's maximum stays within 8 of it (P <= 2^8)
-      const float m_new = (mx > m_run + 8.f) ? mx : m_run;
-      const float mref = m_new == -INFINITY ? 0.f : m_new;
       // ---- the block before has been added into the running output: its P buffer is free
       if (t >= 1 && kb != 0) {
         if (!warp_wait_bounded(&sm.pv_done[g], (uint32_t)(t - 1) & 1u, p.w, abort_flag, 33)) { ok = false; break; }
-        tc_fence_after();
       }
-      {
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld32(trow + kTmS + 32 * c, r);
-          tmem_ld_wait();
-          float x[32];
-          logits(c, r, x);
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) pk[e] = pack_f16x2(ex2_approx(x[2 * e] - mref), ex2_approx(x[2 * e + 1] - mref));
-          tmem_st16(trow + kTmP + 16 * c, pk);
-        }
+      tc_fence_after();
+      const int nvalid = p.N - kb * BT;          // keys of the block inside the grid (all of them but in the last)
+      if (kb == 0) m_run = -INFINITY;
+      // Lazy reference: P is formed against the running reference and the block's maximum checked on the
+      // way; only when some row's maximum exceeds its reference by more than 8 (always in a head's first
+      // block) is P formed again, against the new maximum, so P <= 2^8 stays inside fp16.
+      float mx;
+      pass(st, nvalid, kb != 0, m_run == -INFINITY ? 0.f : m_run, mx);
+      const float m_new = (mx > m_run + 8.f) ? mx : m_run;
+      if (kb == 0 || __any_sync(0xffffffffu, m_new != m_run)) {
+        float unused;
+        pass(st, nvalid, true, m_new == -INFINITY ? 0.f : m_new, unused);
       }
+      const float mref = m_new == -INFINITY ? 0.f : m_new;
       // S and the stage's bias have been read: both go back
       tc_fence_before();
       __syncwarp();
