@@ -35,7 +35,10 @@
 //               16-byte inner-axis grid.)
 // Incoming reads the same a/b buffers through tensor maps whose box runs along
 // the other pair index ("transposed" boxes), and tells the MMA that A and B are
-// M/N-major; no transpose is ever materialised. k beyond N is zero-filled by TMA.
+// M/N-major; no transpose is ever materialised. A third form, with A read as in
+// the outgoing contraction and B as in the incoming one (x_ij = sum_k A_ik B_kj),
+// serves the backward pass's products of dL/dx with a or b. k beyond N is
+// zero-filled by TMA.
 #include "tm_kernels.h"
 
 namespace tmk {
@@ -72,8 +75,8 @@ __device__ __forceinline__ Tile decode(long long t, const ContractParams& p) {
   return r;
 }
 
-// X16: x leaves as fp16 scaled by 2^x_exp, else float32.
-template <bool INCOMING, bool X16>
+// MODE: the operands' forms (ContractMode); X16: x leaves as fp16 scaled by 2^x_exp, else float32.
+template <int MODE, bool X16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     k2_contract(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap,
                 const __grid_constant__ CUtensorMap xmap, const ContractParams p) {
@@ -142,14 +145,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             // the first CTA's "full" barrier counts the bytes of both CTAs' copies
             const uint32_t fb = rank == 0 ? smem_u32(&full[s]) : full0 + (uint32_t)(s * 8);
             if (rank == 0) mbar_expect_tx_u32(fb, 2 * STAGE_BYTES);
-            if (!INCOMING) {
-              // A_c[i][k] = a_ik: rows i, k contiguous (K-major); B_c[j][k] = b_jk likewise.
+            if (MODE != CONTRACT_IN) {
+              // A_c[i][k] = a_ik: rows i, k contiguous (K-major)
               tma_load_3d_pair(sa, &amap, fb, kb * BK, ia, tl.c);
-              tma_load_3d_pair(sb, &bmap, fb, kb * BK, jb, tl.c);
             } else {
-              // a_ki, b_kj: rows k, i (or j) contiguous; 64-wide slabs along i / j (M/N-major).
+              // a_ki: rows k, i contiguous; 64-wide slabs along i (M-major)
               tma_load_3d_pair(sa, &amap, fb, ia, kb * BK, tl.c);
               tma_load_3d_pair(sa + 8192, &amap, fb, ia + 64, kb * BK, tl.c);
+            }
+            if (MODE == CONTRACT_OUT) {
+              // B_c[j][k] = b_jk: rows j, k contiguous (K-major)
+              tma_load_3d_pair(sb, &bmap, fb, kb * BK, jb, tl.c);
+            } else {
+              // b_kj: rows k, j contiguous; 64-wide slabs along j (N-major)
               tma_load_3d_pair(sb, &bmap, fb, jb, kb * BK, tl.c);
               tma_load_3d_pair(sb + 8192, &bmap, fb, jb + 64, kb * BK, tl.c);
             }
@@ -166,8 +174,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       if (lane == 0 && rank == 0) {
         // bf16 operands (the update's a and b) or fp16 ones (the backward pass's)
         const uint32_t fmt = p.ab_f16 ? FMT_F16 : FMT_BF16;
-        const uint32_t idesc_full = make_idesc(BM, BN, fmt, INCOMING, INCOMING);
-        const uint32_t idesc_last = make_idesc(BM, p.last_n, fmt, INCOMING, INCOMING);
+        constexpr bool A_MN = MODE == CONTRACT_IN, B_MN = MODE != CONTRACT_OUT;
+        const uint32_t idesc_full = make_idesc(BM, BN, fmt, A_MN, B_MN);
+        const uint32_t idesc_last = make_idesc(BM, p.last_n, fmt, A_MN, B_MN);
         int s = 0;
         uint32_t ph = 0;
         int local = 0;
@@ -189,14 +198,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             const uint32_t b0 = a0 + A_BYTES;
 #pragma unroll
             for (int ks = 0; ks < BK / 16; ++ks) {
-              uint64_t ad, bd;
-              if (!INCOMING) {
-                ad = make_sdesc_sw128(a0 + ks * 32, 16, 1024);
-                bd = make_sdesc_sw128(b0 + ks * 32, 16, 1024);
-              } else {
-                ad = make_sdesc_sw128(a0 + ks * 2048, 8192, 1024);
-                bd = make_sdesc_sw128(b0 + ks * 2048, 8192, 1024);
-              }
+              const uint64_t ad = A_MN ? make_sdesc_sw128(a0 + ks * 2048, 8192, 1024)
+                                       : make_sdesc_sw128(a0 + ks * 32, 16, 1024);
+              const uint64_t bd = B_MN ? make_sdesc_sw128(b0 + ks * 2048, 8192, 1024)
+                                       : make_sdesc_sw128(b0 + ks * 32, 16, 1024);
               mma_f16_pair(d, ad, bd, idesc, (kb | ks) != 0);
             }
             mma_commit_pair(&empty[s]);
@@ -340,12 +345,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
 }  // namespace
 
-cudaError_t launch_contract_bf16(bool incoming, const CUtensorMap& amap, const CUtensorMap& bmap,
+cudaError_t launch_contract_bf16(int mode, const CUtensorMap& amap, const CUtensorMap& bmap,
                                  const CUtensorMap& xmap, const ContractParams& p, int num_sms, cudaStream_t s) {
   static bool attr_set[kMaxDevices] = {};
   cudaError_t err = once_per_device(attr_set, [] {
-    const void* fns[4] = {(const void*)k2_contract<false, false>, (const void*)k2_contract<true, false>,
-                          (const void*)k2_contract<false, true>, (const void*)k2_contract<true, true>};
+    const void* fns[5] = {(const void*)k2_contract<CONTRACT_OUT, false>, (const void*)k2_contract<CONTRACT_IN, false>,
+                          (const void*)k2_contract<CONTRACT_OUT, true>, (const void*)k2_contract<CONTRACT_IN, true>,
+                          (const void*)k2_contract<CONTRACT_MIXED, false>};
     for (const void* f : fns) {
       cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
       if (e != cudaSuccess) return e;
@@ -353,21 +359,25 @@ cudaError_t launch_contract_bf16(bool incoming, const CUtensorMap& amap, const C
     return cudaSuccess;
   });
   if (err != cudaSuccess) return err;
+  if (mode != CONTRACT_OUT && mode != CONTRACT_IN && mode != CONTRACT_MIXED) return cudaErrorInvalidValue;
+  if (mode == CONTRACT_MIXED && p.x_f16) return cudaErrorInvalidValue;   // float32 x only (backward)
   if (p.total_tiles <= 0) return cudaSuccess;
   long long pairs = num_sms / 2;
   if (pairs > p.total_tiles) pairs = p.total_tiles;
   if (pairs < 1) pairs = 1;
   const int grid = (int)(2 * pairs);
-  if (p.x_f16) {
-    if (incoming)
-      k2_contract<true, true><<<grid, THREADS, SMEM_BYTES, s>>>(amap, bmap, xmap, p);
+  if (mode == CONTRACT_MIXED)
+    k2_contract<CONTRACT_MIXED, false><<<grid, THREADS, SMEM_BYTES, s>>>(amap, bmap, xmap, p);
+  else if (p.x_f16) {
+    if (mode == CONTRACT_IN)
+      k2_contract<CONTRACT_IN, true><<<grid, THREADS, SMEM_BYTES, s>>>(amap, bmap, xmap, p);
     else
-      k2_contract<false, true><<<grid, THREADS, SMEM_BYTES, s>>>(amap, bmap, xmap, p);
+      k2_contract<CONTRACT_OUT, true><<<grid, THREADS, SMEM_BYTES, s>>>(amap, bmap, xmap, p);
   } else {
-    if (incoming)
-      k2_contract<true, false><<<grid, THREADS, SMEM_BYTES, s>>>(amap, bmap, xmap, p);
+    if (mode == CONTRACT_IN)
+      k2_contract<CONTRACT_IN, false><<<grid, THREADS, SMEM_BYTES, s>>>(amap, bmap, xmap, p);
     else
-      k2_contract<false, false><<<grid, THREADS, SMEM_BYTES, s>>>(amap, bmap, xmap, p);
+      k2_contract<CONTRACT_OUT, false><<<grid, THREADS, SMEM_BYTES, s>>>(amap, bmap, xmap, p);
   }
   return cudaGetLastError();
 }

@@ -42,8 +42,6 @@ namespace {
 using namespace pt;
 
 constexpr int kHeads = 4, kHd = 32;
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kQScale = 1.4426950408889634f * 0.17677669529663687f;   // log2(e) / sqrt(32)
 
 struct alignas(1024) TaProjSmem {
   uint8_t zh[TILE], wq[TILE], wk[TILE], wv[TILE], wg[TILE];

@@ -10,7 +10,7 @@
 //     dy = dout sigmoid(gg),  dgg = dout y sigmoid'(gg)
 //     dxh = W_o^T dy,  dzh_g = W_g^T dgg                                  [MMA 2: A = dy, dgg]
 //     dW_g += dgg zh^T,  dW_o += dy xh^T   (summed over the CTA's pairs)   [MMA 3, TMEM-resident]
-//     dx = LN_out backward of dxh -> dX (float32, over x in place), d(gamma_out), d(beta_out)
+//     dx = LN_out backward of dxh -> dX (fp16, times the power of two of a bound), d(gamma_out), d(beta_out)
 //   projection backward (k_bwd_project), per pair p = (i, k), once for a and once for b:
 //     pv = W_v zh, pg = W_gt zh                                            [MMA 1: A = zh]
 //     dpv = dV sigmoid(pg) m_i m_k,  dpg = dV pv m_i m_k sigmoid'(pg)     (dV = dA or dB)
@@ -24,8 +24,14 @@
 // factors from the largest |dout| (k_absmax_bf16, read here from device memory), the per-pair dpv and
 // dpg by factors that bound them from the fp16 contraction operands. Every product's epilogue
 // multiplies its float32 result by the exact inverse of the scales it carries, so all stored
-// gradients (dzh, dX, the parameter partials) are in true units. dX is written as float32 over x
-// and its largest magnitude is recorded, so that k_convert_transpose can scale it into fp16.
+// gradients (dzh, the parameter partials) are in true units. dX leaves as fp16 times the power of two
+// that brings a bound on |dX| to 2^14: with r_x = 1/sqrt(var + eps) <= 1/sqrt(eps), |x_hat| <= sqrt(c),
+// |dX_c| <= r_x (2 + sqrt(c)) max_c |gamma_out,c dxh_c| and |dxh_c| <= ||W_o[:, c]||_1 max |dout|, so the
+// bound is a host constant times the largest |dout| (the same for every block of a block schedule).
+//
+// Blocks. The output backward runs over one block of the pair grid at a time (x of that block from the
+// contraction), the projection backward over a range of whole grid rows; per-CTA partial sums are
+// added to, so that a schedule of launches sums them (the host clears them first).
 //
 // Layout. One CTA of 512 threads per SM, persistent over tiles of 128 consecutive pairs of the
 // flattened N x N grid. Warp w serves the 32 pairs of TMEM lane quarter w % 4 (the lanes it may
@@ -56,7 +62,6 @@ struct alignas(1024) OutSmem {
   uint64_t bar;
   uint32_t tmem_slot;
   int abort_flag;
-  float amax;                           // largest |dX| the CTA wrote
 };
 
 struct alignas(1024) ProjSmem {
@@ -110,13 +115,6 @@ __device__ __forceinline__ void zh_quarter(uint8_t* tile, const float* ln_g, con
   for (int u = 0; u < 4; ++u) put8h(tile, r, 32 * h + 8 * u, f + 8 * u);
 }
 
-// Largest |value| of a warp's lanes as a float (non-negative, so its bits order like integers).
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-
 __global__ void __launch_bounds__(NT, 1) k_bwd_output(const BwdOutParams p) {
   extern __shared__ uint8_t smem_raw[];
   OutSmem& sm = *reinterpret_cast<OutSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -126,7 +124,6 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_output(const BwdOutParams p) {
   if (tid == 0) {
     mbar_init(&sm.bar, 1);
     sm.abort_flag = 0;
-    sm.amax = 0.f;
     fence_mbar_init();
   }
   for (int k = tid; k < 4 * kC; k += NT) sm.ln[k] = p.ln[k];
@@ -151,28 +148,36 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_output(const BwdOutParams p) {
   const float dmax = __uint_as_float(p.amax[0]);
   const float d1 = pow2_scale(dmax, 14), d2 = pow2_scale(dmax * p.y_bound4, 14);
   const float u_dxh = p.u_dxh / d1, u_dzh = p.u_dzh / d2, u_wg = p.u_wg / d2, u_wo = p.u_wo / d1;
+  // dX's fp16 scale, from its bound; the projection backward reads the bound back from amax[1]
+  const float dxb = p.dx_bound * dmax;
+  const float sdx = pow2_scale(dxb, 14);
+  if (blockIdx.x == 0 && tid == 0) p.amax[1] = __float_as_uint(dxb);
 
   float acc_g = 0.f, acc_b = 0.f;                  // channel c0 + lane: sums of dxh n and dxh
   float dx_max = 0.f;                              // largest |dX| this thread writes
+  const long long PB = (long long)p.bi * p.bj;     // pairs of the block
   uint32_t phase = 0;
   int local = 0;
   bool ok = true;
   for (long long t = blockIdx.x; t < p.tiles; t += gridDim.x, ++local) {
-    const long long pr = t * BT + r;
-    const bool valid = pr < p.P;
-    const int i = valid ? (int)(pr / p.N) : 0;
-    const int j = valid ? (int)(pr - (long long)i * p.N) : 0;
-    float* xp = p.x + (long long)i * p.ldx + j + (long long)c0 * p.xplane;
+    const long long pl = t * BT + r;               // pair of the block
+    const bool valid = pl < PB;
+    const int il = valid ? (int)(pl / p.bj) : 0;
+    const int jl = valid ? (int)(pl - (long long)il * p.bj) : 0;
+    const int i = p.i0 + il, j = p.j0 + jl;
+    const long long pr = (long long)i * p.N + j;   // pair of the grid
+    const float* xp = p.x + (long long)il * p.ldx + jl + (long long)c0 * p.xplane;
     {
       // L2 prefetch of what the next tile of this CTA reads: x (one channel per thread of the first
-      // 128), z, dout and the LayerNorm_in statistics
+      // 128) and, for whole grid rows, z, dout and the LayerNorm_in statistics
       const long long tn = t + gridDim.x;
-      if (tn < p.tiles && p.N >= BT) {
-        const long long q0 = tn * BT, q1 = (q0 + BT < p.P) ? q0 + BT : p.P;
-        if (tid < kC) prefetch_plane_rows(p.x + (long long)tid * p.xplane, p.ldx, p.N, q0, q1);
-        else if (tid == kC) prefetch_range(p.z, q0 * 2 * kC, q1 * 2 * kC);
-        else if (tid == kC + 1) prefetch_range(p.dout, q0 * 2 * kC, q1 * 2 * kC);
-        else if (tid == kC + 2) prefetch_range(p.zstat, q0 * 8, q1 * 8);
+      if (tn < p.tiles && p.bj >= BT) {
+        const long long q0 = tn * BT, q1 = (q0 + BT < PB) ? q0 + BT : PB;
+        const long long g0 = (long long)p.i0 * p.N + q0, g1 = (long long)p.i0 * p.N + q1;
+        if (tid < kC) prefetch_plane_rows(p.x + (long long)tid * p.xplane, p.ldx, p.bj, q0, q1);
+        else if (p.bj == p.N && tid == kC) prefetch_range(p.z, g0 * 2 * kC, g1 * 2 * kC);
+        else if (p.bj == p.N && tid == kC + 1) prefetch_range(p.dout, g0 * 2 * kC, g1 * 2 * kC);
+        else if (p.bj == p.N && tid == kC + 2) prefetch_range(p.zstat, g0 * 8, g1 * 8);
       }
     }
 
@@ -271,9 +276,9 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_output(const BwdOutParams p) {
       uint32_t rz[32];
       tmem_ld32(trow + kC + c0, rz);
       tmem_ld_wait();
-      if (valid)
+      if (valid && p.dzh)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) p.dzh[(long long)(c0 + e) * p.P + pr] = __uint_as_float(rz[e]) * u_dzh;
+        for (int e = 0; e < 32; ++e) p.dzh[(long long)(c0 + e) * p.dzh_P + (pr - p.dzh_off)] = __uint_as_float(rz[e]) * u_dzh;
     }
     uint32_t rd[32];
     tmem_ld32(trow + c0, rd);
@@ -303,30 +308,32 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_output(const BwdOutParams p) {
       s1 = ((q0.x + q1.x) + (q2.x + q3.x)) * (1.f / kC);
       s2 = ((q0.y + q1.y) + (q2.y + q3.y)) * (1.f / kC);
     }
-    if (valid) {
-      // over x, in place: this thread has read these 32 values (and no other thread reads them)
+    if (valid && p.dx16) {
+      __half* dp = p.dx16 + (long long)c0 * p.dxplane + (long long)i * p.ldd + j;
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
         const float dx = rx * (__uint_as_float(rd[e]) * g_out[c0 + e] - s1 - xv[e] * s2);
         dx_max = fmaxf(dx_max, fabsf(dx));
-        xp[e * p.xplane] = dx;
+        dp[e * p.dxplane] = __float2half_rn(dx * sdx);
       }
     }
   }
 
-  // ---- the largest |dX| of the CTA, for the fp16 scale of dX
-  dx_max = warp_max(dx_max);
-  if (lane == 0) atomicMax(reinterpret_cast<unsigned*>(&sm.amax), __float_as_uint(dx_max));
-  __syncthreads();
-  if (tid == 0) atomicMax(p.amax + 1, __float_as_uint(sm.amax));
+  // ---- the largest |dX| written (the projection backward's scales of dpv, dpg follow from it)
+  if (p.dx16) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) dx_max = fmaxf(dx_max, __shfl_xor_sync(0xffffffffu, dx_max, o));
+    if (lane == 0) atomicMax(p.amax + 2, __float_as_uint(dx_max));   // non-negative: bits order like values
+  }
 
-  // ---- per-CTA partial sums: d(gamma_out), d(beta_out) over the lane quarters; dW_g, dW_o from TMEM
-  if (ok) {
+  // ---- per-CTA partial sums, added to: d(gamma_out), d(beta_out) over the lane quarters; dW_g, dW_o
+  // from TMEM
+  if (ok && p.part_w && local > 0) {
     sm.red[lq][c0 + lane] = acc_g;
     sm.red[lq][kC + c0 + lane] = acc_b;
     __syncthreads();
     for (int k = tid; k < 2 * kC; k += NT)
-      p.part_ln[(long long)blockIdx.x * 2 * kC + k] = ((sm.red[0][k] + sm.red[1][k]) + sm.red[2][k]) + sm.red[3][k];
+      p.part_ln[(long long)blockIdx.x * 2 * kC + k] += ((sm.red[0][k] + sm.red[1][k]) + sm.red[2][k]) + sm.red[3][k];
     float* pw = p.part_w + (long long)blockIdx.x * 2 * kC * kC + (long long)r * kC + c0;
 #pragma unroll 1
     for (int m = 0; m < 2; ++m) {
@@ -335,7 +342,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_output(const BwdOutParams p) {
       tmem_ld_wait();
       const float u = m == 0 ? u_wg : u_wo;
 #pragma unroll
-      for (int e = 0; e < 32; ++e) pw[m * kC * kC + e] = local > 0 ? __uint_as_float(rr[e]) * u : 0.f;
+      for (int e = 0; e < 32; ++e) pw[m * kC * kC + e] += __uint_as_float(rr[e]) * u;
     }
   }
   tc_fence_before();
@@ -375,29 +382,37 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_project(const BwdProjParams p) {
   const uint32_t a_zh = smem_u32(sm.zh), a_dv = smem_u32(sm.dv), a_dg = smem_u32(sm.dg);
   const uint32_t a_wv = smem_u32(sm.wv), a_wgt = smem_u32(sm.wgt);
   const int c0 = 32 * h;
-  // dV arrives times sx (the fp16 scale of dX, from its recorded maximum) and times the fp16 scale of
-  // its contraction partner (in the host factors below)
-  const float ix = 1.f / pow2_scale(__uint_as_float(p.amax[1]), 14);
-  const float u1 = p.u_dzh_v * ix, u2 = p.u_dzh_g * ix, u3 = p.u_wv * ix, u4 = p.u_wgt * ix;
+  // dV arrives times the fp16 scale of dX (from the bound in amax[1]) and times the fp16 scale of its
+  // contraction partner (in the host factors below)
+  // dpv, dpg are stored times q1, q2: powers of two from the largest |dV| the operands allow (N times
+  // the largest fp16 dX, times the partner's 2^14), which keep them below 2^14 in fp16
+  const float sdx = pow2_scale(__uint_as_float(p.amax[1]), 14);
+  const float raw = p.q_raw * __uint_as_float(p.amax[2]) * sdx;
+  const float q1 = pow2_scale(raw, 14), q2 = pow2_scale(raw * p.q2f, 14);
+  const float u1 = p.u_dzh_v / (q1 * sdx), u2 = p.u_dzh_g / (q2 * sdx), u3 = p.u_wv / (q1 * sdx),
+              u4 = p.u_wgt / (q2 * sdx);
 
   float acc_g = 0.f, acc_b = 0.f;
   uint32_t phase = 0;
   int local = 0;
   bool ok = true;
   for (long long t = blockIdx.x; t < p.tiles; t += gridDim.x, ++local) {
-    const long long pr = t * BT + r;
-    const bool valid = pr < p.P;
-    const int i = valid ? (int)(pr / p.N) : 0;
-    const int k2 = valid ? (int)(pr - (long long)i * p.N) : 0;
+    const long long pl = t * BT + r;               // pair of the range
+    const bool valid = pl < p.P;
+    const long long pr = p.p0 + (valid ? pl : 0);  // pair of the grid
+    const int i = (int)(pr / p.N);
+    const int k2 = (int)(pr - (long long)i * p.N);
+    const long long hz = pr - p.dzh_off;           // its dzh column
     {
       // L2 prefetch of the next tile's dV (threads 0..127), dzh (128..255), z and statistics
       const long long tn = t + gridDim.x;
       if (tn < p.tiles && p.N >= BT) {
         const long long q0 = tn * BT, q1 = (q0 + BT < p.P) ? q0 + BT : p.P;
+        const long long g0 = p.p0 + q0, g1 = p.p0 + q1, h0 = g0 - p.dzh_off, h1 = g1 - p.dzh_off;
         if (tid < kC) prefetch_plane_rows(p.dV + (long long)tid * p.vplane, p.ldv, p.N, q0, q1);
-        else if (tid < 2 * kC) prefetch_range(p.dzh, ((tid - kC) * p.P + q0) * 4, ((tid - kC) * p.P + q1) * 4);
-        else if (tid == 2 * kC) prefetch_range(p.z, q0 * 2 * kC, q1 * 2 * kC);
-        else if (tid == 2 * kC + 1) prefetch_range(p.zstat, q0 * 8, q1 * 8);
+        else if (tid < 2 * kC) prefetch_range(p.dzh, ((tid - kC) * p.dzh_P + h0) * 4, ((tid - kC) * p.dzh_P + h1) * 4);
+        else if (tid == 2 * kC) prefetch_range(p.z, g0 * 2 * kC, g1 * 2 * kC);
+        else if (tid == 2 * kC + 1) prefetch_range(p.zstat, g0 * 8, g1 * 8);
       }
     }
 
@@ -406,7 +421,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_project(const BwdProjParams p) {
     const float m = valid ? (p.mask ? p.mask[i] * p.mask[k2] : 1.f) : 0.f;
     float dv[32];
     {
-      const float* vp = p.dV + (long long)i * p.ldv + k2 + (long long)c0 * p.vplane;
+      const float* vp = p.dV + (long long)(i - p.i_off) * p.ldv + k2 + (long long)c0 * p.vplane;
 #pragma unroll
       for (int e = 0; e < 32; ++e) dv[e] = valid ? vp[e * p.vplane] * m : 0.f;
     }
@@ -435,8 +450,8 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_project(const BwdProjParams p) {
       for (int e = 0; e < 16; ++e) {
         const float d = dv[16 * hh + e];
         const float s = sigmoid_mufu(__uint_as_float(rg[e]) * p.u_pg);
-        fv[e] = d * s * p.q1;
-        fg[e] = d * (__uint_as_float(rv[e]) * p.u_pv) * s * (1.f - s) * p.q2;
+        fv[e] = d * s * q1;
+        fg[e] = d * (__uint_as_float(rv[e]) * p.u_pv) * s * (1.f - s) * q2;
       }
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
@@ -459,7 +474,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_project(const BwdProjParams p) {
     // the earlier terms of dzh, read while the MMA runs
     float dzh[32];
 #pragma unroll
-    for (int e = 0; e < 32; ++e) dzh[e] = valid ? p.dzh[(long long)(c0 + e) * p.P + pr] : 0.f;
+    for (int e = 0; e < 32; ++e) dzh[e] = valid ? p.dzh[(long long)(c0 + e) * p.dzh_P + hz] : 0.f;
     if (!cta_wait(&sm.bar, phase, p.w, &sm.abort_flag, 2)) { ok = false; break; }
     phase ^= 1u;
     tc_fence_after();
@@ -475,7 +490,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_project(const BwdProjParams p) {
     if (!p.final_pass) {
       if (valid)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) p.dzh[(long long)(c0 + e) * p.P + pr] = dzh[e];
+        for (int e = 0; e < 32; ++e) p.dzh[(long long)(c0 + e) * p.dzh_P + hz] = dzh[e];
     } else {
       // LayerNorm_in backward: n = z rstd - rstd mu from the stored statistics
       float n[32];
@@ -525,13 +540,14 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_project(const BwdProjParams p) {
     }
   }
 
-  if (ok) {
+  // per-CTA partial sums, added to
+  if (ok && local > 0) {
     if (p.final_pass) {
       sm.red[lq][c0 + lane] = acc_g;
       sm.red[lq][kC + c0 + lane] = acc_b;
       __syncthreads();
       for (int k = tid; k < 2 * kC; k += NT)
-        p.part_ln[(long long)blockIdx.x * 2 * kC + k] = ((sm.red[0][k] + sm.red[1][k]) + sm.red[2][k]) + sm.red[3][k];
+        p.part_ln[(long long)blockIdx.x * 2 * kC + k] += ((sm.red[0][k] + sm.red[1][k]) + sm.red[2][k]) + sm.red[3][k];
     }
     float* pw = p.part_w + (long long)blockIdx.x * 2 * kC * kC + (long long)r * kC + c0;
 #pragma unroll 1
@@ -541,7 +557,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_project(const BwdProjParams p) {
       tmem_ld_wait();
       const float u = mm == 0 ? u3 : u4;
 #pragma unroll
-      for (int e = 0; e < 32; ++e) pw[mm * kC * kC + e] = local > 0 ? __uint_as_float(rr[e]) * u : 0.f;
+      for (int e = 0; e < 32; ++e) pw[mm * kC * kC + e] += __uint_as_float(rr[e]) * u;
     }
   }
   tc_fence_before();
@@ -572,59 +588,6 @@ __global__ void __launch_bounds__(256) k_absmax_bf16(const __nv_bfloat16* __rest
   }
 }
 
-constexpr int kTransposePlanes = 16;   // channel planes per block (the same 64 x 64 tile of each)
-
-// dX (float32 planes [128][N][ldx], over x) -> fp16 dX and its per-channel transpose dX^T (planes
-// [128][N][ld]), every value times sx = the power of two that brings the largest |dX| (recorded by
-// the output backward) to just below 2^14. 64 x 64 tiles, 16 channel planes per block, two elements
-// per thread: rows start 128-byte aligned and every thread takes an even column pair, so a pair
-// inside the grid moves as one 8-byte load and one 4-byte store (scalar at the grid's ragged edge).
-__global__ void __launch_bounds__(256) k_convert_transpose(const float* __restrict__ in, long long ldx,
-                                                           long long in_plane, const unsigned* __restrict__ amax,
-                                                           __half* __restrict__ out, __half* __restrict__ outT,
-                                                           int N, long long ld, long long plane) {
-  __shared__ __half t[64][64 + 2];
-  const int i0 = blockIdx.y * 64, j0 = blockIdx.x * 64;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8
-  const float sx = pow2_scale(__uint_as_float(*amax), 14);
-  const __half zero = __float2half_rn(0.f);
-  for (int c = blockIdx.z * kTransposePlanes; c < (blockIdx.z + 1) * kTransposePlanes; ++c) {
-    const float* src = in + c * in_plane;
-    __half* dst = out + c * plane;
-    __half* dstT = outT + c * plane;
-    if (c > blockIdx.z * kTransposePlanes) __syncthreads();   // the previous plane's tile has been written out
-    for (int r = ty; r < 64; r += 8) {
-      const int i = i0 + r, j = j0 + 2 * tx;
-      __half2 v;
-      v.x = zero;
-      v.y = zero;
-      if (i < N && j + 1 < N) {
-        const float2 f = *reinterpret_cast<const float2*>(src + (long long)i * ldx + j);
-        v = __floats2half2_rn(f.x * sx, f.y * sx);
-        *reinterpret_cast<__half2*>(dst + (long long)i * ld + j) = v;
-      } else if (i < N && j < N) {
-        v.x = __float2half_rn(src[(long long)i * ldx + j] * sx);
-        dst[(long long)i * ld + j] = v.x;
-      }
-      t[r][2 * tx] = v.x;
-      t[r][2 * tx + 1] = v.y;
-    }
-    __syncthreads();
-    for (int r = ty; r < 64; r += 8) {
-      const int j = j0 + r, i = i0 + 2 * tx;
-      if (j >= N || i >= N) continue;
-      if (i + 1 < N) {
-        __half2 v;
-        v.x = t[2 * tx][r];
-        v.y = t[2 * tx + 1][r];
-        *reinterpret_cast<__half2*>(dstT + (long long)j * ld + i) = v;
-      } else {
-        dstT[(long long)j * ld + i] = t[2 * tx][r];
-      }
-    }
-  }
-}
-
 }  // namespace
 
 constexpr size_t kOutSmemBytes = sizeof(OutSmem) + 1024;
@@ -645,14 +608,6 @@ cudaError_t launch_bwd_project_bf16(const BwdProjParams& p, int grid, cudaStream
   cudaError_t e = cudaFuncSetAttribute(k_bwd_project, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kProjSmemBytes);
   if (e != cudaSuccess) return e;
   k_bwd_project<<<grid, NT, kProjSmemBytes, s>>>(p);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_convert_transpose(const float* in, long long ldx, const unsigned* amax, __half* out, __half* outT,
-                                    int N, long long ld, int planes, cudaStream_t s) {
-  if (planes % kTransposePlanes) return cudaErrorInvalidValue;
-  dim3 grid((N + 63) / 64, (N + 63) / 64, planes / kTransposePlanes);
-  k_convert_transpose<<<grid, 256, 0, s>>>(in, ldx, (long long)N * ldx, amax, out, outT, N, ld, (long long)N * ld);
   return cudaGetLastError();
 }
 

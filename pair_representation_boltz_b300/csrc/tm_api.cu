@@ -310,6 +310,16 @@ tm_status prepare_tensor_core_weights(tm_ctx* c, const tm_weights* w) {
     c->zh_bound = zb;
     c->xh_bound = xb;
     c->y_bound = yb;
+    // dL/dx = r_x (u - mean(u) - n mean(u n)) with u = gamma_out dxh, dxh = W_o^T (dout sigmoid(g)),
+    // n = x_hat: r_x <= 1/sqrt(eps), |n_c| <= sqrt(c_h), |mean(u n)| <= max|u|, |u_c| <= |gamma_out,c|
+    // ||W_o[:, c]||_1 max|dout|
+    double ub = 0;
+    for (int k = 0; k < C; ++k) {
+      double s1 = 0;
+      for (int o = 0; o < C; ++o) s1 += std::fabs((double)w->w_o[(size_t)o * C + k]);
+      ub = std::max(ub, std::fabs((double)w->ln_out_gamma[k]) * s1);
+    }
+    c->dx_bound = (2.0 + std::sqrt((double)C)) / std::sqrt(1e-5) * ub;
     std::vector<float> ln(4 * C);
     for (int k = 0; k < C; ++k) {
       ln[k] = w->ln_in_gamma[k];
@@ -388,21 +398,19 @@ tm_status run_project_bf16(tm_ctx* c, const void* z, const float* mask, int N, f
   return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "projection launch");
 }
 
-tm_status run_contract_bf16(tm_ctx* c, const void* a, const void* b, int N, int ld, bool incoming,
+tm_status run_contract_bf16(tm_ctx* c, const void* a, const void* b, int N, int ld, int mode,
                             int i0, int j0, int bi, int bj, void* x, int ldx, XFormat xf, int x_exp,
                             cudaStream_t s, const tm_options* opt, bool ab_f16, bool accumulate) {
   CUtensorMap amap, bmap;
   const cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)N, (cuuint64_t)kC};
   const cuuint64_t str[2] = {(cuuint64_t)ld * 2, (cuuint64_t)N * ld * 2};
-  if (!incoming) {
-    if (!encode(&amap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a, dims, str, kBoxContractOutA, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode(&bmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, b, dims, str, kBoxContractOutB, CU_TENSOR_MAP_SWIZZLE_128B))
-      return fail(c, TM_ERR_CUDA, "tensor map (a/b, outgoing)");
-  } else {
-    if (!encode(&amap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a, dims, str, kBoxContractIn, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode(&bmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, b, dims, str, kBoxContractIn, CU_TENSOR_MAP_SWIZZLE_128B))
-      return fail(c, TM_ERR_CUDA, "tensor map (a/b, incoming)");
-  }
+  // A along k (outgoing, mixed) or along i (incoming); B along k (outgoing) or along j (incoming, mixed)
+  const bool a_k = mode != CONTRACT_IN, b_k = mode == CONTRACT_OUT;
+  if (!encode(&amap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a, dims, str, a_k ? kBoxContractOutA : kBoxContractIn,
+              CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode(&bmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, b, dims, str, b_k ? kBoxContractOutB : kBoxContractIn,
+              CU_TENSOR_MAP_SWIZZLE_128B))
+    return fail(c, TM_ERR_CUDA, "tensor map (a/b, contraction)");
   ContractParams p;
   p.x = x;
   p.ab_f16 = ab_f16 ? 1 : 0;
@@ -443,7 +451,7 @@ tm_status run_contract_bf16(tm_ctx* c, const void* a, const void* b, int N, int 
   }
   p.w = watch(c, KID_CONTRACT, opt);
   cudaError_t e = timed(c, 1, (long long)kC * bi * bj, s,
-                        [&] { return launch_contract_bf16(incoming, amap, bmap, xmap, p, c->num_sms, s); });
+                        [&] { return launch_contract_bf16(mode, amap, bmap, xmap, p, c->num_sms, s); });
   return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "contraction launch");
 }
 
@@ -692,7 +700,7 @@ tm_status tm_contract_ex(tm_ctx* c, const void* a, const void* b, int N, int ld,
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool inc = dir == TM_INCOMING;
   if (dtype == TM_BF16)
-    return run_contract_bf16(c, a, b, N, ld, inc, i0, j0, bi, bj, x, ldx, x16 ? X_F16 : X_F32,
+    return run_contract_bf16(c, a, b, N, ld, inc ? CONTRACT_IN : CONTRACT_OUT, i0, j0, bi, bj, x, ldx, x16 ? X_F16 : X_F32,
                              x16 ? x16_exponent(c, N) : 0, s, nullptr);
   cudaError_t e = timed(c, 3, (long long)c->c_h * bi * bj, s, [&] {
     return launch_contract_f32(inc, reinterpret_cast<const float*>(a), reinterpret_cast<const float*>(b), N, ld,
@@ -765,7 +773,7 @@ tm_status tm_contract_block(tm_ctx* c, const void* a, const void* b, int B, int 
   if (ld < B || ld % 8) return fail(c, TM_ERR_INVALID, "ld=%d must be >= B and a multiple of 8", ld);
   if (ldx < B || ldx % 4) return fail(c, TM_ERR_INVALID, "ldx=%d must be >= B and a multiple of 4", ldx);
   if (accumulate != 0 && accumulate != 1) return fail(c, TM_ERR_INVALID, "accumulate must be 0 or 1");
-  return run_contract_bf16(c, a, b, B, ld, dir == TM_INCOMING, 0, 0, B, B, x, ldx, X_F32, 0,
+  return run_contract_bf16(c, a, b, B, ld, dir == TM_INCOMING ? CONTRACT_IN : CONTRACT_OUT, 0, 0, B, B, x, ldx, X_F32, 0,
                            reinterpret_cast<cudaStream_t>(stream), nullptr, false, accumulate == 1);
 }
 
@@ -829,7 +837,7 @@ tm_status tm_forward_ex(tm_ctx* c, const void* z, const float* mask, int N, tm_d
       for (int j0 = 0; j0 < N; j0 += B) {
         const int bi = std::min(B, N - i0), bj = std::min(B, N - j0);
         st = run_contract_bf16(c, reinterpret_cast<const __nv_bfloat16*>(a), reinterpret_cast<const __nv_bfloat16*>(b),
-                               N, ld, inc, i0, j0, bi, bj, x, ldx, xf, x_exp, s, opt);
+                               N, ld, inc ? CONTRACT_IN : CONTRACT_OUT, i0, j0, bi, bj, x, ldx, xf, x_exp, s, opt);
         if (st != TM_OK) return st;
         st = run_finish_bf16(c, x, ldx, xf, x_exp, zstat, z, N, i0, j0, bi, bj, out, residual, s, opt);
         if (st != TM_OK) return st;
@@ -969,7 +977,7 @@ tm_status tm_forward_host(tm_ctx* c, const void* z_host, const float* mask_host,
     const size_t row_bytes = (size_t)N * kC * 2;
     for (int k = 0; k < strips; ++k) {
       const int i0 = k * R, bi = std::min(R, N - i0);
-      st = run_contract_bf16(c, a, b, N, ld, dir == TM_INCOMING, i0, 0, bi, N, x, ldx, X_F16, x_exp, s, nullptr);
+      st = run_contract_bf16(c, a, b, N, ld, dir == TM_INCOMING ? CONTRACT_IN : CONTRACT_OUT, i0, 0, bi, N, x, ldx, X_F16, x_exp, s, nullptr);
       if (st == TM_OK && k == 0 && (e = cudaStreamWaitEvent(s, c->ev_out[slot], 0)) != cudaSuccess)
         return cuda_fail(c, e, "event");
       if (st == TM_OK) st = run_finish_bf16(c, x, ldx, X_F16, x_exp, zstat, zd, N, i0, 0, bi, N, od, false, s, nullptr);
@@ -1113,7 +1121,7 @@ extern "C" tm_status tm_forward_noalloc(tm_ctx* c, const void* z, const float* m
   const int x_exp = x16_exponent(c, N);
   st = run_project_bf16(c, z, mask, N, zstat, a, b, ld, s, nullptr);
   if (st == TM_OK)
-    st = run_contract_bf16(c, a, b, N, ld, dir == TM_INCOMING, 0, 0, N, N, x, ldx, X_F16, x_exp, s, nullptr);
+    st = run_contract_bf16(c, a, b, N, ld, dir == TM_INCOMING ? CONTRACT_IN : CONTRACT_OUT, 0, 0, N, N, x, ldx, X_F16, x_exp, s, nullptr);
   if (st == TM_OK) st = run_finish_bf16(c, x, ldx, X_F16, x_exp, zstat, z, N, 0, 0, N, N, out, false, s, nullptr);
   c->timing = timing;
   return st;

@@ -56,6 +56,8 @@ struct tm_ctx {
   void* wbwd = nullptr;
   int bwd_wexp[6] = {};
   double pv_bound[2] = {}, zh_bound = 0, xh_bound = 0, y_bound = 0;
+  // |dL/dx| <= dx_bound * max |dout|: the fp16 scale of the backward's dX
+  double dx_bound = 0;
   // triangle attention: fp16 images of W_q, W_k, W_v, W_g, W_o (each scaled by a power of two), then
   // gamma and beta (times the power of two zh is stored with) and W_b (float32); the factors that undo
   // the scales
@@ -113,7 +115,7 @@ tm_status run_project_bf16(tm_ctx* c, const void* z, const float* mask, int N, f
                            void* b, int ld, cudaStream_t s, const tm_options* opt, bool out_f16 = false,
                            float scale_a = 1.f, float scale_b = 1.f, const float* mask_col = nullptr,
                            bool separate_col_mask = false);
-tm_status run_contract_bf16(tm_ctx* c, const void* a, const void* b, int N, int ld, bool incoming,
+tm_status run_contract_bf16(tm_ctx* c, const void* a, const void* b, int N, int ld, int mode,
                             int i0, int j0, int bi, int bj, void* x, int ldx, XFormat xf, int x_exp,
                             cudaStream_t s, const tm_options* opt, bool ab_f16 = false, bool accumulate = false);
 // 2^(target - E) for the exponent E with 2^(E-1) <= bound < 2^E (bound > 0), else 1: the power of two

@@ -76,7 +76,10 @@ struct FinishParams {
 
 cudaError_t launch_project_bf16(const CUtensorMap& zmap, const CUtensorMap& wmap, const CUtensorMap& amap,
                                 const CUtensorMap& bmap, const ProjectParams& p, int num_sms, cudaStream_t s);
-cudaError_t launch_contract_bf16(bool incoming, const CUtensorMap& amap, const CUtensorMap& bmap,
+// The contraction's operand forms: outgoing x_ij = sum_k a_ik b_jk, incoming x_ij = sum_k a_ki b_kj, and
+// mixed x_ij = sum_k a_ik b_kj (float32 x only).
+enum ContractMode : int { CONTRACT_OUT = 0, CONTRACT_IN = 1, CONTRACT_MIXED = 2 };
+cudaError_t launch_contract_bf16(int mode, const CUtensorMap& amap, const CUtensorMap& bmap,
                                  const CUtensorMap& xmap, const ContractParams& p, int num_sms, cudaStream_t s);
 // x16 selects the fp16 x tile (kBoxFinishX16, double-buffered) instead of the float32 one.
 cudaError_t launch_finish_bf16(bool x16, const CUtensorMap& xmap, const CUtensorMap& zmap,
@@ -154,57 +157,64 @@ cudaError_t launch_outer_sum_f32(const float* U, const float* V, int O, int K, l
 // tensor-core operand is fp16, stored times a power of two; the u_* factors undo, in each product's
 // epilogue, the scales its operands carry (the host's part; a part set by a recorded maximum, amax, is
 // computed on the device).
+// Output backward over one block of the pair grid: pairs (i0 + il, j0 + jl), il < bi, jl < bj (the whole
+// grid: 0, 0, N, N), with x the contraction's block [128][bi][ldx].
 struct BwdOutParams {
   const __nv_bfloat16* z;         // [N][N][128]
   const float2* zstat;            // [N][N] (rstd, -rstd mu) of LayerNorm_in (projection kernel)
-  float* x;                       // [128][N][ldx] float32: the contraction's x times 1 / x_unscale in,
-                                  // dL/dx out (in place)
+  const float* x;                 // [128][bi][ldx] float32: the contraction's x times 1 / x_unscale
   long long ldx, xplane;          // row and channel strides of x
   float x_unscale;
   const __nv_bfloat16* dout;      // [N][N][128]
-  unsigned* amax;                 // [0] largest |dout| (read), [1] largest |dX| (merged in), float bits
+  unsigned* amax;                 // [0] largest |dout| (read); [1] the bound on |dX| that fixes dX's fp16
+                                  // scale (written); [2] largest |dX| (merged in); float bits
+  float dx_bound;                 // |dX| <= dx_bound * largest |dout|
   float y_bound4;                 // bound on |W_o xh| / 4 (dgg's scale)
   float sz, sx;                   // zh, xh are stored times sz, sx
   float u_gg, u_y;                // gg = MMA * u_gg, y = MMA * u_y
   float u_dxh, u_dzh, u_wg, u_wo; // dxh, dzh_g, dW_g, dW_o: host parts of the unscale
-  float* dzh;                     // [128][N*N] written: the gate's term of dL/dzh
-  float* part_w;                  // [grid][2][128][128] per-CTA sums of dW_g, dW_o
-  float* part_ln;                 // [grid][256] per-CTA sums of d(gamma_out), d(beta_out)
+  __half* dx16;                   // [128][N][ldd] fp16 dL/dx times its scale, or nullptr (not written)
+  long long ldd, dxplane;
+  float* dzh;                     // [128][dzh_P]: the gate's term of dL/dzh of pair p at p - dzh_off, or
+  long long dzh_P, dzh_off;       // nullptr (not written)
+  float* part_w;                  // [grid][2][128][128] per-CTA sums of dW_g, dW_o (added to), or nullptr
+  float* part_ln;                 // [grid][256] per-CTA sums of d(gamma_out), d(beta_out) (added to)
   const __half *w_g, *w_o;        // fp16 weight images (times powers of two) in the swizzled tile layout
   const float* ln;                // gamma_in, beta_in, gamma_out, beta_out (float32, 4 x 128)
   int N;
-  long long P, tiles;
+  int i0, j0, bi, bj;
+  long long tiles;                // ceil(bi bj / 128)
   Watch w;
 };
+// Projection backward over the pairs [p0, p0 + P) of the flattened grid (whole rows: p0 = i_off N).
 struct BwdProjParams {
   const __nv_bfloat16* z;
   const float2* zstat;
   const float* mask;              // [N] or nullptr
-  const float* dV;                // [128][N][ldv] float32: dL/da or dL/db times (dX's scale x partner's)
+  const float* dV;                // [128][rows][ldv] float32, rows i_off.. : dL/da or dL/db times (dX's
+                                  // scale x partner's)
   long long ldv, vplane;
-  const unsigned* amax;           // [1]: largest |dX| (float bits), which fixes dX's scale
+  const unsigned* amax;           // [1] the bound on |dX|, which fixes dX's scale; [2] largest |dX| (bits)
   float sz;                       // zh is stored times sz
   float u_pv, u_pg;               // pv = MMA * u_pv, pg = MMA * u_pg
-  float q1, q2;                   // dpv, dpg stored times dV's scale x q1, q2
+  float q_raw, q2f;               // |dV| <= q_raw x (largest fp16 dX); |dpg| / |dpv| <= q2f
   float u_dzh_v, u_dzh_g, u_wv, u_wgt;   // host parts of the unscales of the W^T products and dW
-  float* dzh;                     // [128][N*N], accumulated
+  float* dzh;                     // [128][dzh_P], pair p at p - dzh_off, accumulated
+  long long dzh_P, dzh_off;
   __nv_bfloat16* dz;              // [N][N][128] (final pass)
   int final_pass;                 // 1: add this side's term, then LayerNorm_in backward into dz
-  float* part_w;                  // [grid][2][128][128] per-CTA sums of dW_v, dW_gt
-  float* part_ln;                 // [grid][256] per-CTA sums of d(gamma_in), d(beta_in) (final pass)
+  float* part_w;                  // [grid][2][128][128] per-CTA sums of dW_v, dW_gt (added to)
+  float* part_ln;                 // [grid][256] per-CTA sums of d(gamma_in), d(beta_in) (final pass, added to)
   const __half *w_v, *w_gt;
   const float* ln;                // gamma_in, beta_in
   int N;
-  long long P, tiles;
+  int i_off;
+  long long p0, P, tiles;
   Watch w;
 };
 int bwd_grid(long long tiles, int num_sms);
 cudaError_t launch_bwd_output_bf16(const BwdOutParams& p, int grid, cudaStream_t s);
 cudaError_t launch_bwd_project_bf16(const BwdProjParams& p, int grid, cudaStream_t s);
-// fp16 dX and dX^T planes [planes][N][ld] from the float32 dX planes [planes][N][ldx], times the power of
-// two set by the recorded maximum *amax
-cudaError_t launch_convert_transpose(const float* in, long long ldx, const unsigned* amax, __half* out, __half* outT,
-                                    int N, long long ld, int planes, cudaStream_t s);
 // *out = max(*out, bits of the largest |v|) over n bf16 values
 cudaError_t launch_absmax_bf16(const __nv_bfloat16* v, long long n, unsigned* out, int num_sms, cudaStream_t s);
 // out[e] = sum over q < S of part[q * stride + e], e < E, in order q = 0, 1, ...

@@ -435,11 +435,13 @@ def tm_ctx_info(ctx) -> dict:
     return {"c_z": c_z, "c_hidden": c_h, "layer": layer}
 
 
-def tm_backward(ctx, z, mask, direction, dout, dz, grads=None, stream=None, timeout_ms=0, workspace_limit=0):
+def tm_backward(ctx, z, mask, direction, dout, dz, grads=None, stream=None, timeout_ms=0, workspace_limit=0,
+                block=0):
     """dz = dL/dz and grads[name] = dL/dW for the cotangent dout of out = update(z).
 
     grads: dict of contiguous float32 CUDA tensors keyed by parameter name (a missing key is not
-    written), or None. dz may be dout itself."""
+    written), or None. dz may be dout itself. block: edge of the square blocks of the block-streamed
+    schedule (bf16; 0 = automatic)."""
     g = None
     c_z, c_h, _ = _ctx_dims(ctx)
     if grads is not None:
@@ -450,7 +452,9 @@ def tm_backward(ctx, z, mask, direction, dout, dz, grads=None, stream=None, time
     check_mask(mask, N)
     if grads is not None:
         g = TmGrads(*[_ptr(grads[n]) if n in grads else None for n in WEIGHT_FIELDS])
-    opt = TmOptions(0, timeout_ms, workspace_limit, 0, 0)
+    if not isinstance(block, int) or block < 0:
+        raise ValueError(f"block must be a non-negative int, got {block!r}")
+    opt = TmOptions(block, timeout_ms, workspace_limit, 0, 0)
     _check(ctx, load_library().tm_backward(ctx, _ptr(z), _ptr(mask), N, _dtype_code(z), _direction(direction),
                                            _ptr(dout), _ptr(dz), C.byref(g) if g is not None else None,
                                            _stream(stream), C.byref(opt)))

@@ -157,6 +157,59 @@ def bf16_gate(got, ref):
     return met
 
 
+@pytest.mark.parametrize("direction", ("outgoing", "incoming"))
+def test_backward_bf16_block_streamed(torch_tm, direction):
+    """The block-streamed schedule (blocks of 128 over N = 300: three block rows, the last 44 wide):
+    dz bit for bit the whole-grid schedule's (the same per-pair arithmetic, the same order over k in
+    every contraction), the parameter gradients within float32 reordering of their sums over pairs
+    (the CTAs' shares of the pairs differ), and the oracle's gates."""
+    torch, tm = torch_tm
+    N = 300
+    W = wl.make_weights(128, 128, 3, ln_random=True)
+    z_np = wl.make_z(N, 128, 21, "bf16")
+    m_np = wl.make_mask(N, "scatter", 22)
+    dout_np = _dout(N, 128, 23, "bf16")
+    mod = tm.TriMul(128, 128, W)
+    try:
+        z = z_to_device(z_np)
+        dout = z_to_device(dout_np)
+        m = mask_to_device(m_np)
+        dz_w, g_w = mod.backward(z, dout, m, direction)
+        dz_b, g_b = mod.backward(z, dout, m, direction, block=128)
+        torch.cuda.synchronize()
+        assert tm.tm_sync_status(mod.ctx) == tm.TM_OK
+        assert torch.equal(dz_b, dz_w)
+        for k in g_w:
+            d = (g_b[k] - g_w[k]).abs().max().item()
+            assert d <= 1e-5 * g_w[k].abs().max().item(), (k, d)
+        got = {"z": to_f64(dz_b)}
+        got.update({k: v.double().cpu().numpy() for k, v in g_b.items()})
+    finally:
+        mod.close()
+    ref = oracle.full_backward(wl.as_f64(z_np), m_np, W, direction, wl.as_f64(dout_np), storage="bf16")
+    met = bf16_gate(got, ref)
+    _log(f"bf16_N{N}_block128_{direction}", met)
+
+
+def test_backward_block_edge_is_checked(torch_tm):
+    """A block edge below 128 or off the 8-element grid is refused before any launch."""
+    torch, tm = torch_tm
+    N = 300
+    mod = tm.TriMul(128, 128, wl.make_weights(128, 128, 1))
+    try:
+        z = z_to_device(wl.make_z(N, 128, 1, "bf16"))
+        dout = z_to_device(_dout(N, 128, 2, "bf16"))
+        dz = torch.empty_like(z)
+        launches = tm.tm_launch_count(mod.ctx)
+        for bad in (64, 100):
+            with pytest.raises(tm.TmError) as err:
+                tm.tm_backward(mod.ctx, z, None, "outgoing", dout, dz, None, block=bad)
+            assert err.value.status == tm.TM_ERR_INVALID
+        assert tm.tm_launch_count(mod.ctx) == launches
+    finally:
+        mod.close()
+
+
 def test_backward_bf16_is_deterministic_and_in_place(torch_tm):
     torch, tm = torch_tm
     N = 150

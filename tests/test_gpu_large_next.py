@@ -5,7 +5,8 @@ full mask), in the launch configuration the benchmark times.
   the float64 oracle's sampled lines, with the fixed gates of tests/test_gpu_attention.py;
 * backward: the gradient is linear in the cotangent and every stored rounding commutes with a factor
   of two, so tm_backward(2 dout) must equal 2 tm_backward(dout) bit for bit, for dz and every parameter;
-  all values finite.
+  all values finite. The same at N = 10000, where the backward runs block-streamed with a workspace
+  under 120 GB.
 """
 import numpy as np
 import pytest
@@ -69,6 +70,43 @@ def test_backward_complex3605_is_linear_in_the_cotangent(big, direction):
         assert tm.tm_sync_status(mod.ctx) == tm.TM_OK
         assert torch.isfinite(dz1.float()).all()
         assert torch.equal(dz2, dz1 * 2)
+        for k in g1:
+            assert torch.isfinite(g1[k]).all(), k
+            assert torch.equal(g2[k], g1[k] * 2), k
+    finally:
+        mod.close()
+
+
+def test_backward_n10000_block_streamed(big):
+    """N = 10000 (10^8 pairs): the automatic schedule streams blocks; its workspace stays under 120 GB.
+    2 dout (in place, dz over it) gives 2 dz bit for bit; everything finite, dz not zero."""
+    torch, tm, _, _ = big
+    N = 10000
+    mod = tm.TriMul(128, 128, wl.make_weights(128, 128, 1))
+    try:
+        gen = torch.Generator(device="cuda").manual_seed(11)
+        z = torch.empty((N, N, 128), device="cuda", dtype=torch.bfloat16)
+        dout = torch.empty_like(z)
+        for t in (z, dout):                            # row slabs: no float32 copy of the whole grid
+            for r0 in range(0, N, 500):
+                t[r0:r0 + 500] = torch.randn((min(500, N - r0), N, 128), device="cuda", generator=gen)
+        torch.cuda.empty_cache()
+        dz1, g1 = mod.backward(z, dout, None, "outgoing")
+        torch.cuda.synchronize()
+        assert tm.tm_sync_status(mod.ctx) == tm.TM_OK
+        assert tm.tm_workspace_bytes(mod.ctx) < 120e9, tm.tm_workspace_bytes(mod.ctx)
+        dout.mul_(2)                                   # exact in bf16
+        _, g2 = mod.backward(z, dout, None, "outgoing", dz=dout)
+        torch.cuda.synchronize()
+        assert tm.tm_sync_status(mod.ctx) == tm.TM_OK
+        del z
+        nonzero = False
+        for r0 in range(0, N, 500):                    # row slabs: no full-size temporaries
+            a = dz1[r0:r0 + 500]
+            assert torch.isfinite(a.float()).all()
+            assert torch.equal(dout[r0:r0 + 500], a * 2), r0
+            nonzero = nonzero or bool((a != 0).any())
+        assert nonzero
         for k in g1:
             assert torch.isfinite(g1[k]).all(), k
             assert torch.equal(g2[k], g1[k] * 2), k
