@@ -269,15 +269,25 @@ typedef struct {
  *          before dz is written), must not otherwise overlap dout or z;
  *   grads  device pointers (float32), or NULL to skip every parameter gradient.
  * Precisions: TM_F32 keeps every intermediate in float32 on the CUDA cores.
- * TM_BF16 recomputes a and b in bf16 as the forward stores them and x in
- * float32, and its contractions of the gradient (dX with b and a, the
- * per-pair W^T products, the parameter sums over N^2 pairs) run on the tensor
- * cores from bf16 operands with float32 accumulation; dA and dB are float32.
- * Workspace for TM_BF16: about 2.6 kB per pair (a, b, dX, dX^T in bf16; x
- * then dA, and dB in float32; dzh in float32): 33 GB at N = 3605, 109 GB at
- * N = 6500. Beyond the workspace limit it returns TM_ERR_OOM before any
- * launch. opt: timeout_ms and workspace_limit apply; block, x_storage and
- * residual must be 0. Stream-ordered like tm_forward. */
+ * TM_BF16 recomputes a and b as the forward stores them (bf16 values, held as
+ * fp16 times powers of two) and x in float32; dL/dx leaves the output backward
+ * as fp16 under a power of two fixed by a bound on it (a constant of the weights
+ * times the largest |dout|), and its contractions with b and a, the per-pair
+ * W^T products and the parameter sums over the N^2 pairs run on the tensor
+ * cores from fp16 operands with float32 accumulation; dA and dB are float32.
+ * Schedule and workspace for TM_BF16: a, b and dX (fp16 planes, 768 B per pair)
+ * plus, per row block of B rows, dA, dB and the gate's part of dL/dzh in float32
+ * and one B x B block of x: about 2.3 kB per pair for the whole grid at once
+ * (30 GB at N = 3605, 98 GB at N = 6500); when that would pass 100 GiB (or the
+ * workspace limit), the grid goes in blocks of B (2560, 2048, 1536, ...; N =
+ * 10000: B = 1536, 103 GB): x and the output backward block by block for dX,
+ * then row block by row block x again for dL/dzh, dA and dB of the rows and the
+ * projection backward over them. The result does not depend on B (dz bit for
+ * bit; the parameter sums up to float32 reordering). opt->block sets B (>= 128
+ * and a multiple of 8, or >= N for the whole grid; bf16 only). Beyond the
+ * workspace limit it returns TM_ERR_OOM before any launch. opt: timeout_ms,
+ * workspace_limit and block apply; x_storage and residual must be 0.
+ * Stream-ordered like tm_forward. */
 tm_status tm_backward(tm_ctx* ctx, const void* z, const float* mask, int N, tm_dtype dtype,
                       tm_direction dir, const void* dout, void* dz, const tm_grads* grads,
                       void* stream, const tm_options* opt);
