@@ -63,6 +63,37 @@ def profiled_traffic():
     return float(t.group(1)) if cur == h.group(1) else None
 
 
+def pcie_roofline(torch, host_src, host_dst, bytes_per_step, ms_per_step):
+    """The host-buffer step's bound: its copies at the host link's measured rate, copies in and out at
+    once on two streams (pinned buffers of one z each, best of four), as the step overlaps them."""
+    dev_in = torch.empty_like(host_src, device="cuda")
+    dev_out = torch.empty_like(host_dst, device="cuda")
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    best = None
+    for _ in range(4):
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        s_in.wait_event(e0)
+        s_out.wait_event(e0)
+        with torch.cuda.stream(s_in):
+            dev_in.copy_(host_src, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            host_dst.copy_(dev_out, non_blocking=True)
+        torch.cuda.current_stream().wait_stream(s_in)
+        torch.cuda.current_stream().wait_stream(s_out)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        best = ms if best is None or ms < best else best
+    nbytes = host_src.numel() * host_src.element_size() + host_dst.numel() * host_dst.element_size()
+    peak = nbytes / (best * 1e-3) / 1e9
+    achieved = bytes_per_step / (ms_per_step * 1e-3) / 1e9
+    del dev_in, dev_out
+    return {"bound": "pcie", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "peak_source": "host-to-device and device-to-host copies of one z each at once, measured here"}
+
+
 def device_code_sha256(path: str) -> str:
     """sha256 of a kernel file's device code: the text before its first host launcher definition
     ("cudaError_t launch_"), so that edits to the host-side launcher alone keep a profile's counters
@@ -469,6 +500,9 @@ def run_ours(args, w):
                "h2d_bytes_per_step": len(w.directions) * (zbytes + m_np.nbytes),
                "d2h_bytes_per_step": len(w.directions) * zbytes, "steps": k_e2e,
                "ms_per_step": ms_e2e / k_e2e}
+        e2e["roofline"] = pcie_roofline(torch, zp, outs_h[0], e2e["h2d_bytes_per_step"] + e2e["d2h_bytes_per_step"],
+                                        ms_e2e / k_e2e)
+        del outs_h
 
     # reference point for the contraction: cuBLAS (torch.bmm) over the 128 channel planes, bf16 in, bf16 out.
     # Timed at N rounded up to a multiple of 64 (the row padding the library's own a and b use): at N = 3605 a
