@@ -196,26 +196,66 @@ def _prefetch(base, b0, b1, alloc):
         assert (base + a0) % 16 == 0 and base + a0 >= 0 and base + a1 <= alloc, (base, a0, a1, alloc)
 
 
-@pytest.mark.parametrize("N", [128, 129, 200, 255, 256, 257, 511, 768, 1023, 1025, 3605])
-def test_backward_prefetch_ranges_stay_aligned_and_inside(N):
-    """The per-pair backward kernels prefetch, for the next tile of 128 flattened pairs, row segments of the
-    float32 planes x / dA / dB ([128][N][ldx], ldx a multiple of 32), the matching span of each channel of
-    dzh ([128][N*N]), and the tile's span of z and of the LayerNorm statistics. Every widened range must
-    start on 16 bytes and end inside its allocation."""
-    P, ldx = N * N, _up(N, 32)
-    xplane, xalloc = N * ldx, _up(128 * N * ldx * 4, 256)
-    hb, zst, zb = _up(128 * P * 4, 256), _up(P * 8, 256), P * 256
-    tiles = (P + 127) // 128
-    for tn in sorted(set(range(0, tiles, max(1, tiles // 97))) | {tiles - 1}):
-        q0, q1 = tn * 128, min(tn * 128 + 128, P)
-        i, j0 = divmod(q0, N)
-        n1 = min(q1 - q0, N - j0)
-        for c in (0, 1, 63, 127):
-            base = c * xplane * 4
-            _prefetch(base + i * ldx * 4, 4 * j0, 4 * (j0 + n1), xalloc)
-            if q0 + n1 < q1:
-                assert i + 1 < N
-                _prefetch(base + (i + 1) * ldx * 4, 0, 4 * (q1 - q0 - n1), xalloc)
-            _prefetch(0, (c * P + q0) * 4, (c * P + q1) * 4, hb)
-        _prefetch(0, q0 * 256, q1 * 256, zb)
-        _prefetch(0, q0 * 8, q1 * 8, zst)
+def _backward_blocks(N, B):
+    """The block edge the backward uses (B >= N: the whole grid) and its block rows."""
+    B = min(B, N)
+    return B, [(r0, min(B, N - r0)) for r0 in range(0, N, B)]
+
+
+@pytest.mark.parametrize("N,B", [(128, 128), (129, 129), (200, 200), (255, 255), (256, 256), (257, 257),
+                                 (511, 511), (768, 768), (1023, 1023), (1025, 1025), (3605, 3605),
+                                 (300, 128), (1025, 256), (3605, 1536)])
+def test_backward_prefetch_ranges_stay_aligned_and_inside(N, B):
+    """The per-pair backward kernels prefetch into L2, for the next tile of 128 pairs: the output stage
+    (over a block bi x bj of x [128][bi][ldxB]) row segments of each channel of x and, for whole grid
+    rows, the tile's span of z, dout and the LayerNorm statistics; the projection stage (over the pairs
+    of rb whole rows, dV [128][rb][ldx], the row block's dzh pair-major [rb N][128]) row segments of dV,
+    the tile's dzh rows, z and the statistics. Every widened range must start on 16 bytes and end inside
+    its allocation."""
+    P = N * N
+    B, rows = _backward_blocks(N, B)
+    ldxN, ldxB = _up(N, 32), _up(B, 32)
+    xalloc = _up(128 * B * (ldxN if len(rows) == 1 else ldxB) * 4, 256)
+    valloc = _up(128 * B * ldxN * 4, 256)
+    hb, zst, zb = _up(128 * B * N * 4, 256), _up(P * 8, 256), P * 256
+    ldx = ldxN if len(rows) == 1 else ldxB
+    # output stage, one block
+    for (i0, bi) in rows[:2] + rows[-1:]:
+        for (j0, bj) in rows[:1] + rows[-1:]:
+            PB = bi * bj
+            tiles = (PB + 127) // 128
+            if bj < 128:
+                continue
+            for tn in sorted(set(range(0, tiles, max(1, tiles // 61))) | {tiles - 1}):
+                q0, q1 = tn * 128, min(tn * 128 + 128, PB)
+                il, jl = divmod(q0, bj)
+                n1 = min(q1 - q0, bj - jl)
+                for c in (0, 1, 127):
+                    base = c * bi * ldx * 4
+                    _prefetch(base + il * ldx * 4, 4 * jl, 4 * (jl + n1), xalloc)
+                    if q0 + n1 < q1:
+                        assert il + 1 < bi
+                        _prefetch(base + (il + 1) * ldx * 4, 0, 4 * (q1 - q0 - n1), xalloc)
+                if bj == N:
+                    g0, g1 = i0 * N + q0, i0 * N + q1
+                    _prefetch(0, g0 * 256, g1 * 256, zb)
+                    _prefetch(0, g0 * 8, g1 * 8, zst)
+    # projection stage, one block row
+    for (r0, rb) in rows[:2] + rows[-1:]:
+        Pr = rb * N
+        tiles = (Pr + 127) // 128
+        for tn in sorted(set(range(0, tiles, max(1, tiles // 61))) | {tiles - 1}):
+            q0, q1 = tn * 128, min(tn * 128 + 128, Pr)
+            il, k0 = divmod(q0, N)
+            n1 = min(q1 - q0, N - k0)
+            for c in (0, 1, 127):
+                base = c * rb * ldxN * 4
+                _prefetch(base + il * ldxN * 4, 4 * k0, 4 * (k0 + n1), valloc)
+                if q0 + n1 < q1:
+                    assert il + 1 < rb
+                    _prefetch(base + (il + 1) * ldxN * 4, 0, 4 * (q1 - q0 - n1), valloc)
+            for c in (0, 1, 127):                      # channel planes B N pairs apart (dzh_P)
+                _prefetch(0, (c * B * N + q0) * 4, (c * B * N + q1) * 4, hb)
+            g0, g1 = r0 * N + q0, r0 * N + q1
+            _prefetch(0, g0 * 256, g1 * 256, zb)
+            _prefetch(0, g0 * 8, g1 * 8, zst)
