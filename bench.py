@@ -643,16 +643,19 @@ def run_ours(args, w):
                 "kernels": {n: {"launches": v["launches"], "ms_per_node": v["ms"] / (k_a * len(nodes)),
                                 "share": v["ms"] / atot}
                             for n, v in at.items() if v["launches"]}}
-        # the attention kernel is bound by its exponentials: one ex2 per logit (N^3 H per node) on the
-        # special-function pipe, 16 per clock per SM, at the maximum SM clock
+        # the attention kernel's arithmetic bound: one ex2 per logit (N^3 H per node) on the special-function
+        # pipe, at the rate this device sustains (libtm's probe: independent ex2 chains on every SM); the
+        # nominal unit count (16 per clock per SM at the maximum clock) beside it
         ta = at["attn_attend"]
         if ta["ms"] > 0:
             logits = float(w.N) ** 3 * 4 * ta["launches"]
             ach = logits / (ta["ms"] / 1e3) / 1e12
-            pk = 16 * 148 * 2032e6 / 1e12
+            pk = tm.tm_probe_ex2_rate(amod.ctx) / 1e12
+            nominal = 16 * 148 * 2032e6 / 1e12
             attn["roofline"] = {"bound": "alu", "kernel": "k_ta_attend", "achieved": ach, "peak": pk,
                                 "unit": "Tera-ex2/s", "frac": ach / pk, "traffic": None,
-                                "peak_source": "16 ex2 per clock per SM x 148 SMs x 2032 MHz (nominal)"}
+                                "peak_source": "measured: ex2.approx.ftz.f32 on independent chains, every SM",
+                                "nominal_peak": nominal, "frac_of_nominal": ach / nominal}
         if rank == 0 and world == 1 and not args.no_cpu_baseline:
             attn["cpu_baseline"] = oracle_attention_sample(256)
         amod.close()

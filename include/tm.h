@@ -378,6 +378,15 @@ tm_status tm_ctx_info(const tm_ctx* ctx, int* c_z, int* c_hidden, int* layer);
  * every libtm kernel uses, without faulting or hanging the GPU. */
 tm_status tm_watchdog_selftest(tm_ctx* ctx, int timeout_ms, void* stream);
 
+/* Probe of the special-function pipe: the rate of ex2.approx.ftz.f32 (the
+ * exponential of the triangle attention's softmax) on this device, from a
+ * kernel of independent exponential chains on every SM (4 CTAs of 512 threads
+ * per SM, 8 x 20000 exponentials per thread), timed with CUDA events on
+ * `stream`. Blocks the calling thread until the probe has run. *per_second:
+ * exponentials per second over the whole device. For rooflines; launches no
+ * library work. Errors: TM_ERR_INVALID (NULL argument), TM_ERR_CUDA. */
+tm_status tm_probe_ex2_rate(tm_ctx* ctx, double* per_second, void* stream);
+
 /* Allocation-free forward (the pages have no counterpart; this is a service of
  * the library). Same contract and result as tm_forward for TM_BF16 and
  * 1 <= N <= 128, for callers that may not allocate device memory: code whose

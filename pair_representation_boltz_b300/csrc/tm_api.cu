@@ -1020,6 +1020,29 @@ tm_status tm_watchdog_selftest(tm_ctx* c, int timeout_ms, void* stream) {
   return e == cudaSuccess ? TM_OK : cuda_fail(c, e, "self-test launch");
 }
 
+tm_status tm_probe_ex2_rate(tm_ctx* c, double* per_second, void* stream) {
+  if (!c || !per_second) return TM_ERR_INVALID;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  constexpr int kIters = 20000;
+  const int blocks = 4 * c->num_sms;
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  cudaError_t e = cudaEventCreate(&e0);
+  if (e == cudaSuccess) e = cudaEventCreate(&e1);
+  if (e == cudaSuccess) e = launch_probe_ex2(blocks, 1000, s);   // warm-up
+  if (e == cudaSuccess) e = cudaEventRecord(e0, s);
+  if (e == cudaSuccess) e = launch_probe_ex2(blocks, kIters, s);
+  if (e == cudaSuccess) e = cudaEventRecord(e1, s);
+  if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+  float ms = 0.f;
+  if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, e0, e1);
+  if (e0) cudaEventDestroy(e0);
+  if (e1) cudaEventDestroy(e1);
+  if (e != cudaSuccess) return cuda_fail(c, e, "ex2 probe");
+  c->launches += 2;
+  *per_second = (double)blocks * 512.0 * 8.0 * kIters / (ms * 1e-3);
+  return TM_OK;
+}
+
 tm_status tm_set_timing(tm_ctx* c, int enable) {
   if (!c) return TM_ERR_INVALID;
   for (auto& t : c->timed) {

@@ -294,5 +294,7 @@ cudaError_t once_per_device(bool (&done)[kMaxDevices], F&& set) {
 // ----------------------------------------------------------------- diagnostics
 enum : int { KID_SELFTEST = 9 };
 cudaError_t launch_watchdog_selftest(const Watch& w, cudaStream_t s);
+// blocks CTAs of 512 threads, each thread 8 x iters ex2.approx.ftz.f32
+cudaError_t launch_probe_ex2(int blocks, int iters, cudaStream_t s);
 
 }  // namespace tmk

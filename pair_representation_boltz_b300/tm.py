@@ -9,7 +9,7 @@ GPU every call raises.
 The function names mirror the C ABI: tm_create, tm_forward, tm_forward_ex, tm_forward_host,
 tm_forward_noalloc, tm_pair_update, tm_backward, tm_attn_create, tm_attn_forward,
 tm_project, tm_project_ex, tm_x_exponent, tm_contract, tm_contract_ex, tm_finish, tm_finish_ex,
-tm_project_block, tm_contract_block, tm_sync_status, tm_watchdog_selftest, tm_set_timing,
+tm_project_block, tm_contract_block, tm_sync_status, tm_watchdog_selftest, tm_probe_ex2_rate, tm_set_timing,
 tm_get_timing, tm_launch_count, tm_workspace_bytes, tm_ctx_info, tm_status_string, tm_last_error,
 tm_destroy.
 
@@ -109,6 +109,7 @@ def load_library(path: str = LIB_PATH):
         "tm_attn_forward": (st, [vp, vp, vp, i, i, i, vp, vp, C.POINTER(TmOptions)]),
         "tm_sync_status": (st, [vp, vp]),
         "tm_watchdog_selftest": (st, [vp, i, vp]),
+        "tm_probe_ex2_rate": (st, [vp, C.POINTER(C.c_double), vp]),
         "tm_set_timing": (st, [vp, i]),
         "tm_get_timing": (st, [vp, C.POINTER(TmTiming)]),
         "tm_launch_count": (C.c_longlong, [vp]),
@@ -487,6 +488,13 @@ def tm_sync_status(ctx, stream=None) -> int:
 
 def tm_watchdog_selftest(ctx, timeout_ms: int, stream=None) -> None:
     _check(ctx, load_library().tm_watchdog_selftest(ctx, timeout_ms, _stream(stream)))
+
+
+def tm_probe_ex2_rate(ctx, stream=None) -> float:
+    """Exponentials (ex2.approx.ftz.f32) per second this device sustains (a roofline peak)."""
+    r = C.c_double()
+    _check(ctx, load_library().tm_probe_ex2_rate(ctx, C.byref(r), _stream(stream)))
+    return r.value
 
 
 def tm_set_timing(ctx, enable: bool) -> None:

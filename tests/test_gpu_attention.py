@@ -136,3 +136,18 @@ def test_attention_scales_v_and_the_weight_images(env, gain):
         gate(got, TA.full(wl.as_f64(z_np), np.ones(N), scaled, "starting"))
     finally:
         att.close()
+
+
+def test_ex2_probe_rate_is_plausible(env):
+    """The special-function pipe probe (the attention roofline's peak) returns a rate between a quarter of
+    the nominal unit count (16 per clock per SM at the maximum clock) and two and a half times it."""
+    _, tm, _, _ = env
+    mod = tm.TriMul(128, 128, wl.make_weights(128, 128, 1))
+    try:
+        launches = tm.tm_launch_count(mod.ctx)
+        rate = tm.tm_probe_ex2_rate(mod.ctx)
+        assert tm.tm_launch_count(mod.ctx) == launches + 2
+        nominal = 16 * 148 * 2032e6
+        assert 0.25 * nominal < rate < 2.5 * nominal, rate
+    finally:
+        mod.close()
