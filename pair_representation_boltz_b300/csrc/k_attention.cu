@@ -27,7 +27,7 @@
 //   k_ta_attend: per (row i, two tiles of 128 queries j), heads one after another, keys in blocks of
 //     128, warp-specialised: a TMA warp, an MMA warp and one softmax thread per query row. S = Q K^T
 //     (tcgen05, TMEM; q stored times log2(e)/sqrt(c), the bias times log2(e), so the softmax runs in
-//     base 2); the softmax thread reads its S row in 32-key chunks, adds the bias row (-inf at masked
+//     base 2); the softmax thread reads its S row in 64-key halves, adds the bias row (-inf at masked
 //     keys), and forms P = 2^(x - reference) as fp16 back into TMEM against a lazy running reference,
 //     checking the block maximum on the way (a second pass only when it moved by more than 8); O += P v
 //     (A = P from TMEM, v with a row of ones appended so that the product also gives the row sum of P,
@@ -409,51 +409,54 @@ __global__ void __launch_bounds__(kAttThreads, 1) k_ta_attend(const __grid_const
 #pragma unroll
       for (int u = 0; u < 4; ++u) d4[u] = pack8h(o + 8 * u);
     };
-    // One pass over the block's S row in TMEM, 32 keys at a time (the next chunk's load in flight while
-    // one is computed): logits x = S + bias (base 2), their maximum, and P = 2^(x - ref) into TMEM as
-    // fp16 against the reference ref. pmax: the maximum of the logits.
+    // One pass over the block's S row in TMEM, in two halves of 64 keys, each read by two TMEM loads under
+    // one wait: logits x = S + bias (base 2), their maximum, and P = 2^(x - ref) into TMEM as fp16 against
+    // the reference ref. pmax: the maximum of the logits.
     auto pass = [&](int st, int nvalid, bool write_p, float ref, float& pmax) {
       const float2 nref = make_float2(-ref, -ref);
       float mx = -INFINITY;
-      uint32_t r[2][32];
-      tmem_ld32(trow + kTmS, r[0]);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int hp = 0; hp < 2; ++hp) {
+        uint32_t r[2][32];
+        tmem_ld32(trow + kTmS + 64 * hp, r[0]);
+        tmem_ld32(trow + kTmS + 64 * hp + 32, r[1]);
         tmem_ld_wait();
-        if (c < 3) tmem_ld32(trow + kTmS + 32 * (c + 1), r[(c + 1) & 1]);
-        const uint8_t* brow = sm.b[st][g][c >> 1];
-        float x[32];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          float bv[8];
-          f16x8_to_float(*reinterpret_cast<const uint4*>(brow + sw128_offset((uint32_t)row, (uint32_t)(4 * (c & 1) + u))),
-                         bv);
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * hp + cc;
+          const uint8_t* brow = sm.b[st][g][hp];
 #pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            const float2 v = __fadd2_rn(make_float2(__uint_as_float(r[c & 1][8 * u + e]), __uint_as_float(r[c & 1][8 * u + e + 1])),
-                                        make_float2(bv[e], bv[e + 1]));
-            x[8 * u + e] = v.x;
-            x[8 * u + e + 1] = v.y;
+          for (int u = 0; u < 4; ++u) {
+            float bv[8];
+            f16x8_to_float(*reinterpret_cast<const uint4*>(brow + sw128_offset((uint32_t)row, (uint32_t)(4 * cc + u))), bv);
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+              const float2 v = __fadd2_rn(make_float2(__uint_as_float(r[cc][8 * u + e]), __uint_as_float(r[cc][8 * u + e + 1])),
+                                          make_float2(bv[e], bv[e + 1]));
+              r[cc][8 * u + e] = __float_as_uint(v.x);
+              r[cc][8 * u + e + 1] = __float_as_uint(v.y);
+            }
           }
-        }
-        if (nvalid < BT) {
+          if (nvalid < BT) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (32 * c + e >= nvalid) x[e] = -INFINITY;
-        }
-        float m3[11];
-#pragma unroll
-        for (int e = 0; e < 10; ++e) m3[e] = max3f(x[3 * e], x[3 * e + 1], x[3 * e + 2]);
-        m3[10] = max3f(x[30], x[31], mx);
-        mx = max3f(max3f(m3[0], m3[1], m3[2]), max3f(m3[3], m3[4], m3[5]), max3f(max3f(m3[6], m3[7], m3[8]), m3[9], m3[10]));
-        if (write_p) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float2 d = __fadd2_rn(make_float2(x[2 * e], x[2 * e + 1]), nref);
-            pk[e] = pack_f16x2(ex2_approx(d.x), ex2_approx(d.y));
+            for (int e = 0; e < 32; ++e)
+              if (32 * c + e >= nvalid) r[cc][e] = __float_as_uint(-INFINITY);
           }
-          tmem_st16(trow + kTmP + 16 * c, pk);
+          float m3[11];
+#pragma unroll
+          for (int e = 0; e < 10; ++e)
+            m3[e] = max3f(__uint_as_float(r[cc][3 * e]), __uint_as_float(r[cc][3 * e + 1]), __uint_as_float(r[cc][3 * e + 2]));
+          m3[10] = max3f(__uint_as_float(r[cc][30]), __uint_as_float(r[cc][31]), mx);
+          mx = max3f(max3f(m3[0], m3[1], m3[2]), max3f(m3[3], m3[4], m3[5]), max3f(max3f(m3[6], m3[7], m3[8]), m3[9], m3[10]));
+          if (write_p) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float2 d = __fadd2_rn(make_float2(__uint_as_float(r[cc][2 * e]), __uint_as_float(r[cc][2 * e + 1])), nref);
+              pk[e] = pack_f16x2(ex2_approx(d.x), ex2_approx(d.y));
+            }
+            tmem_st16(trow + kTmP + 16 * c, pk);
+          }
         }
       }
       pmax = mx;
