@@ -41,10 +41,10 @@
 //               staging box (128-byte swizzle) that its lane 0 writes out with
 //               one TMA store per tile, so channel rows leave as 128-byte lines
 //               and no warp waits for another; the store drains while the next
-//               tile's MMA runs. The TMEM loads of each 16-pair chunk are issued
-//               while the chunk before it is computed, and the wait for the last
-//               store to have read the staging box comes after the first chunk's
-//               arithmetic. (Stores straight from the threads, one channel
+//               tile's MMA runs. Each 32-pair half of the warp's accumulator
+//               columns is read by two TMEM loads under one wait (a wait costs a
+//               load's whole latency), and the wait for the last store to have
+//               read the staging box comes after the first chunk's arithmetic. (Stores straight from the threads, one channel
 //               row per lane, scatter each warp instruction over 32 DRAM pages
 //               and ran 6x slower.)
 #include "tm_kernels.h"
@@ -310,21 +310,19 @@ __global__ void __launch_bounds__(THREADS, 1)
           const float2 r2 = __bfloat1622float2(__floats2bfloat162_rn(x, y));
           return pack_f16x2(r2.x * osc, r2.y * osc);
         };
-        // four 16-pair TMEM chunks; the loads of chunk hh + 1 are in flight while chunk hh is computed
-        uint32_t pr[2][16], gt[2][16];
-        tmem_ld16(ta, pr[0]);
-        tmem_ld16(ta + BM, gt[0]);
+        // two 32-pair halves, each read by two TMEM loads under one wait, then computed 16 pairs at a time
+        uint32_t pr[32], gt[32];
 #pragma unroll
         for (int hh = 0; hh < 4; ++hh) {
-          tmem_ld_wait();
-          if (hh < 3) {
-            tmem_ld16(ta + (uint32_t)((hh + 1) * 16), pr[(hh + 1) & 1]);
-            tmem_ld16(ta + BM + (uint32_t)((hh + 1) * 16), gt[(hh + 1) & 1]);
+          if ((hh & 1) == 0) {
+            tmem_ld32(ta + (uint32_t)(hh * 16), pr);
+            tmem_ld32(ta + BM + (uint32_t)(hh * 16), gt);
+            tmem_ld_wait();
           }
           const int p0 = pbase + hh * 16;
           const uint32_t mword = mw[p0 >> 5] >> (p0 & 31);
-          const uint32_t* prc = pr[hh & 1];
-          const uint32_t* gtc = gt[hh & 1];
+          const uint32_t* prc = pr + 16 * (hh & 1);
+          const uint32_t* gtc = gt + 16 * (hh & 1);
           uint32_t packed[8];
           if ((mword & 0xFFFFu) == 0xFFFFu) {
             // all 16 pairs unmasked and inside the grid (warp-uniform): no per-element mask
