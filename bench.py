@@ -184,9 +184,15 @@ PROJECT_BYTES_PER_PAIR = 256 + 512
 FINISH_BYTES_PER_PAIR = 128 * 2 + 256 + 256
 
 
+# Tensor work the projection executes per pair: two 128 x 128 products (projection and gate) for each of
+# a and b, each with bf16 hi and lo weight terms, 2 FLOP per multiply-add.
+PROJECT_TENSOR_FLOP_PER_PAIR = 2 * 2 * 2 * 128 * 128 * 2
+
+
 def add_kernel_bandwidth(kernels, ktime, peaks):
     """GB/s of the projection and finish kernels over their algorithmic bytes, and its fraction of the
-    measured copy bandwidth."""
+    measured copy bandwidth; for the projection also its executed tensor rate against the bf16 peaks (the
+    hi + lo weights make its tensor work, not its bytes, the larger bound)."""
     for name, per_pair in (("project", PROJECT_BYTES_PER_PAIR), ("finish", FINISH_BYTES_PER_PAIR)):
         v = ktime[name]
         if v["ms"] > 0 and name in kernels:
@@ -194,6 +200,12 @@ def add_kernel_bandwidth(kernels, ktime, peaks):
             kernels[name]["gbs"] = gbs
             kernels[name]["frac_of_hbm"] = gbs / peaks["hbm_gbs"]
             kernels[name]["bytes_per_pair"] = per_pair
+            if name == "project":
+                tf = v["units"] * PROJECT_TENSOR_FLOP_PER_PAIR / (v["ms"] / 1e3) / 1e12
+                kernels[name]["tensor_tflops"] = tf
+                kernels[name]["frac_of_bf16_peak"] = tf / peaks["bf16_tflops"]
+                kernels[name]["frac_of_bf16_sustained"] = tf / peaks["bf16_tflops_sustained"]
+                kernels[name]["tensor_flop_per_pair"] = PROJECT_TENSOR_FLOP_PER_PAIR
 
 
 def host_cores():
