@@ -25,14 +25,15 @@
 //     key index innermost, so that it is the K-major operand of the P V product; b per (head, j) with
 //     k innermost.
 //   k_ta_attend: per (row i, two tiles of 128 queries j), heads one after another, keys in blocks of
-//     128, warp-specialised: a TMA warp, an MMA warp and one softmax thread per query row. S = Q K^T
-//     (tcgen05, TMEM; q stored times log2(e)/sqrt(c), the bias times log2(e), so the softmax runs in
-//     base 2); the softmax thread reads its S row in 64-key halves, adds the bias row (-inf at masked
-//     keys), and forms P = 2^(x - reference) as fp16 back into TMEM against a lazy running reference,
-//     checking the block maximum on the way (a second pass only when it moved by more than 8); O += P v
-//     (A = P from TMEM, v with a row of ones appended so that the product also gives the row sum of P,
-//     the softmax denominator) accumulates across a head's blocks in TMEM, and the gate is applied at
-//     the end of each head.
+//     64, warp-specialised: a TMA warp, one MMA warp per query tile and one softmax thread per query
+//     row. S = Q K^T (tcgen05, TMEM, three buffers per tile so that S runs up to three blocks ahead; q
+//     stored times log2(e)/sqrt(c), the bias times log2(e), so the softmax runs in base 2); the softmax
+//     thread reads its S row of the block with two TMEM loads under one wait, adds the bias row (-inf
+//     at masked keys) and forms P = 2^(x - reference) against a lazy running reference while it takes
+//     the block maximum (P again, from the logits in registers, only when the maximum moved by more
+//     than 8), and stores P as fp16 over the S it has read; O += P v (A = P from TMEM, v with a row of
+//     ones appended so that the product also gives the row sum of P, the softmax denominator)
+//     accumulates across a head's blocks in TMEM, and the gate is applied at the end of each head.
 //   k_ta_out: out = W_o o per pair (the ending node writes the transposed pair).
 #include "pair_tile.cuh"
 
@@ -187,37 +188,42 @@ __global__ void __launch_bounds__(NT, 1) k_ta_project(const TaProjectParams p) {
 
 namespace {
 
+constexpr int kKB = 64;                         // keys per block
 constexpr uint32_t kQBytes = 64 * 128 * 2;      // Q box: 64 channels (a head pair) x 128 queries
-constexpr uint32_t kKBytes = 64 * 128 * 2;      // K box: 64 channels x 128 keys
-constexpr uint32_t kVBytes = 64 * 32 * 2;       // one v box: 64 keys x 32 channels of one head
-constexpr uint32_t kVSlot = 64 * 48 * 2;        // its slot: 32 rows of v, a row of ones, 15 rows of zeros
+constexpr uint32_t kKBytes = 64 * kKB * 2;      // K box: 64 channels x 64 keys
+constexpr uint32_t kVBytes = kKB * 32 * 2;      // v box: 64 keys x 32 channels of one head
+constexpr uint32_t kVSlot = kKB * 48 * 2;       // its slot: 32 rows of v, a row of ones, 15 rows of zeros
 constexpr int kPvN = 48;                        // N of the P V product: 32 channels, the row sum, padding
-constexpr uint32_t kBBytes = 64 * 128 * 2;      // one bias box: 64 keys x 128 queries
+constexpr uint32_t kBBytes = kKB * 128 * 2;     // one bias box: 64 keys x 128 queries
 
-static_assert(kBoxTaQK.bytes() == kQBytes && kBoxTaQK.bytes() == kKBytes, "Q/K box fills its slot");
+static_assert(kBoxTaQK.bytes() == kQBytes, "Q box fills its slot");
+static_assert(kBoxTaK.bytes() == kKBytes, "K box fills its slot");
 static_assert(kBoxTaV.bytes() == kVBytes, "v box fills its slot");
 static_assert(kBoxTaBias.bytes() == kBBytes, "bias box fills its slot");
 
 constexpr int kGroups = 2;            // query tiles per CTA, one softmax group each
-constexpr int kStages = 2;            // K, v and bias stages in flight
-constexpr int kAttThreads = 64 + 32 * 4 * kGroups;   // TMA warp, MMA warp, four softmax warps per group
-constexpr uint32_t kStageBytes = kKBytes + kGroups * 2 * kBBytes + 2 * kVBytes;   // what one stage receives
+constexpr int kStages = 4;            // K, v and bias stages in flight
+constexpr int kSBuf = 3;              // S (and P) buffers per group in TMEM
+constexpr int kAttThreads = 32 + 32 * kGroups + 32 * 4 * kGroups;   // TMA warp, an MMA warp and four softmax warps per group
+constexpr uint32_t kStageBytes = kKBytes + kGroups * kBBytes + kVBytes;   // what one stage receives
 
 struct alignas(1024) TaAttSmem {
   uint8_t q[kGroups][kQBytes];                  // per group: 64 channels (a head pair) x 128 queries
-  uint8_t k[kStages][kKBytes];                  // 64 channels x 128 keys
-  uint8_t b[kStages][kGroups][2][kBBytes];      // bias: per group, keys 0..63 and 64..127 of the block
-  uint8_t v[kStages][2][kVSlot];                // keys 0..63 and 64..127, rows = channels (+ ones row)
-  uint64_t q_full, q_free, fin;
+  uint8_t k[kStages][kKBytes];                  // 64 channels x 64 keys
+  uint8_t b[kStages][kGroups][kBBytes];         // bias: per group, the block's 64 keys x 128 queries
+  uint8_t v[kStages][kVSlot];                   // the block's 64 keys, rows = channels (+ ones row)
+  uint64_t q_full, q_free, go1;
   uint64_t kv_full[kStages], kv_empty[kStages];
-  uint64_t s_full[kGroups], s_free[kGroups], p_full[kGroups], pv_done[kGroups];
+  uint64_t s_full[kGroups][kSBuf], p_full[kGroups][kSBuf], pv_done[kGroups][2], pv_last[kGroups], fin[kGroups];
   uint32_t tmem_slot;
   int abort_flag;
 };
 
-// TMEM columns of group g: S (128 keys, float32) at 256 g, P (128 keys as packed fp16 pairs) at
-// 256 g + 128, the P V product (32 channels, the row sum, padding) at 256 g + 192.
-constexpr uint32_t kTmS = 0, kTmP = 128, kTmPV = 192, kTmGroup = 256;
+// TMEM columns of group g (base 256 g): the three block buffers at 0, 64 and 128, each S (64 keys,
+// float32) and then, over its first 32 columns, P (64 keys as packed fp16 pairs) once S has been read;
+// the running output P V (32 channels, the row sum, padding) at 192.
+constexpr uint32_t kTmS = 0, kTmPV = 192, kTmGroup = 256;
+static_assert(kSBuf * kKB <= (int)kTmPV, "S buffers below the running output");
 
 __device__ __forceinline__ float ex2_approx(float v) {
   float r;
@@ -233,22 +239,27 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
 }
 
 // Triangle attention of one CTA: row i of the grid, query tiles 2 jp and 2 jp + 1 (one per softmax
-// group), heads in turn, keys in blocks of 128. Roles:
+// group), heads in turn, keys in blocks of 64. Roles:
 //   warp 0        TMA: per block, K (the head pair's 64 channels), the bias tiles of both groups and
-//                 v (with a row of ones beside it) into one of two stages; Q of both groups per head pair.
-//   warp 1        tcgen05.mma: S_g = Q_g K^T into TMEM (M = 128 queries, N = 128 keys, K = 32), then,
-//                 once group g has stored its P into TMEM, O_g = P_g v (A = P from TMEM, B = v from
-//                 shared memory, N = 48: 32 channels, the row sum from the ones row, padding).
-//   warps 2..9    softmax, thread = query row, group g = the four warps of one query tile: S row +
-//                 bias row -> logits (base 2), and P = 2^(x - m) into TMEM as fp16 against the row's
-//                 running reference m, in one pass that also takes the block maximum. The reference
-//                 is lazy: it moves only when the maximum exceeds it by more than 8 (then P is formed
-//                 again, against the new maximum; always at a head's first block), so P <= 2^8 stays
-//                 inside fp16 and most blocks need one pass and no rescale of the running output. The
-//                 running output O (and its row sum) accumulates in TMEM across a head's blocks; when
-//                 the reference moves, the thread rescales its row of O once the block before has been
-//                 added, before this block's P is released. Each group's work overlaps the other
-//                 group's and the tensor core's.
+//                 v (with a row of ones beside it) into one of four stages; Q of both groups per head pair.
+//   warps 1, 2    tcgen05.mma for group g = warp - 1: S_g = Q_g K^T into one of three TMEM buffers
+//                 (M = 128 queries, N = 64 keys, K = 32), up to three blocks ahead of the softmax, and,
+//                 once the group has stored P of a block over its S, O_g += P_g v (A = P from TMEM, B = v
+//                 from shared memory, N = 48: 32 channels, the row sum from the ones row, padding). The
+//                 product of block t is issued before S of block t + 3 into the same buffer: the tensor
+//                 core runs one thread's MMAs in order, so S of a block complete means every product up
+//                 to three blocks back is complete. Operand descriptors are the tile's plus an offset, and
+//                 the block, stage and buffer indices advance as counters (no division per block).
+//   warps 3..10   softmax, thread = query row, group g = the four warps of one query tile: S row +
+//                 bias row -> logits (base 2), and P = 2^(x - m) against the row's running reference
+//                 m, formed while the block maximum is taken. The reference is lazy: it moves only when
+//                 the maximum exceeds it by more than 8 (always at a head's first block; P is then formed
+//                 again from the logits still in registers), so P <= 2^8 stays inside fp16 and most
+//                 blocks leave the running output as it is. P goes into TMEM as fp16 over the first half
+//                 of the block's S columns. The running output O (and its row sum) accumulates in TMEM
+//                 across a head's blocks; when the reference moves, the thread rescales its row of O once
+//                 the block before has been added, before this block's P is released. The second group
+//                 starts one block behind the first.
 __global__ void __launch_bounds__(kAttThreads, 1) k_ta_attend(const __grid_constant__ CUtensorMap qmap,
                                                               const __grid_constant__ CUtensorMap kmap,
                                                               const __grid_constant__ CUtensorMap vmap,
@@ -267,22 +278,26 @@ __global__ void __launch_bounds__(kAttThreads, 1) k_ta_attend(const __grid_const
     }
     return;
   }
-  const int KB = (p.N + BT - 1) / BT;
+  const int KB = (p.N + kKB - 1) / kKB;
   const int T = 4 * KB;                          // iterations: heads in order, key blocks within a head
 
   if (tid == 0) {
     mbar_init(&sm.q_full, 1);
-    mbar_init(&sm.q_free, 1);
-    mbar_init(&sm.fin, 1);
+    mbar_init(&sm.q_free, kGroups);              // each group's MMA warp
+    mbar_init(&sm.go1, 4);                       // group 0 has finished its first block
     for (int st = 0; st < kStages; ++st) {
       mbar_init(&sm.kv_full[st], 1);
-      mbar_init(&sm.kv_empty[st], 1 + 4 * kGroups);   // the MMA's commit + every softmax warp (bias read)
+      mbar_init(&sm.kv_empty[st], kGroups + 4 * kGroups);   // each MMA warp's commit + every softmax warp (bias read)
     }
     for (int g = 0; g < kGroups; ++g) {
-      mbar_init(&sm.s_full[g], 1);
-      mbar_init(&sm.s_free[g], 4);
-      mbar_init(&sm.p_full[g], 4);
-      mbar_init(&sm.pv_done[g], 1);
+      for (int b = 0; b < kSBuf; ++b) {
+        mbar_init(&sm.s_full[g][b], 1);
+        mbar_init(&sm.p_full[g][b], 4);
+      }
+      mbar_init(&sm.pv_done[g][0], 1);
+      mbar_init(&sm.pv_done[g][1], 1);
+      mbar_init(&sm.pv_last[g], 1);
+      mbar_init(&sm.fin[g], 1);
     }
     sm.abort_flag = 0;
     fence_mbar_init();
@@ -293,9 +308,9 @@ __global__ void __launch_bounds__(kAttThreads, 1) k_ta_attend(const __grid_const
   }
   // rows 32..47 of every v slot, which no copy overwrites: a row of ones (the P V product's column 32
   // is then the row sum of the fp16 P, the softmax denominator) and zeros
-  for (int x = tid; x < kStages * 2 * (int)((kVSlot - kVBytes) / 4); x += kAttThreads) {
+  for (int x = tid; x < kStages * (int)((kVSlot - kVBytes) / 4); x += kAttThreads) {
     const int slot = x / (int)((kVSlot - kVBytes) / 4), w4 = x % (int)((kVSlot - kVBytes) / 4);
-    reinterpret_cast<uint32_t*>(sm.v[slot >> 1][slot & 1] + kVBytes)[w4] = w4 < 32 ? 0x3C003C00u : 0u;
+    reinterpret_cast<uint32_t*>(sm.v[slot] + kVBytes)[w4] = w4 < 32 ? 0x3C003C00u : 0u;
   }
   fence_proxy_async_smem();
   tc_fence_before();
@@ -312,7 +327,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) k_ta_attend(const __grid_const
       tma_prefetch_desc(&vmap);
       tma_prefetch_desc(&bmap);
       for (int t = 0; t < T; ++t) {
-        const int h = t / KB, kb = t - h * KB, st = t & 1;
+        const int h = t / KB, kb = t - h * KB, st = t % kStages, use = t / kStages;
         if (kb == 0 && (h & 1) == 0) {
           // Q of the head pair; the second pair's replaces the first once every S of heads 0, 1 is done
           if (h == 2 && !wait_bounded(&sm.q_free, 0, p.w, abort_flag, 11)) break;
@@ -320,69 +335,88 @@ __global__ void __launch_bounds__(kAttThreads, 1) k_ta_attend(const __grid_const
           for (int g = 0; g < kGroups; ++g)
             tma_load_3d(sm.q[g], &qmap, &sm.q_full, 64 * (h >> 1), (jp * kGroups + g) * BT, i);
         }
-        if (t >= kStages && !wait_bounded(&sm.kv_empty[st], (uint32_t)((t >> 1) - 1) & 1u, p.w, abort_flag, 12)) break;
+        if (use >= 1 && !wait_bounded(&sm.kv_empty[st], (uint32_t)(use - 1) & 1u, p.w, abort_flag, 12)) break;
         mbar_expect_tx(&sm.kv_full[st], kStageBytes);
-        tma_load_3d(sm.k[st], &kmap, &sm.kv_full[st], 64 * (h >> 1), kb * BT, i);
+        tma_load_3d(sm.k[st], &kmap, &sm.kv_full[st], 64 * (h >> 1), kb * kKB, i);
         for (int g = 0; g < kGroups; ++g)
-          for (int hf = 0; hf < 2; ++hf)
-            tma_load_3d(sm.b[st][g][hf], &bmap, &sm.kv_full[st], kb * BT + 64 * hf, (jp * kGroups + g) * BT, h);
-        for (int hf = 0; hf < 2; ++hf)
-          tma_load_3d(sm.v[st][hf], &vmap, &sm.kv_full[st], kb * BT + 64 * hf, kHd * h, i);
+          tma_load_3d(sm.b[st][g], &bmap, &sm.kv_full[st], kb * kKB, (jp * kGroups + g) * BT, h);
+        tma_load_3d(sm.v[st], &vmap, &sm.kv_full[st], kb * kKB, kHd * h, i);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp <= kGroups) {
+    // ------------------------------------------------------------ MMA issuer of group g = warp - 1
     if (lane == 0) {
-      constexpr uint32_t ID_S = make_idesc(128, 128, FMT_F16, false, false);
+      const int g = warp - 1;
+      constexpr uint32_t ID_S = make_idesc(128, kKB, FMT_F16, false, false);
       constexpr uint32_t ID_O = make_idesc(128, kPvN, FMT_F16, false, false);
-      bool ok = true;
-      auto issue_pv = [&](int t) -> bool {   // O_g (+)= P_g v for block t, both groups
-        const int st = t & 1;
-        const bool first = (t % KB) == 0;    // a head's first block starts its running output
-        const uint32_t v0 = smem_u32(sm.v[st][0]);
-        for (int g = 0; g < kGroups; ++g) {
-          if (!wait_bounded(&sm.p_full[g], (uint32_t)t & 1u, p.w, abort_flag, 23)) return false;
-          tc_fence_after();
-          const uint32_t tg = tmem + (uint32_t)g * kTmGroup;
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            mma_f16_ts(tg + kTmPV, tg + kTmP + (uint32_t)ks * 8u,
-                       make_sdesc_sw128(v0 + (ks >> 2) * kVSlot + (ks & 3) * 32, 16, 1024), ID_O,
-                       (ks || !first) ? 1u : 0u);
-          mma_commit(&sm.pv_done[g]);
-        }
-        mma_commit(&sm.kv_empty[st]);      // K and v of this stage have been read
+      const uint32_t tg = tmem + (uint32_t)g * kTmGroup;
+      // descriptors of the operand tiles at offset 0; an operand's descriptor is its tile's plus the
+      // byte offset / 16 (the start-address field, shared memory below 256 KB)
+      const uint64_t dq = make_sdesc_sw128(smem_u32(sm.q[g]), 16, 1024);
+      const uint64_t dk = make_sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
+      const uint64_t dv = make_sdesc_sw128(smem_u32(sm.v[0]), 16, 1024);
+      // block cursors: block t, its head h, key block kb, stage st with its use parity, S buffer b with its
+      // use parity
+      struct Cur {
+        int t, h, kb, st, b;
+        uint32_t sph, bph;
+      };
+      auto next = [&](Cur& c) {
+        ++c.t;
+        if (++c.kb == KB) { c.kb = 0; ++c.h; }
+        if (++c.st == kStages) { c.st = 0; c.sph ^= 1u; }
+        if (++c.b == kSBuf) { c.b = 0; c.bph ^= 1u; }
+      };
+      // S_g of the cursor's block into its buffer (q is stored pre-scaled by log2(e)/sqrt(c))
+      auto issue_s = [&](const Cur& c) -> bool {
+        if (c.kb == 0 && (c.h & 1) == 0 && !wait_bounded(&sm.q_full, (uint32_t)(c.h >> 1) & 1u, p.w, abort_flag, 20)) return false;
+        if (!wait_bounded(&sm.kv_full[c.st], c.sph, p.w, abort_flag, 21)) return false;
+        // the second group starts one block behind the first, so that each group's softmax overlaps
+        // the other's wait for its products
+        if (g == 1 && c.t == 0 && !wait_bounded(&sm.go1, 0u, p.w, abort_flag, 25)) return false;
+        tc_fence_after();
+        const uint32_t hoff = (uint32_t)(64 * (c.h & 1)) >> 4;
+        const uint64_t aq = dq + hoff, bk = dk + ((uint32_t)c.st * (kKBytes >> 4) + hoff);
+        const uint32_t dst = tg + kTmS + (uint32_t)(kKB * c.b);
+        mma_f16(dst, aq, bk, ID_S, 0u);
+        mma_f16(dst, aq + 2, bk + 2, ID_S, 1u);
+        mma_commit(&sm.s_full[g][c.b]);
+        if (c.t == 2 * KB - 1) mma_commit(&sm.q_free);   // every S of heads 0, 1 of this group issued
         return true;
       };
-      for (int t = 0; t < T && ok; ++t) {
-        const int h = t / KB, kb = t - h * KB, st = t & 1;
-        if (kb == 0 && (h & 1) == 0 && !wait_bounded(&sm.q_full, (uint32_t)(h >> 1) & 1u, p.w, abort_flag, 20)) break;
-        if (!wait_bounded(&sm.kv_full[st], (uint32_t)(t >> 1) & 1u, p.w, abort_flag, 21)) break;
-        for (int g = 0; g < kGroups; ++g) {
-          // S_g = Q_g K^T of head h (q is stored pre-scaled by log2(e)/sqrt(c)), once group g has read S_g
-          if (t >= 1 && !wait_bounded(&sm.s_free[g], (uint32_t)(t - 1) & 1u, p.w, abort_flag, 22)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t q0 = smem_u32(sm.q[g]) + 64 * (h & 1), k0 = smem_u32(sm.k[st]) + 64 * (h & 1);
+      // O_g (+)= P_g v of the cursor's block, once the group has stored P (and so has read S) of that
+      // block. The tensor core runs a thread's MMAs in issue order, so S of the block three later, issued
+      // next into the same buffer, overwrites P only after this product has read it.
+      auto issue_pv = [&](const Cur& c) -> bool {
+        if (!wait_bounded(&sm.p_full[g][c.b], c.bph, p.w, abort_flag, 23)) return false;
+        tc_fence_after();
+        const uint64_t bv = dv + (uint32_t)c.st * (kVSlot >> 4);
+        const uint32_t pa = tg + kTmS + (uint32_t)(kKB * c.b);
+        const uint32_t acc0 = c.kb != 0 ? 1u : 0u;    // a head's first block starts its running output
 #pragma unroll
-          for (int ks = 0; ks < 2; ++ks)
-            mma_f16(tmem + (uint32_t)g * kTmGroup + kTmS, make_sdesc_sw128(q0 + 32 * ks, 16, 1024),
-                    make_sdesc_sw128(k0 + 32 * ks, 16, 1024), ID_S, ks ? 1u : 0u);
-          mma_commit(&sm.s_full[g]);
+        for (int ks = 0; ks < kKB / 16; ++ks)
+          mma_f16_ts(tg + kTmPV, pa + (uint32_t)(8 * ks), bv + (uint32_t)(2 * ks), ID_O, ks ? 1u : acc0);
+        mma_commit(&sm.kv_empty[c.st]);    // this group's reads of K and v of the stage are done
+        mma_commit(&sm.pv_done[g][c.t & 1]);
+        return true;
+      };
+      Cur cs{0, 0, 0, 0, 0, 0u, 0u}, cp = cs;
+      bool ok = true;
+      for (int u = 0; u < kSBuf && ok; ++u, next(cs)) ok = issue_s(cs);
+      for (; cp.t < T && ok; next(cp)) {
+        ok = issue_pv(cp);
+        if (ok && cs.t < T) {
+          ok = issue_s(cs);
+          next(cs);
         }
-        if (!ok) break;
-        if (t == 2 * KB - 1) mma_commit(&sm.q_free);   // every S of heads 0, 1 issued: Q may be replaced
-        if (t >= 1 && !issue_pv(t - 1)) ok = false;
       }
-      if (ok) issue_pv(T - 1);
-      mma_commit(&sm.fin);
-      wait_bounded(&sm.fin, 0, p.w, abort_flag, 24);
+      if (ok) mma_commit(&sm.pv_last[g]);   // every product of the group issued
+      mma_commit(&sm.fin[g]);
+      wait_bounded(&sm.fin[g], 0, p.w, abort_flag, 24);
     }
   } else {
     // ------------------------------------------------------------ softmax, thread = query row
-    const int g = (warp - 2) >> 2;             // the group's query tile: 2 jp + g
+    const int g = (warp - 1 - kGroups) >> 2;   // the group's query tile: 2 jp + g
     const int lq = warp & 3;                   // TMEM lane quarter
     const int row = 32 * lq + lane;
     const int j = (jp * kGroups + g) * BT + row;
@@ -409,98 +443,102 @@ __global__ void __launch_bounds__(kAttThreads, 1) k_ta_attend(const __grid_const
 #pragma unroll
       for (int u = 0; u < 4; ++u) d4[u] = pack8h(o + 8 * u);
     };
-    // One pass over the block's S row in TMEM, in two halves of 64 keys, each read by two TMEM loads under
-    // one wait: logits x = S + bias (base 2), their maximum, and P = 2^(x - ref) into TMEM as fp16 against
-    // the reference ref. pmax: the maximum of the logits.
-    auto pass = [&](int st, int nvalid, bool write_p, float ref, float& pmax) {
+    // The block's S row (64 keys, two TMEM loads under one wait) into registers, as logits x = S + bias
+    // (base 2; -inf past the grid's last key), and P = 2^(x - ref) packed as fp16 pairs into pk; returns
+    // the logits' maximum.
+    // byte offsets of the 16-byte units of this thread's bias row (128-byte swizzle)
+    uint32_t boff[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) boff[u] = sw128_offset((uint32_t)row, (uint32_t)u);
+    auto logits = [&](int st, int b, int nvalid, float ref, uint32_t (&r)[2][32], uint32_t (&pk)[2][16]) -> float {
       const float2 nref = make_float2(-ref, -ref);
       float mx = -INFINITY;
+      tmem_ld32(trow + kTmS + kKB * b, r[0]);
+      tmem_ld32(trow + kTmS + kKB * b + 32, r[1]);
+      tmem_ld_wait();
+      const uint8_t* brow = sm.b[st][g];
 #pragma unroll
-      for (int hp = 0; hp < 2; ++hp) {
-        uint32_t r[2][32];
-        tmem_ld32(trow + kTmS + 64 * hp, r[0]);
-        tmem_ld32(trow + kTmS + 64 * hp + 32, r[1]);
-        tmem_ld_wait();
+      for (int cc = 0; cc < 2; ++cc) {
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c = 2 * hp + cc;
-          const uint8_t* brow = sm.b[st][g][hp];
+        for (int u = 0; u < 4; ++u) {
+          float bv[8];
+          f16x8_to_float(*reinterpret_cast<const uint4*>(brow + boff[4 * cc + u]), bv);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            float bv[8];
-            f16x8_to_float(*reinterpret_cast<const uint4*>(brow + sw128_offset((uint32_t)row, (uint32_t)(4 * cc + u))), bv);
-#pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-              const float2 v = __fadd2_rn(make_float2(__uint_as_float(r[cc][8 * u + e]), __uint_as_float(r[cc][8 * u + e + 1])),
-                                          make_float2(bv[e], bv[e + 1]));
-              r[cc][8 * u + e] = __float_as_uint(v.x);
-              r[cc][8 * u + e + 1] = __float_as_uint(v.y);
-            }
-          }
-          if (nvalid < BT) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (32 * c + e >= nvalid) r[cc][e] = __float_as_uint(-INFINITY);
-          }
-          float m3[11];
-#pragma unroll
-          for (int e = 0; e < 10; ++e)
-            m3[e] = max3f(__uint_as_float(r[cc][3 * e]), __uint_as_float(r[cc][3 * e + 1]), __uint_as_float(r[cc][3 * e + 2]));
-          m3[10] = max3f(__uint_as_float(r[cc][30]), __uint_as_float(r[cc][31]), mx);
-          mx = max3f(max3f(m3[0], m3[1], m3[2]), max3f(m3[3], m3[4], m3[5]), max3f(max3f(m3[6], m3[7], m3[8]), m3[9], m3[10]));
-          if (write_p) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const float2 d = __fadd2_rn(make_float2(__uint_as_float(r[cc][2 * e]), __uint_as_float(r[cc][2 * e + 1])), nref);
-              pk[e] = pack_f16x2(ex2_approx(d.x), ex2_approx(d.y));
-            }
-            tmem_st16(trow + kTmP + 16 * c, pk);
+          for (int e = 0; e < 8; e += 2) {
+            const float2 v = __fadd2_rn(make_float2(__uint_as_float(r[cc][8 * u + e]), __uint_as_float(r[cc][8 * u + e + 1])),
+                                        make_float2(bv[e], bv[e + 1]));
+            r[cc][8 * u + e] = __float_as_uint(v.x);
+            r[cc][8 * u + e + 1] = __float_as_uint(v.y);
           }
         }
+        if (nvalid < kKB) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (32 * cc + e >= nvalid) r[cc][e] = __float_as_uint(-INFINITY);
+        }
+        float m3[11];
+#pragma unroll
+        for (int e = 0; e < 10; ++e)
+          m3[e] = max3f(__uint_as_float(r[cc][3 * e]), __uint_as_float(r[cc][3 * e + 1]), __uint_as_float(r[cc][3 * e + 2]));
+        m3[10] = max3f(__uint_as_float(r[cc][30]), __uint_as_float(r[cc][31]), mx);
+        mx = max3f(max3f(m3[0], m3[1], m3[2]), max3f(m3[3], m3[4], m3[5]), max3f(max3f(m3[6], m3[7], m3[8]), m3[9], m3[10]));
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float2 d = __fadd2_rn(make_float2(__uint_as_float(r[cc][2 * e]), __uint_as_float(r[cc][2 * e + 1])), nref);
+          pk[cc][e] = pack_f16x2(ex2_approx(d.x), ex2_approx(d.y));
+        }
       }
-      pmax = mx;
+      return mx;
     };
     bool ok = true;
+    int h = 0, kb = 0, st = 0, b = 0;
+    uint32_t sph = 0, bph = 0;
     for (int t = 0; t < T; ++t) {
-      const int h = t / KB, kb = t - h * KB, st = t & 1;
-      // ---- at a head's first block, the running output holds the head before's, complete
+      // S of this block is complete, and with it the P V product three blocks back
+      if (!warp_wait_bounded(&sm.s_full[g][b], bph, p.w, abort_flag, 30)) { ok = false; break; }
+      // every thread observes the completion of the stage's copies (the bias) before reading them
+      if (!warp_wait_bounded(&sm.kv_full[st], sph, p.w, abort_flag, 31)) { ok = false; break; }
+      tc_fence_after();
+      // ---- at a head's first block, the running output holds the head before's, complete once the
+      // product of the block before is (the products up to three blocks back are)
       if (t >= 1 && kb == 0) {
-        if (!warp_wait_bounded(&sm.pv_done[g], (uint32_t)(t - 1) & 1u, p.w, abort_flag, 32)) { ok = false; break; }
+        if (!warp_wait_bounded(&sm.pv_done[g][(t - 1) & 1], (uint32_t)((t - 1) >> 1) & 1u, p.w, abort_flag, 32)) { ok = false; break; }
         tc_fence_after();
         finalize(h - 1);
       }
-      if (!warp_wait_bounded(&sm.s_full[g], (uint32_t)t & 1u, p.w, abort_flag, 30)) { ok = false; break; }
-      // every thread observes the completion of the stage's copies (the bias) before reading them
-      if (!warp_wait_bounded(&sm.kv_full[st], (uint32_t)(t >> 1) & 1u, p.w, abort_flag, 31)) { ok = false; break; }
-      // ---- the block before has been added into the running output: its P buffer is free
-      if (t >= 1 && kb != 0) {
-        if (!warp_wait_bounded(&sm.pv_done[g], (uint32_t)(t - 1) & 1u, p.w, abort_flag, 33)) { ok = false; break; }
-      }
-      tc_fence_after();
-      const int nvalid = p.N - kb * BT;          // keys of the block inside the grid (all of them but in the last)
+      const int nvalid = p.N - kb * kKB;         // keys of the block inside the grid (all of them but in the last)
       if (kb == 0) m_run = -INFINITY;
-      // Lazy reference: P is formed against the running reference and the block's maximum checked on the
-      // way; only when some row's maximum exceeds its reference by more than 8 (always in a head's first
-      // block) is P formed again, against the new maximum, so P <= 2^8 stays inside fp16.
-      float mx;
-      pass(st, nvalid, kb != 0, m_run == -INFINITY ? 0.f : m_run, mx);
-      const float m_new = (mx > m_run + 8.f) ? mx : m_run;
-      if (kb == 0 || __any_sync(0xffffffffu, m_new != m_run)) {
-        float unused;
-        pass(st, nvalid, true, m_new == -INFINITY ? 0.f : m_new, unused);
-      }
-      const float mref = m_new == -INFINITY ? 0.f : m_new;
-      // S and the stage's bias have been read: both go back
-      tc_fence_before();
+      uint32_t r[2][32], pk[2][16];
+      // P against the running reference, formed while the block's maximum is taken
+      const float mx = logits(st, b, nvalid, m_run == -INFINITY ? 0.f : m_run, r, pk);
+      // the stage's bias has been read
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&sm.s_free[g]);
-        mbar_arrive(&sm.kv_empty[st]);
+      if (lane == 0) mbar_arrive(&sm.kv_empty[st]);
+      // Lazy reference: it moves to the block's maximum only when that exceeds it by more than 8 (always
+      // in a head's first block), so P <= 2^8 stays inside fp16 and most blocks leave the running output
+      // as it is.
+      const float m_new = (mx > m_run + 8.f) ? mx : m_run;
+      const float ref = m_new == -INFINITY ? 0.f : m_new;
+      if (m_new != m_run) {
+        // the reference moved (this row only): P again, from the logits still in registers
+        const float2 nref = make_float2(-ref, -ref);
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float2 d = __fadd2_rn(make_float2(__uint_as_float(r[cc][2 * e]), __uint_as_float(r[cc][2 * e + 1])), nref);
+            pk[cc][e] = pack_f16x2(ex2_approx(d.x), ex2_approx(d.y));
+          }
       }
-      // ---- the reference moved: rescale this row's running output before this block's product adds in
+      // P over the buffer's first 32 columns, whose S is already in registers
+      tmem_st16(trow + kTmS + kKB * b, pk[0]);
+      tmem_st16(trow + kTmS + kKB * b + 16, pk[1]);
+      // ---- the reference moved: rescale this row's running output, once the block before has been
+      // added, before this block's product adds in
       if (kb != 0 && __any_sync(0xffffffffu, m_new != m_run)) {
-        const float alpha = ex2_approx(m_run - mref);
+        if (!warp_wait_bounded(&sm.pv_done[g][(t - 1) & 1], (uint32_t)((t - 1) >> 1) & 1u, p.w, abort_flag, 33)) { ok = false; break; }
+        tc_fence_after();
+        const float alpha = m_new != m_run ? ex2_approx(m_run - ref) : 1.f;
         uint32_t ro[32];
         tmem_ld32(trow + kTmPV, ro);
         const uint32_t rl = tmem_ld1(trow + kTmPV + kHd);
@@ -510,13 +548,22 @@ __global__ void __launch_bounds__(kAttThreads, 1) k_ta_attend(const __grid_const
         tmem_st32(trow + kTmPV, ro);
         tmem_st1(trow + kTmPV + kHd, __float_as_uint(__uint_as_float(rl) * alpha));
       }
+      // S has been read and P stored: both go to the MMA warp
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.p_full[g]);
+      if (lane == 0) {
+        mbar_arrive(&sm.p_full[g][b]);
+        if (g == 0 && t == 0) mbar_arrive(&sm.go1);
+      }
       m_run = m_new;
+      if (++kb == KB) { kb = 0; ++h; }
+      if (++st == kStages) { st = 0; sph ^= 1u; }
+      if (++b == kSBuf) { b = 0; bph ^= 1u; }
     }
-    if (ok && warp_wait_bounded(&sm.pv_done[g], (uint32_t)(T - 1) & 1u, p.w, abort_flag, 34)) {
+    // the last product (every earlier one is complete with it): its own single-use barrier, since the
+    // alternating ones may already be two phases on
+    if (ok && warp_wait_bounded(&sm.pv_last[g], 0u, p.w, abort_flag, 34)) {
       tc_fence_after();
       finalize(3);
     }

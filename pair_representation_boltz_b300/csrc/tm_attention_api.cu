@@ -188,7 +188,7 @@ tm_status tm_attn_forward(tm_ctx* c, const void* z, const float* mask, int N, tm
     const cuuint64_t d[3] = {(cuuint64_t)kC, (cuuint64_t)N, (cuuint64_t)N};
     const cuuint64_t st2[2] = {(cuuint64_t)kC * 2, (cuuint64_t)N * kC * 2};
     if (!encode(&qmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, q, d, st2, kBoxTaQK, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode(&kmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, k, d, st2, kBoxTaQK, CU_TENSOR_MAP_SWIZZLE_128B))
+        !encode(&kmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, k, d, st2, kBoxTaK, CU_TENSOR_MAP_SWIZZLE_128B))
       return fail(c, TM_ERR_CUDA, "tensor map (q/k)");
     const cuuint64_t dv[3] = {(cuuint64_t)N, (cuuint64_t)kC, (cuuint64_t)N};
     const cuuint64_t sv[2] = {(cuuint64_t)ldv * 2, (cuuint64_t)kC * ldv * 2};

@@ -273,6 +273,7 @@ cudaError_t launch_ta_out(const TaOutParams& p, int grid, cudaStream_t s);
 // Box shapes of the attention kernel's tensor maps (elements innermost first, 128-byte swizzle).
 constexpr Box kBoxTaQK{64, 128, 1, 2};     // 64 channels (a head pair) x 128 positions of one row
 constexpr Box kBoxTaV{64, 32, 1, 2};       // 64 keys x 32 channels of one head of one row
+constexpr Box kBoxTaK{64, 64, 1, 2};      // 64 channels (a head pair) x 64 keys of one row
 constexpr Box kBoxTaBias{64, 128, 1, 2};   // 64 keys x 128 queries of one head
 
 // The dynamic shared-memory limit of a kernel is a property of the kernel's instance on one device

@@ -146,31 +146,29 @@ def _box(name):
 def attention_boxes(N, i, jp):
     """Yield (tensor, barrier, iteration, (x, y, z) start, box) for every copy of one attention CTA (row i,
     query tiles 2 jp and 2 jp + 1), in the order the kernel issues them: Q of both tiles at the first block
-    of each head pair on q_full; per iteration t (head t // kblocks, key block t % kblocks) K, the bias
-    tiles of both query tiles and v on the stage's barrier."""
-    qk, vb, bb = _box("kBoxTaQK"), _box("kBoxTaV"), _box("kBoxTaBias")
-    kblocks = (N + 127) // 128
+    of each head pair on q_full; per iteration t (head t // kblocks, key block t % kblocks of 64 keys) K,
+    the bias tiles of both query tiles and v on the stage's barrier."""
+    q, kbox, vb, bb = _box("kBoxTaQK"), _box("kBoxTaK"), _box("kBoxTaV"), _box("kBoxTaBias")
+    kblocks = (N + 63) // 64
     for t in range(4 * kblocks):
         h, kb = divmod(t, kblocks)
         if kb == 0 and h % 2 == 0:
             for g in range(2):
-                yield ("q", "q", h, (64 * (h // 2), (2 * jp + g) * 128, i), qk)
-        yield ("k", "kv", t, (64 * (h // 2), kb * 128, i), qk)
+                yield ("q", "q", h, (64 * (h // 2), (2 * jp + g) * 128, i), q)
+        yield ("k", "kv", t, (64 * (h // 2), kb * 64, i), kbox)
         for g in range(2):
-            for hf in range(2):
-                yield ("bias", "kv", t, (kb * 128 + 64 * hf, (2 * jp + g) * 128, h), bb)
-        for hf in range(2):
-            yield ("v", "kv", t, (kb * 128 + 64 * hf, 32 * h, i), vb)
+            yield ("bias", "kv", t, (kb * 64, (2 * jp + g) * 128, h), bb)
+        yield ("v", "kv", t, (kb * 64, 32 * h, i), vb)
 
 
 @pytest.mark.parametrize("N", [1, 7, 64, 127, 128, 129, 200, 300, 768, 1025, 3605])
 def test_attention_boxes(N):
     """Every attention copy starts at a non-negative, 16-byte-aligned inner coordinate, and the bytes each
     barrier expects per phase equal the boxes it receives (a load past the grid still moves a whole,
-    zero-filled box): 2 Q boxes per head pair; per block K, four bias boxes and two v boxes."""
-    kq, kk, kb_, kv = 64 * 128 * 2, 64 * 128 * 2, 64 * 128 * 2, 64 * 32 * 2   # kQBytes, kKBytes, kBBytes, kVBytes
+    zero-filled box): 2 Q boxes per head pair; per block of 64 keys K, two bias boxes and one v box."""
+    kq, kk, kb_, kv = 64 * 128 * 2, 64 * 64 * 2, 64 * 128 * 2, 64 * 32 * 2     # kQBytes, kKBytes, kBBytes, kVBytes
     expect_q = 2 * kq
-    expect_kv = kk + 2 * 2 * kb_ + 2 * kv                                      # kStageBytes
+    expect_kv = kk + 2 * kb_ + kv                                              # kStageBytes
     jpairs = ((N + 127) // 128 + 1) // 2
     rows = sorted({0, N // 2, N - 1})
     for i in rows:
@@ -179,7 +177,7 @@ def test_attention_boxes(N):
             for name, bar, t, (x, y, z), (d0, d1, d2, esz) in attention_boxes(N, i, jp):
                 assert x >= 0 and y >= 0 and z >= 0 and (x * esz) % 16 == 0, (N, name, x)
                 got[bar][t] = got[bar].get(t, 0) + d0 * d1 * d2 * esz
-            kblocks = (N + 127) // 128
+            kblocks = (N + 63) // 64
             assert got["q"] == {0: expect_q, 2: expect_q}, (N, got["q"])
             assert got["kv"] == {t: expect_kv for t in range(4 * kblocks)}, N
 
