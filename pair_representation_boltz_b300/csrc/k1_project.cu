@@ -24,7 +24,9 @@
 //               the hi and lo weights of the half once at start (128 KB).
 //   warp 1      TMEM (2 x 256 columns) and tcgen05.mma with the channels on
 //               the TMEM lanes: D_proj[c][p] = W'_proj z^T and D_gate[c][p] =
-//               W'_gate z^T (M = 128 channels, N = 128 pairs), hi + lo each.
+//               W'_gate z^T (M = 128 channels, N = 128 pairs), hi + lo each;
+//               operand descriptors are formed once and offset per MMA (a
+//               descriptor built per MMA doubles the thread's issue time).
 //   warps 2..5  LayerNorm statistics, thread = pair: one pass over the z row
 //               (sums of z - z_0 and of its square, fp32x2; the shift by the
 //               row's first value keeps the variance free of cancellation for
@@ -32,21 +34,22 @@
 //               as it is read; one tile ahead of the epilogue, double-buffered
 //               in shared memory behind mbarriers, with the pair mask as one
 //               bit per pair (warp ballot).
-//   warps 6..13 epilogue, thread = channel: two warps per TMEM lane quadrant
-//               split the 128 pairs; per-channel folding constants live in
+//   warps 6..21 epilogue, thread = channel: four warps per TMEM lane quadrant
+//               split the 128 pairs, 32 each (four epilogue warps per SMSP hide
+//               each other's latency); per-channel folding constants live in
 //               registers; two pairs at a time in fp32x2 arithmetic, the
 //               two sigmoids with two exponentials and one shared reciprocal
 //               (three MUFU operations), no branch. Results go through
-//               shared memory: each warp fills its own 32-channel x 64-pair
-//               staging box (128-byte swizzle) that its lane 0 writes out with
-//               one TMA store per tile, so channel rows leave as 128-byte lines
+//               shared memory: each warp fills its own 32-channel x 32-pair
+//               staging box (64-byte swizzle) that its lane 0 writes out with
+//               one TMA store per tile, so channel rows leave as 64-byte lines
 //               and no warp waits for another; the store drains while the next
-//               tile's MMA runs. Each 32-pair half of the warp's accumulator
-//               columns is read by two TMEM loads under one wait (a wait costs a
-//               load's whole latency), and the wait for the last store to have
-//               read the staging box comes after the first chunk's arithmetic. (Stores straight from the threads, one channel
-//               row per lane, scatter each warp instruction over 32 DRAM pages
-//               and ran 6x slower.)
+//               tile's MMA runs. Each 16-pair chunk of the warp's accumulator
+//               columns is read by two TMEM loads (projection, gate) under one
+//               wait, and the wait for the last store to have read the staging
+//               box comes after the first chunk's arithmetic. (Stores straight
+//               from the threads, one channel row per lane, scatter each warp
+//               instruction over 32 DRAM pages and ran 6x slower.)
 #include "tm_kernels.h"
 
 namespace tmk {
@@ -57,7 +60,7 @@ constexpr int STAGES = 2;
 constexpr int Z_BYTES = BM * kC * 2;           // 32 KB (two 16 KB K-chunks)
 constexpr int W_MAT = kC * kC * 2;             // one 128 x 128 bf16 matrix, two K-chunks: 32 KB
 constexpr int W_BYTES = 4 * W_MAT;             // proj hi, proj lo, gate hi, gate lo
-constexpr int STAT_WARPS = 4, EPI_WARPS = 8;
+constexpr int STAT_WARPS = 4, EPI_WARPS = 16;
 constexpr int THREADS = 64 + 32 * (STAT_WARPS + EPI_WARPS);   // TMA, MMA, statistics, epilogue warps
 constexpr int OUT_BYTES = EPI_WARPS * (int)kBoxProjOut.bytes();      // one staging box per epilogue warp
 constexpr int STAT_BUF = (BM / 2) * 16 + 16;   // float4 {rstd_2k, rstd_2k+1, nmu_2k, nmu_2k+1} + 4 mask words
@@ -67,7 +70,7 @@ constexpr int TMEM_COLS = 512;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(2 * kBoxProjZ.bytes() == Z_BYTES, "z tile = two boxes");
 static_assert(2 * kBoxProjW.bytes() == W_MAT, "weight matrix = two boxes");
-static_assert(kBoxProjOut.d0 * 2 == 128 && kBoxProjOut.d2 == 32, "a staging box is 32 channel rows of 128 bytes");
+static_assert(kBoxProjOut.d0 * 2 == 64 && kBoxProjOut.d2 == 32, "a staging box is 32 channel rows of 64 bytes");
 static_assert(OUT_BYTES == 32768, "staging budget");
 
 // F16OUT: a and b leave as fp16, each value rounded to bf16 first (the storage the update defines)
@@ -162,7 +165,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t ph = 0;
         int local = 0;
         if (wait_bounded(wfull, 0, p.w, abort_flag, 12)) {
-          const uint32_t w0 = smem_u32(ws);
+          // descriptors of the weight tiles and of z stage 0; an operand's descriptor is its tile's plus
+          // the byte offset / 16 (the start-address field, shared memory below 256 KB)
+          const uint64_t dw = make_sdesc_sw128(smem_u32(ws), 16, 1024);
+          const uint64_t dz = make_sdesc_sw128(smem_u32(zs), 16, 1024);
           for (long long u = cta; u < p.total_tiles; u += nctas, ++local) {
             const int buf = local & 1;
             const uint32_t use = (uint32_t)(local >> 1);
@@ -170,18 +176,19 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (!wait_bounded(&zfull[s], ph, p.w, abort_flag, 14)) break;
             tc_fence_after();
             const uint32_t d = tmem_base + (uint32_t)(buf * 2 * BM);
-            const uint32_t z0 = smem_u32(zs + s * Z_BYTES);
+            const uint64_t dzs = dz + (uint32_t)(s * (Z_BYTES >> 4));
 #pragma unroll
             for (int kc = 0; kc < 2; ++kc) {
 #pragma unroll
               for (int ks = 0; ks < 4; ++ks) {
-                const uint32_t off = kc * (W_MAT / 2) + ks * 32;
-                const uint64_t bd = make_sdesc_sw128(z0 + kc * (Z_BYTES / 2) + ks * 32, 16, 1024);
+                constexpr uint32_t kW = W_MAT >> 4;
+                const uint32_t off = (uint32_t)(kc * (W_MAT / 2) + ks * 32) >> 4;
+                const uint64_t bd = dzs + (uint32_t)((kc * (Z_BYTES / 2) + ks * 32) >> 4);
                 const uint32_t acc = (kc | ks) != 0;
-                mma_f16(d, make_sdesc_sw128(w0 + 0 * W_MAT + off, 16, 1024), bd, idesc, acc);
-                mma_f16(d, make_sdesc_sw128(w0 + 1 * W_MAT + off, 16, 1024), bd, idesc, 1u);
-                mma_f16(d + BM, make_sdesc_sw128(w0 + 2 * W_MAT + off, 16, 1024), bd, idesc, acc);
-                mma_f16(d + BM, make_sdesc_sw128(w0 + 3 * W_MAT + off, 16, 1024), bd, idesc, 1u);
+                mma_f16(d, dw + off, bd, idesc, acc);
+                mma_f16(d, dw + (kW + off), bd, idesc, 1u);
+                mma_f16(d + BM, dw + (2 * kW + off), bd, idesc, acc);
+                mma_f16(d + BM, dw + (3 * kW + off), bd, idesc, 1u);
               }
             }
             mma_commit(&zempty[s]);
@@ -259,10 +266,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     } else {
       // ------------------------------------------------------------ epilogue, thread = channel
-      const int ew = warp - 2 - STAT_WARPS;    // 0..7
+      const int ew = warp - 2 - STAT_WARPS;    // 0..15
       const int q = warp & 3;                  // TMEM lane quadrant: channels 32q .. 32q+31
       const int c = q * 32 + lane;
-      const int pbase = (ew >> 2) * 64;        // this warp's 64 pair columns
+      const int pbase = (ew >> 2) * 32;        // this warp's 32 pair columns
       const CUtensorMap* omap = half ? &bmap : &amap;
       uint8_t* const box = ostg + ew * (int)kBoxProjOut.bytes();
       const float* cst = p.consts + half * 512;
@@ -310,31 +317,27 @@ __global__ void __launch_bounds__(THREADS, 1)
           const float2 r2 = __bfloat1622float2(__floats2bfloat162_rn(x, y));
           return pack_f16x2(r2.x * osc, r2.y * osc);
         };
-        // two 32-pair halves, each read by two TMEM loads under one wait, then computed 16 pairs at a time
-        uint32_t pr[32], gt[32];
+        // two 16-pair chunks, each read by two TMEM loads (projection, gate) under one wait
 #pragma unroll
-        for (int hh = 0; hh < 4; ++hh) {
-          if ((hh & 1) == 0) {
-            tmem_ld32(ta + (uint32_t)(hh * 16), pr);
-            tmem_ld32(ta + BM + (uint32_t)(hh * 16), gt);
-            tmem_ld_wait();
-          }
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t pr[16], gt[16];
+          tmem_ld16(ta + (uint32_t)(hh * 16), pr);
+          tmem_ld16(ta + BM + (uint32_t)(hh * 16), gt);
+          tmem_ld_wait();
           const int p0 = pbase + hh * 16;
           const uint32_t mword = mw[p0 >> 5] >> (p0 & 31);
-          const uint32_t* prc = pr + 16 * (hh & 1);
-          const uint32_t* gtc = gt + 16 * (hh & 1);
           uint32_t packed[8];
           if ((mword & 0xFFFFu) == 0xFFFFu) {
             // all 16 pairs unmasked and inside the grid (warp-uniform): no per-element mask
 #pragma unroll
             for (int e = 0; e < 16; e += 2) {
-              const float2 v = pair_values(p0, e, prc, gtc);
+              const float2 v = pair_values(p0, e, pr, gt);
               packed[e >> 1] = pack(v.x, v.y);
             }
           } else {
 #pragma unroll
             for (int e = 0; e < 16; e += 2) {
-              const float2 v = pair_values(p0, e, prc, gtc);
+              const float2 v = pair_values(p0, e, pr, gt);
               packed[e >> 1] = pack(((mword >> e) & 1u) ? v.x : 0.f, ((mword >> (e + 1)) & 1u) ? v.y : 0.f);
             }
           }
@@ -344,10 +347,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (lane == 0) bulk_wait_read<0>();
             __syncwarp();
           }
-          // 32 bytes of this channel's 128-byte staging row: 16-byte units 2hh, 2hh+1
+          // 32 bytes of this channel's 64-byte staging row: 16-byte units 2hh, 2hh+1
 #pragma unroll
           for (int k = 0; k < 2; ++k)
-            *reinterpret_cast<uint4*>(box + sw128_offset(lane, hh * 2 + k)) =
+            *reinterpret_cast<uint4*>(box + sw64_offset(lane, hh * 2 + k)) =
                 make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
         }
         // the accumulator and the statistics buffer are free (every TMEM load has been waited for)

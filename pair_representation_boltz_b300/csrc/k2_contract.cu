@@ -177,6 +177,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         constexpr bool A_MN = MODE == CONTRACT_IN, B_MN = MODE != CONTRACT_OUT;
         const uint32_t idesc_full = make_idesc(BM, BN, fmt, A_MN, B_MN);
         const uint32_t idesc_last = make_idesc(BM, p.last_n, fmt, A_MN, B_MN);
+        // descriptors of stage 0's A and B tiles; an operand's descriptor is its tile's plus the byte
+        // offset / 16 (the start-address field, shared memory below 256 KB): formed once, not per MMA
+        const uint32_t t0 = smem_u32(tiles);
+        const uint64_t da = A_MN ? make_sdesc_sw128(t0, 8192, 1024) : make_sdesc_sw128(t0, 16, 1024);
+        const uint64_t db = B_MN ? make_sdesc_sw128(t0 + A_BYTES, 8192, 1024) : make_sdesc_sw128(t0 + A_BYTES, 16, 1024);
+        constexpr uint32_t KS_A = (A_MN ? 2048 : 32) >> 4, KS_B = (B_MN ? 2048 : 32) >> 4;
         int s = 0;
         uint32_t ph = 0;
         int local = 0;
@@ -194,16 +200,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t a0 = smem_u32(tiles + s * STAGE_BYTES);
-            const uint32_t b0 = a0 + A_BYTES;
+            const uint32_t so = (uint32_t)s * (uint32_t)(STAGE_BYTES >> 4);
+            const uint64_t ad = da + so, bd = db + so;
 #pragma unroll
-            for (int ks = 0; ks < BK / 16; ++ks) {
-              const uint64_t ad = A_MN ? make_sdesc_sw128(a0 + ks * 2048, 8192, 1024)
-                                       : make_sdesc_sw128(a0 + ks * 32, 16, 1024);
-              const uint64_t bd = B_MN ? make_sdesc_sw128(b0 + ks * 2048, 8192, 1024)
-                                       : make_sdesc_sw128(b0 + ks * 32, 16, 1024);
-              mma_f16_pair(d, ad, bd, idesc, (kb | ks) != 0);
-            }
+            for (int ks = 0; ks < BK / 16; ++ks)
+              mma_f16_pair(d, ad + (uint32_t)(ks * KS_A), bd + (uint32_t)(ks * KS_B), idesc, (kb | ks) != 0);
             mma_commit_pair(&empty[s]);
             if (++s == STAGES) {
               s = 0;

@@ -342,7 +342,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t ph = 0;
         int local = 0;
         if (wait_bounded(&b.wfull, 0, p.w, abort_flag, 33)) {
-          const uint32_t z0 = smem_u32(sm.zs), o0 = smem_u32(sm.wo), g0 = smem_u32(sm.wg);
+          // operand descriptors formed once; per MMA the tile's descriptor plus the byte offset / 16
+          // (the start-address field, shared memory below 256 KB)
+          const uint64_t dz = make_sdesc_sw128(smem_u32(sm.zs), 16, 1024);
+          const uint64_t dwo = make_sdesc_sw128(smem_u32(sm.wo), 16, 1024);
+          const uint64_t dwg = make_sdesc_sw128(smem_u32(sm.wg), 16, 1024);
+          const uint64_t dx = make_sdesc_sw128(smem_u32(sm.xs), SLOT / 2, 1024);
           for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++local) {
             const int buf = local & 1;
             const int xsl = local & 1;
@@ -352,17 +357,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (!wait_bounded(&b.zfull, ph, p.w, abort_flag, 36)) break;
             tc_fence_after();
             const uint32_t d = tmem_base + (uint32_t)(buf * 2 * kC);
-            const uint32_t x0 = smem_u32(sm.xs + xsl * SLOT);
+            const uint64_t dxs = dx + (uint32_t)((xsl * SLOT) >> 4);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
               // x: 16 channel rows of 128 bytes per K step; the two 64-pair halves are SLOT/2 apart
-              const uint32_t woff = (ks >> 2) * 16384 + (ks & 3) * 32;
-              mma_f16(d, make_sdesc_sw128(x0 + ks * 2048, SLOT / 2, 1024), make_sdesc_sw128(o0 + woff, 16, 1024),
-                      id_y, ks != 0);
-              mma_f16(d + kC, make_sdesc_sw128(z0 + woff, 16, 1024), make_sdesc_sw128(g0 + woff, 16, 1024), id_g,
-                      ks != 0);
-              mma_f16(d + kC, make_sdesc_sw128(z0 + woff, 16, 1024),
-                      make_sdesc_sw128(g0 + 2 * 16384 + woff, 16, 1024), id_g, 1u);
+              const uint32_t woff = (uint32_t)((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+              mma_f16(d, dxs + (uint32_t)((ks * 2048) >> 4), dwo + woff, id_y, ks != 0);
+              mma_f16(d + kC, dz + woff, dwg + woff, id_g, ks != 0);
+              mma_f16(d + kC, dz + woff, dwg + ((2u * 16384u) >> 4) + woff, id_g, 1u);
             }
             mma_commit(&b.xempty[xsl]);
             mma_commit(&b.zempty);
@@ -477,7 +479,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t ph = 0;
         int local = 0;
         if (wait_bounded(&b.wfull, 0, p.w, abort_flag, 33)) {
-          const uint32_t h0 = smem_u32(sm.xh), z0 = smem_u32(sm.zs), o0 = smem_u32(sm.wo), g0 = smem_u32(sm.wg);
+          // operand descriptors formed once; per MMA the tile's descriptor plus the byte offset / 16
+          const uint64_t dh = make_sdesc_sw128(smem_u32(sm.xh), 16, 1024);
+          const uint64_t dz = make_sdesc_sw128(smem_u32(sm.zs), 16, 1024);
+          const uint64_t dwo = make_sdesc_sw128(smem_u32(sm.wo), 16, 1024);
+          const uint64_t dwg = make_sdesc_sw128(smem_u32(sm.wg), 16, 1024);
           for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++local) {
             const int buf = local & 1;
             const uint32_t use = (uint32_t)(local >> 1);
@@ -488,12 +494,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint32_t d = tmem_base + (uint32_t)(buf * 2 * kC);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
-              const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-              mma_f16(d, make_sdesc_sw128(h0 + off, 16, 1024), make_sdesc_sw128(o0 + off, 16, 1024), id_y, ks != 0);
-              mma_f16(d + kC, make_sdesc_sw128(z0 + off, 16, 1024), make_sdesc_sw128(g0 + off, 16, 1024), id_g,
-                      ks != 0);
-              mma_f16(d + kC, make_sdesc_sw128(z0 + off, 16, 1024),
-                      make_sdesc_sw128(g0 + 2 * 16384 + off, 16, 1024), id_g, 1u);
+              const uint32_t off = (uint32_t)((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+              mma_f16(d, dh + off, dwo + off, id_y, ks != 0);
+              mma_f16(d + kC, dz + off, dwg + off, id_g, ks != 0);
+              mma_f16(d + kC, dz + off, dwg + ((2u * 16384u) >> 4) + off, id_g, 1u);
             }
             mma_commit(&b.zempty);
             mma_commit(&b.tfull[buf]);

@@ -111,13 +111,18 @@ constexpr uint32_t ID_KK_H = make_idesc(128, 128, FMT_F16, false, false);
 constexpr uint32_t ID_KM_H = make_idesc(128, 128, FMT_F16, false, true);
 constexpr uint32_t ID_MM_H = make_idesc(128, 128, FMT_F16, true, true);
 
-// D (+)= A B^T over the 128 K of two tiles
+// D (+)= A B^T over the 128 K of two tiles. Each operand's descriptor is formed once and offset per K
+// step (the start-address field holds the byte address / 16, shared memory below 256 KB): one thread
+// issues the eight MMAs about twice as fast as with a descriptor built per MMA.
 __device__ __forceinline__ void mma_tile(uint32_t d, uint32_t a, bool a_mn, uint32_t b, bool b_mn, uint32_t idesc,
                                          bool acc) {
+  const uint64_t da = a_mn ? mndesc(a, 0) : kdesc(a, 0), db = b_mn ? mndesc(b, 0) : kdesc(b, 0);
 #pragma unroll
-  for (int ks = 0; ks < 8; ++ks)
-    mma_f16(d, a_mn ? mndesc(a, ks) : kdesc(a, ks), b_mn ? mndesc(b, ks) : kdesc(b, ks), idesc,
-            (acc || ks != 0) ? 1u : 0u);
+  for (int ks = 0; ks < 8; ++ks) {
+    const uint32_t oa = a_mn ? (uint32_t)ks * (2048u >> 4) : (uint32_t)((ks >> 2) * SLAB + (ks & 3) * 32) >> 4;
+    const uint32_t ob = b_mn ? (uint32_t)ks * (2048u >> 4) : (uint32_t)((ks >> 2) * SLAB + (ks & 3) * 32) >> 4;
+    mma_f16(d, da + oa, db + ob, idesc, (acc || ks != 0) ? 1u : 0u);
+  }
 }
 
 // Wait for the MMA barrier with a CTA-uniform outcome.

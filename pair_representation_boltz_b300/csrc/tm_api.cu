@@ -375,8 +375,8 @@ tm_status run_project_bf16(tm_ctx* c, const void* z, const float* mask, int N, f
   {
     const cuuint64_t od[3] = {(cuuint64_t)N, (cuuint64_t)N, (cuuint64_t)kC};
     const cuuint64_t os[2] = {(cuuint64_t)ld * 2, (cuuint64_t)N * ld * 2};
-    if (!encode(&amap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a, od, os, kBoxProjOut, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode(&bmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, b, od, os, kBoxProjOut, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!encode(&amap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a, od, os, kBoxProjOut, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !encode(&bmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, b, od, os, kBoxProjOut, CU_TENSOR_MAP_SWIZZLE_64B))
       return fail(c, TM_ERR_CUDA, "tensor map (a/b, projection store)");
   }
   ProjectParams p;

@@ -102,7 +102,7 @@ struct Box {
 };
 constexpr Box kBoxProjZ{64, (uint32_t)kProjTileJ, 1, 2};              // z tile, one 64-channel half
 constexpr Box kBoxProjW{64, 128, 1, 2};                               // one K-half of a 128 x 128 weight
-constexpr Box kBoxProjOut{64, 1, 32, 2};                              // a or b store: 64 pairs x 32 channels
+constexpr Box kBoxProjOut{32, 1, 32, 2};                              // a or b store: 32 pairs x 32 channels
 constexpr Box kBoxContractOutA{(uint32_t)kContractBK, (uint32_t)kContractBM / 2, 1, 2};   // one CTA's A rows
 constexpr Box kBoxContractOutB{(uint32_t)kContractBK, (uint32_t)kContractBN / 2, 1, 2};   // one CTA's B rows
 constexpr Box kBoxContractIn{64, (uint32_t)kContractBK, 1, 2};        // incoming: 64-wide slab of i or j
