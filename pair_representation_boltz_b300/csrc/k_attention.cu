@@ -92,6 +92,14 @@ __global__ void __launch_bounds__(NT, 1) k_ta_project(const TaProjectParams p) {
     const int i = valid ? (int)(pr / p.N) : 0;
     const int j = valid ? (int)(pr - (long long)i * p.N) : 0;
     const long long zp = p.transpose ? (long long)j * p.N + i : pr;   // the z pair it reads
+    {
+      // L2 prefetch of the z row this thread's pair reads in the CTA's next tile (one thread per pair)
+      const long long pn = pr + (long long)gridDim.x * BT;
+      if (h == 0 && pn < p.P) {
+        const int in = (int)(pn / p.N), jn = (int)(pn - (long long)in * p.N);
+        prefetch_l2_bulk(p.z + (p.transpose ? (long long)jn * p.N + in : pn) * kC, kC * 2);
+      }
+    }
 
     // ---- LayerNorm of z: quarter statistics combined over the pair's four threads
     float f[32];
@@ -622,6 +630,8 @@ __global__ void __launch_bounds__(NT, 1) k_ta_out(const TaOutParams p) {
     const bool valid = pr < p.P;
     const int i = valid ? (int)(pr / p.N) : 0;
     const int j = valid ? (int)(pr - (long long)i * p.N) : 0;
+    // L2 prefetch of the o row this thread's pair reads in the CTA's next tile (one thread per pair)
+    if (h == 0 && pr + (long long)gridDim.x * BT < p.P) prefetch_l2_bulk(p.o + (pr + (long long)gridDim.x * BT) * kC, kC * 2);
     float f[32];
     if (valid) load32_f16(p.o + pr * kC + c0, f);
     else
