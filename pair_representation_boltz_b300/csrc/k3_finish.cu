@@ -330,6 +330,17 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_expect_tx(&b.zfull, Z_BYTES);
           tma_load_3d(sm.zs, &zmap, &b.zfull, 0, p.j0 + jt * BM, p.i0 + il);
           tma_load_3d(sm.zs + Z_BYTES / 2, &zmap, &b.zfull, 64, p.j0 + jt * BM, p.i0 + il);
+          {
+            // the next tile's z into L2 now: its load waits for this tile's MMAs (one z stage), and
+            // then finds it there instead of in HBM
+            const long long tn = t + gridDim.x;
+            if (tn < p.total_tiles) {
+              const int iln = (int)(tn / p.tiles_j);
+              const int jtn = (int)(tn - (long long)iln * p.tiles_j);
+              tma_prefetch_l2_3d(&zmap, 0, p.j0 + jtn * BM, p.i0 + iln);
+              tma_prefetch_l2_3d(&zmap, 64, p.j0 + jtn * BM, p.i0 + iln);
+            }
+          }
           ph ^= 1u;
         }
       }
@@ -468,6 +479,17 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_expect_tx(&b.zfull, Z_BYTES);
           tma_load_3d(sm.zs, &zmap, &b.zfull, 0, p.j0 + jt * BM, p.i0 + il);
           tma_load_3d(sm.zs + Z_BYTES / 2, &zmap, &b.zfull, 64, p.j0 + jt * BM, p.i0 + il);
+          {
+            // the next tile's z into L2 now: its load waits for this tile's MMAs (one z stage), and
+            // then finds it there instead of in HBM
+            const long long tn = t + gridDim.x;
+            if (tn < p.total_tiles) {
+              const int iln = (int)(tn / p.tiles_j);
+              const int jtn = (int)(tn - (long long)iln * p.tiles_j);
+              tma_prefetch_l2_3d(&zmap, 0, p.j0 + jtn * BM, p.i0 + iln);
+              tma_prefetch_l2_3d(&zmap, 64, p.j0 + jtn * BM, p.i0 + iln);
+            }
+          }
           ph ^= 1u;
         }
       }
