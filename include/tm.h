@@ -308,9 +308,13 @@ tm_status tm_backward(tm_ctx* ctx, const void* z, const float* mask, int N, tm_d
  *
  * Linear layers have no bias; a query row with no valid key (a masked token's
  * row for the starting node, column for the ending node) gives o = 0.
- * Supported: bf16, c_z = 128, H = 4, c = 32; q, k, v, g, b and P are bf16
- * operands of tcgen05 products with float32 accumulation, the softmax runs
- * in float32 (online, one pass over the keys). */
+ * Supported: bf16 z and out, c_z = 128, H = 4, c = 32. Every intermediate (zh,
+ * the weight images, q, k, v, g, the bias b and the softmax weights P, the
+ * gated output o) is fp16, zh, v, o and the weight images times powers of two
+ * that the weights' bounds fix, as operands of tcgen05 products with float32
+ * accumulation; the softmax runs in float32 in base 2, online over key blocks
+ * of 64 against a lazy running reference. Weights whose bound on q, k or b
+ * reaches 2^15 are refused by tm_attn_create (TM_ERR_UNSUPPORTED). */
 typedef enum { TM_ATTN_STARTING = 0, TM_ATTN_ENDING = 1 } tm_attn_node;
 
 /* Host float32 arrays, Linear layout [out][in]. */
@@ -324,13 +328,14 @@ typedef struct {
 /* A context holding one triangle attention layer (freed by tm_destroy; the
  * update's calls reject it with TM_ERR_INVALID). Returns TM_ERR_INVALID for a
  * NULL argument, TM_ERR_UNSUPPORTED for any shape but c_z = 128, H = 4,
- * c = 32. Synchronous; the caller may free its arrays afterwards. */
+ * c = 32 or for weights that could push q, k or the bias past fp16's range.
+ * Synchronous; the caller may free its arrays afterwards. */
 tm_status tm_attn_create(int c_z, int heads, int c_head, const tm_attn_weights* w, tm_ctx** out_ctx);
 
 /* out = triangle attention of the given node over z.
  *   z     device bf16 [N][N][c_z]; mask device float32 [N] or NULL;
  *   out   device bf16 [N][N][c_z], must not overlap z.
- * Workspace: about 1.3 kB per pair (q, k, v, g, o and the bias, bf16).
+ * Workspace: about 1.3 kB per pair (q, k, v, g, o and the bias, fp16).
  * opt: timeout_ms and workspace_limit apply, other fields must be 0. dtype
  * TM_F32 returns TM_ERR_UNSUPPORTED. Stream-ordered like tm_forward. */
 tm_status tm_attn_forward(tm_ctx* ctx, const void* z, const float* mask, int N, tm_dtype dtype,
