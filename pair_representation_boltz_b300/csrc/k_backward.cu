@@ -167,19 +167,6 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_output(const BwdOutParams p) {
     const int i = p.i0 + il, j = p.j0 + jl;
     const long long pr = (long long)i * p.N + j;   // pair of the grid
     const float* xp = p.x + (long long)il * p.ldx + jl + (long long)c0 * p.xplane;
-    {
-      // L2 prefetch of what the next tile of this CTA reads: x (one channel per thread of the first
-      // 128) and, for whole grid rows, z, dout and the LayerNorm_in statistics
-      const long long tn = t + gridDim.x;
-      if (tn < p.tiles && p.bj >= BT) {
-        const long long q0 = tn * BT, q1 = (q0 + BT < PB) ? q0 + BT : PB;
-        const long long g0 = (long long)p.i0 * p.N + q0, g1 = (long long)p.i0 * p.N + q1;
-        if (tid < kC) prefetch_plane_rows(p.x + (long long)tid * p.xplane, p.ldx, p.bj, q0, q1);
-        else if (p.bj == p.N && tid == kC) prefetch_range(p.z, g0 * 2 * kC, g1 * 2 * kC);
-        else if (p.bj == p.N && tid == kC + 1) prefetch_range(p.dout, g0 * 2 * kC, g1 * 2 * kC);
-        else if (p.bj == p.N && tid == kC + 2) prefetch_range(p.zstat, g0 * 8, g1 * 8);
-      }
-    }
 
     // ---- zh; x of this quarter (the contraction's output times x_unscale): (mean, M2), combined over
     // the four quarters (Chan et al.)
@@ -266,6 +253,21 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_output(const BwdOutParams p) {
       mma_tile(tmem + 2 * kC, a_dgg, true, a_zh, true, ID_MM_H, local > 0); // dW_g += dgg zh^T
       mma_tile(tmem + 3 * kC, a_dy, true, a_xh, true, ID_MM_H, local > 0);  // dW_o += dy xh^T
       mma_commit(&sm.bar);
+    }
+    {
+      // L2 prefetch of what the next tile of this CTA reads: x (one channel per thread of the first
+      // 128) and, for whole grid rows, z, dout and the LayerNorm_in statistics; issued here, where the
+      // warps wait for the second MMA group anyway (one bulk request per lane takes the issuing warps
+      // thousands of cycles)
+      const long long tn = t + gridDim.x;
+      if (tn < p.tiles && p.bj >= BT) {
+        const long long q0 = tn * BT, q1 = (q0 + BT < PB) ? q0 + BT : PB;
+        const long long g0 = (long long)p.i0 * p.N + q0, g1 = (long long)p.i0 * p.N + q1;
+        if (tid < kC) prefetch_plane_rows(p.x + (long long)tid * p.xplane, p.ldx, p.bj, q0, q1);
+        else if (p.bj == p.N && tid == kC) prefetch_range(p.z, g0 * 2 * kC, g1 * 2 * kC);
+        else if (p.bj == p.N && tid == kC + 1) prefetch_range(p.dout, g0 * 2 * kC, g1 * 2 * kC);
+        else if (p.bj == p.N && tid == kC + 2) prefetch_range(p.zstat, g0 * 8, g1 * 8);
+      }
     }
     if (!cta_wait(&sm.bar, phase, p.w, &sm.abort_flag, 2)) { ok = false; break; }
     phase ^= 1u;
