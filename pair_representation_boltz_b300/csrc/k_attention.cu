@@ -92,12 +92,19 @@ __global__ void __launch_bounds__(NT, 1) k_ta_project(const TaProjectParams p) {
     const int i = valid ? (int)(pr / p.N) : 0;
     const int j = valid ? (int)(pr - (long long)i * p.N) : 0;
     const long long zp = p.transpose ? (long long)j * p.N + i : pr;   // the z pair it reads
-    {
-      // L2 prefetch of the z row this thread's pair reads in the CTA's next tile (one thread per pair)
+    if (!p.transpose) {
+      // L2 prefetch of the CTA's next tile of z: its pairs' rows are one contiguous run (one request)
+      const long long n0 = (t + gridDim.x) * BT;
+      if (tid == 0 && n0 < p.P) {
+        const long long n1 = n0 + BT < p.P ? n0 + BT : p.P;
+        prefetch_l2_bulk(p.z + n0 * kC, (uint32_t)((n1 - n0) * kC * 2));
+      }
+    } else {
+      // transposed, the rows of the next tile lie N rows apart: one request per pair, by its first thread
       const long long pn = pr + (long long)gridDim.x * BT;
       if (h == 0 && pn < p.P) {
         const int in = (int)(pn / p.N), jn = (int)(pn - (long long)in * p.N);
-        prefetch_l2_bulk(p.z + (p.transpose ? (long long)jn * p.N + in : pn) * kC, kC * 2);
+        prefetch_l2_bulk(p.z + ((long long)jn * p.N + in) * kC, kC * 2);
       }
     }
 
@@ -654,8 +661,14 @@ __global__ void __launch_bounds__(NT, 1) k_ta_out(const TaOutParams p) {
     const bool valid = pr < p.P;
     const int i = valid ? (int)(pr / p.N) : 0;
     const int j = valid ? (int)(pr - (long long)i * p.N) : 0;
-    // L2 prefetch of the o row this thread's pair reads in the CTA's next tile (one thread per pair)
-    if (h == 0 && pr + (long long)gridDim.x * BT < p.P) prefetch_l2_bulk(p.o + (pr + (long long)gridDim.x * BT) * kC, kC * 2);
+    if (tid == 0) {
+      // L2 prefetch of the CTA's next tile of o: its pairs' rows are one contiguous run
+      const long long n0 = (t + gridDim.x) * BT;
+      if (n0 < p.P) {
+        const long long n1 = n0 + BT < p.P ? n0 + BT : p.P;
+        prefetch_l2_bulk(p.o + n0 * kC, (uint32_t)((n1 - n0) * kC * 2));
+      }
+    }
     float f[32];
     if (valid) load32_f16(p.o + pr * kC + c0, f);
     else

@@ -257,3 +257,28 @@ def test_backward_prefetch_ranges_stay_aligned_and_inside(N, B):
             g0, g1 = r0 * N + q0, r0 * N + q1
             _prefetch(0, g0 * 256, g1 * 256, zb)
             _prefetch(0, g0 * 8, g1 * 8, zst)
+
+
+@pytest.mark.parametrize("N", [1, 37, 128, 129, 200, 1023, 3605])
+@pytest.mark.parametrize("grid", [1, 148])
+def test_attention_prefetch_ranges_stay_aligned_and_inside(N, grid):
+    """The triangle attention's per-pair kernels prefetch into L2 the rows of the CTA's next tile of 128
+    pairs: the projection (starting node) and the output stage as one request over the tile's contiguous
+    rows of z (bf16) or o (fp16), 256 bytes per pair; the projection of the ending node one 256-byte
+    request per pair at its transposed row. Every request must start on 16 bytes, span a multiple of 16
+    bytes and lie inside the N^2 x 256-byte buffer."""
+    P = N * N
+    alloc = P * 256
+    tiles = (P + 127) // 128
+    for t in sorted(set(range(0, tiles, max(1, tiles // 97))) | {tiles - 1}):
+        n0 = (t + grid) * 128
+        if n0 < P:
+            n1 = min(n0 + 128, P)
+            b0, nbytes = n0 * 256, (n1 - n0) * 256
+            assert b0 % 16 == 0 and nbytes % 16 == 0 and 0 < nbytes <= 32768 and b0 + nbytes <= alloc
+        for r in (0, 1, 127):
+            pn = t * 128 + r + grid * 128
+            if pn < P:
+                i_n, j_n = divmod(pn, N)
+                b0 = (j_n * N + i_n) * 256
+                assert b0 % 16 == 0 and b0 + 256 <= alloc
