@@ -1,4 +1,4 @@
-"""Host-side replay of the finish kernel's barrier protocol (no GPU needed).
+"""Host-side replay of the finish kernels' barrier protocols (no GPU needed).
 
 The finish kernel with fp16 x (csrc/k3_finish.cu, k3_finish_x16) is a persistent CTA whose roles meet at
 mbarriers: a TMA thread fills two x slots and one z stage per tile (and the weights once), one thread
@@ -208,12 +208,17 @@ class Model:
         self.pending_store[e] = None
 
     # ------------------------------------------------------------------ scheduler
-    def run(self):
+    def _roles(self):
         roles = {"tma": self.producer(), "mma": self.issuer()}
         roles.update({f"st{w}": self.statistics(w) for w in range(LN_WARPS)})
         roles.update({f"epi{e}": self.epilogue(e) for e in range(EPI_WARPS)})
+        return roles
+
+    def run(self):
+        roles = self._roles()
         waiting, done, count, meant = {}, set(), {}, {}
-        producer_side = {"xempty", "zempty", "tempty", "sempty"}   # waits that pass at once on a first use
+        # waits that pass at once on a first use
+        producer_side = {"xempty", "zempty", "tempty", "sempty", "hempty"}
 
         def advance(k):
             try:
@@ -283,3 +288,176 @@ def test_the_model_catches_staging_rewritten_under_a_store():
         WAIT_FOR_STORE = False
 
     assert _caught(Broken) > 0
+
+
+class ModelX32:
+    """The float32-x form (k3_finish_x32): one x slot, read by the four LayerNorm warps (after their z
+    statistics for the same tile), which write the normalised fp16 x-hat operand; the MMA reads x-hat and
+    z; the x-hat buffer is then the epilogue's staging, handed back to the LayerNorm warps through
+    hempty once every epilogue warp's TMA store has read its rows."""
+    HEMPTY_AFTER_STORE = True
+
+    def __init__(self, tiles, seed):
+        self.rng = random.Random(seed)
+        self.tiles = tiles
+        B = Barrier
+        self.xfull, self.xempty = B("xfull", 1), B("xempty", LN_WARPS)
+        self.zfull, self.zempty = B("zfull", 1), B("zempty", 1)
+        self.hfull, self.hempty = B("hfull", LN_WARPS), B("hempty", EPI_WARPS)
+        self.tfull = [B(f"tfull{b}", 1) for b in range(2)]
+        self.tempty = [B(f"tempty{b}", EPI_WARPS) for b in range(2)]
+        self.sfull, self.sempty = B("sfull", LN_WARPS), B("sempty", EPI_WARPS)
+        self.wfull, self.fin = B("wfull", 1), B("fin", 1)
+        self.xslot = self.zstage = None
+        self.x_read, self.z_read = set(), set()
+        self.owner, self.owner_set = None, set()    # x-hat buffer: ("ln" | "epi", tile) and who wrote
+        self.xh_mma_read = -1
+        self.acc, self.acc_read = [None, None], [set(), set()]
+        self.st, self.st_read = {}, set()
+        self.pending_store = [None] * EPI_WARPS
+        self.copies, self.mma = [], []
+
+    def producer(self):
+        self.wfull.expect(1)
+        self.copies.append(("w",))
+        ph = 0
+        for local in range(self.tiles):
+            yield (self.xempty, ph ^ 1, ("xempty",))
+            self.xfull.expect(1)
+            self.copies.append(("x", local))
+            yield (self.zempty, ph ^ 1, ("zempty",))
+            self.zfull.expect(1)
+            self.copies.append(("z", local))
+            ph ^= 1
+
+    def issuer(self):
+        yield (self.wfull, 0, ("wfull",))
+        ph = 0
+        for local in range(self.tiles):
+            buf, use = local & 1, local >> 1
+            yield (self.tempty[buf], (use & 1) ^ 1, ("tempty", buf))
+            yield (self.hfull, ph, ("hfull",))
+            yield (self.zfull, ph, ("zfull",))
+            self.mma.append(("mma", local, buf))
+            self.mma.append(("commit", self.zempty))
+            self.mma.append(("commit", self.tfull[buf]))
+            ph ^= 1
+        self.mma.append(("commit", self.fin))
+        yield (self.fin, 0, ("fin",))
+
+    def layernorm(self, w):
+        ph = 0
+        for local in range(self.tiles):
+            yield (self.zfull, ph, ("zfull",))
+            yield WORK
+            assert self.zstage == local, ("z statistics of another tile", local, self.zstage)
+            self.z_read.add((local, w))
+            yield (self.sempty, (local & 1) ^ 1, ("sempty",))
+            if local >= 1:
+                assert all((local - 1, e) in self.st_read for e in range(EPI_WARPS)), \
+                    ("statistics overwritten before every epilogue warp read them", local)
+            self.st[w] = local
+            self.sfull.arrive()
+            yield (self.xfull, ph, ("xfull",))
+            yield WORK
+            assert self.xslot == local, ("LayerNorm read another tile's x", local, self.xslot)
+            self.x_read.add((local, w))
+            yield (self.hempty, ph ^ 1, ("hempty",))
+            yield WORK
+            if self.owner != ("ln", local):
+                if local >= 1:
+                    assert self.owner == ("epi", local - 1) and self.owner_set == set(range(EPI_WARPS)), \
+                        ("x-hat written over rows the epilogue still stages", local, self.owner)
+                    assert all(s is None for s in self.pending_store), \
+                        ("x-hat written before the stores read the staging rows", local)
+                self.owner, self.owner_set = ("ln", local), set()
+            self.owner_set.add(w)
+            self.xempty.arrive()
+            self.hfull.arrive()
+            ph ^= 1
+
+    def epilogue(self, e):
+        for local in range(self.tiles):
+            buf, use = local & 1, local >> 1
+            yield (self.sfull, local & 1, ("sfull",))
+            yield (self.tfull[buf], use & 1, ("tfull", buf))
+            yield WORK
+            assert all(self.st.get(w) == local for w in range(LN_WARPS)), ("stale statistics", local)
+            self.st_read.add((local, e))
+            self.sempty.arrive()
+            assert self.acc[buf] == local, ("stale accumulator", local, self.acc[buf])
+            self.acc_read[buf].add((local, e))
+            # the staging rows are the x-hat buffer: the MMA of this tile must have read it
+            assert self.xh_mma_read >= local, ("staging written over x-hat the MMA still reads", local)
+            if self.owner != ("epi", local):
+                self.owner, self.owner_set = ("epi", local), set()
+            self.owner_set.add(e)
+            self.tempty[buf].arrive()
+            self.pending_store[e] = local
+            if self.HEMPTY_AFTER_STORE:
+                yield (StoreDrained(self, e), 0, None)
+            self.hempty.arrive()
+
+    def step_copy(self):
+        op = self.copies.pop(self.rng.randrange(len(self.copies)))
+        if op[0] == "w":
+            self.wfull.complete_tx(1)
+        elif op[0] == "x":
+            u = op[1]
+            if u >= 1:
+                assert all((u - 1, w) in self.x_read for w in range(LN_WARPS)), ("x refilled early", u)
+            self.xslot = u
+            self.xfull.complete_tx(1)
+        else:
+            u = op[1]
+            if u >= 1:
+                assert (u - 1, "mma") in self.z_read and all((u - 1, w) in self.z_read for w in range(LN_WARPS)), \
+                    ("z refilled before all its readers were done", u)
+            self.zstage = u
+            self.zfull.complete_tx(1)
+
+    def step_mma(self):
+        op = self.mma.pop(0)
+        if op[0] == "mma":
+            _, local, buf = op
+            assert self.owner == ("ln", local) and self.owner_set == set(range(LN_WARPS)), \
+                ("MMA reads an incomplete or foreign x-hat", local, self.owner)
+            assert self.zstage == local, ("MMA reads another tile's z", local, self.zstage)
+            if local >= 2:
+                assert all((local - 2, e) in self.acc_read[buf] for e in range(EPI_WARPS)), \
+                    ("accumulator overwritten before every epilogue warp read it", local)
+            self.acc[buf] = local
+            self.xh_mma_read = local
+            self.z_read.add((local, "mma"))
+        else:
+            op[1].arrive()
+
+    def step_store(self):
+        e = self.rng.choice([k for k in range(EPI_WARPS) if self.pending_store[k] is not None])
+        tile = self.pending_store[e]
+        assert self.owner == ("epi", tile) and e in self.owner_set, \
+            ("a store read staging rows that were overwritten", tile, self.owner)
+        self.pending_store[e] = None
+
+    run = Model.run
+
+    def _roles(self):
+        roles = {"tma": self.producer(), "mma": self.issuer()}
+        roles.update({f"ln{w}": self.layernorm(w) for w in range(LN_WARPS)})
+        roles.update({f"epi{e}": self.epilogue(e) for e in range(EPI_WARPS)})
+        return roles
+
+
+@pytest.mark.parametrize("tiles", [1, 2, 3, 7, 12])
+@pytest.mark.parametrize("seed", range(8))
+def test_finish_x32_protocol(tiles, seed):
+    ModelX32(tiles, seed).run()
+
+
+def test_the_model_catches_x_hat_handed_back_before_the_stores_read_it():
+    """A planted mistake in the float32-x form: hempty arrived when the store is issued rather than once
+    it has read the staging rows, so the LayerNorm warps can write the next x-hat under it."""
+    class Broken(ModelX32):
+        HEMPTY_AFTER_STORE = False
+
+    assert _caught(Broken, tiles=12, seeds=40) > 0
