@@ -45,6 +45,18 @@ class Barrier:
         return (self.phase & 1) != parity
 
 
+class Always:
+    """A step that needs no barrier: a role's work between a wait and the reads it guards, which the
+    scheduler may interleave with anything else."""
+    name = "work"
+
+    def passes(self, _parity):
+        return True
+
+
+WORK = (Always(), 0, None)
+
+
 class Model:
     def __init__(self, tiles, KB, seed):
         self.rng = random.Random(seed)
@@ -94,6 +106,7 @@ class Model:
         for local in range(self.tiles):
             buf, use = local & 1, local >> 1
             yield (self.tfull[r][buf], use & 1, ("tfull", r, buf))
+            yield WORK
             assert self.acc[buf] == (local, self.KB), ("epilogue reads an unfinished accumulator", local, self.acc[buf])
             self.read[r][buf].add((local, w))
             self.tempty[buf].arrive()
@@ -134,8 +147,9 @@ class Model:
             try:
                 waiting[k] = next(roles[k])
                 key = waiting[k][2]
-                counters[(k, key)] = counters.get((k, key), -1) + 1
-                meant_phase[k] = counters[(k, key)]
+                if key is not None:
+                    counters[(k, key)] = counters.get((k, key), -1) + 1
+                    meant_phase[k] = counters[(k, key)]
             except StopIteration:
                 done.add(k)
                 waiting[k] = None
@@ -157,9 +171,10 @@ class Model:
                 bar = waiting[c][0]
                 # each role waits on a given barrier once per phase, in order: the n-th wait means phase n
                 # (the producers' waits on "empty" start one phase early, as the first pass finds it free)
-                n = meant_phase[c]
-                expect = n if waiting[c][2][0] == "empty" or waiting[c][2][0] == "tempty" else n + 1
-                assert bar.phase == expect, ("a wait passed on another phase", c, bar.name, bar.phase, expect)
+                if waiting[c][2] is not None:
+                    n = meant_phase[c]
+                    expect = n if waiting[c][2][0] == "empty" or waiting[c][2][0] == "tempty" else n + 1
+                    assert bar.phase == expect, ("a wait passed on another phase", c, bar.name, bar.phase, expect)
                 advance(c)
         raise AssertionError("no progress")
 
@@ -194,6 +209,32 @@ def test_the_model_catches_a_release_before_the_mma():
     for seed in range(30):
         try:
             Broken(3, 9, seed).run()
+        except AssertionError:
+            caught += 1
+    assert caught > 0
+
+
+def test_the_model_catches_an_accumulator_handed_back_by_one_cta():
+    """A planted mistake: the accumulator hand-back counted for the first CTA's epilogue only, so the next
+    tile's MMAs can overwrite it while the second CTA's epilogue still reads it."""
+    class Broken(Model):
+        def __init__(self, tiles, KB, seed):
+            super().__init__(tiles, KB, seed)
+            self.tempty = [Barrier(f"tempty{b}", EPI_WARPS) for b in range(2)]
+
+        def epilogue(self, r, w):
+            for local in range(self.tiles):
+                buf, use = local & 1, local >> 1
+                yield (self.tfull[r][buf], use & 1, ("tfull", r, buf))
+                yield WORK
+                assert self.acc[buf] == (local, self.KB), ("epilogue reads an unfinished accumulator", local)
+                self.read[r][buf].add((local, w))
+                if r == 0:
+                    self.tempty[buf].arrive()
+    caught = 0
+    for seed in range(40):
+        try:
+            Broken(6, 2, seed).run()
         except AssertionError:
             caught += 1
     assert caught > 0
