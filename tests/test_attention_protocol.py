@@ -42,6 +42,18 @@ class Barrier:
         return (self.phase & 1) != parity
 
 
+class Always:
+    """A step that needs no barrier: a role's work between a wait and the reads it guards, which the
+    scheduler may interleave with anything else."""
+    name = "work"
+
+    def passes(self, _parity):
+        return True
+
+
+WORK = (Always(), 0, None)
+
+
 class Model:
     def __init__(self, KB, seed):
         self.rng = random.Random(seed)
@@ -134,6 +146,7 @@ class Model:
             h, kb, st, b = t // KB, t % KB, t % STAGES, t % SBUF
             yield (self.s_full[g][b], (t // SBUF) & 1, ("s_full", g, b, t // SBUF))
             yield (self.kv_full[st], (t // STAGES) & 1, ("kv_full", st, t // STAGES))
+            yield WORK
             assert self.s_buf[g][b] == ("S", t) or self.s_buf[g][b] == ("P", t), ("softmax reads stale S", t)
             assert self.stage_block[st] == t, ("softmax reads the wrong bias", t)
             if t >= 1 and kb == 0:
@@ -144,6 +157,8 @@ class Model:
                 yield (self.pv_done[g][(t - 1) & 1], ((t - 1) >> 1) & 1, ("pv_done", g, (t - 1) & 1, (t - 1) >> 1))
                 assert all(s in self.pv_completed[g] for s in range(t)), ("rescaled before a product", t)
                 assert t not in self.pv_completed[g]
+            yield WORK                                         # the pass over S, then P stored over it
+            assert self.s_buf[g][b] == ("S", t) or self.s_buf[g][b] == ("P", t), ("S overwritten during the pass", t)
             if w == SM_WARPS - 1:                              # the last warp's store completes P of the row block
                 self.s_buf[g][b] = ("P", t)
             self.p_full[g][b].arrive()
